@@ -1,0 +1,202 @@
+"""GB300-native chunked Gated Delta Rule.
+
+Python surface of the C library declared in ``include/gdr.h``.  Every step of
+the computation runs in the library's CUDA kernels; this module only
+allocates outputs with PyTorch, marshals pointers and passes the current CUDA
+stream.  There is no CPU fallback: without the built library every call
+raises.
+
+API (shapes follow the FlashQLA skill page, "Core API" / "Low-Level API"):
+
+* ``chunk_gated_delta_rule_fwd(q, k, v, g, beta, ...) -> (g_cumsum, A, o, h, final_state)``
+* ``chunk_gated_delta_rule_bwd(q, k, v, g_cumsum, beta, A, do, ...) -> (dq, dk, dv, dbeta, dg, dh0)``
+* ``chunk_gated_delta_rule(q, k, v, g, beta, ...) -> (o, final_state)`` (autograd)
+* ``prepare_chunks(cu_seqlens, chunk_size=64) -> (chunk_indices, chunk_offsets, total_chunks)``
+"""
+
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _lib
+
+__all__ = ["chunk_gated_delta_rule", "chunk_gated_delta_rule_fwd", "chunk_gated_delta_rule_bwd",
+           "prepare_chunks", "GdrError", "problem", "workspace_bytes"]
+
+GdrError = _lib.GdrError
+
+_DT = {torch.bfloat16: _lib.GDR_BF16, torch.float16: _lib.GDR_FP16, torch.float32: _lib.GDR_FP32}
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def problem(q, v, g, scale=None, cu_seqlens=None, use_qk_l2norm_in_kernel=False, state_v_first=False,
+            num_segments=0, extra_flags=0) -> _lib.Problem:
+    """The gdr_problem struct describing a call with these tensors."""
+    B, T, Hq, K = q.shape
+    Hv, V = v.shape[2], v.shape[3]
+    flags = extra_flags
+    if use_qk_l2norm_in_kernel:
+        flags |= _lib.GDR_L2NORM_QK
+    if state_v_first:
+        flags |= _lib.GDR_STATE_V_FIRST
+    p = _lib.Problem()
+    p.B, p.T, p.Hq, p.Hv, p.K, p.V = B, T, Hq, Hv, K, V
+    p.dtype = _DT.get(q.dtype, 99)
+    p.gate_dtype = _DT.get(g.dtype, 99)
+    p.scale = float(K ** -0.5 if scale is None else scale)
+    if cu_seqlens is not None:
+        p.cu_seqlens = cu_seqlens.data_ptr()
+        p.num_seqs = cu_seqlens.numel() - 1
+    else:
+        p.cu_seqlens = None
+        p.num_seqs = 0
+    p.flags = flags
+    p.num_segments = int(num_segments)
+    return p
+
+
+def workspace_bytes(p: _lib.Problem, backward: bool) -> int:
+    lib = _lib.load()
+    n = ctypes.c_size_t(0)
+    fn = lib.gdr_bwd_workspace_size if backward else lib.gdr_fwd_workspace_size
+    _lib.check(fn(ctypes.byref(p), ctypes.byref(n)), fn.__name__)
+    return int(n.value)
+
+
+def _state_shape(p, v_first):
+    N = p.num_seqs if p.cu_seqlens else p.B
+    return (N, p.Hv, p.V, p.K) if v_first else (N, p.Hv, p.K, p.V)
+
+
+def _cu(cu_seqlens):
+    if cu_seqlens is None:
+        return None
+    if cu_seqlens.dtype != torch.int32:
+        cu_seqlens = cu_seqlens.to(torch.int32)
+    return cu_seqlens.contiguous()
+
+
+def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=True,
+                               cu_seqlens=None, use_qk_l2norm_in_kernel=False, state_v_first=False,
+                               num_segments=0, output_h=False, save_for_backward=True, out=None):
+    """Forward.  Returns (g_cumsum, A, o, h, final_state); h is None unless output_h.
+
+    g_cumsum and A are None when save_for_backward is False.  For packed
+    batches h has gdr_max_chunks rows; rows past the true chunk count are unused.
+    """
+    lib = _lib.load()
+    cu = _cu(cu_seqlens)
+    p = problem(q, v, g, scale, cu, use_qk_l2norm_in_kernel, state_v_first, num_segments)
+    dev = q.device
+    B, T, Hv, V = v.shape
+    o = out if out is not None else torch.empty_like(v)
+    fin = torch.empty(_state_shape(p, state_v_first), dtype=torch.float32, device=dev) if output_final_state else None
+    gcs = A = None
+    if save_for_backward:
+        gcs = torch.empty((B, T, Hv), dtype=torch.float32, device=dev)
+        A = torch.empty((B, T, Hv, _lib.GDR_CHUNK), dtype=q.dtype, device=dev)
+    h = None
+    if output_h:
+        rows = int(lib.gdr_max_chunks(ctypes.byref(p)))
+        h = torch.empty((rows, Hv) + _state_shape(p, state_v_first)[2:], dtype=q.dtype, device=dev)
+    nbytes = workspace_bytes(p, False)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    h0 = None if initial_state is None else initial_state.to(torch.float32).contiguous()
+    st = lib.gdr_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o),
+                     _ptr(fin), _ptr(gcs), _ptr(A), _ptr(h), _ptr(ws), nbytes, _stream(dev))
+    _lib.check(st, "gdr_fwd")
+    return gcs, A, o, h, fin
+
+
+def chunk_gated_delta_rule_bwd(q, k, v, g, beta, A, do, dht=None, scale=None, initial_state=None,
+                               cu_seqlens=None, use_qk_l2norm_in_kernel=False, state_v_first=False,
+                               num_segments=0, gate_dtype=None):
+    """Backward.  ``g`` is the forward's g_cumsum (fp32).  Returns (dq, dk, dv, dbeta, dg, dh0).
+
+    dg and dbeta take beta's dtype (or ``gate_dtype``); dh0 is None without an initial state.
+    """
+    lib = _lib.load()
+    cu = _cu(cu_seqlens)
+    gd = gate_dtype or beta.dtype
+    p = problem(q, v, torch.empty(0, dtype=gd), scale, cu, use_qk_l2norm_in_kernel, state_v_first, num_segments)
+    dev = q.device
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    dg = torch.empty(beta.shape, dtype=gd, device=dev)
+    db = torch.empty(beta.shape, dtype=gd, device=dev)
+    h0 = None if initial_state is None else initial_state.to(torch.float32).contiguous()
+    dh0 = torch.empty(_state_shape(p, state_v_first), dtype=torch.float32, device=dev) if h0 is not None else None
+    dht_ = None if dht is None else dht.to(torch.float32).contiguous()
+    nbytes = workspace_bytes(p, True)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    st = lib.gdr_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A), _ptr(do),
+                     _ptr(dht_), _ptr(h0), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(db), _ptr(dh0), _ptr(ws),
+                     nbytes, _stream(dev))
+    _lib.check(st, "gdr_bwd")
+    return dq, dk, dv, db, dg, dh0
+
+
+def prepare_chunks(cu_seqlens: torch.Tensor, chunk_size: int = _lib.GDR_CHUNK, total_tokens: int = -1):
+    """Chunk tables of a packed batch, computed on the GPU.
+
+    Returns (chunk_indices [max_chunks,2] int32, chunk_offsets [N+1] int32, total_chunks int32 [1]);
+    rows of chunk_indices past total_chunks are zero.
+    """
+    lib = _lib.load()
+    cu = _cu(cu_seqlens)
+    N = cu.numel() - 1
+    T = int(total_tokens)
+    bound = ((T if T >= 0 else 0) + N * (chunk_size - 1)) // chunk_size
+    max_chunks = max(bound, 1)
+    idx = torch.zeros((max_chunks, 2), dtype=torch.int32, device=cu.device)
+    off = torch.empty((N + 1,), dtype=torch.int32, device=cu.device)
+    tot = torch.empty((1,), dtype=torch.int32, device=cu.device)
+    st = lib.gdr_prepare_chunks(_ptr(cu), N, T, chunk_size, _ptr(idx), max_chunks, _ptr(off), _ptr(tot),
+                                _stream(cu.device))
+    _lib.check(st, "gdr_prepare_chunks")
+    return idx, off, tot
+
+
+def get_error(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the device error word."""
+    return int(_lib.load().gdr_get_error(_stream(device)))
+
+
+class _GDR(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, g, beta, scale, initial_state, output_final_state, cu_seqlens,
+                use_qk_l2norm_in_kernel, state_v_first, num_segments):
+        gcs, A, o, _, fin = chunk_gated_delta_rule_fwd(
+            q, k, v, g, beta, scale=scale, initial_state=initial_state, output_final_state=output_final_state,
+            cu_seqlens=cu_seqlens, use_qk_l2norm_in_kernel=use_qk_l2norm_in_kernel, state_v_first=state_v_first,
+            num_segments=num_segments)
+        ctx.save_for_backward(q, k, v, gcs, beta, A, initial_state, cu_seqlens)
+        ctx.opts = (scale, use_qk_l2norm_in_kernel, state_v_first, num_segments, g.dtype)
+        return o, fin
+
+    @staticmethod
+    def backward(ctx, do, dht):
+        q, k, v, gcs, beta, A, h0, cu = ctx.saved_tensors
+        scale, l2, vf, nseg, gdt = ctx.opts
+        dq, dk, dv, db, dg, dh0 = chunk_gated_delta_rule_bwd(
+            q, k, v, gcs, beta, A, do.contiguous(), dht=dht, scale=scale, initial_state=h0, cu_seqlens=cu,
+            use_qk_l2norm_in_kernel=l2, state_v_first=vf, num_segments=nseg, gate_dtype=gdt)
+        return dq, dk, dv, dg, db, None, dh0, None, None, None, None, None
+
+
+def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,
+                           cu_seqlens=None, use_qk_l2norm_in_kernel=False, state_v_first=False, num_segments=0):
+    """Differentiable op: returns (o, final_state or None)."""
+    return _GDR.apply(q, k, v, g, beta, scale, initial_state, output_final_state, cu_seqlens,
+                      use_qk_l2norm_in_kernel, state_v_first, num_segments)

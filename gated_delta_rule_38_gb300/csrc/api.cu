@@ -1,0 +1,353 @@
+// C-ABI entry points: argument validation, workspace layout, launch order,
+// the varlen chunk-table kernel and the device error word.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace gdr {
+
+__device__ unsigned int g_gdr_error_word = 0;
+
+// ---------------------------------------------------------------- chunk tables
+
+// One CTA.  Validates cu_seqlens, then an exclusive scan of ceil(len/chunk)
+// gives the offsets; each sequence's rows of the chunk table follow.
+__global__ void __launch_bounds__(1024) prep_chunks_kernel(const int32_t *__restrict__ cu, int N, int T, int chunk,
+                                                           int32_t *__restrict__ idx, long long max_chunks,
+                                                           int32_t *__restrict__ off, int32_t *__restrict__ total,
+                                                           unsigned *err) {
+    __shared__ int s_bad;
+    __shared__ int s_warp[32];
+    __shared__ long long s_carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    if (tid == 0) {
+        s_bad = (cu[0] != 0 || (T >= 0 && cu[N] != T)) ? 1 : 0;
+        s_carry = 0;
+    }
+    __syncthreads();
+    for (int n = tid; n < N; n += blockDim.x)
+        if (cu[n + 1] < cu[n]) atomicOr(&s_bad, 1);
+    __syncthreads();
+    if (s_bad) {
+        if (tid == 0) {
+            *total = 0;
+            raise_error(err, GDR_ERR_CUSEQLENS);
+        }
+        return;
+    }
+    for (int base = 0; base < N; base += blockDim.x) {
+        const int n = base + tid;
+        const int c = (n < N) ? (cu[n + 1] - cu[n] + chunk - 1) / chunk : 0;
+        int x = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) s_warp[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int w = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            if (lane < nw) s_warp[lane] = w;
+        }
+        __syncthreads();
+        const int incl = x + (warp > 0 ? s_warp[warp - 1] : 0);
+        const long long excl = s_carry + incl - c;
+        if (n < N) {
+            off[n] = (int32_t)excl;
+            for (int i = 0; i < c; ++i) {
+                const long long r = excl + i;
+                if (r < max_chunks) {
+                    idx[2 * r] = n;
+                    idx[2 * r + 1] = i;
+                }
+            }
+        }
+        __syncthreads();
+        if (tid == blockDim.x - 1) s_carry += incl;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        off[N] = (int32_t)s_carry;
+        *total = (int32_t)s_carry;
+    }
+}
+
+cudaError_t launch_prep_chunks(const int32_t *cu, int N, int T, int chunk, int32_t *idx, int64_t max_chunks,
+                               int32_t *off, int32_t *total, unsigned *err, cudaStream_t s) {
+    prep_chunks_kernel<<<1, 1024, 0, s>>>(cu, N, T, chunk, idx, (long long)max_chunks, off, total, err);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- host helpers
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_dev_ok[kMaxDevices];           // 0 unknown, 1 ok, 2 wrong arch
+unsigned *g_err_ptr[kMaxDevices];    // device address of the error word
+
+gdr_status device_state(unsigned **err) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDR_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_dev_ok[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return GDR_ERR_CUDA;
+        if (major != 10 || minor != 3) {
+            g_dev_ok[dev] = 2;
+        } else {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_gdr_error_word) != cudaSuccess) return GDR_ERR_CUDA;
+            g_err_ptr[dev] = static_cast<unsigned *>(p);
+            g_dev_ok[dev] = 1;
+        }
+    }
+    if (g_dev_ok[dev] != 1) return GDR_ERR_DEVICE;
+    *err = g_err_ptr[dev];
+    return GDR_OK;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline size_t esize(gdr_dtype d) { return d == GDR_FP32 ? 4 : 2; }
+
+gdr_status check_problem(const gdr_problem *p) {
+    if (!p) return GDR_ERR_NULL;
+    if (p->K != DK || p->V != DV) return GDR_ERR_SHAPE;
+    if (p->B < 1 || p->T < 0 || p->Hq < 1 || p->Hv < 1 || p->Hv % p->Hq != 0) return GDR_ERR_SHAPE;
+    if (p->cu_seqlens && (p->B != 1 || p->num_seqs < 1)) return GDR_ERR_SHAPE;
+    if (p->num_segments < 0) return GDR_ERR_SHAPE;
+    if (p->dtype != GDR_BF16 && p->dtype != GDR_FP16) return GDR_ERR_DTYPE;
+    if (p->gate_dtype != p->dtype && p->gate_dtype != GDR_FP32) return GDR_ERR_DTYPE;
+    const unsigned rejected = GDR_GATE_IN_KERNEL | GDR_BETA_SIGMOID_IN_KERNEL | GDR_ALLOW_NEG_EIGVAL | GDR_INTER_CARD_CP;
+    const unsigned known = GDR_L2NORM_QK | GDR_STATE_V_FIRST;
+    if ((p->flags & rejected) || (p->flags & ~(known | rejected))) return GDR_ERR_UNSUPPORTED;
+    return GDR_OK;
+}
+
+int num_seqs(const gdr_problem *p) { return p->cu_seqlens ? p->num_seqs : p->B; }
+
+int64_t max_chunks_of(const gdr_problem *p) {
+    if (p->cu_seqlens) return ((int64_t)p->T + (int64_t)p->num_seqs * (C - 1)) / C;
+    return (int64_t)p->B * ((p->T + C - 1) / C);
+}
+
+struct Layout {
+    size_t idx = 0, off = 0, total = 0, gcs = 0, A = 0, h = 0, dhn = 0, bytes = 0;
+};
+
+// Workspace: [varlen chunk tables][fwd: g_cumsum, A scratch | bwd: states, state gradients].
+Layout layout_of(const gdr_problem *p, bool bwd) {
+    Layout L;
+    size_t at = 0;
+    const int64_t mc = max_chunks_of(p);
+    if (p->cu_seqlens) {
+        L.idx = at;
+        at = round_up(at + (size_t)mc * 2 * sizeof(int32_t), 256);
+        L.off = at;
+        at = round_up(at + (size_t)(p->num_seqs + 1) * sizeof(int32_t), 256);
+        L.total = at;
+        at = round_up(at + sizeof(int32_t), 256);
+    }
+    const size_t tok = (size_t)p->B * p->T;
+    if (!bwd) {
+        L.gcs = at;
+        at = round_up(at + tok * p->Hv * sizeof(float), 256);
+        L.A = at;
+        at = round_up(at + tok * p->Hv * C * esize(p->dtype), 256);
+    } else {
+        const size_t st = (size_t)mc * p->Hv * DK * DV * esize(p->dtype);
+        L.h = at;
+        at = round_up(at + st, 256);
+        L.dhn = at;
+        at = round_up(at + st, 256);
+    }
+    L.bytes = at;
+    return L;
+}
+
+Args make_args(const gdr_problem *p, unsigned *err) {
+    Args a;
+    a.B = p->B;
+    a.T = p->T;
+    a.Hq = p->Hq;
+    a.Hv = p->Hv;
+    a.N = num_seqs(p);
+    a.bf16 = p->dtype == GDR_BF16;
+    a.gate_f32 = p->gate_dtype == GDR_FP32;
+    a.l2norm = (p->flags & GDR_L2NORM_QK) != 0;
+    a.v_first = (p->flags & GDR_STATE_V_FIRST) != 0;
+    a.scale = p->scale;
+    a.cu = p->cu_seqlens;
+    a.cidx = a.coff = a.ctotal = nullptr;
+    a.max_chunks = max_chunks_of(p);
+    a.err = err;
+    return a;
+}
+
+gdr_status check_ws(const Layout &L, void *ws, size_t bytes) {
+    if (L.bytes == 0) return GDR_OK;
+    if (!ws || bytes < L.bytes) return GDR_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return GDR_ERR_ALIGN;
+    return GDR_OK;
+}
+
+gdr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA; }
+
+// Build the varlen chunk tables in the workspace (no-op for dense batches).
+gdr_status tables(const gdr_problem *p, Args &a, char *ws, const Layout &L, cudaStream_t s) {
+    if (!p->cu_seqlens) return GDR_OK;
+    a.cidx = reinterpret_cast<int32_t *>(ws + L.idx);
+    a.coff = reinterpret_cast<int32_t *>(ws + L.off);
+    a.ctotal = reinterpret_cast<int32_t *>(ws + L.total);
+    return cuda_status(launch_prep_chunks(p->cu_seqlens, p->num_seqs, p->T, C, const_cast<int32_t *>(a.cidx),
+                                          a.max_chunks, const_cast<int32_t *>(a.coff),
+                                          const_cast<int32_t *>(a.ctotal), a.err, s));
+}
+
+}  // namespace
+}  // namespace gdr
+
+using namespace gdr;
+
+extern "C" {
+
+int64_t gdr_max_chunks(const gdr_problem *p) {
+    if (check_problem(p) != GDR_OK) return -1;
+    return max_chunks_of(p);
+}
+
+gdr_status gdr_prepare_chunks(const int32_t *cu_seqlens, int num_seqs, int total_tokens, int chunk_size,
+                              int32_t *chunk_indices, int64_t max_chunks, int32_t *chunk_offsets,
+                              int32_t *total_chunks, void *stream) {
+    if (!cu_seqlens || !chunk_indices || !chunk_offsets || !total_chunks) return GDR_ERR_NULL;
+    if (num_seqs < 1 || chunk_size < 1 || total_tokens < -1) return GDR_ERR_SHAPE;
+    if (total_tokens >= 0) {
+        const int64_t bound = ((int64_t)total_tokens + (int64_t)num_seqs * (chunk_size - 1)) / chunk_size;
+        if (max_chunks < bound) return GDR_ERR_SHAPE;
+    }
+    unsigned *err = nullptr;
+    gdr_status st = device_state(&err);
+    if (st != GDR_OK) return st;
+    return cuda_status(launch_prep_chunks(cu_seqlens, num_seqs, total_tokens, chunk_size, chunk_indices,
+                                          max_chunks, chunk_offsets, total_chunks, err,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+gdr_status gdr_fwd_workspace_size(const gdr_problem *p, size_t *bytes) {
+    gdr_status st = check_problem(p);
+    if (st != GDR_OK) return st;
+    if (!bytes) return GDR_ERR_NULL;
+    *bytes = layout_of(p, false).bytes;
+    return GDR_OK;
+}
+
+gdr_status gdr_bwd_workspace_size(const gdr_problem *p, size_t *bytes) {
+    gdr_status st = check_problem(p);
+    if (st != GDR_OK) return st;
+    if (!bytes) return GDR_ERR_NULL;
+    *bytes = layout_of(p, true).bytes;
+    return GDR_OK;
+}
+
+gdr_status gdr_fwd(const gdr_problem *p, const void *q, const void *k, const void *v, const void *g,
+                   const void *beta, const float *h0, void *o, float *final_state, float *g_cumsum, void *A,
+                   void *h, void *workspace, size_t workspace_bytes, void *stream) {
+    gdr_status st = check_problem(p);
+    if (st != GDR_OK) return st;
+    if (!q || !k || !v || !g || !beta || !o) return GDR_ERR_NULL;
+    const void *ptrs[] = {q, k, v, g, beta, h0, o, final_state, g_cumsum, A, h, p->cu_seqlens};
+    for (const void *x : ptrs)
+        if (x && !aligned16(x)) return GDR_ERR_ALIGN;
+    const Layout L = layout_of(p, false);
+    if ((st = check_ws(L, workspace, workspace_bytes)) != GDR_OK) return st;
+    unsigned *err = nullptr;
+    if ((st = device_state(&err)) != GDR_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    Args a = make_args(p, err);
+    if ((st = tables(p, a, ws, L, s)) != GDR_OK) return st;
+    float *gcs = g_cumsum ? g_cumsum : reinterpret_cast<float *>(ws + L.gcs);
+    void *Aw = A ? A : static_cast<void *>(ws + L.A);
+    if ((st = cuda_status(launch_wy_fwd(a, k, g, beta, gcs, Aw, s))) != GDR_OK) return st;
+    return cuda_status(launch_chain_fwd(a, q, k, v, gcs, beta, Aw, h0, o, final_state, h, true, s));
+}
+
+gdr_status gdr_bwd(const gdr_problem *p, const void *q, const void *k, const void *v, const float *g_cumsum,
+                   const void *beta, const void *A, const void *dout, const float *dht, const float *h0, void *dq,
+                   void *dk, void *dv, void *dg, void *dbeta, float *dh0, void *workspace, size_t workspace_bytes,
+                   void *stream) {
+    gdr_status st = check_problem(p);
+    if (st != GDR_OK) return st;
+    if (!q || !k || !v || !g_cumsum || !beta || !A || !dout || !dq || !dk || !dv || !dg || !dbeta)
+        return GDR_ERR_NULL;
+    const void *ptrs[] = {q, k, v, g_cumsum, beta, A, dout, dht, h0, dq, dk, dv, dg, dbeta, dh0, p->cu_seqlens};
+    for (const void *x : ptrs)
+        if (x && !aligned16(x)) return GDR_ERR_ALIGN;
+    const Layout L = layout_of(p, true);
+    if ((st = check_ws(L, workspace, workspace_bytes)) != GDR_OK) return st;
+    unsigned *err = nullptr;
+    if ((st = device_state(&err)) != GDR_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *ws = static_cast<char *>(workspace);
+    Args a = make_args(p, err);
+    if ((st = tables(p, a, ws, L, s)) != GDR_OK) return st;
+    void *hw = ws + L.h, *dhw = ws + L.dhn;
+    // states before every chunk (recomputed), then the reverse state-gradient chain,
+    // then every chunk's gradients in parallel
+    if ((st = cuda_status(launch_chain_fwd(a, q, k, v, g_cumsum, beta, A, h0, nullptr, nullptr, hw, false, s))) !=
+        GDR_OK)
+        return st;
+    if ((st = cuda_status(launch_chain_bwd(a, q, k, g_cumsum, beta, A, dout, dht, dhw, dh0, s))) != GDR_OK)
+        return st;
+    return cuda_status(launch_bwd_chunk(a, q, k, v, g_cumsum, beta, A, dout, hw, dhw, dq, dk, dv, dg, dbeta, s));
+}
+
+gdr_status gdr_get_error(void *stream) {
+    unsigned *err = nullptr;
+    gdr_status st = device_state(&err);
+    if (st != GDR_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GDR_ERR_CUDA;
+    unsigned code = 0;
+    if (cudaMemcpy(&code, err, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess) return GDR_ERR_CUDA;
+    const unsigned zero = 0;
+    if (code != 0 && cudaMemcpy(err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    return static_cast<gdr_status>(code);
+}
+
+const char *gdr_status_string(gdr_status s) {
+    switch (s) {
+        case GDR_OK: return "ok";
+        case GDR_ERR_NULL: return "a required pointer is NULL";
+        case GDR_ERR_SHAPE: return "unsupported shape (K and V must be 128, Hv % Hq == 0, B == 1 with cu_seqlens)";
+        case GDR_ERR_DTYPE: return "unsupported dtype (q/k/v must be bf16 or fp16; gates the same or fp32)";
+        case GDR_ERR_UNSUPPORTED: return "unsupported option";
+        case GDR_ERR_DEVICE: return "the current device is not compute capability 10.3 (sm_103a)";
+        case GDR_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned (workspace: 256-byte)";
+        case GDR_ERR_WORKSPACE: return "workspace missing or too small";
+        case GDR_ERR_CUSEQLENS: return "malformed cu_seqlens";
+        case GDR_ERR_TIMEOUT: return "a bounded device-side wait expired";
+        case GDR_ERR_CUDA: return "CUDA runtime error";
+        case GDR_ERR_INTERNAL: return "internal error";
+    }
+    return "unknown status";
+}
+
+int gdr_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,45 @@
+// Host-side launchers shared between the translation units of the library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdr.h"
+
+namespace gdr {
+
+// Everything a kernel needs to address one problem's tensors.
+struct Args {
+    int B, T, Hq, Hv, N;
+    bool bf16;        // element type of q,k,v,... (else fp16)
+    bool gate_f32;    // g, beta (dg, dbeta) are fp32
+    bool l2norm;
+    bool v_first;
+    float scale;
+    const int32_t *cu;       // device cu_seqlens or nullptr
+    const int32_t *cidx;     // device chunk table [max_chunks,2] (varlen)
+    const int32_t *coff;     // device chunk offsets [N+1] (varlen)
+    const int32_t *ctotal;   // device total chunks (varlen)
+    int64_t max_chunks;
+    unsigned *err;           // device error word
+};
+
+cudaError_t launch_prep_chunks(const int32_t *cu, int N, int T, int chunk, int32_t *idx, int64_t max_chunks,
+                               int32_t *off, int32_t *total, unsigned *err, cudaStream_t s);
+
+// Forward: per-chunk gate cumsum and WY matrix.
+cudaError_t launch_wy_fwd(const Args &a, const void *k, const void *g, const void *beta, float *g_cs,
+                          void *A, cudaStream_t s);
+// Forward recurrence + output (o != nullptr) and/or per-chunk states (h != nullptr).
+cudaError_t launch_chain_fwd(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
+                             const void *beta, const void *A, const float *h0, void *o, float *final_state,
+                             void *h, bool h_api_layout, cudaStream_t s);
+// Backward.
+cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
+                             const void *A, const void *dout, const float *dht, void *dhn, float *dh0,
+                             cudaStream_t s);
+cudaError_t launch_bwd_chunk(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
+                             const void *beta, const void *A, const void *dout, const void *h, const void *dhn,
+                             void *dq, void *dk, void *dv, void *dg, void *dbeta, cudaStream_t s);
+
+}  // namespace gdr

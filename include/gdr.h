@@ -1,0 +1,168 @@
+/*
+ * gdr.h -- C ABI of the GB300 (sm_103a) chunked Gated Delta Rule library.
+ *
+ * The operation (FlashQLA skill page, "Core API" and "Low-Level API"
+ * sections; PR #998 "[GDN] Add FlashQLA backend dispatch", Summary):
+ * for every sequence and value head j (q/k head i = j / (H_v/H_q)),
+ *
+ *     S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *     o_t = scale * S_t q_t
+ *
+ * with the state stored as h_t = S_t^T, shape [K,V] (or [V,K] when
+ * GDR_STATE_V_FIRST is set).  q,k are optionally L2-normalised per token and
+ * head inside the kernels (x / sqrt(sum x^2 + 1e-6)).  The library evaluates
+ * it in chunks of 64 tokens (WY/UT form), on the caller's CUDA stream.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor arguments are DEVICE pointers to contiguous row-major memory
+ *   allocated by the caller (the library never allocates device memory and
+ *   never synchronises the stream, except gdr_get_error).  Every tensor
+ *   pointer must be 16-byte aligned (GDR_ERR_ALIGN otherwise).
+ * - Dense batches: q,k [B,T,Hq,K]; v,o,do,dv [B,T,Hv,V]; g,beta,g_cumsum,
+ *   dg,dbeta [B,T,Hv]; A [B,T,Hv,64]; states [B,Hv,K,V].
+ *   Packed variable-length batches (cu_seqlens != NULL): the same with B = 1
+ *   and T = total tokens; states are [N,Hv,K,V] for the N sequences.
+ * - K = V = 128 (GDR_ERR_SHAPE otherwise); Hv % Hq == 0.
+ * - dtype (q,k,v,o,A,h,dq,dk,dv) is bf16 or fp16 (fp32 -> GDR_ERR_DTYPE);
+ *   gate_dtype (g,beta,dg,dbeta) is dtype or fp32.  States, final_state,
+ *   initial_state, dht, dh0 and g_cumsum are fp32.
+ * - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ * - Every call validates its arguments on the host first and launches
+ *   nothing when it returns an error.  Errors found by kernels (a malformed
+ *   cu_seqlens) are latched in a device error word that gdr_get_error reads.
+ */
+#ifndef GDR_H
+#define GDR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdr_status {
+    GDR_OK = 0,
+    GDR_ERR_NULL = 1,        /* a required pointer is NULL */
+    GDR_ERR_SHAPE = 2,       /* K or V != 128, Hv % Hq != 0, B != 1 with cu_seqlens, negative sizes */
+    GDR_ERR_DTYPE = 3,       /* fp32 or unknown q/k/v dtype, bad gate dtype */
+    GDR_ERR_UNSUPPORTED = 4, /* a rejected option (gate/beta activation in kernel, negative
+                                eigenvalues, multi-GPU sequence split) */
+    GDR_ERR_DEVICE = 5,      /* current device is not compute capability 10.3 */
+    GDR_ERR_ALIGN = 6,       /* a tensor pointer is not 16-byte aligned */
+    GDR_ERR_WORKSPACE = 7,   /* workspace NULL or smaller than the size query returns */
+    GDR_ERR_CUSEQLENS = 8,   /* cu_seqlens not starting at 0, decreasing, or not ending at T */
+    GDR_ERR_TIMEOUT = 9,     /* a bounded device-side wait expired */
+    GDR_ERR_CUDA = 10,       /* a CUDA runtime call failed */
+    GDR_ERR_INTERNAL = 11
+} gdr_status;
+
+typedef enum gdr_dtype { GDR_BF16 = 0, GDR_FP16 = 1, GDR_FP32 = 2 } gdr_dtype;
+
+/* gdr_problem.flags */
+#define GDR_L2NORM_QK              (1u << 0)  /* use_qk_l2norm_in_kernel */
+#define GDR_STATE_V_FIRST          (1u << 1)  /* state tensors stored [..,V,K] */
+/* Options that the FlashQLA backend's verifier rejects (PR #998, review of the
+ * verifier); requesting one returns GDR_ERR_UNSUPPORTED. */
+#define GDR_GATE_IN_KERNEL         (1u << 8)
+#define GDR_BETA_SIGMOID_IN_KERNEL (1u << 9)
+#define GDR_ALLOW_NEG_EIGVAL       (1u << 10)
+#define GDR_INTER_CARD_CP          (1u << 11)
+
+#define GDR_CHUNK 64
+
+typedef struct gdr_problem {
+    int B, T;                  /* batch rows and tokens per row (packed: B = 1, T = total) */
+    int Hq, Hv;                /* q/k heads and value heads, Hv % Hq == 0 */
+    int K, V;                  /* head dims, both 128 */
+    gdr_dtype dtype;           /* q, k, v (and o, A, h, dq, dk, dv) */
+    gdr_dtype gate_dtype;      /* g, beta (and dg, dbeta): dtype or GDR_FP32 */
+    float scale;               /* output scale (K^-0.5 is the usual choice) */
+    const int32_t *cu_seqlens; /* DEVICE int32 [num_seqs+1] or NULL for dense */
+    int num_seqs;              /* N when cu_seqlens != NULL (ignored otherwise) */
+    unsigned flags;            /* GDR_* flags above */
+    int num_segments;          /* intra-GPU sequence split: 0 = automatic, 1 = off,
+                                  S > 1 = cut every sequence into S segments */
+} gdr_problem;
+
+/* Upper bound on the number of 64-token chunks of a problem (rows of h and of
+ * chunk_indices): dense B*ceil(T/64); packed (T + N*63)/64. */
+int64_t gdr_max_chunks(const gdr_problem *p);
+
+/*
+ * Varlen chunk tables (FlashQLA documentation page, utilities section:
+ * prepare_lens, prepare_chunk_offsets, prepare_chunk_indices).
+ *   cu_seqlens    [num_seqs+1] int32, device, in
+ *   chunk_indices [max_chunks,2] int32, device, out: row r = (sequence n,
+ *                 chunk c within n), ordered by n then c; rows past the total
+ *                 are left untouched
+ *   chunk_offsets [num_seqs+1] int32, device, out: chunks before sequence n;
+ *                 chunk_offsets[num_seqs] = total
+ *   total_chunks  int32 scalar, device, out
+ * total_tokens (T) is used to validate cu_seqlens[num_seqs] == T; pass -1 to
+ * skip that check.  A malformed cu_seqlens latches GDR_ERR_CUSEQLENS in the
+ * device error word (see gdr_get_error) and writes total_chunks = 0.
+ * Returns GDR_ERR_SHAPE when max_chunks is smaller than the bound
+ * (total_tokens + num_seqs*(chunk_size-1)) / chunk_size.
+ */
+gdr_status gdr_prepare_chunks(const int32_t *cu_seqlens, int num_seqs, int total_tokens,
+                              int chunk_size, int32_t *chunk_indices, int64_t max_chunks,
+                              int32_t *chunk_offsets, int32_t *total_chunks, void *stream);
+
+/* Workspace bytes that gdr_fwd / gdr_bwd need for problem p (host-only; no
+ * device access).  The workspace must be 256-byte aligned. */
+gdr_status gdr_fwd_workspace_size(const gdr_problem *p, size_t *bytes);
+gdr_status gdr_bwd_workspace_size(const gdr_problem *p, size_t *bytes);
+
+/*
+ * Forward (chunk_gated_delta_rule_fwd: FlashQLA skill page, "Low-Level API").
+ *   in : q, k, v, g, beta (layouts above); h0 [N,Hv,K,V] fp32 or NULL (zero start)
+ *   out: o [B,T,Hv,V] (dtype)
+ *        final_state [N,Hv,K,V] fp32, or NULL when not wanted
+ *        g_cumsum [B,T,Hv] fp32: chunk-local inclusive cumsum of g (restarting at
+ *          every chunk and sequence start), or NULL
+ *        A [B,T,Hv,64] (dtype): row t mod 64 of its chunk's (I + L)^-1 with
+ *          L = strictly-lower(diag(beta) (k k^T o exp(G_r - G_s))), zero above the
+ *          diagonal and past the sequence end, or NULL
+ *        h [max_chunks,Hv,K,V] (dtype): the state before every chunk (row of chunk c
+ *          of sequence n = its chunk-table row), or NULL
+ *   g_cumsum and A are what gdr_bwd consumes; pass NULL for both in inference.
+ * State-shaped tensors (h0, final_state, h) use [..,V,K] with GDR_STATE_V_FIRST.
+ */
+gdr_status gdr_fwd(const gdr_problem *p, const void *q, const void *k, const void *v,
+                   const void *g, const void *beta, const float *h0, void *o, float *final_state,
+                   float *g_cumsum, void *A, void *h, void *workspace, size_t workspace_bytes,
+                   void *stream);
+
+/*
+ * Backward (chunk_gated_delta_rule_bwd: FlashQLA skill page, "Low-Level API";
+ * the gate argument is the forward's g_cumsum, as the FlashQLA documentation
+ * page's example passes the forward's returned g).
+ *   in : q, k, v, g_cumsum (fp32), beta, A (from gdr_fwd), dout [B,T,Hv,V],
+ *        dht [N,Hv,K,V] fp32 or NULL (zero), h0 [N,Hv,K,V] fp32 or NULL (zero)
+ *   out: dq, dk [B,T,Hq,K]; dv [B,T,Hv,V] (dtype); dg, dbeta [B,T,Hv] (gate_dtype;
+ *        dg is the gradient w.r.t. the raw per-token log-gate g);
+ *        dh0 [N,Hv,K,V] fp32 or NULL.
+ */
+gdr_status gdr_bwd(const gdr_problem *p, const void *q, const void *k, const void *v,
+                   const float *g_cumsum, const void *beta, const void *A, const void *dout,
+                   const float *dht, const float *h0, void *dq, void *dk, void *dv, void *dg,
+                   void *dbeta, float *dh0, void *workspace, size_t workspace_bytes,
+                   void *stream);
+
+/* Synchronises `stream`, then returns and clears the device error word of the
+ * current device (GDR_OK when no kernel latched an error), or GDR_ERR_CUDA when
+ * the stream reports a CUDA error. */
+gdr_status gdr_get_error(void *stream);
+
+/* Static text for a status code. */
+const char *gdr_status_string(gdr_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int gdr_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDR_H */

@@ -1,0 +1,60 @@
+"""Shared helpers for the parity tests: run the CUDA path and the oracle on
+the same seeded inputs and compare them by relative L2 error (fp64)."""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from gated_delta_rule_38_gb300.inputs import Workload, make_inputs
+
+# Acceptance bound: relative L2 error <= 8e-3 for every output and gradient
+# (PR #998 test plan: fwd+bwd ratio <= 0.008).
+TOL = 8e-3
+
+
+def rel_l2(got, want) -> float:
+    a = np.asarray(got, dtype=np.float64)
+    b = np.asarray(want, dtype=np.float64)
+    assert a.shape == b.shape, (a.shape, b.shape)
+    assert np.isfinite(a).all(), "non-finite values in the CUDA result"
+    den = np.linalg.norm(b.ravel())
+    return float(np.linalg.norm((a - b).ravel()) / max(den, 1e-300))
+
+
+def np64(t) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def oracle_problem(w: Workload, kernel_l2: bool) -> oracle.Problem:
+    return oracle.Problem(B=w.B, T=w.T, Hq=w.Hq, Hv=w.Hv, K=w.K, V=w.V, l2norm=kernel_l2,
+                          state_v_first=w.state_v_first, cu_seqlens=w.cu_seqlens)
+
+
+def to_dev(x, dev="cuda"):
+    return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
+
+
+def cu_tensor(w: Workload, dev="cuda"):
+    return None if w.cu_seqlens is None else torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
+
+
+def gpu_fwd(w: Workload, d, kernel_l2: bool, output_h=False, num_segments=0, gate_f32=False):
+    import gated_delta_rule_38_gb300 as gdr
+    g, beta = d["g"], d["beta"]
+    if gate_f32:
+        g, beta = g.float(), beta.float()
+    return gdr.chunk_gated_delta_rule_fwd(
+        d["q"], d["k"], d["v"], g, beta, initial_state=d["h0"], output_final_state=w.final_state,
+        cu_seqlens=cu_tensor(w), use_qk_l2norm_in_kernel=kernel_l2, state_v_first=w.state_v_first,
+        num_segments=num_segments, output_h=output_h)
+
+
+def gpu_bwd(w: Workload, d, gcs, A, kernel_l2: bool, num_segments=0, gate_f32=False):
+    import gated_delta_rule_38_gb300 as gdr
+    beta = d["beta"].float() if gate_f32 else d["beta"]
+    return gdr.chunk_gated_delta_rule_bwd(
+        d["q"], d["k"], d["v"], gcs, beta, A, d["do"], dht=d["dht"], initial_state=d["h0"],
+        cu_seqlens=cu_tensor(w), use_qk_l2norm_in_kernel=kernel_l2, state_v_first=w.state_v_first,
+        num_segments=num_segments)

@@ -1,0 +1,123 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+and rejects bad arguments on the host before touching a device.
+
+The rejection cases mirror the FlashQLA backend verifier's branches (PR #998
+"[GDN] Add FlashQLA backend dispatch": K != 128, V != 128, gate or beta
+activation in the kernel, negative eigenvalues, inter-card CP, fp32 inputs).
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_delta_rule_38_gb300 import _lib
+from gated_delta_rule_38_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return _lib.load()
+
+
+def prob(**kw):
+    p = _lib.Problem()
+    p.B, p.T, p.Hq, p.Hv, p.K, p.V = 2, 256, 4, 4, 128, 128
+    p.dtype = _lib.GDR_BF16
+    p.gate_dtype = _lib.GDR_BF16
+    p.scale = 128 ** -0.5
+    p.cu_seqlens = None
+    p.num_seqs = 0
+    p.flags = 0
+    p.num_segments = 0
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_exports_match_header(lib):
+    hdr = open(os.path.join(ROOT, "include", "gdr.h")).read()
+    declared = set(re.findall(r"^\s*(?:[\w\s\*]+?)\b(gdr_\w+)\s*\(", hdr, flags=re.M))
+    assert declared == set(_lib.EXPORTS)
+    for name in _lib.EXPORTS:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(12):
+        s = lib.gdr_status_string(code)
+        assert s and len(s) > 1
+    assert lib.gdr_version() >= 100
+
+
+def fwd_call(lib, p, ptr=0x100000, ws=0x200000, ws_bytes=1 << 40, **over):
+    args = dict(q=ptr, k=ptr, v=ptr, g=ptr, beta=ptr, h0=None, o=ptr, fin=None, gcs=None, A=None, h=None)
+    args.update(over)
+    return lib.gdr_fwd(ctypes.byref(p), args["q"], args["k"], args["v"], args["g"], args["beta"], args["h0"],
+                       args["o"], args["fin"], args["gcs"], args["A"], args["h"], ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("K", 64, 2), ("V", 64, 2), ("Hv", 6, 2), ("T", -1, 2), ("B", 0, 2),
+    ("dtype", _lib.GDR_FP32, 3), ("gate_dtype", _lib.GDR_FP16, 3),
+    ("flags", _lib.GDR_GATE_IN_KERNEL, 4), ("flags", _lib.GDR_BETA_SIGMOID_IN_KERNEL, 4),
+    ("flags", _lib.GDR_ALLOW_NEG_EIGVAL, 4), ("flags", _lib.GDR_INTER_CARD_CP, 4), ("flags", 1 << 20, 4),
+])
+def test_verifier_rejections(lib, field, value, status):
+    p = prob(**{field: value})
+    assert fwd_call(lib, p) == status
+    n = ctypes.c_size_t()
+    assert lib.gdr_fwd_workspace_size(ctypes.byref(p), ctypes.byref(n)) == status
+
+
+def test_packed_batch_needs_single_row(lib):
+    p = prob(cu_seqlens=0x100000, num_seqs=3)
+    assert fwd_call(lib, p) == 2
+    p = prob(B=1, cu_seqlens=0x100000, num_seqs=0)
+    assert fwd_call(lib, p) == 2
+
+
+def test_null_align_workspace(lib):
+    p = prob()
+    assert fwd_call(lib, p, q=None) == 1
+    assert fwd_call(lib, p, o=None) == 1
+    assert fwd_call(lib, p, k=0x100008) == 6
+    assert fwd_call(lib, p, ws=None) == 7
+    assert fwd_call(lib, p, ws_bytes=16) == 7
+    assert fwd_call(lib, p, ws=0x200010) == 6
+
+
+def test_valid_call_without_gpu_never_succeeds(lib):
+    """On a machine without a usable sm_103a device a valid call fails loudly."""
+    try:
+        import torch
+        if torch.cuda.is_available():
+            pytest.skip("a GPU is present")
+    except ImportError:
+        pass
+    assert fwd_call(lib, prob()) in (5, 10)
+
+
+def test_workspace_sizes_and_max_chunks(lib):
+    p = prob(B=2, T=4096, Hq=32, Hv=32)
+    assert lib.gdr_max_chunks(ctypes.byref(p)) == 128
+    n = ctypes.c_size_t()
+    assert lib.gdr_fwd_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0
+    tok = 2 * 4096 * 32
+    assert n.value >= tok * 4 + tok * 64 * 2
+    assert lib.gdr_bwd_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0
+    assert n.value >= 2 * 128 * 32 * 128 * 128 * 2
+    pv = prob(B=1, T=5311, Hq=32, Hv=32, cu_seqlens=0x100000, num_seqs=5)
+    assert lib.gdr_max_chunks(ctypes.byref(pv)) == (5311 + 5 * 63) // 64
+
+
+def test_prepare_chunks_host_checks(lib):
+    P = 0x100000
+    # table too small for the bound (T + N*(C-1)) / C
+    assert lib.gdr_prepare_chunks(P, 2, 8, 2, P, 4, P, P, None) == 2
+    assert lib.gdr_prepare_chunks(None, 2, 8, 2, P, 5, P, P, None) == 1
+    assert lib.gdr_prepare_chunks(P, 0, 8, 2, P, 5, P, P, None) == 2
