@@ -26,7 +26,8 @@ STATUS_NAMES = {
 
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ["gdr_max_chunks", "gdr_prepare_chunks", "gdr_fwd_workspace_size", "gdr_bwd_workspace_size",
-           "gdr_fwd", "gdr_bwd", "gdr_get_error", "gdr_status_string", "gdr_version"]
+           "gdr_fwd", "gdr_bwd", "gdr_get_error", "gdr_status_string", "gdr_version", "gdr_profile_enable",
+           "gdr_profile_read"]
 
 
 class Problem(ctypes.Structure):
@@ -79,6 +80,11 @@ def load() -> ctypes.CDLL:
         lib.gdr_get_error.restype = i32
         lib.gdr_status_string.argtypes = [i32]
         lib.gdr_status_string.restype = ctypes.c_char_p
+        lib.gdr_profile_enable.argtypes = [i32]
+        lib.gdr_profile_enable.restype = i32
+        lib.gdr_profile_read.argtypes = [i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_longlong),
+                                         ctypes.POINTER(ctypes.c_double)]
+        lib.gdr_profile_read.restype = i32
         lib.gdr_version.argtypes = []
         lib.gdr_version.restype = i32
         _lib = lib
@@ -95,3 +101,20 @@ def status_string(st: int) -> str:
 def check(st: int, where: str) -> None:
     if st != 0:
         raise GdrError(st, where)
+
+
+def profile_enable(on: bool) -> None:
+    load().gdr_profile_enable(1 if on else 0)
+
+
+def profile_read() -> dict:
+    """{kernel name: (launches, total ms)} of the launches timed since profile_enable(True)."""
+    lib = load()
+    cap = 32
+    names = (ctypes.c_char_p * cap)()
+    cnt = (ctypes.c_longlong * cap)()
+    ms = (ctypes.c_double * cap)()
+    n = lib.gdr_profile_read(cap, names, cnt, ms)
+    if n < 0:
+        raise RuntimeError("gdr_profile_read failed")
+    return {names[i].decode(): (int(cnt[i]), float(ms[i])) for i in range(min(n, cap))}

@@ -5,6 +5,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 #include "launch.h"
@@ -208,15 +209,65 @@ gdr_status check_ws(const Layout &L, void *ws, size_t bytes) {
 
 gdr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA; }
 
+// ---- per-kernel timing: event pairs recorded around each launch while enabled
+enum KernelId { K_PREP = 0, K_WY_FWD, K_CHAIN_FWD, K_CHAIN_FWD_RECOMPUTE, K_CHAIN_BWD, K_BWD_CHUNK, K_COUNT };
+const char *const kKernelNames[K_COUNT] = {"prep_chunks", "wy_fwd", "chain_fwd", "chain_fwd_recompute",
+                                           "chain_bwd", "bwd_chunk"};
+struct Pending {
+    int id;
+    cudaEvent_t a, b;
+};
+struct Profiler {
+    std::mutex mu;
+    bool on = false;
+    std::vector<Pending> pending;
+    std::vector<cudaEvent_t> pool;
+    double ms[K_COUNT] = {};
+    long long count[K_COUNT] = {};
+} g_prof;
+
+cudaEvent_t prof_event() {
+    if (!g_prof.pool.empty()) {
+        cudaEvent_t e = g_prof.pool.back();
+        g_prof.pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+// Launch through f, bracketed by events when profiling is on.
+template <typename F>
+gdr_status timed(int id, cudaStream_t s, F &&f) {
+    cudaEvent_t a = nullptr, b = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_prof.mu);
+        if (g_prof.on) {
+            a = prof_event();
+            b = prof_event();
+        }
+    }
+    if (a) cudaEventRecord(a, s);
+    const cudaError_t e = f();
+    if (b) {
+        cudaEventRecord(b, s);
+        std::lock_guard<std::mutex> lk(g_prof.mu);
+        g_prof.pending.push_back(Pending{id, a, b});
+    }
+    return cuda_status(e);
+}
+
 // Build the varlen chunk tables in the workspace (no-op for dense batches).
 gdr_status tables(const gdr_problem *p, Args &a, char *ws, const Layout &L, cudaStream_t s) {
     if (!p->cu_seqlens) return GDR_OK;
     a.cidx = reinterpret_cast<int32_t *>(ws + L.idx);
     a.coff = reinterpret_cast<int32_t *>(ws + L.off);
     a.ctotal = reinterpret_cast<int32_t *>(ws + L.total);
-    return cuda_status(launch_prep_chunks(p->cu_seqlens, p->num_seqs, p->T, C, const_cast<int32_t *>(a.cidx),
-                                          a.max_chunks, const_cast<int32_t *>(a.coff),
-                                          const_cast<int32_t *>(a.ctotal), a.err, s));
+    return timed(K_PREP, s, [&] {
+        return launch_prep_chunks(p->cu_seqlens, p->num_seqs, p->T, C, const_cast<int32_t *>(a.cidx), a.max_chunks,
+                                  const_cast<int32_t *>(a.coff), const_cast<int32_t *>(a.ctotal), a.err, s);
+    });
 }
 
 }  // namespace
@@ -283,8 +334,9 @@ gdr_status gdr_fwd(const gdr_problem *p, const void *q, const void *k, const voi
     if ((st = tables(p, a, ws, L, s)) != GDR_OK) return st;
     float *gcs = g_cumsum ? g_cumsum : reinterpret_cast<float *>(ws + L.gcs);
     void *Aw = A ? A : static_cast<void *>(ws + L.A);
-    if ((st = cuda_status(launch_wy_fwd(a, k, g, beta, gcs, Aw, s))) != GDR_OK) return st;
-    return cuda_status(launch_chain_fwd(a, q, k, v, gcs, beta, Aw, h0, o, final_state, h, true, s));
+    if ((st = timed(K_WY_FWD, s, [&] { return launch_wy_fwd(a, k, g, beta, gcs, Aw, s); })) != GDR_OK) return st;
+    return timed(K_CHAIN_FWD, s,
+                 [&] { return launch_chain_fwd(a, q, k, v, gcs, beta, Aw, h0, o, final_state, h, true, s); });
 }
 
 gdr_status gdr_bwd(const gdr_problem *p, const void *q, const void *k, const void *v, const float *g_cumsum,
@@ -309,12 +361,16 @@ gdr_status gdr_bwd(const gdr_problem *p, const void *q, const void *k, const voi
     void *hw = ws + L.h, *dhw = ws + L.dhn;
     // states before every chunk (recomputed), then the reverse state-gradient chain,
     // then every chunk's gradients in parallel
-    if ((st = cuda_status(launch_chain_fwd(a, q, k, v, g_cumsum, beta, A, h0, nullptr, nullptr, hw, false, s))) !=
-        GDR_OK)
+    if ((st = timed(K_CHAIN_FWD_RECOMPUTE, s, [&] {
+             return launch_chain_fwd(a, q, k, v, g_cumsum, beta, A, h0, nullptr, nullptr, hw, false, s);
+         })) != GDR_OK)
         return st;
-    if ((st = cuda_status(launch_chain_bwd(a, q, k, g_cumsum, beta, A, dout, dht, dhw, dh0, s))) != GDR_OK)
+    if ((st = timed(K_CHAIN_BWD, s,
+                    [&] { return launch_chain_bwd(a, q, k, g_cumsum, beta, A, dout, dht, dhw, dh0, s); })) != GDR_OK)
         return st;
-    return cuda_status(launch_bwd_chunk(a, q, k, v, g_cumsum, beta, A, dout, hw, dhw, dq, dk, dv, dg, dbeta, s));
+    return timed(K_BWD_CHUNK, s, [&] {
+        return launch_bwd_chunk(a, q, k, v, g_cumsum, beta, A, dout, hw, dhw, dq, dk, dv, dg, dbeta, s);
+    });
 }
 
 gdr_status gdr_get_error(void *stream) {
@@ -349,5 +405,43 @@ const char *gdr_status_string(gdr_status s) {
 }
 
 int gdr_version(void) { return 100; }
+
+gdr_status gdr_profile_enable(int on) {
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    if (on) {
+        for (int i = 0; i < K_COUNT; ++i) {
+            g_prof.ms[i] = 0.0;
+            g_prof.count[i] = 0;
+        }
+    }
+    g_prof.on = on != 0;
+    return GDR_OK;
+}
+
+int gdr_profile_read(int max, const char **names, long long *launches, double *ms) {
+    std::lock_guard<std::mutex> lk(g_prof.mu);
+    int rc = 0;
+    for (const Pending &pd : g_prof.pending) {
+        float t = 0.f;
+        if (cudaEventSynchronize(pd.b) != cudaSuccess || cudaEventElapsedTime(&t, pd.a, pd.b) != cudaSuccess) rc = -1;
+        g_prof.ms[pd.id] += t;
+        g_prof.count[pd.id] += 1;
+        g_prof.pool.push_back(pd.a);
+        g_prof.pool.push_back(pd.b);
+    }
+    g_prof.pending.clear();
+    if (rc < 0) return -1;
+    int n = 0;
+    for (int i = 0; i < K_COUNT; ++i) {
+        if (g_prof.count[i] == 0) continue;
+        if (n < max) {
+            if (names) names[n] = kKernelNames[i];
+            if (launches) launches[n] = g_prof.count[i];
+            if (ms) ms[n] = g_prof.ms[i];
+        }
+        ++n;
+    }
+    return n;
+}
 
 }  // extern "C"

@@ -271,20 +271,50 @@ __device__ __forceinline__ void load_rows_async(const Tile &t, const T *src, lon
 
 // In-place per-row L2 normalisation of a [rows x 128] tile: x / sqrt(sum x^2 + eps),
 // computed in fp32 and rounded once.  One warp per row; identical in every kernel.
+// Each warp takes 8 rows at a time: lane l handles a quarter (32 values) of row l/4.
 template <typename T>
 __device__ __forceinline__ void l2norm_rows(const Tile &t, int rows, int warp, int nwarps, int lane) {
-    for (int r = warp; r < rows; r += nwarps) {
-        const uint32_t a0 = t.addr(r, lane * 4);
-        const uint32_t u0 = lds32(a0), u1 = lds32(a0 + 4);
-        const float2 x0 = Elt<T>::unpack(u0), x1 = Elt<T>::unpack(u1);
-        float ss = x0.x * x0.x + x0.y * x0.y + x1.x * x1.x + x1.y * x1.y;
+    const int rq = lane >> 2, qq = lane & 3;
+    for (int r0 = warp * 8; r0 < rows; r0 += nwarps * 8) {
+        const int r = r0 + rq;
+        uint4 u[4];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t a = t.addr(r, qq * 32 + c * 8);
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                         : "=r"(u[c].x), "=r"(u[c].y), "=r"(u[c].z), "=r"(u[c].w)
+                         : "r"(a));
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 x = Elt<T>::unpack(w[e]);
+                ss += x.x * x.x + x.y * x.y;
+            }
+        }
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
         const float inv = 1.0f / sqrtf(ss + L2_EPS);
-        sts32(a0, Elt<T>::pack(x0.x * inv, x0.y * inv));
-        sts32(a0 + 4, Elt<T>::pack(x1.x * inv, x1.y * inv));
+        if (r < rows) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 x = Elt<T>::unpack(w[e]);
+                    w[e] = Elt<T>::pack(x.x * inv, x.y * inv);
+                }
+                const uint32_t a = t.addr(r, qq * 32 + c * 8);
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(a), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                             "r"(w[3]));
+            }
+        }
     }
 }
+
 
 // ---------------------------------------------------------------- chunk geometry
 

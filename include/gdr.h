@@ -159,6 +159,19 @@ gdr_status gdr_get_error(void *stream);
 /* Static text for a status code. */
 const char *gdr_status_string(gdr_status s);
 
+/*
+ * Per-kernel timing (tracing).  gdr_profile_enable(1) clears the counters and
+ * from then on brackets every kernel the library launches with a pair of CUDA
+ * events recorded on the launch stream (the library owns the events);
+ * gdr_profile_enable(0) stops recording.  gdr_profile_read synchronises on
+ * the pending events, folds them into per-kernel totals and copies up to
+ * `max` entries: kernel name (static string), launch count and summed
+ * milliseconds.  Returns the number of distinct kernels (may exceed max), or
+ * -1 on a CUDA error.  Timing adds two event records per launch.
+ */
+gdr_status gdr_profile_enable(int on);
+int gdr_profile_read(int max, const char **names, long long *launches, double *ms);
+
 /* Library version, major*10000 + minor*100 + patch. */
 int gdr_version(void);
 

@@ -1,0 +1,115 @@
+"""Backward parity: the CUDA path (through the C ABI) against the fp64 oracle's
+reverse-mode gradients, on the same seeded inputs."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_delta_rule_38_gb300.inputs import WORKLOADS, custom, make_inputs
+from harness import TOL, gpu_bwd, gpu_fwd, np64, oracle_problem, rel_l2, to_dev
+
+pytestmark = pytest.mark.gpu
+
+GRADS = ("dq", "dk", "dv", "dbeta", "dg", "dh0")
+
+
+def check_bwd(w, kernel_l2, heads=None, gate_f32=False, num_segments=0):
+    x = make_inputs(w)
+    d = to_dev(x)
+    gcs, A, o, _, fin = gpu_fwd(w, d, kernel_l2, num_segments=num_segments, gate_f32=gate_f32)
+    dq, dk, dv, db, dg, dh0 = gpu_bwd(w, d, gcs, A, kernel_l2, num_segments=num_segments, gate_f32=gate_f32)
+    torch.cuda.synchronize()
+    pb = oracle_problem(w, kernel_l2)
+    ref = oracle.bwd(pb, x["q"], x["k"], x["v"], x["g"], x["beta"], x["do"], h0=x["h0"], dht=x["dht"],
+                     heads=heads)
+    got = {"dq": dq, "dk": dk, "dv": dv, "dbeta": db, "dg": dg, "dh0": dh0}
+    if heads is None:
+        vsel = qsel = slice(None)
+    else:
+        grp = w.Hv // w.Hq
+        vsel = list(heads)
+        qsel = sorted({h // grp for h in heads})
+    errs = {}
+    for key in GRADS:
+        if got[key] is None:
+            assert x["h0"] is None and key == "dh0"
+            continue
+        a = np64(got[key])
+        b = ref[key]
+        if key in ("dq", "dk"):
+            a, b = a[:, :, qsel], b[:, :, qsel]
+        elif key == "dh0":
+            a, b = a[:, vsel], b[:, vsel]
+        else:
+            a, b = a[:, :, vsel], b[:, :, vsel]
+        errs[key] = rel_l2(a, b)
+    for key, e in errs.items():
+        assert e <= TOL, (key, e, errs)
+    return errs
+
+
+def test_tiny():
+    check_bwd(WORKLOADS["tiny"], kernel_l2=False)
+
+
+def test_tiny_kernel_l2norm():
+    check_bwd(custom(B=1, T=256, Hq=2, Hv=2, host_l2=False), kernel_l2=True)
+
+
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 129, 200])
+def test_ragged_lengths(T):
+    check_bwd(custom(B=2, T=T, Hq=1, Hv=2, host_l2=False), kernel_l2=True)
+
+
+def test_varlen_with_empty_and_short_sequences():
+    check_bwd(custom(seq_lens=(7, 0, 130, 64, 1, 65), Hq=2, Hv=2), kernel_l2=False)
+
+
+def test_gva_fp16():
+    check_bwd(custom(B=2, T=150, Hq=1, Hv=4, dtype=torch.float16, host_l2=False), kernel_l2=True)
+
+
+def test_fp32_gates():
+    check_bwd(custom(B=1, T=190, Hq=2, Hv=2), kernel_l2=False, gate_f32=True)
+
+
+def test_no_initial_state():
+    check_bwd(custom(B=1, T=100, Hq=1, Hv=1, has_h0=False, final_state=False), kernel_l2=False)
+
+
+def test_state_v_first_bit_exact():
+    w = custom(B=2, T=150, Hq=1, Hv=2, dtype=torch.float16)
+    d = to_dev(make_inputs(w))
+    gcs, A, _, _, _ = gpu_fwd(w, d, False)
+    ga = gpu_bwd(w, d, gcs, A, False)
+    wt = custom(B=2, T=150, Hq=1, Hv=2, dtype=torch.float16, state_v_first=True)
+    dt = dict(d)
+    dt["h0"] = d["h0"].transpose(-1, -2).contiguous()
+    dt["dht"] = d["dht"].transpose(-1, -2).contiguous()
+    gb = gpu_bwd(wt, dt, gcs, A, False)
+    torch.cuda.synchronize()
+    for a, b in zip(ga[:5], gb[:5]):
+        assert torch.equal(a, b)
+    assert torch.equal(ga[5], gb[5].transpose(-1, -2))
+
+
+def test_autograd_function():
+    import gated_delta_rule_38_gb300 as gdr
+    w = custom(B=1, T=130, Hq=1, Hv=2, host_l2=False)
+    x = make_inputs(w)
+    d = {k: (v.cuda().requires_grad_(True) if v is not None and k in ("q", "k", "v", "g", "beta", "h0") else
+             (v.cuda() if v is not None else None)) for k, v in x.items()}
+    o, fin = gdr.chunk_gated_delta_rule(d["q"], d["k"], d["v"], d["g"], d["beta"], initial_state=d["h0"],
+                                        output_final_state=True, use_qk_l2norm_in_kernel=True)
+    (o.float() * d["do"].float()).sum().add_((fin * d["dht"]).sum()).backward()
+    pb = oracle_problem(w, True)
+    ref = oracle.bwd(pb, x["q"], x["k"], x["v"], x["g"], x["beta"], x["do"], h0=x["h0"], dht=x["dht"])
+    for name, key in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("g", "dg"), ("beta", "dbeta"), ("h0", "dh0")):
+        assert rel_l2(np64(d[name].grad), ref[key]) <= TOL, name
+
+
+@pytest.mark.parametrize("name,heads", [("dense", [0, 17]), ("varlen", [5]), ("gva", [6, 7]), ("long", [3])])
+def test_full_size_sampled_heads(name, heads):
+    w = WORKLOADS[name]
+    check_bwd(w, kernel_l2=not w.host_l2, heads=heads)
