@@ -148,7 +148,7 @@ int64_t max_chunks_of(const gdr_problem *p) {
 }
 
 struct Layout {
-    size_t idx = 0, off = 0, total = 0, gcs = 0, A = 0, h = 0, dhn = 0, bytes = 0;
+    size_t idx = 0, off = 0, total = 0, gcs = 0, A = 0, h = 0, dhn = 0, delta = 0, ddelta = 0, D = 0, hT = 0, bytes = 0;
 };
 
 // Workspace: [varlen chunk tables][fwd: g_cumsum, A scratch | bwd: states, state gradients].
@@ -176,6 +176,15 @@ Layout layout_of(const gdr_problem *p, bool bwd) {
         at = round_up(at + st, 256);
         L.dhn = at;
         at = round_up(at + st, 256);
+        const size_t dsz = (size_t)mc * p->Hv * C * DV * esize(p->dtype);
+        L.delta = at;
+        at = round_up(at + dsz, 256);
+        L.ddelta = at;
+        at = round_up(at + dsz, 256);
+        L.D = at;
+        at = round_up(at + tok * p->Hv * sizeof(float), 256);
+        L.hT = at;
+        at = round_up(at + (size_t)num_seqs(p) * p->Hv * DK * DV * sizeof(float), 256);
     }
     L.bytes = at;
     return L;
@@ -210,9 +219,9 @@ gdr_status check_ws(const Layout &L, void *ws, size_t bytes) {
 gdr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA; }
 
 // ---- per-kernel timing: event pairs recorded around each launch while enabled
-enum KernelId { K_PREP = 0, K_WY_FWD, K_CHAIN_FWD, K_CHAIN_FWD_RECOMPUTE, K_CHAIN_BWD, K_BWD_CHUNK, K_COUNT };
-const char *const kKernelNames[K_COUNT] = {"prep_chunks", "wy_fwd", "chain_fwd", "chain_fwd_recompute",
-                                           "chain_bwd", "bwd_chunk"};
+enum KernelId { K_PREP = 0, K_WY_FWD, K_CHAIN_FWD, K_CHAIN_FWD_RECOMPUTE, K_CHAIN_BWD, K_BWD_CHUNK, K_DG_SCAN, K_COUNT };
+const char *const kKernelNames[K_COUNT] = {"prep_chunks", "wy_fwd",    "chain_fwd", "chain_fwd_recompute",
+                                           "chain_bwd",   "bwd_chunk", "dg_scan"};
 struct Pending {
     int id;
     cudaEvent_t a, b;
@@ -336,7 +345,7 @@ gdr_status gdr_fwd(const gdr_problem *p, const void *q, const void *k, const voi
     void *Aw = A ? A : static_cast<void *>(ws + L.A);
     if ((st = timed(K_WY_FWD, s, [&] { return launch_wy_fwd(a, k, g, beta, gcs, Aw, s); })) != GDR_OK) return st;
     return timed(K_CHAIN_FWD, s,
-                 [&] { return launch_chain_fwd(a, q, k, v, gcs, beta, Aw, h0, o, final_state, h, true, s); });
+                 [&] { return launch_chain_fwd(a, q, k, v, gcs, beta, Aw, h0, o, final_state, h, true, nullptr, s); });
 }
 
 gdr_status gdr_bwd(const gdr_problem *p, const void *q, const void *k, const void *v, const float *g_cumsum,
@@ -358,19 +367,25 @@ gdr_status gdr_bwd(const gdr_problem *p, const void *q, const void *k, const voi
     char *ws = static_cast<char *>(workspace);
     Args a = make_args(p, err);
     if ((st = tables(p, a, ws, L, s)) != GDR_OK) return st;
-    void *hw = ws + L.h, *dhw = ws + L.dhn;
-    // states before every chunk (recomputed), then the reverse state-gradient chain,
-    // then every chunk's gradients in parallel
+    void *hw = ws + L.h, *dhw = ws + L.dhn, *dlw = ws + L.delta, *ddlw = ws + L.ddelta;
+    float *Dw = reinterpret_cast<float *>(ws + L.D), *hTw = reinterpret_cast<float *>(ws + L.hT);
+    // states and Delta of every chunk (recomputed), the reverse state-gradient chain, every chunk's
+    // gradients in parallel, then the sequence-level gate gradient
     if ((st = timed(K_CHAIN_FWD_RECOMPUTE, s, [&] {
-             return launch_chain_fwd(a, q, k, v, g_cumsum, beta, A, h0, nullptr, nullptr, hw, false, s);
+             return launch_chain_fwd(a, q, k, v, g_cumsum, beta, A, h0, nullptr, dht ? hTw : nullptr, hw, false, dlw,
+                                     s);
          })) != GDR_OK)
         return st;
-    if ((st = timed(K_CHAIN_BWD, s,
-                    [&] { return launch_chain_bwd(a, q, k, g_cumsum, beta, A, dout, dht, dhw, dh0, s); })) != GDR_OK)
+    if ((st = timed(K_CHAIN_BWD, s, [&] {
+             return launch_chain_bwd(a, q, k, g_cumsum, beta, A, dout, dht, dhw, ddlw, dh0, s);
+         })) != GDR_OK)
         return st;
-    return timed(K_BWD_CHUNK, s, [&] {
-        return launch_bwd_chunk(a, q, k, v, g_cumsum, beta, A, dout, hw, dhw, dq, dk, dv, dg, dbeta, s);
-    });
+    if ((st = timed(K_BWD_CHUNK, s, [&] {
+             return launch_bwd_chunk_tc(a, q, k, v, g_cumsum, beta, A, dout, hw, dhw, dlw, ddlw, dq, dk, dv, dbeta, Dw,
+                                        s);
+         })) != GDR_OK)
+        return st;
+    return timed(K_DG_SCAN, s, [&] { return launch_dg_scan(a, Dw, dht, hTw, dg, s); });
 }
 
 gdr_status gdr_get_error(void *stream) {

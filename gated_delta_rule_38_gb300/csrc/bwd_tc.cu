@@ -1,0 +1,704 @@
+// Per-chunk gradients of the chunked gated delta rule on tcgen05, and the
+// sequence-level gate-gradient pass.
+//
+// bwd_chunk_tc: one CTA of 256 threads per (chunk, q/k head), visiting the value
+// heads of the group in order.  Tokens are the rows of every product.  Two 64-row
+// operands that share their B operand are stacked into one M=128 MMA, so TMEM
+// lanes 0..63 hold one result and lanes 64..127 the other; dq rows accumulate in
+// the registers of the lane-0..63 threads and dk rows in those of the
+// lane-64..127 threads (each thread holds half a row).  With h the state before
+// the chunk, dH' the gradient after it, Delta and dDelta from the two chains:
+//
+//   round 1: [dO;dDelta] h^T        -> dq += scale e^{G} dO h^T ;  dW = -dDelta h^T
+//            [V;Delta] dH'^T        -> dk += e^{Gl-G} Delta dH'^T
+//            [dO;dDelta] [V;Delta]^T-> dP = dO Delta^T (-> dS = scale dP o Gamma o M), dA2 = dDelta V^T
+//            [Q;K] K^T              -> KK^T
+//   round 2: [A^T;(A diag(beta e^G))^T] [dDelta | dW]
+//                                   -> dv = beta A^T dDelta, A^T dW (dbeta), dk += diag(beta e^G) A^T dW
+//            dW K^T                 -> dA = (dW K^T diag(e^G) + dDelta V^T) diag(beta), strictly lower
+//   round 3: dA A^T -> X ;  dq += dS K ;  dk += dS^T Q
+//   round 4: dL = -A^T X ;  dKK = dL o beta_r Gamma  ;  dbeta += sum_s dL Gamma KK
+//   round 5: dk += dKK K + dKK^T K
+//
+// dbeta_r = e^{G_r} <(A^T dW)_r, k_r> + <(A^T dDelta)_r, v_r> + sum_s dL_rs Gamma_rs KK_rs.
+// The gate gradient uses the exact identity that follows from h_t = e^{G_t} h~_t
+// (the gate enters only through e^{G_t} q_t, e^{-G_t} v_t and the final state):
+//   dg_s = sum_{t >= s} (<q_t, dq_t> - <v_t, dv_t>) + <dh_T, h_T>
+// per sequence and value head (q, dq before the L2-norm chain rule); this kernel
+// writes D_t = <q_t, dq_t> - <v_t, dv_t> and dg_scan finishes the reverse sum.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "umma.cuh"
+
+namespace gdr {
+namespace {
+
+constexpr int NT = 256;
+// ---- shared memory (bytes from a 1024-aligned base)
+constexpr uint32_t S_Q0 = 0, S_K0 = 8192;             // [Q b0][K b0][Q b1][K b1]
+constexpr uint32_t S_DO0 = 32768, S_DD0 = 40960;      // [dO b0][dDelta b0][dO b1][dDelta b1]
+constexpr uint32_t S_X = 65536, S_DW0 = 73728, S_DS = 81920, S_DW1 = 90112;
+constexpr uint32_t S_V0 = 98304, S_D0 = 106496;       // [V b0][Delta b0][V b1][Delta b1]
+constexpr uint32_t S_DA = S_D0, S_DKK = S_D0 + 16384; // reuse Delta's blocks after round 1
+constexpr uint32_t S_H = 131072, S_DH = 163840;       // [128 x 64] blocks of 16 KB
+constexpr uint32_t S_A = 196608, S_AKG = 204800;
+constexpr uint32_t S_F = 212992;                      // scalars
+constexpr uint32_t S_BAR = S_F + 16 * 64 * 4, S_SLOT = S_BAR + 8, S_FLAG = S_SLOT + 4, S_USED = S_FLAG + 4;
+constexpr uint32_t S_BYTES = S_USED + 1024;
+// scalar slots (64 floats each)
+enum { F_G = 0, F_B, F_EG, F_EL, F_QD0, F_QD1, F_VD0, F_VD1, F_KD0, F_KD1, F_LB0, F_LB1 };
+// TMEM columns
+constexpr uint32_t T_R1 = 0, T_R2 = 128, T_R3 = 256, T_R4 = 384, T_R8 = 448, T_COLS = 512;
+
+template <typename T> struct IsBf16 { static constexpr bool value = false; };
+template <> struct IsBf16<__nv_bfloat16> { static constexpr bool value = true; };
+
+struct BcP {
+    const void *q, *k, *v, *A, *beta, *dout, *h, *dhn, *delta, *ddelta;
+    const float *g_cs;
+    void *dq, *dk, *dv, *dbeta;
+    float *D;  // [tokens, Hv] fp32
+    bool gate_f32, l2norm;
+    float scale;
+};
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, bool valid) {
+    const int n = valid ? 4 : 0;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(n));
+}
+
+// rows x 128 (16-bit) from global into two swizzled 64-column blocks `bstride` apart
+template <typename T>
+__device__ __forceinline__ void load_rows128(uint32_t dst, uint32_t bstride, const T *src, long long stride, int rows,
+                                             int valid, int tid) {
+    for (int i = tid; i < rows * 16; i += NT) {
+        const int r = i >> 4, c = i & 15;
+        const bool ok = r < valid;
+        cp_async16(dst + (uint32_t)(c >> 3) * bstride + umma::off(r, (c & 7) * 8, 0), ok ? src + r * stride + c * 8 : src,
+                   ok);
+    }
+}
+template <typename T>
+__device__ __forceinline__ void load_rows64(uint32_t dst, const T *src, long long stride, int valid, int tid) {
+    for (int i = tid; i < 64 * 8; i += NT) {
+        const int r = i >> 3, c = i & 7;
+        const bool ok = r < valid;
+        cp_async16(dst + umma::off(r, c * 8, 0), ok ? src + r * stride + c * 8 : src, ok);
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void store16(uint32_t base, int row, int col0, const float *x) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+        umma::st_shared_v4(base + umma::off(row, col0 + c * 8, 0), Elt<T>::pack(x[c * 8], x[c * 8 + 1]),
+                           Elt<T>::pack(x[c * 8 + 2], x[c * 8 + 3]), Elt<T>::pack(x[c * 8 + 4], x[c * 8 + 5]),
+                           Elt<T>::pack(x[c * 8 + 6], x[c * 8 + 7]));
+}
+
+// 16 values of row `row`, columns col0.. of a swizzled tile, as floats.
+template <typename T>
+__device__ __forceinline__ void load16(uint32_t base, int row, int col0, float *x) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const uint4 u = umma::ld_shared_v4(base + umma::off(row, col0 + c * 8, 0));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = Elt<T>::unpack(w[e]);
+            x[c * 8 + 2 * e] = f.x;
+            x[c * 8 + 2 * e + 1] = f.y;
+        }
+    }
+}
+
+// In-place L2 normalisation of 64 rows of a [64 x 128] swizzled tile (blocks 16 KB apart).
+template <typename T>
+__device__ __forceinline__ void l2norm64(uint32_t base, int rows, int warp, int lane) {
+    const int rq = lane >> 2, qq = lane & 3;
+    const int r = warp * 8 + rq;  // 8 warps x 8 rows
+    uint32_t addr[4];
+    uint4 u[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int ch = qq * 4 + c;
+        addr[c] = base + (uint32_t)(ch >> 3) * 16384u + umma::off(r, (ch & 7) * 8, 0);
+        u[c] = umma::ld_shared_v4(addr[c]);
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 x = Elt<T>::unpack(w[e]);
+            ss += x.x * x.x + x.y * x.y;
+        }
+    }
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    const float inv = 1.0f / sqrtf(ss + L2_EPS);
+    if (r < rows) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 x = Elt<T>::unpack(w[e]);
+                w[e] = Elt<T>::pack(x.x * inv, x.y * inv);
+            }
+            umma::st_shared_v4(addr[c], w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+// dx = (dxh - xh (xh . dxh)) / n with n = sqrt(sum x^2 + eps), xh = x / n; one warp per row.
+template <typename T>
+__device__ __forceinline__ void l2norm_bwd_rows(const float *src, const T *x, long long stride, T *dst, int valid,
+                                                bool l2norm, int warp, int nwarps, int lane) {
+    for (int r = warp; r < valid; r += nwarps) {
+        const T *xr = x + (long long)r * stride;
+        T *dr = dst + (long long)r * stride;
+        float xv[4], gv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            xv[u] = Elt<T>::to_f(xr[lane * 4 + u]);
+            gv[u] = src[r * DK + lane * 4 + u];
+        }
+        if (l2norm) {
+            float ss = xv[0] * xv[0] + xv[1] * xv[1] + xv[2] * xv[2] + xv[3] * xv[3];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            const float inv = 1.0f / sqrtf(ss + L2_EPS);
+            float dot = 0.f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) dot += xv[u] * inv * gv[u];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) gv[u] = (gv[u] - xv[u] * inv * dot) * inv;
+        }
+        uint2 w;
+        w.x = Elt<T>::pack(gv[0], gv[1]);
+        w.y = Elt<T>::pack(gv[2], gv[3]);
+        *reinterpret_cast<uint2 *>(dr + lane * 4) = w;
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, BcP p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem =
+        reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    long long tok0;
+    int valid, n, ci;
+    const int slot = blockIdx.x;
+    if (!geo.chunk(slot, tok0, valid, n, ci)) return;
+    const int hq = blockIdx.y, Hv = geo.Hv, Hq = geo.Hq, grp = Hv / Hq;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int L = (warp & 3) * 32 + lane, hh = warp >> 2, lb = (warp & 3) * 32;
+    const bool upper = L >= 64;
+    const int r = L & 63;  // token row of this thread's TMEM lane
+    constexpr bool bf16 = IsBf16<T>::value;
+    const T *q = static_cast<const T *>(p.q);
+    const T *k = static_cast<const T *>(p.k);
+    const T *v = static_cast<const T *>(p.v);
+    const T *A = static_cast<const T *>(p.A);
+    const T *dout = static_cast<const T *>(p.dout);
+    const T *hs = static_cast<const T *>(p.h);
+    const T *dhs = static_cast<const T *>(p.dhn);
+    const T *dl = static_cast<const T *>(p.delta);
+    const T *ddl = static_cast<const T *>(p.ddelta);
+    float *F = reinterpret_cast<float *>(smem + S_F);
+    auto f = [&](int slot_, int i) -> float & { return F[slot_ * 64 + i]; };
+    const uint32_t bar = sb + S_BAR;
+    volatile int *sflag = reinterpret_cast<volatile int *>(smem + S_FLAG);
+
+    if (tid == 0) {
+        umma::mbar_init(bar, 1);
+        umma::fence_mbar_init();
+        *sflag = 0;
+    }
+    if (warp == 0) umma::alloc(sb + S_SLOT, T_COLS);
+    load_rows128<T>(sb + S_Q0, 16384, q + (tok0 * Hq + hq) * DK, (long long)Hq * DK, 64, valid, tid);
+    load_rows128<T>(sb + S_K0, 16384, k + (tok0 * Hq + hq) * DK, (long long)Hq * DK, 64, valid, tid);
+    cp_async_commit();
+    umma::fence_before();
+    __syncthreads();
+    umma::fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + S_SLOT);
+
+    // instruction descriptors
+    const uint32_t i_n128 = umma::idesc(128, 128, bf16, false, false);
+    const uint32_t i_n64 = umma::idesc(128, 64, bf16, false, false);
+    const uint32_t i_n256_mn = umma::idesc(128, 256, bf16, true, true);
+    const uint32_t i_n128_bmn = umma::idesc(128, 128, bf16, false, true);
+    const uint32_t i_n128_mn = umma::idesc(128, 128, bf16, true, true);
+    const uint32_t i_n64_mn = umma::idesc(128, 64, bf16, true, true);
+    // operand descriptors (K-major: sbo 1024; MN-major: lbo = distance between 64-wide blocks)
+    const uint64_t dDOa = umma::desc(sb + S_DO0, 16, 1024);         // [dO; dDelta] rows, K = value
+    const uint64_t dH = umma::desc(sb + S_H, 16, 1024);             // h[d][e]: n = d, k = e
+    const uint64_t dVa = umma::desc(sb + S_V0, 16, 1024);           // [V; Delta] rows, K = value
+    const uint64_t dDH = umma::desc(sb + S_DH, 16, 1024);           // dH'[d][e]
+    const uint64_t dQa = umma::desc(sb + S_Q0, 16, 1024);           // [Q; K] rows, K = key
+    const uint64_t dKa = umma::desc(sb + S_K0, 16, 1024);           // K rows (n = token), K = key
+    const uint64_t dAmn = umma::desc(sb + S_A, 8192, 1024);         // [A^T; AKG^T] (m = row), k = token
+    const uint64_t dDDmn = umma::desc(sb + S_DD0, 16384, 1024);     // [dDelta | dW] (n = col), k = token
+    const uint64_t dWup = umma::desc(sb + S_DW0 - 8192, 16, 1024);  // rows 64..127 = dW, K = key
+    const uint64_t dDA = umma::desc(sb + S_DA, 16, 1024);           // dA rows, K = token
+    const uint64_t dAk = umma::desc(sb + S_A, 16, 1024);            // A rows as K-major B (n = token)
+    const uint64_t dDS = umma::desc(sb + S_DS, 16, 1024);           // dS rows (lanes 0..63)
+    const uint64_t dKmn = umma::desc(sb + S_K0, 16384, 1024);       // K (n = key col), k = token
+    const uint64_t dQmn = umma::desc(sb + S_Q0, 16384, 1024);       // Q (n = key col), k = token
+    const uint64_t dDSup = umma::desc(sb + S_DS - 8192, 8192, 1024);  // m 64..127 = dS^T
+    const uint64_t dAup = umma::desc(sb + S_A - 8192, 8192, 1024);    // m 64..127 = A^T
+    const uint64_t dXmn = umma::desc(sb + S_X, 8192, 1024);           // X (n = col), k = token
+    const uint64_t dKKk = umma::desc(sb + S_DKK - 8192, 16, 1024);    // rows 64..127 = dKK
+    const uint64_t dKKmn = umma::desc(sb + S_DKK - 8192, 8192, 1024); // m 64..127 = dKK^T
+
+    uint32_t phase = 0;
+    auto wait_mma = [&]() -> bool {
+        if (tid == 0 && !umma::mbar_wait(bar, phase)) {
+            raise_error(geo.err, GDR_ERR_TIMEOUT);
+            *sflag = 1;
+        }
+        phase ^= 1;
+        umma::fence_before();
+        __syncthreads();
+        umma::fence_after();
+        return *sflag == 0;
+    };
+    auto sync_tc = [&]() {
+        umma::fence_async_smem();
+        umma::fence_before();
+        __syncthreads();
+        umma::fence_after();
+    };
+
+    float acc[64];  // dq row (lower lanes) or dk row (upper lanes), key columns 64*hh..
+#pragma unroll
+    for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+    bool ok = true;
+
+    for (int jj = 0; jj < grp && ok; ++jj) {
+        const int j = hq * grp + jj;
+        const long long sbase = ((long long)slot * Hv + j) * DK * DV;
+        const long long dbase = ((long long)slot * Hv + j) * C * DV;
+        load_rows128<T>(sb + S_DO0, 16384, dout + (tok0 * Hv + j) * DV, (long long)Hv * DV, 64, valid, tid);
+        load_rows128<T>(sb + S_DD0, 16384, ddl + dbase, DV, 64, valid, tid);
+        load_rows128<T>(sb + S_V0, 16384, v + (tok0 * Hv + j) * DV, (long long)Hv * DV, 64, valid, tid);
+        load_rows128<T>(sb + S_D0, 16384, dl + dbase, DV, 64, valid, tid);
+        load_rows128<T>(sb + S_H, 16384, hs + sbase, DV, 128, 128, tid);
+        load_rows128<T>(sb + S_DH, 16384, dhs + sbase, DV, 128, 128, tid);
+        load_rows64<T>(sb + S_A, A + (tok0 * Hv + j) * C, (long long)Hv * C, valid, tid);
+        if (tid < C) {
+            const bool okr = tid < valid;
+            cp_async4(sb + S_F + (F_G * 64 + tid) * 4, p.g_cs + (okr ? (tok0 + tid) * Hv + j : 0), okr);
+            f(F_B, tid) = okr ? load_gate<T>(p.beta, (tok0 + tid) * Hv + j, p.gate_f32) : 0.f;
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
+        if (jj == 0 && p.l2norm) {
+            l2norm64<T>(sb + S_Q0, valid, warp, lane);
+            l2norm64<T>(sb + S_K0, valid, warp, lane);
+        }
+        const float Gl = f(F_G, valid - 1);
+        if (tid < C) {
+            f(F_EG, tid) = __expf(f(F_G, tid));
+            f(F_EL, tid) = __expf(Gl - f(F_G, tid));
+        }
+        // AKG = A with column s scaled by beta_s e^{G_s}
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int cix = tid + u * NT, rr = cix >> 3, c = cix & 7;
+            const uint32_t o = umma::off(rr, c * 8, 0);
+            const uint4 a = umma::ld_shared_v4(sb + S_A + o);
+            const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+            uint32_t wk[4];
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+                const int s = c * 8 + 2 * e2;
+                const float2 x = Elt<T>::unpack(w[e2]);
+                wk[e2] = Elt<T>::pack(x.x * f(F_B, s) * __expf(f(F_G, s)), x.y * f(F_B, s + 1) * __expf(f(F_G, s + 1)));
+            }
+            umma::st_shared_v4(sb + S_AKG + o, wk[0], wk[1], wk[2], wk[3]);
+        }
+        sync_tc();
+
+        // ---------------- round 1
+        if (tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t ko = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+                umma::mma(tmem + T_R1, dDOa + ko, dH + ko, i_n128, ks > 0);
+                umma::mma(tmem + T_R2, dVa + ko, dDH + ko, i_n128, ks > 0);
+                umma::mma(tmem + T_R3, dDOa + ko, dVa + ko, i_n128, ks > 0);
+                umma::mma(tmem + T_R4, dQa + ko, dKa + ko, i_n64, ks > 0);
+            }
+            umma::commit(bar);
+        }
+        if (!wait_mma()) {
+            ok = false;
+            break;
+        }
+        float qd = 0.f;  // lower lanes: <q_r, dq_r> of this value head (this thread's half)
+        if (!upper) {
+            const float sc = p.scale * f(F_EG, r);
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) {
+                float x[16], qv[16];
+                umma::ld16(umma::taddr(tmem, lb, T_R1 + hh * 64 + c), x);
+                load16<T>(sb + S_Q0 + hh * 16384, r, c, qv);
+                umma::ld_wait();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    x[u] *= sc;
+                    acc[c + u] += x[u];
+                    qd += qv[u] * x[u];
+                }
+            }
+            // dS = scale dP o Gamma o M  (dP = dO Delta^T in columns 64..127 of R3)
+            const float gr = f(F_G, r);
+#pragma unroll
+            for (int c = 0; c < 32; c += 16) {
+                float x[16];
+                umma::ld16(umma::taddr(tmem, lb, T_R3 + 64 + hh * 32 + c), x);
+                umma::ld_wait();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int s = hh * 32 + c + u;
+                    x[u] = (s <= r && r < valid) ? p.scale * x[u] * __expf(gr - f(F_G, s)) : 0.f;
+                }
+                store16<T>(sb + S_DS, r, hh * 32 + c, x);
+            }
+        } else {
+            // dW = -(dDelta h^T) rows; dk += e^{Gl - G_r} Delta dH'^T
+            const uint32_t wblk = hh ? S_DW1 : S_DW0;
+            const float el = f(F_EL, r);
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) {
+                float x[16], y[16];
+                umma::ld16(umma::taddr(tmem, lb, T_R1 + hh * 64 + c), x);
+                umma::ld16(umma::taddr(tmem, lb, T_R2 + hh * 64 + c), y);
+                umma::ld_wait();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    x[u] = -x[u];
+                    acc[c + u] += el * y[u];
+                }
+                store16<T>(sb + wblk, r, c, x);
+            }
+        }
+        sync_tc();
+
+        // ---------------- round 2
+        if (tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + T_R1, dAmn + ks * 128, dDDmn + ks * 128, i_n256_mn, ks > 0);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t ko = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+                umma::mma(tmem + T_R8, dWup + ko, dKa + ko, i_n64, ks > 0);
+            }
+            umma::commit(bar);
+        }
+        if (!wait_mma()) {
+            ok = false;
+            break;
+        }
+        float vd = 0.f, kd = 0.f;
+        if (!upper) {
+            // dDelta-side: ddelta = A^T dDelta (columns 0..127), A^T dW (128..255)
+            const float br = f(F_B, r);
+            T *dvrow = static_cast<T *>(p.dv) + ((tok0 + r) * Hv + j) * DV + hh * 64;
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) {
+                float x[16], y[16], vv[16], kv[16];
+                umma::ld16(umma::taddr(tmem, lb, T_R1 + hh * 64 + c), x);
+                umma::ld16(umma::taddr(tmem, lb, T_R1 + 128 + hh * 64 + c), y);
+                load16<T>(sb + S_V0 + hh * 16384, r, c, vv);
+                load16<T>(sb + S_K0 + hh * 16384, r, c, kv);
+                umma::ld_wait();
+                uint32_t w[8];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    vd += vv[u] * x[u];
+                    kd += kv[u] * y[u];
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) w[u] = Elt<T>::pack(x[2 * u] * br, x[2 * u + 1] * br);
+                if (r < valid) {
+                    *reinterpret_cast<uint4 *>(dvrow + c) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4 *>(dvrow + c + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+                }
+            }
+        } else {
+            // dk += (A diag(beta e^G))^T dW ; dA = beta_s (e^{G_s} dW K^T + dDelta V^T), strictly lower
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) {
+                float x[16];
+                umma::ld16(umma::taddr(tmem, lb, T_R1 + 128 + hh * 64 + c), x);
+                umma::ld_wait();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) acc[c + u] += x[u];
+            }
+#pragma unroll
+            for (int c = 0; c < 32; c += 16) {
+                float x1[16], x2[16];
+                umma::ld16(umma::taddr(tmem, lb, T_R8 + hh * 32 + c), x1);
+                umma::ld16(umma::taddr(tmem, lb, T_R3 + hh * 32 + c), x2);
+                umma::ld_wait();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int s = hh * 32 + c + u;
+                    x1[u] = (s < r && r < valid) ? f(F_B, s) * (f(F_EG, s) * x1[u] + x2[u]) : 0.f;
+                }
+                store16<T>(sb + S_DA, r, hh * 32 + c, x1);
+            }
+        }
+        sync_tc();
+
+        // ---------------- round 3: X = dA A^T ; dq += dS K ; dk += dS^T Q
+        if (tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                umma::mma(tmem + T_R8, dDA + ks * 2, dAk + ks * 2, i_n64, ks > 0);
+                umma::mma(tmem + T_R1, dDS + ks * 2, dKmn + ks * 128, i_n128_bmn, ks > 0);
+                umma::mma(tmem + T_R2, dDSup + ks * 128, dQmn + ks * 128, i_n128_mn, ks > 0);
+            }
+            umma::commit(bar);
+        }
+        if (!wait_mma()) {
+            ok = false;
+            break;
+        }
+        if (!upper) {
+#pragma unroll
+            for (int c = 0; c < 32; c += 16) {
+                float x[16];
+                umma::ld16(umma::taddr(tmem, lb, T_R8 + hh * 32 + c), x);
+                umma::ld_wait();
+                store16<T>(sb + S_X, r, hh * 32 + c, x);
+            }
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) {
+                float x[16], qv[16];
+                umma::ld16(umma::taddr(tmem, lb, T_R1 + hh * 64 + c), x);
+                load16<T>(sb + S_Q0 + hh * 16384, r, c, qv);
+                umma::ld_wait();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    acc[c + u] += x[u];
+                    qd += qv[u] * x[u];
+                }
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) {
+                float x[16];
+                umma::ld16(umma::taddr(tmem, lb, T_R2 + hh * 64 + c), x);
+                umma::ld_wait();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) acc[c + u] += x[u];
+            }
+        }
+        sync_tc();
+
+        // ---------------- round 4: dL = -A^T X
+        if (tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + T_R8, dAup + ks * 128, dXmn + ks * 128, i_n64_mn, ks > 0);
+            umma::commit(bar);
+        }
+        if (!wait_mma()) {
+            ok = false;
+            break;
+        }
+        float lb_ = 0.f;  // upper lanes: sum_s dL Gamma KK
+        if (upper) {
+            const float gr = f(F_G, r), br = f(F_B, r);
+#pragma unroll
+            for (int c = 0; c < 32; c += 16) {
+                float x[16], kk[16];
+                umma::ld16(umma::taddr(tmem, lb, T_R8 + hh * 32 + c), x);
+                umma::ld16(umma::taddr(tmem, lb, T_R4 + hh * 32 + c), kk);
+                umma::ld_wait();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int s = hh * 32 + c + u;
+                    const bool m = s < r && r < valid;
+                    const float gam = m ? __expf(gr - f(F_G, s)) : 0.f;
+                    const float dlv = m ? -x[u] : 0.f;
+                    lb_ += dlv * gam * kk[u];
+                    x[u] = dlv * br * gam;
+                }
+                store16<T>(sb + S_DKK, r, hh * 32 + c, x);
+            }
+        }
+        sync_tc();
+
+        // ---------------- round 5: dk += dKK K + dKK^T K
+        if (tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                umma::mma(tmem + T_R1, dKKk + ks * 2, dKmn + ks * 128, i_n128_bmn, ks > 0);
+                umma::mma(tmem + T_R1, dKKmn + ks * 128, dKmn + ks * 128, i_n128_mn, true);
+            }
+            umma::commit(bar);
+        }
+        if (!wait_mma()) {
+            ok = false;
+            break;
+        }
+        if (upper) {
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) {
+                float x[16];
+                umma::ld16(umma::taddr(tmem, lb, T_R1 + hh * 64 + c), x);
+                umma::ld_wait();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) acc[c + u] += x[u];
+            }
+            f(F_LB0 + hh, r) = lb_;
+        } else {
+            f(F_QD0 + hh, r) = qd;
+            f(F_VD0 + hh, r) = vd;
+            f(F_KD0 + hh, r) = kd;
+        }
+        __syncthreads();
+        if (tid < C && tid < valid) {
+            const int rr = tid;
+            const float br = f(F_B, rr);
+            const float vdot = f(F_VD0, rr) + f(F_VD1, rr);
+            const float db = f(F_EG, rr) * (f(F_KD0, rr) + f(F_KD1, rr)) + vdot + (f(F_LB0, rr) + f(F_LB1, rr));
+            store_gate<T>(p.dbeta, (tok0 + rr) * Hv + j, p.gate_f32, db);
+            p.D[(tok0 + rr) * Hv + j] = (f(F_QD0, rr) + f(F_QD1, rr)) - br * vdot;
+        }
+        __syncthreads();
+    }
+
+    // ---- dq (lower lanes) and dk (upper lanes): stage fp32, L2-norm chain rule, store
+    float *fq = reinterpret_cast<float *>(smem + S_DO0);           // [64][128] fp32 (32 KB)
+    float *fk = reinterpret_cast<float *>(smem + S_DO0 + 32768);   // [64][128] fp32 (32 KB)
+    if (ok) {
+        float *dst = upper ? fk : fq;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) dst[r * DK + hh * 64 + i] = acc[i];
+    }
+    __syncthreads();
+    if (ok) {
+        const long long rstride = (long long)Hq * DK;
+        l2norm_bwd_rows<T>(fq, q + (tok0 * Hq + hq) * DK, rstride, static_cast<T *>(p.dq) + (tok0 * Hq + hq) * DK,
+                           valid, p.l2norm, warp, 8, lane);
+        l2norm_bwd_rows<T>(fk, k + (tok0 * Hq + hq) * DK, rstride, static_cast<T *>(p.dk) + (tok0 * Hq + hq) * DK,
+                           valid, p.l2norm, warp, 8, lane);
+    }
+    umma::fence_before();
+    __syncthreads();
+    if (warp == 0) umma::dealloc(tmem, T_COLS);
+}
+
+// dg_s = sum_{t >= s} D_t + <dh_T, h_T> over each sequence, per value head.
+template <typename T>
+__global__ void __launch_bounds__(256) dg_scan_kernel(Geo geo, const float *__restrict__ D, const float *__restrict__ dht,
+                                                      const float *__restrict__ hT, void *dg, bool gate_f32) {
+    __shared__ float s_red[8];
+    __shared__ float s_carry;
+    const int j = blockIdx.x, n = blockIdx.y, Hv = geo.Hv;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    long long tok0;
+    int len, row0;
+    geo.seq(n, tok0, len, row0);
+    float hd = 0.f;
+    if (dht) {
+        const long long base = ((long long)n * Hv + j) * DK * DV;
+        for (int i = tid; i < DK * DV; i += 256) hd += dht[base + i] * hT[base + i];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, o);
+    if (lane == 0) s_red[warp] = hd;
+    __syncthreads();
+    if (tid == 0) {
+        float t = 0.f;
+        for (int w = 0; w < 8; ++w) t += s_red[w];
+        s_carry = t;
+    }
+    __syncthreads();
+    // reverse inclusive scan in tiles of 256 tokens, from the end of the sequence
+    for (int end = len; end > 0; end -= 256) {
+        const int t = end - 1 - tid;  // thread 0 takes the last token of the tile
+        float x = (t >= 0) ? D[(tok0 + t) * Hv + j] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) s_red[warp] = x;
+        __syncthreads();
+        float pre = s_carry;
+        for (int w = 0; w < warp; ++w) pre += s_red[w];
+        if (t >= 0) store_gate<T>(dg, (tok0 + t) * Hv + j, gate_f32, x + pre);
+        __syncthreads();
+        if (tid == 0) {
+            float tot = 0.f;
+            for (int w = 0; w < 8; ++w) tot += s_red[w];
+            s_carry += tot;
+        }
+        __syncthreads();
+    }
+}
+
+template <typename T>
+cudaError_t bwd_chunk_tc_t(const Args &a, const BcP &p, cudaStream_t s) {
+    if (a.max_chunks == 0) return cudaSuccess;
+    auto kern = bwd_chunk_tc_kernel<T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S_BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)a.max_chunks, a.Hq);
+    kern<<<grid, NT, S_BYTES, s>>>(make_geo(a), p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_chunk_tc(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
+                                const void *beta, const void *A, const void *dout, const void *h, const void *dhn,
+                                const void *delta, const void *ddelta, void *dq, void *dk, void *dv, void *dbeta,
+                                float *D, cudaStream_t s) {
+    BcP p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.A = A;
+    p.beta = beta;
+    p.dout = dout;
+    p.h = h;
+    p.dhn = dhn;
+    p.delta = delta;
+    p.ddelta = ddelta;
+    p.g_cs = g_cs;
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.dbeta = dbeta;
+    p.D = D;
+    p.gate_f32 = a.gate_f32;
+    p.l2norm = a.l2norm;
+    p.scale = a.scale;
+    return a.bf16 ? bwd_chunk_tc_t<__nv_bfloat16>(a, p, s) : bwd_chunk_tc_t<__half>(a, p, s);
+}
+
+cudaError_t launch_dg_scan(const Args &a, const float *D, const float *dht, const float *hT, void *dg, cudaStream_t s) {
+    dim3 grid(a.Hv, a.N);
+    if (a.bf16)
+        dg_scan_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(make_geo(a), D, dht, hT, dg, a.gate_f32);
+    else
+        dg_scan_kernel<__half><<<grid, 256, 0, s>>>(make_geo(a), D, dht, hT, dg, a.gate_f32);
+    return cudaGetLastError();
+}
+
+}  // namespace gdr

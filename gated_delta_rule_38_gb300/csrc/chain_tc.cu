@@ -1,0 +1,770 @@
+// Forward recurrence on the 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// One CTA of 256 threads per (sequence, value head).  The state is held
+// transposed, S = h^T [V x K] in fp32 registers: row e lives in threads e and
+// e + 128 (one half of the key columns each), and row e is also TMEM lane e of
+// every [V x *] accumulator.  Per
+// chunk of 64 tokens (G = chunk-local cumsum of g, Gl = G at the last valid
+// row), with single-thread MMA issue and three MMA rounds:
+//
+//   round 1:  [Q;K] K^T  -> P = (Q K^T) o Gamma o M (lower, decayed)       (M=128,N=64,K=128)
+//             W^T = K^T (A diag(beta e^G))^T                               (M=128,N=64,K=64)
+//             U^T = V^T (A diag(beta))^T                                   (M=128,N=64,K=64)
+//   round 2:  Delta^T = U^T - S W^T                                        (M=128,N=64,K=128)
+//             O1 = S Q^T                                                   (M=128,N=64,K=128)
+//   round 3:  X = (Delta^T diag(e^{Gl-G})) K                               (M=128,N=128,K=64)
+//             O2 = Delta^T P^T                                             (M=128,N=64,K=64)
+//   epilogue: o_r = scale (e^{G_r} O1[:,r] + O2[:,r]);  S <- e^{Gl} S + X
+//
+// This is the chunk form of S_t = e^{g_t} S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+// o_t = scale S_t q_t, with A = (I + strictly-lower(diag(beta) (K K^T o Gamma)))^-1 from wy_fwd.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "umma.cuh"
+
+namespace gdr {
+namespace {
+
+// ---- shared-memory layout (bytes from a 1024-aligned base)
+// stage (x2): [Q b0][K b0][Q b1][K b1] (8 KB each: 64 rows x 128 B), [V b0][V b1], A (64x64), G[64], beta[64]
+constexpr uint32_t ST_QK = 0, ST_V = 32768, ST_A = 49152, ST_G = 57344, ST_B = 57600, ST_BYTES = 58368;
+constexpr uint32_t P_AKG = 2 * ST_BYTES, P_AB = P_AKG + 8192, P_S = P_AB + 8192, P_W = P_S + 32768,
+                   P_P = P_W + 16384, P_D = P_P + 8192, P_DT = P_D + 16384, P_FAC = P_DT + 16384, P_BAR = P_FAC + 512,
+                   P_SLOT = P_BAR + 8, P_FLAG = P_SLOT + 4, SMEM_USED = P_FLAG + 4;
+constexpr int NT = 256;  // threads per CTA: two per TMEM lane
+constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
+
+// ---- TMEM columns
+constexpr uint32_t T_QK = 0, T_W = 64, T_U = 128, T_O1 = 192, T_O2 = 256, T_X = 320, T_COLS = 512;
+
+struct TcP {
+    const void *q, *k, *v, *A, *beta;
+    const float *g_cs, *h0;
+    void *o, *h;
+    void *delta;  // optional [rows,Hv,64,128]: Delta = U - W h of every chunk
+    float *fin;
+    bool gate_f32, l2norm, v_first, h_api;
+    float scale;
+};
+
+// Copy `valid` rows of a [64 x 128] bf16/fp16 row block (row stride in elements)
+// into two swizzled 64-column blocks that are `bstride` bytes apart; rows past
+// `valid` are zero-filled.
+template <typename T>
+__device__ __forceinline__ void load_tile128(uint32_t dst, uint32_t bstride, const T *src, long long stride, int valid,
+                                             int tid) {
+#pragma unroll
+    for (int i = tid; i < 64 * 16; i += NT) {
+        const int r = i >> 4, c = i & 15;
+        const bool ok = r < valid;
+        cp_async16(dst + (uint32_t)(c >> 3) * bstride + umma::off(r, (c & 7) * 8, 0), ok ? src + r * stride + c * 8 : src,
+                   ok);
+    }
+}
+template <typename T>
+__device__ __forceinline__ void load_tile64(uint32_t dst, const T *src, long long stride, int valid, int tid) {
+#pragma unroll
+    for (int i = tid; i < 64 * 8; i += NT) {
+        const int r = i >> 3, c = i & 7;
+        const bool ok = r < valid;
+        cp_async16(dst + umma::off(r, c * 8, 0), ok ? src + r * stride + c * 8 : src, ok);
+    }
+}
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, bool valid) {
+    const int n = valid ? 4 : 0;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(n));
+}
+
+// In-place x / sqrt(sum x^2 + eps) of `rows` rows of a [64 x 128] swizzled tile
+// (two 64-column blocks `bstride` apart).  Lane l of a warp takes a quarter
+// (32 values) of row 8*pass + l/4.
+template <typename T>
+__device__ __forceinline__ void l2norm_tile(uint32_t base, uint32_t bstride, int rows, int warp, int lane) {
+    const int rq = lane >> 2, qq = lane & 3;
+    for (int r0 = warp * 8; r0 < rows; r0 += 8 * (NT / 32)) {
+        const int r = r0 + rq;
+        uint32_t addr[4];
+        uint4 u[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int ch = qq * 4 + c;  // 16-byte chunk 0..15 of the row
+            addr[c] = base + (uint32_t)(ch >> 3) * bstride + umma::off(r, (ch & 7) * 8, 0);
+            u[c] = umma::ld_shared_v4(addr[c]);
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 x = Elt<T>::unpack(w[e]);
+                ss += x.x * x.x + x.y * x.y;
+            }
+        }
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+        const float inv = 1.0f / sqrtf(ss + L2_EPS);
+        if (r < rows) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 x = Elt<T>::unpack(w[e]);
+                    w[e] = Elt<T>::pack(x.x * inv, x.y * inv);
+                }
+                umma::st_shared_v4(addr[c], w[0], w[1], w[2], w[3]);
+            }
+        }
+    }
+}
+
+// Write 16 fp32 values as columns col0..col0+15 (col0 a multiple of 16) of a swizzled row.
+template <typename T>
+__device__ __forceinline__ void store16(uint32_t base, int row, int col0, const float *x) {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        umma::st_shared_v4(base + umma::off(row, col0 + c * 8, 0), Elt<T>::pack(x[c * 8], x[c * 8 + 1]),
+                           Elt<T>::pack(x[c * 8 + 2], x[c * 8 + 3]), Elt<T>::pack(x[c * 8 + 4], x[c * 8 + 5]),
+                           Elt<T>::pack(x[c * 8 + 6], x[c * 8 + 7]));
+    }
+}
+
+template <typename T> struct IsBf16 { static constexpr bool value = false; };
+template <> struct IsBf16<__nv_bfloat16> { static constexpr bool value = true; };
+
+__device__ __forceinline__ void sync_tc() {
+    umma::fence_async_smem();
+    umma::fence_before();
+    __syncthreads();
+    umma::fence_after();
+}
+
+template <typename T, bool WRITE_O>
+__global__ void __launch_bounds__(NT, 1) chain_fwd_tc_kernel(Geo geo, TcP p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    const int j = blockIdx.y, n = blockIdx.z;
+    const int Hv = geo.Hv, Hq = geo.Hq, hq = j / (Hv / Hq);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // thread (e, hh): TMEM lane / state row e, column half hh
+    const int e = tid & 127, hh = tid >> 7, lb = (warp & 3) * 32;
+    constexpr bool bf16 = IsBf16<T>::value;
+    long long tok0;
+    int len, row0;
+    geo.seq(n, tok0, len, row0);
+    const int nc = (len + C - 1) / C;
+    const T *q = static_cast<const T *>(p.q);
+    const T *k = static_cast<const T *>(p.k);
+    const T *v = static_cast<const T *>(p.v);
+    const T *A = static_cast<const T *>(p.A);
+    const long long st_base = ((long long)n * Hv + j) * DK * DV;
+    const uint32_t bar = sb + P_BAR;
+    volatile int *sflag = reinterpret_cast<volatile int *>(smem + P_FLAG);
+    float *fEG = reinterpret_cast<float *>(smem + P_FAC);  // e^{G_s}
+    float *fEL = fEG + C;                                   // e^{Gl - G_s}
+
+    if (tid == 0) {
+        umma::mbar_init(bar, 1);
+        umma::fence_mbar_init();
+        *sflag = 0;
+    }
+    if (warp == 0) umma::alloc(sb + P_SLOT, T_COLS);
+    umma::fence_before();
+    __syncthreads();
+    umma::fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + P_SLOT);
+
+    // fp32 state: S[e][64*hh + i] = h[64*hh + i][e]
+    float S[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+        const int d = hh * 64 + i;
+        S[i] = p.h0 ? p.h0[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] : 0.f;
+    }
+    auto write_S_tile = [&]() {
+#pragma unroll
+        for (int c = 0; c < 64; c += 16) store16<T>(sb + P_S + hh * 16384, e, c, S + c);
+    };
+    write_S_tile();
+
+    float breg = 0.f;
+    auto prefetch = [&](int i) {
+        const uint32_t st = sb + (i & 1) * ST_BYTES;
+        const long long tb = tok0 + (long long)i * C;
+        const int valid = min(C, len - i * C);
+        if (WRITE_O) load_tile128<T>(st + ST_QK, 16384, q + (tb * Hq + hq) * DK, (long long)Hq * DK, valid, tid);
+        load_tile128<T>(st + ST_QK + 8192, 16384, k + (tb * Hq + hq) * DK, (long long)Hq * DK, valid, tid);
+        load_tile128<T>(st + ST_V, 8192, v + (tb * Hv + j) * DV, (long long)Hv * DV, valid, tid);
+        load_tile64<T>(st + ST_A, A + (tb * Hv + j) * C, (long long)Hv * C, valid, tid);
+        if (tid < C) {
+            const bool ok = tid < valid;
+            cp_async4(st + ST_G + tid * 4, p.g_cs + (ok ? (tb + tid) * Hv + j : 0), ok);
+            breg = ok ? load_gate<T>(p.beta, (tb + tid) * Hv + j, p.gate_f32) : 0.f;
+        }
+        cp_async_commit();
+    };
+    if (nc > 0) prefetch(0);
+
+    uint32_t phase = 0;
+    const uint32_t id_n64 = umma::idesc(128, 64, bf16, false, false);
+    const uint32_t id_n64_amn = umma::idesc(128, 64, bf16, true, false);
+    const uint32_t id_n64_bmn = umma::idesc(128, 64, bf16, false, true);
+    const uint32_t id_n128_bmn = umma::idesc(128, 128, bf16, false, true);
+    // descriptors of the persistent operand tiles
+    const uint64_t dAKG = umma::desc(sb + P_AKG, 16, 1024), dAB = umma::desc(sb + P_AB, 16, 1024);
+    const uint64_t dS = umma::desc(sb + P_S, 16, 1024), dW = umma::desc(sb + P_W, 8192, 1024);
+    const uint64_t dD = umma::desc(sb + P_D, 16, 1024), dDT = umma::desc(sb + P_DT, 16, 1024);
+    const uint64_t dP = umma::desc(sb + P_P, 16, 1024);
+    // one thread waits for the MMAs; the block then meets at a barrier
+    auto wait_mma = [&]() -> bool {
+        if (tid == 0 && !umma::mbar_wait(bar, phase)) {
+            raise_error(geo.err, GDR_ERR_TIMEOUT);
+            *sflag = 1;
+        }
+        phase ^= 1;
+        umma::fence_before();
+        __syncthreads();
+        umma::fence_after();
+        return *sflag == 0;
+    };
+
+    for (int i = 0; i < nc; ++i) {
+        const uint32_t st = sb + (i & 1) * ST_BYTES;
+        const float *sG = reinterpret_cast<const float *>(smem + (i & 1) * ST_BYTES + ST_G);
+        float *sB = reinterpret_cast<float *>(smem + (i & 1) * ST_BYTES + ST_B);
+        cp_async_wait<0>();
+        if (tid < C) sB[tid] = breg;
+        __syncthreads();
+        const int valid = min(C, len - i * C);
+        const float Gl = sG[valid - 1];
+        if (p.l2norm) {
+            if (WRITE_O) l2norm_tile<T>(st + ST_QK, 16384, valid, warp, lane);
+            l2norm_tile<T>(st + ST_QK + 8192, 16384, valid, warp, lane);
+        }
+        if (tid < C) {
+            fEG[tid] = __expf(sG[tid]);
+            fEL[tid] = __expf(Gl - sG[tid]);
+        }
+        // scaled copies of A: columns s times beta_s e^{G_s} (for W) and beta_s (for U)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int ci = tid + u * NT, r = ci >> 3, c = ci & 7;
+            const uint32_t o = umma::off(r, c * 8, 0);
+            const uint4 a = umma::ld_shared_v4(st + ST_A + o);
+            const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+            uint32_t wk[4], wb[4];
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2) {
+                const int s = c * 8 + 2 * q2;
+                const float2 x = Elt<T>::unpack(w[q2]);
+                const float b0 = sB[s], b1 = sB[s + 1];
+                wb[q2] = Elt<T>::pack(x.x * b0, x.y * b1);
+                wk[q2] = Elt<T>::pack(x.x * b0 * __expf(sG[s]), x.y * b1 * __expf(sG[s + 1]));
+            }
+            umma::st_shared_v4(sb + P_AKG + o, wk[0], wk[1], wk[2], wk[3]);
+            umma::st_shared_v4(sb + P_AB + o, wb[0], wb[1], wb[2], wb[3]);
+        }
+        // the state before this chunk (optional output)
+        if (p.h) {
+            T *h = static_cast<T *>(p.h);
+            const long long hb = ((long long)(row0 + i) * Hv + j) * DK * DV;
+            if (p.h_api && p.v_first) {
+                T *hr = h + hb + (long long)e * DK + hh * 64;
+#pragma unroll
+                for (int d = 0; d < 64; d += 8) {
+                    uint4 w;
+                    w.x = Elt<T>::pack(S[d], S[d + 1]);
+                    w.y = Elt<T>::pack(S[d + 2], S[d + 3]);
+                    w.z = Elt<T>::pack(S[d + 4], S[d + 5]);
+                    w.w = Elt<T>::pack(S[d + 6], S[d + 7]);
+                    *reinterpret_cast<uint4 *>(hr + d) = w;
+                }
+            } else {
+                T *hc = h + hb + (long long)(hh * 64) * DV + e;
+#pragma unroll
+                for (int d = 0; d < 64; ++d) hc[d * DV] = Elt<T>::from_f(S[d]);
+            }
+        }
+        sync_tc();
+        if (i + 1 < nc) prefetch(i + 1);
+
+        // ---- round 1
+        // (descriptors of successive K-steps differ only in the start-address field: add offset >> 4)
+        const uint64_t dQa = umma::desc(st + ST_QK, 16, 1024), dKa = umma::desc(st + ST_QK + 8192, 16, 1024);
+        const uint64_t dKmn = umma::desc(st + ST_QK + 8192, 16384, 1024), dVmn = umma::desc(st + ST_V, 8192, 1024);
+        if (tid == 0) {
+            if (WRITE_O) {
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t ko = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+                    umma::mma(tmem + T_QK, dQa + ko, dKa + ko, id_n64, ks > 0);
+                }
+            }
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                umma::mma(tmem + T_W, dKmn + ks * 128, dAKG + ks * 2, id_n64_amn, ks > 0);
+                umma::mma(tmem + T_U, dVmn + ks * 128, dAB + ks * 2, id_n64_amn, ks > 0);
+            }
+            umma::commit(bar);
+        }
+        if (!wait_mma()) break;
+#pragma unroll
+        for (int c = 0; c < 32; c += 16) {
+            // -W row d = e, token columns 32*hh + c .. : MN-major operand rows (key index d)
+            float x[16];
+            umma::ld16(umma::taddr(tmem, lb, T_W + hh * 32 + c), x);
+            umma::ld_wait();
+#pragma unroll
+            for (int u = 0; u < 16; ++u) x[u] = -x[u];
+            store16<T>(sb + P_W, e, hh * 32 + c, x);
+        }
+        if (WRITE_O && e < C) {
+            const int r = e;
+            const float gr = sG[r];
+#pragma unroll
+            for (int c = 0; c < 32; c += 16) {
+                float x[16];
+                umma::ld16(umma::taddr(tmem, lb, T_QK + hh * 32 + c), x);
+                umma::ld_wait();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int s = hh * 32 + c + u;
+                    x[u] = (s <= r && r < valid) ? x[u] * __expf(gr - sG[s]) : 0.f;
+                }
+                store16<T>(sb + P_P, r, hh * 32 + c, x);
+            }
+        }
+        sync_tc();
+
+        // ---- round 2: Delta^T = U^T + S (-W)^T ;  O1 = S Q^T
+        if (tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t so = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+                umma::mma(tmem + T_U, dS + so, dW + ks * 128, id_n64_bmn, true);
+                if (WRITE_O) umma::mma(tmem + T_O1, dS + so, dQa + so, id_n64, ks > 0);
+            }
+            umma::commit(bar);
+        }
+        if (!wait_mma()) break;
+#pragma unroll
+        for (int c = 0; c < 32; c += 16) {
+            float x[16], y[16];
+            umma::ld16(umma::taddr(tmem, lb, T_U + hh * 32 + c), x);
+            umma::ld_wait();
+#pragma unroll
+            for (int u = 0; u < 16; ++u) y[u] = x[u] * fEL[hh * 32 + c + u];
+            store16<T>(sb + P_D, e, hh * 32 + c, x);
+            store16<T>(sb + P_DT, e, hh * 32 + c, y);
+            if (p.delta) {
+                T *dr = static_cast<T *>(p.delta) + ((long long)(row0 + i) * Hv + j) * C * DV +
+                        (long long)(hh * 32 + c) * DV + e;
+#pragma unroll
+                for (int u = 0; u < 16; ++u) dr[u * DV] = Elt<T>::from_f(x[u]);
+            }
+        }
+        sync_tc();
+
+        // ---- round 3: X = Delta~^T K ;  O2 = Delta^T P^T
+        if (tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                umma::mma(tmem + T_X, dDT + ks * 2, dKmn + ks * 128, id_n128_bmn, ks > 0);
+                if (WRITE_O) umma::mma(tmem + T_O2, dD + ks * 2, dP + ks * 2, id_n64, ks > 0);
+            }
+            umma::commit(bar);
+        }
+        if (!wait_mma()) break;
+        {
+            const float eg = __expf(Gl);
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) {
+                float x[16];
+                umma::ld16(umma::taddr(tmem, lb, T_X + hh * 64 + c), x);
+                umma::ld_wait();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) S[c + u] = eg * S[c + u] + x[u];
+            }
+            if (WRITE_O) {
+                T *o = static_cast<T *>(p.o) + ((tok0 + (long long)i * C + hh * 32) * Hv + j) * DV + e;
+                const long long ostride = (long long)Hv * DV;
+#pragma unroll
+                for (int c = 0; c < 32; c += 16) {
+                    float x1[16], x2[16];
+                    umma::ld16(umma::taddr(tmem, lb, T_O1 + hh * 32 + c), x1);
+                    umma::ld16(umma::taddr(tmem, lb, T_O2 + hh * 32 + c), x2);
+                    umma::ld_wait();
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const int r = hh * 32 + c + u;
+                        if (r < valid) o[(c + u) * ostride] = Elt<T>::from_f(p.scale * (fEG[r] * x1[u] + x2[u]));
+                    }
+                }
+            }
+            write_S_tile();
+        }
+        sync_tc();
+    }
+
+    if (p.fin && *sflag == 0) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+            const int d = hh * 64 + i;
+            p.fin[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] = S[i];
+        }
+    }
+    umma::fence_before();
+    __syncthreads();
+    if (warp == 0) umma::dealloc(tmem, T_COLS);
+}
+
+// ============================================================================ reverse chain
+//
+// One CTA of 256 threads per (sequence, value head); chunks in reverse order;
+// dS = dH^T [V x K] (gradient w.r.t. the transposed state) in fp32 registers,
+// thread (e, hh) holding row e, key half hh.  With dS' the gradient arriving at
+// the end of the chunk, K~ = diag(e^{Gl-G}) K and P = (Q K^T) o Gamma o M:
+//
+//   round 1:  [K;Q] Q^T -> P^T rows (scaled, upper part)                  (M=128,N=64,K=128)
+//             W^T = K^T (A diag(beta e^G))^T                              (M=128,N=64,K=64)
+//             E1 = dS' K^T                                                (M=128,N=64,K=128)
+//   round 2:  E2 = dO^T P                                                 (M=128,N=64,K=64)
+//             dDelta^T = E1 diag(e^{Gl-G}) + E2
+//   round 3:  X = (scale dO diag(e^G))^T Q - dDelta^T W                   (M=128,N=128,K=64 x2)
+//   epilogue: dS <- e^{Gl} dS' + X
+// It stores dS' of every chunk (the gradient w.r.t. the state after the chunk)
+// for the per-chunk gradient kernel; the last dS is dh0.
+
+struct TcBwdP {
+    const void *q, *k, *A, *beta, *dout;
+    const float *g_cs, *dht;
+    void *dhn;
+    void *ddelta;  // [rows,Hv,64,128]: dDelta of every chunk
+    float *dh0;
+    bool gate_f32, l2norm, v_first;
+    float scale;
+};
+
+// persistent tiles of the reverse chain (same stage layout as the forward, with
+// [K b][Q b] order in the 32 KB block and dO in place of V)
+constexpr uint32_t B_AKG = 2 * ST_BYTES, B_DS = B_AKG + 8192, B_WT = B_DS + 32768, B_PT = B_WT + 16384,
+                   B_DOG = B_PT + 8192, B_DDT = B_DOG + 16384, B_FAC = B_DDT + 16384, B_BAR = B_FAC + 512,
+                   B_SLOT = B_BAR + 8, B_FLAG = B_SLOT + 4, B_USED = B_FLAG + 4;
+constexpr uint32_t B_SMEM_BYTES = B_USED + 1024;
+constexpr uint32_t TB_KQ = 0, TB_W = 64, TB_E1 = 128, TB_E2 = 192, TB_X = 256, TB_COLS = 512;
+
+template <typename T>
+__global__ void __launch_bounds__(NT, 1) chain_bwd_tc_kernel(Geo geo, TcBwdP p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    const int j = blockIdx.y, n = blockIdx.z;
+    const int Hv = geo.Hv, Hq = geo.Hq, hq = j / (Hv / Hq);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int e = tid & 127, hh = tid >> 7, lb = (warp & 3) * 32;
+    constexpr bool bf16 = IsBf16<T>::value;
+    long long tok0;
+    int len, row0;
+    geo.seq(n, tok0, len, row0);
+    const int nc = (len + C - 1) / C;
+    const T *q = static_cast<const T *>(p.q);
+    const T *k = static_cast<const T *>(p.k);
+    const T *A = static_cast<const T *>(p.A);
+    const T *dout = static_cast<const T *>(p.dout);
+    const long long st_base = ((long long)n * Hv + j) * DK * DV;
+    const uint32_t bar = sb + B_BAR;
+    volatile int *sflag = reinterpret_cast<volatile int *>(smem + B_FLAG);
+    float *fEG = reinterpret_cast<float *>(smem + B_FAC);
+    float *fEL = fEG + C;
+
+    if (tid == 0) {
+        umma::mbar_init(bar, 1);
+        umma::fence_mbar_init();
+        *sflag = 0;
+    }
+    if (warp == 0) umma::alloc(sb + B_SLOT, TB_COLS);
+    umma::fence_before();
+    __syncthreads();
+    umma::fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + B_SLOT);
+
+    float S[64];  // dS[e][64*hh + i] = dH[64*hh + i][e]
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+        const int d = hh * 64 + i;
+        S[i] = p.dht ? p.dht[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] : 0.f;
+    }
+    auto write_S_tile = [&]() {
+#pragma unroll
+        for (int c = 0; c < 64; c += 16) store16<T>(sb + B_DS + hh * 16384, e, c, S + c);
+    };
+    write_S_tile();
+
+    float breg = 0.f;
+    auto prefetch = [&](int i) {
+        const uint32_t st = sb + (i & 1) * ST_BYTES;
+        const long long tb = tok0 + (long long)i * C;
+        const int valid = min(C, len - i * C);
+        load_tile128<T>(st + ST_QK, 16384, k + (tb * Hq + hq) * DK, (long long)Hq * DK, valid, tid);
+        load_tile128<T>(st + ST_QK + 8192, 16384, q + (tb * Hq + hq) * DK, (long long)Hq * DK, valid, tid);
+        load_tile128<T>(st + ST_V, 8192, dout + (tb * Hv + j) * DV, (long long)Hv * DV, valid, tid);
+        load_tile64<T>(st + ST_A, A + (tb * Hv + j) * C, (long long)Hv * C, valid, tid);
+        if (tid < C) {
+            const bool ok = tid < valid;
+            cp_async4(st + ST_G + tid * 4, p.g_cs + (ok ? (tb + tid) * Hv + j : 0), ok);
+            breg = ok ? load_gate<T>(p.beta, (tb + tid) * Hv + j, p.gate_f32) : 0.f;
+        }
+        cp_async_commit();
+    };
+    if (nc > 0) prefetch(nc - 1);
+
+    uint32_t phase = 0;
+    const uint32_t id_n64 = umma::idesc(128, 64, bf16, false, false);
+    const uint32_t id_n64_amn = umma::idesc(128, 64, bf16, true, false);
+    const uint32_t id_n128_ab_mn = umma::idesc(128, 128, bf16, true, true);
+    const uint32_t id_n128 = umma::idesc(128, 128, bf16, false, false);
+    const uint64_t dAKG = umma::desc(sb + B_AKG, 16, 1024), dDS = umma::desc(sb + B_DS, 16, 1024);
+    const uint64_t dWT = umma::desc(sb + B_WT, 16, 1024), dPT = umma::desc(sb + B_PT, 16, 1024);
+    const uint64_t dOG = umma::desc(sb + B_DOG, 8192, 1024), dDDT = umma::desc(sb + B_DDT, 16, 1024);
+    auto wait_mma = [&]() -> bool {
+        if (tid == 0 && !umma::mbar_wait(bar, phase)) {
+            raise_error(geo.err, GDR_ERR_TIMEOUT);
+            *sflag = 1;
+        }
+        phase ^= 1;
+        umma::fence_before();
+        __syncthreads();
+        umma::fence_after();
+        return *sflag == 0;
+    };
+
+    for (int i = nc - 1; i >= 0; --i) {
+        const uint32_t st = sb + (i & 1) * ST_BYTES;
+        const float *sG = reinterpret_cast<const float *>(smem + (i & 1) * ST_BYTES + ST_G);
+        float *sB = reinterpret_cast<float *>(smem + (i & 1) * ST_BYTES + ST_B);
+        cp_async_wait<0>();
+        if (tid < C) sB[tid] = breg;
+        // gradient w.r.t. the state after this chunk, for the per-chunk kernel ([K][V] layout)
+        {
+            T *hc = static_cast<T *>(p.dhn) + ((long long)(row0 + i) * Hv + j) * DK * DV + (long long)(hh * 64) * DV + e;
+#pragma unroll
+            for (int d = 0; d < 64; ++d) hc[d * DV] = Elt<T>::from_f(S[d]);
+        }
+        __syncthreads();
+        const int valid = min(C, len - i * C);
+        const float Gl = sG[valid - 1];
+        if (p.l2norm) {
+            l2norm_tile<T>(st + ST_QK, 16384, valid, warp, lane);
+            l2norm_tile<T>(st + ST_QK + 8192, 16384, valid, warp, lane);
+        }
+        if (tid < C) {
+            fEG[tid] = __expf(sG[tid]);
+            fEL[tid] = __expf(Gl - sG[tid]);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int ci = tid + u * NT, r = ci >> 3, c = ci & 7;
+            const uint32_t o = umma::off(r, c * 8, 0);
+            const uint4 a = umma::ld_shared_v4(st + ST_A + o);
+            const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+            uint32_t wk[4];
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2) {
+                const int s = c * 8 + 2 * q2;
+                const float2 x = Elt<T>::unpack(w[q2]);
+                wk[q2] = Elt<T>::pack(x.x * sB[s] * __expf(sG[s]), x.y * sB[s + 1] * __expf(sG[s + 1]));
+            }
+            umma::st_shared_v4(sb + B_AKG + o, wk[0], wk[1], wk[2], wk[3]);
+        }
+        // scale e^{G_s} dO rows -> dOg (same two-block layout)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int ci = tid + u * NT, r = ci >> 4, c = ci & 15;
+            const uint32_t o = (uint32_t)(c >> 3) * 8192 + umma::off(r, (c & 7) * 8, 0);
+            const uint4 a = umma::ld_shared_v4(st + ST_V + o);
+            const float f = p.scale * __expf(sG[r]);
+            const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+            uint32_t wo[4];
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2) {
+                const float2 x = Elt<T>::unpack(w[q2]);
+                wo[q2] = Elt<T>::pack(x.x * f, x.y * f);
+            }
+            umma::st_shared_v4(sb + B_DOG + o, wo[0], wo[1], wo[2], wo[3]);
+        }
+        sync_tc();
+        if (i > 0) prefetch(i - 1);
+
+        // ---- round 1: [K;Q] Q^T, W^T, E1 = dS' K^T
+        const uint64_t dKa = umma::desc(st + ST_QK, 16, 1024), dQa = umma::desc(st + ST_QK + 8192, 16, 1024);
+        const uint64_t dKmn = umma::desc(st + ST_QK, 16384, 1024), dQmn = umma::desc(st + ST_QK + 8192, 16384, 1024);
+        const uint64_t dOmn = umma::desc(st + ST_V, 8192, 1024);
+        if (tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t ko = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
+                umma::mma(tmem + TB_KQ, dKa + ko, dQa + ko, id_n64, ks > 0);
+                umma::mma(tmem + TB_E1, dDS + ko, dKa + ko, id_n64, ks > 0);
+            }
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + TB_W, dKmn + ks * 128, dAKG + ks * 2, id_n64_amn, ks > 0);
+            umma::commit(bar);
+        }
+        if (!wait_mma()) break;
+#pragma unroll
+        for (int c = 0; c < 32; c += 16) {
+            float x[16];
+            umma::ld16(umma::taddr(tmem, lb, TB_W + hh * 32 + c), x);
+            umma::ld_wait();
+            store16<T>(sb + B_WT, e, hh * 32 + c, x);
+        }
+        if (e < C) {
+            const int r = e;
+            const float gr = sG[r];
+#pragma unroll
+            for (int c = 0; c < 32; c += 16) {
+                float x[16];
+                umma::ld16(umma::taddr(tmem, lb, TB_KQ + hh * 32 + c), x);
+                umma::ld_wait();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int s2 = hh * 32 + c + u;
+                    x[u] = (s2 >= r && s2 < valid) ? x[u] * p.scale * __expf(sG[s2] - gr) : 0.f;
+                }
+                store16<T>(sb + B_PT, r, hh * 32 + c, x);
+            }
+        }
+        sync_tc();
+
+        // ---- round 2: E2 = dO^T P
+        if (tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + TB_E2, dOmn + ks * 128, dPT + ks * 2, id_n64_amn, ks > 0);
+            umma::commit(bar);
+        }
+        if (!wait_mma()) break;
+#pragma unroll
+        for (int c = 0; c < 32; c += 16) {
+            float x1[16], x2[16];
+            umma::ld16(umma::taddr(tmem, lb, TB_E1 + hh * 32 + c), x1);
+            umma::ld16(umma::taddr(tmem, lb, TB_E2 + hh * 32 + c), x2);
+            umma::ld_wait();
+#pragma unroll
+            for (int u = 0; u < 16; ++u) x1[u] = -(x1[u] * fEL[hh * 32 + c + u] + x2[u]);
+            store16<T>(sb + B_DDT, e, hh * 32 + c, x1);
+            T *dr = static_cast<T *>(p.ddelta) + ((long long)(row0 + i) * Hv + j) * C * DV + (long long)(hh * 32 + c) * DV + e;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) dr[u * DV] = Elt<T>::from_f(-x1[u]);
+        }
+        sync_tc();
+
+        // ---- round 3: X = dOg^T Q - dDelta^T W
+        if (tid == 0) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + TB_X, dOG + ks * 128, dQmn + ks * 128, id_n128_ab_mn, ks > 0);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + TB_X, dDDT + ks * 2, dWT + ks * 2, id_n128, true);
+            umma::commit(bar);
+        }
+        if (!wait_mma()) break;
+        {
+            const float eg = __expf(Gl);
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) {
+                float x[16];
+                umma::ld16(umma::taddr(tmem, lb, TB_X + hh * 64 + c), x);
+                umma::ld_wait();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) S[c + u] = eg * S[c + u] + x[u];
+            }
+            write_S_tile();
+        }
+        sync_tc();
+    }
+
+    if (p.dh0 && *sflag == 0) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+            const int d = hh * 64 + i;
+            p.dh0[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] = S[i];
+        }
+    }
+    umma::fence_before();
+    __syncthreads();
+    if (warp == 0) umma::dealloc(tmem, TB_COLS);
+}
+
+template <typename T>
+cudaError_t chain_bwd_tc_t(const Args &a, const TcBwdP &p, cudaStream_t s) {
+    auto kern = chain_bwd_tc_kernel<T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, B_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 grid(1, a.Hv, a.N);
+    kern<<<grid, NT, B_SMEM_BYTES, s>>>(make_geo(a), p);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t chain_fwd_tc_t(const Args &a, const TcP &p, bool write_o, cudaStream_t s) {
+    auto kern = write_o ? chain_fwd_tc_kernel<T, true> : chain_fwd_tc_kernel<T, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    dim3 grid(1, a.Hv, a.N);
+    Geo g = make_geo(a);
+    kern<<<grid, NT, SMEM_BYTES, s>>>(g, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
+                             const void *A, const void *dout, const float *dht, void *dhn, void *ddelta, float *dh0,
+                             cudaStream_t s) {
+    TcBwdP p;
+    p.ddelta = ddelta;
+    p.q = q;
+    p.k = k;
+    p.A = A;
+    p.beta = beta;
+    p.dout = dout;
+    p.g_cs = g_cs;
+    p.dht = dht;
+    p.dhn = dhn;
+    p.dh0 = dh0;
+    p.gate_f32 = a.gate_f32;
+    p.l2norm = a.l2norm;
+    p.v_first = a.v_first;
+    p.scale = a.scale;
+    return a.bf16 ? chain_bwd_tc_t<__nv_bfloat16>(a, p, s) : chain_bwd_tc_t<__half>(a, p, s);
+}
+
+cudaError_t launch_chain_fwd(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
+                             const void *beta, const void *A, const float *h0, void *o, float *final_state, void *h,
+                             bool h_api_layout, void *delta, cudaStream_t s) {
+    TcP p;
+    p.delta = delta;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.A = A;
+    p.beta = beta;
+    p.g_cs = g_cs;
+    p.h0 = h0;
+    p.o = o;
+    p.h = h;
+    p.fin = final_state;
+    p.gate_f32 = a.gate_f32;
+    p.l2norm = a.l2norm;
+    p.v_first = a.v_first;
+    p.h_api = h_api_layout;
+    p.scale = a.scale;
+    return a.bf16 ? chain_fwd_tc_t<__nv_bfloat16>(a, p, o != nullptr, s)
+                  : chain_fwd_tc_t<__half>(a, p, o != nullptr, s);
+}
+
+}  // namespace gdr

@@ -324,6 +324,7 @@ struct Geo {
     const int32_t *cidx;      // varlen chunk table [*,2]
     const int32_t *coff;      // varlen chunk offsets [N+1]
     const int32_t *ctotal;    // varlen total chunks
+    unsigned *err;            // device error word
     __device__ __forceinline__ int nt_dense() const { return (T + C - 1) / C; }
     // Sequence n: first token, length, first chunk row.
     __device__ __forceinline__ void seq(int n, long long &tok0, int &len, int &row0) const {
@@ -368,6 +369,7 @@ inline Geo make_geo(const Args &a) {
     g.cidx = a.cidx;
     g.coff = a.coff;
     g.ctotal = a.ctotal;
+    g.err = a.err;
     return g;
 }
 

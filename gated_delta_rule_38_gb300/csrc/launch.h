@@ -30,16 +30,21 @@ cudaError_t launch_prep_chunks(const int32_t *cu, int N, int T, int chunk, int32
 // Forward: per-chunk gate cumsum and WY matrix.
 cudaError_t launch_wy_fwd(const Args &a, const void *k, const void *g, const void *beta, float *g_cs,
                           void *A, cudaStream_t s);
-// Forward recurrence + output (o != nullptr) and/or per-chunk states (h != nullptr).
+// Forward recurrence + output (o != nullptr) and/or per-chunk states (h != nullptr)
+// and per-chunk Delta = U - W h (delta != nullptr).
 cudaError_t launch_chain_fwd(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
-                             const void *beta, const void *A, const float *h0, void *o, float *final_state,
-                             void *h, bool h_api_layout, cudaStream_t s);
-// Backward.
+                             const void *beta, const void *A, const float *h0, void *o, float *final_state, void *h,
+                             bool h_api_layout, void *delta, cudaStream_t s);
+// Backward: reverse state-gradient chain (dH' and dDelta of every chunk, dh0).
 cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
-                             const void *A, const void *dout, const float *dht, void *dhn, float *dh0,
+                             const void *A, const void *dout, const float *dht, void *dhn, void *ddelta, float *dh0,
                              cudaStream_t s);
-cudaError_t launch_bwd_chunk(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
-                             const void *beta, const void *A, const void *dout, const void *h, const void *dhn,
-                             void *dq, void *dk, void *dv, void *dg, void *dbeta, cudaStream_t s);
+// Backward: per-chunk gradients (dq, dk, dv, dbeta and the gate-gradient terms D).
+cudaError_t launch_bwd_chunk_tc(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
+                                const void *beta, const void *A, const void *dout, const void *h, const void *dhn,
+                                const void *delta, const void *ddelta, void *dq, void *dk, void *dv, void *dbeta,
+                                float *D, cudaStream_t s);
+// Backward: dg = reverse cumsum of D over every sequence + <dht, final state>.
+cudaError_t launch_dg_scan(const Args &a, const float *D, const float *dht, const float *hT, void *dg, cudaStream_t s);
 
 }  // namespace gdr

@@ -357,3 +357,21 @@ def test_h_rows_are_prefix_final_states():
         pp = Problem(B=1, T=T1, Hq=1, Hv=1, K=8, V=8, chunk=16)
         rp = oracle.fwd(pp, **{kk: (vv[:, :T1] if kk != "h0" else vv) for kk, vv in x.items()})
         np.testing.assert_allclose(r["h"][c], rp["final_state"][0], rtol=1e-13, atol=1e-14)
+
+
+def test_gate_gradient_identity():
+    """With h_t = e^{G_t} h~_t the gate enters only through e^{G_t} q_t, e^{-G_t} v_t and the final
+    state, so dg_s = sum_{t>=s} (<q_t, dq_t> - <v_t, dv_t>) + <dh_T, h_T> per sequence and head."""
+    rng = np.random.default_rng(13)
+    cu = [0, 29, 29, 90]
+    pb = Problem(B=1, T=90, Hq=2, Hv=2, K=8, V=6, scale=0.7, chunk=16, cu_seqlens=cu)
+    x = small_inputs(rng, pb)
+    dO = rnd(rng, 1, 90, 2, 6)
+    dht = rnd(rng, 3, 2, 8, 6)
+    f = oracle.fwd(pb, **x)
+    r = oracle.bwd(pb, **x, do=dO, dht=dht)
+    D = (x["q"] * r["dq"]).sum(-1) - (x["v"] * r["dv"]).sum(-1)
+    for n in range(3):
+        s = slice(cu[n], cu[n + 1])
+        ident = np.flip(np.cumsum(np.flip(D[0, s], 0), 0), 0) + (dht[n] * f["final_state"][n]).sum((-1, -2))
+        np.testing.assert_allclose(ident, r["dg"][0, s], rtol=1e-10, atol=1e-12)
