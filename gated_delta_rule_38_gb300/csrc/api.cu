@@ -4,6 +4,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -147,8 +148,28 @@ int64_t max_chunks_of(const gdr_problem *p) {
     return (int64_t)p->B * ((p->T + C - 1) / C);
 }
 
+// Segments per sequence for the intra-GPU sequence split.  Automatic choice: only when the
+// (sequence, value head) streams cannot fill the GPU's SMs; enough segments to occupy them, each
+// at least 4 chunks long.  Host-only (the workspace size must not depend on the device).
+constexpr int64_t kSplitSMs = 152;
+int choose_nseg(const gdr_problem *p) {
+    const int64_t streams = (int64_t)num_seqs(p) * p->Hv;
+    const int64_t maxc = std::max<int64_t>(1, ((int64_t)p->T + C - 1) / C);
+    int64_t s;
+    if (p->num_segments > 0)
+        s = std::min<int64_t>(p->num_segments, maxc);
+    else if (streams * 2 > kSplitSMs)
+        s = 1;
+    else
+        s = std::min<int64_t>(kSplitSMs / streams, maxc / 4);
+    return (int)std::max<int64_t>(1, std::min<int64_t>(s, 64));
+}
+
 struct Layout {
-    size_t idx = 0, off = 0, total = 0, gcs = 0, A = 0, h = 0, dhn = 0, delta = 0, ddelta = 0, D = 0, hT = 0, bytes = 0;
+    size_t idx = 0, off = 0, total = 0, gcs = 0, A = 0, h = 0, dhn = 0, delta = 0, ddelta = 0;
+    size_t seg[3] = {0, 0, 0};
+    int nseg = 1;
+    size_t bytes = 0;
 };
 
 // Workspace: [varlen chunk tables][fwd: g_cumsum, A scratch | bwd: states, state gradients].
@@ -181,13 +202,26 @@ Layout layout_of(const gdr_problem *p, bool bwd) {
         at = round_up(at + dsz, 256);
         L.ddelta = at;
         at = round_up(at + dsz, 256);
-        L.D = at;
-        at = round_up(at + tok * p->Hv * sizeof(float), 256);
-        L.hT = at;
-        at = round_up(at + (size_t)num_seqs(p) * p->Hv * DK * DV * sizeof(float), 256);
+    }
+    L.nseg = choose_nseg(p);
+    if (L.nseg > 1) {
+        const size_t sz = (size_t)num_seqs(p) * p->Hv * L.nseg * DK * DV * sizeof(float);
+        for (int i = 0; i < 3; ++i) {
+            L.seg[i] = at;
+            at = round_up(at + sz, 256);
+        }
     }
     L.bytes = at;
     return L;
+}
+
+SegWs seg_ws(const Layout &L, char *ws) {
+    SegWs sw;
+    sw.nseg = L.nseg;
+    sw.start = L.nseg > 1 ? reinterpret_cast<float *>(ws + L.seg[0]) : nullptr;
+    sw.end0 = L.nseg > 1 ? reinterpret_cast<float *>(ws + L.seg[1]) : nullptr;
+    sw.end1 = L.nseg > 1 ? reinterpret_cast<float *>(ws + L.seg[2]) : nullptr;
+    return sw;
 }
 
 Args make_args(const gdr_problem *p, unsigned *err) {
@@ -219,9 +253,9 @@ gdr_status check_ws(const Layout &L, void *ws, size_t bytes) {
 gdr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA; }
 
 // ---- per-kernel timing: event pairs recorded around each launch while enabled
-enum KernelId { K_PREP = 0, K_WY_FWD, K_CHAIN_FWD, K_CHAIN_FWD_RECOMPUTE, K_CHAIN_BWD, K_BWD_CHUNK, K_DG_SCAN, K_COUNT };
-const char *const kKernelNames[K_COUNT] = {"prep_chunks", "wy_fwd",    "chain_fwd", "chain_fwd_recompute",
-                                           "chain_bwd",   "bwd_chunk", "dg_scan"};
+enum KernelId { K_PREP = 0, K_WY_FWD, K_CHAIN_FWD, K_CHAIN_FWD_RECOMPUTE, K_CHAIN_BWD, K_BWD_CHUNK, K_COUNT };
+const char *const kKernelNames[K_COUNT] = {"prep_chunks", "wy_fwd", "chain_fwd", "chain_fwd_recompute",
+                                           "chain_bwd",   "bwd_chunk"};
 struct Pending {
     int id;
     cudaEvent_t a, b;
@@ -344,8 +378,10 @@ gdr_status gdr_fwd(const gdr_problem *p, const void *q, const void *k, const voi
     float *gcs = g_cumsum ? g_cumsum : reinterpret_cast<float *>(ws + L.gcs);
     void *Aw = A ? A : static_cast<void *>(ws + L.A);
     if ((st = timed(K_WY_FWD, s, [&] { return launch_wy_fwd(a, k, g, beta, gcs, Aw, s); })) != GDR_OK) return st;
-    return timed(K_CHAIN_FWD, s,
-                 [&] { return launch_chain_fwd(a, q, k, v, gcs, beta, Aw, h0, o, final_state, h, true, nullptr, s); });
+    const SegWs sw = seg_ws(L, ws);
+    return timed(K_CHAIN_FWD, s, [&] {
+        return launch_chain_fwd(a, q, k, v, gcs, beta, Aw, h0, o, final_state, h, true, nullptr, sw, s);
+    });
 }
 
 gdr_status gdr_bwd(const gdr_problem *p, const void *q, const void *k, const void *v, const float *g_cumsum,
@@ -368,24 +404,20 @@ gdr_status gdr_bwd(const gdr_problem *p, const void *q, const void *k, const voi
     Args a = make_args(p, err);
     if ((st = tables(p, a, ws, L, s)) != GDR_OK) return st;
     void *hw = ws + L.h, *dhw = ws + L.dhn, *dlw = ws + L.delta, *ddlw = ws + L.ddelta;
-    float *Dw = reinterpret_cast<float *>(ws + L.D), *hTw = reinterpret_cast<float *>(ws + L.hT);
-    // states and Delta of every chunk (recomputed), the reverse state-gradient chain, every chunk's
-    // gradients in parallel, then the sequence-level gate gradient
+    // states and Delta of every chunk (recomputed), the reverse state-gradient chain, then every
+    // chunk's gradients in parallel
+    const SegWs sw = seg_ws(L, ws);
     if ((st = timed(K_CHAIN_FWD_RECOMPUTE, s, [&] {
-             return launch_chain_fwd(a, q, k, v, g_cumsum, beta, A, h0, nullptr, dht ? hTw : nullptr, hw, false, dlw,
-                                     s);
+             return launch_chain_fwd(a, q, k, v, g_cumsum, beta, A, h0, nullptr, nullptr, hw, false, dlw, sw, s);
          })) != GDR_OK)
         return st;
     if ((st = timed(K_CHAIN_BWD, s, [&] {
-             return launch_chain_bwd(a, q, k, g_cumsum, beta, A, dout, dht, dhw, ddlw, dh0, s);
+             return launch_chain_bwd(a, q, k, g_cumsum, beta, A, dout, dht, dhw, ddlw, dh0, sw, s);
          })) != GDR_OK)
         return st;
-    if ((st = timed(K_BWD_CHUNK, s, [&] {
-             return launch_bwd_chunk_tc(a, q, k, v, g_cumsum, beta, A, dout, hw, dhw, dlw, ddlw, dq, dk, dv, dbeta, Dw,
-                                        s);
-         })) != GDR_OK)
-        return st;
-    return timed(K_DG_SCAN, s, [&] { return launch_dg_scan(a, Dw, dht, hTw, dg, s); });
+    return timed(K_BWD_CHUNK, s, [&] {
+        return launch_bwd_chunk_tc(a, q, k, v, g_cumsum, beta, A, dout, hw, dhw, dlw, ddlw, dq, dk, dv, dg, dbeta, s);
+    });
 }
 
 gdr_status gdr_get_error(void *stream) {

@@ -21,11 +21,11 @@
 //   round 5: dk += dKK K + dKK^T K
 //
 // dbeta_r = e^{G_r} <(A^T dW)_r, k_r> + <(A^T dDelta)_r, v_r> + sum_s dL_rs Gamma_rs KK_rs.
-// The gate gradient uses the exact identity that follows from h_t = e^{G_t} h~_t
-// (the gate enters only through e^{G_t} q_t, e^{-G_t} v_t and the final state):
-//   dg_s = sum_{t >= s} (<q_t, dq_t> - <v_t, dv_t>) + <dh_T, h_T>
-// per sequence and value head (q, dq before the L2-norm chain rule); this kernel
-// writes D_t = <q_t, dq_t> - <v_t, dv_t> and dg_scan finishes the reverse sum.
+// dG_r (gradient w.r.t. the chunk-local cumsum G) collects the decay terms of P (E = dP o P)
+// and L (F = dL o L) as row sums minus column sums, <q_r, scale e^{G_r} (dO h^T)_r>,
+// -e^{Gl-G_r} <(Delta dH'^T)_r, k_r>, beta_r e^{G_r} <(A^T dW)_r, k_r>, and at the last valid
+// row e^{Gl} <dH', h> plus the sum of the key terms; dg is its reverse cumsum inside the chunk.
+// All reductions run in a fixed order (deterministic results).
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -45,10 +45,13 @@ constexpr uint32_t S_DA = S_D0, S_DKK = S_D0 + 16384; // reuse Delta's blocks af
 constexpr uint32_t S_H = 131072, S_DH = 163840;       // [128 x 64] blocks of 16 KB
 constexpr uint32_t S_A = 196608, S_AKG = 204800;
 constexpr uint32_t S_F = 212992;                      // scalars
-constexpr uint32_t S_BAR = S_F + 16 * 64 * 4, S_SLOT = S_BAR + 8, S_FLAG = S_SLOT + 4, S_USED = S_FLAG + 4;
+constexpr uint32_t S_BAR = S_F + 32 * 64 * 4, S_SLOT = S_BAR + 8, S_FLAG = S_SLOT + 4, S_USED = S_FLAG + 4;
 constexpr uint32_t S_BYTES = S_USED + 1024;
 // scalar slots (64 floats each)
-enum { F_G = 0, F_B, F_EG, F_EL, F_QD0, F_QD1, F_VD0, F_VD1, F_KD0, F_KD1, F_LB0, F_LB1 };
+enum {
+    F_G = 0, F_B, F_EG, F_EL, F_QD0, F_QD1, F_VD0, F_VD1, F_KD0, F_KD1, F_LB0, F_LB1,
+    F_ER0, F_ER1, F_EC0, F_EC1, F_Z0, F_Z1, F_FR0, F_FR1, F_FC0, F_FC1, F_HD, F_DG, F_COUNT
+};
 // TMEM columns
 constexpr uint32_t T_R1 = 0, T_R2 = 128, T_R3 = 256, T_R4 = 384, T_R8 = 448, T_COLS = 512;
 
@@ -58,8 +61,7 @@ template <> struct IsBf16<__nv_bfloat16> { static constexpr bool value = true; }
 struct BcP {
     const void *q, *k, *v, *A, *beta, *dout, *h, *dhn, *delta, *ddelta;
     const float *g_cs;
-    void *dq, *dk, *dv, *dbeta;
-    float *D;  // [tokens, Hv] fp32
+    void *dq, *dk, *dv, *dg, *dbeta;
     bool gate_f32, l2norm;
     float scale;
 };
@@ -87,6 +89,22 @@ __device__ __forceinline__ void load_rows64(uint32_t dst, const T *src, long lon
         const bool ok = r < valid;
         cp_async16(dst + umma::off(r, c * 8, 0), ok ? src + r * stride + c * 8 : src, ok);
     }
+}
+
+// Column sums of a 32 x 32 block held one row per lane (v[c] = column c): lane l ends
+// with the sum over the 32 lanes of column l (a fixed-order butterfly, 31 shuffles).
+__device__ __forceinline__ float colsum32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < o; ++i) {
+            const float send = up ? v[i] : v[i + o];
+            const float keep = up ? v[i + o] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0];
 }
 
 template <typename T>
@@ -361,37 +379,64 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, BcP p) {
                     qd += qv[u] * x[u];
                 }
             }
-            // dS = scale dP o Gamma o M  (dP = dO Delta^T in columns 64..127 of R3)
+            // dS = scale dP o Gamma o M  (dP = dO Delta^T in columns 64..127 of R3);
+            // E = dS o (Q K^T) = dP o P gives the decay terms of dG (row sums minus column sums)
             const float gr = f(F_G, r);
+            float ev[32], er = 0.f;
 #pragma unroll
             for (int c = 0; c < 32; c += 16) {
-                float x[16];
+                float x[16], qk[16];
                 umma::ld16(umma::taddr(tmem, lb, T_R3 + 64 + hh * 32 + c), x);
+                umma::ld16(umma::taddr(tmem, lb, T_R4 + hh * 32 + c), qk);
                 umma::ld_wait();
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const int s = hh * 32 + c + u;
                     x[u] = (s <= r && r < valid) ? p.scale * x[u] * __expf(gr - f(F_G, s)) : 0.f;
+                    ev[c + u] = x[u] * qk[u];
+                    er += ev[c + u];
                 }
                 store16<T>(sb + S_DS, r, hh * 32 + c, x);
             }
+            f(F_ER0 + hh, r) = er;
+            f(F_EC0 + (warp & 1), hh * 32 + lane) = colsum32(ev, lane);
         } else {
             // dW = -(dDelta h^T) rows; dk += e^{Gl - G_r} Delta dH'^T
             const uint32_t wblk = hh ? S_DW1 : S_DW0;
             const float el = f(F_EL, r);
+            float z = 0.f;  // e^{Gl-G_r} <(Delta dH'^T)_r, k_r>: dG terms of the decayed keys
 #pragma unroll
             for (int c = 0; c < 64; c += 16) {
-                float x[16], y[16];
+                float x[16], y[16], kv[16];
                 umma::ld16(umma::taddr(tmem, lb, T_R1 + hh * 64 + c), x);
                 umma::ld16(umma::taddr(tmem, lb, T_R2 + hh * 64 + c), y);
+                load16<T>(sb + S_K0 + hh * 16384, r, c, kv);
                 umma::ld_wait();
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     x[u] = -x[u];
                     acc[c + u] += el * y[u];
+                    z += el * y[u] * kv[u];
                 }
                 store16<T>(sb + wblk, r, c, x);
             }
+            f(F_Z0 + hh, r) = z;
+        }
+        {
+            // <dH', h> over the whole state (both tiles share one layout, so equal offsets hold equal elements)
+            float hd = 0.f;
+#pragma unroll 4
+            for (int u = 0; u < 16; ++u) {
+                const uint32_t o = (uint32_t)(tid * 16 + u) * 8u;
+                const uint2 a = *reinterpret_cast<const uint2 *>(smem + S_H + o);
+                const uint2 b = *reinterpret_cast<const uint2 *>(smem + S_DH + o);
+                const float2 a0 = Elt<T>::unpack(a.x), a1 = Elt<T>::unpack(a.y);
+                const float2 b0 = Elt<T>::unpack(b.x), b1 = Elt<T>::unpack(b.y);
+                hd += a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, o);
+            if (lane == 0) f(F_HD, warp) = hd;
         }
         sync_tc();
 
@@ -486,15 +531,11 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, BcP p) {
             }
 #pragma unroll
             for (int c = 0; c < 64; c += 16) {
-                float x[16], qv[16];
+                float x[16];
                 umma::ld16(umma::taddr(tmem, lb, T_R1 + hh * 64 + c), x);
-                load16<T>(sb + S_Q0 + hh * 16384, r, c, qv);
                 umma::ld_wait();
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    acc[c + u] += x[u];
-                    qd += qv[u] * x[u];
-                }
+                for (int u = 0; u < 16; ++u) acc[c + u] += x[u];
             }
         } else {
 #pragma unroll
@@ -521,6 +562,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, BcP p) {
         float lb_ = 0.f;  // upper lanes: sum_s dL Gamma KK
         if (upper) {
             const float gr = f(F_G, r), br = f(F_B, r);
+            float fv[32], fr = 0.f;  // F = dL o L: decay terms of dG
 #pragma unroll
             for (int c = 0; c < 32; c += 16) {
                 float x[16], kk[16];
@@ -535,9 +577,13 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, BcP p) {
                     const float dlv = m ? -x[u] : 0.f;
                     lb_ += dlv * gam * kk[u];
                     x[u] = dlv * br * gam;
+                    fv[c + u] = x[u] * kk[u];
+                    fr += fv[c + u];
                 }
                 store16<T>(sb + S_DKK, r, hh * 32 + c, x);
             }
+            f(F_FR0 + hh, r) = fr;
+            f(F_FC0 + ((warp & 3) - 2), hh * 32 + lane) = colsum32(fv, lane);
         }
         sync_tc();
 
@@ -570,13 +616,52 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, BcP p) {
             f(F_KD0 + hh, r) = kd;
         }
         __syncthreads();
-        if (tid < C && tid < valid) {
-            const int rr = tid;
-            const float br = f(F_B, rr);
-            const float vdot = f(F_VD0, rr) + f(F_VD1, rr);
-            const float db = f(F_EG, rr) * (f(F_KD0, rr) + f(F_KD1, rr)) + vdot + (f(F_LB0, rr) + f(F_LB1, rr));
-            store_gate<T>(p.dbeta, (tok0 + rr) * Hv + j, p.gate_f32, db);
-            p.D[(tok0 + rr) * Hv + j] = (f(F_QD0, rr) + f(F_QD1, rr)) - br * vdot;
+        if (warp == 0) {
+            // dG_r = E row - E column + <q_r, dq_inter_r> - z_r + beta_r e^{G_r} <(A^T dW)_r, k_r>
+            //        + F row - F column; the last valid row adds e^{Gl} <dH', h> + sum_s z_s
+            float dgv[2], zs = 0.f;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int rr = lane + 32 * hf;
+                const float z = f(F_Z0, rr) + f(F_Z1, rr);
+                zs += z;
+                const float kd2 = f(F_KD0, rr) + f(F_KD1, rr);
+                const float dG = (f(F_ER0, rr) + f(F_ER1, rr)) - (f(F_EC0, rr) + f(F_EC1, rr)) +
+                                 (f(F_QD0, rr) + f(F_QD1, rr)) - z + f(F_B, rr) * f(F_EG, rr) * kd2 +
+                                 (f(F_FR0, rr) + f(F_FR1, rr)) - (f(F_FC0, rr) + f(F_FC1, rr));
+                dgv[hf] = rr < valid ? dG : 0.f;
+                if (rr < valid) {
+                    const float vdot = f(F_VD0, rr) + f(F_VD1, rr);
+                    store_gate<T>(p.dbeta, (tok0 + rr) * Hv + j, p.gate_f32,
+                                  f(F_EG, rr) * kd2 + vdot + (f(F_LB0, rr) + f(F_LB1, rr)));
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);
+            float hd = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) hd += f(F_HD, w);
+            const float extra = __expf(Gl) * hd + zs;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf)
+                if (lane + 32 * hf == valid - 1) dgv[hf] += extra;
+            // dg_s = sum_{r >= s} dG_r within the chunk
+            float y1 = dgv[1], y0 = dgv[0];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float t1 = __shfl_down_sync(0xffffffffu, y1, o);
+                const float t0 = __shfl_down_sync(0xffffffffu, y0, o);
+                if (lane + o < 32) {
+                    y1 += t1;
+                    y0 += t0;
+                }
+            }
+            y0 += __shfl_sync(0xffffffffu, y1, 0);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int rr = lane + 32 * hf;
+                if (rr < valid) store_gate<T>(p.dg, (tok0 + rr) * Hv + j, p.gate_f32, hf ? y1 : y0);
+            }
         }
         __syncthreads();
     }
@@ -602,56 +687,6 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, BcP p) {
     if (warp == 0) umma::dealloc(tmem, T_COLS);
 }
 
-// dg_s = sum_{t >= s} D_t + <dh_T, h_T> over each sequence, per value head.
-template <typename T>
-__global__ void __launch_bounds__(256) dg_scan_kernel(Geo geo, const float *__restrict__ D, const float *__restrict__ dht,
-                                                      const float *__restrict__ hT, void *dg, bool gate_f32) {
-    __shared__ float s_red[8];
-    __shared__ float s_carry;
-    const int j = blockIdx.x, n = blockIdx.y, Hv = geo.Hv;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    long long tok0;
-    int len, row0;
-    geo.seq(n, tok0, len, row0);
-    float hd = 0.f;
-    if (dht) {
-        const long long base = ((long long)n * Hv + j) * DK * DV;
-        for (int i = tid; i < DK * DV; i += 256) hd += dht[base + i] * hT[base + i];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, o);
-    if (lane == 0) s_red[warp] = hd;
-    __syncthreads();
-    if (tid == 0) {
-        float t = 0.f;
-        for (int w = 0; w < 8; ++w) t += s_red[w];
-        s_carry = t;
-    }
-    __syncthreads();
-    // reverse inclusive scan in tiles of 256 tokens, from the end of the sequence
-    for (int end = len; end > 0; end -= 256) {
-        const int t = end - 1 - tid;  // thread 0 takes the last token of the tile
-        float x = (t >= 0) ? D[(tok0 + t) * Hv + j] : 0.f;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
-        }
-        if (lane == 31) s_red[warp] = x;
-        __syncthreads();
-        float pre = s_carry;
-        for (int w = 0; w < warp; ++w) pre += s_red[w];
-        if (t >= 0) store_gate<T>(dg, (tok0 + t) * Hv + j, gate_f32, x + pre);
-        __syncthreads();
-        if (tid == 0) {
-            float tot = 0.f;
-            for (int w = 0; w < 8; ++w) tot += s_red[w];
-            s_carry += tot;
-        }
-        __syncthreads();
-    }
-}
-
 template <typename T>
 cudaError_t bwd_chunk_tc_t(const Args &a, const BcP &p, cudaStream_t s) {
     if (a.max_chunks == 0) return cudaSuccess;
@@ -667,8 +702,8 @@ cudaError_t bwd_chunk_tc_t(const Args &a, const BcP &p, cudaStream_t s) {
 
 cudaError_t launch_bwd_chunk_tc(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
                                 const void *beta, const void *A, const void *dout, const void *h, const void *dhn,
-                                const void *delta, const void *ddelta, void *dq, void *dk, void *dv, void *dbeta,
-                                float *D, cudaStream_t s) {
+                                const void *delta, const void *ddelta, void *dq, void *dk, void *dv, void *dg,
+                                void *dbeta, cudaStream_t s) {
     BcP p;
     p.q = q;
     p.k = k;
@@ -685,20 +720,11 @@ cudaError_t launch_bwd_chunk_tc(const Args &a, const void *q, const void *k, con
     p.dk = dk;
     p.dv = dv;
     p.dbeta = dbeta;
-    p.D = D;
+    p.dg = dg;
     p.gate_f32 = a.gate_f32;
     p.l2norm = a.l2norm;
     p.scale = a.scale;
     return a.bf16 ? bwd_chunk_tc_t<__nv_bfloat16>(a, p, s) : bwd_chunk_tc_t<__half>(a, p, s);
-}
-
-cudaError_t launch_dg_scan(const Args &a, const float *D, const float *dht, const float *hT, void *dg, cudaStream_t s) {
-    dim3 grid(a.Hv, a.N);
-    if (a.bf16)
-        dg_scan_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(make_geo(a), D, dht, hT, dg, a.gate_f32);
-    else
-        dg_scan_kernel<__half><<<grid, 256, 0, s>>>(make_geo(a), D, dht, hT, dg, a.gate_f32);
-    return cudaGetLastError();
 }
 
 }  // namespace gdr

@@ -45,6 +45,13 @@ struct TcP {
     void *o, *h;
     void *delta;  // optional [rows,Hv,64,128]: Delta = U - W h of every chunk
     float *fin;
+    // sequence split into nseg segments of whole chunks (1 = no split):
+    //   affine pass: block x = 2*seg + kind; kind 0 starts from zero, kind 1 from the identity with
+    //                zero values; both write their end state (S-form [V][K] fp32) to seg_end[kind]
+    //   full pass  : block x = seg; starts from seg_start (S-form) when given
+    int nseg;
+    const float *seg_start;  // [N,Hv,nseg,128,128]
+    float *seg_end0, *seg_end1;
     bool gate_f32, l2norm, v_first, h_api;
     float scale;
 };
@@ -143,7 +150,7 @@ __device__ __forceinline__ void sync_tc() {
     umma::fence_after();
 }
 
-template <typename T, bool WRITE_O>
+template <typename T, bool WRITE_O, bool AFFINE>
 __global__ void __launch_bounds__(NT, 1) chain_fwd_tc_kernel(Geo geo, TcP p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -157,12 +164,18 @@ __global__ void __launch_bounds__(NT, 1) chain_fwd_tc_kernel(Geo geo, TcP p) {
     long long tok0;
     int len, row0;
     geo.seq(n, tok0, len, row0);
-    const int nc = (len + C - 1) / C;
+    const int nc_all = (len + C - 1) / C;
+    // this block's segment of chunks [cb, ce)
+    const int seg = AFFINE ? (int)blockIdx.x >> 1 : (int)blockIdx.x;
+    const int kind = AFFINE ? (int)blockIdx.x & 1 : 0;  // 1: identity start, zero values
+    const int sl = (nc_all + p.nseg - 1) / p.nseg;
+    const int cb = min(nc_all, seg * sl), ce = min(nc_all, cb + sl);
     const T *q = static_cast<const T *>(p.q);
     const T *k = static_cast<const T *>(p.k);
     const T *v = static_cast<const T *>(p.v);
     const T *A = static_cast<const T *>(p.A);
     const long long st_base = ((long long)n * Hv + j) * DK * DV;
+    const long long seg_base = (((long long)n * Hv + j) * p.nseg + seg) * DK * DV;
     const uint32_t bar = sb + P_BAR;
     volatile int *sflag = reinterpret_cast<volatile int *>(smem + P_FLAG);
     float *fEG = reinterpret_cast<float *>(smem + P_FAC);  // e^{G_s}
@@ -184,7 +197,12 @@ __global__ void __launch_bounds__(NT, 1) chain_fwd_tc_kernel(Geo geo, TcP p) {
 #pragma unroll
     for (int i = 0; i < 64; ++i) {
         const int d = hh * 64 + i;
-        S[i] = p.h0 ? p.h0[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] : 0.f;
+        if (AFFINE)
+            S[i] = (kind == 1 && d == e) ? 1.f : 0.f;
+        else if (p.seg_start)
+            S[i] = p.seg_start[seg_base + (long long)e * DK + d];
+        else
+            S[i] = p.h0 ? p.h0[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] : 0.f;
     }
     auto write_S_tile = [&]() {
 #pragma unroll
@@ -199,7 +217,8 @@ __global__ void __launch_bounds__(NT, 1) chain_fwd_tc_kernel(Geo geo, TcP p) {
         const int valid = min(C, len - i * C);
         if (WRITE_O) load_tile128<T>(st + ST_QK, 16384, q + (tb * Hq + hq) * DK, (long long)Hq * DK, valid, tid);
         load_tile128<T>(st + ST_QK + 8192, 16384, k + (tb * Hq + hq) * DK, (long long)Hq * DK, valid, tid);
-        load_tile128<T>(st + ST_V, 8192, v + (tb * Hv + j) * DV, (long long)Hv * DV, valid, tid);
+        // the identity-start affine pass runs with zero values (U = 0)
+        load_tile128<T>(st + ST_V, 8192, v + (tb * Hv + j) * DV, (long long)Hv * DV, kind == 1 ? 0 : valid, tid);
         load_tile64<T>(st + ST_A, A + (tb * Hv + j) * C, (long long)Hv * C, valid, tid);
         if (tid < C) {
             const bool ok = tid < valid;
@@ -208,7 +227,7 @@ __global__ void __launch_bounds__(NT, 1) chain_fwd_tc_kernel(Geo geo, TcP p) {
         }
         cp_async_commit();
     };
-    if (nc > 0) prefetch(0);
+    if (cb < ce) prefetch(cb);
 
     uint32_t phase = 0;
     const uint32_t id_n64 = umma::idesc(128, 64, bf16, false, false);
@@ -233,7 +252,7 @@ __global__ void __launch_bounds__(NT, 1) chain_fwd_tc_kernel(Geo geo, TcP p) {
         return *sflag == 0;
     };
 
-    for (int i = 0; i < nc; ++i) {
+    for (int i = cb; i < ce; ++i) {
         const uint32_t st = sb + (i & 1) * ST_BYTES;
         const float *sG = reinterpret_cast<const float *>(smem + (i & 1) * ST_BYTES + ST_G);
         float *sB = reinterpret_cast<float *>(smem + (i & 1) * ST_BYTES + ST_B);
@@ -270,7 +289,7 @@ __global__ void __launch_bounds__(NT, 1) chain_fwd_tc_kernel(Geo geo, TcP p) {
             umma::st_shared_v4(sb + P_AB + o, wb[0], wb[1], wb[2], wb[3]);
         }
         // the state before this chunk (optional output)
-        if (p.h) {
+        if (!AFFINE && p.h) {
             T *h = static_cast<T *>(p.h);
             const long long hb = ((long long)(row0 + i) * Hv + j) * DK * DV;
             if (p.h_api && p.v_first) {
@@ -291,7 +310,7 @@ __global__ void __launch_bounds__(NT, 1) chain_fwd_tc_kernel(Geo geo, TcP p) {
             }
         }
         sync_tc();
-        if (i + 1 < nc) prefetch(i + 1);
+        if (i + 1 < ce) prefetch(i + 1);
 
         // ---- round 1
         // (descriptors of successive K-steps differ only in the start-address field: add offset >> 4)
@@ -361,7 +380,7 @@ __global__ void __launch_bounds__(NT, 1) chain_fwd_tc_kernel(Geo geo, TcP p) {
             for (int u = 0; u < 16; ++u) y[u] = x[u] * fEL[hh * 32 + c + u];
             store16<T>(sb + P_D, e, hh * 32 + c, x);
             store16<T>(sb + P_DT, e, hh * 32 + c, y);
-            if (p.delta) {
+            if (!AFFINE && p.delta) {
                 T *dr = static_cast<T *>(p.delta) + ((long long)(row0 + i) * Hv + j) * C * DV +
                         (long long)(hh * 32 + c) * DV + e;
 #pragma unroll
@@ -411,11 +430,17 @@ __global__ void __launch_bounds__(NT, 1) chain_fwd_tc_kernel(Geo geo, TcP p) {
         sync_tc();
     }
 
-    if (p.fin && *sflag == 0) {
+    if (*sflag == 0) {
+        if (AFFINE) {
+            float *dst = (kind ? p.seg_end1 : p.seg_end0) + seg_base + (long long)e * DK + hh * 64;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-            const int d = hh * 64 + i;
-            p.fin[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] = S[i];
+            for (int i = 0; i < 64; i += 4) *reinterpret_cast<float4 *>(dst + i) = make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
+        } else if (p.fin && seg == p.nseg - 1) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                const int d = hh * 64 + i;
+                p.fin[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] = S[i];
+            }
         }
     }
     umma::fence_before();
@@ -448,6 +473,12 @@ struct TcBwdP {
     float *dh0;
     bool gate_f32, l2norm, v_first;
     float scale;
+    // sequence split, mirrored: segment seg covers chunks [cb, ce), walked from ce-1 down to cb;
+    // the affine pass (block x = 2*seg + kind; kind 1 = identity start with dO = 0) writes the
+    // gradient at the segment start; the full pass starts from seg_start at the segment end
+    int nseg;
+    const float *seg_start;
+    float *seg_end0, *seg_end1;
 };
 
 // persistent tiles of the reverse chain (same stage layout as the forward, with
@@ -458,7 +489,7 @@ constexpr uint32_t B_AKG = 2 * ST_BYTES, B_DS = B_AKG + 8192, B_WT = B_DS + 3276
 constexpr uint32_t B_SMEM_BYTES = B_USED + 1024;
 constexpr uint32_t TB_KQ = 0, TB_W = 64, TB_E1 = 128, TB_E2 = 192, TB_X = 256, TB_COLS = 512;
 
-template <typename T>
+template <typename T, bool AFFINE>
 __global__ void __launch_bounds__(NT, 1) chain_bwd_tc_kernel(Geo geo, TcBwdP p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -471,12 +502,17 @@ __global__ void __launch_bounds__(NT, 1) chain_bwd_tc_kernel(Geo geo, TcBwdP p) 
     long long tok0;
     int len, row0;
     geo.seq(n, tok0, len, row0);
-    const int nc = (len + C - 1) / C;
+    const int nc_all = (len + C - 1) / C;
+    const int seg = AFFINE ? (int)blockIdx.x >> 1 : (int)blockIdx.x;
+    const int kind = AFFINE ? (int)blockIdx.x & 1 : 0;
+    const int sl = (nc_all + p.nseg - 1) / p.nseg;
+    const int cb = min(nc_all, seg * sl), ce = min(nc_all, cb + sl);
     const T *q = static_cast<const T *>(p.q);
     const T *k = static_cast<const T *>(p.k);
     const T *A = static_cast<const T *>(p.A);
     const T *dout = static_cast<const T *>(p.dout);
     const long long st_base = ((long long)n * Hv + j) * DK * DV;
+    const long long seg_base = (((long long)n * Hv + j) * p.nseg + seg) * DK * DV;
     const uint32_t bar = sb + B_BAR;
     volatile int *sflag = reinterpret_cast<volatile int *>(smem + B_FLAG);
     float *fEG = reinterpret_cast<float *>(smem + B_FAC);
@@ -497,7 +533,12 @@ __global__ void __launch_bounds__(NT, 1) chain_bwd_tc_kernel(Geo geo, TcBwdP p) 
 #pragma unroll
     for (int i = 0; i < 64; ++i) {
         const int d = hh * 64 + i;
-        S[i] = p.dht ? p.dht[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] : 0.f;
+        if (AFFINE)
+            S[i] = (kind == 1 && d == e) ? 1.f : 0.f;
+        else if (p.seg_start)
+            S[i] = p.seg_start[seg_base + (long long)e * DK + d];
+        else
+            S[i] = p.dht ? p.dht[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] : 0.f;
     }
     auto write_S_tile = [&]() {
 #pragma unroll
@@ -512,7 +553,7 @@ __global__ void __launch_bounds__(NT, 1) chain_bwd_tc_kernel(Geo geo, TcBwdP p) 
         const int valid = min(C, len - i * C);
         load_tile128<T>(st + ST_QK, 16384, k + (tb * Hq + hq) * DK, (long long)Hq * DK, valid, tid);
         load_tile128<T>(st + ST_QK + 8192, 16384, q + (tb * Hq + hq) * DK, (long long)Hq * DK, valid, tid);
-        load_tile128<T>(st + ST_V, 8192, dout + (tb * Hv + j) * DV, (long long)Hv * DV, valid, tid);
+        load_tile128<T>(st + ST_V, 8192, dout + (tb * Hv + j) * DV, (long long)Hv * DV, kind == 1 ? 0 : valid, tid);
         load_tile64<T>(st + ST_A, A + (tb * Hv + j) * C, (long long)Hv * C, valid, tid);
         if (tid < C) {
             const bool ok = tid < valid;
@@ -521,7 +562,7 @@ __global__ void __launch_bounds__(NT, 1) chain_bwd_tc_kernel(Geo geo, TcBwdP p) 
         }
         cp_async_commit();
     };
-    if (nc > 0) prefetch(nc - 1);
+    if (cb < ce) prefetch(ce - 1);
 
     uint32_t phase = 0;
     const uint32_t id_n64 = umma::idesc(128, 64, bf16, false, false);
@@ -543,14 +584,14 @@ __global__ void __launch_bounds__(NT, 1) chain_bwd_tc_kernel(Geo geo, TcBwdP p) 
         return *sflag == 0;
     };
 
-    for (int i = nc - 1; i >= 0; --i) {
+    for (int i = ce - 1; i >= cb; --i) {
         const uint32_t st = sb + (i & 1) * ST_BYTES;
         const float *sG = reinterpret_cast<const float *>(smem + (i & 1) * ST_BYTES + ST_G);
         float *sB = reinterpret_cast<float *>(smem + (i & 1) * ST_BYTES + ST_B);
         cp_async_wait<0>();
         if (tid < C) sB[tid] = breg;
         // gradient w.r.t. the state after this chunk, for the per-chunk kernel ([K][V] layout)
-        {
+        if (!AFFINE) {
             T *hc = static_cast<T *>(p.dhn) + ((long long)(row0 + i) * Hv + j) * DK * DV + (long long)(hh * 64) * DV + e;
 #pragma unroll
             for (int d = 0; d < 64; ++d) hc[d * DV] = Elt<T>::from_f(S[d]);
@@ -598,7 +639,7 @@ __global__ void __launch_bounds__(NT, 1) chain_bwd_tc_kernel(Geo geo, TcBwdP p) 
             umma::st_shared_v4(sb + B_DOG + o, wo[0], wo[1], wo[2], wo[3]);
         }
         sync_tc();
-        if (i > 0) prefetch(i - 1);
+        if (i > cb) prefetch(i - 1);
 
         // ---- round 1: [K;Q] Q^T, W^T, E1 = dS' K^T
         const uint64_t dKa = umma::desc(st + ST_QK, 16, 1024), dQa = umma::desc(st + ST_QK + 8192, 16, 1024);
@@ -657,9 +698,12 @@ __global__ void __launch_bounds__(NT, 1) chain_bwd_tc_kernel(Geo geo, TcBwdP p) 
 #pragma unroll
             for (int u = 0; u < 16; ++u) x1[u] = -(x1[u] * fEL[hh * 32 + c + u] + x2[u]);
             store16<T>(sb + B_DDT, e, hh * 32 + c, x1);
-            T *dr = static_cast<T *>(p.ddelta) + ((long long)(row0 + i) * Hv + j) * C * DV + (long long)(hh * 32 + c) * DV + e;
+            if (!AFFINE) {
+                T *dr = static_cast<T *>(p.ddelta) + ((long long)(row0 + i) * Hv + j) * C * DV +
+                        (long long)(hh * 32 + c) * DV + e;
 #pragma unroll
-            for (int u = 0; u < 16; ++u) dr[u * DV] = Elt<T>::from_f(-x1[u]);
+                for (int u = 0; u < 16; ++u) dr[u * DV] = Elt<T>::from_f(-x1[u]);
+            }
         }
         sync_tc();
 
@@ -687,11 +731,17 @@ __global__ void __launch_bounds__(NT, 1) chain_bwd_tc_kernel(Geo geo, TcBwdP p) 
         sync_tc();
     }
 
-    if (p.dh0 && *sflag == 0) {
+    if (*sflag == 0) {
+        if (AFFINE) {
+            float *dst = (kind ? p.seg_end1 : p.seg_end0) + seg_base + (long long)e * DK + hh * 64;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-            const int d = hh * 64 + i;
-            p.dh0[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] = S[i];
+            for (int i = 0; i < 64; i += 4) *reinterpret_cast<float4 *>(dst + i) = make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
+        } else if (p.dh0 && seg == 0) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                const int d = hh * 64 + i;
+                p.dh0[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] = S[i];
+            }
         }
     }
     umma::fence_before();
@@ -700,33 +750,85 @@ __global__ void __launch_bounds__(NT, 1) chain_bwd_tc_kernel(Geo geo, TcBwdP p) 
 }
 
 template <typename T>
-cudaError_t chain_bwd_tc_t(const Args &a, const TcBwdP &p, cudaStream_t s) {
-    auto kern = chain_bwd_tc_kernel<T>;
+cudaError_t chain_bwd_tc_t(const Args &a, const TcBwdP &p, bool affine, cudaStream_t s) {
+    auto kern = affine ? chain_bwd_tc_kernel<T, true> : chain_bwd_tc_kernel<T, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, B_SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid(1, a.Hv, a.N);
+    dim3 grid(affine ? 2 * p.nseg : p.nseg, a.Hv, a.N);
     kern<<<grid, NT, B_SMEM_BYTES, s>>>(make_geo(a), p);
     return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t chain_fwd_tc_t(const Args &a, const TcP &p, bool write_o, cudaStream_t s) {
-    auto kern = write_o ? chain_fwd_tc_kernel<T, true> : chain_fwd_tc_kernel<T, false>;
+cudaError_t chain_fwd_tc_t(const Args &a, const TcP &p, bool write_o, bool affine, cudaStream_t s) {
+    auto kern = affine ? chain_fwd_tc_kernel<T, false, true>
+                       : (write_o ? chain_fwd_tc_kernel<T, true, false> : chain_fwd_tc_kernel<T, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid(1, a.Hv, a.N);
-    Geo g = make_geo(a);
-    kern<<<grid, NT, SMEM_BYTES, s>>>(g, p);
+    dim3 grid(affine ? 2 * p.nseg : p.nseg, a.Hv, a.N);
+    kern<<<grid, NT, SMEM_BYTES, s>>>(make_geo(a), p);
     return cudaGetLastError();
+}
+
+// Segment start states: S_0 = init (API state layout, or zero), S_{s+1} = S_s P_s + Q_s in fp32,
+// walking segments forward (or backward when reverse), with P = seg_end1, Q = seg_end0 (S-form).
+// One block per (16-row slice of the value index, head, sequence).
+__global__ void __launch_bounds__(256) seg_scan_kernel(int Hv, int nseg, bool reverse, const float *__restrict__ init,
+                                                       bool v_first, const float *__restrict__ P,
+                                                       const float *__restrict__ Q, float *__restrict__ out) {
+    __shared__ float sS[16][DK];
+    const int blk = blockIdx.x, j = blockIdx.y, n = blockIdx.z;
+    const int tid = threadIdx.x, rr = tid >> 4, cb = (tid & 15) * 8;
+    const int e = blk * 16 + rr;
+    const long long st_base = ((long long)n * Hv + j) * DK * DV;
+    for (int i = 0; i < 8; ++i) {
+        const int d = cb + i;
+        sS[rr][d] = init ? init[st_base + (v_first ? (long long)e * DK + d : (long long)d * DV + e)] : 0.f;
+    }
+    __syncthreads();
+    for (int t = 0; t < nseg; ++t) {
+        const int sg = reverse ? nseg - 1 - t : t;
+        const long long sbase = (((long long)n * Hv + j) * nseg + sg) * DK * DV;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            acc[i] = sS[rr][cb + i];
+            out[sbase + (long long)e * DK + cb + i] = acc[i];
+        }
+        if (t + 1 == nseg) break;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = Q[sbase + (long long)e * DK + cb + i];
+        for (int d2 = 0; d2 < DK; ++d2) {
+            const float a = sS[rr][d2];
+            const float4 p0 = *reinterpret_cast<const float4 *>(P + sbase + (long long)d2 * DK + cb);
+            const float4 p1 = *reinterpret_cast<const float4 *>(P + sbase + (long long)d2 * DK + cb + 4);
+            acc[0] += a * p0.x;
+            acc[1] += a * p0.y;
+            acc[2] += a * p0.z;
+            acc[3] += a * p0.w;
+            acc[4] += a * p1.x;
+            acc[5] += a * p1.y;
+            acc[6] += a * p1.z;
+            acc[7] += a * p1.w;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sS[rr][cb + i] = acc[i];
+        __syncthreads();
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
                              const void *A, const void *dout, const float *dht, void *dhn, void *ddelta, float *dh0,
-                             cudaStream_t s) {
+                             const SegWs &sw, cudaStream_t s) {
     TcBwdP p;
     p.ddelta = ddelta;
+    p.nseg = sw.nseg;
+    p.seg_start = nullptr;
+    p.seg_end0 = sw.end0;
+    p.seg_end1 = sw.end1;
     p.q = q;
     p.k = k;
     p.A = A;
@@ -740,14 +842,27 @@ cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const 
     p.l2norm = a.l2norm;
     p.v_first = a.v_first;
     p.scale = a.scale;
-    return a.bf16 ? chain_bwd_tc_t<__nv_bfloat16>(a, p, s) : chain_bwd_tc_t<__half>(a, p, s);
+    cudaError_t e;
+    if (sw.nseg > 1) {
+        e = a.bf16 ? chain_bwd_tc_t<__nv_bfloat16>(a, p, true, s) : chain_bwd_tc_t<__half>(a, p, true, s);
+        if (e != cudaSuccess) return e;
+        seg_scan_kernel<<<dim3(DV / 16, a.Hv, a.N), 256, 0, s>>>(a.Hv, sw.nseg, true, dht, a.v_first, sw.end1,
+                                                                 sw.end0, sw.start);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        p.seg_start = sw.start;
+    }
+    return a.bf16 ? chain_bwd_tc_t<__nv_bfloat16>(a, p, false, s) : chain_bwd_tc_t<__half>(a, p, false, s);
 }
 
 cudaError_t launch_chain_fwd(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
                              const void *beta, const void *A, const float *h0, void *o, float *final_state, void *h,
-                             bool h_api_layout, void *delta, cudaStream_t s) {
+                             bool h_api_layout, void *delta, const SegWs &sw, cudaStream_t s) {
     TcP p;
     p.delta = delta;
+    p.nseg = sw.nseg;
+    p.seg_start = nullptr;
+    p.seg_end0 = sw.end0;
+    p.seg_end1 = sw.end1;
     p.q = q;
     p.k = k;
     p.v = v;
@@ -763,8 +878,17 @@ cudaError_t launch_chain_fwd(const Args &a, const void *q, const void *k, const 
     p.v_first = a.v_first;
     p.h_api = h_api_layout;
     p.scale = a.scale;
-    return a.bf16 ? chain_fwd_tc_t<__nv_bfloat16>(a, p, o != nullptr, s)
-                  : chain_fwd_tc_t<__half>(a, p, o != nullptr, s);
+    cudaError_t e;
+    if (sw.nseg > 1) {
+        e = a.bf16 ? chain_fwd_tc_t<__nv_bfloat16>(a, p, false, true, s) : chain_fwd_tc_t<__half>(a, p, false, true, s);
+        if (e != cudaSuccess) return e;
+        seg_scan_kernel<<<dim3(DV / 16, a.Hv, a.N), 256, 0, s>>>(a.Hv, sw.nseg, false, h0, a.v_first, sw.end1, sw.end0,
+                                                                 sw.start);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        p.seg_start = sw.start;
+    }
+    return a.bf16 ? chain_fwd_tc_t<__nv_bfloat16>(a, p, o != nullptr, false, s)
+                  : chain_fwd_tc_t<__half>(a, p, o != nullptr, false, s);
 }
 
 }  // namespace gdr

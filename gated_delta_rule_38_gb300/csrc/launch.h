@@ -24,6 +24,13 @@ struct Args {
     unsigned *err;           // device error word
 };
 
+// Workspace of the intra-GPU sequence split (nseg segments per sequence; nseg == 1: no split):
+// three [N,Hv,nseg,128,128] fp32 arrays of transposed states.
+struct SegWs {
+    int nseg;
+    float *start, *end0, *end1;
+};
+
 cudaError_t launch_prep_chunks(const int32_t *cu, int N, int T, int chunk, int32_t *idx, int64_t max_chunks,
                                int32_t *off, int32_t *total, unsigned *err, cudaStream_t s);
 
@@ -34,17 +41,15 @@ cudaError_t launch_wy_fwd(const Args &a, const void *k, const void *g, const voi
 // and per-chunk Delta = U - W h (delta != nullptr).
 cudaError_t launch_chain_fwd(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
                              const void *beta, const void *A, const float *h0, void *o, float *final_state, void *h,
-                             bool h_api_layout, void *delta, cudaStream_t s);
+                             bool h_api_layout, void *delta, const SegWs &sw, cudaStream_t s);
 // Backward: reverse state-gradient chain (dH' and dDelta of every chunk, dh0).
 cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
                              const void *A, const void *dout, const float *dht, void *dhn, void *ddelta, float *dh0,
-                             cudaStream_t s);
-// Backward: per-chunk gradients (dq, dk, dv, dbeta and the gate-gradient terms D).
+                             const SegWs &sw, cudaStream_t s);
+// Backward: per-chunk gradients (dq, dk, dv, dg, dbeta).
 cudaError_t launch_bwd_chunk_tc(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
                                 const void *beta, const void *A, const void *dout, const void *h, const void *dhn,
-                                const void *delta, const void *ddelta, void *dq, void *dk, void *dv, void *dbeta,
-                                float *D, cudaStream_t s);
-// Backward: dg = reverse cumsum of D over every sequence + <dht, final state>.
-cudaError_t launch_dg_scan(const Args &a, const float *D, const float *dht, const float *hT, void *dg, cudaStream_t s);
+                                const void *delta, const void *ddelta, void *dq, void *dk, void *dv, void *dg,
+                                void *dbeta, cudaStream_t s);
 
 }  // namespace gdr
