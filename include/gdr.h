@@ -151,6 +151,29 @@ gdr_status gdr_bwd(const gdr_problem *p, const void *q, const void *k, const voi
                    void *dbeta, float *dh0, void *workspace, size_t workspace_bytes,
                    void *stream);
 
+/*
+ * Forward for callers that cannot allocate device memory (no counterpart on the
+ * pages: it is an addition of this library).  Some callers may not call
+ * cudaMalloc at all -- code running inside a memory pool it does not own, embedded
+ * runtimes that forbid allocation after start-up, or code in a region where an
+ * allocation would synchronise the device.  This entry point computes what gdr_fwd
+ * computes for o and final_state (no g_cumsum, A or h outputs) but takes no
+ * workspace: it uses a 64 MiB scratch array that is part of the library's device
+ * image, held by every GPU that loads the library until the process exits.  It
+ * allocates nothing itself and calls no allocating routine.
+ *   in/out: as gdr_fwd (q, k, v, g, beta, h0 nullable; o; final_state nullable).
+ *   Returns GDR_ERR_WORKSPACE when the problem's forward workspace
+ *   (gdr_fwd_workspace_size) exceeds 64 MiB; every other error as gdr_fwd.
+ * The first call on a device looks up the scratch array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call before
+ * any stream capture.  All calls share the one array: calls whose work overlaps on
+ * the GPU (different streams, or different host threads without ordering) race on
+ * it and must be serialised by the caller.  Nothing in the array has to start at
+ * zero; each call writes every scratch value before reading it.
+ */
+gdr_status gdr_fwd_noalloc(const gdr_problem *p, const void *q, const void *k, const void *v, const void *g,
+                           const void *beta, const float *h0, void *o, float *final_state, void *stream);
+
 /* Synchronises `stream`, then returns and clears the device error word of the
  * current device (GDR_OK when no kernel latched an error), or GDR_ERR_CUDA when
  * the stream reports a CUDA error. */
