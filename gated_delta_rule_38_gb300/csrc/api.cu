@@ -148,21 +148,28 @@ int64_t max_chunks_of(const gdr_problem *p) {
     return (int64_t)p->B * ((p->T + C - 1) / C);
 }
 
-// Segments per sequence for the intra-GPU sequence split.  Automatic choice: only when the
-// (sequence, value head) streams cannot fill the GPU's SMs; enough segments to occupy them, each
-// at least 4 chunks long.  Host-only (the workspace size must not depend on the device).
+// Segments per sequence for the intra-GPU sequence split.  Every chain CTA occupies one SM, so with
+// S segments the affine pass runs ceil(2 S streams / SMs) waves and the full pass ceil(S streams / SMs)
+// waves, each over ceil(chunks / S) chunks (an affine chunk costs about 0.7 of a full one), plus a
+// scan whose cost grows with S.  The automatic choice minimises that estimate; S = 1 means no split.
+// Host-only (the workspace size must not depend on the device).
 constexpr int64_t kSplitSMs = 152;
 int choose_nseg(const gdr_problem *p) {
-    const int64_t streams = (int64_t)num_seqs(p) * p->Hv;
+    const int64_t streams = std::max<int64_t>(1, (int64_t)num_seqs(p) * p->Hv);
     const int64_t maxc = std::max<int64_t>(1, ((int64_t)p->T + C - 1) / C);
-    int64_t s;
-    if (p->num_segments > 0)
-        s = std::min<int64_t>(p->num_segments, maxc);
-    else if (streams * 2 > kSplitSMs)
-        s = 1;
-    else
-        s = std::min<int64_t>(kSplitSMs / streams, maxc / 4);
-    return (int)std::max<int64_t>(1, std::min<int64_t>(s, 64));
+    if (p->num_segments > 0) return (int)std::max<int64_t>(1, std::min<int64_t>({p->num_segments, maxc, 64}));
+    auto waves = [&](int64_t ctas) { return (ctas + kSplitSMs - 1) / kSplitSMs; };
+    double best = (double)waves(streams) * (double)maxc;
+    int best_s = 1;
+    for (int64_t s = 2; s <= std::min<int64_t>(64, maxc); ++s) {
+        const double per = (double)((maxc + s - 1) / s);
+        const double cost = per * (0.7 * (double)waves(2 * s * streams) + (double)waves(s * streams)) + 2.0 * (double)s;
+        if (cost < 0.9 * best) {
+            best = cost;
+            best_s = (int)s;
+        }
+    }
+    return best_s;
 }
 
 struct Layout {
@@ -253,9 +260,11 @@ gdr_status check_ws(const Layout &L, void *ws, size_t bytes) {
 gdr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA; }
 
 // ---- per-kernel timing: event pairs recorded around each launch while enabled
-enum KernelId { K_PREP = 0, K_WY_FWD, K_CHAIN_FWD, K_CHAIN_FWD_RECOMPUTE, K_CHAIN_BWD, K_BWD_CHUNK, K_COUNT };
-const char *const kKernelNames[K_COUNT] = {"prep_chunks", "wy_fwd", "chain_fwd", "chain_fwd_recompute",
-                                           "chain_bwd",   "bwd_chunk"};
+enum KernelId {
+    K_PREP = 0, K_WY_FWD, K_CHAIN_FWD, K_CHAIN_FWD_RECOMPUTE, K_CHAIN_BWD, K_CHAIN_PAIR, K_BWD_CHUNK, K_COUNT
+};
+const char *const kKernelNames[K_COUNT] = {"prep_chunks", "wy_fwd",     "chain_fwd", "chain_fwd_recompute",
+                                           "chain_bwd",   "chain_pair", "bwd_chunk"};
 struct Pending {
     int id;
     cudaEvent_t a, b;
@@ -407,14 +416,20 @@ gdr_status gdr_bwd(const gdr_problem *p, const void *q, const void *k, const voi
     // states and Delta of every chunk (recomputed), the reverse state-gradient chain, then every
     // chunk's gradients in parallel
     const SegWs sw = seg_ws(L, ws);
-    if ((st = timed(K_CHAIN_FWD_RECOMPUTE, s, [&] {
+    if (sw.nseg == 1) {
+        if ((st = timed(K_CHAIN_PAIR, s, [&] {
+                 return launch_chain_pair(a, q, k, v, g_cumsum, beta, A, h0, hw, dlw, dout, dht, dhw, ddlw, dh0, s);
+             })) != GDR_OK)
+            return st;
+    } else if ((st = timed(K_CHAIN_FWD_RECOMPUTE, s, [&] {
              return launch_chain_fwd(a, q, k, v, g_cumsum, beta, A, h0, nullptr, nullptr, hw, false, dlw, sw, s);
-         })) != GDR_OK)
+         })) != GDR_OK) {
         return st;
-    if ((st = timed(K_CHAIN_BWD, s, [&] {
-             return launch_chain_bwd(a, q, k, g_cumsum, beta, A, dout, dht, dhw, ddlw, dh0, sw, s);
-         })) != GDR_OK)
+    } else if ((st = timed(K_CHAIN_BWD, s, [&] {
+                    return launch_chain_bwd(a, q, k, g_cumsum, beta, A, dout, dht, dhw, ddlw, dh0, sw, s);
+                })) != GDR_OK) {
         return st;
+    }
     return timed(K_BWD_CHUNK, s, [&] {
         return launch_bwd_chunk_tc(a, q, k, v, g_cumsum, beta, A, dout, hw, dhw, dlw, ddlw, dq, dk, dv, dg, dbeta, s);
     });

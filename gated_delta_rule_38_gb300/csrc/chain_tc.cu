@@ -151,11 +151,10 @@ __device__ __forceinline__ void sync_tc() {
 }
 
 template <typename T, bool WRITE_O, bool AFFINE>
-__global__ void __launch_bounds__(NT, 1) chain_fwd_tc_kernel(Geo geo, TcP p) {
+__device__ __forceinline__ void chain_fwd_body(const Geo &geo, const TcP &p, const int bx, const int j, const int n) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
-    const int j = blockIdx.y, n = blockIdx.z;
     const int Hv = geo.Hv, Hq = geo.Hq, hq = j / (Hv / Hq);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // thread (e, hh): TMEM lane / state row e, column half hh
@@ -166,8 +165,8 @@ __global__ void __launch_bounds__(NT, 1) chain_fwd_tc_kernel(Geo geo, TcP p) {
     geo.seq(n, tok0, len, row0);
     const int nc_all = (len + C - 1) / C;
     // this block's segment of chunks [cb, ce)
-    const int seg = AFFINE ? (int)blockIdx.x >> 1 : (int)blockIdx.x;
-    const int kind = AFFINE ? (int)blockIdx.x & 1 : 0;  // 1: identity start, zero values
+    const int seg = AFFINE ? bx >> 1 : bx;
+    const int kind = AFFINE ? bx & 1 : 0;  // 1: identity start, zero values
     const int sl = (nc_all + p.nseg - 1) / p.nseg;
     const int cb = min(nc_all, seg * sl), ce = min(nc_all, cb + sl);
     const T *q = static_cast<const T *>(p.q);
@@ -490,11 +489,10 @@ constexpr uint32_t B_SMEM_BYTES = B_USED + 1024;
 constexpr uint32_t TB_KQ = 0, TB_W = 64, TB_E1 = 128, TB_E2 = 192, TB_X = 256, TB_COLS = 512;
 
 template <typename T, bool AFFINE>
-__global__ void __launch_bounds__(NT, 1) chain_bwd_tc_kernel(Geo geo, TcBwdP p) {
+__device__ __forceinline__ void chain_bwd_body(const Geo &geo, const TcBwdP &p, const int bx, const int j, const int n) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
-    const int j = blockIdx.y, n = blockIdx.z;
     const int Hv = geo.Hv, Hq = geo.Hq, hq = j / (Hv / Hq);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int e = tid & 127, hh = tid >> 7, lb = (warp & 3) * 32;
@@ -503,8 +501,8 @@ __global__ void __launch_bounds__(NT, 1) chain_bwd_tc_kernel(Geo geo, TcBwdP p) 
     int len, row0;
     geo.seq(n, tok0, len, row0);
     const int nc_all = (len + C - 1) / C;
-    const int seg = AFFINE ? (int)blockIdx.x >> 1 : (int)blockIdx.x;
-    const int kind = AFFINE ? (int)blockIdx.x & 1 : 0;
+    const int seg = AFFINE ? bx >> 1 : bx;
+    const int kind = AFFINE ? bx & 1 : 0;
     const int sl = (nc_all + p.nseg - 1) / p.nseg;
     const int cb = min(nc_all, seg * sl), ce = min(nc_all, cb + sl);
     const T *q = static_cast<const T *>(p.q);
@@ -749,6 +747,26 @@ __global__ void __launch_bounds__(NT, 1) chain_bwd_tc_kernel(Geo geo, TcBwdP p) 
     if (warp == 0) umma::dealloc(tmem, TB_COLS);
 }
 
+template <typename T, bool WRITE_O, bool AFFINE>
+__global__ void __launch_bounds__(NT, 1) chain_fwd_tc_kernel(Geo geo, TcP p) {
+    chain_fwd_body<T, WRITE_O, AFFINE>(geo, p, blockIdx.x, blockIdx.y, blockIdx.z);
+}
+
+template <typename T, bool AFFINE>
+__global__ void __launch_bounds__(NT, 1) chain_bwd_tc_kernel(Geo geo, TcBwdP p) {
+    chain_bwd_body<T, AFFINE>(geo, p, blockIdx.x, blockIdx.y, blockIdx.z);
+}
+
+// The backward's two chains are independent: blocks z < N recompute the forward states,
+// blocks z >= N run the reverse state-gradient chain, side by side on the GPU.
+template <typename T>
+__global__ void __launch_bounds__(NT, 1) chain_pair_kernel(Geo geo, TcP pf, TcBwdP pb) {
+    if ((int)blockIdx.z < geo.N)
+        chain_fwd_body<T, false, false>(geo, pf, blockIdx.x, blockIdx.y, blockIdx.z);
+    else
+        chain_bwd_body<T, false>(geo, pb, blockIdx.x, blockIdx.y, blockIdx.z - geo.N);
+}
+
 template <typename T>
 cudaError_t chain_bwd_tc_t(const Args &a, const TcBwdP &p, bool affine, cudaStream_t s) {
     auto kern = affine ? chain_bwd_tc_kernel<T, true> : chain_bwd_tc_kernel<T, false>;
@@ -820,15 +838,11 @@ __global__ void __launch_bounds__(256) seg_scan_kernel(int Hv, int nseg, bool re
 
 }  // namespace
 
-cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
-                             const void *A, const void *dout, const float *dht, void *dhn, void *ddelta, float *dh0,
-                             const SegWs &sw, cudaStream_t s) {
+namespace {
+
+TcBwdP bwd_params(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta, const void *A,
+                  const void *dout, const float *dht, void *dhn, void *ddelta, float *dh0, const SegWs &sw) {
     TcBwdP p;
-    p.ddelta = ddelta;
-    p.nseg = sw.nseg;
-    p.seg_start = nullptr;
-    p.seg_end0 = sw.end0;
-    p.seg_end1 = sw.end1;
     p.q = q;
     p.k = k;
     p.A = A;
@@ -837,11 +851,62 @@ cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const 
     p.g_cs = g_cs;
     p.dht = dht;
     p.dhn = dhn;
+    p.ddelta = ddelta;
     p.dh0 = dh0;
     p.gate_f32 = a.gate_f32;
     p.l2norm = a.l2norm;
     p.v_first = a.v_first;
     p.scale = a.scale;
+    p.nseg = sw.nseg;
+    p.seg_start = nullptr;
+    p.seg_end0 = sw.end0;
+    p.seg_end1 = sw.end1;
+    return p;
+}
+
+TcP fwd_params(const Args &a, const void *q, const void *k, const void *v, const float *g_cs, const void *beta,
+               const void *A, const float *h0, void *o, float *final_state, void *h, bool h_api_layout, void *delta,
+               const SegWs &sw) {
+    TcP p;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.A = A;
+    p.beta = beta;
+    p.g_cs = g_cs;
+    p.h0 = h0;
+    p.o = o;
+    p.h = h;
+    p.delta = delta;
+    p.fin = final_state;
+    p.gate_f32 = a.gate_f32;
+    p.l2norm = a.l2norm;
+    p.v_first = a.v_first;
+    p.h_api = h_api_layout;
+    p.scale = a.scale;
+    p.nseg = sw.nseg;
+    p.seg_start = nullptr;
+    p.seg_end0 = sw.end0;
+    p.seg_end1 = sw.end1;
+    return p;
+}
+
+template <typename T>
+cudaError_t chain_pair_t(const Args &a, const TcP &pf, const TcBwdP &pb, cudaStream_t s) {
+    auto kern = chain_pair_kernel<T>;
+    const uint32_t smem = SMEM_BYTES > B_SMEM_BYTES ? SMEM_BYTES : B_SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(1, a.Hv, 2 * a.N), NT, smem, s>>>(make_geo(a), pf, pb);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
+                             const void *A, const void *dout, const float *dht, void *dhn, void *ddelta, float *dh0,
+                             const SegWs &sw, cudaStream_t s) {
+    TcBwdP p = bwd_params(a, q, k, g_cs, beta, A, dout, dht, dhn, ddelta, dh0, sw);
     cudaError_t e;
     if (sw.nseg > 1) {
         e = a.bf16 ? chain_bwd_tc_t<__nv_bfloat16>(a, p, true, s) : chain_bwd_tc_t<__half>(a, p, true, s);
@@ -857,27 +922,7 @@ cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const 
 cudaError_t launch_chain_fwd(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
                              const void *beta, const void *A, const float *h0, void *o, float *final_state, void *h,
                              bool h_api_layout, void *delta, const SegWs &sw, cudaStream_t s) {
-    TcP p;
-    p.delta = delta;
-    p.nseg = sw.nseg;
-    p.seg_start = nullptr;
-    p.seg_end0 = sw.end0;
-    p.seg_end1 = sw.end1;
-    p.q = q;
-    p.k = k;
-    p.v = v;
-    p.A = A;
-    p.beta = beta;
-    p.g_cs = g_cs;
-    p.h0 = h0;
-    p.o = o;
-    p.h = h;
-    p.fin = final_state;
-    p.gate_f32 = a.gate_f32;
-    p.l2norm = a.l2norm;
-    p.v_first = a.v_first;
-    p.h_api = h_api_layout;
-    p.scale = a.scale;
+    TcP p = fwd_params(a, q, k, v, g_cs, beta, A, h0, o, final_state, h, h_api_layout, delta, sw);
     cudaError_t e;
     if (sw.nseg > 1) {
         e = a.bf16 ? chain_fwd_tc_t<__nv_bfloat16>(a, p, false, true, s) : chain_fwd_tc_t<__half>(a, p, false, true, s);
@@ -889,6 +934,15 @@ cudaError_t launch_chain_fwd(const Args &a, const void *q, const void *k, const 
     }
     return a.bf16 ? chain_fwd_tc_t<__nv_bfloat16>(a, p, o != nullptr, false, s)
                   : chain_fwd_tc_t<__half>(a, p, o != nullptr, false, s);
+}
+
+cudaError_t launch_chain_pair(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
+                              const void *beta, const void *A, const float *h0, void *h, void *delta, const void *dout,
+                              const float *dht, void *dhn, void *ddelta, float *dh0, cudaStream_t s) {
+    SegWs none{1, nullptr, nullptr, nullptr};
+    const TcP pf = fwd_params(a, q, k, v, g_cs, beta, A, h0, nullptr, nullptr, h, false, delta, none);
+    const TcBwdP pb = bwd_params(a, q, k, g_cs, beta, A, dout, dht, dhn, ddelta, dh0, none);
+    return a.bf16 ? chain_pair_t<__nv_bfloat16>(a, pf, pb, s) : chain_pair_t<__half>(a, pf, pb, s);
 }
 
 }  // namespace gdr

@@ -46,6 +46,11 @@ cudaError_t launch_chain_fwd(const Args &a, const void *q, const void *k, const 
 cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
                              const void *A, const void *dout, const float *dht, void *dhn, void *ddelta, float *dh0,
                              const SegWs &sw, cudaStream_t s);
+// Backward, no sequence split: both chains above (forward recompute without output, reverse chain) in
+// one launch, side by side.
+cudaError_t launch_chain_pair(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
+                              const void *beta, const void *A, const float *h0, void *h, void *delta, const void *dout,
+                              const float *dht, void *dhn, void *ddelta, float *dh0, cudaStream_t s);
 // Backward: per-chunk gradients (dq, dk, dv, dg, dbeta).
 cudaError_t launch_bwd_chunk_tc(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
                                 const void *beta, const void *A, const void *dout, const void *h, const void *dhn,
