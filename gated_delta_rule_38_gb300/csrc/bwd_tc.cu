@@ -28,14 +28,18 @@
 // All reductions run in a fixed order (deterministic results).
 #include <cuda_runtime.h>
 
+#include <cuda.h>
+
 #include "common.cuh"
 #include "launch.h"
+#include "tmap.h"
 #include "umma.cuh"
 
 namespace gdr {
 namespace {
 
 constexpr int NT = 256;
+constexpr int FLD = DK + 1;  // row stride (floats) of the fp32 dq/dk staging
 // ---- shared memory (bytes from a 1024-aligned base)
 constexpr uint32_t S_Q0 = 0, S_K0 = 8192;             // [Q b0][K b0][Q b1][K b1]
 constexpr uint32_t S_DO0 = 32768, S_DD0 = 40960;      // [dO b0][dDelta b0][dO b1][dDelta b1]
@@ -45,7 +49,8 @@ constexpr uint32_t S_DA = S_D0, S_DKK = S_D0 + 16384; // reuse Delta's blocks af
 constexpr uint32_t S_H = 131072, S_DH = 163840;       // [128 x 64] blocks of 16 KB
 constexpr uint32_t S_A = 196608, S_AKG = 204800;
 constexpr uint32_t S_F = 212992;                      // scalars
-constexpr uint32_t S_BAR = S_F + 32 * 64 * 4, S_SLOT = S_BAR + 8, S_FLAG = S_SLOT + 4, S_USED = S_FLAG + 4;
+constexpr uint32_t S_BAR = S_F + 32 * 64 * 4, S_LBAR = S_BAR + 8, S_SLOT = S_LBAR + 8, S_FLAG = S_SLOT + 4,
+                   S_USED = S_FLAG + 4;
 constexpr uint32_t S_BYTES = S_USED + 1024;
 // scalar slots (64 floats each)
 enum {
@@ -59,6 +64,9 @@ template <typename T> struct IsBf16 { static constexpr bool value = false; };
 template <> struct IsBf16<__nv_bfloat16> { static constexpr bool value = true; };
 
 struct BcP {
+    // TMA maps: q, k [tokens][Hq][128]; dO, v [tokens][Hv][128]; A [tokens][Hv][64];
+    // states h, dH' [rows*Hv][128][128]; Delta, dDelta [rows*Hv][64][128]
+    CUtensorMap tq, tk, tdo, tv, ta, th, tdh, td, tdd;
     const void *q, *k, *v, *A, *beta, *dout, *h, *dhn, *delta, *ddelta;
     const float *g_cs;
     void *dq, *dk, *dv, *dg, *dbeta;
@@ -69,26 +77,6 @@ struct BcP {
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, bool valid) {
     const int n = valid ? 4 : 0;
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(n));
-}
-
-// rows x 128 (16-bit) from global into two swizzled 64-column blocks `bstride` apart
-template <typename T>
-__device__ __forceinline__ void load_rows128(uint32_t dst, uint32_t bstride, const T *src, long long stride, int rows,
-                                             int valid, int tid) {
-    for (int i = tid; i < rows * 16; i += NT) {
-        const int r = i >> 4, c = i & 15;
-        const bool ok = r < valid;
-        cp_async16(dst + (uint32_t)(c >> 3) * bstride + umma::off(r, (c & 7) * 8, 0), ok ? src + r * stride + c * 8 : src,
-                   ok);
-    }
-}
-template <typename T>
-__device__ __forceinline__ void load_rows64(uint32_t dst, const T *src, long long stride, int valid, int tid) {
-    for (int i = tid; i < 64 * 8; i += NT) {
-        const int r = i >> 3, c = i & 7;
-        const bool ok = r < valid;
-        cp_async16(dst + umma::off(r, c * 8, 0), ok ? src + r * stride + c * 8 : src, ok);
-    }
 }
 
 // Column sums of a 32 x 32 block held one row per lane (v[c] = column c): lane l ends
@@ -183,7 +171,7 @@ __device__ __forceinline__ void l2norm_bwd_rows(const float *src, const T *x, lo
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             xv[u] = Elt<T>::to_f(xr[lane * 4 + u]);
-            gv[u] = src[r * DK + lane * 4 + u];
+            gv[u] = src[r * FLD + lane * 4 + u];
         }
         if (l2norm) {
             float ss = xv[0] * xv[0] + xv[1] * xv[1] + xv[2] * xv[2] + xv[3] * xv[3];
@@ -206,7 +194,7 @@ __device__ __forceinline__ void l2norm_bwd_rows(const float *src, const T *x, lo
 }
 
 template <typename T>
-__global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, BcP p) {
+__global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __grid_constant__ BcP p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -223,27 +211,19 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, BcP p) {
     constexpr bool bf16 = IsBf16<T>::value;
     const T *q = static_cast<const T *>(p.q);
     const T *k = static_cast<const T *>(p.k);
-    const T *v = static_cast<const T *>(p.v);
-    const T *A = static_cast<const T *>(p.A);
-    const T *dout = static_cast<const T *>(p.dout);
-    const T *hs = static_cast<const T *>(p.h);
-    const T *dhs = static_cast<const T *>(p.dhn);
-    const T *dl = static_cast<const T *>(p.delta);
-    const T *ddl = static_cast<const T *>(p.ddelta);
     float *F = reinterpret_cast<float *>(smem + S_F);
     auto f = [&](int slot_, int i) -> float & { return F[slot_ * 64 + i]; };
     const uint32_t bar = sb + S_BAR;
     volatile int *sflag = reinterpret_cast<volatile int *>(smem + S_FLAG);
 
+    const uint32_t lbar = sb + S_LBAR;  // tile loads
     if (tid == 0) {
         umma::mbar_init(bar, 1);
+        umma::mbar_init(lbar, 1);
         umma::fence_mbar_init();
         *sflag = 0;
     }
     if (warp == 0) umma::alloc(sb + S_SLOT, T_COLS);
-    load_rows128<T>(sb + S_Q0, 16384, q + (tok0 * Hq + hq) * DK, (long long)Hq * DK, 64, valid, tid);
-    load_rows128<T>(sb + S_K0, 16384, k + (tok0 * Hq + hq) * DK, (long long)Hq * DK, 64, valid, tid);
-    cp_async_commit();
     umma::fence_before();
     __syncthreads();
     umma::fence_after();
@@ -277,7 +257,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, BcP p) {
     const uint64_t dKKk = umma::desc(sb + S_DKK - 8192, 16, 1024);    // rows 64..127 = dKK
     const uint64_t dKKmn = umma::desc(sb + S_DKK - 8192, 8192, 1024); // m 64..127 = dKK^T
 
-    uint32_t phase = 0;
+    uint32_t phase = 0, lphase = 0;
     auto wait_mma = [&]() -> bool {
         if (tid == 0 && !umma::mbar_wait(bar, phase)) {
             raise_error(geo.err, GDR_ERR_TIMEOUT);
@@ -303,15 +283,32 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, BcP p) {
 
     for (int jj = 0; jj < grp && ok; ++jj) {
         const int j = hq * grp + jj;
-        const long long sbase = ((long long)slot * Hv + j) * DK * DV;
-        const long long dbase = ((long long)slot * Hv + j) * C * DV;
-        load_rows128<T>(sb + S_DO0, 16384, dout + (tok0 * Hv + j) * DV, (long long)Hv * DV, 64, valid, tid);
-        load_rows128<T>(sb + S_DD0, 16384, ddl + dbase, DV, 64, valid, tid);
-        load_rows128<T>(sb + S_V0, 16384, v + (tok0 * Hv + j) * DV, (long long)Hv * DV, 64, valid, tid);
-        load_rows128<T>(sb + S_D0, 16384, dl + dbase, DV, 64, valid, tid);
-        load_rows128<T>(sb + S_H, 16384, hs + sbase, DV, 128, 128, tid);
-        load_rows128<T>(sb + S_DH, 16384, dhs + sbase, DV, 128, 128, tid);
-        load_rows64<T>(sb + S_A, A + (tok0 * Hv + j) * C, (long long)Hv * C, valid, tid);
+        if (tid == 0) {
+            // every tile lands in the 128-byte-swizzled layout of the MMA operands; rows past the end of
+            // the sequence carry the next sequence's data (harmless: each product that reads them is
+            // masked, and dDelta is stored zero there)
+            const int t = (int)tok0, row = slot * Hv + j;
+            tma::expect_tx(lbar, (jj == 0 ? 32768u : 0u) + 4 * 16384u + 2 * 32768u + 8192u);
+            if (jj == 0) {
+                tma::load3d(sb + S_Q0, &p.tq, 0, hq, t, lbar);
+                tma::load3d(sb + S_Q0 + 16384, &p.tq, 64, hq, t, lbar);
+                tma::load3d(sb + S_K0, &p.tk, 0, hq, t, lbar);
+                tma::load3d(sb + S_K0 + 16384, &p.tk, 64, hq, t, lbar);
+            }
+            tma::load3d(sb + S_DO0, &p.tdo, 0, j, t, lbar);
+            tma::load3d(sb + S_DO0 + 16384, &p.tdo, 64, j, t, lbar);
+            tma::load3d(sb + S_DD0, &p.tdd, 0, 0, row, lbar);
+            tma::load3d(sb + S_DD0 + 16384, &p.tdd, 64, 0, row, lbar);
+            tma::load3d(sb + S_V0, &p.tv, 0, j, t, lbar);
+            tma::load3d(sb + S_V0 + 16384, &p.tv, 64, j, t, lbar);
+            tma::load3d(sb + S_D0, &p.td, 0, 0, row, lbar);
+            tma::load3d(sb + S_D0 + 16384, &p.td, 64, 0, row, lbar);
+            tma::load3d(sb + S_H, &p.th, 0, 0, row, lbar);
+            tma::load3d(sb + S_H + 16384, &p.th, 64, 0, row, lbar);
+            tma::load3d(sb + S_DH, &p.tdh, 0, 0, row, lbar);
+            tma::load3d(sb + S_DH + 16384, &p.tdh, 64, 0, row, lbar);
+            tma::load3d(sb + S_A, &p.ta, 0, j, t, lbar);
+        }
         if (tid < C) {
             const bool okr = tid < valid;
             cp_async4(sb + S_F + (F_G * 64 + tid) * 4, p.g_cs + (okr ? (tok0 + tid) * Hv + j : 0), okr);
@@ -319,7 +316,16 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, BcP p) {
         }
         cp_async_commit();
         cp_async_wait<0>();
+        if (!umma::mbar_wait(lbar, lphase)) {
+            raise_error(geo.err, GDR_ERR_TIMEOUT);
+            *sflag = 1;
+        }
+        lphase ^= 1u;
         __syncthreads();
+        if (*sflag) {
+            ok = false;
+            break;
+        }
         if (jj == 0 && p.l2norm) {
             l2norm64<T>(sb + S_Q0, valid, warp, lane);
             l2norm64<T>(sb + S_K0, valid, warp, lane);
@@ -334,7 +340,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, BcP p) {
         for (int u = 0; u < 2; ++u) {
             const int cix = tid + u * NT, rr = cix >> 3, c = cix & 7;
             const uint32_t o = umma::off(rr, c * 8, 0);
-            const uint4 a = umma::ld_shared_v4(sb + S_A + o);
+            uint4 a = umma::ld_shared_v4(sb + S_A + o);
+            if (rr >= valid) a = make_uint4(0u, 0u, 0u, 0u);
             const uint32_t w[4] = {a.x, a.y, a.z, a.w};
             uint32_t wk[4];
 #pragma unroll
@@ -667,12 +674,14 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, BcP p) {
     }
 
     // ---- dq (lower lanes) and dk (upper lanes): stage fp32, L2-norm chain rule, store
-    float *fq = reinterpret_cast<float *>(smem + S_DO0);           // [64][128] fp32 (32 KB)
-    float *fk = reinterpret_cast<float *>(smem + S_DO0 + 32768);   // [64][128] fp32 (32 KB)
+    // [64][129] fp32 each (a row stride of 129 words spreads the rows written by one warp over all banks);
+    // every tile is dead by now, so the staging may overlap any of them
+    float *fq = reinterpret_cast<float *>(smem + S_DO0);
+    float *fk = reinterpret_cast<float *>(smem + S_DO0 + 64 * FLD * 4);
     if (ok) {
         float *dst = upper ? fk : fq;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) dst[r * DK + hh * 64 + i] = acc[i];
+        for (int i = 0; i < 64; ++i) dst[r * FLD + hh * 64 + i] = acc[i];
     }
     __syncthreads();
     if (ok) {
@@ -705,6 +714,18 @@ cudaError_t launch_bwd_chunk_tc(const Args &a, const void *q, const void *k, con
                                 const void *delta, const void *ddelta, void *dq, void *dk, void *dv, void *dg,
                                 void *dbeta, cudaStream_t s) {
     BcP p;
+    const uint64_t tokens = (uint64_t)a.B * (uint64_t)a.T, rows = (uint64_t)a.max_chunks * a.Hv;
+    const bool bf = a.bf16;
+    if (!make_tmap_3d(&p.tq, q, bf, DK, a.Hq, tokens, DK * 2, (uint64_t)a.Hq * DK * 2, 64, 1, 64) ||
+        !make_tmap_3d(&p.tk, k, bf, DK, a.Hq, tokens, DK * 2, (uint64_t)a.Hq * DK * 2, 64, 1, 64) ||
+        !make_tmap_3d(&p.tdo, dout, bf, DV, a.Hv, tokens, DV * 2, (uint64_t)a.Hv * DV * 2, 64, 1, 64) ||
+        !make_tmap_3d(&p.tv, v, bf, DV, a.Hv, tokens, DV * 2, (uint64_t)a.Hv * DV * 2, 64, 1, 64) ||
+        !make_tmap_3d(&p.ta, A, bf, C, a.Hv, tokens, C * 2, (uint64_t)a.Hv * C * 2, 64, 1, 64) ||
+        !make_tmap_3d(&p.th, h, bf, DV, DK, rows, DV * 2, (uint64_t)DK * DV * 2, 64, 128, 1) ||
+        !make_tmap_3d(&p.tdh, dhn, bf, DV, DK, rows, DV * 2, (uint64_t)DK * DV * 2, 64, 128, 1) ||
+        !make_tmap_3d(&p.td, delta, bf, DV, C, rows, DV * 2, (uint64_t)C * DV * 2, 64, 64, 1) ||
+        !make_tmap_3d(&p.tdd, ddelta, bf, DV, C, rows, DV * 2, (uint64_t)C * DV * 2, 64, 64, 1))
+        return cudaErrorInvalidValue;
     p.q = q;
     p.k = k;
     p.v = v;

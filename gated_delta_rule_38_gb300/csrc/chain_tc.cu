@@ -1,9 +1,9 @@
 // Forward recurrence on the 5th-generation tensor cores (tcgen05 + TMEM).
 //
-// One CTA of 256 threads per (sequence, value head).  The state is held
-// transposed, S = h^T [V x K] in fp32 registers: row e lives in threads e and
-// e + 128 (one half of the key columns each), and row e is also TMEM lane e of
-// every [V x *] accumulator.  Per
+// One CTA of 512 threads per (sequence, value head).  The state is held
+// transposed, S = h^T [V x K] in fp32 registers: row e lives in threads e,
+// e + 128, e + 256 and e + 384 (a quarter of the key columns each), and row e is
+// also TMEM lane e of every [V x *] accumulator.  Per
 // chunk of 64 tokens (G = chunk-local cumsum of g, Gl = G at the last valid
 // row), with single-thread MMA issue and three MMA rounds:
 //
@@ -20,8 +20,11 @@
 // o_t = scale S_t q_t, with A = (I + strictly-lower(diag(beta) (K K^T o Gamma)))^-1 from wy_fwd.
 #include <cuda_runtime.h>
 
+#include <cuda.h>
+
 #include "common.cuh"
 #include "launch.h"
+#include "tmap.h"
 #include "umma.cuh"
 
 namespace gdr {
@@ -32,14 +35,18 @@ namespace {
 constexpr uint32_t ST_QK = 0, ST_V = 32768, ST_A = 49152, ST_G = 57344, ST_B = 57600, ST_BYTES = 58368;
 constexpr uint32_t P_AKG = 2 * ST_BYTES, P_AB = P_AKG + 8192, P_S = P_AB + 8192, P_W = P_S + 32768,
                    P_P = P_W + 16384, P_D = P_P + 8192, P_DT = P_D + 16384, P_FAC = P_DT + 16384, P_BAR = P_FAC + 512,
-                   P_SLOT = P_BAR + 8, P_FLAG = P_SLOT + 4, SMEM_USED = P_FLAG + 4;
-constexpr int NT = 256;  // threads per CTA: two per TMEM lane
+                   P_SLOT = P_BAR + 8, P_FLAG = P_SLOT + 4, P_SBAR = P_FLAG + 4, SMEM_USED = P_SBAR + 16;
+constexpr int NT = 512;       // threads per CTA: four per TMEM lane
+constexpr int QN = NT / 128;  // threads sharing a TMEM lane (state row)
+constexpr int SW = DK / QN;   // state columns per thread
+constexpr int EW = C / QN;    // columns per thread of a 64-wide accumulator
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the base
 
 // ---- TMEM columns
 constexpr uint32_t T_QK = 0, T_W = 64, T_U = 128, T_O1 = 192, T_O2 = 256, T_X = 320, T_COLS = 512;
 
 struct TcP {
+    CUtensorMap tq, tk, tv, ta;  // TMA maps of q, k ([tokens][Hq][128]), v ([tokens][Hv][128]), A ([tokens][Hv][64])
     const void *q, *k, *v, *A, *beta;
     const float *g_cs, *h0;
     void *o, *h;
@@ -157,8 +164,8 @@ __device__ __forceinline__ void chain_fwd_body(const Geo &geo, const TcP &p, con
     const uint32_t sb = smem_u32(smem);
     const int Hv = geo.Hv, Hq = geo.Hq, hq = j / (Hv / Hq);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // thread (e, hh): TMEM lane / state row e, column half hh
-    const int e = tid & 127, hh = tid >> 7, lb = (warp & 3) * 32;
+    // thread (e, qq): TMEM lane / state row e, column quarter qq
+    const int e = tid & 127, qq = tid >> 7, lb = (warp & 3) * 32;
     constexpr bool bf16 = IsBf16<T>::value;
     long long tok0;
     int len, row0;
@@ -169,10 +176,6 @@ __device__ __forceinline__ void chain_fwd_body(const Geo &geo, const TcP &p, con
     const int kind = AFFINE ? bx & 1 : 0;  // 1: identity start, zero values
     const int sl = (nc_all + p.nseg - 1) / p.nseg;
     const int cb = min(nc_all, seg * sl), ce = min(nc_all, cb + sl);
-    const T *q = static_cast<const T *>(p.q);
-    const T *k = static_cast<const T *>(p.k);
-    const T *v = static_cast<const T *>(p.v);
-    const T *A = static_cast<const T *>(p.A);
     const long long st_base = ((long long)n * Hv + j) * DK * DV;
     const long long seg_base = (((long long)n * Hv + j) * p.nseg + seg) * DK * DV;
     const uint32_t bar = sb + P_BAR;
@@ -180,8 +183,11 @@ __device__ __forceinline__ void chain_fwd_body(const Geo &geo, const TcP &p, con
     float *fEG = reinterpret_cast<float *>(smem + P_FAC);  // e^{G_s}
     float *fEL = fEG + C;                                   // e^{Gl - G_s}
 
+    const bool use_v = !(AFFINE && kind == 1);  // the identity-start affine pass has zero values
     if (tid == 0) {
         umma::mbar_init(bar, 1);
+        umma::mbar_init(sb + P_SBAR, 1);
+        umma::mbar_init(sb + P_SBAR + 8, 1);
         umma::fence_mbar_init();
         *sflag = 0;
     }
@@ -191,11 +197,11 @@ __device__ __forceinline__ void chain_fwd_body(const Geo &geo, const TcP &p, con
     umma::fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + P_SLOT);
 
-    // fp32 state: S[e][64*hh + i] = h[64*hh + i][e]
-    float S[64];
+    // fp32 state: S[e][SW*qq + i] = h[SW*qq + i][e]
+    float S[SW];
 #pragma unroll
-    for (int i = 0; i < 64; ++i) {
-        const int d = hh * 64 + i;
+    for (int i = 0; i < SW; ++i) {
+        const int d = qq * SW + i;
         if (AFFINE)
             S[i] = (kind == 1 && d == e) ? 1.f : 0.f;
         else if (p.seg_start)
@@ -205,20 +211,37 @@ __device__ __forceinline__ void chain_fwd_body(const Geo &geo, const TcP &p, con
     }
     auto write_S_tile = [&]() {
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) store16<T>(sb + P_S + hh * 16384, e, c, S + c);
+        for (int c = 0; c < SW; c += 16) {
+            const int col = qq * SW + c;
+            store16<T>(sb + P_S + (col >> 6) * 16384, e, col & 63, S + c);
+        }
     };
     write_S_tile();
 
     float breg = 0.f;
+    uint32_t sphase[2] = {0u, 0u};
+    unsigned pend = 0;  // stages with a tile load in flight
     auto prefetch = [&](int i) {
-        const uint32_t st = sb + (i & 1) * ST_BYTES;
+        const uint32_t st = sb + (i & 1) * ST_BYTES, sbar = sb + P_SBAR + (i & 1) * 8;
+        pend |= 1u << (i & 1);
         const long long tb = tok0 + (long long)i * C;
         const int valid = min(C, len - i * C);
-        if (WRITE_O) load_tile128<T>(st + ST_QK, 16384, q + (tb * Hq + hq) * DK, (long long)Hq * DK, valid, tid);
-        load_tile128<T>(st + ST_QK + 8192, 16384, k + (tb * Hq + hq) * DK, (long long)Hq * DK, valid, tid);
-        // the identity-start affine pass runs with zero values (U = 0)
-        load_tile128<T>(st + ST_V, 8192, v + (tb * Hv + j) * DV, (long long)Hv * DV, kind == 1 ? 0 : valid, tid);
-        load_tile64<T>(st + ST_A, A + (tb * Hv + j) * C, (long long)Hv * C, valid, tid);
+        if (tid == 0) {
+            // tiles of 64 rows x 128 bytes land in the 128-byte-swizzled layout the MMAs read
+            tma::expect_tx(sbar, (WRITE_O ? 16384u : 0u) + 16384u + (use_v ? 16384u : 0u) + 8192u);
+            const int t = (int)tb;
+            if (WRITE_O) {
+                tma::load3d(st + ST_QK, &p.tq, 0, hq, t, sbar);
+                tma::load3d(st + ST_QK + 16384, &p.tq, 64, hq, t, sbar);
+            }
+            tma::load3d(st + ST_QK + 8192, &p.tk, 0, hq, t, sbar);
+            tma::load3d(st + ST_QK + 24576, &p.tk, 64, hq, t, sbar);
+            if (use_v) {
+                tma::load3d(st + ST_V, &p.tv, 0, j, t, sbar);
+                tma::load3d(st + ST_V + 8192, &p.tv, 64, j, t, sbar);
+            }
+            tma::load3d(st + ST_A, &p.ta, 0, j, t, sbar);
+        }
         if (tid < C) {
             const bool ok = tid < valid;
             cp_async4(st + ST_G + tid * 4, p.g_cs + (ok ? (tb + tid) * Hv + j : 0), ok);
@@ -257,7 +280,14 @@ __device__ __forceinline__ void chain_fwd_body(const Geo &geo, const TcP &p, con
         float *sB = reinterpret_cast<float *>(smem + (i & 1) * ST_BYTES + ST_B);
         cp_async_wait<0>();
         if (tid < C) sB[tid] = breg;
+        if (!umma::mbar_wait(sb + P_SBAR + (i & 1) * 8, sphase[i & 1])) {
+            raise_error(geo.err, GDR_ERR_TIMEOUT);
+            *sflag = 1;
+        }
+        sphase[i & 1] ^= 1u;
+        pend &= ~(1u << (i & 1));
         __syncthreads();
+        if (*sflag) break;
         const int valid = min(C, len - i * C);
         const float Gl = sG[valid - 1];
         if (p.l2norm) {
@@ -270,10 +300,11 @@ __device__ __forceinline__ void chain_fwd_body(const Geo &geo, const TcP &p, con
         }
         // scaled copies of A: columns s times beta_s e^{G_s} (for W) and beta_s (for U)
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < (C * 8) / NT; ++u) {
             const int ci = tid + u * NT, r = ci >> 3, c = ci & 7;
             const uint32_t o = umma::off(r, c * 8, 0);
-            const uint4 a = umma::ld_shared_v4(st + ST_A + o);
+            uint4 a = umma::ld_shared_v4(st + ST_A + o);
+            if (r >= valid) a = make_uint4(0u, 0u, 0u, 0u);
             const uint32_t w[4] = {a.x, a.y, a.z, a.w};
             uint32_t wk[4], wb[4];
 #pragma unroll
@@ -292,9 +323,9 @@ __device__ __forceinline__ void chain_fwd_body(const Geo &geo, const TcP &p, con
             T *h = static_cast<T *>(p.h);
             const long long hb = ((long long)(row0 + i) * Hv + j) * DK * DV;
             if (p.h_api && p.v_first) {
-                T *hr = h + hb + (long long)e * DK + hh * 64;
+                T *hr = h + hb + (long long)e * DK + qq * SW;
 #pragma unroll
-                for (int d = 0; d < 64; d += 8) {
+                for (int d = 0; d < SW; d += 8) {
                     uint4 w;
                     w.x = Elt<T>::pack(S[d], S[d + 1]);
                     w.y = Elt<T>::pack(S[d + 2], S[d + 3]);
@@ -303,9 +334,9 @@ __device__ __forceinline__ void chain_fwd_body(const Geo &geo, const TcP &p, con
                     *reinterpret_cast<uint4 *>(hr + d) = w;
                 }
             } else {
-                T *hc = h + hb + (long long)(hh * 64) * DV + e;
+                T *hc = h + hb + (long long)(qq * SW) * DV + e;
 #pragma unroll
-                for (int d = 0; d < 64; ++d) hc[d * DV] = Elt<T>::from_f(S[d]);
+                for (int d = 0; d < SW; ++d) hc[d * DV] = Elt<T>::from_f(S[d]);
             }
         }
         sync_tc();
@@ -326,35 +357,35 @@ __device__ __forceinline__ void chain_fwd_body(const Geo &geo, const TcP &p, con
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 umma::mma(tmem + T_W, dKmn + ks * 128, dAKG + ks * 2, id_n64_amn, ks > 0);
-                umma::mma(tmem + T_U, dVmn + ks * 128, dAB + ks * 2, id_n64_amn, ks > 0);
+                if (use_v) umma::mma(tmem + T_U, dVmn + ks * 128, dAB + ks * 2, id_n64_amn, ks > 0);
             }
             umma::commit(bar);
         }
         if (!wait_mma()) break;
 #pragma unroll
-        for (int c = 0; c < 32; c += 16) {
-            // -W row d = e, token columns 32*hh + c .. : MN-major operand rows (key index d)
+        for (int c = 0; c < EW; c += 16) {
+            // -W row d = e, token columns EW*qq + c .. : MN-major operand rows (key index d)
             float x[16];
-            umma::ld16(umma::taddr(tmem, lb, T_W + hh * 32 + c), x);
+            umma::ld16(umma::taddr(tmem, lb, T_W + qq * EW + c), x);
             umma::ld_wait();
 #pragma unroll
             for (int u = 0; u < 16; ++u) x[u] = -x[u];
-            store16<T>(sb + P_W, e, hh * 32 + c, x);
+            store16<T>(sb + P_W, e, qq * EW + c, x);
         }
         if (WRITE_O && e < C) {
             const int r = e;
             const float gr = sG[r];
 #pragma unroll
-            for (int c = 0; c < 32; c += 16) {
+            for (int c = 0; c < EW; c += 16) {
                 float x[16];
-                umma::ld16(umma::taddr(tmem, lb, T_QK + hh * 32 + c), x);
+                umma::ld16(umma::taddr(tmem, lb, T_QK + qq * EW + c), x);
                 umma::ld_wait();
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
-                    const int s = hh * 32 + c + u;
+                    const int s = qq * EW + c + u;
                     x[u] = (s <= r && r < valid) ? x[u] * __expf(gr - sG[s]) : 0.f;
                 }
-                store16<T>(sb + P_P, r, hh * 32 + c, x);
+                store16<T>(sb + P_P, r, qq * EW + c, x);
             }
         }
         sync_tc();
@@ -364,24 +395,24 @@ __device__ __forceinline__ void chain_fwd_body(const Geo &geo, const TcP &p, con
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t so = ((ks >> 2) * 16384 + (ks & 3) * 32) >> 4;
-                umma::mma(tmem + T_U, dS + so, dW + ks * 128, id_n64_bmn, true);
+                umma::mma(tmem + T_U, dS + so, dW + ks * 128, id_n64_bmn, use_v || ks > 0);
                 if (WRITE_O) umma::mma(tmem + T_O1, dS + so, dQa + so, id_n64, ks > 0);
             }
             umma::commit(bar);
         }
         if (!wait_mma()) break;
 #pragma unroll
-        for (int c = 0; c < 32; c += 16) {
+        for (int c = 0; c < EW; c += 16) {
             float x[16], y[16];
-            umma::ld16(umma::taddr(tmem, lb, T_U + hh * 32 + c), x);
+            umma::ld16(umma::taddr(tmem, lb, T_U + qq * EW + c), x);
             umma::ld_wait();
 #pragma unroll
-            for (int u = 0; u < 16; ++u) y[u] = x[u] * fEL[hh * 32 + c + u];
-            store16<T>(sb + P_D, e, hh * 32 + c, x);
-            store16<T>(sb + P_DT, e, hh * 32 + c, y);
+            for (int u = 0; u < 16; ++u) y[u] = x[u] * fEL[qq * EW + c + u];
+            store16<T>(sb + P_D, e, qq * EW + c, x);
+            store16<T>(sb + P_DT, e, qq * EW + c, y);
             if (!AFFINE && p.delta) {
                 T *dr = static_cast<T *>(p.delta) + ((long long)(row0 + i) * Hv + j) * C * DV +
-                        (long long)(hh * 32 + c) * DV + e;
+                        (long long)(qq * EW + c) * DV + e;
 #pragma unroll
                 for (int u = 0; u < 16; ++u) dr[u * DV] = Elt<T>::from_f(x[u]);
             }
@@ -401,25 +432,25 @@ __device__ __forceinline__ void chain_fwd_body(const Geo &geo, const TcP &p, con
         {
             const float eg = __expf(Gl);
 #pragma unroll
-            for (int c = 0; c < 64; c += 16) {
+            for (int c = 0; c < SW; c += 16) {
                 float x[16];
-                umma::ld16(umma::taddr(tmem, lb, T_X + hh * 64 + c), x);
+                umma::ld16(umma::taddr(tmem, lb, T_X + qq * SW + c), x);
                 umma::ld_wait();
 #pragma unroll
                 for (int u = 0; u < 16; ++u) S[c + u] = eg * S[c + u] + x[u];
             }
             if (WRITE_O) {
-                T *o = static_cast<T *>(p.o) + ((tok0 + (long long)i * C + hh * 32) * Hv + j) * DV + e;
+                T *o = static_cast<T *>(p.o) + ((tok0 + (long long)i * C + qq * EW) * Hv + j) * DV + e;
                 const long long ostride = (long long)Hv * DV;
 #pragma unroll
-                for (int c = 0; c < 32; c += 16) {
+                for (int c = 0; c < EW; c += 16) {
                     float x1[16], x2[16];
-                    umma::ld16(umma::taddr(tmem, lb, T_O1 + hh * 32 + c), x1);
-                    umma::ld16(umma::taddr(tmem, lb, T_O2 + hh * 32 + c), x2);
+                    umma::ld16(umma::taddr(tmem, lb, T_O1 + qq * EW + c), x1);
+                    umma::ld16(umma::taddr(tmem, lb, T_O2 + qq * EW + c), x2);
                     umma::ld_wait();
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
-                        const int r = hh * 32 + c + u;
+                        const int r = qq * EW + c + u;
                         if (r < valid) o[(c + u) * ostride] = Elt<T>::from_f(p.scale * (fEG[r] * x1[u] + x2[u]));
                     }
                 }
@@ -431,17 +462,20 @@ __device__ __forceinline__ void chain_fwd_body(const Geo &geo, const TcP &p, con
 
     if (*sflag == 0) {
         if (AFFINE) {
-            float *dst = (kind ? p.seg_end1 : p.seg_end0) + seg_base + (long long)e * DK + hh * 64;
+            float *dst = (kind ? p.seg_end1 : p.seg_end0) + seg_base + (long long)e * DK + qq * SW;
 #pragma unroll
-            for (int i = 0; i < 64; i += 4) *reinterpret_cast<float4 *>(dst + i) = make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
+            for (int i = 0; i < SW; i += 4) *reinterpret_cast<float4 *>(dst + i) = make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
         } else if (p.fin && seg == p.nseg - 1) {
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                const int d = hh * 64 + i;
+            for (int i = 0; i < SW; ++i) {
+                const int d = qq * SW + i;
                 p.fin[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] = S[i];
             }
         }
     }
+    // after an error, let tile loads still in flight land before the block exits (bounded)
+    for (int st2 = 0; st2 < 2; ++st2)
+        if (pend & (1u << st2)) umma::mbar_wait(sb + P_SBAR + st2 * 8, sphase[st2], 4000000L);
     umma::fence_before();
     __syncthreads();
     if (warp == 0) umma::dealloc(tmem, T_COLS);
@@ -449,9 +483,9 @@ __device__ __forceinline__ void chain_fwd_body(const Geo &geo, const TcP &p, con
 
 // ============================================================================ reverse chain
 //
-// One CTA of 256 threads per (sequence, value head); chunks in reverse order;
+// One CTA of 512 threads per (sequence, value head); chunks in reverse order;
 // dS = dH^T [V x K] (gradient w.r.t. the transposed state) in fp32 registers,
-// thread (e, hh) holding row e, key half hh.  With dS' the gradient arriving at
+// thread (e, qq) holding row e, key quarter qq.  With dS' the gradient arriving at
 // the end of the chunk, K~ = diag(e^{Gl-G}) K and P = (Q K^T) o Gamma o M:
 //
 //   round 1:  [K;Q] Q^T -> P^T rows (scaled, upper part)                  (M=128,N=64,K=128)
@@ -465,6 +499,7 @@ __device__ __forceinline__ void chain_fwd_body(const Geo &geo, const TcP &p, con
 // for the per-chunk gradient kernel; the last dS is dh0.
 
 struct TcBwdP {
+    CUtensorMap tq, tk, tdo, ta;  // TMA maps of q, k, dO, A
     const void *q, *k, *A, *beta, *dout;
     const float *g_cs, *dht;
     void *dhn;
@@ -484,7 +519,7 @@ struct TcBwdP {
 // [K b][Q b] order in the 32 KB block and dO in place of V)
 constexpr uint32_t B_AKG = 2 * ST_BYTES, B_DS = B_AKG + 8192, B_WT = B_DS + 32768, B_PT = B_WT + 16384,
                    B_DOG = B_PT + 8192, B_DDT = B_DOG + 16384, B_FAC = B_DDT + 16384, B_BAR = B_FAC + 512,
-                   B_SLOT = B_BAR + 8, B_FLAG = B_SLOT + 4, B_USED = B_FLAG + 4;
+                   B_SLOT = B_BAR + 8, B_FLAG = B_SLOT + 4, B_SBAR = B_FLAG + 4, B_USED = B_SBAR + 16;
 constexpr uint32_t B_SMEM_BYTES = B_USED + 1024;
 constexpr uint32_t TB_KQ = 0, TB_W = 64, TB_E1 = 128, TB_E2 = 192, TB_X = 256, TB_COLS = 512;
 
@@ -495,7 +530,7 @@ __device__ __forceinline__ void chain_bwd_body(const Geo &geo, const TcBwdP &p, 
     const uint32_t sb = smem_u32(smem);
     const int Hv = geo.Hv, Hq = geo.Hq, hq = j / (Hv / Hq);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int e = tid & 127, hh = tid >> 7, lb = (warp & 3) * 32;
+    const int e = tid & 127, qq = tid >> 7, lb = (warp & 3) * 32;
     constexpr bool bf16 = IsBf16<T>::value;
     long long tok0;
     int len, row0;
@@ -505,10 +540,6 @@ __device__ __forceinline__ void chain_bwd_body(const Geo &geo, const TcBwdP &p, 
     const int kind = AFFINE ? bx & 1 : 0;
     const int sl = (nc_all + p.nseg - 1) / p.nseg;
     const int cb = min(nc_all, seg * sl), ce = min(nc_all, cb + sl);
-    const T *q = static_cast<const T *>(p.q);
-    const T *k = static_cast<const T *>(p.k);
-    const T *A = static_cast<const T *>(p.A);
-    const T *dout = static_cast<const T *>(p.dout);
     const long long st_base = ((long long)n * Hv + j) * DK * DV;
     const long long seg_base = (((long long)n * Hv + j) * p.nseg + seg) * DK * DV;
     const uint32_t bar = sb + B_BAR;
@@ -516,8 +547,11 @@ __device__ __forceinline__ void chain_bwd_body(const Geo &geo, const TcBwdP &p, 
     float *fEG = reinterpret_cast<float *>(smem + B_FAC);
     float *fEL = fEG + C;
 
+    const bool use_do = !(AFFINE && kind == 1);  // the identity-start affine pass has dO = 0
     if (tid == 0) {
         umma::mbar_init(bar, 1);
+        umma::mbar_init(sb + B_SBAR, 1);
+        umma::mbar_init(sb + B_SBAR + 8, 1);
         umma::fence_mbar_init();
         *sflag = 0;
     }
@@ -527,10 +561,10 @@ __device__ __forceinline__ void chain_bwd_body(const Geo &geo, const TcBwdP &p, 
     umma::fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + B_SLOT);
 
-    float S[64];  // dS[e][64*hh + i] = dH[64*hh + i][e]
+    float S[SW];  // dS[e][SW*qq + i] = dH[SW*qq + i][e]
 #pragma unroll
-    for (int i = 0; i < 64; ++i) {
-        const int d = hh * 64 + i;
+    for (int i = 0; i < SW; ++i) {
+        const int d = qq * SW + i;
         if (AFFINE)
             S[i] = (kind == 1 && d == e) ? 1.f : 0.f;
         else if (p.seg_start)
@@ -540,19 +574,34 @@ __device__ __forceinline__ void chain_bwd_body(const Geo &geo, const TcBwdP &p, 
     }
     auto write_S_tile = [&]() {
 #pragma unroll
-        for (int c = 0; c < 64; c += 16) store16<T>(sb + B_DS + hh * 16384, e, c, S + c);
+        for (int c = 0; c < SW; c += 16) {
+            const int col = qq * SW + c;
+            store16<T>(sb + B_DS + (col >> 6) * 16384, e, col & 63, S + c);
+        }
     };
     write_S_tile();
 
     float breg = 0.f;
+    uint32_t sphase[2] = {0u, 0u};
+    unsigned pend = 0;  // stages with a tile load in flight
     auto prefetch = [&](int i) {
-        const uint32_t st = sb + (i & 1) * ST_BYTES;
+        const uint32_t st = sb + (i & 1) * ST_BYTES, sbar = sb + B_SBAR + (i & 1) * 8;
+        pend |= 1u << (i & 1);
         const long long tb = tok0 + (long long)i * C;
         const int valid = min(C, len - i * C);
-        load_tile128<T>(st + ST_QK, 16384, k + (tb * Hq + hq) * DK, (long long)Hq * DK, valid, tid);
-        load_tile128<T>(st + ST_QK + 8192, 16384, q + (tb * Hq + hq) * DK, (long long)Hq * DK, valid, tid);
-        load_tile128<T>(st + ST_V, 8192, dout + (tb * Hv + j) * DV, (long long)Hv * DV, kind == 1 ? 0 : valid, tid);
-        load_tile64<T>(st + ST_A, A + (tb * Hv + j) * C, (long long)Hv * C, valid, tid);
+        if (tid == 0) {
+            tma::expect_tx(sbar, 16384u + 16384u + (use_do ? 16384u : 0u) + 8192u);
+            const int t = (int)tb;
+            tma::load3d(st + ST_QK, &p.tk, 0, hq, t, sbar);
+            tma::load3d(st + ST_QK + 16384, &p.tk, 64, hq, t, sbar);
+            tma::load3d(st + ST_QK + 8192, &p.tq, 0, hq, t, sbar);
+            tma::load3d(st + ST_QK + 24576, &p.tq, 64, hq, t, sbar);
+            if (use_do) {
+                tma::load3d(st + ST_V, &p.tdo, 0, j, t, sbar);
+                tma::load3d(st + ST_V + 8192, &p.tdo, 64, j, t, sbar);
+            }
+            tma::load3d(st + ST_A, &p.ta, 0, j, t, sbar);
+        }
         if (tid < C) {
             const bool ok = tid < valid;
             cp_async4(st + ST_G + tid * 4, p.g_cs + (ok ? (tb + tid) * Hv + j : 0), ok);
@@ -588,13 +637,20 @@ __device__ __forceinline__ void chain_bwd_body(const Geo &geo, const TcBwdP &p, 
         float *sB = reinterpret_cast<float *>(smem + (i & 1) * ST_BYTES + ST_B);
         cp_async_wait<0>();
         if (tid < C) sB[tid] = breg;
+        if (!umma::mbar_wait(sb + B_SBAR + (i & 1) * 8, sphase[i & 1])) {
+            raise_error(geo.err, GDR_ERR_TIMEOUT);
+            *sflag = 1;
+        }
+        sphase[i & 1] ^= 1u;
+        pend &= ~(1u << (i & 1));
         // gradient w.r.t. the state after this chunk, for the per-chunk kernel ([K][V] layout)
         if (!AFFINE) {
-            T *hc = static_cast<T *>(p.dhn) + ((long long)(row0 + i) * Hv + j) * DK * DV + (long long)(hh * 64) * DV + e;
+            T *hc = static_cast<T *>(p.dhn) + ((long long)(row0 + i) * Hv + j) * DK * DV + (long long)(qq * SW) * DV + e;
 #pragma unroll
-            for (int d = 0; d < 64; ++d) hc[d * DV] = Elt<T>::from_f(S[d]);
+            for (int d = 0; d < SW; ++d) hc[d * DV] = Elt<T>::from_f(S[d]);
         }
         __syncthreads();
+        if (*sflag) break;
         const int valid = min(C, len - i * C);
         const float Gl = sG[valid - 1];
         if (p.l2norm) {
@@ -606,10 +662,11 @@ __device__ __forceinline__ void chain_bwd_body(const Geo &geo, const TcBwdP &p, 
             fEL[tid] = __expf(Gl - sG[tid]);
         }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < (C * 8) / NT; ++u) {
             const int ci = tid + u * NT, r = ci >> 3, c = ci & 7;
             const uint32_t o = umma::off(r, c * 8, 0);
-            const uint4 a = umma::ld_shared_v4(st + ST_A + o);
+            uint4 a = umma::ld_shared_v4(st + ST_A + o);
+            if (r >= valid) a = make_uint4(0u, 0u, 0u, 0u);
             const uint32_t w[4] = {a.x, a.y, a.z, a.w};
             uint32_t wk[4];
 #pragma unroll
@@ -622,11 +679,11 @@ __device__ __forceinline__ void chain_bwd_body(const Geo &geo, const TcBwdP &p, 
         }
         // scale e^{G_s} dO rows -> dOg (same two-block layout)
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < (C * 16) / NT; ++u) {
             const int ci = tid + u * NT, r = ci >> 4, c = ci & 15;
             const uint32_t o = (uint32_t)(c >> 3) * 8192 + umma::off(r, (c & 7) * 8, 0);
             const uint4 a = umma::ld_shared_v4(st + ST_V + o);
-            const float f = p.scale * __expf(sG[r]);
+            const float f = (r < valid && use_do) ? p.scale * __expf(sG[r]) : 0.f;
             const uint32_t w[4] = {a.x, a.y, a.z, a.w};
             uint32_t wo[4];
 #pragma unroll
@@ -656,26 +713,26 @@ __device__ __forceinline__ void chain_bwd_body(const Geo &geo, const TcBwdP &p, 
         }
         if (!wait_mma()) break;
 #pragma unroll
-        for (int c = 0; c < 32; c += 16) {
+        for (int c = 0; c < EW; c += 16) {
             float x[16];
-            umma::ld16(umma::taddr(tmem, lb, TB_W + hh * 32 + c), x);
+            umma::ld16(umma::taddr(tmem, lb, TB_W + qq * EW + c), x);
             umma::ld_wait();
-            store16<T>(sb + B_WT, e, hh * 32 + c, x);
+            store16<T>(sb + B_WT, e, qq * EW + c, x);
         }
         if (e < C) {
             const int r = e;
             const float gr = sG[r];
 #pragma unroll
-            for (int c = 0; c < 32; c += 16) {
+            for (int c = 0; c < EW; c += 16) {
                 float x[16];
-                umma::ld16(umma::taddr(tmem, lb, TB_KQ + hh * 32 + c), x);
+                umma::ld16(umma::taddr(tmem, lb, TB_KQ + qq * EW + c), x);
                 umma::ld_wait();
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
-                    const int s2 = hh * 32 + c + u;
+                    const int s2 = qq * EW + c + u;
                     x[u] = (s2 >= r && s2 < valid) ? x[u] * p.scale * __expf(sG[s2] - gr) : 0.f;
                 }
-                store16<T>(sb + B_PT, r, hh * 32 + c, x);
+                store16<T>(sb + B_PT, r, qq * EW + c, x);
             }
         }
         sync_tc();
@@ -683,24 +740,29 @@ __device__ __forceinline__ void chain_bwd_body(const Geo &geo, const TcBwdP &p, 
         // ---- round 2: E2 = dO^T P
         if (tid == 0) {
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + TB_E2, dOmn + ks * 128, dPT + ks * 2, id_n64_amn, ks > 0);
+            for (int ks = 0; ks < 4; ++ks)
+                if (use_do) umma::mma(tmem + TB_E2, dOmn + ks * 128, dPT + ks * 2, id_n64_amn, ks > 0);
             umma::commit(bar);
         }
         if (!wait_mma()) break;
 #pragma unroll
-        for (int c = 0; c < 32; c += 16) {
+        for (int c = 0; c < EW; c += 16) {
             float x1[16], x2[16];
-            umma::ld16(umma::taddr(tmem, lb, TB_E1 + hh * 32 + c), x1);
-            umma::ld16(umma::taddr(tmem, lb, TB_E2 + hh * 32 + c), x2);
+            umma::ld16(umma::taddr(tmem, lb, TB_E1 + qq * EW + c), x1);
+            umma::ld16(umma::taddr(tmem, lb, TB_E2 + qq * EW + c), x2);
             umma::ld_wait();
+            if (!use_do) {
 #pragma unroll
-            for (int u = 0; u < 16; ++u) x1[u] = -(x1[u] * fEL[hh * 32 + c + u] + x2[u]);
-            store16<T>(sb + B_DDT, e, hh * 32 + c, x1);
+                for (int u = 0; u < 16; ++u) x2[u] = 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) x1[u] = -(x1[u] * fEL[qq * EW + c + u] + x2[u]);
+            store16<T>(sb + B_DDT, e, qq * EW + c, x1);
             if (!AFFINE) {
                 T *dr = static_cast<T *>(p.ddelta) + ((long long)(row0 + i) * Hv + j) * C * DV +
-                        (long long)(hh * 32 + c) * DV + e;
+                        (long long)(qq * EW + c) * DV + e;
 #pragma unroll
-                for (int u = 0; u < 16; ++u) dr[u * DV] = Elt<T>::from_f(-x1[u]);
+                for (int u = 0; u < 16; ++u) dr[u * DV] = Elt<T>::from_f(qq * EW + c + u < valid ? -x1[u] : 0.f);
             }
         }
         sync_tc();
@@ -708,18 +770,19 @@ __device__ __forceinline__ void chain_bwd_body(const Geo &geo, const TcBwdP &p, 
         // ---- round 3: X = dOg^T Q - dDelta^T W
         if (tid == 0) {
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + TB_X, dOG + ks * 128, dQmn + ks * 128, id_n128_ab_mn, ks > 0);
+            for (int ks = 0; ks < 4; ++ks)
+                if (use_do) umma::mma(tmem + TB_X, dOG + ks * 128, dQmn + ks * 128, id_n128_ab_mn, ks > 0);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + TB_X, dDDT + ks * 2, dWT + ks * 2, id_n128, true);
+            for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + TB_X, dDDT + ks * 2, dWT + ks * 2, id_n128, use_do || ks > 0);
             umma::commit(bar);
         }
         if (!wait_mma()) break;
         {
             const float eg = __expf(Gl);
 #pragma unroll
-            for (int c = 0; c < 64; c += 16) {
+            for (int c = 0; c < SW; c += 16) {
                 float x[16];
-                umma::ld16(umma::taddr(tmem, lb, TB_X + hh * 64 + c), x);
+                umma::ld16(umma::taddr(tmem, lb, TB_X + qq * SW + c), x);
                 umma::ld_wait();
 #pragma unroll
                 for (int u = 0; u < 16; ++u) S[c + u] = eg * S[c + u] + x[u];
@@ -731,36 +794,39 @@ __device__ __forceinline__ void chain_bwd_body(const Geo &geo, const TcBwdP &p, 
 
     if (*sflag == 0) {
         if (AFFINE) {
-            float *dst = (kind ? p.seg_end1 : p.seg_end0) + seg_base + (long long)e * DK + hh * 64;
+            float *dst = (kind ? p.seg_end1 : p.seg_end0) + seg_base + (long long)e * DK + qq * SW;
 #pragma unroll
-            for (int i = 0; i < 64; i += 4) *reinterpret_cast<float4 *>(dst + i) = make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
+            for (int i = 0; i < SW; i += 4) *reinterpret_cast<float4 *>(dst + i) = make_float4(S[i], S[i + 1], S[i + 2], S[i + 3]);
         } else if (p.dh0 && seg == 0) {
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                const int d = hh * 64 + i;
+            for (int i = 0; i < SW; ++i) {
+                const int d = qq * SW + i;
                 p.dh0[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] = S[i];
             }
         }
     }
+    for (int st2 = 0; st2 < 2; ++st2)
+        if (pend & (1u << st2)) umma::mbar_wait(sb + B_SBAR + st2 * 8, sphase[st2], 4000000L);
     umma::fence_before();
     __syncthreads();
     if (warp == 0) umma::dealloc(tmem, TB_COLS);
 }
 
 template <typename T, bool WRITE_O, bool AFFINE>
-__global__ void __launch_bounds__(NT, 1) chain_fwd_tc_kernel(Geo geo, TcP p) {
+__global__ void __launch_bounds__(NT, 1) chain_fwd_tc_kernel(Geo geo, const __grid_constant__ TcP p) {
     chain_fwd_body<T, WRITE_O, AFFINE>(geo, p, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
 template <typename T, bool AFFINE>
-__global__ void __launch_bounds__(NT, 1) chain_bwd_tc_kernel(Geo geo, TcBwdP p) {
+__global__ void __launch_bounds__(NT, 1) chain_bwd_tc_kernel(Geo geo, const __grid_constant__ TcBwdP p) {
     chain_bwd_body<T, AFFINE>(geo, p, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
 // The backward's two chains are independent: blocks z < N recompute the forward states,
 // blocks z >= N run the reverse state-gradient chain, side by side on the GPU.
 template <typename T>
-__global__ void __launch_bounds__(NT, 1) chain_pair_kernel(Geo geo, TcP pf, TcBwdP pb) {
+__global__ void __launch_bounds__(NT, 1) chain_pair_kernel(Geo geo, const __grid_constant__ TcP pf,
+                                                           const __grid_constant__ TcBwdP pb) {
     if ((int)blockIdx.z < geo.N)
         chain_fwd_body<T, false, false>(geo, pf, blockIdx.x, blockIdx.y, blockIdx.z);
     else
@@ -840,9 +906,20 @@ __global__ void __launch_bounds__(256) seg_scan_kernel(int Hv, int nseg, bool re
 
 namespace {
 
+// [tokens][heads][cols] map with 64 x 1 x 64 boxes
+bool tile_map(CUtensorMap *m, const void *base, const Args &a, int heads, int cols) {
+    const uint64_t tokens = (uint64_t)a.B * (uint64_t)a.T;
+    return make_tmap_3d(m, base, a.bf16, (uint64_t)cols, (uint64_t)heads, tokens, (uint64_t)cols * 2,
+                        (uint64_t)heads * cols * 2, 64, 1, 64);
+}
+
 TcBwdP bwd_params(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta, const void *A,
                   const void *dout, const float *dht, void *dhn, void *ddelta, float *dh0, const SegWs &sw) {
     TcBwdP p;
+    p.nseg = -1;  // marks a failed tensor-map encoding
+    if (!tile_map(&p.tq, q, a, a.Hq, DK) || !tile_map(&p.tk, k, a, a.Hq, DK) || !tile_map(&p.tdo, dout, a, a.Hv, DV) ||
+        !tile_map(&p.ta, A, a, a.Hv, C))
+        return p;
     p.q = q;
     p.k = k;
     p.A = A;
@@ -868,6 +945,10 @@ TcP fwd_params(const Args &a, const void *q, const void *k, const void *v, const
                const void *A, const float *h0, void *o, float *final_state, void *h, bool h_api_layout, void *delta,
                const SegWs &sw) {
     TcP p;
+    p.nseg = -1;  // marks a failed tensor-map encoding
+    if (!tile_map(&p.tq, q, a, a.Hq, DK) || !tile_map(&p.tk, k, a, a.Hq, DK) || !tile_map(&p.tv, v, a, a.Hv, DV) ||
+        !tile_map(&p.ta, A, a, a.Hv, C))
+        return p;
     p.q = q;
     p.k = k;
     p.v = v;
@@ -907,6 +988,7 @@ cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const 
                              const void *A, const void *dout, const float *dht, void *dhn, void *ddelta, float *dh0,
                              const SegWs &sw, cudaStream_t s) {
     TcBwdP p = bwd_params(a, q, k, g_cs, beta, A, dout, dht, dhn, ddelta, dh0, sw);
+    if (p.nseg < 1) return cudaErrorInvalidValue;
     cudaError_t e;
     if (sw.nseg > 1) {
         e = a.bf16 ? chain_bwd_tc_t<__nv_bfloat16>(a, p, true, s) : chain_bwd_tc_t<__half>(a, p, true, s);
@@ -923,6 +1005,7 @@ cudaError_t launch_chain_fwd(const Args &a, const void *q, const void *k, const 
                              const void *beta, const void *A, const float *h0, void *o, float *final_state, void *h,
                              bool h_api_layout, void *delta, const SegWs &sw, cudaStream_t s) {
     TcP p = fwd_params(a, q, k, v, g_cs, beta, A, h0, o, final_state, h, h_api_layout, delta, sw);
+    if (p.nseg < 1) return cudaErrorInvalidValue;
     cudaError_t e;
     if (sw.nseg > 1) {
         e = a.bf16 ? chain_fwd_tc_t<__nv_bfloat16>(a, p, false, true, s) : chain_fwd_tc_t<__half>(a, p, false, true, s);
@@ -942,6 +1025,7 @@ cudaError_t launch_chain_pair(const Args &a, const void *q, const void *k, const
     SegWs none{1, nullptr, nullptr, nullptr};
     const TcP pf = fwd_params(a, q, k, v, g_cs, beta, A, h0, nullptr, nullptr, h, false, delta, none);
     const TcBwdP pb = bwd_params(a, q, k, g_cs, beta, A, dout, dht, dhn, ddelta, dh0, none);
+    if (pf.nseg < 1 || pb.nseg < 1) return cudaErrorInvalidValue;
     return a.bf16 ? chain_pair_t<__nv_bfloat16>(a, pf, pb, s) : chain_pair_t<__half>(a, pf, pb, s);
 }
 

@@ -1,0 +1,15 @@
+// Host-side creation of TMA tensor maps (driver entry point looked up through the runtime).
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+namespace gdr {
+
+// A rank-3 tiled map over a row-major [dim2][dim1][dim0] tensor of 16-bit elements (dim0 contiguous),
+// strides in bytes for dims 1 and 2, a box of box0 x box1 x box2 elements, 128-byte swizzle, zero fill
+// outside the tensor.  Returns false when the driver refuses the map.
+bool make_tmap_3d(CUtensorMap *map, const void *base, bool bf16, uint64_t dim0, uint64_t dim1, uint64_t dim2,
+                  uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1, uint32_t box2);
+
+}  // namespace gdr

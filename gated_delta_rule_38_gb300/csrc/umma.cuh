@@ -116,3 +116,24 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 
 }  // namespace umma
 }  // namespace gdr
+
+namespace gdr {
+namespace tma {
+
+// 3-D tiled bulk tensor load into shared memory; completion is counted in bytes on `mbar`.
+// `map` must live in kernel-parameter (grid-constant) memory.
+__device__ __forceinline__ void load3d(uint32_t dst, const void *map, int c0, int c1, int c2, uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::
+            "r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(mbar)
+        : "memory");
+}
+
+// One arrival that also announces `bytes` of transactions on the barrier's current phase.
+__device__ __forceinline__ void expect_tx(uint32_t mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mbar), "r"(bytes) : "memory");
+}
+
+}  // namespace tma
+}  // namespace gdr
