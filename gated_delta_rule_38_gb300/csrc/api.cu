@@ -388,6 +388,10 @@ gdr_status gdr_fwd(const gdr_problem *p, const void *q, const void *k, const voi
     void *Aw = A ? A : static_cast<void *>(ws + L.A);
     if ((st = timed(K_WY_FWD, s, [&] { return launch_wy_fwd(a, k, g, beta, gcs, Aw, s); })) != GDR_OK) return st;
     const SegWs sw = seg_ws(L, ws);
+    if (sw.nseg == 1)
+        return timed(K_CHAIN_FWD, s, [&] {
+            return launch_chain_ws(a, q, k, v, gcs, beta, Aw, h0, nullptr, o, final_state, h, a.v_first, nullptr, s);
+        });
     return timed(K_CHAIN_FWD, s, [&] {
         return launch_chain_fwd(a, q, k, v, gcs, beta, Aw, h0, o, final_state, h, true, nullptr, sw, s);
     });

@@ -42,6 +42,12 @@ cudaError_t launch_wy_fwd(const Args &a, const void *k, const void *g, const voi
 cudaError_t launch_chain_fwd(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
                              const void *beta, const void *A, const float *h0, void *o, float *final_state, void *h,
                              bool h_api_layout, void *delta, const SegWs &sw, cudaStream_t s);
+// Forward recurrence, warp-specialised (one CTA per value-column slice); no sequence split.
+// o != nullptr: output rows; h: state before every chunk ([rows,Hv,K,V], or [..,V,K] when
+// h_vfirst); delta: Delta of every chunk; seg_start: transposed fp32 start states replacing h0.
+cudaError_t launch_chain_ws(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
+                            const void *beta, const void *A, const float *h0, const float *seg_start, void *o,
+                            float *final_state, void *h, bool h_vfirst, void *delta, cudaStream_t s);
 // Backward: reverse state-gradient chain (dH' and dDelta of every chunk, dh0).
 cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
                              const void *A, const void *dout, const float *dht, void *dhn, void *ddelta, float *dh0,
