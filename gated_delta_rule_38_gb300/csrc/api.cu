@@ -173,7 +173,7 @@ int choose_nseg(const gdr_problem *p) {
 }
 
 struct Layout {
-    size_t idx = 0, off = 0, total = 0, gcs = 0, A = 0, h = 0, dhn = 0, delta = 0, ddelta = 0;
+    size_t idx = 0, off = 0, total = 0, gcs = 0, A = 0, P = 0, rq = 0, rk = 0, h = 0, dhn = 0, delta = 0, ddelta = 0;
     size_t seg[3] = {0, 0, 0};
     int nseg = 1;
     size_t bytes = 0;
@@ -193,11 +193,23 @@ Layout layout_of(const gdr_problem *p, bool bwd) {
         at = round_up(at + sizeof(int32_t), 256);
     }
     const size_t tok = (size_t)p->B * p->T;
+    L.nseg = choose_nseg(p);
     if (!bwd) {
         L.gcs = at;
         at = round_up(at + tok * p->Hv * sizeof(float), 256);
         L.A = at;
         at = round_up(at + tok * p->Hv * C * esize(p->dtype), 256);
+        if (L.nseg == 1) {
+            // the decayed causal attention block and the inverse q/k norms for the unsplit recurrence
+            L.P = at;
+            at = round_up(at + tok * p->Hv * C * esize(p->dtype), 256);
+            if (p->flags & GDR_L2NORM_QK) {
+                L.rq = at;
+                at = round_up(at + tok * p->Hv * sizeof(float), 256);
+                L.rk = at;
+                at = round_up(at + tok * p->Hv * sizeof(float), 256);
+            }
+        }
     } else {
         const size_t st = (size_t)mc * p->Hv * DK * DV * esize(p->dtype);
         L.h = at;
@@ -210,7 +222,6 @@ Layout layout_of(const gdr_problem *p, bool bwd) {
         L.ddelta = at;
         at = round_up(at + dsz, 256);
     }
-    L.nseg = choose_nseg(p);
     if (L.nseg > 1) {
         const size_t sz = (size_t)num_seqs(p) * p->Hv * L.nseg * DK * DV * sizeof(float);
         for (int i = 0; i < 3; ++i) {
@@ -386,11 +397,17 @@ gdr_status gdr_fwd(const gdr_problem *p, const void *q, const void *k, const voi
     if ((st = tables(p, a, ws, L, s)) != GDR_OK) return st;
     float *gcs = g_cumsum ? g_cumsum : reinterpret_cast<float *>(ws + L.gcs);
     void *Aw = A ? A : static_cast<void *>(ws + L.A);
-    if ((st = timed(K_WY_FWD, s, [&] { return launch_wy_fwd(a, k, g, beta, gcs, Aw, s); })) != GDR_OK) return st;
     const SegWs sw = seg_ws(L, ws);
+    void *Pw = sw.nseg == 1 ? static_cast<void *>(ws + L.P) : nullptr;
+    float *rqw = (sw.nseg == 1 && a.l2norm) ? reinterpret_cast<float *>(ws + L.rq) : nullptr;
+    float *rkw = (sw.nseg == 1 && a.l2norm) ? reinterpret_cast<float *>(ws + L.rk) : nullptr;
+    if ((st = timed(K_WY_FWD, s, [&] { return launch_wy_fwd(a, q, k, g, beta, gcs, Aw, Pw, rqw, rkw, s); })) !=
+        GDR_OK)
+        return st;
     if (sw.nseg == 1)
         return timed(K_CHAIN_FWD, s, [&] {
-            return launch_chain_ws(a, q, k, v, gcs, beta, Aw, h0, nullptr, o, final_state, h, a.v_first, nullptr, s);
+            return launch_chain_ws(a, q, k, v, gcs, beta, Aw, Pw, rqw, rkw, h0, nullptr, o, final_state, h, a.v_first,
+                                   nullptr, s);
         });
     return timed(K_CHAIN_FWD, s, [&] {
         return launch_chain_fwd(a, q, k, v, gcs, beta, Aw, h0, o, final_state, h, true, nullptr, sw, s);

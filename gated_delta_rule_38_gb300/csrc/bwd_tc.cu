@@ -55,7 +55,7 @@ constexpr uint32_t S_BYTES = S_USED + 1024;
 // scalar slots (64 floats each)
 enum {
     F_G = 0, F_B, F_EG, F_EL, F_QD0, F_QD1, F_VD0, F_VD1, F_KD0, F_KD1, F_LB0, F_LB1,
-    F_ER0, F_ER1, F_EC0, F_EC1, F_Z0, F_Z1, F_FR0, F_FR1, F_FC0, F_FC1, F_HD, F_DG, F_COUNT
+    F_ER0, F_ER1, F_EC0, F_EC1, F_Z0, F_Z1, F_FR0, F_FR1, F_FC0, F_FC1, F_HD, F_DG, F_IQ, F_IK, F_COUNT
 };
 // TMEM columns
 constexpr uint32_t T_R1 = 0, T_R2 = 128, T_R3 = 256, T_R4 = 384, T_R8 = 448, T_COLS = 512;
@@ -122,7 +122,7 @@ __device__ __forceinline__ void load16(uint32_t base, int row, int col0, float *
 
 // In-place L2 normalisation of 64 rows of a [64 x 128] swizzled tile (blocks 16 KB apart).
 template <typename T>
-__device__ __forceinline__ void l2norm64(uint32_t base, int rows, int warp, int lane) {
+__device__ __forceinline__ void l2norm64(uint32_t base, int rows, int warp, int lane, float *inv_out) {
     const int rq = lane >> 2, qq = lane & 3;
     const int r = warp * 8 + rq;  // 8 warps x 8 rows
     uint32_t addr[4];
@@ -146,6 +146,7 @@ __device__ __forceinline__ void l2norm64(uint32_t base, int rows, int warp, int 
     ss += __shfl_xor_sync(0xffffffffu, ss, 1);
     ss += __shfl_xor_sync(0xffffffffu, ss, 2);
     const float inv = 1.0f / sqrtf(ss + L2_EPS);
+    if (r < rows && qq == 0) inv_out[r] = inv;
     if (r < rows) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -160,36 +161,37 @@ __device__ __forceinline__ void l2norm64(uint32_t base, int rows, int warp, int 
     }
 }
 
-// dx = (dxh - xh (xh . dxh)) / n with n = sqrt(sum x^2 + eps), xh = x / n; one warp per row.
+// dx = (dxh - xh (xh . dxh)) / n with n = sqrt(sum x^2 + eps) and xh = x / n, from the normalised
+// tile in shared memory (two swizzled 64-column blocks 16 KB apart) and the inverse norms; one warp per
+// row, lane l owns columns 4l..4l+3.
 template <typename T>
-__device__ __forceinline__ void l2norm_bwd_rows(const float *src, const T *x, long long stride, T *dst, int valid,
-                                                bool l2norm, int warp, int nwarps, int lane) {
+__device__ __forceinline__ void l2norm_bwd_rows(const float *src, uint32_t xtile, const float *inv, T *dst,
+                                                long long stride, int valid, bool l2norm, int warp, int nwarps,
+                                                int lane) {
+    const int col = lane * 4;
     for (int r = warp; r < valid; r += nwarps) {
-        const T *xr = x + (long long)r * stride;
         T *dr = dst + (long long)r * stride;
-        float xv[4], gv[4];
+        float gv[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            xv[u] = Elt<T>::to_f(xr[lane * 4 + u]);
-            gv[u] = src[r * FLD + lane * 4 + u];
-        }
+        for (int u = 0; u < 4; ++u) gv[u] = src[r * FLD + col + u];
         if (l2norm) {
-            float ss = xv[0] * xv[0] + xv[1] * xv[1] + xv[2] * xv[2] + xv[3] * xv[3];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            const float inv = 1.0f / sqrtf(ss + L2_EPS);
-            float dot = 0.f;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) dot += xv[u] * inv * gv[u];
+            uint2 w;
+            asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];\n"
+                         : "=r"(w.x), "=r"(w.y)
+                         : "r"(xtile + (uint32_t)(col >> 6) * 16384u + umma::off(r, col & 63, 0)));
+            const float2 x0 = Elt<T>::unpack(w.x), x1 = Elt<T>::unpack(w.y);
+            const float xv[4] = {x0.x, x0.y, x1.x, x1.y};
+            float dot = xv[0] * gv[0] + xv[1] * gv[1] + xv[2] * gv[2] + xv[3] * gv[3];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+            const float iv = inv[r];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) gv[u] = (gv[u] - xv[u] * inv * dot) * inv;
+            for (int u = 0; u < 4; ++u) gv[u] = (gv[u] - xv[u] * dot) * iv;
         }
         uint2 w;
         w.x = Elt<T>::pack(gv[0], gv[1]);
         w.y = Elt<T>::pack(gv[2], gv[3]);
-        *reinterpret_cast<uint2 *>(dr + lane * 4) = w;
+        *reinterpret_cast<uint2 *>(dr + col) = w;
     }
 }
 
@@ -209,8 +211,6 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
     const bool upper = L >= 64;
     const int r = L & 63;  // token row of this thread's TMEM lane
     constexpr bool bf16 = IsBf16<T>::value;
-    const T *q = static_cast<const T *>(p.q);
-    const T *k = static_cast<const T *>(p.k);
     float *F = reinterpret_cast<float *>(smem + S_F);
     auto f = [&](int slot_, int i) -> float & { return F[slot_ * 64 + i]; };
     const uint32_t bar = sb + S_BAR;
@@ -327,8 +327,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             break;
         }
         if (jj == 0 && p.l2norm) {
-            l2norm64<T>(sb + S_Q0, valid, warp, lane);
-            l2norm64<T>(sb + S_K0, valid, warp, lane);
+            l2norm64<T>(sb + S_Q0, valid, warp, lane, &f(F_IQ, 0));
+            l2norm64<T>(sb + S_K0, valid, warp, lane, &f(F_IK, 0));
         }
         const float Gl = f(F_G, valid - 1);
         if (tid < C) {
@@ -686,9 +686,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
     __syncthreads();
     if (ok) {
         const long long rstride = (long long)Hq * DK;
-        l2norm_bwd_rows<T>(fq, q + (tok0 * Hq + hq) * DK, rstride, static_cast<T *>(p.dq) + (tok0 * Hq + hq) * DK,
+        l2norm_bwd_rows<T>(fq, sb + S_Q0, &f(F_IQ, 0), static_cast<T *>(p.dq) + (tok0 * Hq + hq) * DK, rstride,
                            valid, p.l2norm, warp, 8, lane);
-        l2norm_bwd_rows<T>(fk, k + (tok0 * Hq + hq) * DK, rstride, static_cast<T *>(p.dk) + (tok0 * Hq + hq) * DK,
+        l2norm_bwd_rows<T>(fk, sb + S_K0, &f(F_IK, 0), static_cast<T *>(p.dk) + (tok0 * Hq + hq) * DK, rstride,
                            valid, p.l2norm, warp, 8, lane);
     }
     umma::fence_before();

@@ -6,19 +6,17 @@
 // columns).  The slice of h lives in fp32 registers of eight "state" warps
 // (TMEM lane = key row d) and, rounded, in shared memory as the B operand of
 // the MMAs.  With G the chunk-local cumsum of g, Gl = G at the last valid row,
-// rq / rk the inverse L2 norms of the q / k rows (1 without normalisation) and
-// A = (I + strictly-lower(diag(beta)(K K^T o Gamma)))^-1 from wy_fwd, a chunk is
+// rq / rk the inverse L2 norms of the q / k rows (1 without normalisation),
+// A = (I + strictly-lower(diag(beta)(K K^T o Gamma)))^-1 and the decayed causal
+// block P = scale (q^ k^T o Gamma) from wy_fwd, a chunk is
 //
-//   state-independent products, issued one chunk ahead so that they overlap
-//   the previous chunk's recurrence:
-//     [. ; Q] K^T                       -> Q K^T in TMEM lanes 64..127   (M=128, N=64, K=128)
-//     K^T (A diag(beta e^G rk))^T       -> W^T                           (M=128, N=64, K=64)
-//     [A diag(beta) ; 0] V              -> U in lanes 0..63, 0 above     (M=128, N=BV, K=64)
-//     epilogues: -W^T and Q~^T = (diag(scale rq e^G) Q)^T into one MN-major operand;
-//                K~ = diag(rk e^{Gl-G}) K in place; P = Q K^T o (scale rq_r rk_s e^{G_r-G_s}), s <= r
+//   state-independent products, issued while the previous chunk's recurrence runs:
+//     [0 ; A diag(beta e^G rk)] K   -> W in TMEM lanes 64..127                (M=128, N=128, K=64)
+//     [A diag(beta) ; 0] V          -> U in lanes 0..63, 0 in 64..127         (M=128, N=BV,  K=64)
+//     preparation: Q~ = diag(scale rq e^G) Q in place; the -W epilogue fills the rows above Q~
 //   the recurrence, two dependent MMA rounds:
-//     round A:  [-W ; Q~] h added to [U ; 0]  -> Delta (lanes 0..63), Q~ h (lanes 64..127)
-//     round B:  X = K~^T Delta ;  [. ; P] Delta added to lanes 64..127 -> the output rows
+//     round A:  [-W ; Q~] h added to [U ; 0]  -> Delta = U - W h (lanes 0..63), Q~ h (64..127)
+//     round B:  X = K^T (diag(rk e^{Gl-G}) Delta) ;  [. ; P] Delta added to lanes 64..127 -> output rows
 //     epilogue: h <- e^{Gl} h + X
 //
 // This is the chunk form of S_t = e^{g_t} S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
@@ -26,11 +24,14 @@
 // WY/UT representation, PR #998 "[GDN] Add FlashQLA backend dispatch").
 //
 // Warp roles (one CTA per SM):
-//   warp 0        lane 0 issues every MMA (single-thread issue, commits to mbarriers)
-//   warp 1        lane 0 issues the TMA tile loads into a two-stage ring
-//   warps 2, 3    TMEM lanes 64..127: the P epilogue and the output rows
-//   warps 4..11   the state: TMEM lane 32*(w%4)+l, value columns of half (w-4)/4 of the slice
-//   warps 12..15  per-chunk preparation: norms, gate factors, scaled copies of A, -W^T, Q~^T, K~
+//   warp 0            lane 0 issues every MMA (single thread; the next chunk's products are issued in
+//                     small groups around round B so that round B never waits behind them)
+//   warp 1            lane 0 issues the TMA tile loads into a two-stage ring
+//   warps 2,3         TMEM lanes 64..127: the -W epilogue and the output rows
+//   warps 4..11       the state: TMEM lane 32*(w%4)+l, value columns of half (w-4)/4 of the slice;
+//                     warps 4,5,8,9 also move Delta (lanes 0..63) into shared memory
+//   warps 12..15      per-chunk preparation (one warp per scheduler): gate factors, scaled copies of
+//                     A, Q~
 // Hand-offs go through mbarriers whose phases each complete once per chunk; every wait is
 // bounded and gives up early once another role has raised the block's error flag.
 #include <cuda_runtime.h>
@@ -48,39 +49,38 @@ namespace {
 constexpr int WS_NT = 512;
 constexpr long kWaitPolls = 40000000L;
 
-// factor arrays (64 floats each), two sets (chunk parity)
-enum { FG = 0, FRQ, FRK, FRQS, FCQ, FCK, FAKG, FAB, NF };
+// factor arrays (64 floats each), four sets (chunk index mod 4)
+enum { FG = 0, FRQ, FRK, FB, FCQ, FCK, FAKG, FAB, NF };
 
 template <int BV>
 struct Lay {
-    // stage: [V b0 | Q b0 | A or V b1 | Q b1 | K b0 | K b1 (| A)], 8 KB blocks of 64 rows x 128 B
-    static constexpr uint32_t ST_V = 0, ST_Q0 = 8192, ST_Q1 = 24576, ST_K0 = 32768;
-    static constexpr uint32_t ST_A = BV == 128 ? 49152 : 16384;
-    static constexpr uint32_t ST_BYTES = BV == 128 ? 57344 : 49152;
-    static constexpr uint32_t WQ = 2 * ST_BYTES;  // MN-major [-W^T | Q~^T], 16 KB blocks of 128 d-rows
-    static constexpr uint32_t AKG = WQ + 32768;   // [r][s] K-major
-    static constexpr uint32_t PT0 = AKG + 8192;   // P of even chunks (its MMA reads AKG as rows 0..63)
-    static constexpr uint32_t AB = PT0 + 8192;    // [r][s], followed by 8 KB of zeros
+    // stage: [-W b0 | Q~ b0 | -W b1 | Q~ b1 | K b0 | K b1 | V | A | P], 8 KB blocks of 64 rows x 128 B
+    // ([-W; Q~] is one K-major 128-row operand per key half, [A; P] one 128-row operand)
+    static constexpr uint32_t ST_W0 = 0, ST_Q0 = 8192, ST_W1 = 16384, ST_Q1 = 24576, ST_K0 = 32768,
+                              ST_V = 49152, ST_A = ST_V + BV * 128, ST_P = ST_A + 8192, ST_BYTES = ST_P + 8192;
+    static constexpr uint32_t AB = 2 * ST_BYTES;  // [A diag(beta) ; 0] and [0 ; A diag(beta e^G rk)]
     static constexpr uint32_t Z = AB + 8192;
-    static constexpr uint32_t DL = Z + 8192;       // Delta [64 s][BV]: BV/64 blocks of 8 KB
-    static constexpr uint32_t PT1 = DL + BV * 128;  // P of odd chunks (rows 0..63 of its MMA: Delta)
-    static constexpr uint32_t H = PT1 + 8192;       // h [128 d][BV]: BV/64 blocks of 16 KB
-    static constexpr uint32_t F = H + BV * 256;
-    static constexpr uint32_t BAR = F + 2 * NF * 256;
+    static constexpr uint32_t AKG = Z + 8192;
+    static constexpr uint32_t DL = AKG + 8192;      // Delta [64 s][BV]: BV/64 blocks of 8 KB
+    static constexpr uint32_t DT = DL + BV * 128;   // diag(rk e^{Gl-G}) Delta
+    static constexpr uint32_t H = DT + BV * 128;    // h [128 d][BV]: BV/64 blocks of 16 KB
+    static constexpr uint32_t F = H + BV * 256;     // factor sets (4, by chunk index mod 4)
+    static constexpr uint32_t BAR = F + 4 * NF * 256;
     // barriers
-    static constexpr uint32_t B_FULL = BAR, B_EMPTY = BAR + 16, B_PREP = BAR + 32, B_EPIP = BAR + 40,
-                              B_MP = BAR + 48, B_MA = BAR + 56, B_EPIA = BAR + 64, B_MB = BAR + 72,
-                              B_EPIB = BAR + 80, B_MO = BAR + 88, B_OFREE = BAR + 104, B_DONE = BAR + 120;
-    static constexpr uint32_t SLOT = BAR + 128, FLAG = SLOT + 4, USED = FLAG + 12;
+    static constexpr uint32_t B_FULL = BAR, B_EMPTY = BAR + 16, B_PREP = BAR + 32, B_EPIW = BAR + 40,
+                              B_MPW = BAR + 48, B_MA = BAR + 56, B_EPIA = BAR + 64, B_MB = BAR + 72,
+                              B_EPIB = BAR + 80, B_MO = BAR + 88, B_OFREE = BAR + 104, B_DONE = BAR + 120,
+                              B_MPU = BAR + 128;
+    static constexpr uint32_t SLOT = BAR + 136, FLAG = SLOT + 4, USED = FLAG + 12;
     static constexpr uint32_t BYTES = USED + 1024;  // slack for aligning the base
     // TMEM columns
-    static constexpr uint32_t T_D0 = 0, T_D1 = BV, T_X = 2 * BV, T_QK = 3 * BV, T_W = 3 * BV + 64;
+    static constexpr uint32_t T_W = 0, T_D0 = 128, T_D1 = 128 + BV, T_X = 128 + 2 * BV;
 };
 static_assert(Lay<64>::BYTES <= 232448, "shared memory");
 
 struct WsP {
-    CUtensorMap tq, tk, tv, ta;  // [tokens][heads][cols] maps, boxes 64 x 1 x 64
-    const float *g_cs, *h0;
+    CUtensorMap tq, tk, tv, tp, ta;  // [tokens][heads][cols] maps, boxes 64 x 1 x 64
+    const float *g_cs, *h0, *rq, *rk;  // rq, rk: inverse q/k norms [tokens,Hv] (l2norm only)
     const void *beta;
     void *o;
     float *fin;
@@ -91,10 +91,22 @@ struct WsP {
     float scale;
 };
 
+// One test of a barrier phase that may suspend the thread until the phase completes (or a short
+// hardware time limit passes): waiting warps leave the issue slots to the working ones.
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
         "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// One non-blocking test (the MMA thread polls several barriers in turn).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(done)
         : "r"(bar), "r"(parity)
         : "memory");
@@ -177,7 +189,7 @@ __global__ void __launch_bounds__(WS_NT, 1) chain_ws_kernel(Geo geo, const __gri
     const int nc = (len + C - 1) / C;
     volatile int *flag = reinterpret_cast<volatile int *>(smem + L::FLAG);
     float *F = reinterpret_cast<float *>(smem + L::F);
-    auto fa = [&](int par, int which) -> float * { return F + (par * NF + which) * 64; };
+    auto fa = [&](int lc, int which) -> float * { return F + ((lc & 3) * NF + which) * 64; };
 
     if (tid == 0) {
         umma::mbar_init(sb + L::B_FULL, 1);
@@ -185,9 +197,10 @@ __global__ void __launch_bounds__(WS_NT, 1) chain_ws_kernel(Geo geo, const __gri
         umma::mbar_init(sb + L::B_EMPTY, 1);
         umma::mbar_init(sb + L::B_EMPTY + 8, 1);
         umma::mbar_init(sb + L::B_PREP, 4);
-        umma::mbar_init(sb + L::B_EPIP, WRITE_O ? 6 : 4);
-        umma::mbar_init(sb + L::B_MP, 2);  // the commit, and the issuing thread's own arrival
-        umma::mbar_init(sb + L::B_MA, 1);
+        umma::mbar_init(sb + L::B_EPIW, 2);
+        umma::mbar_init(sb + L::B_MPW, 1);
+        umma::mbar_init(sb + L::B_MPU, 1);
+        umma::mbar_init(sb + L::B_MA, 2);
         umma::mbar_init(sb + L::B_EPIA, 4);
         umma::mbar_init(sb + L::B_MB, 1);
         umma::mbar_init(sb + L::B_EPIB, 8);
@@ -199,7 +212,7 @@ __global__ void __launch_bounds__(WS_NT, 1) chain_ws_kernel(Geo geo, const __gri
         umma::fence_mbar_init();
         *flag = 0;
     }
-    // zero block below A diag(beta) (rows 64..127 of the U product)
+    // the zero block between A diag(beta e^G rk) and A diag(beta)
     for (int i = tid; i < 8192 / 16; i += WS_NT) st_v4(sb + L::Z + i * 16, 0u, 0u, 0u, 0u);
     umma::fence_async_smem();
     if (warp == 0) umma::alloc(sb + L::SLOT, 512);
@@ -217,15 +230,16 @@ __global__ void __launch_bounds__(WS_NT, 1) chain_ws_kernel(Geo geo, const __gri
                 if (lc >= 2 && !wait_phase(sb + L::B_EMPTY + 8 * s, ((lc >> 1) - 1) & 1, flag, geo.err)) break;
                 const uint32_t st = sb + s * L::ST_BYTES, full = sb + L::B_FULL + 8 * s;
                 const int t = (int)(tok0 + (long long)lc * C);
-                tma::expect_tx(full, (WRITE_O ? 16384u : 0u) + 16384u + (uint32_t)BV * 128u + 8192u);
+                tma::expect_tx(full, (WRITE_O ? 16384u + 8192u : 0u) + 16384u + (uint32_t)BV * 128u + 8192u);
                 if (WRITE_O) {
                     tma::load3d(st + L::ST_Q0, &p.tq, 0, hq, t, full);
                     tma::load3d(st + L::ST_Q1, &p.tq, 64, hq, t, full);
+                    tma::load3d(st + L::ST_P, &p.tp, 0, j, t, full);
                 }
                 tma::load3d(st + L::ST_K0, &p.tk, 0, hq, t, full);
                 tma::load3d(st + L::ST_K0 + 8192, &p.tk, 64, hq, t, full);
                 tma::load3d(st + L::ST_V, &p.tv, v0, j, t, full);
-                if (BV == 128) tma::load3d(st + L::ST_V + 16384, &p.tv, v0 + 64, j, t, full);
+                if (BV == 128) tma::load3d(st + L::ST_V + 8192, &p.tv, v0 + 64, j, t, full);
                 tma::load3d(st + L::ST_A, &p.ta, 0, j, t, full);
                 ++issued[s];
             }
@@ -236,74 +250,101 @@ __global__ void __launch_bounds__(WS_NT, 1) chain_ws_kernel(Geo geo, const __gri
     } else if (warp == 0) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
-            const uint32_t id_qk = umma::idesc(128, 64, bf16, false, false);
-            const uint32_t id_w = umma::idesc(128, 64, bf16, true, false);
-            const uint32_t id_u = umma::idesc(128, BV, bf16, false, true);
-            const uint32_t id_mn = umma::idesc(128, BV, bf16, true, true);
-            const uint32_t id_o = umma::idesc(128, BV, bf16, false, true);
-            const uint64_t dAKG = umma::desc(sb + L::AKG, 16, 1024), dAB = umma::desc(sb + L::AB, 16, 1024);
-            const uint64_t dWQ = umma::desc(sb + L::WQ, 16384, 1024), dH = umma::desc(sb + L::H, 16384, 1024);
-            const uint64_t dDL = umma::desc(sb + L::DL, 8192, 1024);
-            const uint64_t dP0 = umma::desc(sb + L::PT0 - 8192, 16, 1024), dP1 = umma::desc(sb + L::PT1 - 8192, 16, 1024);
-            auto issue_p = [&](int lc) {
-                const int s = lc & 1;
-                const uint32_t st = sb + s * L::ST_BYTES;
-                if (WRITE_O) {
-                    const uint64_t aq = umma::desc(st, 16, 1024), bk = umma::desc(st + L::ST_K0, 16, 1024);
+            const uint32_t id_w = umma::idesc(128, 128, bf16, false, true);
+            const uint32_t id_bv = umma::idesc(128, BV, bf16, false, true);   // K-major A, MN-major B
+            const uint32_t id_mn = umma::idesc(128, BV, bf16, true, true);    // MN-major A and B
+            const uint64_t dZAKG = umma::desc(sb + L::Z, 16, 1024), dABZ = umma::desc(sb + L::AB, 16, 1024);
+            const uint64_t dH = umma::desc(sb + L::H, 16384, 1024);
+            const uint64_t dDL = umma::desc(sb + L::DL, 8192, 1024), dDT = umma::desc(sb + L::DT, 8192, 1024);
+            auto issue_w = [&](int lc) {  // W of chunk lc
+                const uint32_t st = sb + (lc & 1) * L::ST_BYTES;
+                const uint64_t bk = umma::desc(st + L::ST_K0, 8192, 1024);
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        umma::mma(tmem + L::T_QK, aq + ((((ks >> 2) * 16384) + (ks & 3) * 32) >> 4),
-                                  bk + ((((ks >> 2) * 8192) + (ks & 3) * 32) >> 4), id_qk, ks > 0);
-                }
-                const uint64_t akmn = umma::desc(st + L::ST_K0, 8192, 1024), bv = umma::desc(st + L::ST_V, 16384, 1024);
+                for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + L::T_W, dZAKG + ks * 2, bk + ks * 128, id_w, ks > 0);
+            };
+            auto issue_u = [&](int lc) {  // U of chunk lc (also zeroes the output lanes 64..127)
+                const uint32_t st = sb + (lc & 1) * L::ST_BYTES;
+                const uint64_t bv = umma::desc(st + L::ST_V, 8192, 1024);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    umma::mma(tmem + L::T_W, akmn + ks * 128, dAKG + ks * 2, id_w, ks > 0);
-                    umma::mma(tmem + (s ? L::T_D1 : L::T_D0), dAB + ks * 2, bv + ks * 128, id_u, ks > 0);
-                }
-                umma::commit(sb + L::B_MP);
-                mbar_arrive(sb + L::B_MP);
+                for (int ks = 0; ks < 4; ++ks)
+                    umma::mma(tmem + ((lc & 1) ? L::T_D1 : L::T_D0), dABZ + ks * 2, bv + ks * 128, id_bv, ks > 0);
             };
             bool ok = true;
             if (nc > 0) {
                 ok = wait_phase(sb + L::B_PREP, 0, flag, geo.err) && wait_phase(sb + L::B_FULL, 0, flag, geo.err);
                 umma::fence_after();
-                if (ok) issue_p(0);
+                if (ok) {
+                    issue_w(0);
+                    umma::commit(sb + L::B_MPW);
+                    issue_u(0);
+                    umma::commit(sb + L::B_MPU);
+                }
             }
             for (int lc = 0; lc < nc && ok; ++lc) {
                 const int b = lc & 1;
                 const uint32_t st = sb + b * L::ST_BYTES;
                 const uint32_t tD = b ? L::T_D1 : L::T_D0;
-                // round A: needs this chunk's -W^T / Q~^T / K~ / P and the state tile
-                if (!(ok = wait_phase(sb + L::B_EPIP, lc & 1, flag, geo.err) &&
+                // round A: needs -W (rows above Q~) and the state tile
+                if (!(ok = wait_phase(sb + L::B_EPIW, lc & 1, flag, geo.err) &&
                            wait_phase(sb + L::B_EPIB, lc & 1, flag, geo.err)))
                     break;
                 umma::fence_after();
+                {
+                    const uint64_t aqw = umma::desc(st + L::ST_W0, 16, 1024);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) umma::mma(tmem + tD, dWQ + ks * 128, dH + ks * 128, id_mn, true);
+                    for (int ks = 0; ks < 8; ++ks)
+                        umma::mma(tmem + tD, aqw + ((((ks >> 2) * 16384) + (ks & 3) * 32) >> 4), dH + ks * 128, id_bv,
+                                  true);
+                }
                 umma::commit(sb + L::B_MA);
-                // the next chunk's state-independent products run while round A's epilogue works
-                if (lc + 1 < nc) {
-                    const int b1 = (lc + 1) & 1;
-                    if (!(ok = wait_phase(sb + L::B_PREP, (lc + 1) & 1, flag, geo.err) &&
-                               wait_phase(sb + L::B_FULL + 8 * b1, ((lc + 1) >> 1) & 1, flag, geo.err) &&
-                               (!WRITE_O || lc < 1 || wait_phase(sb + L::B_OFREE + 8 * b1, ((lc - 1) >> 1) & 1, flag, geo.err))))
-                        break;
-                    umma::fence_after();
-                    issue_p(lc + 1);
-                }
-                // round B: needs Delta
-                if (!(ok = wait_phase(sb + L::B_EPIA, lc & 1, flag, geo.err))) break;
-                umma::fence_after();
-                const uint64_t akt = umma::desc(st + L::ST_K0, 8192, 1024);
+                mbar_arrive(sb + L::B_MA);
+                // round B as soon as Delta is in shared memory; the next chunk's W group goes in whenever
+                // its inputs are ready, its U group (needed only by the next round A) after round B
+                const bool next = lc + 1 < nc;
+                bool b_done = false, w_done = !next, u_done = !next;
+                for (long it = 0; !(b_done && w_done && u_done); ++it) {
+                    if (!b_done && mbar_test(sb + L::B_EPIA, lc & 1)) {
+                        umma::fence_after();
+                        const uint64_t akt = umma::desc(st + L::ST_K0, 8192, 1024);
+                        const uint64_t ap = umma::desc(st + L::ST_A, 16, 1024);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    umma::mma(tmem + L::T_X, akt + ks * 128, dDL + ks * 128, id_mn, ks > 0);
-                    if (WRITE_O) umma::mma(tmem + tD, (b ? dP1 : dP0) + ks * 2, dDL + ks * 128, id_o, true);
+                        for (int ks = 0; ks < 4; ++ks) {
+                            umma::mma(tmem + L::T_X, akt + ks * 128, dDT + ks * 128, id_mn, ks > 0);
+                            if (WRITE_O) umma::mma(tmem + tD, ap + ks * 2, dDL + ks * 128, id_bv, true);
+                        }
+                        umma::commit(sb + L::B_MB);
+                        umma::commit(sb + L::B_EMPTY + 8 * b);
+                        umma::commit(sb + L::B_MO + 8 * b);
+                        b_done = true;
+                        continue;
+                    }
+                    if (!w_done && mbar_test(sb + L::B_PREP, (lc + 1) & 1) &&
+                        mbar_test(sb + L::B_FULL + 8 * (b ^ 1), ((lc + 1) >> 1) & 1)) {
+                        umma::fence_after();
+                        issue_w(lc + 1);
+                        umma::commit(sb + L::B_MPW);
+                        w_done = true;
+                        continue;
+                    }
+                    if (!u_done && w_done && b_done &&
+                        (!WRITE_O || lc < 1 || mbar_test(sb + L::B_OFREE + 8 * (b ^ 1), ((lc - 1) >> 1) & 1))) {
+                        umma::fence_after();
+                        issue_u(lc + 1);
+                        umma::commit(sb + L::B_MPU);
+                        u_done = true;
+                        continue;
+                    }
+                    if ((it & 127) == 127 && *flag) {
+                        ok = false;
+                        break;
+                    }
+                    if (it > kWaitPolls) {
+                        raise_error(geo.err, GDR_ERR_TIMEOUT);
+                        *flag = 1;
+                        ok = false;
+                        break;
+                    }
                 }
-                umma::commit(sb + L::B_MB);
-                umma::commit(sb + L::B_EMPTY + 8 * b);
-                umma::commit(sb + L::B_MO + 8 * b);
             }
             // every MMA issued so far completes before TMEM is released
             umma::commit(sb + L::B_DONE);
@@ -311,156 +352,117 @@ __global__ void __launch_bounds__(WS_NT, 1) chain_ws_kernel(Geo geo, const __gri
         }
     } else if (warp >= 12) {
         // ------------------------------------------------------------ preparation (128 threads)
-        const int at = tid - 384;
-        const int lb = (warp & 3) * 32;  // == at & ~31
-        float greg = 0.f, breg = 0.f;
+        const int at = (warp - 12) * 32 + lane;  // 0..127
+        float x0 = 0.f, x1 = 0.f;  // prefetched: G, rq (threads 0..63) or beta, rk (64..127)
         auto fetch = [&](int lc) {
             const int valid = min(C, len - lc * C);
             const int r = at & 63;
+            x0 = 0.f;
+            x1 = 1.f;
             if (r < valid) {
                 const long long ti = (tok0 + (long long)lc * C + r) * Hv + j;
-                if (at < 64)
-                    greg = p.g_cs[ti];
-                else
-                    breg = load_gate<T>(p.beta, ti, p.gate_f32);
-            } else {
-                greg = 0.f;
-                breg = 0.f;
+                if (at < 64) {
+                    x0 = p.g_cs[ti];
+                    if (p.l2norm && WRITE_O) x1 = p.rq[ti];
+                } else {
+                    x0 = load_gate<T>(p.beta, ti, p.gate_f32);
+                    if (p.l2norm) x1 = p.rk[ti];
+                }
             }
         };
         if (nc > 0) fetch(0);
         for (int lc = 0; lc < nc; ++lc) {
-            const int b = lc & 1, s = lc & 1;
+            const int s = lc & 1;
             const uint32_t st = sb + s * L::ST_BYTES;
             const int valid = min(C, len - lc * C);
-            if (at < 64)
-                fa(b, FG)[at] = greg;
-            else
-                fa(b, FAB)[at - 64] = breg;  // raw beta for now
-            if (lc + 1 < nc) fetch(lc + 1);
-            if (!group_and(warp_wait(sb + L::B_FULL + 8 * s, (lc >> 1) & 1, flag, geo.err, lane), 1, 128)) break;
-            // inverse norms of the q rows (threads 0..63) and k rows (64..127)
-            if (p.l2norm && (WRITE_O || at >= 64)) {
-                const int r = at & 63;
-                const uint32_t b0 = st + (at < 64 ? L::ST_Q0 : L::ST_K0);
-                const uint32_t b1 = st + (at < 64 ? L::ST_Q1 : L::ST_K0 + 8192);
-                float ss = 0.f;
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const uint4 u = umma::ld_shared_v4((c < 8 ? b0 : b1) + umma::off(r, (c & 7) * 8, 0));
-                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 x = Elt<T>::unpack(w[e]);
-                        ss = fmaf(x.x, x.x, fmaf(x.y, x.y, ss));
-                    }
-                }
-                fa(b, at < 64 ? FRQ : FRK)[r] = 1.0f / sqrtf(ss + L2_EPS);
+            if (at < 64) {
+                fa(lc, FG)[at] = x0;
+                fa(lc, FRQ)[at] = x1;
+            } else {
+                fa(lc, FB)[at - 64] = x0;
+                fa(lc, FRK)[at - 64] = x1;
             }
+            if (lc + 1 < nc) fetch(lc + 1);
             asm volatile("bar.sync 1, 128;\n" ::: "memory");
             if (at < 64) {
                 const int r = at;
                 const bool ok = r < valid;
-                const float gr = fa(b, FG)[r], Gl = fa(b, FG)[valid - 1];
-                const float rq = (p.l2norm && WRITE_O) ? fa(b, FRQ)[r] : 1.f;
-                const float rk = p.l2norm ? fa(b, FRK)[r] : 1.f;
-                const float be = fa(b, FAB)[r];
+                const float gr = fa(lc, FG)[r], Gl = fa(lc, FG)[valid - 1];
+                const float rq = fa(lc, FRQ)[r], rk = fa(lc, FRK)[r], be = fa(lc, FB)[r];
                 const float eg = __expf(gr);
-                fa(b, FRQS)[r] = ok ? p.scale * rq : 0.f;
-                fa(b, FRK)[r] = ok ? rk : 0.f;
-                fa(b, FCQ)[r] = ok ? p.scale * rq * eg : 0.f;
-                fa(b, FCK)[r] = ok ? rk * __expf(Gl - gr) : 0.f;
-                fa(b, FAKG)[r] = ok ? be * eg * rk : 0.f;
-                fa(b, FAB)[r] = ok ? be : 0.f;
+                fa(lc, FCQ)[r] = ok ? p.scale * rq * eg : 0.f;
+                fa(lc, FCK)[r] = ok ? rk * __expf(Gl - gr) : 0.f;
+                fa(lc, FAKG)[r] = ok ? be * eg * rk : 0.f;
+                fa(lc, FAB)[r] = ok ? be : 0.f;
             }
-            asm volatile("bar.sync 1, 128;\n" ::: "memory");
-            // A diag(beta e^G rk) and A diag(beta): thread -> row at/2, 32 columns; rows past the end are zero
+            // the stage's tiles, and the previous chunk's W and U groups done with the scaled copies of A
+            bool ok = warp_wait(sb + L::B_FULL + 8 * s, (lc >> 1) & 1, flag, geo.err, lane);
+            if (ok && lc > 0) ok = warp_wait(sb + L::B_MPU, (lc - 1) & 1, flag, geo.err, lane);
+            if (!group_and(ok, 1, 128)) break;
             {
+                // A diag(beta e^G rk) and A diag(beta): thread -> row at/2, 32 columns; rows past the end are
+                // zero.  Every shared load is issued before the first store (the stores are ordered asm).
                 const int r = at >> 1, c0 = (at & 1) * 32;
-                const float *fk = fa(b, FAKG), *fb = fa(b, FAB);
+                const bool okr = r < valid;
+                const float4 *fk4 = reinterpret_cast<const float4 *>(fa(lc, FAKG) + c0);
+                const float4 *fb4 = reinterpret_cast<const float4 *>(fa(lc, FAB) + c0);
+                uint4 u[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) u[c] = umma::ld_shared_v4(st + L::ST_A + umma::off(r, c0 + c * 8, 0));
+                float fkv[32], fbv[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 a = fk4[i], bq = fb4[i];
+                    fkv[4 * i] = a.x, fkv[4 * i + 1] = a.y, fkv[4 * i + 2] = a.z, fkv[4 * i + 3] = a.w;
+                    fbv[4 * i] = bq.x, fbv[4 * i + 1] = bq.y, fbv[4 * i + 2] = bq.z, fbv[4 * i + 3] = bq.w;
+                }
+                uint32_t wk[16], wb[16];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const int col = c0 + c * 8;
-                    const uint32_t o = umma::off(r, col, 0);
-                    const uint4 u = umma::ld_shared_v4(st + L::ST_A + o);
-                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-                    uint32_t wk[4], wb[4];
+                    const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 x = Elt<T>::unpack(w[e]);
-                        const bool ok = r < valid;
-                        wk[e] = Elt<T>::pack(ok ? x.x * fk[col + 2 * e] : 0.f, ok ? x.y * fk[col + 2 * e + 1] : 0.f);
-                        wb[e] = Elt<T>::pack(ok ? x.x * fb[col + 2 * e] : 0.f, ok ? x.y * fb[col + 2 * e + 1] : 0.f);
+                        const int i = c * 8 + 2 * e;
+                        wk[c * 4 + e] = Elt<T>::pack(okr ? x.x * fkv[i] : 0.f, okr ? x.y * fkv[i + 1] : 0.f);
+                        wb[c * 4 + e] = Elt<T>::pack(okr ? x.x * fbv[i] : 0.f, okr ? x.y * fbv[i + 1] : 0.f);
                     }
-                    st_v4(sb + L::AKG + o, wk[0], wk[1], wk[2], wk[3]);
-                    st_v4(sb + L::AB + o, wb[0], wb[1], wb[2], wb[3]);
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t o = umma::off(r, c0 + c * 8, 0);
+                    st_v4(sb + L::AKG + o, wk[4 * c], wk[4 * c + 1], wk[4 * c + 2], wk[4 * c + 3]);
+                    st_v4(sb + L::AB + o, wb[4 * c], wb[4 * c + 1], wb[4 * c + 2], wb[4 * c + 3]);
+                }
+            }
+            if (WRITE_O) {
+                // Q~ = diag(scale rq e^G) Q in place: thread -> row at & 63, key half at >> 6
+                const int r = at & 63;
+                const float cq = fa(lc, FCQ)[r];
+                const uint32_t blk = st + ((at >> 6) ? L::ST_Q1 : L::ST_Q0);
+                uint4 u[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) u[c] = umma::ld_shared_v4(blk + umma::off(r, c * 8, 0));
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
+                    uint32_t o4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 x = Elt<T>::unpack(w[e]);
+                        o4[e] = Elt<T>::pack(x.x * cq, x.y * cq);
+                    }
+                    st_v4(blk + umma::off(r, c * 8, 0), o4[0], o4[1], o4[2], o4[3]);
                 }
             }
             umma::fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(sb + L::B_PREP);
-            // ---- after the state-independent products of this chunk
-            if (!group_and(warp_wait(sb + L::B_MP, lc & 1, flag, geo.err, lane), 1, 128)) break;
-            umma::fence_after();
-            {
-                // -W^T row d = at: 64 token columns into the MN-major block 0 of WQ
-#pragma unroll
-                for (int c = 0; c < 64; c += 16) {
-                    float x[16];
-                    umma::ld16(umma::taddr(tmem, lb, L::T_W + c), x);
-                    umma::ld_wait();
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) x[u] = -x[u];
-                    store_row16<T>(sb + L::WQ, at, c, x);
-                }
-            }
-            umma::fence_before();
-            if (WRITE_O) {
-                // Q~^T: thread -> q row r = at & 63, key half at >> 6; element (d, r) of block 1 of WQ
-                const int r = at & 63, dh = at >> 6;
-                const float cq = fa(b, FCQ)[r];
-                const uint32_t src = st + (dh ? L::ST_Q1 : L::ST_Q0), dst = sb + L::WQ + 16384;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 u = umma::ld_shared_v4(src + umma::off(r, c * 8, 0));
-                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 x = Elt<T>::unpack(w[e]);
-                        const int d = dh * 64 + c * 8 + 2 * e;
-                        const uint16_t lo = to_bits<T>(x.x * cq), hi = to_bits<T>(x.y * cq);
-                        asm volatile("st.shared.u16 [%0], %1;\n" ::"r"(dst + umma::off(d, r, 0)), "h"(lo));
-                        asm volatile("st.shared.u16 [%0], %1;\n" ::"r"(dst + umma::off(d + 1, r, 0)), "h"(hi));
-                    }
-                }
-            }
-            {
-                // K~ in place: thread -> k row s = at & 63, key half at >> 6
-                const int s2 = at & 63, dh = at >> 6;
-                const float ck = fa(b, FCK)[s2];
-                const uint32_t blk = st + L::ST_K0 + dh * 8192;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint32_t a = blk + umma::off(s2, c * 8, 0);
-                    const uint4 u = umma::ld_shared_v4(a);
-                    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-                    uint32_t o4[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 x = Elt<T>::unpack(w[e]);
-                        o4[e] = Elt<T>::pack(x.x * ck, x.y * ck);
-                    }
-                    st_v4(a, o4[0], o4[1], o4[2], o4[3]);
-                }
-            }
-            umma::fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sb + L::B_EPIP);
         }
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------------------------ state (256 threads)
         const int sw = warp - 4, q4 = warp & 3, cg = sw >> 2;
-        const int d = q4 * 32 + lane;  // TMEM lane: key row of h, token row of Delta
+        const int d = q4 * 32 + lane;  // TMEM lane: key row of h; for q4 < 2 also token row d of Delta
         constexpr int HW = BV / 2;     // value columns per thread
         const int cb0 = cg * HW;
         const long long st_base = ((long long)n * Hv + j) * DK * DV;
@@ -513,25 +515,31 @@ __global__ void __launch_bounds__(WS_NT, 1) chain_ws_kernel(Geo geo, const __gri
                 }
             }
             if (q4 < 2) {
-                // Delta rows (lanes 0..63) -> the B operand of round B
+                // Delta rows (lanes 0..63): Delta for the output product, diag(rk e^{Gl-G}) Delta for X
                 if (!warp_wait(sb + L::B_MA, lc & 1, flag, geo.err, lane)) break;
                 umma::fence_after();
+                const int sr = d;
+                const float ck = fa(lc, FCK)[sr];
+                float xa[HW];
+#pragma unroll
+                for (int i = 0; i < HW; i += 16) umma::ld16(umma::taddr(tmem, q4 * 32, tD + cb0 + i), xa + i);
+                umma::ld_wait();
 #pragma unroll
                 for (int i = 0; i < HW; i += 16) {
-                    float x[16];
-                    umma::ld16(umma::taddr(tmem, q4 * 32, tD + cb0 + i), x);
-                    umma::ld_wait();
+                    float *x = xa + i, y[16];
                     const int col = cb0 + i;
-                    store_row16<T>(sb + L::DL + (col >> 6) * 8192, d, col & 63, x);
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) y[u] = x[u] * ck;
+                    if (WRITE_O) store_row16<T>(sb + L::DL + (col >> 6) * 8192, sr, col & 63, x);
+                    store_row16<T>(sb + L::DT + (col >> 6) * 8192, sr, col & 63, y);
                     if (p.delta) {
-                        T *dr = static_cast<T *>(p.delta) + (((long long)(row0 + lc) * Hv + j) * C + d) * DV + v0 + col;
-                        uint4 w0, w1;
-                        w0 = make_uint4(Elt<T>::pack(x[0], x[1]), Elt<T>::pack(x[2], x[3]), Elt<T>::pack(x[4], x[5]),
-                                        Elt<T>::pack(x[6], x[7]));
-                        w1 = make_uint4(Elt<T>::pack(x[8], x[9]), Elt<T>::pack(x[10], x[11]),
-                                        Elt<T>::pack(x[12], x[13]), Elt<T>::pack(x[14], x[15]));
-                        *reinterpret_cast<uint4 *>(dr) = w0;
-                        *reinterpret_cast<uint4 *>(dr + 8) = w1;
+                        T *dr = static_cast<T *>(p.delta) + (((long long)(row0 + lc) * Hv + j) * C + sr) * DV + v0 + col;
+                        *reinterpret_cast<uint4 *>(dr) =
+                            make_uint4(Elt<T>::pack(x[0], x[1]), Elt<T>::pack(x[2], x[3]), Elt<T>::pack(x[4], x[5]),
+                                       Elt<T>::pack(x[6], x[7]));
+                        *reinterpret_cast<uint4 *>(dr + 8) =
+                            make_uint4(Elt<T>::pack(x[8], x[9]), Elt<T>::pack(x[10], x[11]),
+                                       Elt<T>::pack(x[12], x[13]), Elt<T>::pack(x[14], x[15]));
                     }
                 }
                 umma::fence_before();
@@ -541,13 +549,13 @@ __global__ void __launch_bounds__(WS_NT, 1) chain_ws_kernel(Geo geo, const __gri
             }
             if (!warp_wait(sb + L::B_MB, lc & 1, flag, geo.err, lane)) break;
             umma::fence_after();
+            {
+                float xb[HW];
 #pragma unroll
-            for (int i = 0; i < HW; i += 16) {
-                float x[16];
-                umma::ld16(umma::taddr(tmem, q4 * 32, L::T_X + cb0 + i), x);
+                for (int i = 0; i < HW; i += 16) umma::ld16(umma::taddr(tmem, q4 * 32, L::T_X + cb0 + i), xb + i);
                 umma::ld_wait();
 #pragma unroll
-                for (int u = 0; u < 16; ++u) hS[i + u] = fmaf(egl, hS[i + u], x[u]);
+                for (int i = 0; i < HW; ++i) hS[i] = fmaf(egl, hS[i], xb[i]);
             }
             umma::fence_before();
             write_h();
@@ -559,60 +567,63 @@ __global__ void __launch_bounds__(WS_NT, 1) chain_ws_kernel(Geo geo, const __gri
                 p.fin[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] = hS[i];
             }
         }
-    } else if (WRITE_O) {
-        // ------------------------------------------------------------ P and output rows (warps 2, 3)
-        const int r = tid - 64;  // token row; TMEM lane 64 + r
+    } else {
+        // ------------------------------------------------------------ -W and output rows (warps 2, 3)
+        const int r = (warp - 2) * 32 + lane;  // token row; TMEM lane 64 + r
         const int lb = 32 * (warp & 3);
-        for (int lc = 0; lc < nc; ++lc) {
+        auto out_rows = [&](int lc) -> bool {
             const int b = lc & 1;
             const int valid = min(C, len - lc * C);
-            if (!warp_wait(sb + L::B_MP, lc & 1, flag, geo.err, lane)) break;
+            if (!warp_wait(sb + L::B_MO + 8 * b, (lc >> 1) & 1, flag, geo.err, lane)) return false;
             umma::fence_after();
-            {
-                const float *fg = fa(b, FG), *frk = fa(b, FRK);
-                const float gr = fg[r], rr = fa(b, FRQS)[r];
-                const uint32_t dst = sb + (b ? L::PT1 : L::PT0);
+            const uint32_t tD = b ? L::T_D1 : L::T_D0;
+            T *orow = static_cast<T *>(p.o) + ((tok0 + (long long)lc * C + r) * Hv + j) * DV + v0;
 #pragma unroll
-                for (int c = 0; c < 64; c += 16) {
-                    float x[16];
-                    umma::ld16(umma::taddr(tmem, lb, L::T_QK + c), x);
-                    umma::ld_wait();
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const int s2 = c + u;
-                        x[u] = (s2 <= r && r < valid) ? x[u] * rr * frk[s2] * __expf(gr - fg[s2]) : 0.f;
-                    }
-                    store_row16<T>(dst, r, c, x);
-                }
-            }
-            umma::fence_before();
-            umma::fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sb + L::B_EPIP);
-            if (!warp_wait(sb + L::B_MO + 8 * b, (lc >> 1) & 1, flag, geo.err, lane)) break;
-            umma::fence_after();
-            {
-                const uint32_t tD = b ? L::T_D1 : L::T_D0;
-                T *orow = static_cast<T *>(p.o) + ((tok0 + (long long)lc * C + r) * Hv + j) * DV + v0;
-#pragma unroll
-                for (int c = 0; c < BV; c += 16) {
-                    float x[16];
-                    umma::ld16(umma::taddr(tmem, lb, tD + c), x);
-                    umma::ld_wait();
-                    if (r < valid) {
-                        *reinterpret_cast<uint4 *>(orow + c) =
-                            make_uint4(Elt<T>::pack(x[0], x[1]), Elt<T>::pack(x[2], x[3]), Elt<T>::pack(x[4], x[5]),
-                                       Elt<T>::pack(x[6], x[7]));
-                        *reinterpret_cast<uint4 *>(orow + c + 8) =
-                            make_uint4(Elt<T>::pack(x[8], x[9]), Elt<T>::pack(x[10], x[11]),
-                                       Elt<T>::pack(x[12], x[13]), Elt<T>::pack(x[14], x[15]));
-                    }
+            for (int c = 0; c < BV; c += 16) {
+                float x[16];
+                umma::ld16(umma::taddr(tmem, lb, tD + c), x);
+                umma::ld_wait();  // (one 16-column slice at a time keeps the warp's registers low)
+                if (r < valid) {
+                    *reinterpret_cast<uint4 *>(orow + c) =
+                        make_uint4(Elt<T>::pack(x[0], x[1]), Elt<T>::pack(x[2], x[3]), Elt<T>::pack(x[4], x[5]),
+                                   Elt<T>::pack(x[6], x[7]));
+                    *reinterpret_cast<uint4 *>(orow + c + 8) =
+                        make_uint4(Elt<T>::pack(x[8], x[9]), Elt<T>::pack(x[10], x[11]), Elt<T>::pack(x[12], x[13]),
+                                   Elt<T>::pack(x[14], x[15]));
                 }
             }
             umma::fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(sb + L::B_OFREE + 8 * b);
+            return true;
+        };
+        bool ok = true;
+        for (int lc = 0; lc < nc && ok; ++lc) {
+            if (!warp_wait(sb + L::B_MPW, lc & 1, flag, geo.err, lane)) break;
+            umma::fence_after();
+            {
+                // -W row r (128 key columns) into the rows above Q~ of this chunk's stage
+                const uint32_t st = sb + (lc & 1) * L::ST_BYTES;
+#pragma unroll
+                for (int c = 0; c < 128; c += 64) {
+                    float x[64];
+#pragma unroll
+                    for (int u = 0; u < 64; u += 16) umma::ld16(umma::taddr(tmem, lb, L::T_W + c + u), x + u);
+                    umma::ld_wait();
+#pragma unroll
+                    for (int u = 0; u < 64; ++u) x[u] = -x[u];
+                    const uint32_t blk = st + (c < 64 ? L::ST_W0 : L::ST_W1);
+#pragma unroll
+                    for (int u = 0; u < 64; u += 16) store_row16<T>(blk, r, u, x + u);
+                }
+            }
+            umma::fence_before();
+            umma::fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sb + L::B_EPIW);
+            if (WRITE_O && lc > 0) ok = out_rows(lc - 1);
         }
+        if (WRITE_O && ok && nc > 0) out_rows(nc - 1);
     }
 
     umma::fence_before();
@@ -639,13 +650,16 @@ cudaError_t chain_ws_t(const Args &a, const WsP &p, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_chain_ws(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
-                            const void *beta, const void *A, const float *h0, const float *seg_start, void *o,
-                            float *final_state, void *h, bool h_vfirst, void *delta, cudaStream_t s) {
+                            const void *beta, const void *A, const void *P, const float *rq, const float *rk,
+                            const float *h0, const float *seg_start, void *o, float *final_state, void *h,
+                            bool h_vfirst, void *delta, cudaStream_t s) {
     WsP p;
     if (!ws_map(&p.tq, q, a, a.Hq, DK) || !ws_map(&p.tk, k, a, a.Hq, DK) || !ws_map(&p.tv, v, a, a.Hv, DV) ||
-        !ws_map(&p.ta, A, a, a.Hv, C))
+        !ws_map(&p.ta, A, a, a.Hv, C) || (o && !ws_map(&p.tp, P, a, a.Hv, C)))
         return cudaErrorInvalidValue;
     p.g_cs = g_cs;
+    p.rq = rq;
+    p.rk = rk;
     p.h0 = h0;
     p.beta = beta;
     p.o = o;

@@ -3,8 +3,11 @@
 //   wy_fwd     one CTA per (chunk, value head): chunk-local cumsum of the
 //              log-gate, L = strictly-lower(diag(beta) (K K^T o exp(G_r - G_s))),
 //              A = (I + L)^-1 (16x16 diagonal blocks by substitution in fp32,
-//              off-diagonal blocks merged with tf32 tensor-core products).
-// The recurrence and output that consume A live in chain_tc.cu.
+//              off-diagonal blocks merged with tf32 tensor-core products), and the
+//              state-independent attention block P = scale (q^ k^T o exp(G_r - G_s)),
+//              s <= r, with the inverse q/k norms the recurrence applies as factors.
+//              Without A (chunk_p) it reads G and produces P and the norms only.
+// The recurrences that consume A and P live in chain_ws.cu / chain_tc.cu.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -15,19 +18,31 @@ namespace gdr {
 // ============================================================================ wy_fwd
 
 constexpr int LDF = 68;  // fp32 row stride of the 64x64 matrices (bank spread)
-constexpr int WY_SMEM = C * DK * 2 + 2 * C * LDF * 4 + 2 * C * 4 + 4 * 16 * 20 * 4;
+constexpr int WY_SMEM = 2 * C * DK * 2 + 2 * C * LDF * 4 + 4 * C * 4 + 4 * 16 * 20 * 4;
+
+struct WyArgs {
+    const void *q, *k, *g, *beta;
+    bool gate_f32, l2norm;
+    bool full;      // compute G from g (written to g_cs) and A; else read G from g_cs, no A
+    float scale;
+    float *g_cs;
+    void *A_out;    // [tokens,Hv,64] or nullptr
+    void *P_out;    // [tokens,Hv,64]: scale (q^ k^T o Gamma), lower incl. diagonal, or nullptr
+    float *rq_out, *rk_out;  // [tokens,Hv] inverse norms (with l2norm), or nullptr
+};
 
 template <typename T>
-__global__ void __launch_bounds__(128) wy_fwd_kernel(Geo geo, const T *__restrict__ k, const void *__restrict__ g,
-                                                     const void *__restrict__ beta, bool gate_f32, bool l2norm,
-                                                     float *__restrict__ g_cs, T *__restrict__ A_out) {
+__global__ void __launch_bounds__(128) wy_fwd_kernel(Geo geo, const WyArgs w) {
     extern __shared__ __align__(1024) unsigned char smem[];
     T *sk = reinterpret_cast<T *>(smem);
-    float *Lm = reinterpret_cast<float *>(smem + C * DK * 2);
+    T *sq = reinterpret_cast<T *>(smem + C * DK * 2);
+    float *Lm = reinterpret_cast<float *>(smem + 2 * C * DK * 2);
     float *Ai = Lm + C * LDF;
     float *sG = Ai + C * LDF;
     float *sB = sG + C;
-    float *scr = sB + C;  // [4 warps][16][20]
+    float *sRQ = sB + C;
+    float *sRK = sRQ + C;
+    float *scr = sRK + C;  // [4 warps][16][20]
 
     long long tok0;
     int len, n, ci;
@@ -36,23 +51,31 @@ __global__ void __launch_bounds__(128) wy_fwd_kernel(Geo geo, const T *__restric
     const int hq = j / (Hv / Hq);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int gq = lane >> 2, tq = lane & 3;
+    const bool want_p = w.P_out != nullptr;
 
-    const Tile tk = make_tile(sk, DK);
-    load_rows_async<T>(tk, k + (tok0 * Hq + hq) * DK, (long long)Hq * DK, C, len, DK, tid, 128);
+    const Tile tk = make_tile(sk, DK), tqt = make_tile(sq, DK);
+    load_rows_async<T>(tk, static_cast<const T *>(w.k) + (tok0 * Hq + hq) * DK, (long long)Hq * DK, C, len, DK, tid,
+                       128);
+    if (want_p)
+        load_rows_async<T>(tqt, static_cast<const T *>(w.q) + (tok0 * Hq + hq) * DK, (long long)Hq * DK, C, len, DK,
+                           tid, 128);
     cp_async_commit();
     if (tid < C) {
         float gv = 0.f, bv = 0.f;
         if (tid < len) {
-            gv = load_gate<T>(g, (tok0 + tid) * Hv + j, gate_f32);
-            bv = load_gate<T>(beta, (tok0 + tid) * Hv + j, gate_f32);
+            gv = w.full ? load_gate<T>(w.g, (tok0 + tid) * Hv + j, w.gate_f32) : w.g_cs[(tok0 + tid) * Hv + j];
+            bv = load_gate<T>(w.beta, (tok0 + tid) * Hv + j, w.gate_f32);
         }
         sG[tid] = gv;
         sB[tid] = bv;
     }
     cp_async_wait<0>();
     __syncthreads();
-    if (l2norm) l2norm_rows<T>(tk, len, warp, 4, lane);
-    if (warp == 0) {
+    if (w.l2norm) {
+        l2norm_rows<T>(tk, len, warp, 4, lane, sRK);
+        if (want_p) l2norm_rows<T>(tqt, len, warp, 4, lane, sRQ);
+    }
+    if (w.full && warp == 0) {
         float x0 = sG[lane], x1 = sG[lane + 32];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -66,20 +89,157 @@ __global__ void __launch_bounds__(128) wy_fwd_kernel(Geo geo, const T *__restric
         x1 += __shfl_sync(0xffffffffu, x0, 31);
         sG[lane] = x0;
         sG[lane + 32] = x1;
-        if (lane < len) g_cs[(tok0 + lane) * Hv + j] = x0;
-        if (lane + 32 < len) g_cs[(tok0 + lane + 32) * Hv + j] = x1;
+        if (lane < len) w.g_cs[(tok0 + lane) * Hv + j] = x0;
+        if (lane + 32 < len) w.g_cs[(tok0 + lane + 32) * Hv + j] = x1;
     }
     __syncthreads();
+    if (w.l2norm && tid < len) {
+        if (w.rk_out) w.rk_out[(tok0 + tid) * Hv + j] = sRK[tid];
+        if (w.rq_out && want_p) w.rq_out[(tok0 + tid) * Hv + j] = sRQ[tid];
+    }
 
-    // ---- L (warp w owns rows 16w..16w+15; only column tiles at or left of the diagonal)
-    {
+    if (w.A_out) {
+        // ---- L (warp w owns rows 16w..16w+15; only column tiles at or left of the diagonal)
+        {
+            float acc[8][4];
+            zero_acc<8>(acc);
+            const int r0 = warp * 16;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                uint32_t a[4];
+                load_a(a, tk, r0, ks * 16, false, lane);
+#pragma unroll
+                for (int np = 0; np < 4; ++np) {
+                    if (np <= warp) {
+                        uint32_t b[4];
+                        load_b2(b, tk, np * 16, ks * 16, false, lane);
+                        mma16816<T>(acc[2 * np], a, b[0], b[1]);
+                        mma16816<T>(acc[2 * np + 1], a, b[2], b[3]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int r = r0 + gq + 8 * hh;
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int s = nt * 8 + tq * 2 + e;
+                        float val = 0.f;
+                        if (s < r && r < len) val = sB[r] * __expf(sG[r] - sG[s]) * acc[nt][2 * hh + e];
+                        Lm[r * LDF + s] = val;
+                    }
+                }
+        }
+        __syncthreads();
+
+        // ---- diagonal 16x16 blocks: warp w, lane c < 16 solves column c of (I + L_ww)^-1
+        if (lane < 16) {
+            const int b0 = warp * 16;
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float acc = 0.f;
+#pragma unroll
+                for (int s = 0; s < i; ++s) acc += Lm[(b0 + i) * LDF + b0 + s] * x[s];
+                x[i] = (i == lane) ? 1.f : (i > lane ? -acc : 0.f);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Ai[(b0 + i) * LDF + b0 + lane] = x[i];
+        }
+        __syncthreads();
+
+        // ---- off-diagonal blocks, one block row at a time:
+        //      A_ij = -A_ii * sum_{k=j}^{i-1} L_ik A_kj
+        float *ws = scr + warp * 16 * 20;
+        for (int bi = 1; bi < 4; ++bi) {
+            if (warp < bi) {
+                const int bj = warp;
+                float r[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                for (int kb = bj; kb < bi; ++kb) {
+#pragma unroll
+                    for (int k8 = 0; k8 < 2; ++k8) {
+                        const int kc = kb * 16 + k8 * 8;
+                        uint32_t a[4];
+                        a[0] = to_tf32(Lm[(bi * 16 + gq) * LDF + kc + tq]);
+                        a[1] = to_tf32(Lm[(bi * 16 + gq + 8) * LDF + kc + tq]);
+                        a[2] = to_tf32(Lm[(bi * 16 + gq) * LDF + kc + tq + 4]);
+                        a[3] = to_tf32(Lm[(bi * 16 + gq + 8) * LDF + kc + tq + 4]);
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            const uint32_t b0 = to_tf32(Ai[(kc + tq) * LDF + bj * 16 + nt * 8 + gq]);
+                            const uint32_t b1 = to_tf32(Ai[(kc + tq + 4) * LDF + bj * 16 + nt * 8 + gq]);
+                            mma1688_tf32(r[nt], a, b0, b1);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    ws[gq * 20 + nt * 8 + tq * 2] = r[nt][0];
+                    ws[gq * 20 + nt * 8 + tq * 2 + 1] = r[nt][1];
+                    ws[(gq + 8) * 20 + nt * 8 + tq * 2] = r[nt][2];
+                    ws[(gq + 8) * 20 + nt * 8 + tq * 2 + 1] = r[nt][3];
+                }
+                __syncwarp();
+                float o[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int k8 = 0; k8 < 2; ++k8) {
+                    const int kc = bi * 16 + k8 * 8;
+                    uint32_t a[4];
+                    a[0] = to_tf32(Ai[(bi * 16 + gq) * LDF + kc + tq]);
+                    a[1] = to_tf32(Ai[(bi * 16 + gq + 8) * LDF + kc + tq]);
+                    a[2] = to_tf32(Ai[(bi * 16 + gq) * LDF + kc + tq + 4]);
+                    a[3] = to_tf32(Ai[(bi * 16 + gq + 8) * LDF + kc + tq + 4]);
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const uint32_t b0 = to_tf32(ws[(k8 * 8 + tq) * 20 + nt * 8 + gq]);
+                        const uint32_t b1 = to_tf32(ws[(k8 * 8 + tq + 4) * 20 + nt * 8 + gq]);
+                        mma1688_tf32(o[nt], a, b0, b1);
+                    }
+                }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int c = bj * 16 + nt * 8 + tq * 2;
+                    Ai[(bi * 16 + gq) * LDF + c] = -o[nt][0];
+                    Ai[(bi * 16 + gq) * LDF + c + 1] = -o[nt][1];
+                    Ai[(bi * 16 + gq + 8) * LDF + c] = -o[nt][2];
+                    Ai[(bi * 16 + gq + 8) * LDF + c + 1] = -o[nt][3];
+                }
+                __syncwarp();
+            }
+            __syncthreads();
+        }
+
+        // ---- A out: row r of the chunk at token tok0 + r, zero above the diagonal
+        for (int i = tid; i < C * 8; i += 128) {
+            const int r = i >> 3, c0 = (i & 7) * 8;
+            if (r >= len) continue;
+            uint32_t wv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int c = c0 + 2 * e;
+                const float lo = (c <= r) ? Ai[r * LDF + c] : 0.f;
+                const float hi = (c + 1 <= r) ? Ai[r * LDF + c + 1] : 0.f;
+                wv[e] = Elt<T>::pack(lo, hi);
+            }
+            *reinterpret_cast<uint4 *>(static_cast<T *>(w.A_out) + ((tok0 + r) * Hv + j) * C + c0) =
+                make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+    }
+
+    // ---- P = scale (q^ k^T o exp(G_r - G_s)) for s <= r < len (warp w owns rows 16w..16w+15), staged
+    //      as bf16/fp16 rows in the dead L buffer, then stored row by row
+    if (want_p) {
+        __syncthreads();
+        T *sp = reinterpret_cast<T *>(Lm);  // [64][64]
         float acc[8][4];
         zero_acc<8>(acc);
         const int r0 = warp * 16;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             uint32_t a[4];
-            load_a(a, tk, r0, ks * 16, false, lane);
+            load_a(a, tqt, r0, ks * 16, false, lane);
 #pragma unroll
             for (int np = 0; np < 4; ++np) {
                 if (np <= warp) {
@@ -94,129 +254,71 @@ __global__ void __launch_bounds__(128) wy_fwd_kernel(Geo geo, const T *__restric
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                const int r = r0 + gq + 8 * hh;
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int s = nt * 8 + tq * 2 + e;
-                    float val = 0.f;
-                    if (s < r && r < len) val = sB[r] * __expf(sG[r] - sG[s]) * acc[nt][2 * hh + e];
-                    Lm[r * LDF + s] = val;
-                }
+                const int r = r0 + gq + 8 * hh, s0 = nt * 8 + tq * 2;
+                const float v0 = (s0 <= r && r < len) ? w.scale * __expf(sG[r] - sG[s0]) * acc[nt][2 * hh] : 0.f;
+                const float v1 =
+                    (s0 + 1 <= r && r < len) ? w.scale * __expf(sG[r] - sG[s0 + 1]) * acc[nt][2 * hh + 1] : 0.f;
+                *reinterpret_cast<uint32_t *>(sp + r * C + s0) = Elt<T>::pack(v0, v1);
             }
-    }
-    __syncthreads();
-
-    // ---- diagonal 16x16 blocks: warp w, lane c < 16 solves column c of (I + L_ww)^-1
-    if (lane < 16) {
-        const int b0 = warp * 16;
-        float x[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float acc = 0.f;
-#pragma unroll
-            for (int s = 0; s < i; ++s) acc += Lm[(b0 + i) * LDF + b0 + s] * x[s];
-            x[i] = (i == lane) ? 1.f : (i > lane ? -acc : 0.f);
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) Ai[(b0 + i) * LDF + b0 + lane] = x[i];
-    }
-    __syncthreads();
-
-    // ---- off-diagonal blocks, one block row at a time:
-    //      A_ij = -A_ii * sum_{k=j}^{i-1} L_ik A_kj
-    float *ws = scr + warp * 16 * 20;
-    for (int bi = 1; bi < 4; ++bi) {
-        if (warp < bi) {
-            const int bj = warp;
-            float r[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            for (int kb = bj; kb < bi; ++kb) {
-#pragma unroll
-                for (int k8 = 0; k8 < 2; ++k8) {
-                    const int kc = kb * 16 + k8 * 8;
-                    uint32_t a[4];
-                    a[0] = to_tf32(Lm[(bi * 16 + gq) * LDF + kc + tq]);
-                    a[1] = to_tf32(Lm[(bi * 16 + gq + 8) * LDF + kc + tq]);
-                    a[2] = to_tf32(Lm[(bi * 16 + gq) * LDF + kc + tq + 4]);
-                    a[3] = to_tf32(Lm[(bi * 16 + gq + 8) * LDF + kc + tq + 4]);
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt) {
-                        const uint32_t b0 = to_tf32(Ai[(kc + tq) * LDF + bj * 16 + nt * 8 + gq]);
-                        const uint32_t b1 = to_tf32(Ai[(kc + tq + 4) * LDF + bj * 16 + nt * 8 + gq]);
-                        mma1688_tf32(r[nt], a, b0, b1);
-                    }
-                }
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                ws[gq * 20 + nt * 8 + tq * 2] = r[nt][0];
-                ws[gq * 20 + nt * 8 + tq * 2 + 1] = r[nt][1];
-                ws[(gq + 8) * 20 + nt * 8 + tq * 2] = r[nt][2];
-                ws[(gq + 8) * 20 + nt * 8 + tq * 2 + 1] = r[nt][3];
-            }
-            __syncwarp();
-            float o[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-            for (int k8 = 0; k8 < 2; ++k8) {
-                const int kc = bi * 16 + k8 * 8;
-                uint32_t a[4];
-                a[0] = to_tf32(Ai[(bi * 16 + gq) * LDF + kc + tq]);
-                a[1] = to_tf32(Ai[(bi * 16 + gq + 8) * LDF + kc + tq]);
-                a[2] = to_tf32(Ai[(bi * 16 + gq) * LDF + kc + tq + 4]);
-                a[3] = to_tf32(Ai[(bi * 16 + gq + 8) * LDF + kc + tq + 4]);
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const uint32_t b0 = to_tf32(ws[(k8 * 8 + tq) * 20 + nt * 8 + gq]);
-                    const uint32_t b1 = to_tf32(ws[(k8 * 8 + tq + 4) * 20 + nt * 8 + gq]);
-                    mma1688_tf32(o[nt], a, b0, b1);
-                }
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int c = bj * 16 + nt * 8 + tq * 2;
-                Ai[(bi * 16 + gq) * LDF + c] = -o[nt][0];
-                Ai[(bi * 16 + gq) * LDF + c + 1] = -o[nt][1];
-                Ai[(bi * 16 + gq + 8) * LDF + c] = -o[nt][2];
-                Ai[(bi * 16 + gq + 8) * LDF + c + 1] = -o[nt][3];
-            }
-            __syncwarp();
-        }
         __syncthreads();
-    }
-
-    // ---- A out: row r of the chunk at token tok0 + r, zero above the diagonal
-    for (int i = tid; i < C * 8; i += 128) {
-        const int r = i >> 3, c0 = (i & 7) * 8;
-        if (r >= len) continue;
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int c = c0 + 2 * e;
-            const float lo = (c <= r) ? Ai[r * LDF + c] : 0.f;
-            const float hi = (c + 1 <= r) ? Ai[r * LDF + c + 1] : 0.f;
-            w[e] = Elt<T>::pack(lo, hi);
+        for (int i = tid; i < C * 8; i += 128) {
+            const int r = i >> 3, c0 = (i & 7) * 8;
+            if (r >= len) continue;
+            *reinterpret_cast<uint4 *>(static_cast<T *>(w.P_out) + ((tok0 + r) * Hv + j) * C + c0) =
+                *reinterpret_cast<const uint4 *>(sp + r * C + c0);
         }
-        *reinterpret_cast<uint4 *>(A_out + ((tok0 + r) * Hv + j) * C + c0) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
 // ============================================================================ launchers
 
 template <typename T>
-static cudaError_t wy_fwd_t(const Args &a, const void *k, const void *g, const void *beta, float *g_cs, void *A,
-                            cudaStream_t s) {
+static cudaError_t wy_fwd_t(const Args &a, const WyArgs &w, cudaStream_t s) {
     if (a.max_chunks == 0) return cudaSuccess;
     auto kern = wy_fwd_kernel<T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, WY_SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)a.max_chunks, a.Hv);
-    kern<<<grid, 128, WY_SMEM, s>>>(make_geo(a), static_cast<const T *>(k), g, beta, a.gate_f32, a.l2norm, g_cs,
-                                    static_cast<T *>(A));
+    kern<<<grid, 128, WY_SMEM, s>>>(make_geo(a), w);
     return cudaGetLastError();
 }
 
-cudaError_t launch_wy_fwd(const Args &a, const void *k, const void *g, const void *beta, float *g_cs, void *A,
-                          cudaStream_t s) {
-    return a.bf16 ? wy_fwd_t<__nv_bfloat16>(a, k, g, beta, g_cs, A, s) : wy_fwd_t<__half>(a, k, g, beta, g_cs, A, s);
+cudaError_t launch_wy_fwd(const Args &a, const void *q, const void *k, const void *g, const void *beta, float *g_cs,
+                          void *A, void *P, float *rq, float *rk, cudaStream_t s) {
+    WyArgs w;
+    w.q = q;
+    w.k = k;
+    w.g = g;
+    w.beta = beta;
+    w.gate_f32 = a.gate_f32;
+    w.l2norm = a.l2norm;
+    w.full = true;
+    w.scale = a.scale;
+    w.g_cs = g_cs;
+    w.A_out = A;
+    w.P_out = P;
+    w.rq_out = rq;
+    w.rk_out = rk;
+    return a.bf16 ? wy_fwd_t<__nv_bfloat16>(a, w, s) : wy_fwd_t<__half>(a, w, s);
+}
+
+cudaError_t launch_chunk_p(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta, void *P,
+                           float *rq, float *rk, cudaStream_t s) {
+    WyArgs w;
+    w.q = q;
+    w.k = k;
+    w.g = nullptr;
+    w.beta = beta;
+    w.gate_f32 = a.gate_f32;
+    w.l2norm = a.l2norm;
+    w.full = false;
+    w.scale = a.scale;
+    w.g_cs = const_cast<float *>(g_cs);
+    w.A_out = nullptr;
+    w.P_out = P;
+    w.rq_out = rq;
+    w.rk_out = rk;
+    return a.bf16 ? wy_fwd_t<__nv_bfloat16>(a, w, s) : wy_fwd_t<__half>(a, w, s);
 }
 
 }  // namespace gdr

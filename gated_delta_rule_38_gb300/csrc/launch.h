@@ -34,9 +34,14 @@ struct SegWs {
 cudaError_t launch_prep_chunks(const int32_t *cu, int N, int T, int chunk, int32_t *idx, int64_t max_chunks,
                                int32_t *off, int32_t *total, unsigned *err, cudaStream_t s);
 
-// Forward: per-chunk gate cumsum and WY matrix.
-cudaError_t launch_wy_fwd(const Args &a, const void *k, const void *g, const void *beta, float *g_cs,
-                          void *A, cudaStream_t s);
+// Forward: per-chunk gate cumsum, WY matrix A and (P != nullptr) the decayed causal attention block
+// P = scale (q^ k^T o Gamma) [tokens,Hv,64] with the inverse q/k norms rq, rk [tokens,Hv] (written only
+// with in-kernel L2 normalisation).
+cudaError_t launch_wy_fwd(const Args &a, const void *q, const void *k, const void *g, const void *beta, float *g_cs,
+                          void *A, void *P, float *rq, float *rk, cudaStream_t s);
+// The same P, rq, rk from a given g_cumsum (no A).
+cudaError_t launch_chunk_p(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta, void *P,
+                           float *rq, float *rk, cudaStream_t s);
 // Forward recurrence + output (o != nullptr) and/or per-chunk states (h != nullptr)
 // and per-chunk Delta = U - W h (delta != nullptr).
 cudaError_t launch_chain_fwd(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
@@ -45,9 +50,12 @@ cudaError_t launch_chain_fwd(const Args &a, const void *q, const void *k, const 
 // Forward recurrence, warp-specialised (one CTA per value-column slice); no sequence split.
 // o != nullptr: output rows; h: state before every chunk ([rows,Hv,K,V], or [..,V,K] when
 // h_vfirst); delta: Delta of every chunk; seg_start: transposed fp32 start states replacing h0.
+// P, rq, rk: from launch_wy_fwd / launch_chunk_p (P is read only when o != nullptr; rq, rk only with
+// in-kernel L2 normalisation).
 cudaError_t launch_chain_ws(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
-                            const void *beta, const void *A, const float *h0, const float *seg_start, void *o,
-                            float *final_state, void *h, bool h_vfirst, void *delta, cudaStream_t s);
+                            const void *beta, const void *A, const void *P, const float *rq, const float *rk,
+                            const float *h0, const float *seg_start, void *o, float *final_state, void *h,
+                            bool h_vfirst, void *delta, cudaStream_t s);
 // Backward: reverse state-gradient chain (dH' and dDelta of every chunk, dh0).
 cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
                              const void *A, const void *dout, const float *dht, void *dhn, void *ddelta, float *dh0,

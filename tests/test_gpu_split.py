@@ -50,7 +50,9 @@ def test_split_matches_unsplit():
     o1 = gpu_fwd(w, x, False, num_segments=1)[2]
     o4 = gpu_fwd(w, x, False, num_segments=4)[2]
     torch.cuda.synchronize()
-    assert rel_l2(np64(o4), np64(o1)) < 2e-3
+    # the unsplit forward and the split forward are different kernels (different rounding points), each
+    # within TOL of the oracle; they agree to within that same bound
+    assert rel_l2(np64(o4), np64(o1)) < TOL
 
 
 def test_split_state_v_first_bit_exact():
