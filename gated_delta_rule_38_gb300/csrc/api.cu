@@ -221,6 +221,16 @@ Layout layout_of(const gdr_problem *p, bool bwd) {
         at = round_up(at + dsz, 256);
         L.ddelta = at;
         at = round_up(at + dsz, 256);
+        if (L.nseg == 1) {
+            L.P = at;
+            at = round_up(at + tok * p->Hv * C * esize(p->dtype), 256);
+            if (p->flags & GDR_L2NORM_QK) {
+                L.rq = at;
+                at = round_up(at + tok * p->Hv * sizeof(float), 256);
+                L.rk = at;
+                at = round_up(at + tok * p->Hv * sizeof(float), 256);
+            }
+        }
     }
     if (L.nseg > 1) {
         const size_t sz = (size_t)num_seqs(p) * p->Hv * L.nseg * DK * DV * sizeof(float);
@@ -272,10 +282,11 @@ gdr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_E
 
 // ---- per-kernel timing: event pairs recorded around each launch while enabled
 enum KernelId {
-    K_PREP = 0, K_WY_FWD, K_CHAIN_FWD, K_CHAIN_FWD_RECOMPUTE, K_CHAIN_BWD, K_CHAIN_PAIR, K_BWD_CHUNK, K_COUNT
+    K_PREP = 0, K_WY_FWD, K_CHAIN_FWD, K_CHAIN_FWD_RECOMPUTE, K_CHAIN_BWD, K_CHAIN_PAIR, K_BWD_CHUNK, K_CHUNK_P,
+    K_COUNT
 };
 const char *const kKernelNames[K_COUNT] = {"prep_chunks", "wy_fwd",     "chain_fwd", "chain_fwd_recompute",
-                                           "chain_bwd",   "chain_pair", "bwd_chunk"};
+                                           "chain_bwd",   "chain_pair", "bwd_chunk", "chunk_p"};
 struct Pending {
     int id;
     cudaEvent_t a, b;
@@ -438,8 +449,15 @@ gdr_status gdr_bwd(const gdr_problem *p, const void *q, const void *k, const voi
     // chunk's gradients in parallel
     const SegWs sw = seg_ws(L, ws);
     if (sw.nseg == 1) {
+        void *Pw = ws + L.P;
+        float *rqw = a.l2norm ? reinterpret_cast<float *>(ws + L.rq) : nullptr;
+        float *rkw = a.l2norm ? reinterpret_cast<float *>(ws + L.rk) : nullptr;
+        if ((st = timed(K_CHUNK_P, s, [&] { return launch_chunk_p(a, q, k, g_cumsum, beta, Pw, rqw, rkw, s); })) !=
+            GDR_OK)
+            return st;
         if ((st = timed(K_CHAIN_PAIR, s, [&] {
-                 return launch_chain_pair(a, q, k, v, g_cumsum, beta, A, h0, hw, dlw, dout, dht, dhw, ddlw, dh0, s);
+                 return launch_chain_ws_pair(a, q, k, v, g_cumsum, beta, A, Pw, rqw, rkw, h0, hw, dlw, dout, dht, dhw,
+                                             ddlw, dh0, s);
              })) != GDR_OK)
             return st;
     } else if ((st = timed(K_CHAIN_FWD_RECOMPUTE, s, [&] {

@@ -52,19 +52,24 @@ constexpr long kWaitPolls = 40000000L;
 // factor arrays (64 floats each), four sets (chunk index mod 4)
 enum { FG = 0, FRQ, FRK, FB, FCQ, FCK, FAKG, FAB, NF };
 
-template <int BV>
+template <int BV, bool WRITE_O = true>
 struct Lay {
-    // stage: [-W b0 | Q~ b0 | -W b1 | Q~ b1 | K b0 | K b1 | V | A | P], 8 KB blocks of 64 rows x 128 B
-    // ([-W; Q~] is one K-major 128-row operand per key half, [A; P] one 128-row operand)
-    static constexpr uint32_t ST_W0 = 0, ST_Q0 = 8192, ST_W1 = 16384, ST_Q1 = 24576, ST_K0 = 32768,
-                              ST_V = 49152, ST_A = ST_V + BV * 128, ST_P = ST_A + 8192, ST_BYTES = ST_P + 8192;
+    // stage, 8 KB blocks of 64 rows x 128 B:
+    //   with the output: [-W b0 | Q~ b0 | -W b1 | Q~ b1 | K b0 | K b1 | V | A | P]
+    //   without it:      [-W b0 | K b0 | -W b1 | K b1 | V | A]      (K doubles as the idle rows of round A)
+    // ([-W; Q~] (or [-W; K]) is one K-major 128-row operand per key half, [A; P] one 128-row operand)
+    static constexpr uint32_t ST_W0 = 0, ST_Q0 = 8192, ST_W1 = 16384, ST_Q1 = 24576;
+    static constexpr uint32_t ST_K0 = WRITE_O ? 32768 : 8192, ST_K1 = WRITE_O ? 40960 : 24576;
+    static constexpr uint32_t LBO_K = ST_K1 - ST_K0;
+    static constexpr uint32_t ST_V = WRITE_O ? 49152 : 32768, ST_A = ST_V + BV * 128, ST_P = ST_A + 8192;
+    static constexpr uint32_t ST_BYTES = WRITE_O ? ST_P + 8192 : ST_A + 8192;
     static constexpr uint32_t AB = 2 * ST_BYTES;  // [A diag(beta) ; 0] and [0 ; A diag(beta e^G rk)]
     static constexpr uint32_t Z = AB + 8192;
     static constexpr uint32_t AKG = Z + 8192;
-    static constexpr uint32_t DL = AKG + 8192;      // Delta [64 s][BV]: BV/64 blocks of 8 KB
-    static constexpr uint32_t DT = DL + BV * 128;   // diag(rk e^{Gl-G}) Delta
-    static constexpr uint32_t H = DT + BV * 128;    // h [128 d][BV]: BV/64 blocks of 16 KB
-    static constexpr uint32_t F = H + BV * 256;     // factor sets (4, by chunk index mod 4)
+    static constexpr uint32_t DT = AKG + 8192;                    // diag(rk e^{Gl-G}) Delta [64 s][BV]
+    static constexpr uint32_t DL = WRITE_O ? DT + BV * 128 : DT;  // Delta (output product only)
+    static constexpr uint32_t H = DL + BV * 128;                  // h [128 d][BV]: BV/64 blocks of 16 KB
+    static constexpr uint32_t F = H + BV * 256;                   // factor sets (4, by chunk index mod 4)
     static constexpr uint32_t BAR = F + 4 * NF * 256;
     // barriers
     static constexpr uint32_t B_FULL = BAR, B_EMPTY = BAR + 16, B_PREP = BAR + 32, B_EPIW = BAR + 40,
@@ -76,7 +81,8 @@ struct Lay {
     // TMEM columns
     static constexpr uint32_t T_W = 0, T_D0 = 128, T_D1 = 128 + BV, T_X = 128 + 2 * BV;
 };
-static_assert(Lay<64>::BYTES <= 232448, "shared memory");
+static_assert(Lay<64>::BYTES <= 232448 && Lay<128, false>::BYTES <= 232448, "shared memory");
+static_assert(Lay<128, false>::T_X + 128 <= 512, "tensor memory");
 
 struct WsP {
     CUtensorMap tq, tk, tv, tp, ta;  // [tokens][heads][cols] maps, boxes 64 x 1 x 64
@@ -172,13 +178,12 @@ __device__ __forceinline__ uint16_t to_bits(float x) {
 }
 
 template <typename T, int BV, bool WRITE_O>
-__global__ void __launch_bounds__(WS_NT, 1) chain_ws_kernel(Geo geo, const __grid_constant__ WsP p) {
-    using L = Lay<BV>;
+__device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const int vh, const int j, const int n) {
+    using L = Lay<BV, WRITE_O>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
-    const int vh = blockIdx.x, j = blockIdx.y, n = blockIdx.z;
     const int v0 = vh * BV;
     const int Hv = geo.Hv, Hq = geo.Hq, hq = j / (Hv / Hq);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -237,7 +242,7 @@ __global__ void __launch_bounds__(WS_NT, 1) chain_ws_kernel(Geo geo, const __gri
                     tma::load3d(st + L::ST_P, &p.tp, 0, j, t, full);
                 }
                 tma::load3d(st + L::ST_K0, &p.tk, 0, hq, t, full);
-                tma::load3d(st + L::ST_K0 + 8192, &p.tk, 64, hq, t, full);
+                tma::load3d(st + L::ST_K1, &p.tk, 64, hq, t, full);
                 tma::load3d(st + L::ST_V, &p.tv, v0, j, t, full);
                 if (BV == 128) tma::load3d(st + L::ST_V + 8192, &p.tv, v0 + 64, j, t, full);
                 tma::load3d(st + L::ST_A, &p.ta, 0, j, t, full);
@@ -258,7 +263,7 @@ __global__ void __launch_bounds__(WS_NT, 1) chain_ws_kernel(Geo geo, const __gri
             const uint64_t dDL = umma::desc(sb + L::DL, 8192, 1024), dDT = umma::desc(sb + L::DT, 8192, 1024);
             auto issue_w = [&](int lc) {  // W of chunk lc
                 const uint32_t st = sb + (lc & 1) * L::ST_BYTES;
-                const uint64_t bk = umma::desc(st + L::ST_K0, 8192, 1024);
+                const uint64_t bk = umma::desc(st + L::ST_K0, L::LBO_K, 1024);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + L::T_W, dZAKG + ks * 2, bk + ks * 128, id_w, ks > 0);
             };
@@ -305,7 +310,7 @@ __global__ void __launch_bounds__(WS_NT, 1) chain_ws_kernel(Geo geo, const __gri
                 for (long it = 0; !(b_done && w_done && u_done); ++it) {
                     if (!b_done && mbar_test(sb + L::B_EPIA, lc & 1)) {
                         umma::fence_after();
-                        const uint64_t akt = umma::desc(st + L::ST_K0, 8192, 1024);
+                        const uint64_t akt = umma::desc(st + L::ST_K0, L::LBO_K, 1024);
                         const uint64_t ap = umma::desc(st + L::ST_A, 16, 1024);
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks) {
@@ -520,14 +525,17 @@ __global__ void __launch_bounds__(WS_NT, 1) chain_ws_kernel(Geo geo, const __gri
                 umma::fence_after();
                 const int sr = d;
                 const float ck = fa(lc, FCK)[sr];
-                float xa[HW];
+                constexpr int NB = HW < 32 ? HW : 32;  // columns per TMEM load batch
 #pragma unroll
-                for (int i = 0; i < HW; i += 16) umma::ld16(umma::taddr(tmem, q4 * 32, tD + cb0 + i), xa + i);
+                for (int i0 = 0; i0 < HW; i0 += NB) {
+                float xa[NB];
+#pragma unroll
+                for (int i = 0; i < NB; i += 16) umma::ld16(umma::taddr(tmem, q4 * 32, tD + cb0 + i0 + i), xa + i);
                 umma::ld_wait();
 #pragma unroll
-                for (int i = 0; i < HW; i += 16) {
+                for (int i = 0; i < NB; i += 16) {
                     float *x = xa + i, y[16];
-                    const int col = cb0 + i;
+                    const int col = cb0 + i0 + i;
 #pragma unroll
                     for (int u = 0; u < 16; ++u) y[u] = x[u] * ck;
                     if (WRITE_O) store_row16<T>(sb + L::DL + (col >> 6) * 8192, sr, col & 63, x);
@@ -542,6 +550,7 @@ __global__ void __launch_bounds__(WS_NT, 1) chain_ws_kernel(Geo geo, const __gri
                                        Elt<T>::pack(x[12], x[13]), Elt<T>::pack(x[14], x[15]));
                     }
                 }
+                }
                 umma::fence_before();
                 umma::fence_async_smem();
                 __syncwarp();
@@ -550,12 +559,16 @@ __global__ void __launch_bounds__(WS_NT, 1) chain_ws_kernel(Geo geo, const __gri
             if (!warp_wait(sb + L::B_MB, lc & 1, flag, geo.err, lane)) break;
             umma::fence_after();
             {
-                float xb[HW];
+                constexpr int NB = HW < 32 ? HW : 32;
 #pragma unroll
-                for (int i = 0; i < HW; i += 16) umma::ld16(umma::taddr(tmem, q4 * 32, L::T_X + cb0 + i), xb + i);
-                umma::ld_wait();
+                for (int i0 = 0; i0 < HW; i0 += NB) {
+                    float xb[NB];
 #pragma unroll
-                for (int i = 0; i < HW; ++i) hS[i] = fmaf(egl, hS[i], xb[i]);
+                    for (int i = 0; i < NB; i += 16) umma::ld16(umma::taddr(tmem, q4 * 32, L::T_X + cb0 + i0 + i), xb + i);
+                    umma::ld_wait();
+#pragma unroll
+                    for (int i = 0; i < NB; ++i) hS[i0 + i] = fmaf(egl, hS[i0 + i], xb[i]);
+                }
             }
             umma::fence_before();
             write_h();
@@ -631,6 +644,435 @@ __global__ void __launch_bounds__(WS_NT, 1) chain_ws_kernel(Geo geo, const __gri
     if (warp == 0) umma::dealloc(tmem, 512);
 }
 
+template <typename T, int BV, bool WRITE_O>
+__global__ void __launch_bounds__(WS_NT, 1) chain_ws_kernel(Geo geo, const __grid_constant__ WsP p) {
+    ws_fwd_body<T, BV, WRITE_O>(geo, p, blockIdx.x, blockIdx.y, blockIdx.z);
+}
+
+// ============================================================================ reverse chain
+//
+// The gradient of the state, dh [K x V], runs the chunks backwards; its value columns are independent,
+// so one CTA of 512 threads owns one (sequence, value head) with all 128 columns (the warp roles of the
+// forward).  With dh' the gradient after chunk c, P = scale (q^ k^T o Gamma) (lower), Q~ = diag(scale rq e^G) Q
+// and W = A diag(beta e^G rk) K:
+//
+//   dDelta = diag(rk e^{Gl-G}) (K dh') + P^T dO                     [64 x V]
+//   dh     = e^{Gl} dh' + Q~^T dO - W^T dDelta                        [K x V]
+//
+//   state-independent:  P^T dO -> T_P, Q~^T dO -> T_Y (the base of round B), W -> T_W (the -W epilogue)
+//   round A:  E = [K ; .] dh'                  (lanes 0..63)           M=128, N=128, K=128
+//   round B:  T_Y += (-W)^T dDelta                                     M=128, N=128, K=64
+// It stores dh' of every chunk (the gradient after the chunk) and dDelta for the per-chunk gradients;
+// the last dh is dh0.
+
+struct RLay {
+    // stage: [Q~ b0 | Q~ b1 | K b0 | K b1 | dO b0 | dO b1 | A | P], 8 KB blocks of 64 rows x 128 B
+    static constexpr uint32_t ST_Q0 = 0, ST_K0 = 16384, ST_DO = 32768, ST_A = 49152, ST_P = 57344,
+                              ST_BYTES = 65536;
+    static constexpr uint32_t WS = 2 * ST_BYTES;  // -W [64 s][128 d]: two 8 KB blocks (one buffer)
+    static constexpr uint32_t Z = WS + 16384;     // zeros, then A diag(beta e^G rk): [0 ; A diag(..)]
+    static constexpr uint32_t AKG = Z + 8192;
+    static constexpr uint32_t DL = AKG + 8192;    // dDelta [64 s][128]: two 8 KB blocks
+    static constexpr uint32_t H = DL + 16384;     // dh' [128 d][128]: two 16 KB blocks
+    static constexpr uint32_t F = H + 32768;
+    static constexpr uint32_t BAR = F + 4 * NF * 256;
+    static constexpr uint32_t B_FULL = BAR, B_EMPTY = BAR + 16, B_PREP = BAR + 32, B_EPIW = BAR + 40,
+                              B_MPW = BAR + 48, B_MA = BAR + 56, B_EPIA = BAR + 64, B_MB = BAR + 72,
+                              B_EPIB = BAR + 80, B_DONE = BAR + 88;
+    static constexpr uint32_t SLOT = BAR + 96, FLAG = SLOT + 4, USED = FLAG + 12;
+    static constexpr uint32_t BYTES = USED + 1024;
+    static constexpr uint32_t T_W = 0, T_E = 128, T_P = 256, T_Y = 384;
+};
+static_assert(RLay::BYTES <= 232448, "shared memory");
+
+struct RevP {
+    CUtensorMap tq, tk, tdo, tp, ta;  // [tokens][heads][cols] maps, boxes 64 x 1 x 64
+    const float *g_cs, *rq, *rk, *dht;
+    const void *beta;
+    void *dhn;     // [rows,Hv,K,V]: the gradient after every chunk
+    void *ddelta;  // [rows,Hv,64,V]
+    float *dh0;
+    bool gate_f32, l2norm, v_first;
+    float scale;
+};
+
+template <typename T>
+__device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const int j, const int n) {
+    using L = RLay;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem =
+        reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    const int Hv = geo.Hv, Hq = geo.Hq, hq = j / (Hv / Hq);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr bool bf16 = IsBf16<T>::value;
+    long long tok0;
+    int len, row0;
+    geo.seq(n, tok0, len, row0);
+    const int nc = (len + C - 1) / C;
+    auto chunk_of = [&](int lc) { return nc - 1 - lc; };
+    volatile int *flag = reinterpret_cast<volatile int *>(smem + L::FLAG);
+    float *F = reinterpret_cast<float *>(smem + L::F);
+    auto fa = [&](int lc, int which) -> float * { return F + ((lc & 3) * NF + which) * 64; };
+
+    if (tid == 0) {
+        umma::mbar_init(sb + L::B_FULL, 1);
+        umma::mbar_init(sb + L::B_FULL + 8, 1);
+        umma::mbar_init(sb + L::B_EMPTY, 1);
+        umma::mbar_init(sb + L::B_EMPTY + 8, 1);
+        umma::mbar_init(sb + L::B_PREP, 4);
+        umma::mbar_init(sb + L::B_EPIW, 2);
+        umma::mbar_init(sb + L::B_MPW, 1);
+        umma::mbar_init(sb + L::B_MA, 2);  // the commit, and the issuing thread's own arrival
+        umma::mbar_init(sb + L::B_EPIA, 4);
+        umma::mbar_init(sb + L::B_MB, 1);
+        umma::mbar_init(sb + L::B_EPIB, 8);
+        umma::mbar_init(sb + L::B_DONE, 1);
+        umma::fence_mbar_init();
+        *flag = 0;
+    }
+    for (int i = tid; i < 8192 / 16; i += WS_NT) st_v4(sb + L::Z + i * 16, 0u, 0u, 0u, 0u);
+    umma::fence_async_smem();
+    if (warp == 0) umma::alloc(sb + L::SLOT, 512);
+    umma::fence_before();
+    __syncthreads();
+    umma::fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::SLOT);
+
+    if (warp == 1) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int issued[2] = {0, 0};
+            for (int lc = 0; lc < nc && !*flag; ++lc) {
+                const int s = lc & 1;
+                if (lc >= 2 && !wait_phase(sb + L::B_EMPTY + 8 * s, ((lc >> 1) - 1) & 1, flag, geo.err)) break;
+                const uint32_t st = sb + s * L::ST_BYTES, full = sb + L::B_FULL + 8 * s;
+                const int t = (int)(tok0 + (long long)chunk_of(lc) * C);
+                tma::expect_tx(full, 65536u);
+                tma::load3d(st + L::ST_Q0, &p.tq, 0, hq, t, full);
+                tma::load3d(st + L::ST_Q0 + 8192, &p.tq, 64, hq, t, full);
+                tma::load3d(st + L::ST_K0, &p.tk, 0, hq, t, full);
+                tma::load3d(st + L::ST_K0 + 8192, &p.tk, 64, hq, t, full);
+                tma::load3d(st + L::ST_DO, &p.tdo, 0, j, t, full);
+                tma::load3d(st + L::ST_DO + 8192, &p.tdo, 64, j, t, full);
+                tma::load3d(st + L::ST_A, &p.ta, 0, j, t, full);
+                tma::load3d(st + L::ST_P, &p.tp, 0, j, t, full);
+                ++issued[s];
+            }
+            for (int s = 0; s < 2; ++s)
+                if (issued[s] > 0) umma::mbar_wait(sb + L::B_FULL + 8 * s, (issued[s] - 1) & 1, 4000000L);
+        }
+    } else if (warp == 0) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            const uint32_t id_kmn = umma::idesc(128, 128, bf16, false, true);  // K-major A, MN-major B
+            const uint32_t id_mn = umma::idesc(128, 128, bf16, true, true);
+            const uint64_t dZAKG = umma::desc(sb + L::Z, 16, 1024), dH = umma::desc(sb + L::H, 16384, 1024);
+            const uint64_t dWS = umma::desc(sb + L::WS, 8192, 1024), dDL = umma::desc(sb + L::DL, 8192, 1024);
+            auto issue_pw = [&](int lc) {  // P^T dO and W of chunk lc
+                const uint32_t st = sb + (lc & 1) * L::ST_BYTES;
+                const uint64_t ap = umma::desc(st + L::ST_P, 8192, 1024), bdo = umma::desc(st + L::ST_DO, 8192, 1024);
+                const uint64_t bk = umma::desc(st + L::ST_K0, 8192, 1024);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + L::T_P, ap + ks * 128, bdo + ks * 128, id_mn, ks > 0);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + L::T_W, dZAKG + ks * 2, bk + ks * 128, id_kmn, ks > 0);
+                umma::commit(sb + L::B_MPW);
+            };
+            bool ok = true;
+            if (nc > 0) {
+                ok = wait_phase(sb + L::B_PREP, 0, flag, geo.err) && wait_phase(sb + L::B_FULL, 0, flag, geo.err);
+                umma::fence_after();
+                if (ok) issue_pw(0);
+            }
+            for (int lc = 0; lc < nc && ok; ++lc) {
+                const int b = lc & 1;
+                const uint32_t st = sb + b * L::ST_BYTES;
+                // round A on the state tile
+                if (!(ok = wait_phase(sb + L::B_EPIB, lc & 1, flag, geo.err))) break;
+                umma::fence_after();
+                {
+                    const uint64_t ak = umma::desc(st + L::ST_K0, 16, 1024);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        umma::mma(tmem + L::T_E, ak + ((((ks >> 2) * 8192) + (ks & 3) * 32) >> 4), dH + ks * 128, id_kmn,
+                                  ks > 0);
+                }
+                umma::commit(sb + L::B_MA);
+                mbar_arrive(sb + L::B_MA);
+                // Q~^T dO, the base that round B adds to
+                {
+                    const uint64_t aq = umma::desc(st + L::ST_Q0, 8192, 1024), bdo = umma::desc(st + L::ST_DO, 8192, 1024);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + L::T_Y, aq + ks * 128, bdo + ks * 128, id_mn, ks > 0);
+                }
+                // round B: needs dDelta and -W
+                if (!(ok = wait_phase(sb + L::B_EPIA, lc & 1, flag, geo.err) &&
+                           wait_phase(sb + L::B_EPIW, lc & 1, flag, geo.err)))
+                    break;
+                umma::fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + L::T_Y, dWS + ks * 128, dDL + ks * 128, id_mn, true);
+                umma::commit(sb + L::B_MB);
+                umma::commit(sb + L::B_EMPTY + 8 * b);
+                if (lc + 1 < nc) {
+                    if (!(ok = wait_phase(sb + L::B_PREP, (lc + 1) & 1, flag, geo.err) &&
+                               wait_phase(sb + L::B_FULL + 8 * (b ^ 1), ((lc + 1) >> 1) & 1, flag, geo.err)))
+                        break;
+                    umma::fence_after();
+                    issue_pw(lc + 1);
+                }
+            }
+            umma::commit(sb + L::B_DONE);
+            umma::mbar_wait(sb + L::B_DONE, 0, 4000000L);
+        }
+    } else if (warp >= 12) {
+        // ------------------------------------------------------------ preparation (128 threads)
+        const int at = (warp - 12) * 32 + lane;
+        float x0 = 0.f, x1 = 0.f;
+        auto fetch = [&](int lc) {
+            const int c = chunk_of(lc);
+            const int valid = min(C, len - c * C);
+            const int r = at & 63;
+            x0 = 0.f;
+            x1 = 1.f;
+            if (r < valid) {
+                const long long ti = (tok0 + (long long)c * C + r) * Hv + j;
+                if (at < 64) {
+                    x0 = p.g_cs[ti];
+                    if (p.l2norm) x1 = p.rq[ti];
+                } else {
+                    x0 = load_gate<T>(p.beta, ti, p.gate_f32);
+                    if (p.l2norm) x1 = p.rk[ti];
+                }
+            }
+        };
+        if (nc > 0) fetch(0);
+        for (int lc = 0; lc < nc; ++lc) {
+            const int s = lc & 1;
+            const uint32_t st = sb + s * L::ST_BYTES;
+            const int valid = min(C, len - chunk_of(lc) * C);
+            if (at < 64) {
+                fa(lc, FG)[at] = x0;
+                fa(lc, FRQ)[at] = x1;
+            } else {
+                fa(lc, FB)[at - 64] = x0;
+                fa(lc, FRK)[at - 64] = x1;
+            }
+            if (lc + 1 < nc) fetch(lc + 1);
+            asm volatile("bar.sync 1, 128;\n" ::: "memory");
+            if (at < 64) {
+                const int r = at;
+                const bool okr = r < valid;
+                const float gr = fa(lc, FG)[r], Gl = fa(lc, FG)[valid - 1];
+                const float rq = fa(lc, FRQ)[r], rk = fa(lc, FRK)[r], be = fa(lc, FB)[r];
+                const float eg = __expf(gr);
+                fa(lc, FCQ)[r] = okr ? p.scale * rq * eg : 0.f;
+                fa(lc, FCK)[r] = okr ? rk * __expf(Gl - gr) : 0.f;
+                fa(lc, FAKG)[r] = okr ? be * eg * rk : 0.f;
+            }
+            // the stage's tiles, and the previous chunk's W group done with A diag(beta e^G rk)
+            bool ok = warp_wait(sb + L::B_FULL + 8 * s, (lc >> 1) & 1, flag, geo.err, lane);
+            if (ok && lc > 0) ok = warp_wait(sb + L::B_MPW, (lc - 1) & 1, flag, geo.err, lane);
+            if (!group_and(ok, 1, 128)) break;
+            {
+                // A diag(beta e^G rk): thread -> row at/2, 32 columns; rows past the end are zero
+                const int r = at >> 1, c0 = (at & 1) * 32;
+                const bool okr = r < valid;
+                const float4 *fk4 = reinterpret_cast<const float4 *>(fa(lc, FAKG) + c0);
+                uint4 u[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) u[c] = umma::ld_shared_v4(st + L::ST_A + umma::off(r, c0 + c * 8, 0));
+                float fkv[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 a = fk4[i];
+                    fkv[4 * i] = a.x, fkv[4 * i + 1] = a.y, fkv[4 * i + 2] = a.z, fkv[4 * i + 3] = a.w;
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
+                    uint32_t wk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 x = Elt<T>::unpack(w[e]);
+                        const int i = c * 8 + 2 * e;
+                        wk[e] = Elt<T>::pack(okr ? x.x * fkv[i] : 0.f, okr ? x.y * fkv[i + 1] : 0.f);
+                    }
+                    st_v4(sb + L::AKG + umma::off(r, c0 + c * 8, 0), wk[0], wk[1], wk[2], wk[3]);
+                }
+            }
+            {
+                // Q~ = diag(scale rq e^G) Q in place: thread -> row at & 63, key half at >> 6
+                const int r = at & 63;
+                const float cq = fa(lc, FCQ)[r];
+                const uint32_t blk = st + L::ST_Q0 + (at >> 6) * 8192;
+                uint4 u[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) u[c] = umma::ld_shared_v4(blk + umma::off(r, c * 8, 0));
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
+                    uint32_t o4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 x = Elt<T>::unpack(w[e]);
+                        o4[e] = Elt<T>::pack(x.x * cq, x.y * cq);
+                    }
+                    st_v4(blk + umma::off(r, c * 8, 0), o4[0], o4[1], o4[2], o4[3]);
+                }
+            }
+            if (valid < C && at >= valid && at < C) {
+                // P rows past the end of the sequence belong to other tokens: zero them (P^T dO sums rows)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) st_v4(st + L::ST_P + umma::off(at, c * 8, 0), 0u, 0u, 0u, 0u);
+            }
+            umma::fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sb + L::B_PREP);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ state gradient (256 threads)
+        const int sw = warp - 4, q4 = warp & 3, cg = sw >> 2;
+        const int d = q4 * 32 + lane;
+        constexpr int HW = 64;
+        const int cb0 = cg * HW;
+        const long long st_base = ((long long)n * Hv + j) * DK * DV;
+        float hS[HW];
+#pragma unroll
+        for (int i = 0; i < HW; ++i) {
+            const int e = cb0 + i;
+            hS[i] = p.dht ? p.dht[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] : 0.f;
+        }
+        auto write_h = [&]() {
+#pragma unroll
+            for (int i = 0; i < HW; i += 16) {
+                const int col = cb0 + i;
+                store_row16<T>(sb + L::H + (col >> 6) * 16384, d, col & 63, hS + i);
+            }
+            umma::fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sb + L::B_EPIB);
+        };
+        write_h();
+        float glo = 0.f;
+        auto fetch_gl = [&](int lc) {
+            const int c = chunk_of(lc);
+            const int valid = min(C, len - c * C);
+            glo = p.g_cs[(tok0 + (long long)c * C + valid - 1) * Hv + j];
+        };
+        if (nc > 0) fetch_gl(0);
+        for (int lc = 0; lc < nc; ++lc) {
+            const int c = chunk_of(lc);
+            const float egl = __expf(glo);
+            if (lc + 1 < nc) fetch_gl(lc + 1);
+            if (p.dhn) {
+                // the gradient after this chunk
+                T *hr = static_cast<T *>(p.dhn) + ((long long)(row0 + c) * Hv + j) * DK * DV + (long long)d * DV + cb0;
+#pragma unroll
+                for (int i = 0; i < HW; i += 8)
+                    *reinterpret_cast<uint4 *>(hr + i) =
+                        make_uint4(Elt<T>::pack(hS[i], hS[i + 1]), Elt<T>::pack(hS[i + 2], hS[i + 3]),
+                                   Elt<T>::pack(hS[i + 4], hS[i + 5]), Elt<T>::pack(hS[i + 6], hS[i + 7]));
+            }
+            if (q4 < 2) {
+                // dDelta rows (lanes 0..63): diag(rk e^{Gl-G}) E + P^T dO
+                if (!warp_wait(sb + L::B_MA, lc & 1, flag, geo.err, lane)) break;
+                umma::fence_after();
+                const int sr = d;
+                const float ck = fa(lc, FCK)[sr];
+#pragma unroll
+                for (int i = 0; i < HW; i += 16) {
+                    float x[16], y[16];
+                    umma::ld16(umma::taddr(tmem, q4 * 32, L::T_E + cb0 + i), x);
+                    umma::ld16(umma::taddr(tmem, q4 * 32, L::T_P + cb0 + i), y);
+                    umma::ld_wait();
+                    const int col = cb0 + i;
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) x[u] = fmaf(ck, x[u], y[u]);
+                    store_row16<T>(sb + L::DL + (col >> 6) * 8192, sr, col & 63, x);
+                    if (p.ddelta) {
+                        T *dr = static_cast<T *>(p.ddelta) + (((long long)(row0 + c) * Hv + j) * C + sr) * DV + col;
+                        *reinterpret_cast<uint4 *>(dr) =
+                            make_uint4(Elt<T>::pack(x[0], x[1]), Elt<T>::pack(x[2], x[3]), Elt<T>::pack(x[4], x[5]),
+                                       Elt<T>::pack(x[6], x[7]));
+                        *reinterpret_cast<uint4 *>(dr + 8) =
+                            make_uint4(Elt<T>::pack(x[8], x[9]), Elt<T>::pack(x[10], x[11]),
+                                       Elt<T>::pack(x[12], x[13]), Elt<T>::pack(x[14], x[15]));
+                    }
+                }
+                umma::fence_before();
+                umma::fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sb + L::B_EPIA);
+            }
+            if (!warp_wait(sb + L::B_MB, lc & 1, flag, geo.err, lane)) break;
+            umma::fence_after();
+#pragma unroll
+            for (int i0 = 0; i0 < HW; i0 += 32) {
+                float xb[32];
+                umma::ld16(umma::taddr(tmem, q4 * 32, L::T_Y + cb0 + i0), xb);
+                umma::ld16(umma::taddr(tmem, q4 * 32, L::T_Y + cb0 + i0 + 16), xb + 16);
+                umma::ld_wait();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) hS[i0 + i] = fmaf(egl, hS[i0 + i], xb[i]);
+            }
+            umma::fence_before();
+            write_h();
+        }
+        if (!*flag && p.dh0) {
+#pragma unroll
+            for (int i = 0; i < HW; ++i) {
+                const int e = cb0 + i;
+                p.dh0[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] = hS[i];
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ -W (warps 2, 3; TMEM lanes 64..127)
+        const int r = (warp - 2) * 32 + lane;
+        const int lb = 32 * (warp & 3);
+        for (int lc = 0; lc < nc; ++lc) {
+            if (!warp_wait(sb + L::B_MPW, lc & 1, flag, geo.err, lane)) break;
+            umma::fence_after();
+#pragma unroll
+            for (int c = 0; c < 128; c += 64) {
+                float x[64];
+#pragma unroll
+                for (int u = 0; u < 64; u += 16) umma::ld16(umma::taddr(tmem, lb, L::T_W + c + u), x + u);
+                umma::ld_wait();
+#pragma unroll
+                for (int u = 0; u < 64; ++u) x[u] = -x[u];
+#pragma unroll
+                for (int u = 0; u < 64; u += 16) store_row16<T>(sb + L::WS + (c >> 6) * 8192, r, u, x + u);
+            }
+            umma::fence_before();
+            umma::fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sb + L::B_EPIW);
+        }
+    }
+
+    umma::fence_before();
+    __syncthreads();
+    if (warp == 0) umma::dealloc(tmem, 512);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(WS_NT, 1) chain_rev_kernel(Geo geo, const __grid_constant__ RevP p) {
+    ws_rev_body<T>(geo, p, blockIdx.y, blockIdx.z);
+}
+
+// The backward's two chains side by side: blocks z < N recompute the forward states (all 128 value
+// columns, no output), blocks z >= N run the reverse chain.
+template <typename T>
+__global__ void __launch_bounds__(WS_NT, 1) chain_ws_pair_kernel(Geo geo, const __grid_constant__ WsP pf,
+                                                                 const __grid_constant__ RevP pb) {
+    if ((int)blockIdx.z < geo.N)
+        ws_fwd_body<T, 128, false>(geo, pf, 0, blockIdx.y, blockIdx.z);
+    else
+        ws_rev_body<T>(geo, pb, blockIdx.y, blockIdx.z - geo.N);
+}
+
 bool ws_map(CUtensorMap *m, const void *base, const Args &a, int heads, int cols) {
     const uint64_t tokens = (uint64_t)a.B * (uint64_t)a.T;
     return make_tmap_3d(m, base, a.bf16, (uint64_t)cols, (uint64_t)heads, tokens, (uint64_t)cols * 2,
@@ -640,14 +1082,65 @@ bool ws_map(CUtensorMap *m, const void *base, const Args &a, int heads, int cols
 template <typename T, int BV, bool WRITE_O>
 cudaError_t chain_ws_t(const Args &a, const WsP &p, cudaStream_t s) {
     auto kern = chain_ws_kernel<T, BV, WRITE_O>;
-    const uint32_t bytes = Lay<BV>::BYTES;
+    const uint32_t bytes = Lay<BV, WRITE_O>::BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     kern<<<dim3(DV / BV, a.Hv, a.N), WS_NT, bytes, s>>>(make_geo(a), p);
     return cudaGetLastError();
 }
 
+template <typename T>
+cudaError_t chain_ws_pair_t(const Args &a, const WsP &pf, const RevP &pb, cudaStream_t s) {
+    auto kern = chain_ws_pair_kernel<T>;
+    const uint32_t bytes = Lay<128, false>::BYTES > RLay::BYTES ? Lay<128, false>::BYTES : RLay::BYTES;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(1, a.Hv, 2 * a.N), WS_NT, bytes, s>>>(make_geo(a), pf, pb);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_chain_ws_pair(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
+                                 const void *beta, const void *A, const void *P, const float *rq, const float *rk,
+                                 const float *h0, void *h, void *delta, const void *dout, const float *dht,
+                                 void *dhn, void *ddelta, float *dh0, cudaStream_t s) {
+    WsP pf;
+    RevP pb;
+    if (!ws_map(&pf.tq, q, a, a.Hq, DK) || !ws_map(&pf.tk, k, a, a.Hq, DK) || !ws_map(&pf.tv, v, a, a.Hv, DV) ||
+        !ws_map(&pf.ta, A, a, a.Hv, C) || !ws_map(&pb.tq, q, a, a.Hq, DK) || !ws_map(&pb.tk, k, a, a.Hq, DK) ||
+        !ws_map(&pb.tdo, dout, a, a.Hv, DV) || !ws_map(&pb.tp, P, a, a.Hv, C) || !ws_map(&pb.ta, A, a, a.Hv, C))
+        return cudaErrorInvalidValue;
+    pf.tp = pb.tp;
+    pf.g_cs = g_cs;
+    pf.h0 = h0;
+    pf.rq = rq;
+    pf.rk = rk;
+    pf.beta = beta;
+    pf.o = nullptr;
+    pf.fin = nullptr;
+    pf.h = h;
+    pf.delta = delta;
+    pf.seg_start = nullptr;
+    pf.gate_f32 = a.gate_f32;
+    pf.l2norm = a.l2norm;
+    pf.v_first = a.v_first;
+    pf.h_vfirst = false;
+    pf.scale = a.scale;
+    pb.g_cs = g_cs;
+    pb.rq = rq;
+    pb.rk = rk;
+    pb.dht = dht;
+    pb.beta = beta;
+    pb.dhn = dhn;
+    pb.ddelta = ddelta;
+    pb.dh0 = dh0;
+    pb.gate_f32 = a.gate_f32;
+    pb.l2norm = a.l2norm;
+    pb.v_first = a.v_first;
+    pb.scale = a.scale;
+    return a.bf16 ? chain_ws_pair_t<__nv_bfloat16>(a, pf, pb, s) : chain_ws_pair_t<__half>(a, pf, pb, s);
+}
 
 cudaError_t launch_chain_ws(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
                             const void *beta, const void *A, const void *P, const float *rq, const float *rk,

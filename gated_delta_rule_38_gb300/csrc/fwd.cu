@@ -18,7 +18,11 @@ namespace gdr {
 // ============================================================================ wy_fwd
 
 constexpr int LDF = 68;  // fp32 row stride of the 64x64 matrices (bank spread)
-constexpr int WY_SMEM = 2 * C * DK * 2 + 2 * C * LDF * 4 + 4 * C * 4 + 4 * 16 * 20 * 4;
+constexpr int LDP = C + 8;  // bf16 row stride of the P staging (bank spread)
+// [K tile 16 KB][Q tile 16 KB, later L][.. A^-1][gate arrays]; the merge scratch reuses the K tile and the
+// P staging the A^-1 buffer, so four CTAs fit on an SM
+constexpr int WY_SMEM = C * DK * 2 + 2 * C * LDF * 4 + 4 * C * 4;
+static_assert(C * DK * 2 <= C * LDF * 4, "the Q tile must fit under L");
 
 struct WyArgs {
     const void *q, *k, *g, *beta;
@@ -36,13 +40,14 @@ __global__ void __launch_bounds__(128) wy_fwd_kernel(Geo geo, const WyArgs w) {
     extern __shared__ __align__(1024) unsigned char smem[];
     T *sk = reinterpret_cast<T *>(smem);
     T *sq = reinterpret_cast<T *>(smem + C * DK * 2);
-    float *Lm = reinterpret_cast<float *>(smem + 2 * C * DK * 2);
+    float *Lm = reinterpret_cast<float *>(smem + C * DK * 2);  // over the Q tile once P is out
     float *Ai = Lm + C * LDF;
     float *sG = Ai + C * LDF;
     float *sB = sG + C;
     float *sRQ = sB + C;
     float *sRK = sRQ + C;
-    float *scr = sRK + C;  // [4 warps][16][20]
+    float *scr = reinterpret_cast<float *>(smem);  // [4 warps][16][20], over the K tile once L is built
+    T *sp = reinterpret_cast<T *>(Ai);             // P staging [64][LDP], before A^-1 is built
 
     long long tok0;
     int len, n, ci;
@@ -96,6 +101,46 @@ __global__ void __launch_bounds__(128) wy_fwd_kernel(Geo geo, const WyArgs w) {
     if (w.l2norm && tid < len) {
         if (w.rk_out) w.rk_out[(tok0 + tid) * Hv + j] = sRK[tid];
         if (w.rq_out && want_p) w.rq_out[(tok0 + tid) * Hv + j] = sRQ[tid];
+    }
+
+    // ---- P = scale (q^ k^T o exp(G_r - G_s)) for s <= r < len (warp w owns rows 16w..16w+15), staged
+    //      as rows in the not yet used A^-1 buffer, then stored row by row
+    if (want_p) {
+        float acc[8][4];
+        zero_acc<8>(acc);
+        const int r0 = warp * 16;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            uint32_t a[4];
+            load_a(a, tqt, r0, ks * 16, false, lane);
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                if (np <= warp) {
+                    uint32_t b[4];
+                    load_b2(b, tk, np * 16, ks * 16, false, lane);
+                    mma16816<T>(acc[2 * np], a, b[0], b[1]);
+                    mma16816<T>(acc[2 * np + 1], a, b[2], b[3]);
+                }
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int r = r0 + gq + 8 * hh, s0 = nt * 8 + tq * 2;
+                const float v0 = (s0 <= r && r < len) ? w.scale * __expf(sG[r] - sG[s0]) * acc[nt][2 * hh] : 0.f;
+                const float v1 =
+                    (s0 + 1 <= r && r < len) ? w.scale * __expf(sG[r] - sG[s0 + 1]) * acc[nt][2 * hh + 1] : 0.f;
+                *reinterpret_cast<uint32_t *>(sp + r * LDP + s0) = Elt<T>::pack(v0, v1);
+            }
+        __syncthreads();
+        for (int i = tid; i < C * 8; i += 128) {
+            const int r = i >> 3, c0 = (i & 7) * 8;
+            if (r >= len) continue;
+            *reinterpret_cast<uint4 *>(static_cast<T *>(w.P_out) + ((tok0 + r) * Hv + j) * C + c0) =
+                *reinterpret_cast<const uint4 *>(sp + r * LDP + c0);
+        }
+        __syncthreads();  // the Q tile becomes L
     }
 
     if (w.A_out) {
@@ -228,46 +273,6 @@ __global__ void __launch_bounds__(128) wy_fwd_kernel(Geo geo, const WyArgs w) {
         }
     }
 
-    // ---- P = scale (q^ k^T o exp(G_r - G_s)) for s <= r < len (warp w owns rows 16w..16w+15), staged
-    //      as bf16/fp16 rows in the dead L buffer, then stored row by row
-    if (want_p) {
-        __syncthreads();
-        T *sp = reinterpret_cast<T *>(Lm);  // [64][64]
-        float acc[8][4];
-        zero_acc<8>(acc);
-        const int r0 = warp * 16;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            uint32_t a[4];
-            load_a(a, tqt, r0, ks * 16, false, lane);
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                if (np <= warp) {
-                    uint32_t b[4];
-                    load_b2(b, tk, np * 16, ks * 16, false, lane);
-                    mma16816<T>(acc[2 * np], a, b[0], b[1]);
-                    mma16816<T>(acc[2 * np + 1], a, b[2], b[3]);
-                }
-            }
-        }
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int r = r0 + gq + 8 * hh, s0 = nt * 8 + tq * 2;
-                const float v0 = (s0 <= r && r < len) ? w.scale * __expf(sG[r] - sG[s0]) * acc[nt][2 * hh] : 0.f;
-                const float v1 =
-                    (s0 + 1 <= r && r < len) ? w.scale * __expf(sG[r] - sG[s0 + 1]) * acc[nt][2 * hh + 1] : 0.f;
-                *reinterpret_cast<uint32_t *>(sp + r * C + s0) = Elt<T>::pack(v0, v1);
-            }
-        __syncthreads();
-        for (int i = tid; i < C * 8; i += 128) {
-            const int r = i >> 3, c0 = (i & 7) * 8;
-            if (r >= len) continue;
-            *reinterpret_cast<uint4 *>(static_cast<T *>(w.P_out) + ((tok0 + r) * Hv + j) * C + c0) =
-                *reinterpret_cast<const uint4 *>(sp + r * C + c0);
-        }
-    }
 }
 
 // ============================================================================ launchers

@@ -56,6 +56,13 @@ cudaError_t launch_chain_ws(const Args &a, const void *q, const void *k, const v
                             const void *beta, const void *A, const void *P, const float *rq, const float *rk,
                             const float *h0, const float *seg_start, void *o, float *final_state, void *h,
                             bool h_vfirst, void *delta, cudaStream_t s);
+// Backward without a sequence split, warp-specialised: the forward recompute (states h and Delta of every
+// chunk, no output) and the reverse chain (dH' and dDelta of every chunk, dh0) in one launch, one CTA each
+// per (sequence, value head).  P, rq, rk from launch_chunk_p.
+cudaError_t launch_chain_ws_pair(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
+                                 const void *beta, const void *A, const void *P, const float *rq, const float *rk,
+                                 const float *h0, void *h, void *delta, const void *dout, const float *dht,
+                                 void *dhn, void *ddelta, float *dh0, cudaStream_t s);
 // Backward: reverse state-gradient chain (dH' and dDelta of every chunk, dh0).
 cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
                              const void *A, const void *dout, const float *dht, void *dhn, void *ddelta, float *dh0,
