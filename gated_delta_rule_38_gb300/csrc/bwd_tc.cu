@@ -39,7 +39,6 @@ namespace gdr {
 namespace {
 
 constexpr int NT = 256;
-constexpr int FLD = DK + 1;  // row stride (floats) of the fp32 dq/dk staging
 // ---- shared memory (bytes from a 1024-aligned base)
 constexpr uint32_t S_Q0 = 0, S_K0 = 8192;             // [Q b0][K b0][Q b1][K b1]
 constexpr uint32_t S_DO0 = 32768, S_DD0 = 40960;      // [dO b0][dDelta b0][dO b1][dDelta b1]
@@ -55,7 +54,7 @@ constexpr uint32_t S_BYTES = S_USED + 1024;
 // scalar slots (64 floats each)
 enum {
     F_G = 0, F_B, F_EG, F_EL, F_QD0, F_QD1, F_VD0, F_VD1, F_KD0, F_KD1, F_LB0, F_LB1,
-    F_ER0, F_ER1, F_EC0, F_EC1, F_Z0, F_Z1, F_FR0, F_FR1, F_FC0, F_FC1, F_HD, F_DG, F_IQ, F_IK, F_COUNT
+    F_ER0, F_ER1, F_EC0, F_EC1, F_Z0, F_Z1, F_FR0, F_FR1, F_FC0, F_FC1, F_HD, F_DG, F_IQ, F_IK, F_DP, F_COUNT = F_DP + 4
 };
 // TMEM columns
 constexpr uint32_t T_R1 = 0, T_R2 = 128, T_R3 = 256, T_R4 = 384, T_R8 = 448, T_COLS = 512;
@@ -158,40 +157,6 @@ __device__ __forceinline__ void l2norm64(uint32_t base, int rows, int warp, int 
             }
             umma::st_shared_v4(addr[c], w[0], w[1], w[2], w[3]);
         }
-    }
-}
-
-// dx = (dxh - xh (xh . dxh)) / n with n = sqrt(sum x^2 + eps) and xh = x / n, from the normalised
-// tile in shared memory (two swizzled 64-column blocks 16 KB apart) and the inverse norms; one warp per
-// row, lane l owns columns 4l..4l+3.
-template <typename T>
-__device__ __forceinline__ void l2norm_bwd_rows(const float *src, uint32_t xtile, const float *inv, T *dst,
-                                                long long stride, int valid, bool l2norm, int warp, int nwarps,
-                                                int lane) {
-    const int col = lane * 4;
-    for (int r = warp; r < valid; r += nwarps) {
-        T *dr = dst + (long long)r * stride;
-        float gv[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) gv[u] = src[r * FLD + col + u];
-        if (l2norm) {
-            uint2 w;
-            asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];\n"
-                         : "=r"(w.x), "=r"(w.y)
-                         : "r"(xtile + (uint32_t)(col >> 6) * 16384u + umma::off(r, col & 63, 0)));
-            const float2 x0 = Elt<T>::unpack(w.x), x1 = Elt<T>::unpack(w.y);
-            const float xv[4] = {x0.x, x0.y, x1.x, x1.y};
-            float dot = xv[0] * gv[0] + xv[1] * gv[1] + xv[2] * gv[2] + xv[3] * gv[3];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-            const float iv = inv[r];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) gv[u] = (gv[u] - xv[u] * dot) * iv;
-        }
-        uint2 w;
-        w.x = Elt<T>::pack(gv[0], gv[1]);
-        w.y = Elt<T>::pack(gv[2], gv[3]);
-        *reinterpret_cast<uint2 *>(dr + col) = w;
     }
 }
 
@@ -430,11 +395,12 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             f(F_Z0 + hh, r) = z;
         }
         {
-            // <dH', h> over the whole state (both tiles share one layout, so equal offsets hold equal elements)
+            // <dH', h> over the whole state (both tiles share one layout, so equal offsets hold equal elements);
+            // consecutive threads read consecutive 8-byte words (no bank conflicts)
             float hd = 0.f;
 #pragma unroll 4
             for (int u = 0; u < 16; ++u) {
-                const uint32_t o = (uint32_t)(tid * 16 + u) * 8u;
+                const uint32_t o = (uint32_t)(u * NT + tid) * 8u;
                 const uint2 a = *reinterpret_cast<const uint2 *>(smem + S_H + o);
                 const uint2 b = *reinterpret_cast<const uint2 *>(smem + S_DH + o);
                 const float2 a0 = Elt<T>::unpack(a.x), a1 = Elt<T>::unpack(a.y);
@@ -673,23 +639,53 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
         __syncthreads();
     }
 
-    // ---- dq (lower lanes) and dk (upper lanes): stage fp32, L2-norm chain rule, store
-    // [64][129] fp32 each (a row stride of 129 words spreads the rows written by one warp over all banks);
-    // every tile is dead by now, so the staging may overlap any of them
-    float *fq = reinterpret_cast<float *>(smem + S_DO0);
-    float *fk = reinterpret_cast<float *>(smem + S_DO0 + 64 * FLD * 4);
-    if (ok) {
-        float *dst = upper ? fk : fq;
+    // ---- dq (lower lanes) and dk (upper lanes), straight from the registers: with xh the normalised row
+    //      (the q or k tile in shared memory) and n its norm, dx = (dxh - xh (xh . dxh)) / n; the two
+    //      column halves of a row meet through one partial dot product each
+    const uint32_t xt = sb + (upper ? S_K0 : S_Q0) + hh * 16384;
+    float *dp = &f(F_DP, 0);  // [2 halves][128 lanes]
+    if (ok && p.l2norm) {
+        float part = 0.f;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) dst[r * FLD + hh * 64 + i] = acc[i];
+        for (int c = 0; c < 8; ++c) {
+            const uint4 u = umma::ld_shared_v4(xt + umma::off(r, c * 8, 0));
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 x = Elt<T>::unpack(w[e]);
+                part = fmaf(x.x, acc[c * 8 + 2 * e], fmaf(x.y, acc[c * 8 + 2 * e + 1], part));
+            }
+        }
+        dp[hh * 128 + L] = part;
     }
     __syncthreads();
-    if (ok) {
-        const long long rstride = (long long)Hq * DK;
-        l2norm_bwd_rows<T>(fq, sb + S_Q0, &f(F_IQ, 0), static_cast<T *>(p.dq) + (tok0 * Hq + hq) * DK, rstride,
-                           valid, p.l2norm, warp, 8, lane);
-        l2norm_bwd_rows<T>(fk, sb + S_K0, &f(F_IK, 0), static_cast<T *>(p.dk) + (tok0 * Hq + hq) * DK, rstride,
-                           valid, p.l2norm, warp, 8, lane);
+    if (ok && r < valid) {
+        const float dot = p.l2norm ? dp[L] + dp[128 + L] : 0.f;
+        const float inv = p.l2norm ? f(upper ? F_IK : F_IQ, r) : 1.f;
+        T *dst = static_cast<T *>(upper ? p.dk : p.dq) + ((tok0 + r) * Hq + hq) * DK + hh * 64;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            float xv[8];
+            if (p.l2norm) {
+                const uint4 u = umma::ld_shared_v4(xt + umma::off(r, c * 8, 0));
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 x = Elt<T>::unpack(w[e]);
+                    xv[2 * e] = x.x;
+                    xv[2 * e + 1] = x.y;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xv[e] = 0.f;
+            }
+            uint32_t o4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                o4[e] = Elt<T>::pack((acc[c * 8 + 2 * e] - xv[2 * e] * dot) * inv,
+                                     (acc[c * 8 + 2 * e + 1] - xv[2 * e + 1] * dot) * inv);
+            *reinterpret_cast<uint4 *>(dst + c * 8) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+        }
     }
     umma::fence_before();
     __syncthreads();
