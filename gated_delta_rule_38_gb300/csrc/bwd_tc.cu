@@ -71,12 +71,8 @@ struct BcP {
     void *dq, *dk, *dv, *dg, *dbeta;
     bool gate_f32, l2norm;
     float scale;
+    int nslots;  // chunk slots (dense: B * ceil(T/64); varlen: the chunk-table bound)
 };
-
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, bool valid) {
-    const int n = valid ? 4 : 0;
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(n));
-}
 
 // Column sums of a 32 x 32 block held one row per lane (v[c] = column c): lane l ends
 // with the sum over the 32 lanes of column l (a fixed-order butterfly, 31 shuffles).
@@ -166,11 +162,23 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
     unsigned char *smem =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
-    long long tok0;
-    int valid, n, ci;
-    const int slot = blockIdx.x;
-    if (!geo.chunk(slot, tok0, valid, n, ci)) return;
-    const int hq = blockIdx.y, Hv = geo.Hv, Hq = geo.Hq, grp = Hv / Hq;
+    const int Hv = geo.Hv, Hq = geo.Hq, grp = Hv / Hq;
+    // Persistent: this CTA walks the work items w = blockIdx.x, + gridDim.x, ... (item = chunk slot x q/k
+    // head, each with the grp value heads of its group: one "unit" per value head).  The tiles of the next
+    // unit are prefetched into buffers as soon as the current unit is done with them.
+    const long nitems = (long)p.nslots * Hq;
+    auto item_ok = [&](long w_) {
+        long long t_;
+        int v_, n_, c_;
+        return geo.chunk((int)(w_ / Hq), t_, v_, n_, c_);
+    };
+    auto next_item = [&](long w_) -> long {
+        for (; w_ < nitems; w_ += gridDim.x)
+            if (item_ok(w_)) return w_;
+        return -1;
+    };
+    long wit = next_item(blockIdx.x);
+    if (wit < 0) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int L = (warp & 3) * 32 + lane, hh = warp >> 2, lb = (warp & 3) * 32;
     const bool upper = L >= 64;
@@ -242,50 +250,94 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
     };
 
     float acc[64];  // dq row (lower lanes) or dk row (upper lanes), key columns 64*hh..
-#pragma unroll
-    for (int i = 0; i < 64; ++i) acc[i] = 0.f;
     bool ok = true;
 
-    for (int jj = 0; jj < grp && ok; ++jj) {
-        const int j = hq * grp + jj;
-        if (tid == 0) {
-            // every tile lands in the 128-byte-swizzled layout of the MMA operands; rows past the end of
-            // the sequence carry the next sequence's data (harmless: each product that reads them is
-            // masked, and dDelta is stored zero there)
-            const int t = (int)tok0, row = slot * Hv + j;
-            tma::expect_tx(lbar, (jj == 0 ? 32768u : 0u) + 4 * 16384u + 2 * 32768u + 8192u);
-            if (jj == 0) {
-                tma::load3d(sb + S_Q0, &p.tq, 0, hq, t, lbar);
-                tma::load3d(sb + S_Q0 + 16384, &p.tq, 64, hq, t, lbar);
-                tma::load3d(sb + S_K0, &p.tk, 0, hq, t, lbar);
-                tma::load3d(sb + S_K0 + 16384, &p.tk, 64, hq, t, lbar);
-            }
-            tma::load3d(sb + S_DO0, &p.tdo, 0, j, t, lbar);
-            tma::load3d(sb + S_DO0 + 16384, &p.tdo, 64, j, t, lbar);
-            tma::load3d(sb + S_DD0, &p.tdd, 0, 0, row, lbar);
-            tma::load3d(sb + S_DD0 + 16384, &p.tdd, 64, 0, row, lbar);
-            tma::load3d(sb + S_V0, &p.tv, 0, j, t, lbar);
-            tma::load3d(sb + S_V0 + 16384, &p.tv, 64, j, t, lbar);
-            tma::load3d(sb + S_D0, &p.td, 0, 0, row, lbar);
-            tma::load3d(sb + S_D0 + 16384, &p.td, 64, 0, row, lbar);
+    // tile loads of unit (item w_, value head jj_ of its group), in three groups by the point where the
+    // current unit frees the buffers: 1 = h, dH', dO (after round 1); 2 = V, dDelta (after round 2);
+    // 3 = Delta, A and, for the first head of an item, q and k (after the unit).  All bytes of a unit are
+    // announced on the load barrier with its first group.
+    auto unit_bytes = [&](int jj_) -> uint32_t { return 32768u * 2 + 16384u + 16384u * 2 + 16384u + 8192u +
+                                                         (jj_ == 0 ? 32768u : 0u); };
+    auto issue = [&](long w_, int jj_, int group) {
+        long long t_;
+        int v_, n_, c_;
+        const int slot_ = (int)(w_ / Hq), hq_ = (int)(w_ % Hq), j_ = hq_ * grp + jj_;
+        geo.chunk(slot_, t_, v_, n_, c_);
+        const int t = (int)t_, row = slot_ * Hv + j_;
+        if (group == 1) {
+            tma::expect_tx(lbar, unit_bytes(jj_));
             tma::load3d(sb + S_H, &p.th, 0, 0, row, lbar);
             tma::load3d(sb + S_H + 16384, &p.th, 64, 0, row, lbar);
             tma::load3d(sb + S_DH, &p.tdh, 0, 0, row, lbar);
             tma::load3d(sb + S_DH + 16384, &p.tdh, 64, 0, row, lbar);
-            tma::load3d(sb + S_A, &p.ta, 0, j, t, lbar);
+            tma::load3d(sb + S_DO0, &p.tdo, 0, j_, t, lbar);
+            tma::load3d(sb + S_DO0 + 16384, &p.tdo, 64, j_, t, lbar);
+        } else if (group == 2) {
+            tma::load3d(sb + S_V0, &p.tv, 0, j_, t, lbar);
+            tma::load3d(sb + S_V0 + 16384, &p.tv, 64, j_, t, lbar);
+            tma::load3d(sb + S_DD0, &p.tdd, 0, 0, row, lbar);
+            tma::load3d(sb + S_DD0 + 16384, &p.tdd, 64, 0, row, lbar);
+        } else {
+            tma::load3d(sb + S_D0, &p.td, 0, 0, row, lbar);
+            tma::load3d(sb + S_D0 + 16384, &p.td, 64, 0, row, lbar);
+            tma::load3d(sb + S_A, &p.ta, 0, j_, t, lbar);
+            if (jj_ == 0) {
+                tma::load3d(sb + S_Q0, &p.tq, 0, hq_, t, lbar);
+                tma::load3d(sb + S_Q0 + 16384, &p.tq, 64, hq_, t, lbar);
+                tma::load3d(sb + S_K0, &p.tk, 0, hq_, t, lbar);
+                tma::load3d(sb + S_K0 + 16384, &p.tk, 64, hq_, t, lbar);
+            }
+        }
+    };
+    // gates of a unit (threads 0..63), fetched one unit ahead into registers
+    float gnext = 0.f, bnext = 0.f;
+    auto fetch_gates = [&](long w_, int jj_) {
+        if (tid < C) {
+            long long t_;
+            int v_, n_, c_;
+            geo.chunk((int)(w_ / Hq), t_, v_, n_, c_);
+            const long long ti = (t_ + tid) * Hv + (int)(w_ % Hq) * grp + jj_;
+            gnext = tid < v_ ? p.g_cs[ti] : 0.f;
+            bnext = tid < v_ ? load_gate<T>(p.beta, ti, p.gate_f32) : 0.f;
+        }
+    };
+    int jj = 0;
+    bool posted = false;  // a unit's loads are announced and not yet waited for
+    if (tid == 0) {
+        issue(wit, 0, 1);
+        issue(wit, 0, 2);
+        issue(wit, 0, 3);
+    }
+    posted = true;
+    fetch_gates(wit, 0);
+
+    while (ok) {
+        long long tok0;
+        int valid, n, ci;
+        const int slot = (int)(wit / Hq), hq = (int)(wit % Hq);
+        geo.chunk(slot, tok0, valid, n, ci);
+        const int j = hq * grp + jj;
+        // the unit after this one
+        long wn = wit;
+        int jn = jj + 1;
+        if (jn == grp) {
+            jn = 0;
+            wn = next_item(wit + gridDim.x);
+        }
+        if (jj == 0) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) acc[i] = 0.f;
         }
         if (tid < C) {
-            const bool okr = tid < valid;
-            cp_async4(sb + S_F + (F_G * 64 + tid) * 4, p.g_cs + (okr ? (tok0 + tid) * Hv + j : 0), okr);
-            f(F_B, tid) = okr ? load_gate<T>(p.beta, (tok0 + tid) * Hv + j, p.gate_f32) : 0.f;
+            f(F_G, tid) = gnext;
+            f(F_B, tid) = bnext;
         }
-        cp_async_commit();
-        cp_async_wait<0>();
         if (!umma::mbar_wait(lbar, lphase)) {
             raise_error(geo.err, GDR_ERR_TIMEOUT);
             *sflag = 1;
         }
         lphase ^= 1u;
+        posted = false;
         __syncthreads();
         if (*sflag) {
             ok = false;
@@ -412,6 +464,12 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             if (lane == 0) f(F_HD, warp) = hd;
         }
         sync_tc();
+        // h, dH' and dO are free: the next unit's first tile group
+        if (wn >= 0) {
+            if (tid == 0) issue(wn, jn, 1);
+            posted = true;
+            fetch_gates(wn, jn);
+        }
 
         // ---------------- round 2
         if (tid == 0) {
@@ -479,6 +537,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             }
         }
         sync_tc();
+        if (tid == 0 && wn >= 0) issue(wn, jn, 2);  // V and dDelta are free
 
         // ---------------- round 3: X = dA A^T ; dq += dS K ; dk += dS^T Q
         if (tid == 0) {
@@ -613,7 +672,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             for (int o = 16; o > 0; o >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);
             float hd = 0.f;
 #pragma unroll
-            for (int w = 0; w < 8; ++w) hd += f(F_HD, w);
+            for (int wi = 0; wi < 8; ++wi) hd += f(F_HD, wi);
             const float extra = __expf(Gl) * hd + zs;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf)
@@ -637,8 +696,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             }
         }
         __syncthreads();
-    }
-
+        if (jj + 1 == grp) {
     // ---- dq (lower lanes) and dk (upper lanes), straight from the registers: with xh the normalised row
     //      (the q or k tile in shared memory) and n its norm, dx = (dxh - xh (xh . dxh)) / n; the two
     //      column halves of a row meet through one partial dot product each
@@ -687,6 +745,18 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             *reinterpret_cast<uint4 *>(dst + c * 8) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
         }
     }
+        }
+        // Delta, A (and q, k for a new item) are free: the next unit's last tile group
+        umma::fence_async_smem();
+        __syncthreads();
+        if (wn < 0) break;
+        if (tid == 0) issue(wn, jn, 3);
+        wit = wn;
+        jj = jn;
+    }
+    // after an error, let a prefetch in flight land before the block exits (bounded)
+    if (tid == 0 && posted) umma::mbar_wait(lbar, lphase, 4000000L);
+
     umma::fence_before();
     __syncthreads();
     if (warp == 0) umma::dealloc(tmem, T_COLS);
@@ -698,7 +768,11 @@ cudaError_t bwd_chunk_tc_t(const Args &a, const BcP &p, cudaStream_t s) {
     auto kern = bwd_chunk_tc_kernel<T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)a.max_chunks, a.Hq);
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const long items = (long)a.max_chunks * a.Hq;
+    const unsigned grid = (unsigned)(items < sms ? items : sms);  // one persistent CTA per SM
     kern<<<grid, NT, S_BYTES, s>>>(make_geo(a), p);
     return cudaGetLastError();
 }
@@ -741,6 +815,7 @@ cudaError_t launch_bwd_chunk_tc(const Args &a, const void *q, const void *k, con
     p.gate_f32 = a.gate_f32;
     p.l2norm = a.l2norm;
     p.scale = a.scale;
+    p.nslots = (int)a.max_chunks;
     return a.bf16 ? bwd_chunk_tc_t<__nv_bfloat16>(a, p, s) : bwd_chunk_tc_t<__half>(a, p, s);
 }
 
