@@ -38,7 +38,7 @@
 namespace gdr {
 namespace {
 
-constexpr int NT = 256;
+constexpr int NT = 512;
 // ---- shared memory (bytes from a 1024-aligned base)
 constexpr uint32_t S_Q0 = 0, S_K0 = 8192;             // [Q b0][K b0][Q b1][K b1]
 constexpr uint32_t S_DO0 = 32768, S_DD0 = 40960;      // [dO b0][dDelta b0][dO b1][dDelta b1]
@@ -48,13 +48,15 @@ constexpr uint32_t S_DA = S_D0, S_DKK = S_D0 + 16384; // reuse Delta's blocks af
 constexpr uint32_t S_H = 131072, S_DH = 163840;       // [128 x 64] blocks of 16 KB
 constexpr uint32_t S_A = 196608, S_AKG = 204800;
 constexpr uint32_t S_F = 212992;                      // scalars
-constexpr uint32_t S_BAR = S_F + 32 * 64 * 4, S_LBAR = S_BAR + 8, S_SLOT = S_LBAR + 8, S_FLAG = S_SLOT + 4,
+constexpr uint32_t S_BAR = S_F + 48 * 64 * 4, S_LBAR = S_BAR + 8, S_SLOT = S_LBAR + 8, S_FLAG = S_SLOT + 4,
                    S_USED = S_FLAG + 4;
 constexpr uint32_t S_BYTES = S_USED + 1024;
 // scalar slots (64 floats each)
+// (per column quarter q of a row: slot + q; column sums per row half: slot + 0/1)
 enum {
-    F_G = 0, F_B, F_EG, F_EL, F_QD0, F_QD1, F_VD0, F_VD1, F_KD0, F_KD1, F_LB0, F_LB1,
-    F_ER0, F_ER1, F_EC0, F_EC1, F_Z0, F_Z1, F_FR0, F_FR1, F_FC0, F_FC1, F_HD, F_DG, F_IQ, F_IK, F_DP, F_COUNT = F_DP + 4
+    F_G = 0, F_B, F_EG, F_EL, F_QD0, F_VD0 = F_QD0 + 4, F_KD0 = F_VD0 + 4, F_LB0 = F_KD0 + 4, F_ER0 = F_LB0 + 4,
+    F_EC0 = F_ER0 + 4, F_Z0 = F_EC0 + 2, F_FR0 = F_Z0 + 4, F_FC0 = F_FR0 + 4, F_HD = F_FC0 + 2, F_DG, F_IQ, F_IK,
+    F_DP, F_COUNT = F_DP + 8
 };
 // TMEM columns
 constexpr uint32_t T_R1 = 0, T_R2 = 128, T_R3 = 256, T_R4 = 384, T_R8 = 448, T_COLS = 512;
@@ -74,11 +76,11 @@ struct BcP {
     int nslots;  // chunk slots (dense: B * ceil(T/64); varlen: the chunk-table bound)
 };
 
-// Column sums of a 32 x 32 block held one row per lane (v[c] = column c): lane l ends
-// with the sum over the 32 lanes of column l (a fixed-order butterfly, 31 shuffles).
-__device__ __forceinline__ float colsum32(float (&v)[32], int lane) {
+// Column sums of a 32 x 16 block held one row per lane (v[c] = column c): lane l ends with the sum over
+// the 32 lanes of column l & 15 (fixed-order butterfly, 16 shuffles).
+__device__ __forceinline__ float colsum16(float (&v)[16], int lane) {
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
+    for (int o = 8; o >= 1; o >>= 1) {
         const bool up = (lane & o) != 0;
 #pragma unroll
         for (int i = 0; i < o; ++i) {
@@ -87,7 +89,7 @@ __device__ __forceinline__ float colsum32(float (&v)[32], int lane) {
             v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
         }
     }
-    return v[0];
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
 }
 
 template <typename T>
@@ -119,7 +121,7 @@ __device__ __forceinline__ void load16(uint32_t base, int row, int col0, float *
 template <typename T>
 __device__ __forceinline__ void l2norm64(uint32_t base, int rows, int warp, int lane, float *inv_out) {
     const int rq = lane >> 2, qq = lane & 3;
-    const int r = warp * 8 + rq;  // 8 warps x 8 rows
+    const int r = warp * 8 + rq;  // warps 0..7 x 8 rows
     uint32_t addr[4];
     uint4 u[4];
 #pragma unroll
@@ -180,7 +182,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
     long wit = next_item(blockIdx.x);
     if (wit < 0) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int L = (warp & 3) * 32 + lane, hh = warp >> 2, lb = (warp & 3) * 32;
+    const int L = (warp & 3) * 32 + lane, qc = warp >> 2, lb = (warp & 3) * 32;  // qc: column quarter
     const bool upper = L >= 64;
     const int r = L & 63;  // token row of this thread's TMEM lane
     constexpr bool bf16 = IsBf16<T>::value;
@@ -249,7 +251,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
         umma::fence_after();
     };
 
-    float acc[64];  // dq row (lower lanes) or dk row (upper lanes), key columns 64*hh..
+    float acc[32];  // dq row (lower lanes) or dk row (upper lanes), key columns 32*qc..
     bool ok = true;
 
     // tile loads of unit (item w_, value head jj_ of its group), in three groups by the point where the
@@ -326,7 +328,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
         }
         if (jj == 0) {
 #pragma unroll
-            for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+            for (int i = 0; i < 32; ++i) acc[i] = 0.f;
         }
         if (tid < C) {
             f(F_G, tid) = gnext;
@@ -344,8 +346,10 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             break;
         }
         if (jj == 0 && p.l2norm) {
-            l2norm64<T>(sb + S_Q0, valid, warp, lane, &f(F_IQ, 0));
-            l2norm64<T>(sb + S_K0, valid, warp, lane, &f(F_IK, 0));
+            if (warp < 8) {
+                l2norm64<T>(sb + S_Q0, valid, warp, lane, &f(F_IQ, 0));
+                l2norm64<T>(sb + S_K0, valid, warp, lane, &f(F_IK, 0));
+            }
         }
         const float Gl = f(F_G, valid - 1);
         if (tid < C) {
@@ -354,7 +358,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
         }
         // AKG = A with column s scaled by beta_s e^{G_s}
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < (C * 8) / NT; ++u) {
             const int cix = tid + u * NT, rr = cix >> 3, c = cix & 7;
             const uint32_t o = umma::off(rr, c * 8, 0);
             uint4 a = umma::ld_shared_v4(sb + S_A + o);
@@ -391,10 +395,10 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
         if (!upper) {
             const float sc = p.scale * f(F_EG, r);
 #pragma unroll
-            for (int c = 0; c < 64; c += 16) {
+            for (int c = 0; c < 32; c += 16) {
                 float x[16], qv[16];
-                umma::ld16(umma::taddr(tmem, lb, T_R1 + hh * 64 + c), x);
-                load16<T>(sb + S_Q0 + hh * 16384, r, c, qv);
+                umma::ld16(umma::taddr(tmem, lb, T_R1 + qc * 32 + c), x);
+                load16<T>(sb + S_Q0 + (qc >> 1) * 16384, r, (qc & 1) * 32 + c, qv);
                 umma::ld_wait();
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
@@ -406,35 +410,36 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             // dS = scale dP o Gamma o M  (dP = dO Delta^T in columns 64..127 of R3);
             // E = dS o (Q K^T) = dP o P gives the decay terms of dG (row sums minus column sums)
             const float gr = f(F_G, r);
-            float ev[32], er = 0.f;
-#pragma unroll
-            for (int c = 0; c < 32; c += 16) {
+            float ev[16], er = 0.f;
+            {
+                const int c = 0;
                 float x[16], qk[16];
-                umma::ld16(umma::taddr(tmem, lb, T_R3 + 64 + hh * 32 + c), x);
-                umma::ld16(umma::taddr(tmem, lb, T_R4 + hh * 32 + c), qk);
+                umma::ld16(umma::taddr(tmem, lb, T_R3 + 64 + qc * 16), x);
+                umma::ld16(umma::taddr(tmem, lb, T_R4 + qc * 16), qk);
                 umma::ld_wait();
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
-                    const int s = hh * 32 + c + u;
+                    const int s = qc * 16 + u;
                     x[u] = (s <= r && r < valid) ? p.scale * x[u] * __expf(gr - f(F_G, s)) : 0.f;
                     ev[c + u] = x[u] * qk[u];
                     er += ev[c + u];
                 }
-                store16<T>(sb + S_DS, r, hh * 32 + c, x);
+                store16<T>(sb + S_DS, r, qc * 16 + c, x);
             }
-            f(F_ER0 + hh, r) = er;
-            f(F_EC0 + (warp & 1), hh * 32 + lane) = colsum32(ev, lane);
+            f(F_ER0 + qc, r) = er;
+            const float cs = colsum16(ev, lane);
+            if (lane < 16) f(F_EC0 + (warp & 1), qc * 16 + lane) = cs;
         } else {
             // dW = -(dDelta h^T) rows; dk += e^{Gl - G_r} Delta dH'^T
-            const uint32_t wblk = hh ? S_DW1 : S_DW0;
+            const uint32_t wblk = (qc >> 1) ? S_DW1 : S_DW0;
             const float el = f(F_EL, r);
             float z = 0.f;  // e^{Gl-G_r} <(Delta dH'^T)_r, k_r>: dG terms of the decayed keys
 #pragma unroll
-            for (int c = 0; c < 64; c += 16) {
+            for (int c = 0; c < 32; c += 16) {
                 float x[16], y[16], kv[16];
-                umma::ld16(umma::taddr(tmem, lb, T_R1 + hh * 64 + c), x);
-                umma::ld16(umma::taddr(tmem, lb, T_R2 + hh * 64 + c), y);
-                load16<T>(sb + S_K0 + hh * 16384, r, c, kv);
+                umma::ld16(umma::taddr(tmem, lb, T_R1 + qc * 32 + c), x);
+                umma::ld16(umma::taddr(tmem, lb, T_R2 + qc * 32 + c), y);
+                load16<T>(sb + S_K0 + (qc >> 1) * 16384, r, (qc & 1) * 32 + c, kv);
                 umma::ld_wait();
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
@@ -442,16 +447,16 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                     acc[c + u] += el * y[u];
                     z += el * y[u] * kv[u];
                 }
-                store16<T>(sb + wblk, r, c, x);
+                store16<T>(sb + wblk, r, (qc & 1) * 32 + c, x);
             }
-            f(F_Z0 + hh, r) = z;
+            f(F_Z0 + qc, r) = z;
         }
         {
             // <dH', h> over the whole state (both tiles share one layout, so equal offsets hold equal elements);
             // consecutive threads read consecutive 8-byte words (no bank conflicts)
             float hd = 0.f;
 #pragma unroll 4
-            for (int u = 0; u < 16; ++u) {
+            for (int u = 0; u < (DK * DV * 2 / 8) / NT; ++u) {
                 const uint32_t o = (uint32_t)(u * NT + tid) * 8u;
                 const uint2 a = *reinterpret_cast<const uint2 *>(smem + S_H + o);
                 const uint2 b = *reinterpret_cast<const uint2 *>(smem + S_DH + o);
@@ -490,14 +495,14 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
         if (!upper) {
             // dDelta-side: ddelta = A^T dDelta (columns 0..127), A^T dW (128..255)
             const float br = f(F_B, r);
-            T *dvrow = static_cast<T *>(p.dv) + ((tok0 + r) * Hv + j) * DV + hh * 64;
+            T *dvrow = static_cast<T *>(p.dv) + ((tok0 + r) * Hv + j) * DV + qc * 32;
 #pragma unroll
-            for (int c = 0; c < 64; c += 16) {
+            for (int c = 0; c < 32; c += 16) {
                 float x[16], y[16], vv[16], kv[16];
-                umma::ld16(umma::taddr(tmem, lb, T_R1 + hh * 64 + c), x);
-                umma::ld16(umma::taddr(tmem, lb, T_R1 + 128 + hh * 64 + c), y);
-                load16<T>(sb + S_V0 + hh * 16384, r, c, vv);
-                load16<T>(sb + S_K0 + hh * 16384, r, c, kv);
+                umma::ld16(umma::taddr(tmem, lb, T_R1 + qc * 32 + c), x);
+                umma::ld16(umma::taddr(tmem, lb, T_R1 + 128 + qc * 32 + c), y);
+                load16<T>(sb + S_V0 + (qc >> 1) * 16384, r, (qc & 1) * 32 + c, vv);
+                load16<T>(sb + S_K0 + (qc >> 1) * 16384, r, (qc & 1) * 32 + c, kv);
                 umma::ld_wait();
                 uint32_t w[8];
 #pragma unroll
@@ -515,25 +520,25 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
         } else {
             // dk += (A diag(beta e^G))^T dW ; dA = beta_s (e^{G_s} dW K^T + dDelta V^T), strictly lower
 #pragma unroll
-            for (int c = 0; c < 64; c += 16) {
+            for (int c = 0; c < 32; c += 16) {
                 float x[16];
-                umma::ld16(umma::taddr(tmem, lb, T_R1 + 128 + hh * 64 + c), x);
+                umma::ld16(umma::taddr(tmem, lb, T_R1 + 128 + qc * 32 + c), x);
                 umma::ld_wait();
 #pragma unroll
                 for (int u = 0; u < 16; ++u) acc[c + u] += x[u];
             }
-#pragma unroll
-            for (int c = 0; c < 32; c += 16) {
+            {
+                const int c = 0;
                 float x1[16], x2[16];
-                umma::ld16(umma::taddr(tmem, lb, T_R8 + hh * 32 + c), x1);
-                umma::ld16(umma::taddr(tmem, lb, T_R3 + hh * 32 + c), x2);
+                umma::ld16(umma::taddr(tmem, lb, T_R8 + qc * 16), x1);
+                umma::ld16(umma::taddr(tmem, lb, T_R3 + qc * 16), x2);
                 umma::ld_wait();
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
-                    const int s = hh * 32 + c + u;
+                    const int s = qc * 16 + u;
                     x1[u] = (s < r && r < valid) ? f(F_B, s) * (f(F_EG, s) * x1[u] + x2[u]) : 0.f;
                 }
-                store16<T>(sb + S_DA, r, hh * 32 + c, x1);
+                store16<T>(sb + S_DA, r, qc * 16 + c, x1);
             }
         }
         sync_tc();
@@ -554,26 +559,25 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             break;
         }
         if (!upper) {
+            {
+                float x[16];
+                umma::ld16(umma::taddr(tmem, lb, T_R8 + qc * 16), x);
+                umma::ld_wait();
+                store16<T>(sb + S_X, r, qc * 16, x);
+            }
 #pragma unroll
             for (int c = 0; c < 32; c += 16) {
                 float x[16];
-                umma::ld16(umma::taddr(tmem, lb, T_R8 + hh * 32 + c), x);
-                umma::ld_wait();
-                store16<T>(sb + S_X, r, hh * 32 + c, x);
-            }
-#pragma unroll
-            for (int c = 0; c < 64; c += 16) {
-                float x[16];
-                umma::ld16(umma::taddr(tmem, lb, T_R1 + hh * 64 + c), x);
+                umma::ld16(umma::taddr(tmem, lb, T_R1 + qc * 32 + c), x);
                 umma::ld_wait();
 #pragma unroll
                 for (int u = 0; u < 16; ++u) acc[c + u] += x[u];
             }
         } else {
 #pragma unroll
-            for (int c = 0; c < 64; c += 16) {
+            for (int c = 0; c < 32; c += 16) {
                 float x[16];
-                umma::ld16(umma::taddr(tmem, lb, T_R2 + hh * 64 + c), x);
+                umma::ld16(umma::taddr(tmem, lb, T_R2 + qc * 32 + c), x);
                 umma::ld_wait();
 #pragma unroll
                 for (int u = 0; u < 16; ++u) acc[c + u] += x[u];
@@ -594,16 +598,16 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
         float lb_ = 0.f;  // upper lanes: sum_s dL Gamma KK
         if (upper) {
             const float gr = f(F_G, r), br = f(F_B, r);
-            float fv[32], fr = 0.f;  // F = dL o L: decay terms of dG
-#pragma unroll
-            for (int c = 0; c < 32; c += 16) {
+            float fv[16], fr = 0.f;  // F = dL o L: decay terms of dG
+            {
+                const int c = 0;
                 float x[16], kk[16];
-                umma::ld16(umma::taddr(tmem, lb, T_R8 + hh * 32 + c), x);
-                umma::ld16(umma::taddr(tmem, lb, T_R4 + hh * 32 + c), kk);
+                umma::ld16(umma::taddr(tmem, lb, T_R8 + qc * 16), x);
+                umma::ld16(umma::taddr(tmem, lb, T_R4 + qc * 16), kk);
                 umma::ld_wait();
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
-                    const int s = hh * 32 + c + u;
+                    const int s = qc * 16 + u;
                     const bool m = s < r && r < valid;
                     const float gam = m ? __expf(gr - f(F_G, s)) : 0.f;
                     const float dlv = m ? -x[u] : 0.f;
@@ -612,10 +616,11 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                     fv[c + u] = x[u] * kk[u];
                     fr += fv[c + u];
                 }
-                store16<T>(sb + S_DKK, r, hh * 32 + c, x);
+                store16<T>(sb + S_DKK, r, qc * 16 + c, x);
             }
-            f(F_FR0 + hh, r) = fr;
-            f(F_FC0 + ((warp & 3) - 2), hh * 32 + lane) = colsum32(fv, lane);
+            f(F_FR0 + qc, r) = fr;
+            const float cs = colsum16(fv, lane);
+            if (lane < 16) f(F_FC0 + ((warp & 3) - 2), qc * 16 + lane) = cs;
         }
         sync_tc();
 
@@ -634,18 +639,18 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
         }
         if (upper) {
 #pragma unroll
-            for (int c = 0; c < 64; c += 16) {
+            for (int c = 0; c < 32; c += 16) {
                 float x[16];
-                umma::ld16(umma::taddr(tmem, lb, T_R1 + hh * 64 + c), x);
+                umma::ld16(umma::taddr(tmem, lb, T_R1 + qc * 32 + c), x);
                 umma::ld_wait();
 #pragma unroll
                 for (int u = 0; u < 16; ++u) acc[c + u] += x[u];
             }
-            f(F_LB0 + hh, r) = lb_;
+            f(F_LB0 + qc, r) = lb_;
         } else {
-            f(F_QD0 + hh, r) = qd;
-            f(F_VD0 + hh, r) = vd;
-            f(F_KD0 + hh, r) = kd;
+            f(F_QD0 + qc, r) = qd;
+            f(F_VD0 + qc, r) = vd;
+            f(F_KD0 + qc, r) = kd;
         }
         __syncthreads();
         if (warp == 0) {
@@ -655,24 +660,23 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 const int rr = lane + 32 * hf;
-                const float z = f(F_Z0, rr) + f(F_Z1, rr);
+                auto q4 = [&](int slot0) {  // the four column-quarter partials, in a fixed order
+                    return (f(slot0, rr) + f(slot0 + 1, rr)) + (f(slot0 + 2, rr) + f(slot0 + 3, rr));
+                };
+                const float z = q4(F_Z0);
                 zs += z;
-                const float kd2 = f(F_KD0, rr) + f(F_KD1, rr);
-                const float dG = (f(F_ER0, rr) + f(F_ER1, rr)) - (f(F_EC0, rr) + f(F_EC1, rr)) +
-                                 (f(F_QD0, rr) + f(F_QD1, rr)) - z + f(F_B, rr) * f(F_EG, rr) * kd2 +
-                                 (f(F_FR0, rr) + f(F_FR1, rr)) - (f(F_FC0, rr) + f(F_FC1, rr));
+                const float kd2 = q4(F_KD0);
+                const float dG = q4(F_ER0) - (f(F_EC0, rr) + f(F_EC0 + 1, rr)) + q4(F_QD0) - z +
+                                 f(F_B, rr) * f(F_EG, rr) * kd2 + q4(F_FR0) - (f(F_FC0, rr) + f(F_FC0 + 1, rr));
                 dgv[hf] = rr < valid ? dG : 0.f;
-                if (rr < valid) {
-                    const float vdot = f(F_VD0, rr) + f(F_VD1, rr);
-                    store_gate<T>(p.dbeta, (tok0 + rr) * Hv + j, p.gate_f32,
-                                  f(F_EG, rr) * kd2 + vdot + (f(F_LB0, rr) + f(F_LB1, rr)));
-                }
+                if (rr < valid) store_gate<T>(p.dbeta, (tok0 + rr) * Hv + j, p.gate_f32,
+                                              f(F_EG, rr) * kd2 + q4(F_VD0) + q4(F_LB0));
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);
             float hd = 0.f;
 #pragma unroll
-            for (int wi = 0; wi < 8; ++wi) hd += f(F_HD, wi);
+            for (int wi = 0; wi < NT / 32; ++wi) hd += f(F_HD, wi);
             const float extra = __expf(Gl) * hd + zs;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf)
@@ -700,13 +704,14 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
     // ---- dq (lower lanes) and dk (upper lanes), straight from the registers: with xh the normalised row
     //      (the q or k tile in shared memory) and n its norm, dx = (dxh - xh (xh . dxh)) / n; the two
     //      column halves of a row meet through one partial dot product each
-    const uint32_t xt = sb + (upper ? S_K0 : S_Q0) + hh * 16384;
-    float *dp = &f(F_DP, 0);  // [2 halves][128 lanes]
+    const uint32_t xt = sb + (upper ? S_K0 : S_Q0) + (qc >> 1) * 16384;
+    const int xc = (qc & 1) * 32;  // this thread's key columns within the 64-column block
+    float *dp = &f(F_DP, 0);  // [4 quarters][128 lanes]
     if (ok && p.l2norm) {
         float part = 0.f;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const uint4 u = umma::ld_shared_v4(xt + umma::off(r, c * 8, 0));
+        for (int c = 0; c < 4; ++c) {
+            const uint4 u = umma::ld_shared_v4(xt + umma::off(r, xc + c * 8, 0));
             const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -714,18 +719,18 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                 part = fmaf(x.x, acc[c * 8 + 2 * e], fmaf(x.y, acc[c * 8 + 2 * e + 1], part));
             }
         }
-        dp[hh * 128 + L] = part;
+        dp[qc * 128 + L] = part;
     }
     __syncthreads();
     if (ok && r < valid) {
-        const float dot = p.l2norm ? dp[L] + dp[128 + L] : 0.f;
+        const float dot = p.l2norm ? (dp[L] + dp[128 + L]) + (dp[256 + L] + dp[384 + L]) : 0.f;
         const float inv = p.l2norm ? f(upper ? F_IK : F_IQ, r) : 1.f;
-        T *dst = static_cast<T *>(upper ? p.dk : p.dq) + ((tok0 + r) * Hq + hq) * DK + hh * 64;
+        T *dst = static_cast<T *>(upper ? p.dk : p.dq) + ((tok0 + r) * Hq + hq) * DK + qc * 32;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < 4; ++c) {
             float xv[8];
             if (p.l2norm) {
-                const uint4 u = umma::ld_shared_v4(xt + umma::off(r, c * 8, 0));
+                const uint4 u = umma::ld_shared_v4(xt + umma::off(r, xc + c * 8, 0));
                 const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
