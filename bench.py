@@ -30,6 +30,9 @@ import torch  # noqa: E402
 from gated_delta_rule_38_gb300.inputs import WORKLOADS, make_inputs  # noqa: E402
 
 METRIC = "GDN fwd+bwd tokens/s & TFLOP/s (H=32,K=V=128,bf16) vs roofline, 1xGB300"
+# DRAM bytes (read + write) per launch on the dense workload from one ncu capture of each kernel as it
+# stands (profiles/*_dense_B2_T4096_H32.md); an entry must be removed when its kernel changes.
+NCU_TRAFFIC = {"bwd_chunk": 882.9e6, "chain_pair": 784.7e6, "chain_fwd": 322.3e6}
 C = 64
 L2_BYTES = 129 * 2 ** 20
 
@@ -211,15 +214,18 @@ def run_ours(args):
     name, (cnt, kms) = max(prof.items(), key=lambda kv: kv[1][1])
     per_launch_ms = kms / cnt
     kernel_bytes = {
-        # algorithmic bytes one launch of each kernel must move
+        # algorithmic bytes one launch of each kernel must move: the per-chunk gradient kernel reads every
+        # input of the backward and writes every gradient; the forward recurrence reads the forward's inputs
+        # and writes o
         "bwd_chunk": bwd_b, "chain_fwd": fwd_b, "chain_bwd": bwd_b * 0.5, "chain_fwd_recompute": fwd_b,
-        "wy_fwd": fwd_b * 0.4,
+        "chain_pair": bwd_b * 0.5, "wy_fwd": fwd_b * 0.4, "chunk_p": fwd_b * 0.4,
     }
     kb = kernel_bytes.get(name, fwd_b + bwd_b)
     achieved = kb / (per_launch_ms * 1e-3) / 1e9
+    traffic = NCU_TRAFFIC.get(name) if args.workload == "dense" else None
     roofline = {"kernel": name, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": None, "peak_source": src,
-                "share": round(kms / tot, 3)}
+                "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_source": src,
+                "share": round(kms / tot, 3), "algorithmic_bytes": int(kb)}
     rl_us = max((fwd_b + bwd_b) / (hbm * 1e9), (fwd_f + bwd_f) / (tf_sus * 1e12)) * 1e6
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
