@@ -76,6 +76,25 @@ def work(w, backward=True):
     return (fwd_f, fwd_b, bwd_f, bwd_b) if backward else (fwd_f, fwd_b, 0, 0)
 
 
+def rank_seed(rank: int) -> int:
+    """Each rank draws its own batch (weak scaling over independent streams; no data-path collective)."""
+    return 42 + rank
+
+
+def max_over_ranks(x: float, dist, device) -> float:
+    """The job's time is the slowest rank's (max-reduce; the identity without a process group)."""
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, seconds: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * world / seconds
+
+
 class Clocks:
     """nvidia-smi sampler running during the timed region."""
 
@@ -137,7 +156,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     w = WORKLOADS[args.workload]
     l2 = not w.host_l2
-    x = make_inputs(w, seed=42 + rank)  # every rank: its own batch (weak scaling, no collective)
+    x = make_inputs(w, seed=rank_seed(rank))  # every rank: its own batch (weak scaling, no collective)
     dev = torch.device("cuda", local)
     d = {k: (v.to(dev) if v is not None else None) for k, v in x.items()}
     cu = None if w.cu_seqlens is None else torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
@@ -172,11 +191,7 @@ def run_ours(args):
         torch.cuda.synchronize()
     _lib.profile_enable(False)
     prof = _lib.profile_read()
-    ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / args.steps, dist, dev)
 
     # ---- end to end: pinned host inputs -> device, step, gradients -> host
     keys = ["q", "k", "v", "g", "beta", "do"] + [k for k in ("h0", "dht") if x[k] is not None]
@@ -198,17 +213,13 @@ def run_ours(args):
         outs = [t for t in (o,) + tuple(grads) if t is not None]
         host = [t.to("cpu", non_blocking=False) for t in outs]
     torch.cuda.synchronize()
-    e2e_s = (time.perf_counter() - t0) / args.steps
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, dist, dev)
     d2h = sum(t.numel() * t.element_size() for t in outs)
-    if dist:
-        t = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
 
     fwd_f, fwd_b, bwd_f, bwd_b = work(w)
     hbm, tf_burst, tf_sus, src = peaks()
     tokens = w.tokens * world
-    value = tokens / (ms * 1e-3)
+    value = job_throughput(w.tokens, world, ms * 1e-3)
     # dominant kernel by measured time share
     tot = sum(v[1] for v in prof.values()) or 1.0
     name, (cnt, kms) = max(prof.items(), key=lambda kv: kv[1][1])
