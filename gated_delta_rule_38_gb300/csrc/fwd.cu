@@ -24,6 +24,33 @@ constexpr int LDP = C + 8;  // bf16 row stride of the P staging (bank spread)
 constexpr int WY_SMEM = C * DK * 2 + 2 * C * LDF * 4 + 4 * C * 4;
 static_assert(C * DK * 2 <= C * LDF * 4, "the Q tile must fit under L");
 
+// 1 / sqrt(sum x^2 + eps) of every row r < rows of a [rows x 128] tile (fp32 sums of the stored values);
+// each warp takes 8 rows at a time, lane l a quarter (32 values) of row l/4.
+template <typename T>
+__device__ __forceinline__ void row_inv_norms(const Tile &t, int rows, int warp, int nwarps, int lane, float *inv_out) {
+    const int rq = lane >> 2, qq = lane & 3;
+    for (int r0 = warp * 8; r0 < rows; r0 += nwarps * 8) {
+        const int r = r0 + rq;
+        float ss = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint4 u;
+            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                         : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
+                         : "r"(t.addr(r, qq * 32 + c * 8)));
+            const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 x = Elt<T>::unpack(wv[e]);
+                ss = fmaf(x.x, x.x, fmaf(x.y, x.y, ss));
+            }
+        }
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+        if (r < rows && qq == 0) inv_out[r] = 1.0f / sqrtf(ss + L2_EPS);
+    }
+}
+
 struct WyArgs {
     const void *q, *k, *g, *beta;
     bool gate_f32, l2norm;
@@ -76,9 +103,14 @@ __global__ void __launch_bounds__(128) wy_fwd_kernel(Geo geo, const WyArgs w) {
     }
     cp_async_wait<0>();
     __syncthreads();
+    // inverse L2 norms of the q and k rows (1 without normalisation): the tiles stay as loaded and the
+    // norms enter P and L as row / column factors
     if (w.l2norm) {
-        l2norm_rows<T>(tk, len, warp, 4, lane, sRK);
-        if (want_p) l2norm_rows<T>(tqt, len, warp, 4, lane, sRQ);
+        row_inv_norms<T>(tk, len, warp, 4, lane, sRK);
+        if (want_p) row_inv_norms<T>(tqt, len, warp, 4, lane, sRQ);
+    } else if (tid < C) {
+        sRK[tid] = 1.f;
+        sRQ[tid] = 1.f;
     }
     if (w.full && warp == 0) {
         float x0 = sG[lane], x1 = sG[lane + 32];
@@ -128,9 +160,12 @@ __global__ void __launch_bounds__(128) wy_fwd_kernel(Geo geo, const WyArgs w) {
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const int r = r0 + gq + 8 * hh, s0 = nt * 8 + tq * 2;
-                const float v0 = (s0 <= r && r < len) ? w.scale * __expf(sG[r] - sG[s0]) * acc[nt][2 * hh] : 0.f;
-                const float v1 =
-                    (s0 + 1 <= r && r < len) ? w.scale * __expf(sG[r] - sG[s0 + 1]) * acc[nt][2 * hh + 1] : 0.f;
+                const float rr = w.scale * sRQ[r];
+                const float v0 =
+                    (s0 <= r && r < len) ? rr * sRK[s0] * __expf(sG[r] - sG[s0]) * acc[nt][2 * hh] : 0.f;
+                const float v1 = (s0 + 1 <= r && r < len)
+                                     ? rr * sRK[s0 + 1] * __expf(sG[r] - sG[s0 + 1]) * acc[nt][2 * hh + 1]
+                                     : 0.f;
                 *reinterpret_cast<uint32_t *>(sp + r * LDP + s0) = Elt<T>::pack(v0, v1);
             }
         __syncthreads();
@@ -172,7 +207,7 @@ __global__ void __launch_bounds__(128) wy_fwd_kernel(Geo geo, const WyArgs w) {
                     for (int e = 0; e < 2; ++e) {
                         const int s = nt * 8 + tq * 2 + e;
                         float val = 0.f;
-                        if (s < r && r < len) val = sB[r] * __expf(sG[r] - sG[s]) * acc[nt][2 * hh + e];
+                        if (s < r && r < len) val = sB[r] * sRK[r] * sRK[s] * __expf(sG[r] - sG[s]) * acc[nt][2 * hh + e];
                         Lm[r * LDF + s] = val;
                     }
                 }
