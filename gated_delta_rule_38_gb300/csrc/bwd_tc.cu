@@ -652,6 +652,30 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             f(F_VD0 + qc, r) = vd;
             f(F_KD0 + qc, r) = kd;
         }
+        // the dq / dk partial dot products of the L2-norm chain rule (last value head of the item) go with
+        // the round-5 results, so one barrier serves both the dG reduction and the stores, and warp 0's dG
+        // work overlaps the other warps' stores
+        const bool last_head = jj + 1 == grp;
+    // ---- dq (lower lanes) and dk (upper lanes), straight from the registers: with xh the normalised row
+    //      (the q or k tile in shared memory) and n its norm, dx = (dxh - xh (xh . dxh)) / n; the two
+    //      column halves of a row meet through one partial dot product each
+    const uint32_t xt = sb + (upper ? S_K0 : S_Q0) + (qc >> 1) * 16384;
+    const int xc = (qc & 1) * 32;  // this thread's key columns within the 64-column block
+    float *dp = &f(F_DP, 0);  // [4 quarters][128 lanes]
+    if (last_head && ok && p.l2norm) {
+        float part = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint4 u = umma::ld_shared_v4(xt + umma::off(r, xc + c * 8, 0));
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 x = Elt<T>::unpack(w[e]);
+                part = fmaf(x.x, acc[c * 8 + 2 * e], fmaf(x.y, acc[c * 8 + 2 * e + 1], part));
+            }
+        }
+        dp[qc * 128 + L] = part;
+    }
         __syncthreads();
         if (warp == 0) {
             // dG_r = E row - E column + <q_r, dq_inter_r> - z_r + beta_r e^{G_r} <(A^T dW)_r, k_r>
@@ -699,29 +723,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                 if (rr < valid) store_gate<T>(p.dg, (tok0 + rr) * Hv + j, p.gate_f32, hf ? y1 : y0);
             }
         }
-        __syncthreads();
-        if (jj + 1 == grp) {
-    // ---- dq (lower lanes) and dk (upper lanes), straight from the registers: with xh the normalised row
-    //      (the q or k tile in shared memory) and n its norm, dx = (dxh - xh (xh . dxh)) / n; the two
-    //      column halves of a row meet through one partial dot product each
-    const uint32_t xt = sb + (upper ? S_K0 : S_Q0) + (qc >> 1) * 16384;
-    const int xc = (qc & 1) * 32;  // this thread's key columns within the 64-column block
-    float *dp = &f(F_DP, 0);  // [4 quarters][128 lanes]
-    if (ok && p.l2norm) {
-        float part = 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const uint4 u = umma::ld_shared_v4(xt + umma::off(r, xc + c * 8, 0));
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 x = Elt<T>::unpack(w[e]);
-                part = fmaf(x.x, acc[c * 8 + 2 * e], fmaf(x.y, acc[c * 8 + 2 * e + 1], part));
-            }
-        }
-        dp[qc * 128 + L] = part;
-    }
-    __syncthreads();
+        if (last_head) {
     if (ok && r < valid) {
         const float dot = p.l2norm ? (dp[L] + dp[128 + L]) + (dp[256 + L] + dp[384 + L]) : 0.f;
         const float inv = p.l2norm ? f(upper ? F_IK : F_IQ, r) : 1.f;

@@ -76,7 +76,10 @@ struct Lay {
                               B_MPW = BAR + 48, B_MA = BAR + 56, B_EPIA = BAR + 64, B_MB = BAR + 72,
                               B_EPIB = BAR + 80, B_MO = BAR + 88, B_OFREE = BAR + 104, B_DONE = BAR + 120,
                               B_MPU = BAR + 128;
-    static constexpr uint32_t SLOT = BAR + 136, FLAG = SLOT + 4, USED = FLAG + 12;
+    // the stage is loaded and released in two groups: "early" (q, v, A: done after round A) and "late"
+    // (k, P: done after round B); B_FULL / B_EMPTY belong to the early group
+    static constexpr uint32_t B_FULLL = BAR + 136, B_EMPTYL = BAR + 152;
+    static constexpr uint32_t SLOT = BAR + 168, FLAG = SLOT + 4, USED = FLAG + 12;
     static constexpr uint32_t BYTES = USED + 1024;  // slack for aligning the base
     // TMEM columns
     static constexpr uint32_t T_W = 0, T_D0 = 128, T_D1 = 128 + BV, T_X = 128 + 2 * BV;
@@ -201,6 +204,10 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
         umma::mbar_init(sb + L::B_FULL + 8, 1);
         umma::mbar_init(sb + L::B_EMPTY, 1);
         umma::mbar_init(sb + L::B_EMPTY + 8, 1);
+        umma::mbar_init(sb + L::B_FULLL, 1);
+        umma::mbar_init(sb + L::B_FULLL + 8, 1);
+        umma::mbar_init(sb + L::B_EMPTYL, 1);
+        umma::mbar_init(sb + L::B_EMPTYL + 8, 1);
         umma::mbar_init(sb + L::B_PREP, 4);
         umma::mbar_init(sb + L::B_EPIW, 2);
         umma::mbar_init(sb + L::B_MPW, 1);
@@ -229,28 +236,36 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
     if (warp == 1) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int issued[2] = {0, 0};
+            int issued[2] = {0, 0}, issued_l[2] = {0, 0};
             for (int lc = 0; lc < nc && !*flag; ++lc) {
                 const int s = lc & 1;
-                if (lc >= 2 && !wait_phase(sb + L::B_EMPTY + 8 * s, ((lc >> 1) - 1) & 1, flag, geo.err)) break;
-                const uint32_t st = sb + s * L::ST_BYTES, full = sb + L::B_FULL + 8 * s;
+                const uint32_t st = sb + s * L::ST_BYTES;
                 const int t = (int)(tok0 + (long long)lc * C);
-                tma::expect_tx(full, (WRITE_O ? 16384u + 8192u : 0u) + 16384u + (uint32_t)BV * 128u + 8192u);
+                // early group: free once round A of chunk lc - 2 has run
+                if (lc >= 2 && !wait_phase(sb + L::B_EMPTY + 8 * s, ((lc >> 1) - 1) & 1, flag, geo.err)) break;
+                const uint32_t fe = sb + L::B_FULL + 8 * s, fl = sb + L::B_FULLL + 8 * s;
+                tma::expect_tx(fe, (WRITE_O ? 16384u : 0u) + (uint32_t)BV * 128u + 8192u);
                 if (WRITE_O) {
-                    tma::load3d(st + L::ST_Q0, &p.tq, 0, hq, t, full);
-                    tma::load3d(st + L::ST_Q1, &p.tq, 64, hq, t, full);
-                    tma::load3d(st + L::ST_P, &p.tp, 0, j, t, full);
+                    tma::load3d(st + L::ST_Q0, &p.tq, 0, hq, t, fe);
+                    tma::load3d(st + L::ST_Q1, &p.tq, 64, hq, t, fe);
                 }
-                tma::load3d(st + L::ST_K0, &p.tk, 0, hq, t, full);
-                tma::load3d(st + L::ST_K1, &p.tk, 64, hq, t, full);
-                tma::load3d(st + L::ST_V, &p.tv, v0, j, t, full);
-                if (BV == 128) tma::load3d(st + L::ST_V + 8192, &p.tv, v0 + 64, j, t, full);
-                tma::load3d(st + L::ST_A, &p.ta, 0, j, t, full);
+                tma::load3d(st + L::ST_V, &p.tv, v0, j, t, fe);
+                if (BV == 128) tma::load3d(st + L::ST_V + 8192, &p.tv, v0 + 64, j, t, fe);
+                tma::load3d(st + L::ST_A, &p.ta, 0, j, t, fe);
                 ++issued[s];
+                // late group: free once round B of chunk lc - 2 has run
+                if (lc >= 2 && !wait_phase(sb + L::B_EMPTYL + 8 * s, ((lc >> 1) - 1) & 1, flag, geo.err)) break;
+                tma::expect_tx(fl, 16384u + (WRITE_O ? 8192u : 0u));
+                tma::load3d(st + L::ST_K0, &p.tk, 0, hq, t, fl);
+                tma::load3d(st + L::ST_K1, &p.tk, 64, hq, t, fl);
+                if (WRITE_O) tma::load3d(st + L::ST_P, &p.tp, 0, j, t, fl);
+                ++issued_l[s];
             }
             // let every load in flight land before the block can exit (bounded)
-            for (int s = 0; s < 2; ++s)
+            for (int s = 0; s < 2; ++s) {
                 if (issued[s] > 0) umma::mbar_wait(sb + L::B_FULL + 8 * s, (issued[s] - 1) & 1, 4000000L);
+                if (issued_l[s] > 0) umma::mbar_wait(sb + L::B_FULLL + 8 * s, (issued_l[s] - 1) & 1, 4000000L);
+            }
         }
     } else if (warp == 0) {
         // ------------------------------------------------------------ MMA issue
@@ -276,7 +291,8 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
             };
             bool ok = true;
             if (nc > 0) {
-                ok = wait_phase(sb + L::B_PREP, 0, flag, geo.err) && wait_phase(sb + L::B_FULL, 0, flag, geo.err);
+                ok = wait_phase(sb + L::B_PREP, 0, flag, geo.err) && wait_phase(sb + L::B_FULL, 0, flag, geo.err) &&
+                     wait_phase(sb + L::B_FULLL, 0, flag, geo.err);
                 umma::fence_after();
                 if (ok) {
                     issue_w(0);
@@ -303,6 +319,7 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                 }
                 umma::commit(sb + L::B_MA);
                 mbar_arrive(sb + L::B_MA);
+                umma::commit(sb + L::B_EMPTY + 8 * b);  // q, v and A of this chunk are done
                 // round B as soon as Delta is in shared memory; the next chunk's W group goes in whenever
                 // its inputs are ready, its U group (needed only by the next round A) after round B
                 const bool next = lc + 1 < nc;
@@ -318,13 +335,13 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                             if (WRITE_O) umma::mma(tmem + tD, ap + ks * 2, dDL + ks * 128, id_bv, true);
                         }
                         umma::commit(sb + L::B_MB);
-                        umma::commit(sb + L::B_EMPTY + 8 * b);
+                        umma::commit(sb + L::B_EMPTYL + 8 * b);  // k and P are done
                         umma::commit(sb + L::B_MO + 8 * b);
                         b_done = true;
                         continue;
                     }
                     if (!w_done && mbar_test(sb + L::B_PREP, (lc + 1) & 1) &&
-                        mbar_test(sb + L::B_FULL + 8 * (b ^ 1), ((lc + 1) >> 1) & 1)) {
+                        mbar_test(sb + L::B_FULLL + 8 * (b ^ 1), ((lc + 1) >> 1) & 1)) {
                         umma::fence_after();
                         issue_w(lc + 1);
                         umma::commit(sb + L::B_MPW);
