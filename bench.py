@@ -194,28 +194,47 @@ def run_ours(args):
     prof = _lib.profile_read()
     ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / args.steps, dist, dev)
 
-    # ---- end to end: pinned host inputs -> device, step, gradients -> host
+    # ---- end to end: pinned host inputs -> device, step, every output -> pinned host buffers.  Steps are
+    # pipelined over two device input sets: the copy stream brings step i+1's inputs in while step i
+    # computes, and the read-back stream takes step i's outputs out while step i+1 computes.
     keys = ["q", "k", "v", "g", "beta", "do"] + [k for k in ("h0", "dht") if x[k] is not None]
     hx = {k: x[k].pin_memory() for k in keys}
     h2d = sum(hx[k].numel() * hx[k].element_size() for k in keys)
-    bufs = {k: torch.empty_like(d[k]) for k in keys}
-    outs = None
+    bufs = [{k: torch.empty_like(d[k]) for k in keys} for _ in range(2)]
+    o, grads = step(d)
+    shapes = [t for t in (o,) + tuple(grads) if t is not None]
+    hout = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in shapes] for _ in range(2)]
+    d2h = sum(t.numel() * t.element_size() for t in shapes)
+    copy_s, read_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    buf_free = [None, None]
     for it in range(args.warmup + args.steps):
         if it == args.warmup:
             torch.cuda.synchronize()
             if dist:
                 dist.barrier()
             t0 = time.perf_counter()
-        for k in keys:
-            bufs[k].copy_(hx[k], non_blocking=True)
+        j = it % 2
+        with torch.cuda.stream(copy_s):
+            if buf_free[j] is not None:
+                copy_s.wait_event(buf_free[j])
+            for k in keys:
+                bufs[j][k].copy_(hx[k], non_blocking=True)
+            in_ready[j].record(copy_s)
+        stream.wait_event(in_ready[j])
         dd = dict(d)
-        dd.update(bufs)
+        dd.update(bufs[j])
         o, grads = step(dd)
+        buf_free[j] = torch.cuda.Event()
+        buf_free[j].record(stream)
         outs = [t for t in (o,) + tuple(grads) if t is not None]
-        host = [t.to("cpu", non_blocking=False) for t in outs]
+        with torch.cuda.stream(read_s):
+            read_s.wait_event(buf_free[j])
+            for t, h in zip(outs, hout[j]):
+                h.copy_(t, non_blocking=True)
+                t.record_stream(read_s)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, dist, dev)
-    d2h = sum(t.numel() * t.element_size() for t in outs)
 
     fwd_f, fwd_b, bwd_f, bwd_b = work(w)
     hbm, tf_burst, tf_sus, src = peaks()

@@ -1,12 +1,14 @@
 // Per-chunk gradients of the chunked gated delta rule on tcgen05, and the
 // sequence-level gate-gradient pass.
 //
-// bwd_chunk_tc: one CTA of 256 threads per (chunk, q/k head), visiting the value
-// heads of the group in order.  Tokens are the rows of every product.  Two 64-row
-// operands that share their B operand are stacked into one M=128 MMA, so TMEM
-// lanes 0..63 hold one result and lanes 64..127 the other; dq rows accumulate in
-// the registers of the lane-0..63 threads and dk rows in those of the
-// lane-64..127 threads (each thread holds half a row).  With h the state before
+// bwd_chunk_tc: one persistent CTA of 512 threads per SM walks (chunk, q/k head)
+// items, visiting the value heads of each item's group in order.  Tokens are the
+// rows of every product.  Two 64-row operands that share their B operand are
+// stacked into one M=128 MMA, so TMEM lanes 0..63 hold one result and lanes
+// 64..127 the other; dq rows accumulate in the registers of the lane-0..63
+// threads and dk rows in those of the lane-64..127 threads (each thread holds a
+// quarter of a row).  dq is stored after round 3 of the item's last head, dk
+// after round 5.  With h the state before
 // the chunk, dH' the gradient after it, Delta and dDelta from the two chains:
 //
 //   round 1: [dO;dDelta] h^T        -> dq += scale e^{G} dO h^T ;  dW = -dDelta h^T
@@ -67,7 +69,8 @@ template <> struct IsBf16<__nv_bfloat16> { static constexpr bool value = true; }
 struct BcP {
     // TMA maps: q, k [tokens][Hq][128]; dO, v [tokens][Hv][128]; A [tokens][Hv][64];
     // states h, dH' [rows*Hv][128][128]; Delta, dDelta [rows*Hv][64][128]
-    CUtensorMap tq, tk, tdo, tv, ta, th, tdh, td, tdd;
+    // outputs dq, dk [tokens][Hq][128], dv [tokens][Hv][128] (full chunks leave by TMA stores)
+    CUtensorMap tq, tk, tdo, tv, ta, th, tdh, td, tdd, tdq, tdk, tdv;
     const void *q, *k, *v, *A, *beta, *dout, *h, *dhn, *delta, *ddelta;
     const float *g_cs;
     void *dq, *dk, *dv, *dg, *dbeta;
@@ -117,7 +120,16 @@ __device__ __forceinline__ void load16(uint32_t base, int row, int col0, float *
     }
 }
 
+// A gate element's raw bits (bf16 / fp16 in the low half) as a float.
+template <typename T> __device__ __forceinline__ float bits_to_f(uint32_t b);
+template <> __device__ __forceinline__ float bits_to_f<__nv_bfloat16>(uint32_t b) { return __uint_as_float(b << 16); }
+template <> __device__ __forceinline__ float bits_to_f<__half>(uint32_t b) {
+    return __half2float(__ushort_as_half((unsigned short)b));
+}
+
 // In-place L2 normalisation of 64 rows of a [64 x 128] swizzled tile (blocks 16 KB apart).
+// Eight warps per tile, four lanes per row; lane quarter qq takes 16-byte chunks 2qq, 2qq+1 of each 64-column
+// block, so the eight lanes of a quarter-warp access hit eight distinct bank groups.
 template <typename T>
 __device__ __forceinline__ void l2norm64(uint32_t base, int rows, int warp, int lane, float *inv_out) {
     const int rq = lane >> 2, qq = lane & 3;
@@ -126,8 +138,7 @@ __device__ __forceinline__ void l2norm64(uint32_t base, int rows, int warp, int 
     uint4 u[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        const int ch = qq * 4 + c;
-        addr[c] = base + (uint32_t)(ch >> 3) * 16384u + umma::off(r, (ch & 7) * 8, 0);
+        addr[c] = base + (uint32_t)(c >> 1) * 16384u + umma::off(r, (qq * 2 + (c & 1)) * 8, 0);
         u[c] = umma::ld_shared_v4(addr[c]);
     }
     float ss = 0.f;
@@ -184,6 +195,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int L = (warp & 3) * 32 + lane, qc = warp >> 2, lb = (warp & 3) * 32;  // qc: column quarter
     const bool upper = L >= 64;
+    const int uw = (warp >> 2) * 2 + (warp & 1);  // index of this warp among the upper (or lower) eight
     const int r = L & 63;  // token row of this thread's TMEM lane
     constexpr bool bf16 = IsBf16<T>::value;
     float *F = reinterpret_cast<float *>(smem + S_F);
@@ -291,21 +303,94 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             }
         }
     };
-    // gates of a unit (threads 0..63), fetched one unit ahead into registers
-    float gnext = 0.f, bnext = 0.f;
+    // gates of a unit (threads GT..GT+63), fetched one unit ahead as raw loads that are converted only at the
+    // next unit's top, so no thread waits for them in the middle of a unit
+    constexpr int GT = 64;
+    // (each value is written by its own predicated load and read by nothing before that point)
+    float gnext = 0.f, bnext32 = 0.f;
+    uint32_t bnext16 = 0u;
     auto fetch_gates = [&](long w_, int jj_) {
-        if (tid < C) {
+        const int i = tid - GT;
+        if (i >= 0 && i < C) {
             long long t_;
             int v_, n_, c_;
             geo.chunk((int)(w_ / Hq), t_, v_, n_, c_);
-            const long long ti = (t_ + tid) * Hv + (int)(w_ % Hq) * grp + jj_;
-            gnext = tid < v_ ? p.g_cs[ti] : 0.f;
-            bnext = tid < v_ ? load_gate<T>(p.beta, ti, p.gate_f32) : 0.f;
+            const long long ti = (t_ + i) * Hv + (int)(w_ % Hq) * grp + jj_;
+            gnext = 0.f;
+            bnext32 = 0.f;
+            bnext16 = 0u;
+            if (i < v_) gnext = p.g_cs[ti];
+            if (i < v_ && p.gate_f32) bnext32 = static_cast<const float *>(p.beta)[ti];
+            if (i < v_ && !p.gate_f32) bnext16 = static_cast<const unsigned short *>(p.beta)[ti];
         }
     };
+    // the tile loads of groups 1 and 3 are issued by thread TT (an upper-lane thread, whose epilogues are the
+    // lighter ones), those of group 2 by the MMA thread right after it has issued round 3
+    constexpr int TT = 64;
+    // Full chunks (64 valid rows) leave through shared memory: the rows are written into freed operand blocks in
+    // the tile layout and thread ST (a lower-lane thread) stores them with TMA; a ragged chunk's rows are stored
+    // directly (its tail rows belong to the next sequence).  Staging blocks: dv -> dW's (after round 2),
+    // dq -> X and dW0 (after round 4), dk -> dS and dW1 (after round 5).  ST waits for its stores to finish
+    // reading before a barrier that precedes the next writes to those blocks.
+    constexpr int ST = 32;
+    // dq (lower lanes) / dk (upper lanes) rows, straight from the registers: with xh the normalised row (the q
+    // or k tile in shared memory) and n its norm, dx = (dxh - xh (xh . dxh)) / n; the four column quarters of a
+    // row meet through one partial dot product each
+    const uint32_t xt = sb + (upper ? S_K0 : S_Q0) + (qc >> 1) * 16384;
+    const int xc = (qc & 1) * 32;  // this thread's key columns within the 64-column block
+    float *dp = &f(F_DP, 0);       // [4 quarters][128 lanes]
+    auto dot_partial = [&]() {
+        float part = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint4 u = umma::ld_shared_v4(xt + umma::off(r, xc + c * 8, 0));
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 x = Elt<T>::unpack(w[e]);
+                part = fmaf(x.x, acc[c * 8 + 2 * e], fmaf(x.y, acc[c * 8 + 2 * e + 1], part));
+            }
+        }
+        dp[qc * 128 + L] = part;
+    };
+    auto store_row = [&](long long tok0_, int valid_, int hq_) {
+        const bool staged = valid_ == C;
+        if (!staged && r >= valid_) return;
+        const float dot = p.l2norm ? (dp[L] + dp[128 + L]) + (dp[256 + L] + dp[384 + L]) : 0.f;
+        const float inv = p.l2norm ? f(upper ? F_IK : F_IQ, r) : 1.f;
+        T *dst = static_cast<T *>(upper ? p.dk : p.dq) + ((tok0_ + r) * Hq + hq_) * DK + qc * 32;
+        const uint32_t stg = sb + (upper ? ((qc >> 1) ? S_DW1 : S_DS) : ((qc >> 1) ? S_DW0 : S_X));
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float xv[8];
+            if (p.l2norm) {
+                const uint4 u = umma::ld_shared_v4(xt + umma::off(r, xc + c * 8, 0));
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 x = Elt<T>::unpack(w[e]);
+                    xv[2 * e] = x.x;
+                    xv[2 * e + 1] = x.y;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xv[e] = 0.f;
+            }
+            uint32_t o4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                o4[e] = Elt<T>::pack((acc[c * 8 + 2 * e] - xv[2 * e] * dot) * inv,
+                                     (acc[c * 8 + 2 * e + 1] - xv[2 * e + 1] * dot) * inv);
+            if (staged)
+                umma::st_shared_v4(stg + umma::off(r, xc + c * 8, 0), o4[0], o4[1], o4[2], o4[3]);
+            else
+                *reinterpret_cast<uint4 *>(dst + c * 8) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+        }
+    };
+
     int jj = 0;
     bool posted = false;  // a unit's loads are announced and not yet waited for
-    if (tid == 0) {
+    if (tid == TT) {
         issue(wit, 0, 1);
         issue(wit, 0, 2);
         issue(wit, 0, 3);
@@ -319,6 +404,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
         const int slot = (int)(wit / Hq), hq = (int)(wit % Hq);
         geo.chunk(slot, tok0, valid, n, ci);
         const int j = hq * grp + jj;
+        const bool last_head = jj + 1 == grp;  // dq and dk of the item are complete in this unit
         // the unit after this one
         long wn = wit;
         int jn = jj + 1;
@@ -330,9 +416,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
 #pragma unroll
             for (int i = 0; i < 32; ++i) acc[i] = 0.f;
         }
-        if (tid < C) {
-            f(F_G, tid) = gnext;
-            f(F_B, tid) = bnext;
+        if (tid >= GT && tid < GT + C) {
+            f(F_G, tid - GT) = gnext;
+            f(F_B, tid - GT) = p.gate_f32 ? bnext32 : bits_to_f<T>(bnext16);
         }
         if (!umma::mbar_wait(lbar, lphase)) {
             raise_error(geo.err, GDR_ERR_TIMEOUT);
@@ -340,17 +426,14 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
         }
         lphase ^= 1u;
         posted = false;
+        if (tid == ST) tma::wait_read();  // the previous unit's dq / dk staging blocks are free again
         __syncthreads();
         if (*sflag) {
             ok = false;
             break;
         }
-        if (jj == 0 && p.l2norm) {
-            if (warp < 8) {
-                l2norm64<T>(sb + S_Q0, valid, warp, lane, &f(F_IQ, 0));
-                l2norm64<T>(sb + S_K0, valid, warp, lane, &f(F_IK, 0));
-            }
-        }
+        if (jj == 0 && p.l2norm)  // warps 0..7 normalise the q rows, warps 8..15 the k rows
+            l2norm64<T>(sb + (warp < 8 ? S_Q0 : S_K0), valid, warp & 7, lane, &f(warp < 8 ? F_IQ : F_IK, 0));
         const float Gl = f(F_G, valid - 1);
         if (tid < C) {
             f(F_EG, tid) = __expf(f(F_G, tid));
@@ -451,13 +534,15 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             }
             f(F_Z0 + qc, r) = z;
         }
-        {
-            // <dH', h> over the whole state (both tiles share one layout, so equal offsets hold equal elements);
-            // consecutive threads read consecutive 8-byte words (no bank conflicts)
+        if (upper) {
+            // <dH', h> over the whole state (both tiles share one layout, so equal offsets hold equal elements),
+            // on the upper-lane warps, whose round-1 epilogue is the shorter one; consecutive threads read
+            // consecutive 8-byte words (no bank conflicts)
+            const int ut = uw * 32 + lane;
             float hd = 0.f;
 #pragma unroll 4
-            for (int u = 0; u < (DK * DV * 2 / 8) / NT; ++u) {
-                const uint32_t o = (uint32_t)(u * NT + tid) * 8u;
+            for (int u = 0; u < (DK * DV * 2 / 8) / (NT / 2); ++u) {
+                const uint32_t o = (uint32_t)(u * (NT / 2) + ut) * 8u;
                 const uint2 a = *reinterpret_cast<const uint2 *>(smem + S_H + o);
                 const uint2 b = *reinterpret_cast<const uint2 *>(smem + S_DH + o);
                 const float2 a0 = Elt<T>::unpack(a.x), a1 = Elt<T>::unpack(a.y);
@@ -466,15 +551,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, o);
-            if (lane == 0) f(F_HD, warp) = hd;
+            if (lane == 0) f(F_HD, uw) = hd;
         }
         sync_tc();
-        // h, dH' and dO are free: the next unit's first tile group
-        if (wn >= 0) {
-            if (tid == 0) issue(wn, jn, 1);
-            posted = true;
-            fetch_gates(wn, jn);
-        }
 
         // ---------------- round 2
         if (tid == 0) {
@@ -486,6 +565,12 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                 umma::mma(tmem + T_R8, dWup + ko, dKa + ko, i_n64, ks > 0);
             }
             umma::commit(bar);
+        }
+        // h, dH' and dO are free: the next unit's first tile group
+        if (wn >= 0) {
+            if (tid == TT) issue(wn, jn, 1);
+            posted = true;
+            fetch_gates(wn, jn);
         }
         if (!wait_mma()) {
             ok = false;
@@ -512,9 +597,23 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                 }
 #pragma unroll
                 for (int u = 0; u < 8; ++u) w[u] = Elt<T>::pack(x[2 * u] * br, x[2 * u + 1] * br);
-                if (r < valid) {
+                if (valid == C) {
+                    const uint32_t stg = sb + ((qc >> 1) ? S_DW1 : S_DW0);
+                    const int col = (qc & 1) * 32 + c;
+                    umma::st_shared_v4(stg + umma::off(r, col, 0), w[0], w[1], w[2], w[3]);
+                    umma::st_shared_v4(stg + umma::off(r, col + 8, 0), w[4], w[5], w[6], w[7]);
+                } else if (r < valid) {
                     *reinterpret_cast<uint4 *>(dvrow + c) = make_uint4(w[0], w[1], w[2], w[3]);
                     *reinterpret_cast<uint4 *>(dvrow + c + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+                }
+            }
+            if (valid == C) {
+                umma::fence_async_smem();
+                asm volatile("bar.sync 2, 256;\n" ::: "memory");  // the eight lower-lane warps
+                if (tid == ST) {
+                    tma::store3d(&p.tdv, 0, j, (int)tok0, sb + S_DW0);
+                    tma::store3d(&p.tdv, 64, j, (int)tok0, sb + S_DW1);
+                    tma::commit_group();
                 }
             }
         } else {
@@ -542,7 +641,6 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             }
         }
         sync_tc();
-        if (tid == 0 && wn >= 0) issue(wn, jn, 2);  // V and dDelta are free
 
         // ---------------- round 3: X = dA A^T ; dq += dS K ; dk += dS^T Q
         if (tid == 0) {
@@ -553,6 +651,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                 umma::mma(tmem + T_R2, dDSup + ks * 128, dQmn + ks * 128, i_n128_mn, ks > 0);
             }
             umma::commit(bar);
+            // V and dDelta are free (round 3 reads V's second block only as the unread partner rows of dA)
+            if (wn >= 0) issue(wn, jn, 2);
         }
         if (!wait_mma()) {
             ok = false;
@@ -621,6 +721,21 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             f(F_FR0 + qc, r) = fr;
             const float cs = colsum16(fv, lane);
             if (lane < 16) f(F_FC0 + ((warp & 3) - 2), qc * 16 + lane) = cs;
+        } else if (last_head) {
+            // dq is complete after round 3: the lower-lane warps store it while the upper ones work on dKK
+            if (p.l2norm) dot_partial();
+            if (tid == ST) tma::wait_read();  // dv's staging block dW0 is free again
+            asm volatile("bar.sync 2, 256;\n" ::: "memory");  // the eight lower-lane warps
+            store_row(tok0, valid, hq);
+            if (valid == C) {
+                umma::fence_async_smem();
+                asm volatile("bar.sync 2, 256;\n" ::: "memory");
+                if (tid == ST) {
+                    tma::store3d(&p.tdq, 0, hq, (int)tok0, sb + S_X);
+                    tma::store3d(&p.tdq, 64, hq, (int)tok0, sb + S_DW0);
+                    tma::commit_group();
+                }
+            }
         }
         sync_tc();
 
@@ -652,117 +767,64 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             f(F_VD0 + qc, r) = vd;
             f(F_KD0 + qc, r) = kd;
         }
-        // the dq / dk partial dot products of the L2-norm chain rule (last value head of the item) go with
-        // the round-5 results, so one barrier serves both the dG reduction and the stores, and warp 0's dG
-        // work overlaps the other warps' stores
-        const bool last_head = jj + 1 == grp;
-    // ---- dq (lower lanes) and dk (upper lanes), straight from the registers: with xh the normalised row
-    //      (the q or k tile in shared memory) and n its norm, dx = (dxh - xh (xh . dxh)) / n; the two
-    //      column halves of a row meet through one partial dot product each
-    const uint32_t xt = sb + (upper ? S_K0 : S_Q0) + (qc >> 1) * 16384;
-    const int xc = (qc & 1) * 32;  // this thread's key columns within the 64-column block
-    float *dp = &f(F_DP, 0);  // [4 quarters][128 lanes]
-    if (last_head && ok && p.l2norm) {
-        float part = 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const uint4 u = umma::ld_shared_v4(xt + umma::off(r, xc + c * 8, 0));
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 x = Elt<T>::unpack(w[e]);
-                part = fmaf(x.x, acc[c * 8 + 2 * e], fmaf(x.y, acc[c * 8 + 2 * e + 1], part));
-            }
-        }
-        dp[qc * 128 + L] = part;
-    }
+        // dk's partial dot products of the L2-norm chain rule go with the round-5 results, so one barrier
+        // serves both the dG reduction and the dk stores
+        if (upper && last_head && p.l2norm) dot_partial();
         __syncthreads();
-        if (warp == 0) {
+        if (warp < 2) {
             // dG_r = E row - E column + <q_r, dq_inter_r> - z_r + beta_r e^{G_r} <(A^T dW)_r, k_r>
-            //        + F row - F column; the last valid row adds e^{Gl} <dH', h> + sum_s z_s
-            float dgv[2], zs = 0.f;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int rr = lane + 32 * hf;
-                auto q4 = [&](int slot0) {  // the four column-quarter partials, in a fixed order
-                    return (f(slot0, rr) + f(slot0 + 1, rr)) + (f(slot0 + 2, rr) + f(slot0 + 3, rr));
-                };
-                const float z = q4(F_Z0);
-                zs += z;
-                const float kd2 = q4(F_KD0);
-                const float dG = q4(F_ER0) - (f(F_EC0, rr) + f(F_EC0 + 1, rr)) + q4(F_QD0) - z +
-                                 f(F_B, rr) * f(F_EG, rr) * kd2 + q4(F_FR0) - (f(F_FC0, rr) + f(F_FC0 + 1, rr));
-                dgv[hf] = rr < valid ? dG : 0.f;
-                if (rr < valid) store_gate<T>(p.dbeta, (tok0 + rr) * Hv + j, p.gate_f32,
-                                              f(F_EG, rr) * kd2 + q4(F_VD0) + q4(F_LB0));
-            }
+            //        + F row - F column; every valid row's dg also carries e^{Gl} <dH', h> + sum_s z_s (the
+            //        last valid row's extra terms, summed backwards).  Warp w takes rows 32w..32w+31.
+            const int rr = warp * 32 + lane;
+            const bool vr = rr < valid;
+            auto q4 = [&](int slot0) {  // the four column-quarter partials, in a fixed order
+                return (f(slot0, rr) + f(slot0 + 1, rr)) + (f(slot0 + 2, rr) + f(slot0 + 3, rr));
+            };
+            const float z = q4(F_Z0);
+            const float kd2 = q4(F_KD0);
+            const float dG = q4(F_ER0) - (f(F_EC0, rr) + f(F_EC0 + 1, rr)) + q4(F_QD0) - z +
+                             f(F_B, rr) * f(F_EG, rr) * kd2 + q4(F_FR0) - (f(F_FC0, rr) + f(F_FC0 + 1, rr));
+            if (vr)
+                store_gate<T>(p.dbeta, (tok0 + rr) * Hv + j, p.gate_f32, f(F_EG, rr) * kd2 + q4(F_VD0) + q4(F_LB0));
+            float zs = vr ? z : 0.f;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);
-            float hd = 0.f;
-#pragma unroll
-            for (int wi = 0; wi < NT / 32; ++wi) hd += f(F_HD, wi);
-            const float extra = __expf(Gl) * hd + zs;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf)
-                if (lane + 32 * hf == valid - 1) dgv[hf] += extra;
-            // dg_s = sum_{r >= s} dG_r within the chunk
-            float y1 = dgv[1], y0 = dgv[0];
+            // dg_s = sum_{r >= s} dG_r within the chunk: suffix sums inside the warp, then warp 1's total
+            float y = vr ? dG : 0.f;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const float t1 = __shfl_down_sync(0xffffffffu, y1, o);
-                const float t0 = __shfl_down_sync(0xffffffffu, y0, o);
-                if (lane + o < 32) {
-                    y1 += t1;
-                    y0 += t0;
-                }
+                const float t = __shfl_down_sync(0xffffffffu, y, o);
+                if (lane + o < 32) y += t;
             }
-            y0 += __shfl_sync(0xffffffffu, y1, 0);
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                const int rr = lane + 32 * hf;
-                if (rr < valid) store_gate<T>(p.dg, (tok0 + rr) * Hv + j, p.gate_f32, hf ? y1 : y0);
+            if (lane == 0) {
+                f(F_DG, 2 * warp) = zs;
+                f(F_DG, 2 * warp + 1) = y;
             }
+            asm volatile("bar.sync 1, 64;\n" ::: "memory");  // warps 0 and 1
+            float hd = 0.f;
+#pragma unroll
+            for (int wi = 0; wi < 8; ++wi) hd += f(F_HD, wi);
+            const float extra = __expf(Gl) * hd + (f(F_DG, 0) + f(F_DG, 2));
+            const float tail = warp == 0 ? f(F_DG, 3) : 0.f;
+            if (vr) store_gate<T>(p.dg, (tok0 + rr) * Hv + j, p.gate_f32, y + tail + extra);
         }
-        if (last_head) {
-    if (ok && r < valid) {
-        const float dot = p.l2norm ? (dp[L] + dp[128 + L]) + (dp[256 + L] + dp[384 + L]) : 0.f;
-        const float inv = p.l2norm ? f(upper ? F_IK : F_IQ, r) : 1.f;
-        T *dst = static_cast<T *>(upper ? p.dk : p.dq) + ((tok0 + r) * Hq + hq) * DK + qc * 32;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float xv[8];
-            if (p.l2norm) {
-                const uint4 u = umma::ld_shared_v4(xt + umma::off(r, xc + c * 8, 0));
-                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 x = Elt<T>::unpack(w[e]);
-                    xv[2 * e] = x.x;
-                    xv[2 * e + 1] = x.y;
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) xv[e] = 0.f;
-            }
-            uint32_t o4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                o4[e] = Elt<T>::pack((acc[c * 8 + 2 * e] - xv[2 * e] * dot) * inv,
-                                     (acc[c * 8 + 2 * e + 1] - xv[2 * e + 1] * dot) * inv);
-            *reinterpret_cast<uint4 *>(dst + c * 8) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
-        }
-    }
-        }
+        if (upper && last_head) store_row(tok0, valid, hq);
         // Delta, A (and q, k for a new item) are free: the next unit's last tile group
         umma::fence_async_smem();
         __syncthreads();
+        if (tid == ST && last_head && valid == C) {
+            tma::store3d(&p.tdk, 0, hq, (int)tok0, sb + S_DS);
+            tma::store3d(&p.tdk, 64, hq, (int)tok0, sb + S_DW1);
+            tma::commit_group();
+        }
         if (wn < 0) break;
-        if (tid == 0) issue(wn, jn, 3);
+        if (tid == TT) issue(wn, jn, 3);
         wit = wn;
         jj = jn;
     }
     // after an error, let a prefetch in flight land before the block exits (bounded)
     if (tid == 0 && posted) umma::mbar_wait(lbar, lphase, 4000000L);
+    if (tid == ST) tma::wait_all();  // the staged output rows are written before shared memory goes away
 
     umma::fence_before();
     __syncthreads();
@@ -801,7 +863,10 @@ cudaError_t launch_bwd_chunk_tc(const Args &a, const void *q, const void *k, con
         !make_tmap_3d(&p.th, h, bf, DV, DK, rows, DV * 2, (uint64_t)DK * DV * 2, 64, 128, 1) ||
         !make_tmap_3d(&p.tdh, dhn, bf, DV, DK, rows, DV * 2, (uint64_t)DK * DV * 2, 64, 128, 1) ||
         !make_tmap_3d(&p.td, delta, bf, DV, C, rows, DV * 2, (uint64_t)C * DV * 2, 64, 64, 1) ||
-        !make_tmap_3d(&p.tdd, ddelta, bf, DV, C, rows, DV * 2, (uint64_t)C * DV * 2, 64, 64, 1))
+        !make_tmap_3d(&p.tdd, ddelta, bf, DV, C, rows, DV * 2, (uint64_t)C * DV * 2, 64, 64, 1) ||
+        !make_tmap_3d(&p.tdq, dq, bf, DK, a.Hq, tokens, DK * 2, (uint64_t)a.Hq * DK * 2, 64, 1, 64) ||
+        !make_tmap_3d(&p.tdk, dk, bf, DK, a.Hq, tokens, DK * 2, (uint64_t)a.Hq * DK * 2, 64, 1, 64) ||
+        !make_tmap_3d(&p.tdv, dv, bf, DV, a.Hv, tokens, DV * 2, (uint64_t)a.Hv * DV * 2, 64, 1, 64))
         return cudaErrorInvalidValue;
     p.q = q;
     p.k = k;

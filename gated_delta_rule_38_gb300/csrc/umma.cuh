@@ -130,6 +130,19 @@ __device__ __forceinline__ void load3d(uint32_t dst, const void *map, int c0, in
         : "memory");
 }
 
+// 3-D tiled bulk tensor store from shared memory (same box and swizzle as the loads), as one bulk group of the
+// issuing thread; `commit_group` closes the group, `wait_read` waits until the thread's groups have finished
+// reading shared memory, `wait_all` until they are complete.
+__device__ __forceinline__ void store3d(const void *map, int c0, int c1, int c2, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];\n" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void commit_group() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+__device__ __forceinline__ void wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+
 // One arrival that also announces `bytes` of transactions on the barrier's current phase.
 __device__ __forceinline__ void expect_tx(uint32_t mbar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mbar), "r"(bytes) : "memory");
