@@ -179,18 +179,35 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
     // Persistent: this CTA walks the work items w = blockIdx.x, + gridDim.x, ... (item = chunk slot x q/k
     // head, each with the grp value heads of its group: one "unit" per value head).  The tiles of the next
     // unit are prefetched into buffers as soon as the current unit is done with them.
-    const long nitems = (long)p.nslots * Hq;
-    auto item_ok = [&](long w_) {
+    // (32-bit item arithmetic: the host keeps chunk slots x Hq below 2^31)
+    const int nitems = p.nslots * Hq;
+    auto item_ok = [&](int w_) {
         long long t_;
         int v_, n_, c_;
-        return geo.chunk((int)(w_ / Hq), t_, v_, n_, c_);
+        return geo.chunk(w_ / Hq, t_, v_, n_, c_);
     };
-    auto next_item = [&](long w_) -> long {
-        for (; w_ < nitems; w_ += gridDim.x)
+    auto next_item = [&](int w_) -> int {
+        for (; w_ < nitems; w_ += (int)gridDim.x)
             if (item_ok(w_)) return w_;
         return -1;
     };
-    long wit = next_item(blockIdx.x);
+    // a unit's place: first token t, valid rows, q/k head, value head, state row (chunk row x Hv + value head)
+    struct Pos {
+        int t, valid, hq, j, row;
+    };
+    auto locate = [&](int w_, int jj_) {
+        Pos u;
+        const int slot_ = w_ / Hq;
+        long long t_;
+        int n_, c_;
+        geo.chunk(slot_, t_, u.valid, n_, c_);
+        u.t = (int)t_;
+        u.hq = w_ - slot_ * Hq;
+        u.j = u.hq * grp + jj_;
+        u.row = slot_ * Hv + u.j;
+        return u;
+    };
+    int wit = next_item(blockIdx.x);
     if (wit < 0) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int L = (warp & 3) * 32 + lane, qc = warp >> 2, lb = (warp & 3) * 32;  // qc: column quarter
@@ -266,18 +283,16 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
     float acc[32];  // dq row (lower lanes) or dk row (upper lanes), key columns 32*qc..
     bool ok = true;
 
-    // tile loads of unit (item w_, value head jj_ of its group), in three groups by the point where the
-    // current unit frees the buffers: 1 = h, dH', dO (after round 1); 2 = V, dDelta (after round 2);
-    // 3 = Delta, A and, for the first head of an item, q and k (after the unit).  All bytes of a unit are
-    // announced on the load barrier with its first group.
+    // tile loads of unit u (value head jj_ of its item's group), in groups by the point where the current
+    // unit frees the buffers: 1 = h, dH', dO (after round 1, beside round 2); 2 = V, dDelta (after round 3 is issued);
+    // 3 = Delta's first column block (the dA block, after round 4 is issued); 4 = A (after round 5 is
+    // issued); 5 = q for the first head of an item (after dq is stored); 6 = k for the first head of an item
+    // and Delta's second column block (the dKK block, after the unit).  All bytes of a unit are announced on
+    // the load barrier with its first group.
     auto unit_bytes = [&](int jj_) -> uint32_t { return 32768u * 2 + 16384u + 16384u * 2 + 16384u + 8192u +
                                                          (jj_ == 0 ? 32768u : 0u); };
-    auto issue = [&](long w_, int jj_, int group) {
-        long long t_;
-        int v_, n_, c_;
-        const int slot_ = (int)(w_ / Hq), hq_ = (int)(w_ % Hq), j_ = hq_ * grp + jj_;
-        geo.chunk(slot_, t_, v_, n_, c_);
-        const int t = (int)t_, row = slot_ * Hv + j_;
+    auto issue = [&](const Pos &u, int jj_, int group) {
+        const int t = u.t, row = u.row, j_ = u.j, hq_ = u.hq;
         if (group == 1) {
             tma::expect_tx(lbar, unit_bytes(jj_));
             tma::load3d(sb + S_H, &p.th, 0, 0, row, lbar);
@@ -291,13 +306,18 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             tma::load3d(sb + S_V0 + 16384, &p.tv, 64, j_, t, lbar);
             tma::load3d(sb + S_DD0, &p.tdd, 0, 0, row, lbar);
             tma::load3d(sb + S_DD0 + 16384, &p.tdd, 64, 0, row, lbar);
-        } else {
+        } else if (group == 3) {
             tma::load3d(sb + S_D0, &p.td, 0, 0, row, lbar);
-            tma::load3d(sb + S_D0 + 16384, &p.td, 64, 0, row, lbar);
+        } else if (group == 4) {
             tma::load3d(sb + S_A, &p.ta, 0, j_, t, lbar);
+        } else if (group == 5) {
             if (jj_ == 0) {
                 tma::load3d(sb + S_Q0, &p.tq, 0, hq_, t, lbar);
                 tma::load3d(sb + S_Q0 + 16384, &p.tq, 64, hq_, t, lbar);
+            }
+        } else {
+            tma::load3d(sb + S_D0 + 16384, &p.td, 64, 0, row, lbar);
+            if (jj_ == 0) {
                 tma::load3d(sb + S_K0, &p.tk, 0, hq_, t, lbar);
                 tma::load3d(sb + S_K0 + 16384, &p.tk, 64, hq_, t, lbar);
             }
@@ -309,13 +329,10 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
     // (each value is written by its own predicated load and read by nothing before that point)
     float gnext = 0.f, bnext32 = 0.f;
     uint32_t bnext16 = 0u;
-    auto fetch_gates = [&](long w_, int jj_) {
-        const int i = tid - GT;
+    auto fetch_gates = [&](const Pos &u) {
+        const int i = tid - GT, v_ = u.valid;
         if (i >= 0 && i < C) {
-            long long t_;
-            int v_, n_, c_;
-            geo.chunk((int)(w_ / Hq), t_, v_, n_, c_);
-            const long long ti = (t_ + i) * Hv + (int)(w_ % Hq) * grp + jj_;
+            const long long ti = ((long long)u.t + i) * Hv + u.j;
             gnext = 0.f;
             bnext32 = 0.f;
             bnext16 = 0u;
@@ -324,8 +341,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             if (i < v_ && !p.gate_f32) bnext16 = static_cast<const unsigned short *>(p.beta)[ti];
         }
     };
-    // the tile loads of groups 1 and 3 are issued by thread TT (an upper-lane thread, whose epilogues are the
-    // lighter ones), those of group 2 by the MMA thread right after it has issued round 3
+    // the tile loads of groups 1 and 6 are issued by thread TT (an upper-lane thread, whose epilogues are the
+    // lighter ones), those of groups 2, 3 and 4 by the MMA thread right after it has issued rounds 3, 4 and 5,
+    // and group 5 by thread ST once dq has left
     constexpr int TT = 64;
     // Full chunks (64 valid rows) leave through shared memory: the rows are written into freed operand blocks in
     // the tile layout and thread ST (a lower-lane thread) stores them with TMA; a ragged chunk's rows are stored
@@ -390,28 +408,25 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
 
     int jj = 0;
     bool posted = false;  // a unit's loads are announced and not yet waited for
-    if (tid == TT) {
-        issue(wit, 0, 1);
-        issue(wit, 0, 2);
-        issue(wit, 0, 3);
-    }
+    Pos cur = locate(wit, 0);
+    if (tid == TT)
+        for (int g = 1; g <= 6; ++g) issue(cur, 0, g);
     posted = true;
-    fetch_gates(wit, 0);
+    fetch_gates(cur);
 
     while (ok) {
-        long long tok0;
-        int valid, n, ci;
-        const int slot = (int)(wit / Hq), hq = (int)(wit % Hq);
-        geo.chunk(slot, tok0, valid, n, ci);
-        const int j = hq * grp + jj;
+        const long long tok0 = cur.t;
+        const int valid = cur.valid, hq = cur.hq, j = cur.j;
         const bool last_head = jj + 1 == grp;  // dq and dk of the item are complete in this unit
-        // the unit after this one
-        long wn = wit;
+        // the unit after this one, located once here (while the tiles are still on their way)
+        int wn = wit;
         int jn = jj + 1;
         if (jn == grp) {
             jn = 0;
-            wn = next_item(wit + gridDim.x);
+            wn = next_item(wit + (int)gridDim.x);
         }
+        Pos nxt = cur;
+        if (wn >= 0) nxt = locate(wn, jn);
         if (jj == 0) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) acc[i] = 0.f;
@@ -568,9 +583,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
         }
         // h, dH' and dO are free: the next unit's first tile group
         if (wn >= 0) {
-            if (tid == TT) issue(wn, jn, 1);
+            if (tid == TT) issue(nxt, jn, 1);
             posted = true;
-            fetch_gates(wn, jn);
+            fetch_gates(nxt);
         }
         if (!wait_mma()) {
             ok = false;
@@ -652,7 +667,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             }
             umma::commit(bar);
             // V and dDelta are free (round 3 reads V's second block only as the unread partner rows of dA)
-            if (wn >= 0) issue(wn, jn, 2);
+            if (wn >= 0) issue(nxt, jn, 2);
         }
         if (!wait_mma()) {
             ok = false;
@@ -690,6 +705,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + T_R8, dAup + ks * 128, dXmn + ks * 128, i_n64_mn, ks > 0);
             umma::commit(bar);
+            if (wn >= 0) issue(nxt, jn, 3);  // round 3 has read dA: Delta's first block is free
         }
         if (!wait_mma()) {
             ok = false;
@@ -727,14 +743,15 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             if (tid == ST) tma::wait_read();  // dv's staging block dW0 is free again
             asm volatile("bar.sync 2, 256;\n" ::: "memory");  // the eight lower-lane warps
             store_row(tok0, valid, hq);
-            if (valid == C) {
-                umma::fence_async_smem();
-                asm volatile("bar.sync 2, 256;\n" ::: "memory");
-                if (tid == ST) {
+            umma::fence_async_smem();
+            asm volatile("bar.sync 2, 256;\n" ::: "memory");
+            if (tid == ST) {
+                if (valid == C) {
                     tma::store3d(&p.tdq, 0, hq, (int)tok0, sb + S_X);
                     tma::store3d(&p.tdq, 64, hq, (int)tok0, sb + S_DW0);
                     tma::commit_group();
                 }
+                if (wn >= 0) issue(nxt, jn, 5);  // the q tile has been read for the last time
             }
         }
         sync_tc();
@@ -747,6 +764,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                 umma::mma(tmem + T_R1, dKKmn + ks * 128, dKmn + ks * 128, i_n128_mn, true);
             }
             umma::commit(bar);
+            if (wn >= 0) issue(nxt, jn, 4);  // round 4 has read A
         }
         if (!wait_mma()) {
             ok = false;
@@ -818,9 +836,10 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             tma::commit_group();
         }
         if (wn < 0) break;
-        if (tid == TT) issue(wn, jn, 3);
+        if (tid == TT) issue(nxt, jn, 6);
         wit = wn;
         jj = jn;
+        cur = nxt;
     }
     // after an error, let a prefetch in flight land before the block exits (bounded)
     if (tid == 0 && posted) umma::mbar_wait(lbar, lphase, 4000000L);
@@ -834,6 +853,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
 template <typename T>
 cudaError_t bwd_chunk_tc_t(const Args &a, const BcP &p, cudaStream_t s) {
     if (a.max_chunks == 0) return cudaSuccess;
+    if ((long long)a.max_chunks * a.Hq >= (1ll << 31)) return cudaErrorInvalidValue;  // 32-bit item indices
     auto kern = bwd_chunk_tc_kernel<T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S_BYTES);
     if (e != cudaSuccess) return e;
