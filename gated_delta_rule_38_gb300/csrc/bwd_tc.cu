@@ -15,8 +15,7 @@
 //            [V;Delta] dH'^T        -> dk += e^{Gl-G} Delta dH'^T
 //            [dO;dDelta] [V;Delta]^T-> dP = dO Delta^T (-> dS = scale dP o Gamma o M), dA2 = dDelta V^T
 //            [Q;K] K^T              -> KK^T
-//   round 2: [A^T;(A diag(beta e^G))^T] [dDelta | dW]
-//                                   -> dv = beta A^T dDelta, A^T dW (dbeta), dk += diag(beta e^G) A^T dW
+//   round 2: [A^T;A^T] [dDelta | dW]  -> dv = beta A^T dDelta, A^T dW (dbeta), dk += diag(beta e^G) A^T dW
 //            dW K^T                 -> dA = (dW K^T diag(e^G) + dDelta V^T) diag(beta), strictly lower
 //   round 3: dA A^T -> X ;  dq += dS K ;  dk += dS^T Q
 //   round 4: dL = -A^T X ;  dKK = dL o beta_r Gamma  ;  dbeta += sum_s dL Gamma KK
@@ -48,9 +47,9 @@ constexpr uint32_t S_X = 65536, S_DW0 = 73728, S_DS = 81920, S_DW1 = 90112;
 constexpr uint32_t S_V0 = 98304, S_D0 = 106496;       // [V b0][Delta b0][V b1][Delta b1]
 constexpr uint32_t S_DA = S_D0, S_DKK = S_D0 + 16384; // reuse Delta's blocks after round 1
 constexpr uint32_t S_H = 131072, S_DH = 163840;       // [128 x 64] blocks of 16 KB
-constexpr uint32_t S_A = 196608, S_AKG = 204800;
+constexpr uint32_t S_A = 196608, S_A2 = 204800;   // A, and a second copy of it (the stacked round-2 operand)
 constexpr uint32_t S_F = 212992;                      // scalars
-constexpr uint32_t S_BAR = S_F + 48 * 64 * 4, S_LBAR = S_BAR + 8, S_SLOT = S_LBAR + 8, S_FLAG = S_SLOT + 4,
+constexpr uint32_t S_BAR = S_F + 50 * 64 * 4, S_LBAR = S_BAR + 8, S_SLOT = S_LBAR + 8, S_FLAG = S_SLOT + 4,
                    S_USED = S_FLAG + 4;
 constexpr uint32_t S_BYTES = S_USED + 1024;
 // scalar slots (64 floats each)
@@ -58,7 +57,7 @@ constexpr uint32_t S_BYTES = S_USED + 1024;
 enum {
     F_G = 0, F_B, F_EG, F_EL, F_QD0, F_VD0 = F_QD0 + 4, F_KD0 = F_VD0 + 4, F_LB0 = F_KD0 + 4, F_ER0 = F_LB0 + 4,
     F_EC0 = F_ER0 + 4, F_Z0 = F_EC0 + 2, F_FR0 = F_Z0 + 4, F_FC0 = F_FR0 + 4, F_HD = F_FC0 + 2, F_DG, F_IQ, F_IK,
-    F_DP, F_COUNT = F_DP + 8
+    F_MQ, F_MK, F_DP, F_COUNT = F_DP + 8
 };
 // TMEM columns
 constexpr uint32_t T_R1 = 0, T_R2 = 128, T_R3 = 256, T_R4 = 384, T_R8 = 448, T_COLS = 512;
@@ -128,23 +127,19 @@ template <> __device__ __forceinline__ float bits_to_f<__half>(uint32_t b) {
 }
 
 // In-place L2 normalisation of 64 rows of a [64 x 128] swizzled tile (blocks 16 KB apart).
-// Eight warps per tile, four lanes per row; lane quarter qq takes 16-byte chunks 2qq, 2qq+1 of each 64-column
-// block, so the eight lanes of a quarter-warp access hit eight distinct bank groups.
+// Row norms of the 64 rows of a [64 x 128] swizzled tile (blocks 16 KB apart), read only: eight warps per tile,
+// four lanes per row; lane quarter qq takes 16-byte chunks 2qq, 2qq+1 of each 64-column block, so the eight
+// lanes of a quarter-warp access hit eight distinct bank groups.  n_out[r] = 1 / sqrt(|x_r|^2 + eps) (the
+// factor that normalises the row), m_out[r] = sqrt(|x_r|^2 + eps).
 template <typename T>
-__device__ __forceinline__ void l2norm64(uint32_t base, int rows, int warp, int lane, float *inv_out) {
+__device__ __forceinline__ void row_norms64(uint32_t base, int warp, int lane, float *n_out, float *m_out) {
     const int rq = lane >> 2, qq = lane & 3;
     const int r = warp * 8 + rq;  // warps 0..7 x 8 rows
-    uint32_t addr[4];
-    uint4 u[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        addr[c] = base + (uint32_t)(c >> 1) * 16384u + umma::off(r, (qq * 2 + (c & 1)) * 8, 0);
-        u[c] = umma::ld_shared_v4(addr[c]);
-    }
     float ss = 0.f;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
+        const uint4 u = umma::ld_shared_v4(base + (uint32_t)(c >> 1) * 16384u + umma::off(r, (qq * 2 + (c & 1)) * 8, 0));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float2 x = Elt<T>::unpack(w[e]);
@@ -153,19 +148,10 @@ __device__ __forceinline__ void l2norm64(uint32_t base, int rows, int warp, int 
     }
     ss += __shfl_xor_sync(0xffffffffu, ss, 1);
     ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-    const float inv = 1.0f / sqrtf(ss + L2_EPS);
-    if (r < rows && qq == 0) inv_out[r] = inv;
-    if (r < rows) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 x = Elt<T>::unpack(w[e]);
-                w[e] = Elt<T>::pack(x.x * inv, x.y * inv);
-            }
-            umma::st_shared_v4(addr[c], w[0], w[1], w[2], w[3]);
-        }
+    if (qq == 0) {
+        const float m = sqrtf(ss + L2_EPS);
+        n_out[r] = 1.0f / m;
+        m_out[r] = m;
     }
 }
 
@@ -247,7 +233,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
     const uint64_t dDH = umma::desc(sb + S_DH, 16, 1024);           // dH'[d][e]
     const uint64_t dQa = umma::desc(sb + S_Q0, 16, 1024);           // [Q; K] rows, K = key
     const uint64_t dKa = umma::desc(sb + S_K0, 16, 1024);           // K rows (n = token), K = key
-    const uint64_t dAmn = umma::desc(sb + S_A, 8192, 1024);         // [A^T; AKG^T] (m = row), k = token
+    const uint64_t dAmn = umma::desc(sb + S_A, 8192, 1024);         // [A^T; A^T] (m = row), k = token
     const uint64_t dDDmn = umma::desc(sb + S_DD0, 16384, 1024);     // [dDelta | dW] (n = col), k = token
     const uint64_t dWup = umma::desc(sb + S_DW0 - 8192, 16, 1024);  // rows 64..127 = dW, K = key
     const uint64_t dDA = umma::desc(sb + S_DA, 16, 1024);           // dA rows, K = token
@@ -289,7 +275,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
     // issued); 5 = q for the first head of an item (after dq is stored); 6 = k for the first head of an item
     // and Delta's second column block (the dKK block, after the unit).  All bytes of a unit are announced on
     // the load barrier with its first group.
-    auto unit_bytes = [&](int jj_) -> uint32_t { return 32768u * 2 + 16384u + 16384u * 2 + 16384u + 8192u +
+    auto unit_bytes = [&](int jj_) -> uint32_t { return 32768u * 2 + 16384u + 16384u * 2 + 16384u + 8192u * 2 +
                                                          (jj_ == 0 ? 32768u : 0u); };
     auto issue = [&](const Pos &u, int jj_, int group) {
         const int t = u.t, row = u.row, j_ = u.j, hq_ = u.hq;
@@ -310,6 +296,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             tma::load3d(sb + S_D0, &p.td, 0, 0, row, lbar);
         } else if (group == 4) {
             tma::load3d(sb + S_A, &p.ta, 0, j_, t, lbar);
+            tma::load3d(sb + S_A2, &p.ta, 0, j_, t, lbar);
         } else if (group == 5) {
             if (jj_ == 0) {
                 tma::load3d(sb + S_Q0, &p.tq, 0, hq_, t, lbar);
@@ -351,9 +338,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
     // dq -> X and dW0 (after round 4), dk -> dS and dW1 (after round 5).  ST waits for its stores to finish
     // reading before a barrier that precedes the next writes to those blocks.
     constexpr int ST = 32;
-    // dq (lower lanes) / dk (upper lanes) rows, straight from the registers: with xh the normalised row (the q
-    // or k tile in shared memory) and n its norm, dx = (dxh - xh (xh . dxh)) / n; the four column quarters of a
-    // row meet through one partial dot product each
+    // dq (lower lanes) / dk (upper lanes) rows, straight from the registers: with x the raw row (the q or k tile
+    // in shared memory), n = 1 / sqrt(|x|^2 + eps) and xh = n x, dx = (dxh - xh (xh . dxh)) n
+    // = (dxh - x n^2 (x . dxh)) n; the four column quarters of a row meet through one partial dot product each
     const uint32_t xt = sb + (upper ? S_K0 : S_Q0) + (qc >> 1) * 16384;
     const int xc = (qc & 1) * 32;  // this thread's key columns within the 64-column block
     float *dp = &f(F_DP, 0);       // [4 quarters][128 lanes]
@@ -374,8 +361,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
     auto store_row = [&](long long tok0_, int valid_, int hq_) {
         const bool staged = valid_ == C;
         if (!staged && r >= valid_) return;
-        const float dot = p.l2norm ? (dp[L] + dp[128 + L]) + (dp[256 + L] + dp[384 + L]) : 0.f;
         const float inv = p.l2norm ? f(upper ? F_IK : F_IQ, r) : 1.f;
+        const float dot = p.l2norm ? inv * inv * ((dp[L] + dp[128 + L]) + (dp[256 + L] + dp[384 + L])) : 0.f;
         T *dst = static_cast<T *>(upper ? p.dk : p.dq) + ((tok0_ + r) * Hq + hq_) * DK + qc * 32;
         const uint32_t stg = sb + (upper ? ((qc >> 1) ? S_DW1 : S_DS) : ((qc >> 1) ? S_DW0 : S_X));
 #pragma unroll
@@ -442,38 +429,16 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
         lphase ^= 1u;
         posted = false;
         if (tid == ST) tma::wait_read();  // the previous unit's dq / dk staging blocks are free again
+        umma::fence_before();
         __syncthreads();
+        umma::fence_after();
         if (*sflag) {
             ok = false;
             break;
         }
-        if (jj == 0 && p.l2norm)  // warps 0..7 normalise the q rows, warps 8..15 the k rows
-            l2norm64<T>(sb + (warp < 8 ? S_Q0 : S_K0), valid, warp & 7, lane, &f(warp < 8 ? F_IQ : F_IK, 0));
-        const float Gl = f(F_G, valid - 1);
-        if (tid < C) {
-            f(F_EG, tid) = __expf(f(F_G, tid));
-            f(F_EL, tid) = __expf(Gl - f(F_G, tid));
-        }
-        // AKG = A with column s scaled by beta_s e^{G_s}
-#pragma unroll
-        for (int u = 0; u < (C * 8) / NT; ++u) {
-            const int cix = tid + u * NT, rr = cix >> 3, c = cix & 7;
-            const uint32_t o = umma::off(rr, c * 8, 0);
-            uint4 a = umma::ld_shared_v4(sb + S_A + o);
-            if (rr >= valid) a = make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-            uint32_t wk[4];
-#pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-                const int s = c * 8 + 2 * e2;
-                const float2 x = Elt<T>::unpack(w[e2]);
-                wk[e2] = Elt<T>::pack(x.x * f(F_B, s) * __expf(f(F_G, s)), x.y * f(F_B, s + 1) * __expf(f(F_G, s + 1)));
-            }
-            umma::st_shared_v4(sb + S_AKG + o, wk[0], wk[1], wk[2], wk[3]);
-        }
-        sync_tc();
 
-        // ---------------- round 1
+        // ---------------- round 1 (raw q and k tiles: the L2 normalisation enters every product that uses
+        //                  them as a per-row or per-column factor, so nothing has to be rewritten first)
         if (tid == 0) {
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
@@ -484,6 +449,20 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                 umma::mma(tmem + T_R4, dQa + ko, dKa + ko, i_n64, ks > 0);
             }
             umma::commit(bar);
+        }
+        // while round 1 runs: decays, and the q / k row norms of a new item (warps 0..7 q, 8..15 k)
+        const float Gl = f(F_G, valid - 1);
+        if (tid < C) {
+            f(F_EG, tid) = __expf(f(F_G, tid));
+            f(F_EL, tid) = __expf(Gl - f(F_G, tid));
+        }
+        if (jj == 0) {
+            if (p.l2norm) {
+                row_norms64<T>(sb + (warp < 8 ? S_Q0 : S_K0), warp & 7, lane, &f(warp < 8 ? F_IQ : F_IK, 0),
+                               &f(warp < 8 ? F_MQ : F_MK, 0));
+            } else if (tid < 4 * C) {
+                f(F_IQ + (tid >> 6), tid & 63) = 1.f;  // F_IQ, F_IK, F_MQ, F_MK
+            }
         }
         if (!wait_mma()) {
             ok = false;
@@ -505,8 +484,11 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                     qd += qv[u] * x[u];
                 }
             }
-            // dS = scale dP o Gamma o M  (dP = dO Delta^T in columns 64..127 of R3);
-            // E = dS o (Q K^T) = dP o P gives the decay terms of dG (row sums minus column sums)
+            const float nqr = f(F_IQ, r);
+            qd *= nqr;  // <q^_r, .> with q^ = nq q
+            // dS = scale dP o Gamma o M  (dP = dO Delta^T in columns 64..127 of R3), stored as
+            // dS'' = diag(nq) dS diag(nk) for the raw-tile products of round 3;
+            // E = dS o (Q^ K^^T) = dS'' o (Q K^T) gives the decay terms of dG (row sums minus column sums)
             const float gr = f(F_G, r);
             float ev[16], er = 0.f;
             {
@@ -518,7 +500,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const int s = qc * 16 + u;
-                    x[u] = (s <= r && r < valid) ? p.scale * x[u] * __expf(gr - f(F_G, s)) : 0.f;
+                    x[u] = (s <= r && r < valid) ? p.scale * x[u] * __expf(gr - f(F_G, s)) * nqr * f(F_IK, s) : 0.f;
                     ev[c + u] = x[u] * qk[u];
                     er += ev[c + u];
                 }
@@ -547,7 +529,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                 }
                 store16<T>(sb + wblk, r, (qc & 1) * 32 + c, x);
             }
-            f(F_Z0 + qc, r) = z;
+            f(F_Z0 + qc, r) = z * f(F_IK, r);
         }
         if (upper) {
             // <dH', h> over the whole state (both tiles share one layout, so equal offsets hold equal elements),
@@ -614,7 +596,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                 for (int u = 0; u < 8; ++u) w[u] = Elt<T>::pack(x[2 * u] * br, x[2 * u + 1] * br);
                 if (valid == C) {
                     const uint32_t stg = sb + ((qc >> 1) ? S_DW1 : S_DW0);
-                    const int col = (qc & 1) * 32 + c;
+                    const int col = (qc & 1) * 32 + c;  // (16-byte aligned)
                     umma::st_shared_v4(stg + umma::off(r, col, 0), w[0], w[1], w[2], w[3]);
                     umma::st_shared_v4(stg + umma::off(r, col + 8, 0), w[4], w[5], w[6], w[7]);
                 } else if (r < valid) {
@@ -622,6 +604,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                     *reinterpret_cast<uint4 *>(dvrow + c + 8) = make_uint4(w[4], w[5], w[6], w[7]);
                 }
             }
+            kd *= f(F_IK, r);  // <k^_r, .>
             if (valid == C) {
                 umma::fence_async_smem();
                 asm volatile("bar.sync 2, 256;\n" ::: "memory");  // the eight lower-lane warps
@@ -632,14 +615,15 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                 }
             }
         } else {
-            // dk += (A diag(beta e^G))^T dW ; dA = beta_s (e^{G_s} dW K^T + dDelta V^T), strictly lower
+            // dk += diag(beta e^G) A^T dW ; dA = beta_s (e^{G_s} dW K^^T + dDelta V^T), strictly lower
+            const float bg = f(F_B, r) * f(F_EG, r);
 #pragma unroll
             for (int c = 0; c < 32; c += 16) {
                 float x[16];
                 umma::ld16(umma::taddr(tmem, lb, T_R1 + 128 + qc * 32 + c), x);
                 umma::ld_wait();
 #pragma unroll
-                for (int u = 0; u < 16; ++u) acc[c + u] += x[u];
+                for (int u = 0; u < 16; ++u) acc[c + u] += bg * x[u];
             }
             {
                 const int c = 0;
@@ -650,14 +634,14 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const int s = qc * 16 + u;
-                    x1[u] = (s < r && r < valid) ? f(F_B, s) * (f(F_EG, s) * x1[u] + x2[u]) : 0.f;
+                    x1[u] = (s < r && r < valid) ? f(F_B, s) * (f(F_EG, s) * f(F_IK, s) * x1[u] + x2[u]) : 0.f;
                 }
                 store16<T>(sb + S_DA, r, qc * 16 + c, x1);
             }
         }
         sync_tc();
 
-        // ---------------- round 3: X = dA A^T ; dq += dS K ; dk += dS^T Q
+        // ---------------- round 3: X = dA A^T ; dq += dS K^ = diag(1/nq) dS'' K ; dk += dS^T Q^ = diag(1/nk) dS''^T Q
         if (tid == 0) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
@@ -680,22 +664,24 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                 umma::ld_wait();
                 store16<T>(sb + S_X, r, qc * 16, x);
             }
+            const float mq = f(F_MQ, r);
 #pragma unroll
             for (int c = 0; c < 32; c += 16) {
                 float x[16];
                 umma::ld16(umma::taddr(tmem, lb, T_R1 + qc * 32 + c), x);
                 umma::ld_wait();
 #pragma unroll
-                for (int u = 0; u < 16; ++u) acc[c + u] += x[u];
+                for (int u = 0; u < 16; ++u) acc[c + u] += mq * x[u];
             }
         } else {
+            const float mk = f(F_MK, r);
 #pragma unroll
             for (int c = 0; c < 32; c += 16) {
                 float x[16];
                 umma::ld16(umma::taddr(tmem, lb, T_R2 + qc * 32 + c), x);
                 umma::ld_wait();
 #pragma unroll
-                for (int u = 0; u < 16; ++u) acc[c + u] += x[u];
+                for (int u = 0; u < 16; ++u) acc[c + u] += mk * x[u];
             }
         }
         sync_tc();
@@ -711,9 +697,11 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             ok = false;
             break;
         }
-        float lb_ = 0.f;  // upper lanes: sum_s dL Gamma KK
+        float lb_ = 0.f;  // upper lanes: sum_s dL Gamma K^K^^T
         if (upper) {
-            const float gr = f(F_G, r), br = f(F_B, r);
+            // dKK = dL o beta_r Gamma, stored as dKK'' = diag(nk) dKK diag(nk) for the raw-tile products of
+            // round 5; K^K^^T = nk_r nk_s (K K^T)
+            const float gr = f(F_G, r), br = f(F_B, r), nkr = f(F_IK, r);
             float fv[16], fr = 0.f;  // F = dL o L: decay terms of dG
             {
                 const int c = 0;
@@ -727,10 +715,12 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                     const bool m = s < r && r < valid;
                     const float gam = m ? __expf(gr - f(F_G, s)) : 0.f;
                     const float dlv = m ? -x[u] : 0.f;
-                    lb_ += dlv * gam * kk[u];
-                    x[u] = dlv * br * gam;
-                    fv[c + u] = x[u] * kk[u];
+                    const float nks = f(F_IK, s), kkh = kk[u] * nkr * nks;
+                    lb_ += dlv * gam * kkh;
+                    const float dkk = dlv * br * gam;
+                    fv[c + u] = dkk * kkh;
                     fr += fv[c + u];
+                    x[u] = dkk * nkr * nks;
                 }
                 store16<T>(sb + S_DKK, r, qc * 16 + c, x);
             }
@@ -756,7 +746,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
         }
         sync_tc();
 
-        // ---------------- round 5: dk += dKK K + dKK^T K
+        // ---------------- round 5: dk += dKK K^ + dKK^T K^ = diag(1/nk) (dKK'' K + dKK''^T K)
         if (tid == 0) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
@@ -771,13 +761,14 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             break;
         }
         if (upper) {
+            const float mk = f(F_MK, r);
 #pragma unroll
             for (int c = 0; c < 32; c += 16) {
                 float x[16];
                 umma::ld16(umma::taddr(tmem, lb, T_R1 + qc * 32 + c), x);
                 umma::ld_wait();
 #pragma unroll
-                for (int u = 0; u < 16; ++u) acc[c + u] += x[u];
+                for (int u = 0; u < 16; ++u) acc[c + u] += mk * x[u];
             }
             f(F_LB0 + qc, r) = lb_;
         } else {
