@@ -452,7 +452,7 @@ gdr_status gdr_bwd(const gdr_problem *p, const void *q, const void *k, const voi
         void *Pw = ws + L.P;
         float *rqw = a.l2norm ? reinterpret_cast<float *>(ws + L.rq) : nullptr;
         float *rkw = a.l2norm ? reinterpret_cast<float *>(ws + L.rk) : nullptr;
-        if ((st = timed(K_CHUNK_P, s, [&] { return launch_chunk_p(a, q, k, g_cumsum, beta, Pw, rqw, rkw, s); })) !=
+        if ((st = timed(K_CHUNK_P, s, [&] { return launch_chunk_p_tc(a, q, k, g_cumsum, Pw, rqw, rkw, s); })) !=
             GDR_OK)
             return st;
         if ((st = timed(K_CHAIN_PAIR, s, [&] {

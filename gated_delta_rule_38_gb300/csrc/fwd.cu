@@ -6,7 +6,7 @@
 //              off-diagonal blocks merged with tf32 tensor-core products), and the
 //              state-independent attention block P = scale (q^ k^T o exp(G_r - G_s)),
 //              s <= r, with the inverse q/k norms the recurrence applies as factors.
-//              Without A (chunk_p) it reads G and produces P and the norms only.
+//              (The backward's P from a given g_cumsum comes from chunk_p_tc.cu.)
 // The recurrences that consume A and P live in chain_ws.cu / chain_tc.cu.
 #include <cuda_runtime.h>
 
@@ -54,7 +54,6 @@ __device__ __forceinline__ void row_inv_norms(const Tile &t, int rows, int warp,
 struct WyArgs {
     const void *q, *k, *g, *beta;
     bool gate_f32, l2norm;
-    bool full;      // compute G from g (written to g_cs) and A; else read G from g_cs, no A
     float scale;
     float *g_cs;
     void *A_out;    // [tokens,Hv,64] or nullptr
@@ -95,7 +94,7 @@ __global__ void __launch_bounds__(128) wy_fwd_kernel(Geo geo, const WyArgs w) {
     if (tid < C) {
         float gv = 0.f, bv = 0.f;
         if (tid < len) {
-            gv = w.full ? load_gate<T>(w.g, (tok0 + tid) * Hv + j, w.gate_f32) : w.g_cs[(tok0 + tid) * Hv + j];
+            gv = load_gate<T>(w.g, (tok0 + tid) * Hv + j, w.gate_f32);
             bv = load_gate<T>(w.beta, (tok0 + tid) * Hv + j, w.gate_f32);
         }
         sG[tid] = gv;
@@ -112,7 +111,7 @@ __global__ void __launch_bounds__(128) wy_fwd_kernel(Geo geo, const WyArgs w) {
         sRK[tid] = 1.f;
         sRQ[tid] = 1.f;
     }
-    if (w.full && warp == 0) {
+    if (warp == 0) {
         float x0 = sG[lane], x1 = sG[lane + 32];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -332,29 +331,9 @@ cudaError_t launch_wy_fwd(const Args &a, const void *q, const void *k, const voi
     w.beta = beta;
     w.gate_f32 = a.gate_f32;
     w.l2norm = a.l2norm;
-    w.full = true;
     w.scale = a.scale;
     w.g_cs = g_cs;
     w.A_out = A;
-    w.P_out = P;
-    w.rq_out = rq;
-    w.rk_out = rk;
-    return a.bf16 ? wy_fwd_t<__nv_bfloat16>(a, w, s) : wy_fwd_t<__half>(a, w, s);
-}
-
-cudaError_t launch_chunk_p(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta, void *P,
-                           float *rq, float *rk, cudaStream_t s) {
-    WyArgs w;
-    w.q = q;
-    w.k = k;
-    w.g = nullptr;
-    w.beta = beta;
-    w.gate_f32 = a.gate_f32;
-    w.l2norm = a.l2norm;
-    w.full = false;
-    w.scale = a.scale;
-    w.g_cs = const_cast<float *>(g_cs);
-    w.A_out = nullptr;
     w.P_out = P;
     w.rq_out = rq;
     w.rk_out = rk;

@@ -39,9 +39,9 @@ cudaError_t launch_prep_chunks(const int32_t *cu, int N, int T, int chunk, int32
 // with in-kernel L2 normalisation).
 cudaError_t launch_wy_fwd(const Args &a, const void *q, const void *k, const void *g, const void *beta, float *g_cs,
                           void *A, void *P, float *rq, float *rk, cudaStream_t s);
-// The same P, rq, rk from a given g_cumsum (no A).
-cudaError_t launch_chunk_p(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta, void *P,
-                           float *rq, float *rk, cudaStream_t s);
+// The same P, rq, rk from a given g_cumsum (no A), on tcgen05 (one persistent CTA per SM).
+cudaError_t launch_chunk_p_tc(const Args &a, const void *q, const void *k, const float *g_cs, void *P, float *rq,
+                              float *rk, cudaStream_t s);
 // Forward recurrence + output (o != nullptr) and/or per-chunk states (h != nullptr)
 // and per-chunk Delta = U - W h (delta != nullptr).
 cudaError_t launch_chain_fwd(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
@@ -50,7 +50,7 @@ cudaError_t launch_chain_fwd(const Args &a, const void *q, const void *k, const 
 // Forward recurrence, warp-specialised (one CTA per value-column slice); no sequence split.
 // o != nullptr: output rows; h: state before every chunk ([rows,Hv,K,V], or [..,V,K] when
 // h_vfirst); delta: Delta of every chunk; seg_start: transposed fp32 start states replacing h0.
-// P, rq, rk: from launch_wy_fwd / launch_chunk_p (P is read only when o != nullptr; rq, rk only with
+// P, rq, rk: from launch_wy_fwd / launch_chunk_p_tc (P is read only when o != nullptr; rq, rk only with
 // in-kernel L2 normalisation).
 cudaError_t launch_chain_ws(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
                             const void *beta, const void *A, const void *P, const float *rq, const float *rk,
@@ -58,7 +58,7 @@ cudaError_t launch_chain_ws(const Args &a, const void *q, const void *k, const v
                             bool h_vfirst, void *delta, cudaStream_t s);
 // Backward without a sequence split, warp-specialised: the forward recompute (states h and Delta of every
 // chunk, no output) and the reverse chain (dH' and dDelta of every chunk, dh0) in one launch, one CTA each
-// per (sequence, value head).  P, rq, rk from launch_chunk_p.
+// per (sequence, value head).  P, rq, rk from launch_chunk_p_tc.
 cudaError_t launch_chain_ws_pair(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
                                  const void *beta, const void *A, const void *P, const float *rq, const float *rk,
                                  const float *h0, void *h, void *delta, const void *dout, const float *dht,
