@@ -49,7 +49,7 @@ constexpr uint32_t S_DA = S_D0, S_DKK = S_D0 + 16384; // reuse Delta's blocks af
 constexpr uint32_t S_H = 131072, S_DH = 163840;       // [128 x 64] blocks of 16 KB
 constexpr uint32_t S_A = 196608, S_A2 = 204800;   // A, and a second copy of it (the stacked round-2 operand)
 constexpr uint32_t S_F = 212992;                      // scalars
-constexpr uint32_t S_BAR = S_F + 50 * 64 * 4, S_LBAR = S_BAR + 8, S_SLOT = S_LBAR + 8, S_FLAG = S_SLOT + 4,
+constexpr uint32_t S_BAR = S_F + 52 * 64 * 4, S_LBAR = S_BAR + 8, S_SLOT = S_LBAR + 8, S_FLAG = S_SLOT + 4,
                    S_USED = S_FLAG + 4;
 constexpr uint32_t S_BYTES = S_USED + 1024;
 // scalar slots (64 floats each)
@@ -57,7 +57,7 @@ constexpr uint32_t S_BYTES = S_USED + 1024;
 enum {
     F_G = 0, F_B, F_EG, F_EL, F_QD0, F_VD0 = F_QD0 + 4, F_KD0 = F_VD0 + 4, F_LB0 = F_KD0 + 4, F_ER0 = F_LB0 + 4,
     F_EC0 = F_ER0 + 4, F_Z0 = F_EC0 + 2, F_FR0 = F_Z0 + 4, F_FC0 = F_FR0 + 4, F_HD = F_FC0 + 2, F_DG, F_IQ, F_IK,
-    F_MQ, F_MK, F_DP, F_COUNT = F_DP + 8
+    F_MQ, F_MK, F_PDG, F_PDB, F_DP, F_COUNT = F_DP + 8
 };
 // TMEM columns
 constexpr uint32_t T_R1 = 0, T_R2 = 128, T_R3 = 256, T_R4 = 384, T_R8 = 448, T_COLS = 512;
@@ -468,8 +468,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             ok = false;
             break;
         }
-        float qd = 0.f;  // lower lanes: <q_r, dq_r> of this value head (this thread's half)
         if (!upper) {
+            float qd = 0.f;  // <q_r, dq_r> of this value head (this thread's quarter of the row)
             const float sc = p.scale * f(F_EG, r);
 #pragma unroll
             for (int c = 0; c < 32; c += 16) {
@@ -485,7 +485,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                 }
             }
             const float nqr = f(F_IQ, r);
-            qd *= nqr;  // <q^_r, .> with q^ = nq q
+            f(F_QD0 + qc, r) = qd * nqr;  // <q^_r, .> with q^ = nq q
             // dS = scale dP o Gamma o M  (dP = dO Delta^T in columns 64..127 of R3), stored as
             // dS'' = diag(nq) dS diag(nk) for the raw-tile products of round 3;
             // E = dS o (Q^ K^^T) = dS'' o (Q K^T) gives the decay terms of dG (row sums minus column sums)
@@ -573,8 +573,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             ok = false;
             break;
         }
-        float vd = 0.f, kd = 0.f;
         if (!upper) {
+            float vd = 0.f, kd = 0.f;
             // dDelta-side: ddelta = A^T dDelta (columns 0..127), A^T dW (128..255)
             const float br = f(F_B, r);
             T *dvrow = static_cast<T *>(p.dv) + ((tok0 + r) * Hv + j) * DV + qc * 32;
@@ -604,7 +604,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                     *reinterpret_cast<uint4 *>(dvrow + c + 8) = make_uint4(w[4], w[5], w[6], w[7]);
                 }
             }
-            kd *= f(F_IK, r);  // <k^_r, .>
+            f(F_VD0 + qc, r) = vd;
+            f(F_KD0 + qc, r) = kd * f(F_IK, r);  // <k^_r, .>
             if (valid == C) {
                 umma::fence_async_smem();
                 asm volatile("bar.sync 2, 256;\n" ::: "memory");  // the eight lower-lane warps
@@ -727,7 +728,33 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             f(F_FR0 + qc, r) = fr;
             const float cs = colsum16(fv, lane);
             if (lane < 16) f(F_FC0 + ((warp & 3) - 2), qc * 16 + lane) = cs;
-        } else if (last_head) {
+        } else {
+            if (warp < 2) {
+                // the dG / dbeta terms known by now (all but F and the dKK ones), for rows 32 warp..:
+                // dG_r = E row - E column + <q_r, dq_inter_r> - z_r + beta_r e^{G_r} <(A^T dW)_r, k_r> (+ F row
+                // - F column at the end); dbeta_r = e^{G_r} <(A^T dW)_r, k_r> + <(A^T dDelta)_r, v_r> (+ the
+                // dKK term at the end); and this warp's share of sum_s z_s
+                const int rr = warp * 32 + lane;
+                auto q4 = [&](int slot0) {  // the four column-quarter partials, in a fixed order
+                    return (f(slot0, rr) + f(slot0 + 1, rr)) + (f(slot0 + 2, rr) + f(slot0 + 3, rr));
+                };
+                const float z = q4(F_Z0), kd2 = q4(F_KD0);
+                f(F_PDG, rr) = q4(F_ER0) - (f(F_EC0, rr) + f(F_EC0 + 1, rr)) + q4(F_QD0) - z +
+                               f(F_B, rr) * f(F_EG, rr) * kd2;
+                f(F_PDB, rr) = f(F_EG, rr) * kd2 + q4(F_VD0);
+                float zs = rr < valid ? z : 0.f;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);
+                if (lane == 0) f(F_DG, 2 * warp) = zs;
+                if (warp == 0 && lane == 0) {
+                    float hd = 0.f;
+#pragma unroll
+                    for (int wi = 0; wi < 8; ++wi) hd += f(F_HD, wi);
+                    f(F_DG, 4) = hd;
+                }
+            }
+        }
+        if (!upper && last_head) {
             // dq is complete after round 3: the lower-lane warps store it while the upper ones work on dKK
             if (p.l2norm) dot_partial();
             if (tid == ST) tma::wait_read();  // dv's staging block dW0 is free again
@@ -771,33 +798,22 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                 for (int u = 0; u < 16; ++u) acc[c + u] += mk * x[u];
             }
             f(F_LB0 + qc, r) = lb_;
-        } else {
-            f(F_QD0 + qc, r) = qd;
-            f(F_VD0 + qc, r) = vd;
-            f(F_KD0 + qc, r) = kd;
         }
         // dk's partial dot products of the L2-norm chain rule go with the round-5 results, so one barrier
         // serves both the dG reduction and the dk stores
         if (upper && last_head && p.l2norm) dot_partial();
         __syncthreads();
         if (warp < 2) {
-            // dG_r = E row - E column + <q_r, dq_inter_r> - z_r + beta_r e^{G_r} <(A^T dW)_r, k_r>
-            //        + F row - F column; every valid row's dg also carries e^{Gl} <dH', h> + sum_s z_s (the
-            //        last valid row's extra terms, summed backwards).  Warp w takes rows 32w..32w+31.
+            // dG_r = (the round-4 partial) + F row - F column; every valid row's dg also carries
+            // e^{Gl} <dH', h> + sum_s z_s (the last valid row's extra terms, summed backwards).  Warp w takes
+            // rows 32w..32w+31.
             const int rr = warp * 32 + lane;
             const bool vr = rr < valid;
             auto q4 = [&](int slot0) {  // the four column-quarter partials, in a fixed order
                 return (f(slot0, rr) + f(slot0 + 1, rr)) + (f(slot0 + 2, rr) + f(slot0 + 3, rr));
             };
-            const float z = q4(F_Z0);
-            const float kd2 = q4(F_KD0);
-            const float dG = q4(F_ER0) - (f(F_EC0, rr) + f(F_EC0 + 1, rr)) + q4(F_QD0) - z +
-                             f(F_B, rr) * f(F_EG, rr) * kd2 + q4(F_FR0) - (f(F_FC0, rr) + f(F_FC0 + 1, rr));
-            if (vr)
-                store_gate<T>(p.dbeta, (tok0 + rr) * Hv + j, p.gate_f32, f(F_EG, rr) * kd2 + q4(F_VD0) + q4(F_LB0));
-            float zs = vr ? z : 0.f;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) zs += __shfl_xor_sync(0xffffffffu, zs, o);
+            const float dG = f(F_PDG, rr) + q4(F_FR0) - (f(F_FC0, rr) + f(F_FC0 + 1, rr));
+            if (vr) store_gate<T>(p.dbeta, (tok0 + rr) * Hv + j, p.gate_f32, f(F_PDB, rr) + q4(F_LB0));
             // dg_s = sum_{r >= s} dG_r within the chunk: suffix sums inside the warp, then warp 1's total
             float y = vr ? dG : 0.f;
 #pragma unroll
@@ -805,15 +821,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                 const float t = __shfl_down_sync(0xffffffffu, y, o);
                 if (lane + o < 32) y += t;
             }
-            if (lane == 0) {
-                f(F_DG, 2 * warp) = zs;
-                f(F_DG, 2 * warp + 1) = y;
-            }
+            if (lane == 0) f(F_DG, 2 * warp + 1) = y;
             asm volatile("bar.sync 1, 64;\n" ::: "memory");  // warps 0 and 1
-            float hd = 0.f;
-#pragma unroll
-            for (int wi = 0; wi < 8; ++wi) hd += f(F_HD, wi);
-            const float extra = __expf(Gl) * hd + (f(F_DG, 0) + f(F_DG, 2));
+            const float extra = __expf(Gl) * f(F_DG, 4) + (f(F_DG, 0) + f(F_DG, 2));
             const float tail = warp == 0 ? f(F_DG, 3) : 0.f;
             if (vr) store_gate<T>(p.dg, (tok0 + rr) * Hv + j, p.gate_f32, y + tail + extra);
         }
