@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
 
     uint32_t phase = 0, lphase = 0;
     auto wait_mma = [&]() -> bool {
-        if (tid == 0 && !umma::mbar_wait(bar, phase)) {
+        if (tid == 0 && !umma::mbar_spin(bar, phase)) {
             raise_error(geo.err, GDR_ERR_TIMEOUT);
             *sflag = 1;
         }
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             f(F_G, tid - GT) = gnext;
             f(F_B, tid - GT) = p.gate_f32 ? bnext32 : bits_to_f<T>(bnext16);
         }
-        if (!umma::mbar_wait(lbar, lphase)) {
+        if (tid == 0 && !umma::mbar_spin(lbar, lphase)) {  // the barrier below passes it on
             raise_error(geo.err, GDR_ERR_TIMEOUT);
             *sflag = 1;
         }

@@ -67,7 +67,7 @@ struct Lay {
     static constexpr uint32_t Z = AB + 8192;
     static constexpr uint32_t AKG = Z + 8192;
     static constexpr uint32_t DT = AKG + 8192;                    // diag(rk e^{Gl-G}) Delta [64 s][BV]
-    static constexpr uint32_t DL = WRITE_O ? DT + BV * 128 : DT;  // Delta (output product only)
+    static constexpr uint32_t DL = DT + BV * 128;                 // Delta (output product; stored Delta)
     static constexpr uint32_t H = DL + BV * 128;                  // h [128 d][BV]: BV/64 blocks of 16 KB
     static constexpr uint32_t F = H + BV * 256;                   // factor sets (4, by chunk index mod 4)
     static constexpr uint32_t BAR = F + 4 * NF * 256;
@@ -98,19 +98,12 @@ struct WsP {
     const float *seg_start;  // optional start states, transposed [N,Hv,V,K] fp32 (replaces h0)
     bool gate_f32, l2norm, v_first, h_vfirst;
     float scale;
+    // with all 128 value columns in one CTA and the [K,V] layout, h and Delta leave by TMA store from the
+    // bf16 tiles in shared memory: each state warp stores its own 32-row x 64-column box
+    bool tma_h, tma_delta;
+    CUtensorMap th, tdl;  // h [rows*Hv][128][128], Delta [rows*Hv][64][128]; boxes 64 x 32 x 1
 };
 
-// One test of a barrier phase that may suspend the thread until the phase completes (or a short
-// hardware time limit passes): waiting warps leave the issue slots to the working ones.
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return done != 0;
-}
 // One non-blocking test (the MMA thread polls several barriers in turn).
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     uint32_t done;
@@ -126,10 +119,12 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }
 
 // Wait for the phase of `bar` with the given parity.  Gives up when the block's flag is raised by
-// another role, or after a bound (then it latches GDR_ERR_TIMEOUT and raises the flag itself).
+// another role, or after a bound (then it latches GDR_ERR_TIMEOUT and raises the flag itself).  It spins
+// on a non-suspending test: a thread suspended in try_wait for long was seen to resume several hundred
+// cycles after the phase completed, on the chain's critical path (only one lane of a waiting warp polls).
 __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *flag, unsigned *err) {
     for (long it = 0; it < kWaitPolls; ++it) {
-        if (mbar_try(bar, parity)) return true;
+        if (mbar_test(bar, parity)) return true;
         if ((it & 127) == 127 && *flag) return false;
     }
     raise_error(err, GDR_ERR_TIMEOUT);
@@ -499,7 +494,12 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
             else
                 hS[i] = 0.f;
         }
-        auto write_h = [&]() {
+        // the state before chunk lcn into the operand tile (and, with tma_h, on to h by this warp's box)
+        auto write_h = [&](int lcn) {
+            if (p.tma_h) {
+                if (lane == 0) tma::wait_read();  // the box stored from this tile last time has been read
+                __syncwarp();
+            }
 #pragma unroll
             for (int i = 0; i < HW; i += 16) {
                 const int col = cb0 + i;
@@ -507,9 +507,16 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
             }
             umma::fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(sb + L::B_EPIB);
+            if (lane == 0) {
+                mbar_arrive(sb + L::B_EPIB);
+                if (p.tma_h && lcn < nc) {
+                    tma::store3d(&p.th, v0 + cb0, q4 * 32, (row0 + lcn) * Hv + j,
+                                 sb + L::H + (cb0 >> 6) * 16384 + q4 * 4096);
+                    tma::commit_group();
+                }
+            }
         };
-        write_h();
+        write_h(0);
         float glo = 0.f;
         auto fetch_gl = [&](int lc) {
             const int valid = min(C, len - lc * C);
@@ -521,7 +528,7 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
             const uint32_t tD = b ? L::T_D1 : L::T_D0;
             const float egl = __expf(glo);
             if (lc + 1 < nc) fetch_gl(lc + 1);
-            if (p.h) {
+            if (p.h && !p.tma_h) {
                 // the state before this chunk
                 T *hb = static_cast<T *>(p.h) + ((long long)(row0 + lc) * Hv + j) * DK * DV;
                 if (p.h_vfirst) {
@@ -542,6 +549,10 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                 umma::fence_after();
                 const int sr = d;
                 const float ck = fa(lc, FCK)[sr];
+                if (p.tma_delta) {
+                    if (lane == 0) tma::wait_read();  // the Delta box stored last chunk has been read
+                    __syncwarp();
+                }
                 constexpr int NB = HW < 32 ? HW : 32;  // columns per TMEM load batch
 #pragma unroll
                 for (int i0 = 0; i0 < HW; i0 += NB) {
@@ -555,9 +566,9 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                     const int col = cb0 + i0 + i;
 #pragma unroll
                     for (int u = 0; u < 16; ++u) y[u] = x[u] * ck;
-                    if (WRITE_O) store_row16<T>(sb + L::DL + (col >> 6) * 8192, sr, col & 63, x);
+                    if (WRITE_O || p.tma_delta) store_row16<T>(sb + L::DL + (col >> 6) * 8192, sr, col & 63, x);
                     store_row16<T>(sb + L::DT + (col >> 6) * 8192, sr, col & 63, y);
-                    if (p.delta) {
+                    if (p.delta && !p.tma_delta) {
                         T *dr = static_cast<T *>(p.delta) + (((long long)(row0 + lc) * Hv + j) * C + sr) * DV + v0 + col;
                         *reinterpret_cast<uint4 *>(dr) =
                             make_uint4(Elt<T>::pack(x[0], x[1]), Elt<T>::pack(x[2], x[3]), Elt<T>::pack(x[4], x[5]),
@@ -571,7 +582,14 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                 umma::fence_before();
                 umma::fence_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(sb + L::B_EPIA);
+                if (lane == 0) {
+                    mbar_arrive(sb + L::B_EPIA);
+                    if (p.tma_delta) {
+                        tma::store3d(&p.tdl, v0 + cb0, q4 * 32, (row0 + lc) * Hv + j,
+                                     sb + L::DL + (cb0 >> 6) * 8192 + q4 * 4096);
+                        tma::commit_group();
+                    }
+                }
             }
             if (!warp_wait(sb + L::B_MB, lc & 1, flag, geo.err, lane)) break;
             umma::fence_after();
@@ -588,8 +606,9 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                 }
             }
             umma::fence_before();
-            write_h();
+            write_h(lc + 1);
         }
+        if (lane == 0 && (p.tma_h || p.tma_delta)) tma::wait_all();  // the stored boxes are complete
         if (!*flag && p.fin) {
 #pragma unroll
             for (int i = 0; i < HW; ++i) {
@@ -711,6 +730,9 @@ struct RevP {
     float *dh0;
     bool gate_f32, l2norm, v_first;
     float scale;
+    // dH' and dDelta leave by TMA store from the bf16 tiles in shared memory (each state warp its own
+    // 32-row x 64-column box); boxes 64 x 32 x 1
+    CUtensorMap tdh, tdd;
 };
 
 template <typename T>
@@ -961,7 +983,12 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
             const int e = cb0 + i;
             hS[i] = p.dht ? p.dht[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] : 0.f;
         }
-        auto write_h = [&]() {
+        // dh' of step lcn (the gradient after chunk chunk_of(lcn)) into the operand tile, and on to dH'
+        auto write_h = [&](int lcn) {
+            if (p.dhn) {
+                if (lane == 0) tma::wait_read();  // the box stored from this tile last time has been read
+                __syncwarp();
+            }
 #pragma unroll
             for (int i = 0; i < HW; i += 16) {
                 const int col = cb0 + i;
@@ -969,9 +996,16 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
             }
             umma::fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(sb + L::B_EPIB);
+            if (lane == 0) {
+                mbar_arrive(sb + L::B_EPIB);
+                if (p.dhn && lcn < nc) {
+                    tma::store3d(&p.tdh, cb0, q4 * 32, (row0 + chunk_of(lcn)) * Hv + j,
+                                 sb + L::H + (cb0 >> 6) * 16384 + q4 * 4096);
+                    tma::commit_group();
+                }
+            }
         };
-        write_h();
+        write_h(0);
         float glo = 0.f;
         auto fetch_gl = [&](int lc) {
             const int c = chunk_of(lc);
@@ -983,21 +1017,16 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
             const int c = chunk_of(lc);
             const float egl = __expf(glo);
             if (lc + 1 < nc) fetch_gl(lc + 1);
-            if (p.dhn) {
-                // the gradient after this chunk
-                T *hr = static_cast<T *>(p.dhn) + ((long long)(row0 + c) * Hv + j) * DK * DV + (long long)d * DV + cb0;
-#pragma unroll
-                for (int i = 0; i < HW; i += 8)
-                    *reinterpret_cast<uint4 *>(hr + i) =
-                        make_uint4(Elt<T>::pack(hS[i], hS[i + 1]), Elt<T>::pack(hS[i + 2], hS[i + 3]),
-                                   Elt<T>::pack(hS[i + 4], hS[i + 5]), Elt<T>::pack(hS[i + 6], hS[i + 7]));
-            }
             if (q4 < 2) {
                 // dDelta rows (lanes 0..63): diag(rk e^{Gl-G}) E + P^T dO
                 if (!warp_wait(sb + L::B_MA, lc & 1, flag, geo.err, lane)) break;
                 umma::fence_after();
                 const int sr = d;
                 const float ck = fa(lc, FCK)[sr];
+                if (p.ddelta) {
+                    if (lane == 0) tma::wait_read();  // the dDelta box stored last step has been read
+                    __syncwarp();
+                }
 #pragma unroll
                 for (int i = 0; i < HW; i += 16) {
                     float x[16], y[16];
@@ -1008,20 +1037,17 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
 #pragma unroll
                     for (int u = 0; u < 16; ++u) x[u] = fmaf(ck, x[u], y[u]);
                     store_row16<T>(sb + L::DL + (col >> 6) * 8192, sr, col & 63, x);
-                    if (p.ddelta) {
-                        T *dr = static_cast<T *>(p.ddelta) + (((long long)(row0 + c) * Hv + j) * C + sr) * DV + col;
-                        *reinterpret_cast<uint4 *>(dr) =
-                            make_uint4(Elt<T>::pack(x[0], x[1]), Elt<T>::pack(x[2], x[3]), Elt<T>::pack(x[4], x[5]),
-                                       Elt<T>::pack(x[6], x[7]));
-                        *reinterpret_cast<uint4 *>(dr + 8) =
-                            make_uint4(Elt<T>::pack(x[8], x[9]), Elt<T>::pack(x[10], x[11]),
-                                       Elt<T>::pack(x[12], x[13]), Elt<T>::pack(x[14], x[15]));
-                    }
                 }
                 umma::fence_before();
                 umma::fence_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(sb + L::B_EPIA);
+                if (lane == 0) {
+                    mbar_arrive(sb + L::B_EPIA);
+                    if (p.ddelta) {
+                        tma::store3d(&p.tdd, cb0, q4 * 32, (row0 + c) * Hv + j, sb + L::DL + (cb0 >> 6) * 8192 + q4 * 4096);
+                        tma::commit_group();
+                    }
+                }
             }
             if (!warp_wait(sb + L::B_MB, lc & 1, flag, geo.err, lane)) break;
             umma::fence_after();
@@ -1035,8 +1061,9 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
                 for (int i = 0; i < 32; ++i) hS[i0 + i] = fmaf(egl, hS[i0 + i], xb[i]);
             }
             umma::fence_before();
-            write_h();
+            write_h(lc + 1);
         }
+        if (lane == 0 && (p.dhn || p.ddelta)) tma::wait_all();  // the stored boxes are complete
         if (!*flag && p.dh0) {
 #pragma unroll
             for (int i = 0; i < HW; ++i) {
@@ -1129,6 +1156,15 @@ cudaError_t launch_chain_ws_pair(const Args &a, const void *q, const void *k, co
         !ws_map(&pb.tdo, dout, a, a.Hv, DV) || !ws_map(&pb.tp, P, a, a.Hv, C) || !ws_map(&pb.ta, A, a, a.Hv, C))
         return cudaErrorInvalidValue;
     pf.tp = pb.tp;
+    const uint64_t srows = (uint64_t)a.max_chunks * a.Hv;
+    auto box_map = [&](CUtensorMap *m, void *base, uint64_t rows_per) {  // [srows][rows_per][128], 64 x 32 boxes
+        return make_tmap_3d(m, base, a.bf16, DV, rows_per, srows, DV * 2, rows_per * DV * 2, 64, 32, 1);
+    };
+    pf.tma_h = h != nullptr;
+    pf.tma_delta = delta != nullptr;
+    if ((h && !box_map(&pf.th, h, DK)) || (delta && !box_map(&pf.tdl, delta, C)) ||
+        (dhn && !box_map(&pb.tdh, dhn, DK)) || (ddelta && !box_map(&pb.tdd, ddelta, C)))
+        return cudaErrorInvalidValue;
     pf.g_cs = g_cs;
     pf.h0 = h0;
     pf.rq = rq;
@@ -1182,6 +1218,8 @@ cudaError_t launch_chain_ws(const Args &a, const void *q, const void *k, const v
     p.v_first = a.v_first;
     p.h_vfirst = h_vfirst;
     p.scale = a.scale;
+    p.tma_h = false;  // (64-column slices: direct stores)
+    p.tma_delta = false;
     if (o)
         return a.bf16 ? chain_ws_t<__nv_bfloat16, 64, true>(a, p, s) : chain_ws_t<__half, 64, true>(a, p, s);
     return a.bf16 ? chain_ws_t<__nv_bfloat16, 64, false>(a, p, s) : chain_ws_t<__half, 64, false>(a, p, s);

@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(PT, 2) chunk_p_tc_kernel(Geo geo, const __grid
     while (cur.y >= 0) {
         const uint32_t st = sb + (uint32_t)stage * ST_BYTES;
         if (tid == 0) {
-            if (umma::mbar_wait(full0 + 8u * (uint32_t)stage, (fph >> stage) & 1u)) {
+            if (umma::mbar_spin(full0 + 8u * (uint32_t)stage, (fph >> stage) & 1u)) {
                 fph ^= 1u << stage;
                 seen[stage] += 1;
             } else {
@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(PT, 2) chunk_p_tc_kernel(Geo geo, const __grid
             (half ? nk : nq)[r] = 1.f;
         }
         if (tid == 0) {
-            if (umma::mbar_wait(mbar, mph)) {
+            if (umma::mbar_spin(mbar, mph)) {
                 mph ^= 1u;
                 mma_out = false;
             } else {

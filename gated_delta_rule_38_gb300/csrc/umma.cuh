@@ -73,6 +73,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, long l
     return false;
 }
 
+// The same wait by spinning on a non-suspending test: a thread that has waited a long time in try_wait was
+// seen to resume several hundred cycles after the phase completed, so waits on a critical path spin.
+__device__ __forceinline__ bool mbar_spin(uint32_t mbar, uint32_t parity, long limit = 200000000L) {
+    uint32_t done = 0;
+    for (long it = 0; it < limit; ++it) {
+        asm volatile(
+            "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(mbar), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::); }
 // Generic-proxy shared stores -> visible to the tensor core (async proxy).
