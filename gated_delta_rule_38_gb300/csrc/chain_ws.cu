@@ -70,7 +70,8 @@ struct Lay {
     static constexpr uint32_t DL = DT + BV * 128;                 // Delta (output product; stored Delta)
     static constexpr uint32_t H = DL + BV * 128;                  // h [128 d][BV]: BV/64 blocks of 16 KB
     static constexpr uint32_t F = H + BV * 256;                   // factor sets (4, by chunk index mod 4)
-    static constexpr uint32_t BAR = F + 4 * NF * 256;
+    static constexpr uint32_t OST = F + 4 * NF * 256;             // output rows of a full chunk [64][BV]
+    static constexpr uint32_t BAR = OST + (WRITE_O ? BV * 128 : 0);
     // barriers
     static constexpr uint32_t B_FULL = BAR, B_EMPTY = BAR + 16, B_PREP = BAR + 32, B_EPIW = BAR + 40,
                               B_MPW = BAR + 48, B_MA = BAR + 56, B_EPIA = BAR + 64, B_MB = BAR + 72,
@@ -102,6 +103,7 @@ struct WsP {
     // bf16 tiles in shared memory: each state warp stores its own 32-row x 64-column box
     bool tma_h, tma_delta;
     CUtensorMap th, tdl;  // h [rows*Hv][128][128], Delta [rows*Hv][64][128]; boxes 64 x 32 x 1
+    CUtensorMap to;       // o [tokens][Hv][128], boxes 64 x 1 x 32 (full chunks' output rows)
 };
 
 // One non-blocking test (the MMA thread polls several barriers in turn).
@@ -627,23 +629,45 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
             umma::fence_after();
             const uint32_t tD = b ? L::T_D1 : L::T_D0;
             T *orow = static_cast<T *>(p.o) + ((tok0 + (long long)lc * C + r) * Hv + j) * DV + v0;
+            // a full chunk's rows leave through the staging tile, this warp's 32 rows as one TMA box (scattered
+            // row stores would crowd the memory instruction queue of the schedulers the state warps share);
+            // a ragged chunk's rows are stored directly (its tail rows belong to the next sequence)
+            const bool staged = valid == C;
+            const uint32_t ost = sb + L::OST;
+            if (staged) {
+                if (lane == 0) tma::wait_read();  // the previous box has left the staging tile
+                __syncwarp();
+            }
 #pragma unroll
             for (int c = 0; c < BV; c += 16) {
                 float x[16];
                 umma::ld16(umma::taddr(tmem, lb, tD + c), x);
                 umma::ld_wait();  // (one 16-column slice at a time keeps the warp's registers low)
-                if (r < valid) {
-                    *reinterpret_cast<uint4 *>(orow + c) =
-                        make_uint4(Elt<T>::pack(x[0], x[1]), Elt<T>::pack(x[2], x[3]), Elt<T>::pack(x[4], x[5]),
-                                   Elt<T>::pack(x[6], x[7]));
-                    *reinterpret_cast<uint4 *>(orow + c + 8) =
-                        make_uint4(Elt<T>::pack(x[8], x[9]), Elt<T>::pack(x[10], x[11]), Elt<T>::pack(x[12], x[13]),
-                                   Elt<T>::pack(x[14], x[15]));
+                const uint32_t w0 = Elt<T>::pack(x[0], x[1]), w1 = Elt<T>::pack(x[2], x[3]),
+                               w2 = Elt<T>::pack(x[4], x[5]), w3 = Elt<T>::pack(x[6], x[7]),
+                               w4 = Elt<T>::pack(x[8], x[9]), w5 = Elt<T>::pack(x[10], x[11]),
+                               w6 = Elt<T>::pack(x[12], x[13]), w7 = Elt<T>::pack(x[14], x[15]);
+                if (staged) {
+                    st_v4(ost + (uint32_t)(c >> 6) * 8192u + umma::off(r, (c & 63), 0), w0, w1, w2, w3);
+                    st_v4(ost + (uint32_t)(c >> 6) * 8192u + umma::off(r, (c & 63) + 8, 0), w4, w5, w6, w7);
+                } else if (r < valid) {
+                    *reinterpret_cast<uint4 *>(orow + c) = make_uint4(w0, w1, w2, w3);
+                    *reinterpret_cast<uint4 *>(orow + c + 8) = make_uint4(w4, w5, w6, w7);
                 }
             }
             umma::fence_before();
+            if (staged) umma::fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(sb + L::B_OFREE + 8 * b);
+            if (lane == 0) {
+                mbar_arrive(sb + L::B_OFREE + 8 * b);
+                if (staged) {
+                    const int t0 = (int)(tok0 + (long long)lc * C) + (warp - 2) * 32;
+#pragma unroll
+                    for (int cb = 0; cb < BV; cb += 64)
+                        tma::store3d(&p.to, v0 + cb, j, t0, ost + (uint32_t)(cb >> 6) * 8192u + (warp - 2) * 4096);
+                    tma::commit_group();
+                }
+            }
             return true;
         };
         bool ok = true;
@@ -673,6 +697,7 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
             if (WRITE_O && lc > 0) ok = out_rows(lc - 1);
         }
         if (WRITE_O && ok && nc > 0) out_rows(nc - 1);
+        if (WRITE_O && lane == 0) tma::wait_all();  // the output boxes are complete
     }
 
     umma::fence_before();
@@ -1200,8 +1225,10 @@ cudaError_t launch_chain_ws(const Args &a, const void *q, const void *k, const v
                             const float *h0, const float *seg_start, void *o, float *final_state, void *h,
                             bool h_vfirst, void *delta, cudaStream_t s) {
     WsP p;
+    const uint64_t tokens = (uint64_t)a.B * (uint64_t)a.T;
     if (!ws_map(&p.tq, q, a, a.Hq, DK) || !ws_map(&p.tk, k, a, a.Hq, DK) || !ws_map(&p.tv, v, a, a.Hv, DV) ||
-        !ws_map(&p.ta, A, a, a.Hv, C) || (o && !ws_map(&p.tp, P, a, a.Hv, C)))
+        !ws_map(&p.ta, A, a, a.Hv, C) || (o && !ws_map(&p.tp, P, a, a.Hv, C)) ||
+        (o && !make_tmap_3d(&p.to, o, a.bf16, DV, a.Hv, tokens, DV * 2, (uint64_t)a.Hv * DV * 2, 64, 1, 32)))
         return cudaErrorInvalidValue;
     p.g_cs = g_cs;
     p.rq = rq;
