@@ -267,58 +267,6 @@ __device__ __forceinline__ void load_rows_async(const Tile &t, const T *src, lon
     }
 }
 
-// ---------------------------------------------------------------- row operations
-
-// In-place per-row L2 normalisation of a [rows x 128] tile: x / sqrt(sum x^2 + eps),
-// computed in fp32 and rounded once.  One warp per row; identical in every kernel.
-// Each warp takes 8 rows at a time: lane l handles a quarter (32 values) of row l/4.
-// When inv_out is given, inv_out[r] receives 1 / sqrt(sum x^2 + eps) of every row r < rows.
-template <typename T>
-__device__ __forceinline__ void l2norm_rows(const Tile &t, int rows, int warp, int nwarps, int lane,
-                                            float *inv_out = nullptr) {
-    const int rq = lane >> 2, qq = lane & 3;
-    for (int r0 = warp * 8; r0 < rows; r0 += nwarps * 8) {
-        const int r = r0 + rq;
-        uint4 u[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const uint32_t a = t.addr(r, qq * 32 + c * 8);
-            asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
-                         : "=r"(u[c].x), "=r"(u[c].y), "=r"(u[c].z), "=r"(u[c].w)
-                         : "r"(a));
-        }
-        float ss = 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 x = Elt<T>::unpack(w[e]);
-                ss += x.x * x.x + x.y * x.y;
-            }
-        }
-        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-        const float inv = 1.0f / sqrtf(ss + L2_EPS);
-        if (r < rows) {
-            if (inv_out && qq == 0) inv_out[r] = inv;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 x = Elt<T>::unpack(w[e]);
-                    w[e] = Elt<T>::pack(x.x * inv, x.y * inv);
-                }
-                const uint32_t a = t.addr(r, qq * 32 + c * 8);
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(a), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-                             "r"(w[3]));
-            }
-        }
-    }
-}
-
-
 // ---------------------------------------------------------------- chunk geometry
 
 struct Geo {
