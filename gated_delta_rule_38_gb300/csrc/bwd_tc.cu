@@ -827,8 +827,14 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             const float tail = warp == 0 ? f(F_DG, 3) : 0.f;
             if (vr) store_gate<T>(p.dg, (tok0 + rr) * Hv + j, p.gate_f32, y + tail + extra);
         }
-        if (upper && last_head) store_row(tok0, valid, hq);
-        // Delta, A (and q, k for a new item) are free: the next unit's last tile group
+        if (upper) {
+            if (last_head) store_row(tok0, valid, hq);
+            // k and Delta's second block are free once the upper-lane warps are done (the lower ones no longer
+            // read them): the next unit's last tile group goes in while warps 0 and 1 finish dG
+            umma::fence_async_smem();
+            asm volatile("bar.sync 3, 256;\n" ::: "memory");  // the eight upper-lane warps
+            if (tid == TT && wn >= 0) issue(nxt, jn, 6);
+        }
         umma::fence_async_smem();
         __syncthreads();
         if (tid == ST && last_head && valid == C) {
@@ -837,7 +843,6 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             tma::commit_group();
         }
         if (wn < 0) break;
-        if (tid == TT) issue(nxt, jn, 6);
         wit = wn;
         jj = jn;
         cur = nxt;
