@@ -545,9 +545,10 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                                        Elt<T>::pack(hS[i + 4], hS[i + 5]), Elt<T>::pack(hS[i + 6], hS[i + 7]));
                 }
             }
-            if (q4 < 2) {
+            bool okw = true;  // every state warp reaches the hardware barrier below, failed or not
+            if (q4 < 2) okw = warp_wait(sb + L::B_MA, lc & 1, flag, geo.err, lane);
+            if (q4 < 2 && okw) {
                 // Delta rows (lanes 0..63): Delta for the output product, diag(rk e^{Gl-G}) Delta for X
-                if (!warp_wait(sb + L::B_MA, lc & 1, flag, geo.err, lane)) break;
                 umma::fence_after();
                 const int sr = d;
                 const float ck = fa(lc, FCK)[sr];
@@ -593,7 +594,11 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                     }
                 }
             }
-            if (!warp_wait(sb + L::B_MB, lc & 1, flag, geo.err, lane)) break;
+            // round B's barrier is polled by one warp and passed on to the other state warps by a hardware
+            // barrier: warps that polled it themselves from the schedulers shared with the -W / output
+            // warps were seen to pass it several hundred cycles late
+            if (warp == 4 && okw) okw = warp_wait(sb + L::B_MB, lc & 1, flag, geo.err, lane);
+            if (!group_and(okw, 2, 256)) break;  // the eight state warps: all go on, or all leave
             umma::fence_after();
             {
                 constexpr int NB = HW < 32 ? HW : 32;
