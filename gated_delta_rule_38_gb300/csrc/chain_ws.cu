@@ -1047,9 +1047,10 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
             const int c = chunk_of(lc);
             const float egl = __expf(glo);
             if (lc + 1 < nc) fetch_gl(lc + 1);
-            if (q4 < 2) {
+            bool okw = true;  // every state warp reaches the hardware barrier below, failed or not
+            if (q4 < 2) okw = warp_wait(sb + L::B_MA, lc & 1, flag, geo.err, lane);
+            if (q4 < 2 && okw) {
                 // dDelta rows (lanes 0..63): diag(rk e^{Gl-G}) E + P^T dO
-                if (!warp_wait(sb + L::B_MA, lc & 1, flag, geo.err, lane)) break;
                 umma::fence_after();
                 const int sr = d;
                 const float ck = fa(lc, FCK)[sr];
@@ -1079,7 +1080,10 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
                     }
                 }
             }
-            if (!warp_wait(sb + L::B_MB, lc & 1, flag, geo.err, lane)) break;
+            // round B's barrier: polled by warp 4, passed on to the other state warps by a hardware barrier
+            // (as in the forward chain)
+            if (warp == 4 && okw) okw = warp_wait(sb + L::B_MB, lc & 1, flag, geo.err, lane);
+            if (!group_and(okw, 2, 256)) break;  // the eight state warps: all go on, or all leave
             umma::fence_after();
 #pragma unroll
             for (int i0 = 0; i0 < HW; i0 += 32) {
