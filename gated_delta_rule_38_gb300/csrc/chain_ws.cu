@@ -415,8 +415,13 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                 fa(lc, FAB)[r] = ok ? be : 0.f;
             }
             // the stage's tiles, and the previous chunk's W and U groups done with the scaled copies of A
-            bool ok = warp_wait(sb + L::B_FULL + 8 * s, (lc >> 1) & 1, flag, geo.err, lane);
-            if (ok && lc > 0) ok = warp_wait(sb + L::B_MPU, (lc - 1) & 1, flag, geo.err, lane);
+            // (warp 12 polls the barriers and the four prep warps share the result through a hardware barrier:
+            // fewer warps polling mbarriers on one scheduler see their phases sooner)
+            bool ok = true;
+            if (warp == 12) {
+                ok = warp_wait(sb + L::B_FULL + 8 * s, (lc >> 1) & 1, flag, geo.err, lane);
+                if (ok && lc > 0) ok = warp_wait(sb + L::B_MPU, (lc - 1) & 1, flag, geo.err, lane);
+            }
             if (!group_and(ok, 1, 128)) break;
             {
                 // A diag(beta e^G rk) and A diag(beta): thread -> row at/2, 32 columns; rows past the end are
@@ -941,8 +946,12 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
                 fa(lc, FAKG)[r] = okr ? be * eg * rk : 0.f;
             }
             // the stage's tiles, and the previous chunk's W group done with A diag(beta e^G rk)
-            bool ok = warp_wait(sb + L::B_FULL + 8 * s, (lc >> 1) & 1, flag, geo.err, lane);
-            if (ok && lc > 0) ok = warp_wait(sb + L::B_MPW, (lc - 1) & 1, flag, geo.err, lane);
+            // (warp 12 polls, the four prep warps share the result through a hardware barrier)
+            bool ok = true;
+            if (warp == 12) {
+                ok = warp_wait(sb + L::B_FULL + 8 * s, (lc >> 1) & 1, flag, geo.err, lane);
+                if (ok && lc > 0) ok = warp_wait(sb + L::B_MPW, (lc - 1) & 1, flag, geo.err, lane);
+            }
             if (!group_and(ok, 1, 128)) break;
             {
                 // A diag(beta e^G rk): thread -> row at/2, 32 columns; rows past the end are zero
