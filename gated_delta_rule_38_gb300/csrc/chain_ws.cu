@@ -415,10 +415,10 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                 fa(lc, FAB)[r] = ok ? be : 0.f;
             }
             // the stage's tiles, and the previous chunk's W and U groups done with the scaled copies of A
-            // (warp 12 polls the barriers and the four prep warps share the result through a hardware barrier:
+            // (warp 14 polls the barriers and the four prep warps share the result through a hardware barrier:
             // fewer warps polling mbarriers on one scheduler see their phases sooner)
             bool ok = true;
-            if (warp == 12) {
+            if (warp == 14) {
                 ok = warp_wait(sb + L::B_FULL + 8 * s, (lc >> 1) & 1, flag, geo.err, lane);
                 if (ok && lc > 0) ok = warp_wait(sb + L::B_MPU, (lc - 1) & 1, flag, geo.err, lane);
             }
@@ -550,8 +550,13 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                                        Elt<T>::pack(hS[i + 4], hS[i + 5]), Elt<T>::pack(hS[i + 6], hS[i + 7]));
                 }
             }
-            bool okw = true;  // every state warp reaches the hardware barrier below, failed or not
-            if (q4 < 2) okw = warp_wait(sb + L::B_MA, lc & 1, flag, geo.err, lane);
+            bool okw = true;  // every state warp reaches the hardware barriers below, failed or not
+            // round A's barrier: polled by warp 5 alone and shared with the other Delta-row warps (4, 8, 9)
+            // through a hardware barrier, so that the MMA thread is the only warp polling on its scheduler
+            if (q4 < 2) {
+                if (warp == 5) okw = warp_wait(sb + L::B_MA, lc & 1, flag, geo.err, lane);
+                okw = group_and(okw, 3, 128);
+            }
             if (q4 < 2 && okw) {
                 // Delta rows (lanes 0..63): Delta for the output product, diag(rk e^{Gl-G}) Delta for X
                 umma::fence_after();
@@ -599,10 +604,10 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                     }
                 }
             }
-            // round B's barrier is polled by one warp and passed on to the other state warps by a hardware
-            // barrier: warps that polled it themselves from the schedulers shared with the -W / output
-            // warps were seen to pass it several hundred cycles late
-            if (warp == 4 && okw) okw = warp_wait(sb + L::B_MB, lc & 1, flag, geo.err, lane);
+            // round B's barrier is polled by one warp (5, after its Delta rows) and passed on to the other state
+            // warps by a hardware barrier: warps that polled it themselves from the schedulers shared with
+            // other polling warps were seen to pass it several hundred cycles late
+            if (warp == 5 && okw) okw = warp_wait(sb + L::B_MB, lc & 1, flag, geo.err, lane);
             if (!group_and(okw, 2, 256)) break;  // the eight state warps: all go on, or all leave
             umma::fence_after();
             {
@@ -946,9 +951,9 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
                 fa(lc, FAKG)[r] = okr ? be * eg * rk : 0.f;
             }
             // the stage's tiles, and the previous chunk's W group done with A diag(beta e^G rk)
-            // (warp 12 polls, the four prep warps share the result through a hardware barrier)
+            // (warp 14 polls, the four prep warps share the result through a hardware barrier)
             bool ok = true;
-            if (warp == 12) {
+            if (warp == 14) {
                 ok = warp_wait(sb + L::B_FULL + 8 * s, (lc >> 1) & 1, flag, geo.err, lane);
                 if (ok && lc > 0) ok = warp_wait(sb + L::B_MPW, (lc - 1) & 1, flag, geo.err, lane);
             }
@@ -1056,8 +1061,13 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
             const int c = chunk_of(lc);
             const float egl = __expf(glo);
             if (lc + 1 < nc) fetch_gl(lc + 1);
-            bool okw = true;  // every state warp reaches the hardware barrier below, failed or not
-            if (q4 < 2) okw = warp_wait(sb + L::B_MA, lc & 1, flag, geo.err, lane);
+            bool okw = true;  // every state warp reaches the hardware barriers below, failed or not
+            // round A's barrier: polled by warp 5 alone and shared with the other Delta-row warps (4, 8, 9)
+            // through a hardware barrier, so that the MMA thread is the only warp polling on its scheduler
+            if (q4 < 2) {
+                if (warp == 5) okw = warp_wait(sb + L::B_MA, lc & 1, flag, geo.err, lane);
+                okw = group_and(okw, 3, 128);
+            }
             if (q4 < 2 && okw) {
                 // dDelta rows (lanes 0..63): diag(rk e^{Gl-G}) E + P^T dO
                 umma::fence_after();
@@ -1091,7 +1101,7 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
             }
             // round B's barrier: polled by warp 4, passed on to the other state warps by a hardware barrier
             // (as in the forward chain)
-            if (warp == 4 && okw) okw = warp_wait(sb + L::B_MB, lc & 1, flag, geo.err, lane);
+            if (warp == 5 && okw) okw = warp_wait(sb + L::B_MB, lc & 1, flag, geo.err, lane);
             if (!group_and(okw, 2, 256)) break;  // the eight state warps: all go on, or all leave
             umma::fence_after();
 #pragma unroll
