@@ -62,7 +62,7 @@ struct WyArgs {
 };
 
 template <typename T>
-__global__ void __launch_bounds__(128) wy_fwd_kernel(Geo geo, const WyArgs w) {
+__global__ void __launch_bounds__(128, 4) wy_fwd_kernel(Geo geo, const WyArgs w) {
     extern __shared__ __align__(1024) unsigned char smem[];
     T *sk = reinterpret_cast<T *>(smem);
     T *sq = reinterpret_cast<T *>(smem + C * DK * 2);
@@ -134,38 +134,52 @@ __global__ void __launch_bounds__(128) wy_fwd_kernel(Geo geo, const WyArgs w) {
         if (w.rq_out && want_p) w.rq_out[(tok0 + tid) * Hv + j] = sRQ[tid];
     }
 
-    // ---- P = scale (q^ k^T o exp(G_r - G_s)) for s <= r < len (warp w owns rows 16w..16w+15), staged
-    //      as rows in the not yet used A^-1 buffer, then stored row by row
+    // ---- P = scale (q^ k^T o exp(G_r - G_s)) for s <= r < len and L = strictly-lower(diag(beta) (k^ k^T o
+    //      exp(G_r - G_s))) in one pass (warp w owns rows 16w..16w+15, column tiles at or left of the diagonal):
+    //      both products take the same K fragments, and each decay factor serves both.  P is staged as rows
+    //      in the not yet used A^-1 buffer and stored row by row; L goes over the Q tile once every warp has
+    //      read its fragments.
+    const bool want_a = w.A_out != nullptr;
     if (want_p) {
-        float acc[8][4];
-        zero_acc<8>(acc);
+        float accp[8][4], accl[8][4];
+        zero_acc<8>(accp);
+        zero_acc<8>(accl);
         const int r0 = warp * 16;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-            uint32_t a[4];
-            load_a(a, tqt, r0, ks * 16, false, lane);
+            uint32_t aq[4], ak[4];
+            load_a(aq, tqt, r0, ks * 16, false, lane);
+            if (want_a) load_a(ak, tk, r0, ks * 16, false, lane);
 #pragma unroll
             for (int np = 0; np < 4; ++np) {
                 if (np <= warp) {
                     uint32_t b[4];
                     load_b2(b, tk, np * 16, ks * 16, false, lane);
-                    mma16816<T>(acc[2 * np], a, b[0], b[1]);
-                    mma16816<T>(acc[2 * np + 1], a, b[2], b[3]);
+                    mma16816<T>(accp[2 * np], aq, b[0], b[1]);
+                    mma16816<T>(accp[2 * np + 1], aq, b[2], b[3]);
+                    if (want_a) {
+                        mma16816<T>(accl[2 * np], ak, b[0], b[1]);
+                        mma16816<T>(accl[2 * np + 1], ak, b[2], b[3]);
+                    }
                 }
             }
         }
+        __syncthreads();  // every warp has its Q and K fragments: the Q tile may become L
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const int r = r0 + gq + 8 * hh, s0 = nt * 8 + tq * 2;
+                const float g0 = __expf(sG[r] - sG[s0]), g1 = __expf(sG[r] - sG[s0 + 1]);
                 const float rr = w.scale * sRQ[r];
-                const float v0 =
-                    (s0 <= r && r < len) ? rr * sRK[s0] * __expf(sG[r] - sG[s0]) * acc[nt][2 * hh] : 0.f;
-                const float v1 = (s0 + 1 <= r && r < len)
-                                     ? rr * sRK[s0 + 1] * __expf(sG[r] - sG[s0 + 1]) * acc[nt][2 * hh + 1]
-                                     : 0.f;
+                const float v0 = (s0 <= r && r < len) ? rr * sRK[s0] * g0 * accp[nt][2 * hh] : 0.f;
+                const float v1 = (s0 + 1 <= r && r < len) ? rr * sRK[s0 + 1] * g1 * accp[nt][2 * hh + 1] : 0.f;
                 *reinterpret_cast<uint32_t *>(sp + r * LDP + s0) = Elt<T>::pack(v0, v1);
+                if (want_a) {
+                    const float lr = sB[r] * sRK[r];
+                    Lm[r * LDF + s0] = (s0 < r && r < len) ? lr * sRK[s0] * g0 * accl[nt][2 * hh] : 0.f;
+                    Lm[r * LDF + s0 + 1] = (s0 + 1 < r && r < len) ? lr * sRK[s0 + 1] * g1 * accl[nt][2 * hh + 1] : 0.f;
+                }
             }
         __syncthreads();
         for (int i = tid; i < C * 8; i += 128) {
@@ -174,12 +188,12 @@ __global__ void __launch_bounds__(128) wy_fwd_kernel(Geo geo, const WyArgs w) {
             *reinterpret_cast<uint4 *>(static_cast<T *>(w.P_out) + ((tok0 + r) * Hv + j) * C + c0) =
                 *reinterpret_cast<const uint4 *>(sp + r * LDP + c0);
         }
-        __syncthreads();  // the Q tile becomes L
+        __syncthreads();  // the staging rows are read: the A^-1 buffer is free
     }
 
-    if (w.A_out) {
-        // ---- L (warp w owns rows 16w..16w+15; only column tiles at or left of the diagonal)
-        {
+    if (want_a) {
+        if (!want_p) {
+            // ---- L alone (warp w owns rows 16w..16w+15; only column tiles at or left of the diagonal)
             float acc[8][4];
             zero_acc<8>(acc);
             const int r0 = warp * 16;
