@@ -103,13 +103,12 @@ __global__ void __launch_bounds__(128, 4) wy_fwd_kernel(Geo geo, const WyArgs w)
     cp_async_wait<0>();
     __syncthreads();
     // inverse L2 norms of the q and k rows (1 without normalisation): the tiles stay as loaded and the
-    // norms enter P and L as row / column factors
-    if (w.l2norm) {
-        row_inv_norms<T>(tk, len, warp, 4, lane, sRK);
-        if (want_p) row_inv_norms<T>(tqt, len, warp, 4, lane, sRQ);
-    } else if (tid < C) {
-        sRK[tid] = 1.f;
-        sRQ[tid] = 1.f;
+    // norms enter P and L as row / column factors.  With P they come from the MMA pass's own fragments.
+    if (!want_p) {
+        if (w.l2norm)
+            row_inv_norms<T>(tk, len, warp, 4, lane, sRK);
+        else if (tid < C)
+            sRK[tid] = 1.f;
     }
     if (warp == 0) {
         float x0 = sG[lane], x1 = sG[lane + 32];
@@ -129,10 +128,13 @@ __global__ void __launch_bounds__(128, 4) wy_fwd_kernel(Geo geo, const WyArgs w)
         if (lane + 32 < len) w.g_cs[(tok0 + lane + 32) * Hv + j] = x1;
     }
     __syncthreads();
-    if (w.l2norm && tid < len) {
-        if (w.rk_out) w.rk_out[(tok0 + tid) * Hv + j] = sRK[tid];
-        if (w.rq_out && want_p) w.rq_out[(tok0 + tid) * Hv + j] = sRQ[tid];
-    }
+    auto store_norms = [&]() {
+        if (w.l2norm && tid < len) {
+            if (w.rk_out) w.rk_out[(tok0 + tid) * Hv + j] = sRK[tid];
+            if (w.rq_out && want_p) w.rq_out[(tok0 + tid) * Hv + j] = sRQ[tid];
+        }
+    };
+    if (!want_p) store_norms();
 
     // ---- P = scale (q^ k^T o exp(G_r - G_s)) for s <= r < len and L = strictly-lower(diag(beta) (k^ k^T o
     //      exp(G_r - G_s))) in one pass (warp w owns rows 16w..16w+15, column tiles at or left of the diagonal):
@@ -145,11 +147,21 @@ __global__ void __launch_bounds__(128, 4) wy_fwd_kernel(Geo geo, const WyArgs w)
         zero_acc<8>(accp);
         zero_acc<8>(accl);
         const int r0 = warp * 16;
+        // sums of squares of this thread's fragment entries: rows r0 + gq (lo) and r0 + gq + 8 (hi) of q and k
+        float sq_lo = 0.f, sq_hi = 0.f, sk_lo = 0.f, sk_hi = 0.f;
+        auto ssq = [](uint32_t u) {
+            const float2 x = Elt<T>::unpack(u);
+            return x.x * x.x + x.y * x.y;
+        };
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
             uint32_t aq[4], ak[4];
             load_a(aq, tqt, r0, ks * 16, false, lane);
-            if (want_a) load_a(ak, tk, r0, ks * 16, false, lane);
+            load_a(ak, tk, r0, ks * 16, false, lane);
+            sq_lo += ssq(aq[0]) + ssq(aq[2]);
+            sq_hi += ssq(aq[1]) + ssq(aq[3]);
+            sk_lo += ssq(ak[0]) + ssq(ak[2]);
+            sk_hi += ssq(ak[1]) + ssq(ak[3]);
 #pragma unroll
             for (int np = 0; np < 4; ++np) {
                 if (np <= warp) {
@@ -164,7 +176,22 @@ __global__ void __launch_bounds__(128, 4) wy_fwd_kernel(Geo geo, const WyArgs w)
                 }
             }
         }
-        __syncthreads();  // every warp has its Q and K fragments: the Q tile may become L
+        // the four lanes of a row group (tq) hold disjoint columns of the same two rows
+#pragma unroll
+        for (int o = 1; o <= 2; o <<= 1) {
+            sq_lo += __shfl_xor_sync(0xffffffffu, sq_lo, o);
+            sq_hi += __shfl_xor_sync(0xffffffffu, sq_hi, o);
+            sk_lo += __shfl_xor_sync(0xffffffffu, sk_lo, o);
+            sk_hi += __shfl_xor_sync(0xffffffffu, sk_hi, o);
+        }
+        if (tq == 0) {
+            sRQ[r0 + gq] = w.l2norm ? 1.0f / sqrtf(sq_lo + L2_EPS) : 1.f;
+            sRQ[r0 + gq + 8] = w.l2norm ? 1.0f / sqrtf(sq_hi + L2_EPS) : 1.f;
+            sRK[r0 + gq] = w.l2norm ? 1.0f / sqrtf(sk_lo + L2_EPS) : 1.f;
+            sRK[r0 + gq + 8] = w.l2norm ? 1.0f / sqrtf(sk_hi + L2_EPS) : 1.f;
+        }
+        __syncthreads();  // every warp has its Q and K fragments (the Q tile may become L) and the norms are in
+        store_norms();
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
