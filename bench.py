@@ -32,8 +32,7 @@ from gated_delta_rule_38_gb300.inputs import WORKLOADS, make_inputs  # noqa: E40
 METRIC = "GDN fwd+bwd tokens/s & TFLOP/s (H=32,K=V=128,bf16) vs roofline, 1xGB300"
 # DRAM bytes (read + write) per launch on the dense workload from one ncu capture of each kernel as it
 # stands (profiles/*_dense_B2_T4096_H32.md); an entry must be removed when its kernel changes.
-NCU_TRAFFIC = {"wy_fwd": 172.4e6, "chain_fwd": 324.0e6, "chunk_p": 151.4e6, "chain_pair": 794.9e6,
-               "bwd_chunk": 883.1e6}
+NCU_TRAFFIC = {"chain_fwd": 324.0e6, "chunk_p": 151.4e6, "chain_pair": 794.9e6, "bwd_chunk": 883.1e6}
 C = 64
 L2_BYTES = 129 * 2 ** 20
 
@@ -163,13 +162,16 @@ def run_ours(args):
     cu = None if w.cu_seqlens is None else torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
 
+    # the forward hands its decayed causal blocks and q/k norms to the backward (one buffer, reused by the steps)
+    saved = gdr.saved_buffer(d["q"], d["v"], d["g"], cu_seqlens=cu, use_qk_l2norm_in_kernel=l2)
+
     def step(dd):
         gcs, A, o, _, fin = gdr.chunk_gated_delta_rule_fwd(
             dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], initial_state=dd["h0"],
-            output_final_state=w.final_state, cu_seqlens=cu, use_qk_l2norm_in_kernel=l2)
+            output_final_state=w.final_state, cu_seqlens=cu, use_qk_l2norm_in_kernel=l2, saved=saved)
         grads = gdr.chunk_gated_delta_rule_bwd(
             dd["q"], dd["k"], dd["v"], gcs, dd["beta"], A, dd["do"], dht=dd["dht"], initial_state=dd["h0"],
-            cu_seqlens=cu, use_qk_l2norm_in_kernel=l2)
+            cu_seqlens=cu, use_qk_l2norm_in_kernel=l2, saved=saved)
         return o, grads
 
     for _ in range(args.warmup):

@@ -23,7 +23,7 @@ import torch
 
 from . import _lib
 
-__all__ = ["chunk_gated_delta_rule", "chunk_gated_delta_rule_fwd", "chunk_gated_delta_rule_bwd",
+__all__ = ["chunk_gated_delta_rule", "chunk_gated_delta_rule_fwd", "chunk_gated_delta_rule_bwd", "saved_buffer",
            "prepare_chunks", "GdrError", "problem", "workspace_bytes"]
 
 GdrError = _lib.GdrError
@@ -86,13 +86,25 @@ def _cu(cu_seqlens):
     return cu_seqlens.contiguous()
 
 
+def saved_buffer(q, v, g, scale=None, cu_seqlens=None, use_qk_l2norm_in_kernel=False, state_v_first=False,
+                 num_segments=0):
+    """A device buffer for the forward's decayed causal blocks and q/k norms (``saved=`` of the forward and
+    backward below), or None when the problem keeps nothing (the intra-GPU split path)."""
+    lib = _lib.load()
+    p = problem(q, v, g, scale, _cu(cu_seqlens), use_qk_l2norm_in_kernel, state_v_first, num_segments)
+    n = ctypes.c_size_t(0)
+    _lib.check(lib.gdr_saved_bytes(ctypes.byref(p), ctypes.byref(n)), "gdr_saved_bytes")
+    return torch.empty(int(n.value), dtype=torch.uint8, device=q.device) if n.value else None
+
+
 def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=True,
                                cu_seqlens=None, use_qk_l2norm_in_kernel=False, state_v_first=False,
-                               num_segments=0, output_h=False, save_for_backward=True, out=None):
+                               num_segments=0, output_h=False, save_for_backward=True, out=None, saved=None):
     """Forward.  Returns (g_cumsum, A, o, h, final_state); h is None unless output_h.
 
     g_cumsum and A are None when save_for_backward is False.  For packed
     batches h has gdr_max_chunks rows; rows past the true chunk count are unused.
+    ``saved`` (from saved_buffer) receives the decayed causal blocks and q/k norms for the backward.
     """
     lib = _lib.load()
     cu = _cu(cu_seqlens)
@@ -112,18 +124,20 @@ def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
     nbytes = workspace_bytes(p, False)
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
     h0 = None if initial_state is None else initial_state.to(torch.float32).contiguous()
-    st = lib.gdr_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o),
-                     _ptr(fin), _ptr(gcs), _ptr(A), _ptr(h), _ptr(ws), nbytes, _stream(dev))
-    _lib.check(st, "gdr_fwd")
+    st = lib.gdr_fwd_ex(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o),
+                        _ptr(fin), _ptr(gcs), _ptr(A), _ptr(h), _ptr(ws), nbytes, _ptr(saved), _stream(dev))
+    _lib.check(st, "gdr_fwd_ex")
     return gcs, A, o, h, fin
 
 
 def chunk_gated_delta_rule_bwd(q, k, v, g, beta, A, do, dht=None, scale=None, initial_state=None,
                                cu_seqlens=None, use_qk_l2norm_in_kernel=False, state_v_first=False,
-                               num_segments=0, gate_dtype=None):
+                               num_segments=0, gate_dtype=None, saved=None):
     """Backward.  ``g`` is the forward's g_cumsum (fp32).  Returns (dq, dk, dv, dbeta, dg, dh0).
 
     dg and dbeta take beta's dtype (or ``gate_dtype``); dh0 is None without an initial state.
+    ``saved`` is the buffer the forward filled for the same problem and inputs (the backward then skips
+    recomputing the decayed causal blocks); None recomputes them.
     """
     lib = _lib.load()
     cu = _cu(cu_seqlens)
@@ -140,10 +154,10 @@ def chunk_gated_delta_rule_bwd(q, k, v, g, beta, A, do, dht=None, scale=None, in
     dht_ = None if dht is None else dht.to(torch.float32).contiguous()
     nbytes = workspace_bytes(p, True)
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
-    st = lib.gdr_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A), _ptr(do),
-                     _ptr(dht_), _ptr(h0), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(db), _ptr(dh0), _ptr(ws),
-                     nbytes, _stream(dev))
-    _lib.check(st, "gdr_bwd")
+    st = lib.gdr_bwd_ex(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A), _ptr(do),
+                        _ptr(dht_), _ptr(h0), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(db), _ptr(dh0), _ptr(ws),
+                        nbytes, _ptr(saved), _stream(dev))
+    _lib.check(st, "gdr_bwd_ex")
     return dq, dk, dv, db, dg, dh0
 
 
@@ -177,21 +191,24 @@ class _GDR(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, g, beta, scale, initial_state, output_final_state, cu_seqlens,
                 use_qk_l2norm_in_kernel, state_v_first, num_segments):
+        saved = saved_buffer(q, v, g, scale=scale, cu_seqlens=cu_seqlens,
+                             use_qk_l2norm_in_kernel=use_qk_l2norm_in_kernel, state_v_first=state_v_first,
+                             num_segments=num_segments)
         gcs, A, o, _, fin = chunk_gated_delta_rule_fwd(
             q, k, v, g, beta, scale=scale, initial_state=initial_state, output_final_state=output_final_state,
             cu_seqlens=cu_seqlens, use_qk_l2norm_in_kernel=use_qk_l2norm_in_kernel, state_v_first=state_v_first,
-            num_segments=num_segments)
-        ctx.save_for_backward(q, k, v, gcs, beta, A, initial_state, cu_seqlens)
+            num_segments=num_segments, saved=saved)
+        ctx.save_for_backward(q, k, v, gcs, beta, A, initial_state, cu_seqlens, saved)
         ctx.opts = (scale, use_qk_l2norm_in_kernel, state_v_first, num_segments, g.dtype)
         return o, fin
 
     @staticmethod
     def backward(ctx, do, dht):
-        q, k, v, gcs, beta, A, h0, cu = ctx.saved_tensors
+        q, k, v, gcs, beta, A, h0, cu, saved = ctx.saved_tensors
         scale, l2, vf, nseg, gdt = ctx.opts
         dq, dk, dv, db, dg, dh0 = chunk_gated_delta_rule_bwd(
             q, k, v, gcs, beta, A, do.contiguous(), dht=dht, scale=scale, initial_state=h0, cu_seqlens=cu,
-            use_qk_l2norm_in_kernel=l2, state_v_first=vf, num_segments=nseg, gate_dtype=gdt)
+            use_qk_l2norm_in_kernel=l2, state_v_first=vf, num_segments=nseg, gate_dtype=gdt, saved=saved)
         return dq, dk, dv, dg, db, None, dh0, None, None, None, None, None
 
 

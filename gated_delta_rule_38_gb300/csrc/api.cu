@@ -243,6 +243,27 @@ Layout layout_of(const gdr_problem *p, bool bwd) {
     return L;
 }
 
+// The forward's decayed causal blocks and inverse q/k norms, kept for the backward (gdr_fwd_ex / gdr_bwd_ex):
+// [P: tokens x Hv x 64 (dtype)][rq: tokens x Hv fp32][rk: tokens x Hv fp32], 256-byte aligned parts; empty
+// when the problem runs the intra-GPU split (that path uses no P).
+struct SavedLayout {
+    size_t P = 0, rq = 0, rk = 0, bytes = 0;
+};
+SavedLayout saved_layout_of(const gdr_problem *p) {
+    SavedLayout S;
+    if (choose_nseg(p) != 1) return S;
+    const size_t tok = (size_t)p->B * p->T;
+    size_t at = 0;
+    S.P = at;
+    at = round_up(at + tok * p->Hv * C * esize(p->dtype), 256);
+    S.rq = at;
+    at = round_up(at + tok * p->Hv * sizeof(float), 256);
+    S.rk = at;
+    at = round_up(at + tok * p->Hv * sizeof(float), 256);
+    S.bytes = at;
+    return S;
+}
+
 SegWs seg_ws(const Layout &L, char *ws) {
     SegWs sw;
     sw.nseg = L.nseg;
@@ -389,13 +410,28 @@ gdr_status gdr_bwd_workspace_size(const gdr_problem *p, size_t *bytes) {
     return GDR_OK;
 }
 
+gdr_status gdr_saved_bytes(const gdr_problem *p, size_t *bytes) {
+    if (!bytes) return GDR_ERR_NULL;
+    gdr_status st = check_problem(p);
+    if (st != GDR_OK) return st;
+    *bytes = saved_layout_of(p).bytes;
+    return GDR_OK;
+}
+
 gdr_status gdr_fwd(const gdr_problem *p, const void *q, const void *k, const void *v, const void *g,
                    const void *beta, const float *h0, void *o, float *final_state, float *g_cumsum, void *A,
                    void *h, void *workspace, size_t workspace_bytes, void *stream) {
+    return gdr_fwd_ex(p, q, k, v, g, beta, h0, o, final_state, g_cumsum, A, h, workspace, workspace_bytes, nullptr,
+                      stream);
+}
+
+gdr_status gdr_fwd_ex(const gdr_problem *p, const void *q, const void *k, const void *v, const void *g,
+                      const void *beta, const float *h0, void *o, float *final_state, float *g_cumsum, void *A,
+                      void *h, void *workspace, size_t workspace_bytes, void *saved, void *stream) {
     gdr_status st = check_problem(p);
     if (st != GDR_OK) return st;
     if (!q || !k || !v || !g || !beta || !o) return GDR_ERR_NULL;
-    const void *ptrs[] = {q, k, v, g, beta, h0, o, final_state, g_cumsum, A, h, p->cu_seqlens};
+    const void *ptrs[] = {q, k, v, g, beta, h0, o, final_state, g_cumsum, A, h, p->cu_seqlens, saved};
     for (const void *x : ptrs)
         if (x && !aligned16(x)) return GDR_ERR_ALIGN;
     const Layout L = layout_of(p, false);
@@ -409,9 +445,12 @@ gdr_status gdr_fwd(const gdr_problem *p, const void *q, const void *k, const voi
     float *gcs = g_cumsum ? g_cumsum : reinterpret_cast<float *>(ws + L.gcs);
     void *Aw = A ? A : static_cast<void *>(ws + L.A);
     const SegWs sw = seg_ws(L, ws);
-    void *Pw = sw.nseg == 1 ? static_cast<void *>(ws + L.P) : nullptr;
-    float *rqw = (sw.nseg == 1 && a.l2norm) ? reinterpret_cast<float *>(ws + L.rq) : nullptr;
-    float *rkw = (sw.nseg == 1 && a.l2norm) ? reinterpret_cast<float *>(ws + L.rk) : nullptr;
+    // P and the norms go to the caller's saved buffer when one is given (the backward then skips its P pass)
+    const SavedLayout S = saved_layout_of(p);
+    char *sv = (saved && S.bytes) ? static_cast<char *>(saved) : nullptr;
+    void *Pw = sw.nseg == 1 ? static_cast<void *>(sv ? sv + S.P : ws + L.P) : nullptr;
+    float *rqw = (sw.nseg == 1 && a.l2norm) ? reinterpret_cast<float *>(sv ? sv + S.rq : ws + L.rq) : nullptr;
+    float *rkw = (sw.nseg == 1 && a.l2norm) ? reinterpret_cast<float *>(sv ? sv + S.rk : ws + L.rk) : nullptr;
     if ((st = timed(K_WY_FWD, s, [&] { return launch_wy_fwd(a, q, k, g, beta, gcs, Aw, Pw, rqw, rkw, s); })) !=
         GDR_OK)
         return st;
@@ -429,11 +468,19 @@ gdr_status gdr_bwd(const gdr_problem *p, const void *q, const void *k, const voi
                    const void *beta, const void *A, const void *dout, const float *dht, const float *h0, void *dq,
                    void *dk, void *dv, void *dg, void *dbeta, float *dh0, void *workspace, size_t workspace_bytes,
                    void *stream) {
+    return gdr_bwd_ex(p, q, k, v, g_cumsum, beta, A, dout, dht, h0, dq, dk, dv, dg, dbeta, dh0, workspace,
+                      workspace_bytes, nullptr, stream);
+}
+
+gdr_status gdr_bwd_ex(const gdr_problem *p, const void *q, const void *k, const void *v, const float *g_cumsum,
+                      const void *beta, const void *A, const void *dout, const float *dht, const float *h0, void *dq,
+                      void *dk, void *dv, void *dg, void *dbeta, float *dh0, void *workspace,
+                      size_t workspace_bytes, const void *saved, void *stream) {
     gdr_status st = check_problem(p);
     if (st != GDR_OK) return st;
     if (!q || !k || !v || !g_cumsum || !beta || !A || !dout || !dq || !dk || !dv || !dg || !dbeta)
         return GDR_ERR_NULL;
-    const void *ptrs[] = {q, k, v, g_cumsum, beta, A, dout, dht, h0, dq, dk, dv, dg, dbeta, dh0, p->cu_seqlens};
+    const void *ptrs[] = {q, k, v, g_cumsum, beta, A, dout, dht, h0, dq, dk, dv, dg, dbeta, dh0, p->cu_seqlens, saved};
     for (const void *x : ptrs)
         if (x && !aligned16(x)) return GDR_ERR_ALIGN;
     const Layout L = layout_of(p, true);
@@ -449,11 +496,15 @@ gdr_status gdr_bwd(const gdr_problem *p, const void *q, const void *k, const voi
     // chunk's gradients in parallel
     const SegWs sw = seg_ws(L, ws);
     if (sw.nseg == 1) {
-        void *Pw = ws + L.P;
-        float *rqw = a.l2norm ? reinterpret_cast<float *>(ws + L.rq) : nullptr;
-        float *rkw = a.l2norm ? reinterpret_cast<float *>(ws + L.rk) : nullptr;
-        if ((st = timed(K_CHUNK_P, s, [&] { return launch_chunk_p_tc(a, q, k, g_cumsum, Pw, rqw, rkw, s); })) !=
-            GDR_OK)
+        // P and the norms: from the forward's saved buffer when given, else recomputed from g_cumsum
+        const SavedLayout S = saved_layout_of(p);
+        const char *sv = (saved && S.bytes) ? static_cast<const char *>(saved) : nullptr;
+        void *Pw = sv ? const_cast<char *>(sv + S.P) : ws + L.P;
+        float *rqw = a.l2norm ? reinterpret_cast<float *>(sv ? const_cast<char *>(sv + S.rq) : ws + L.rq) : nullptr;
+        float *rkw = a.l2norm ? reinterpret_cast<float *>(sv ? const_cast<char *>(sv + S.rk) : ws + L.rk) : nullptr;
+        if (!sv &&
+            (st = timed(K_CHUNK_P, s, [&] { return launch_chunk_p_tc(a, q, k, g_cumsum, Pw, rqw, rkw, s); })) !=
+                GDR_OK)
             return st;
         if ((st = timed(K_CHAIN_PAIR, s, [&] {
                  return launch_chain_ws_pair(a, q, k, v, g_cumsum, beta, A, Pw, rqw, rkw, h0, hw, dlw, dout, dht, dhw,

@@ -152,6 +152,31 @@ gdr_status gdr_bwd(const gdr_problem *p, const void *q, const void *k, const voi
                    void *stream);
 
 /*
+ * Forward and backward that hand the forward's decayed causal blocks
+ * P = scale (q^ k^T o exp(G_r - G_s)) (s <= r) and inverse q/k norms on to the
+ * backward instead of having the backward recompute them (no counterpart on the
+ * pages: an addition of this library; results equal gdr_fwd / gdr_bwd up to
+ * rounding, since the two passes compute the same quantities in different kernels).
+ *   gdr_saved_bytes: bytes of the saved buffer for problem p (host-only; 0 when p
+ *     runs the intra-GPU sequence split, which uses no P -- the buffer is then unused).
+ *   saved: DEVICE buffer of at least gdr_saved_bytes bytes, 256-byte aligned, owned by
+ *     the caller; NULL gives gdr_fwd / gdr_bwd exactly.  gdr_fwd_ex writes it;
+ *     gdr_bwd_ex reads it and must get the buffer written by gdr_fwd_ex for the same
+ *     problem and the same q, k, g (the library cannot check this).
+ *   Other arguments, layouts and errors as gdr_fwd / gdr_bwd.
+ */
+gdr_status gdr_saved_bytes(const gdr_problem *p, size_t *bytes);
+gdr_status gdr_fwd_ex(const gdr_problem *p, const void *q, const void *k, const void *v,
+                      const void *g, const void *beta, const float *h0, void *o,
+                      float *final_state, float *g_cumsum, void *A, void *h, void *workspace,
+                      size_t workspace_bytes, void *saved, void *stream);
+gdr_status gdr_bwd_ex(const gdr_problem *p, const void *q, const void *k, const void *v,
+                      const float *g_cumsum, const void *beta, const void *A, const void *dout,
+                      const float *dht, const float *h0, void *dq, void *dk, void *dv, void *dg,
+                      void *dbeta, float *dh0, void *workspace, size_t workspace_bytes,
+                      const void *saved, void *stream);
+
+/*
  * Forward for callers that cannot allocate device memory (no counterpart on the
  * pages: it is an addition of this library).  Some callers may not call
  * cudaMalloc at all -- code running inside a memory pool it does not own, embedded

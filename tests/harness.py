@@ -40,7 +40,7 @@ def cu_tensor(w: Workload, dev="cuda"):
     return None if w.cu_seqlens is None else torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
 
 
-def gpu_fwd(w: Workload, d, kernel_l2: bool, output_h=False, num_segments=0, gate_f32=False):
+def gpu_fwd(w: Workload, d, kernel_l2: bool, output_h=False, num_segments=0, gate_f32=False, saved=None):
     import gated_delta_rule_38_gb300 as gdr
     g, beta = d["g"], d["beta"]
     if gate_f32:
@@ -48,13 +48,21 @@ def gpu_fwd(w: Workload, d, kernel_l2: bool, output_h=False, num_segments=0, gat
     return gdr.chunk_gated_delta_rule_fwd(
         d["q"], d["k"], d["v"], g, beta, initial_state=d["h0"], output_final_state=w.final_state,
         cu_seqlens=cu_tensor(w), use_qk_l2norm_in_kernel=kernel_l2, state_v_first=w.state_v_first,
-        num_segments=num_segments, output_h=output_h)
+        num_segments=num_segments, output_h=output_h, saved=saved)
 
 
-def gpu_bwd(w: Workload, d, gcs, A, kernel_l2: bool, num_segments=0, gate_f32=False):
+def gpu_bwd(w: Workload, d, gcs, A, kernel_l2: bool, num_segments=0, gate_f32=False, saved=None):
     import gated_delta_rule_38_gb300 as gdr
     beta = d["beta"].float() if gate_f32 else d["beta"]
     return gdr.chunk_gated_delta_rule_bwd(
         d["q"], d["k"], d["v"], gcs, beta, A, d["do"], dht=d["dht"], initial_state=d["h0"],
         cu_seqlens=cu_tensor(w), use_qk_l2norm_in_kernel=kernel_l2, state_v_first=w.state_v_first,
-        num_segments=num_segments)
+        num_segments=num_segments, saved=saved)
+
+
+def gpu_saved(w: Workload, d, kernel_l2: bool, num_segments=0, gate_f32=False):
+    """The forward-to-backward buffer for this workload (None when the problem keeps nothing)."""
+    import gated_delta_rule_38_gb300 as gdr
+    g = d["g"].float() if gate_f32 else d["g"]
+    return gdr.saved_buffer(d["q"], d["v"], g, cu_seqlens=cu_tensor(w), use_qk_l2norm_in_kernel=kernel_l2,
+                            state_v_first=w.state_v_first, num_segments=num_segments)

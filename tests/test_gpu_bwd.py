@@ -7,18 +7,20 @@ import torch
 
 import oracle
 from gated_delta_rule_38_gb300.inputs import WORKLOADS, custom, make_inputs
-from harness import TOL, gpu_bwd, gpu_fwd, np64, oracle_problem, rel_l2, to_dev
+from harness import TOL, gpu_bwd, gpu_fwd, gpu_saved, np64, oracle_problem, rel_l2, to_dev
 
 pytestmark = pytest.mark.gpu
 
 GRADS = ("dq", "dk", "dv", "dbeta", "dg", "dh0")
 
 
-def check_bwd(w, kernel_l2, heads=None, gate_f32=False, num_segments=0):
+def check_bwd(w, kernel_l2, heads=None, gate_f32=False, num_segments=0, saved=False):
     x = make_inputs(w)
     d = to_dev(x)
-    gcs, A, o, _, fin = gpu_fwd(w, d, kernel_l2, num_segments=num_segments, gate_f32=gate_f32)
-    dq, dk, dv, db, dg, dh0 = gpu_bwd(w, d, gcs, A, kernel_l2, num_segments=num_segments, gate_f32=gate_f32)
+    sv = gpu_saved(w, d, kernel_l2, num_segments=num_segments, gate_f32=gate_f32) if saved else None
+    gcs, A, o, _, fin = gpu_fwd(w, d, kernel_l2, num_segments=num_segments, gate_f32=gate_f32, saved=sv)
+    dq, dk, dv, db, dg, dh0 = gpu_bwd(w, d, gcs, A, kernel_l2, num_segments=num_segments, gate_f32=gate_f32,
+                                      saved=sv)
     torch.cuda.synchronize()
     pb = oracle_problem(w, kernel_l2)
     ref = oracle.bwd(pb, x["q"], x["k"], x["v"], x["g"], x["beta"], x["do"], h0=x["h0"], dht=x["dht"],
@@ -55,6 +57,20 @@ def test_tiny():
 
 def test_tiny_kernel_l2norm():
     check_bwd(custom(B=1, T=256, Hq=2, Hv=2, host_l2=False), kernel_l2=True)
+
+
+# the forward's decayed causal blocks and q/k norms handed to the backward (no recompute there)
+@pytest.mark.parametrize("kernel_l2", [False, True])
+def test_saved_blocks(kernel_l2):
+    check_bwd(custom(B=2, T=200, Hq=2, Hv=2, host_l2=not kernel_l2), kernel_l2=kernel_l2, saved=True)
+
+
+def test_saved_blocks_varlen():
+    check_bwd(custom(seq_lens=(7, 0, 130, 64, 1, 65), Hq=2, Hv=2, host_l2=False), kernel_l2=True, saved=True)
+
+
+def test_saved_blocks_gva_fp16():
+    check_bwd(custom(B=2, T=150, Hq=1, Hv=4, dtype=torch.float16, host_l2=False), kernel_l2=True, saved=True)
 
 
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 129, 200])
