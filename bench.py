@@ -32,8 +32,7 @@ from gated_delta_rule_38_gb300.inputs import WORKLOADS, make_inputs  # noqa: E40
 METRIC = "GDN fwd+bwd tokens/s & TFLOP/s (H=32,K=V=128,bf16) vs roofline, 1xGB300"
 # DRAM bytes (read + write) per launch on the dense workload from one ncu capture of each kernel as it
 # stands (profiles/*_dense_B2_T4096_H32.md); an entry must be removed when its kernel changes.
-NCU_TRAFFIC = {"wy_fwd": 172.2e6, "chain_fwd": 324.0e6, "chunk_p": 151.4e6, "chain_pair": 794.9e6,
-               "bwd_chunk": 883.1e6}
+NCU_TRAFFIC = {"wy_fwd": 172.2e6, "chunk_p": 151.4e6, "bwd_chunk": 883.1e6}
 C = 64
 L2_BYTES = 129 * 2 ** 20
 
@@ -252,7 +251,7 @@ def run_ours(args):
         # input of the backward and writes every gradient; the forward recurrence reads the forward's inputs
         # and writes o
         "bwd_chunk": bwd_b, "chain_fwd": fwd_b, "chain_bwd": bwd_b * 0.5, "chain_fwd_recompute": fwd_b,
-        "chain_pair": bwd_b * 0.5, "wy_fwd": fwd_b * 0.4, "chunk_p": fwd_b * 0.4,
+        "chain_pair": bwd_b * 0.5, "chain_rev": bwd_b * 0.5, "wy_fwd": fwd_b * 0.4, "chunk_p": fwd_b * 0.4,
     }
     kb = kernel_bytes.get(name, fwd_b + bwd_b)
     achieved = kb / (per_launch_ms * 1e-3) / 1e9

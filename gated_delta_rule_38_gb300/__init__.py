@@ -88,8 +88,9 @@ def _cu(cu_seqlens):
 
 def saved_buffer(q, v, g, scale=None, cu_seqlens=None, use_qk_l2norm_in_kernel=False, state_v_first=False,
                  num_segments=0):
-    """A device buffer for the forward's decayed causal blocks and q/k norms (``saved=`` of the forward and
-    backward below), or None when the problem keeps nothing (the intra-GPU split path)."""
+    """A device buffer for what the forward keeps for the backward (``saved=`` of the forward and backward
+    below): the decayed causal blocks, the q/k norms, the state before every chunk and Delta of every chunk.
+    None when the problem keeps nothing (the intra-GPU split path)."""
     lib = _lib.load()
     p = problem(q, v, g, scale, _cu(cu_seqlens), use_qk_l2norm_in_kernel, state_v_first, num_segments)
     n = ctypes.c_size_t(0)
@@ -104,8 +105,11 @@ def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
 
     g_cumsum and A are None when save_for_backward is False.  For packed
     batches h has gdr_max_chunks rows; rows past the true chunk count are unused.
-    ``saved`` (from saved_buffer) receives the decayed causal blocks and q/k norms for the backward.
+    ``saved`` (from saved_buffer) receives the decayed causal blocks, q/k norms, states and Delta for the
+    backward; it excludes ``output_h`` (the states then live in ``saved``).
     """
+    if output_h and saved is not None:
+        raise ValueError("output_h and saved are exclusive: with saved, the states are kept in the saved buffer")
     lib = _lib.load()
     cu = _cu(cu_seqlens)
     p = problem(q, v, g, scale, cu, use_qk_l2norm_in_kernel, state_v_first, num_segments)
@@ -137,7 +141,7 @@ def chunk_gated_delta_rule_bwd(q, k, v, g, beta, A, do, dht=None, scale=None, in
 
     dg and dbeta take beta's dtype (or ``gate_dtype``); dh0 is None without an initial state.
     ``saved`` is the buffer the forward filled for the same problem and inputs (the backward then skips
-    recomputing the decayed causal blocks); None recomputes them.
+    recomputing the decayed causal blocks, the states and Delta); None recomputes them.
     """
     lib = _lib.load()
     cu = _cu(cu_seqlens)

@@ -247,12 +247,13 @@ Layout layout_of(const gdr_problem *p, bool bwd) {
 // [P: tokens x Hv x 64 (dtype)][rq: tokens x Hv fp32][rk: tokens x Hv fp32], 256-byte aligned parts; empty
 // when the problem runs the intra-GPU split (that path uses no P).
 struct SavedLayout {
-    size_t P = 0, rq = 0, rk = 0, bytes = 0;
+    size_t P = 0, rq = 0, rk = 0, h = 0, delta = 0, bytes = 0;
 };
 SavedLayout saved_layout_of(const gdr_problem *p) {
     SavedLayout S;
     if (choose_nseg(p) != 1) return S;
     const size_t tok = (size_t)p->B * p->T;
+    const size_t mc = (size_t)max_chunks_of(p);
     size_t at = 0;
     S.P = at;
     at = round_up(at + tok * p->Hv * C * esize(p->dtype), 256);
@@ -260,6 +261,10 @@ SavedLayout saved_layout_of(const gdr_problem *p) {
     at = round_up(at + tok * p->Hv * sizeof(float), 256);
     S.rk = at;
     at = round_up(at + tok * p->Hv * sizeof(float), 256);
+    S.h = at;
+    at = round_up(at + mc * p->Hv * DK * DV * esize(p->dtype), 256);
+    S.delta = at;
+    at = round_up(at + mc * p->Hv * C * DV * esize(p->dtype), 256);
     S.bytes = at;
     return S;
 }
@@ -304,10 +309,11 @@ gdr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_E
 // ---- per-kernel timing: event pairs recorded around each launch while enabled
 enum KernelId {
     K_PREP = 0, K_WY_FWD, K_CHAIN_FWD, K_CHAIN_FWD_RECOMPUTE, K_CHAIN_BWD, K_CHAIN_PAIR, K_BWD_CHUNK, K_CHUNK_P,
-    K_COUNT
+    K_CHAIN_REV, K_COUNT
 };
 const char *const kKernelNames[K_COUNT] = {"prep_chunks", "wy_fwd",     "chain_fwd", "chain_fwd_recompute",
-                                           "chain_bwd",   "chain_pair", "bwd_chunk", "chunk_p"};
+                                           "chain_bwd",   "chain_pair", "bwd_chunk", "chunk_p",
+                                           "chain_rev"};
 struct Pending {
     int id;
     cudaEvent_t a, b;
@@ -434,6 +440,8 @@ gdr_status gdr_fwd_ex(const gdr_problem *p, const void *q, const void *k, const 
     const void *ptrs[] = {q, k, v, g, beta, h0, o, final_state, g_cumsum, A, h, p->cu_seqlens, saved};
     for (const void *x : ptrs)
         if (x && !aligned16(x)) return GDR_ERR_ALIGN;
+    // with a saved buffer the states go there (one copy of them per call)
+    if (h && saved && saved_layout_of(p).bytes) return GDR_ERR_UNSUPPORTED;
     const Layout L = layout_of(p, false);
     if ((st = check_ws(L, workspace, workspace_bytes)) != GDR_OK) return st;
     unsigned *err = nullptr;
@@ -451,13 +459,16 @@ gdr_status gdr_fwd_ex(const gdr_problem *p, const void *q, const void *k, const 
     void *Pw = sw.nseg == 1 ? static_cast<void *>(sv ? sv + S.P : ws + L.P) : nullptr;
     float *rqw = (sw.nseg == 1 && a.l2norm) ? reinterpret_cast<float *>(sv ? sv + S.rq : ws + L.rq) : nullptr;
     float *rkw = (sw.nseg == 1 && a.l2norm) ? reinterpret_cast<float *>(sv ? sv + S.rk : ws + L.rk) : nullptr;
+    // ... and the state before every chunk and Delta of every chunk (the backward then runs no forward recompute)
+    void *hs = sv ? static_cast<void *>(sv + S.h) : h;
+    void *dls = sv ? static_cast<void *>(sv + S.delta) : nullptr;
     if ((st = timed(K_WY_FWD, s, [&] { return launch_wy_fwd(a, q, k, g, beta, gcs, Aw, Pw, rqw, rkw, s); })) !=
         GDR_OK)
         return st;
     if (sw.nseg == 1)
         return timed(K_CHAIN_FWD, s, [&] {
-            return launch_chain_ws(a, q, k, v, gcs, beta, Aw, Pw, rqw, rkw, h0, nullptr, o, final_state, h, a.v_first,
-                                   nullptr, s);
+            return launch_chain_ws(a, q, k, v, gcs, beta, Aw, Pw, rqw, rkw, h0, nullptr, o, final_state, hs,
+                                   sv ? false : a.v_first, dls, s);
         });
     return timed(K_CHAIN_FWD, s, [&] {
         return launch_chain_fwd(a, q, k, v, gcs, beta, Aw, h0, o, final_state, h, true, nullptr, sw, s);
@@ -502,15 +513,24 @@ gdr_status gdr_bwd_ex(const gdr_problem *p, const void *q, const void *k, const 
         void *Pw = sv ? const_cast<char *>(sv + S.P) : ws + L.P;
         float *rqw = a.l2norm ? reinterpret_cast<float *>(sv ? const_cast<char *>(sv + S.rq) : ws + L.rq) : nullptr;
         float *rkw = a.l2norm ? reinterpret_cast<float *>(sv ? const_cast<char *>(sv + S.rk) : ws + L.rk) : nullptr;
-        if (!sv &&
-            (st = timed(K_CHUNK_P, s, [&] { return launch_chunk_p_tc(a, q, k, g_cumsum, Pw, rqw, rkw, s); })) !=
+        if (sv) {
+            // the states and Delta are the forward's: the reverse chain alone, in 64-column slices
+            hw = const_cast<char *>(sv + S.h);
+            dlw = const_cast<char *>(sv + S.delta);
+            if ((st = timed(K_CHAIN_REV, s, [&] {
+                     return launch_chain_rev(a, q, k, g_cumsum, beta, A, Pw, rqw, rkw, dout, dht, dhw, ddlw, dh0, s);
+                 })) != GDR_OK)
+                return st;
+        } else {
+            if ((st = timed(K_CHUNK_P, s, [&] { return launch_chunk_p_tc(a, q, k, g_cumsum, Pw, rqw, rkw, s); })) !=
                 GDR_OK)
-            return st;
-        if ((st = timed(K_CHAIN_PAIR, s, [&] {
-                 return launch_chain_ws_pair(a, q, k, v, g_cumsum, beta, A, Pw, rqw, rkw, h0, hw, dlw, dout, dht, dhw,
-                                             ddlw, dh0, s);
-             })) != GDR_OK)
-            return st;
+                return st;
+            if ((st = timed(K_CHAIN_PAIR, s, [&] {
+                     return launch_chain_ws_pair(a, q, k, v, g_cumsum, beta, A, Pw, rqw, rkw, h0, hw, dlw, dout, dht,
+                                                 dhw, ddlw, dh0, s);
+                 })) != GDR_OK)
+                return st;
+        }
     } else if ((st = timed(K_CHAIN_FWD_RECOMPUTE, s, [&] {
              return launch_chain_fwd(a, q, k, v, g_cumsum, beta, A, h0, nullptr, nullptr, hw, false, dlw, sw, s);
          })) != GDR_OK) {

@@ -143,6 +143,57 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return ok != 0;
 }
 
+// Named-barrier arrival without waiting, and arrival with waiting, over `nthreads` threads.
+__device__ __forceinline__ void bar_arrive(int id, int nthreads) {
+    asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// TMA stores of the state warps' tiles.  Each state warp holds 32 rows (its TMEM lane quadrant q4) of
+// HW = BV/2 columns; a stored box is 32 rows x 64 columns.  With BV = 128 a warp owns its box; with BV = 64
+// warps 4+q4 (cg 0, which issues the store) and 8+q4 (cg 1) share one, and two hardware barriers per pair
+// order the hand-offs: barrier 4+q4 "the box stored from this tile last time has been read" (issuer
+// arrives, partner waits), barrier 8+q4 "the partner's rows are written" (partner arrives, issuer waits).
+// Both warps of a pair pass the same sequence of these barriers, which interlocks them: neither can
+// arrive twice on one barrier before the other has passed it.
+template <int BV>
+struct BoxStore {
+    int q4, cg, lane;
+    __device__ __forceinline__ bool issuer() const { return BV == 128 || cg == 0; }
+    // before the tile is rewritten; `newer_pending`: the issuer has one more recent store group in flight
+    // (of the other tile) that may stay in flight
+    __device__ __forceinline__ void free_tile(bool newer_pending) const {
+        if (issuer() && lane == 0) {
+            if (newer_pending)
+                tma::wait_read1();
+            else
+                tma::wait_read();
+        }
+        __syncwarp();
+        if (BV == 64) {
+            if (cg == 0)
+                bar_arrive(4 + q4, 64);
+            else
+                bar_sync(4 + q4, 64);
+        }
+    }
+    // after the rows are written and fenced for the async proxy: stores the box (map coordinates x, y, z)
+    __device__ __forceinline__ void store(const CUtensorMap *map, int x, int y, int z, uint32_t src) const {
+        if (BV == 64) {
+            if (cg == 0)
+                bar_sync(8 + q4, 64);
+            else
+                bar_arrive(8 + q4, 64);
+        }
+        if (issuer() && lane == 0) {
+            tma::store3d(map, x, y, z, src);
+            tma::commit_group();
+        }
+    }
+};
+
 // Barrier `id` over `nthreads` threads that also ANDs a predicate across them.
 __device__ __forceinline__ bool group_and(bool v, int id, int nthreads) {
     uint32_t r;
@@ -501,12 +552,12 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
             else
                 hS[i] = 0.f;
         }
-        // the state before chunk lcn into the operand tile (and, with tma_h, on to h by this warp's box)
+        const BoxStore<BV> box{q4, cg, lane};
+        const int bx = cb0 & ~63;  // first column of the stored box that holds this warp's columns
+        // the state before chunk lcn into the operand tile (and, with tma_h, on to h as a TMA box)
         auto write_h = [&](int lcn) {
-            if (p.tma_h) {
-                if (lane == 0) tma::wait_read();  // the box stored from this tile last time has been read
-                __syncwarp();
-            }
+            // (a Delta-row warp's newer group in flight is this chunk's Delta box)
+            if (p.tma_h) box.free_tile(q4 < 2 && p.tma_delta && lcn > 0);
 #pragma unroll
             for (int i = 0; i < HW; i += 16) {
                 const int col = cb0 + i;
@@ -514,14 +565,9 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
             }
             umma::fence_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(sb + L::B_EPIB);
-                if (p.tma_h && lcn < nc) {
-                    tma::store3d(&p.th, v0 + cb0, q4 * 32, (row0 + lcn) * Hv + j,
-                                 sb + L::H + (cb0 >> 6) * 16384 + q4 * 4096);
-                    tma::commit_group();
-                }
-            }
+            if (lane == 0) mbar_arrive(sb + L::B_EPIB);
+            if (p.tma_h && lcn < nc)
+                box.store(&p.th, v0 + bx, q4 * 32, (row0 + lcn) * Hv + j, sb + L::H + (bx >> 6) * 16384 + q4 * 4096);
         };
         write_h(0);
         float glo = 0.f;
@@ -562,10 +608,8 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                 umma::fence_after();
                 const int sr = d;
                 const float ck = fa(lc, FCK)[sr];
-                if (p.tma_delta) {
-                    if (lane == 0) tma::wait_read();  // the Delta box stored last chunk has been read
-                    __syncwarp();
-                }
+                // the Delta box stored last chunk has been read (the state box stored since may stay in flight)
+                if (p.tma_delta) box.free_tile(p.tma_h);
                 constexpr int NB = HW < 32 ? HW : 32;  // columns per TMEM load batch
 #pragma unroll
                 for (int i0 = 0; i0 < HW; i0 += NB) {
@@ -595,14 +639,9 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                 umma::fence_before();
                 umma::fence_async_smem();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(sb + L::B_EPIA);
-                    if (p.tma_delta) {
-                        tma::store3d(&p.tdl, v0 + cb0, q4 * 32, (row0 + lc) * Hv + j,
-                                     sb + L::DL + (cb0 >> 6) * 8192 + q4 * 4096);
-                        tma::commit_group();
-                    }
-                }
+                if (lane == 0) mbar_arrive(sb + L::B_EPIA);
+                if (p.tma_delta)
+                    box.store(&p.tdl, v0 + bx, q4 * 32, (row0 + lc) * Hv + j, sb + L::DL + (bx >> 6) * 8192 + q4 * 4096);
             }
             // round B's barrier is polled by one warp (5, after its Delta rows) and passed on to the other state
             // warps by a hardware barrier: warps that polled it themselves from the schedulers shared with
@@ -625,7 +664,7 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
             umma::fence_before();
             write_h(lc + 1);
         }
-        if (lane == 0 && (p.tma_h || p.tma_delta)) tma::wait_all();  // the stored boxes are complete
+        if (lane == 0 && (p.tma_h || p.tma_delta)) tma::wait_all();  // the stored boxes are complete (issuers)
         if (!*flag && p.fin) {
 #pragma unroll
             for (int i = 0; i < HW; ++i) {
@@ -775,9 +814,10 @@ struct RevP {
     CUtensorMap tdh, tdd;
 };
 
-template <typename T>
-__device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const int j, const int n) {
+template <typename T, int BV>
+__device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const int vh, const int j, const int n) {
     using L = RLay;
+    const int v0 = vh * BV;  // this block's value columns v0 .. v0+BV-1
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -827,13 +867,13 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
                 if (lc >= 2 && !wait_phase(sb + L::B_EMPTY + 8 * s, ((lc >> 1) - 1) & 1, flag, geo.err)) break;
                 const uint32_t st = sb + s * L::ST_BYTES, full = sb + L::B_FULL + 8 * s;
                 const int t = (int)(tok0 + (long long)chunk_of(lc) * C);
-                tma::expect_tx(full, 65536u);
+                tma::expect_tx(full, 49152u + (uint32_t)BV * 128u);
                 tma::load3d(st + L::ST_Q0, &p.tq, 0, hq, t, full);
                 tma::load3d(st + L::ST_Q0 + 8192, &p.tq, 64, hq, t, full);
                 tma::load3d(st + L::ST_K0, &p.tk, 0, hq, t, full);
                 tma::load3d(st + L::ST_K0 + 8192, &p.tk, 64, hq, t, full);
-                tma::load3d(st + L::ST_DO, &p.tdo, 0, j, t, full);
-                tma::load3d(st + L::ST_DO + 8192, &p.tdo, 64, j, t, full);
+                tma::load3d(st + L::ST_DO, &p.tdo, v0, j, t, full);
+                if (BV == 128) tma::load3d(st + L::ST_DO + 8192, &p.tdo, v0 + 64, j, t, full);
                 tma::load3d(st + L::ST_A, &p.ta, 0, j, t, full);
                 tma::load3d(st + L::ST_P, &p.tp, 0, j, t, full);
                 ++issued[s];
@@ -844,8 +884,9 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
     } else if (warp == 0) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
-            const uint32_t id_kmn = umma::idesc(128, 128, bf16, false, true);  // K-major A, MN-major B
-            const uint32_t id_mn = umma::idesc(128, 128, bf16, true, true);
+            const uint32_t id_kmn = umma::idesc(128, 128, bf16, false, true);  // K-major A, MN-major B (W)
+            const uint32_t id_kbv = umma::idesc(128, BV, bf16, false, true);   // the same, N = BV
+            const uint32_t id_mn = umma::idesc(128, BV, bf16, true, true);     // MN-major A and B, N = BV
             const uint64_t dZAKG = umma::desc(sb + L::Z, 16, 1024), dH = umma::desc(sb + L::H, 16384, 1024);
             const uint64_t dWS = umma::desc(sb + L::WS, 8192, 1024), dDL = umma::desc(sb + L::DL, 8192, 1024);
             auto issue_pw = [&](int lc) {  // P^T dO and W of chunk lc
@@ -874,7 +915,7 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
                     const uint64_t ak = umma::desc(st + L::ST_K0, 16, 1024);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        umma::mma(tmem + L::T_E, ak + ((((ks >> 2) * 8192) + (ks & 3) * 32) >> 4), dH + ks * 128, id_kmn,
+                        umma::mma(tmem + L::T_E, ak + ((((ks >> 2) * 8192) + (ks & 3) * 32) >> 4), dH + ks * 128, id_kbv,
                                   ks > 0);
                 }
                 umma::commit(sb + L::B_MA);
@@ -1018,21 +1059,21 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
         // ------------------------------------------------------------ state gradient (256 threads)
         const int sw = warp - 4, q4 = warp & 3, cg = sw >> 2;
         const int d = q4 * 32 + lane;
-        constexpr int HW = 64;
+        constexpr int HW = BV / 2;  // value columns per thread
         const int cb0 = cg * HW;
         const long long st_base = ((long long)n * Hv + j) * DK * DV;
         float hS[HW];
 #pragma unroll
         for (int i = 0; i < HW; ++i) {
-            const int e = cb0 + i;
+            const int e = v0 + cb0 + i;
             hS[i] = p.dht ? p.dht[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] : 0.f;
         }
+        const BoxStore<BV> box{q4, cg, lane};
+        const int bx = cb0 & ~63;  // first column of the stored box that holds this warp's columns
         // dh' of step lcn (the gradient after chunk chunk_of(lcn)) into the operand tile, and on to dH'
         auto write_h = [&](int lcn) {
-            if (p.dhn) {
-                if (lane == 0) tma::wait_read();  // the box stored from this tile last time has been read
-                __syncwarp();
-            }
+            // (a dDelta-row warp's newer group in flight is this step's dDelta box)
+            if (p.dhn) box.free_tile(q4 < 2 && p.ddelta && lcn > 0);
 #pragma unroll
             for (int i = 0; i < HW; i += 16) {
                 const int col = cb0 + i;
@@ -1040,14 +1081,10 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
             }
             umma::fence_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(sb + L::B_EPIB);
-                if (p.dhn && lcn < nc) {
-                    tma::store3d(&p.tdh, cb0, q4 * 32, (row0 + chunk_of(lcn)) * Hv + j,
-                                 sb + L::H + (cb0 >> 6) * 16384 + q4 * 4096);
-                    tma::commit_group();
-                }
-            }
+            if (lane == 0) mbar_arrive(sb + L::B_EPIB);
+            if (p.dhn && lcn < nc)
+                box.store(&p.tdh, v0 + bx, q4 * 32, (row0 + chunk_of(lcn)) * Hv + j,
+                          sb + L::H + (bx >> 6) * 16384 + q4 * 4096);
         };
         write_h(0);
         float glo = 0.f;
@@ -1073,10 +1110,8 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
                 umma::fence_after();
                 const int sr = d;
                 const float ck = fa(lc, FCK)[sr];
-                if (p.ddelta) {
-                    if (lane == 0) tma::wait_read();  // the dDelta box stored last step has been read
-                    __syncwarp();
-                }
+                // the dDelta box stored last step has been read (the dh' box stored since may stay in flight)
+                if (p.ddelta) box.free_tile(p.dhn != nullptr);
 #pragma unroll
                 for (int i = 0; i < HW; i += 16) {
                     float x[16], y[16];
@@ -1091,13 +1126,9 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
                 umma::fence_before();
                 umma::fence_async_smem();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(sb + L::B_EPIA);
-                    if (p.ddelta) {
-                        tma::store3d(&p.tdd, cb0, q4 * 32, (row0 + c) * Hv + j, sb + L::DL + (cb0 >> 6) * 8192 + q4 * 4096);
-                        tma::commit_group();
-                    }
-                }
+                if (lane == 0) mbar_arrive(sb + L::B_EPIA);
+                if (p.ddelta)
+                    box.store(&p.tdd, v0 + bx, q4 * 32, (row0 + c) * Hv + j, sb + L::DL + (bx >> 6) * 8192 + q4 * 4096);
             }
             // round B's barrier: polled by warp 4, passed on to the other state warps by a hardware barrier
             // (as in the forward chain)
@@ -1120,7 +1151,7 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
         if (!*flag && p.dh0) {
 #pragma unroll
             for (int i = 0; i < HW; ++i) {
-                const int e = cb0 + i;
+                const int e = v0 + cb0 + i;
                 p.dh0[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] = hS[i];
             }
         }
@@ -1154,9 +1185,9 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
     if (warp == 0) umma::dealloc(tmem, 512);
 }
 
-template <typename T>
+template <typename T, int BV>
 __global__ void __launch_bounds__(WS_NT, 1) chain_rev_kernel(Geo geo, const __grid_constant__ RevP p) {
-    ws_rev_body<T>(geo, p, blockIdx.y, blockIdx.z);
+    ws_rev_body<T, BV>(geo, p, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
 // The backward's two chains side by side: blocks z < N recompute the forward states (all 128 value
@@ -1167,13 +1198,29 @@ __global__ void __launch_bounds__(WS_NT, 1) chain_ws_pair_kernel(Geo geo, const 
     if ((int)blockIdx.z < geo.N)
         ws_fwd_body<T, 128, false>(geo, pf, 0, blockIdx.y, blockIdx.z);
     else
-        ws_rev_body<T>(geo, pb, blockIdx.y, blockIdx.z - geo.N);
+        ws_rev_body<T, 128>(geo, pb, 0, blockIdx.y, blockIdx.z - geo.N);
 }
 
 bool ws_map(CUtensorMap *m, const void *base, const Args &a, int heads, int cols) {
     const uint64_t tokens = (uint64_t)a.B * (uint64_t)a.T;
     return make_tmap_3d(m, base, a.bf16, (uint64_t)cols, (uint64_t)heads, tokens, (uint64_t)cols * 2,
                         (uint64_t)heads * cols * 2, 64, 1, 64);
+}
+
+// Per-chunk tiles [rows x Hv][rows_per][128 columns] (states, Delta and their gradients), 64 x 32 boxes.
+bool box_map(CUtensorMap *m, void *base, const Args &a, uint64_t rows_per) {
+    const uint64_t srows = (uint64_t)a.max_chunks * a.Hv;
+    return make_tmap_3d(m, base, a.bf16, DV, rows_per, srows, DV * 2, rows_per * DV * 2, 64, 32, 1);
+}
+
+template <typename T>
+cudaError_t chain_rev_t(const Args &a, const RevP &p, cudaStream_t s) {
+    constexpr int BV = 64;
+    auto kern = chain_rev_kernel<T, BV>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, RLay::BYTES);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(DV / BV, a.Hv, a.N), WS_NT, RLay::BYTES, s>>>(make_geo(a), p);
+    return cudaGetLastError();
 }
 
 template <typename T, int BV, bool WRITE_O>
@@ -1209,14 +1256,10 @@ cudaError_t launch_chain_ws_pair(const Args &a, const void *q, const void *k, co
         !ws_map(&pb.tdo, dout, a, a.Hv, DV) || !ws_map(&pb.tp, P, a, a.Hv, C) || !ws_map(&pb.ta, A, a, a.Hv, C))
         return cudaErrorInvalidValue;
     pf.tp = pb.tp;
-    const uint64_t srows = (uint64_t)a.max_chunks * a.Hv;
-    auto box_map = [&](CUtensorMap *m, void *base, uint64_t rows_per) {  // [srows][rows_per][128], 64 x 32 boxes
-        return make_tmap_3d(m, base, a.bf16, DV, rows_per, srows, DV * 2, rows_per * DV * 2, 64, 32, 1);
-    };
     pf.tma_h = h != nullptr;
     pf.tma_delta = delta != nullptr;
-    if ((h && !box_map(&pf.th, h, DK)) || (delta && !box_map(&pf.tdl, delta, C)) ||
-        (dhn && !box_map(&pb.tdh, dhn, DK)) || (ddelta && !box_map(&pb.tdd, ddelta, C)))
+    if ((h && !box_map(&pf.th, h, a, DK)) || (delta && !box_map(&pf.tdl, delta, a, C)) ||
+        (dhn && !box_map(&pb.tdh, dhn, a, DK)) || (ddelta && !box_map(&pb.tdd, ddelta, a, C)))
         return cudaErrorInvalidValue;
     pf.g_cs = g_cs;
     pf.h0 = h0;
@@ -1248,6 +1291,29 @@ cudaError_t launch_chain_ws_pair(const Args &a, const void *q, const void *k, co
     return a.bf16 ? chain_ws_pair_t<__nv_bfloat16>(a, pf, pb, s) : chain_ws_pair_t<__half>(a, pf, pb, s);
 }
 
+cudaError_t launch_chain_rev(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
+                             const void *A, const void *P, const float *rq, const float *rk, const void *dout,
+                             const float *dht, void *dhn, void *ddelta, float *dh0, cudaStream_t s) {
+    RevP pb;
+    if (!ws_map(&pb.tq, q, a, a.Hq, DK) || !ws_map(&pb.tk, k, a, a.Hq, DK) || !ws_map(&pb.tdo, dout, a, a.Hv, DV) ||
+        !ws_map(&pb.tp, P, a, a.Hv, C) || !ws_map(&pb.ta, A, a, a.Hv, C) ||
+        (dhn && !box_map(&pb.tdh, dhn, a, DK)) || (ddelta && !box_map(&pb.tdd, ddelta, a, C)))
+        return cudaErrorInvalidValue;
+    pb.g_cs = g_cs;
+    pb.rq = rq;
+    pb.rk = rk;
+    pb.dht = dht;
+    pb.beta = beta;
+    pb.dhn = dhn;
+    pb.ddelta = ddelta;
+    pb.dh0 = dh0;
+    pb.gate_f32 = a.gate_f32;
+    pb.l2norm = a.l2norm;
+    pb.v_first = a.v_first;
+    pb.scale = a.scale;
+    return a.bf16 ? chain_rev_t<__nv_bfloat16>(a, pb, s) : chain_rev_t<__half>(a, pb, s);
+}
+
 cudaError_t launch_chain_ws(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
                             const void *beta, const void *A, const void *P, const float *rq, const float *rk,
                             const float *h0, const float *seg_start, void *o, float *final_state, void *h,
@@ -1273,8 +1339,11 @@ cudaError_t launch_chain_ws(const Args &a, const void *q, const void *k, const v
     p.v_first = a.v_first;
     p.h_vfirst = h_vfirst;
     p.scale = a.scale;
-    p.tma_h = false;  // (64-column slices: direct stores)
-    p.tma_delta = false;
+    // the states leave as TMA boxes (the [K][V] layout; the [V][K] layout by direct stores), Delta likewise
+    p.tma_h = h != nullptr && !h_vfirst;
+    p.tma_delta = delta != nullptr;
+    if ((p.tma_h && !box_map(&p.th, h, a, DK)) || (p.tma_delta && !box_map(&p.tdl, delta, a, C)))
+        return cudaErrorInvalidValue;
     if (o)
         return a.bf16 ? chain_ws_t<__nv_bfloat16, 64, true>(a, p, s) : chain_ws_t<__half, 64, true>(a, p, s);
     return a.bf16 ? chain_ws_t<__nv_bfloat16, 64, false>(a, p, s) : chain_ws_t<__half, 64, false>(a, p, s);

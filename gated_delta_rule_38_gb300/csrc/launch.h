@@ -63,6 +63,12 @@ cudaError_t launch_chain_ws_pair(const Args &a, const void *q, const void *k, co
                                  const void *beta, const void *A, const void *P, const float *rq, const float *rk,
                                  const float *h0, void *h, void *delta, const void *dout, const float *dht,
                                  void *dhn, void *ddelta, float *dh0, cudaStream_t s);
+// Backward without a sequence split, the reverse chain alone (dH' and dDelta of every chunk, dh0), warp-
+// specialised, one CTA per (sequence, value head, 64-column slice); for callers that hold the forward's
+// states and Delta.  P, rq, rk as for launch_chain_ws_pair.
+cudaError_t launch_chain_rev(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
+                             const void *A, const void *P, const float *rq, const float *rk, const void *dout,
+                             const float *dht, void *dhn, void *ddelta, float *dh0, cudaStream_t s);
 // Backward: reverse state-gradient chain (dH' and dDelta of every chunk, dh0).
 cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
                              const void *A, const void *dout, const float *dht, void *dhn, void *ddelta, float *dh0,

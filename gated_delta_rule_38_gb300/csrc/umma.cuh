@@ -156,6 +156,8 @@ __device__ __forceinline__ void store3d(const void *map, int c0, int c1, int c2,
 }
 __device__ __forceinline__ void commit_group() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+// ... until all but the most recent group have finished reading shared memory
+__device__ __forceinline__ void wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory"); }
 __device__ __forceinline__ void wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 
 // One arrival that also announces `bytes` of transactions on the barrier's current phase.

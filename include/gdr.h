@@ -152,17 +152,22 @@ gdr_status gdr_bwd(const gdr_problem *p, const void *q, const void *k, const voi
                    void *stream);
 
 /*
- * Forward and backward that hand the forward's decayed causal blocks
- * P = scale (q^ k^T o exp(G_r - G_s)) (s <= r) and inverse q/k norms on to the
- * backward instead of having the backward recompute them (no counterpart on the
- * pages: an addition of this library; results equal gdr_fwd / gdr_bwd up to
- * rounding, since the two passes compute the same quantities in different kernels).
+ * Forward and backward that hand on to the backward what it would otherwise
+ * recompute (no counterpart on the pages: an addition of this library): the decayed
+ * causal blocks P = scale (q^ k^T o exp(G_r - G_s)) (s <= r), the inverse q/k norms,
+ * the state before every chunk and Delta = U - W h of every chunk.  The backward then
+ * runs the reverse state-gradient chain alone.  Results equal gdr_fwd / gdr_bwd up to
+ * rounding (the same quantities, computed by other kernels).  The buffer costs
+ * memory: for B x T tokens and Hv heads about B*T*Hv*(128 + 8 + 2*128*128/64 + 2*128)
+ * bytes at 16-bit data, i.e. about 0.9 KB per token and head.
  *   gdr_saved_bytes: bytes of the saved buffer for problem p (host-only; 0 when p
  *     runs the intra-GPU sequence split, which uses no P -- the buffer is then unused).
  *   saved: DEVICE buffer of at least gdr_saved_bytes bytes, 256-byte aligned, owned by
  *     the caller; NULL gives gdr_fwd / gdr_bwd exactly.  gdr_fwd_ex writes it;
  *     gdr_bwd_ex reads it and must get the buffer written by gdr_fwd_ex for the same
- *     problem and the same q, k, g (the library cannot check this).
+ *     problem, the same q, k, v, g, beta and h0 (the library cannot check this).
+ *   h: must be NULL when saved is used (GDR_ERR_UNSUPPORTED otherwise): the states
+ *     are then kept in the saved buffer.
  *   Other arguments, layouts and errors as gdr_fwd / gdr_bwd.
  */
 gdr_status gdr_saved_bytes(const gdr_problem *p, size_t *bytes);
