@@ -308,6 +308,20 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                 tma::load3d(st + L::ST_K1, &p.tk, 64, hq, t, fl);
                 if (WRITE_O) tma::load3d(st + L::ST_P, &p.tp, 0, j, t, fl);
                 ++issued_l[s];
+                // the next chunk's boxes into L2 now: its loads wait for this stage's turn, a chunk from now
+                if (lc + 1 < nc) {
+                    const int tn = t + C;
+                    if (WRITE_O) {
+                        tma::prefetch3d(&p.tq, 0, hq, tn);
+                        tma::prefetch3d(&p.tq, 64, hq, tn);
+                        tma::prefetch3d(&p.tp, 0, j, tn);
+                    }
+                    tma::prefetch3d(&p.tv, v0, j, tn);
+                    if (BV == 128) tma::prefetch3d(&p.tv, v0 + 64, j, tn);
+                    tma::prefetch3d(&p.ta, 0, j, tn);
+                    tma::prefetch3d(&p.tk, 0, hq, tn);
+                    tma::prefetch3d(&p.tk, 64, hq, tn);
+                }
             }
             // let every load in flight land before the block can exit (bounded)
             for (int s = 0; s < 2; ++s) {
@@ -877,6 +891,18 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
                 tma::load3d(st + L::ST_A, &p.ta, 0, j, t, full);
                 tma::load3d(st + L::ST_P, &p.tp, 0, j, t, full);
                 ++issued[s];
+                // the next chunk's boxes into L2 now: its loads wait for this stage's turn, a chunk from now
+                if (lc + 1 < nc) {
+                    const int tn = (int)(tok0 + (long long)chunk_of(lc + 1) * C);
+                    tma::prefetch3d(&p.tq, 0, hq, tn);
+                    tma::prefetch3d(&p.tq, 64, hq, tn);
+                    tma::prefetch3d(&p.tk, 0, hq, tn);
+                    tma::prefetch3d(&p.tk, 64, hq, tn);
+                    tma::prefetch3d(&p.tdo, v0, j, tn);
+                    if (BV == 128) tma::prefetch3d(&p.tdo, v0 + 64, j, tn);
+                    tma::prefetch3d(&p.ta, 0, j, tn);
+                    tma::prefetch3d(&p.tp, 0, j, tn);
+                }
             }
             for (int s = 0; s < 2; ++s)
                 if (issued[s] > 0) umma::mbar_wait(sb + L::B_FULL + 8 * s, (issued[s] - 1) & 1, 4000000L);

@@ -145,6 +145,14 @@ __device__ __forceinline__ void load3d(uint32_t dst, const void *map, int c0, in
         : "memory");
 }
 
+// A hint that brings a box into L2 ahead of its load (no shared memory, no completion to wait for).
+__device__ __forceinline__ void prefetch3d(const void *map, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 // 3-D tiled bulk tensor store from shared memory (same box and swizzle as the loads), as one bulk group of the
 // issuing thread; `commit_group` closes the group, `wait_read` waits until the thread's groups have finished
 // reading shared memory, `wait_all` until they are complete.

@@ -121,3 +121,29 @@ def test_prepare_chunks_host_checks(lib):
     assert lib.gdr_prepare_chunks(P, 2, 8, 2, P, 4, P, P, None) == 2
     assert lib.gdr_prepare_chunks(None, 2, 8, 2, P, 5, P, P, None) == 1
     assert lib.gdr_prepare_chunks(P, 0, 8, 2, P, 5, P, P, None) == 2
+
+
+def test_saved_buffer_size_and_exclusive_states(lib):
+    """The saved buffer holds P, the q/k norms, the per-chunk states and Delta; it excludes an h output."""
+    p = prob(B=2, T=4096, Hq=32, Hv=32)
+    n = ctypes.c_size_t()
+    assert lib.gdr_saved_bytes(ctypes.byref(p), ctypes.byref(n)) == 0
+    tok, rows = 2 * 4096 * 32, 128 * 32
+    assert n.value == tok * 64 * 2 + 2 * tok * 4 + rows * 128 * 128 * 2 + rows * 64 * 128 * 2
+    P = 0x100000
+    st = lib.gdr_fwd_ex(ctypes.byref(p), P, P, P, P, P, None, P, None, None, None, P, 0x200000, 1 << 40, P, None)
+    assert st == 4
+    # the split path keeps nothing, so there the two do not clash (the call goes on to the device checks)
+    ps = prob(B=1, T=65536, Hq=16, Hv=16, num_segments=4)
+    assert lib.gdr_saved_bytes(ctypes.byref(ps), ctypes.byref(n)) == 0 and n.value == 0
+    st = lib.gdr_fwd_ex(ctypes.byref(ps), P, P, P, P, P, None, P, None, None, None, P, 0x200000, 1 << 40, P, None)
+    assert st != 4
+
+
+def test_binding_rejects_states_with_saved():
+    import torch
+    import gated_delta_rule_38_gb300 as gdr
+    x = torch.zeros(1, 64, 1, 128, dtype=torch.bfloat16)
+    g = torch.zeros(1, 64, 1)
+    with pytest.raises(ValueError):
+        gdr.chunk_gated_delta_rule_fwd(x, x, x, g, g, output_h=True, saved=torch.zeros(16, dtype=torch.uint8))

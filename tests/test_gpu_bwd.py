@@ -69,6 +69,14 @@ def test_saved_blocks_varlen():
     check_bwd(custom(seq_lens=(7, 0, 130, 64, 1, 65), Hq=2, Hv=2, host_l2=False), kernel_l2=True, saved=True)
 
 
+def test_saved_state_v_first():
+    check_bwd(custom(B=2, T=150, Hq=1, Hv=2, state_v_first=True), kernel_l2=False, saved=True)
+
+
+def test_saved_no_initial_state():
+    check_bwd(custom(B=1, T=100, Hq=1, Hv=1, has_h0=False, final_state=False), kernel_l2=False, saved=True)
+
+
 def test_saved_blocks_gva_fp16():
     check_bwd(custom(B=2, T=150, Hq=1, Hv=4, dtype=torch.float16, host_l2=False), kernel_l2=True, saved=True)
 
@@ -125,7 +133,10 @@ def test_autograd_function():
         assert rel_l2(np64(d[name].grad), ref[key]) <= TOL, name
 
 
-@pytest.mark.parametrize("name,heads", [("dense", [0, 17]), ("varlen", [5]), ("gva", [6, 7]), ("long", [3])])
-def test_full_size_sampled_heads(name, heads):
+# full sizes: the dense case as the training step runs it (the forward's saved buffer, the reverse chain alone)
+# and without the buffer (forward recompute beside the reverse chain); the long sequence runs the split path
+@pytest.mark.parametrize("name,heads,saved", [("dense", [0, 17], True), ("dense", [31], False),
+                                              ("varlen", [5], True), ("gva", [6, 7], True), ("long", [3], False)])
+def test_full_size_sampled_heads(name, heads, saved):
     w = WORKLOADS[name]
-    check_bwd(w, kernel_l2=not w.host_l2, heads=heads)
+    check_bwd(w, kernel_l2=not w.host_l2, heads=heads, saved=saved)
