@@ -13,11 +13,11 @@
 //   state-independent products, issued while the previous chunk's recurrence runs:
 //     [0 ; A diag(beta e^G rk)] K   -> W in TMEM lanes 64..127                (M=128, N=128, K=64)
 //     [A diag(beta) ; 0] V          -> U in lanes 0..63, 0 in 64..127         (M=128, N=BV,  K=64)
-//     preparation: Q~ = diag(scale rq e^G) Q in place; the -W epilogue fills the rows above Q~
+//     the -W epilogue fills the rows above Q in the stage
 //   the recurrence, two dependent MMA rounds:
-//     round A:  [-W ; Q~] h added to [U ; 0]  -> Delta = U - W h (lanes 0..63), Q~ h (64..127)
-//     round B:  X = K^T (diag(rk e^{Gl-G}) Delta) ;  [. ; P] Delta added to lanes 64..127 -> output rows
-//     epilogue: h <- e^{Gl} h + X
+//     round A:  [-W ; Q] h added to [U ; 0]   -> Delta = U - W h (lanes 0..63), Q h (64..127)
+//     round B:  X = K^T (diag(rk e^{Gl-G}) Delta) ;  [. ; P] Delta -> its own columns (lanes 64..127)
+//     epilogues: h <- e^{Gl} h + X ; output rows o = diag(scale rq e^G) Q h + P Delta
 //
 // This is the chunk form of S_t = e^{g_t} S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
 // o_t = scale S_t q_t (FlashQLA skill page, "Core API"; gated delta rule chunk form with the
@@ -30,8 +30,7 @@
 //   warps 2,3         TMEM lanes 64..127: the -W epilogue and the output rows
 //   warps 4..11       the state: TMEM lane 32*(w%4)+l, value columns of half (w-4)/4 of the slice;
 //                     warps 4,5,8,9 also move Delta (lanes 0..63) into shared memory
-//   warps 12..15      per-chunk preparation (one warp per scheduler): gate factors, scaled copies of
-//                     A, Q~
+//   warps 12..15      per-chunk preparation (one warp per scheduler): gate factors, scaled copies of A
 // Hand-offs go through mbarriers whose phases each complete once per chunk; every wait is
 // bounded and gives up early once another role has raised the block's error flag.
 #include <cuda_runtime.h>
@@ -55,9 +54,9 @@ enum { FG = 0, FRQ, FRK, FB, FCQ, FCK, FAKG, FAB, NF };
 template <int BV, bool WRITE_O = true>
 struct Lay {
     // stage, 8 KB blocks of 64 rows x 128 B:
-    //   with the output: [-W b0 | Q~ b0 | -W b1 | Q~ b1 | K b0 | K b1 | V | A | P]
+    //   with the output: [-W b0 | Q b0 | -W b1 | Q b1 | K b0 | K b1 | V | A | P]
     //   without it:      [-W b0 | K b0 | -W b1 | K b1 | V | A]      (K doubles as the idle rows of round A)
-    // ([-W; Q~] (or [-W; K]) is one K-major 128-row operand per key half, [A; P] one 128-row operand)
+    // ([-W; Q] (or [-W; K]) is one K-major 128-row operand per key half, [A; P] one 128-row operand)
     static constexpr uint32_t ST_W0 = 0, ST_Q0 = 8192, ST_W1 = 16384, ST_Q1 = 24576;
     static constexpr uint32_t ST_K0 = WRITE_O ? 32768 : 8192, ST_K1 = WRITE_O ? 40960 : 24576;
     static constexpr uint32_t LBO_K = ST_K1 - ST_K0;
@@ -84,9 +83,11 @@ struct Lay {
     static constexpr uint32_t BYTES = USED + 1024;  // slack for aligning the base
     // TMEM columns
     static constexpr uint32_t T_W = 0, T_D0 = 128, T_D1 = 128 + BV, T_X = 128 + 2 * BV;
+    // P Delta of the output rows, by chunk parity (lanes 64..127; with the output only)
+    static constexpr uint32_t T_PD0 = 128 + 3 * BV, T_PD1 = 128 + 4 * BV;
 };
 static_assert(Lay<64>::BYTES <= 232448 && Lay<128, false>::BYTES <= 232448, "shared memory");
-static_assert(Lay<128, false>::T_X + 128 <= 512, "tensor memory");
+static_assert(Lay<128, false>::T_X + 128 <= 512 && Lay<64>::T_PD1 + 64 <= 512, "tensor memory");
 
 struct WsP {
     CUtensorMap tq, tk, tv, tp, ta;  // [tokens][heads][cols] maps, boxes 64 x 1 x 64
@@ -194,6 +195,17 @@ struct BoxStore {
     }
 };
 
+// Warp-uniform waits for the roles whose work one lane issues (TMA producer, MMA issuer): the whole warp
+// runs the role's loop and lane 0 alone issues, so no lane of the warp sits at the block's final barrier
+// while lane 0 works.
+__device__ __forceinline__ bool uwait(uint32_t bar, uint32_t parity, volatile int *flag, unsigned *err) {
+    return __all_sync(0xffffffffu, wait_phase(bar, parity, flag, err));
+}
+__device__ __forceinline__ bool utest(uint32_t bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_test(bar, parity));
+}
+__device__ __forceinline__ bool uflag(volatile int *flag) { return __any_sync(0xffffffffu, *flag != 0); }
+
 // Barrier `id` over `nthreads` threads that also ANDs a predicate across them.
 __device__ __forceinline__ bool group_and(bool v, int id, int nthreads) {
     uint32_t r;
@@ -283,44 +295,45 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
 
     if (warp == 1) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        {
+            const bool l0 = lane == 0;
             int issued[2] = {0, 0}, issued_l[2] = {0, 0};
-            for (int lc = 0; lc < nc && !*flag; ++lc) {
+            for (int lc = 0; lc < nc && !uflag(flag); ++lc) {
                 const int s = lc & 1;
                 const uint32_t st = sb + s * L::ST_BYTES;
                 const int t = (int)(tok0 + (long long)lc * C);
                 // early group: free once round A of chunk lc - 2 has run
-                if (lc >= 2 && !wait_phase(sb + L::B_EMPTY + 8 * s, ((lc >> 1) - 1) & 1, flag, geo.err)) break;
+                if (lc >= 2 && !uwait(sb + L::B_EMPTY + 8 * s, ((lc >> 1) - 1) & 1, flag, geo.err)) break;
                 const uint32_t fe = sb + L::B_FULL + 8 * s, fl = sb + L::B_FULLL + 8 * s;
-                tma::expect_tx(fe, (WRITE_O ? 16384u : 0u) + (uint32_t)BV * 128u + 8192u);
+                if (l0) tma::expect_tx(fe, (WRITE_O ? 16384u : 0u) + (uint32_t)BV * 128u + 8192u);
                 if (WRITE_O) {
-                    tma::load3d(st + L::ST_Q0, &p.tq, 0, hq, t, fe);
-                    tma::load3d(st + L::ST_Q1, &p.tq, 64, hq, t, fe);
+                    if (l0) tma::load3d(st + L::ST_Q0, &p.tq, 0, hq, t, fe);
+                    if (l0) tma::load3d(st + L::ST_Q1, &p.tq, 64, hq, t, fe);
                 }
-                tma::load3d(st + L::ST_V, &p.tv, v0, j, t, fe);
-                if (BV == 128) tma::load3d(st + L::ST_V + 8192, &p.tv, v0 + 64, j, t, fe);
-                tma::load3d(st + L::ST_A, &p.ta, 0, j, t, fe);
+                if (l0) tma::load3d(st + L::ST_V, &p.tv, v0, j, t, fe);
+                if (BV == 128 && l0) tma::load3d(st + L::ST_V + 8192, &p.tv, v0 + 64, j, t, fe);
+                if (l0) tma::load3d(st + L::ST_A, &p.ta, 0, j, t, fe);
                 ++issued[s];
                 // late group: free once round B of chunk lc - 2 has run
-                if (lc >= 2 && !wait_phase(sb + L::B_EMPTYL + 8 * s, ((lc >> 1) - 1) & 1, flag, geo.err)) break;
-                tma::expect_tx(fl, 16384u + (WRITE_O ? 8192u : 0u));
-                tma::load3d(st + L::ST_K0, &p.tk, 0, hq, t, fl);
-                tma::load3d(st + L::ST_K1, &p.tk, 64, hq, t, fl);
-                if (WRITE_O) tma::load3d(st + L::ST_P, &p.tp, 0, j, t, fl);
+                if (lc >= 2 && !uwait(sb + L::B_EMPTYL + 8 * s, ((lc >> 1) - 1) & 1, flag, geo.err)) break;
+                if (l0) tma::expect_tx(fl, 16384u + (WRITE_O ? 8192u : 0u));
+                if (l0) tma::load3d(st + L::ST_K0, &p.tk, 0, hq, t, fl);
+                if (l0) tma::load3d(st + L::ST_K1, &p.tk, 64, hq, t, fl);
+                if (WRITE_O && l0) tma::load3d(st + L::ST_P, &p.tp, 0, j, t, fl);
                 ++issued_l[s];
                 // the next chunk's boxes into L2 now: its loads wait for this stage's turn, a chunk from now
                 if (lc + 1 < nc) {
                     const int tn = t + C;
                     if (WRITE_O) {
-                        tma::prefetch3d(&p.tq, 0, hq, tn);
-                        tma::prefetch3d(&p.tq, 64, hq, tn);
-                        tma::prefetch3d(&p.tp, 0, j, tn);
+                        if (l0) tma::prefetch3d(&p.tq, 0, hq, tn);
+                        if (l0) tma::prefetch3d(&p.tq, 64, hq, tn);
+                        if (l0) tma::prefetch3d(&p.tp, 0, j, tn);
                     }
-                    tma::prefetch3d(&p.tv, v0, j, tn);
-                    if (BV == 128) tma::prefetch3d(&p.tv, v0 + 64, j, tn);
-                    tma::prefetch3d(&p.ta, 0, j, tn);
-                    tma::prefetch3d(&p.tk, 0, hq, tn);
-                    tma::prefetch3d(&p.tk, 64, hq, tn);
+                    if (l0) tma::prefetch3d(&p.tv, v0, j, tn);
+                    if (BV == 128 && l0) tma::prefetch3d(&p.tv, v0 + 64, j, tn);
+                    if (l0) tma::prefetch3d(&p.ta, 0, j, tn);
+                    if (l0) tma::prefetch3d(&p.tk, 0, hq, tn);
+                    if (l0) tma::prefetch3d(&p.tk, 64, hq, tn);
                 }
             }
             // let every load in flight land before the block can exit (bounded)
@@ -331,7 +344,8 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
         }
     } else if (warp == 0) {
         // ------------------------------------------------------------ MMA issue
-        if (lane == 0) {
+        {
+            const bool l0 = lane == 0;
             const uint32_t id_w = umma::idesc(128, 128, bf16, false, true);
             const uint32_t id_bv = umma::idesc(128, BV, bf16, false, true);   // K-major A, MN-major B
             const uint32_t id_mn = umma::idesc(128, BV, bf16, true, true);    // MN-major A and B
@@ -342,83 +356,88 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                 const uint32_t st = sb + (lc & 1) * L::ST_BYTES;
                 const uint64_t bk = umma::desc(st + L::ST_K0, L::LBO_K, 1024);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + L::T_W, dZAKG + ks * 2, bk + ks * 128, id_w, ks > 0);
+                for (int ks = 0; ks < 4; ++ks) if (l0) umma::mma(tmem + L::T_W, dZAKG + ks * 2, bk + ks * 128, id_w, ks > 0);
             };
             auto issue_u = [&](int lc) {  // U of chunk lc (also zeroes the output lanes 64..127)
                 const uint32_t st = sb + (lc & 1) * L::ST_BYTES;
                 const uint64_t bv = umma::desc(st + L::ST_V, 8192, 1024);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    umma::mma(tmem + ((lc & 1) ? L::T_D1 : L::T_D0), dABZ + ks * 2, bv + ks * 128, id_bv, ks > 0);
+                    if (l0) umma::mma(tmem + ((lc & 1) ? L::T_D1 : L::T_D0), dABZ + ks * 2, bv + ks * 128, id_bv, ks > 0);
             };
             bool ok = true;
             if (nc > 0) {
-                ok = wait_phase(sb + L::B_PREP, 0, flag, geo.err) && wait_phase(sb + L::B_FULL, 0, flag, geo.err) &&
-                     wait_phase(sb + L::B_FULLL, 0, flag, geo.err);
+                ok = uwait(sb + L::B_PREP, 0, flag, geo.err) && uwait(sb + L::B_FULL, 0, flag, geo.err) &&
+                     uwait(sb + L::B_FULLL, 0, flag, geo.err);
                 umma::fence_after();
                 if (ok) {
                     issue_w(0);
-                    umma::commit(sb + L::B_MPW);
+                    if (l0) umma::commit(sb + L::B_MPW);
                     issue_u(0);
-                    umma::commit(sb + L::B_MPU);
+                    if (l0) umma::commit(sb + L::B_MPU);
                 }
             }
             for (int lc = 0; lc < nc && ok; ++lc) {
                 const int b = lc & 1;
                 const uint32_t st = sb + b * L::ST_BYTES;
                 const uint32_t tD = b ? L::T_D1 : L::T_D0;
-                // round A: needs -W (rows above Q~) and the state tile
-                if (!(ok = wait_phase(sb + L::B_EPIW, lc & 1, flag, geo.err) &&
-                           wait_phase(sb + L::B_EPIB, lc & 1, flag, geo.err)))
+                // round A: needs -W (rows above Q) and the state tile
+                if (!(ok = uwait(sb + L::B_EPIW, lc & 1, flag, geo.err) &&
+                           uwait(sb + L::B_EPIB, lc & 1, flag, geo.err)))
                     break;
                 umma::fence_after();
                 {
                     const uint64_t aqw = umma::desc(st + L::ST_W0, 16, 1024);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        umma::mma(tmem + tD, aqw + ((((ks >> 2) * 16384) + (ks & 3) * 32) >> 4), dH + ks * 128, id_bv,
+                        if (l0) umma::mma(tmem + tD, aqw + ((((ks >> 2) * 16384) + (ks & 3) * 32) >> 4), dH + ks * 128, id_bv,
                                   true);
                 }
-                umma::commit(sb + L::B_MA);
-                mbar_arrive(sb + L::B_MA);
-                umma::commit(sb + L::B_EMPTY + 8 * b);  // q, v and A of this chunk are done
+                if (l0) umma::commit(sb + L::B_MA);
+                if (l0) mbar_arrive(sb + L::B_MA);
+                if (l0) umma::commit(sb + L::B_EMPTY + 8 * b);  // q, v and A of this chunk are done
                 // round B as soon as Delta is in shared memory; the next chunk's W group goes in whenever
                 // its inputs are ready, its U group (needed only by the next round A) after round B
                 const bool next = lc + 1 < nc;
                 bool b_done = false, w_done = !next, u_done = !next;
                 for (long it = 0; !(b_done && w_done && u_done); ++it) {
-                    if (!b_done && mbar_test(sb + L::B_EPIA, lc & 1)) {
+                    if (!b_done && utest(sb + L::B_EPIA, lc & 1)) {
                         umma::fence_after();
                         const uint64_t akt = umma::desc(st + L::ST_K0, L::LBO_K, 1024);
                         const uint64_t ap = umma::desc(st + L::ST_A, 16, 1024);
+                        // X first, with its own commit: the state epilogue waits for X alone, not for the output
+                        // product issued after it
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            umma::mma(tmem + L::T_X, akt + ks * 128, dDT + ks * 128, id_mn, ks > 0);
-                            if (WRITE_O) umma::mma(tmem + tD, ap + ks * 2, dDL + ks * 128, id_bv, true);
+                        for (int ks = 0; ks < 4; ++ks) if (l0) umma::mma(tmem + L::T_X, akt + ks * 128, dDT + ks * 128, id_mn, ks > 0);
+                        if (l0) umma::commit(sb + L::B_MB);
+                        if (WRITE_O) {
+                            // P Delta into its own columns: the output epilogue scales the Q h rows alone
+                            const uint32_t tPD = b ? L::T_PD1 : L::T_PD0;
+#pragma unroll
+                            for (int ks = 0; ks < 4; ++ks) if (l0) umma::mma(tmem + tPD, ap + ks * 2, dDL + ks * 128, id_bv, ks > 0);
                         }
-                        umma::commit(sb + L::B_MB);
-                        umma::commit(sb + L::B_EMPTYL + 8 * b);  // k and P are done
-                        umma::commit(sb + L::B_MO + 8 * b);
+                        if (l0) umma::commit(sb + L::B_EMPTYL + 8 * b);  // k and P are done
+                        if (l0) umma::commit(sb + L::B_MO + 8 * b);
                         b_done = true;
                         continue;
                     }
-                    if (!w_done && mbar_test(sb + L::B_PREP, (lc + 1) & 1) &&
-                        mbar_test(sb + L::B_FULLL + 8 * (b ^ 1), ((lc + 1) >> 1) & 1)) {
+                    if (!w_done && utest(sb + L::B_PREP, (lc + 1) & 1) &&
+                        utest(sb + L::B_FULLL + 8 * (b ^ 1), ((lc + 1) >> 1) & 1)) {
                         umma::fence_after();
                         issue_w(lc + 1);
-                        umma::commit(sb + L::B_MPW);
+                        if (l0) umma::commit(sb + L::B_MPW);
                         w_done = true;
                         continue;
                     }
                     if (!u_done && w_done && b_done &&
-                        (!WRITE_O || lc < 1 || mbar_test(sb + L::B_OFREE + 8 * (b ^ 1), ((lc - 1) >> 1) & 1))) {
+                        (!WRITE_O || lc < 1 || utest(sb + L::B_OFREE + 8 * (b ^ 1), ((lc - 1) >> 1) & 1))) {
                         umma::fence_after();
                         issue_u(lc + 1);
-                        umma::commit(sb + L::B_MPU);
+                        if (l0) umma::commit(sb + L::B_MPU);
                         u_done = true;
                         continue;
                     }
-                    if ((it & 127) == 127 && *flag) {
+                    if ((it & 127) == 127 && uflag(flag)) {
                         ok = false;
                         break;
                     }
@@ -431,7 +450,7 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                 }
             }
             // every MMA issued so far completes before TMEM is released
-            umma::commit(sb + L::B_DONE);
+            if (l0) umma::commit(sb + L::B_DONE);
             umma::mbar_wait(sb + L::B_DONE, 0, 4000000L);
         }
     } else if (warp >= 12) {
@@ -522,26 +541,6 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                     const uint32_t o = umma::off(r, c0 + c * 8, 0);
                     st_v4(sb + L::AKG + o, wk[4 * c], wk[4 * c + 1], wk[4 * c + 2], wk[4 * c + 3]);
                     st_v4(sb + L::AB + o, wb[4 * c], wb[4 * c + 1], wb[4 * c + 2], wb[4 * c + 3]);
-                }
-            }
-            if (WRITE_O) {
-                // Q~ = diag(scale rq e^G) Q in place: thread -> row at & 63, key half at >> 6
-                const int r = at & 63;
-                const float cq = fa(lc, FCQ)[r];
-                const uint32_t blk = st + ((at >> 6) ? L::ST_Q1 : L::ST_Q0);
-                uint4 u[8];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) u[c] = umma::ld_shared_v4(blk + umma::off(r, c * 8, 0));
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
-                    uint32_t o4[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 x = Elt<T>::unpack(w[e]);
-                        o4[e] = Elt<T>::pack(x.x * cq, x.y * cq);
-                    }
-                    st_v4(blk + umma::off(r, c * 8, 0), o4[0], o4[1], o4[2], o4[3]);
                 }
             }
             umma::fence_async_smem();
@@ -695,7 +694,8 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
             const int valid = min(C, len - lc * C);
             if (!warp_wait(sb + L::B_MO + 8 * b, (lc >> 1) & 1, flag, geo.err, lane)) return false;
             umma::fence_after();
-            const uint32_t tD = b ? L::T_D1 : L::T_D0;
+            const uint32_t tD = b ? L::T_D1 : L::T_D0, tPD = b ? L::T_PD1 : L::T_PD0;
+            const float cq = fa(lc, FCQ)[r];  // scale rq e^G of this row (0 past the end)
             T *orow = static_cast<T *>(p.o) + ((tok0 + (long long)lc * C + r) * Hv + j) * DV + v0;
             // a full chunk's rows leave through the staging tile, this warp's 32 rows as one TMA box (scattered
             // row stores would crowd the memory instruction queue of the schedulers the state warps share);
@@ -708,9 +708,12 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
             }
 #pragma unroll
             for (int c = 0; c < BV; c += 16) {
-                float x[16];
+                float x[16], y[16];
                 umma::ld16(umma::taddr(tmem, lb, tD + c), x);
+                umma::ld16(umma::taddr(tmem, lb, tPD + c), y);
                 umma::ld_wait();  // (one 16-column slice at a time keeps the warp's registers low)
+#pragma unroll
+                for (int u = 0; u < 16; ++u) x[u] = fmaf(cq, x[u], y[u]);  // o = diag(scale rq e^G) Q h + P Delta
                 const uint32_t w0 = Elt<T>::pack(x[0], x[1]), w1 = Elt<T>::pack(x[2], x[3]),
                                w2 = Elt<T>::pack(x[4], x[5]), w3 = Elt<T>::pack(x[6], x[7]),
                                w4 = Elt<T>::pack(x[8], x[9]), w5 = Elt<T>::pack(x[10], x[11]),
@@ -743,7 +746,7 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
             if (!warp_wait(sb + L::B_MPW, lc & 1, flag, geo.err, lane)) break;
             umma::fence_after();
             {
-                // -W row r (128 key columns) into the rows above Q~ of this chunk's stage
+                // -W row r (128 key columns) into the rows above Q of this chunk's stage
                 const uint32_t st = sb + (lc & 1) * L::ST_BYTES;
 #pragma unroll
                 for (int c = 0; c < 128; c += 64) {
@@ -874,34 +877,35 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
 
     if (warp == 1) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        {
+            const bool l0 = lane == 0;
             int issued[2] = {0, 0};
-            for (int lc = 0; lc < nc && !*flag; ++lc) {
+            for (int lc = 0; lc < nc && !uflag(flag); ++lc) {
                 const int s = lc & 1;
-                if (lc >= 2 && !wait_phase(sb + L::B_EMPTY + 8 * s, ((lc >> 1) - 1) & 1, flag, geo.err)) break;
+                if (lc >= 2 && !uwait(sb + L::B_EMPTY + 8 * s, ((lc >> 1) - 1) & 1, flag, geo.err)) break;
                 const uint32_t st = sb + s * L::ST_BYTES, full = sb + L::B_FULL + 8 * s;
                 const int t = (int)(tok0 + (long long)chunk_of(lc) * C);
-                tma::expect_tx(full, 49152u + (uint32_t)BV * 128u);
-                tma::load3d(st + L::ST_Q0, &p.tq, 0, hq, t, full);
-                tma::load3d(st + L::ST_Q0 + 8192, &p.tq, 64, hq, t, full);
-                tma::load3d(st + L::ST_K0, &p.tk, 0, hq, t, full);
-                tma::load3d(st + L::ST_K0 + 8192, &p.tk, 64, hq, t, full);
-                tma::load3d(st + L::ST_DO, &p.tdo, v0, j, t, full);
-                if (BV == 128) tma::load3d(st + L::ST_DO + 8192, &p.tdo, v0 + 64, j, t, full);
-                tma::load3d(st + L::ST_A, &p.ta, 0, j, t, full);
-                tma::load3d(st + L::ST_P, &p.tp, 0, j, t, full);
+                if (l0) tma::expect_tx(full, 49152u + (uint32_t)BV * 128u);
+                if (l0) tma::load3d(st + L::ST_Q0, &p.tq, 0, hq, t, full);
+                if (l0) tma::load3d(st + L::ST_Q0 + 8192, &p.tq, 64, hq, t, full);
+                if (l0) tma::load3d(st + L::ST_K0, &p.tk, 0, hq, t, full);
+                if (l0) tma::load3d(st + L::ST_K0 + 8192, &p.tk, 64, hq, t, full);
+                if (l0) tma::load3d(st + L::ST_DO, &p.tdo, v0, j, t, full);
+                if (BV == 128 && l0) tma::load3d(st + L::ST_DO + 8192, &p.tdo, v0 + 64, j, t, full);
+                if (l0) tma::load3d(st + L::ST_A, &p.ta, 0, j, t, full);
+                if (l0) tma::load3d(st + L::ST_P, &p.tp, 0, j, t, full);
                 ++issued[s];
                 // the next chunk's boxes into L2 now: its loads wait for this stage's turn, a chunk from now
                 if (lc + 1 < nc) {
                     const int tn = (int)(tok0 + (long long)chunk_of(lc + 1) * C);
-                    tma::prefetch3d(&p.tq, 0, hq, tn);
-                    tma::prefetch3d(&p.tq, 64, hq, tn);
-                    tma::prefetch3d(&p.tk, 0, hq, tn);
-                    tma::prefetch3d(&p.tk, 64, hq, tn);
-                    tma::prefetch3d(&p.tdo, v0, j, tn);
-                    if (BV == 128) tma::prefetch3d(&p.tdo, v0 + 64, j, tn);
-                    tma::prefetch3d(&p.ta, 0, j, tn);
-                    tma::prefetch3d(&p.tp, 0, j, tn);
+                    if (l0) tma::prefetch3d(&p.tq, 0, hq, tn);
+                    if (l0) tma::prefetch3d(&p.tq, 64, hq, tn);
+                    if (l0) tma::prefetch3d(&p.tk, 0, hq, tn);
+                    if (l0) tma::prefetch3d(&p.tk, 64, hq, tn);
+                    if (l0) tma::prefetch3d(&p.tdo, v0, j, tn);
+                    if (BV == 128 && l0) tma::prefetch3d(&p.tdo, v0 + 64, j, tn);
+                    if (l0) tma::prefetch3d(&p.ta, 0, j, tn);
+                    if (l0) tma::prefetch3d(&p.tp, 0, j, tn);
                 }
             }
             for (int s = 0; s < 2; ++s)
@@ -909,7 +913,8 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
         }
     } else if (warp == 0) {
         // ------------------------------------------------------------ MMA issue
-        if (lane == 0) {
+        {
+            const bool l0 = lane == 0;
             const uint32_t id_kmn = umma::idesc(128, 128, bf16, false, true);  // K-major A, MN-major B (W)
             const uint32_t id_kbv = umma::idesc(128, BV, bf16, false, true);   // the same, N = BV
             const uint32_t id_mn = umma::idesc(128, BV, bf16, true, true);     // MN-major A and B, N = BV
@@ -920,14 +925,14 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
                 const uint64_t ap = umma::desc(st + L::ST_P, 8192, 1024), bdo = umma::desc(st + L::ST_DO, 8192, 1024);
                 const uint64_t bk = umma::desc(st + L::ST_K0, 8192, 1024);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + L::T_P, ap + ks * 128, bdo + ks * 128, id_mn, ks > 0);
+                for (int ks = 0; ks < 4; ++ks) if (l0) umma::mma(tmem + L::T_P, ap + ks * 128, bdo + ks * 128, id_mn, ks > 0);
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + L::T_W, dZAKG + ks * 2, bk + ks * 128, id_kmn, ks > 0);
-                umma::commit(sb + L::B_MPW);
+                for (int ks = 0; ks < 4; ++ks) if (l0) umma::mma(tmem + L::T_W, dZAKG + ks * 2, bk + ks * 128, id_kmn, ks > 0);
+                if (l0) umma::commit(sb + L::B_MPW);
             };
             bool ok = true;
             if (nc > 0) {
-                ok = wait_phase(sb + L::B_PREP, 0, flag, geo.err) && wait_phase(sb + L::B_FULL, 0, flag, geo.err);
+                ok = uwait(sb + L::B_PREP, 0, flag, geo.err) && uwait(sb + L::B_FULL, 0, flag, geo.err);
                 umma::fence_after();
                 if (ok) issue_pw(0);
             }
@@ -935,41 +940,41 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
                 const int b = lc & 1;
                 const uint32_t st = sb + b * L::ST_BYTES;
                 // round A on the state tile
-                if (!(ok = wait_phase(sb + L::B_EPIB, lc & 1, flag, geo.err))) break;
+                if (!(ok = uwait(sb + L::B_EPIB, lc & 1, flag, geo.err))) break;
                 umma::fence_after();
                 {
                     const uint64_t ak = umma::desc(st + L::ST_K0, 16, 1024);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)
-                        umma::mma(tmem + L::T_E, ak + ((((ks >> 2) * 8192) + (ks & 3) * 32) >> 4), dH + ks * 128, id_kbv,
+                        if (l0) umma::mma(tmem + L::T_E, ak + ((((ks >> 2) * 8192) + (ks & 3) * 32) >> 4), dH + ks * 128, id_kbv,
                                   ks > 0);
                 }
-                umma::commit(sb + L::B_MA);
-                mbar_arrive(sb + L::B_MA);
+                if (l0) umma::commit(sb + L::B_MA);
+                if (l0) mbar_arrive(sb + L::B_MA);
                 // Q~^T dO, the base that round B adds to
                 {
                     const uint64_t aq = umma::desc(st + L::ST_Q0, 8192, 1024), bdo = umma::desc(st + L::ST_DO, 8192, 1024);
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + L::T_Y, aq + ks * 128, bdo + ks * 128, id_mn, ks > 0);
+                    for (int ks = 0; ks < 4; ++ks) if (l0) umma::mma(tmem + L::T_Y, aq + ks * 128, bdo + ks * 128, id_mn, ks > 0);
                 }
                 // round B: needs dDelta and -W
-                if (!(ok = wait_phase(sb + L::B_EPIA, lc & 1, flag, geo.err) &&
-                           wait_phase(sb + L::B_EPIW, lc & 1, flag, geo.err)))
+                if (!(ok = uwait(sb + L::B_EPIA, lc & 1, flag, geo.err) &&
+                           uwait(sb + L::B_EPIW, lc & 1, flag, geo.err)))
                     break;
                 umma::fence_after();
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + L::T_Y, dWS + ks * 128, dDL + ks * 128, id_mn, true);
-                umma::commit(sb + L::B_MB);
-                umma::commit(sb + L::B_EMPTY + 8 * b);
+                for (int ks = 0; ks < 4; ++ks) if (l0) umma::mma(tmem + L::T_Y, dWS + ks * 128, dDL + ks * 128, id_mn, true);
+                if (l0) umma::commit(sb + L::B_MB);
+                if (l0) umma::commit(sb + L::B_EMPTY + 8 * b);
                 if (lc + 1 < nc) {
-                    if (!(ok = wait_phase(sb + L::B_PREP, (lc + 1) & 1, flag, geo.err) &&
-                               wait_phase(sb + L::B_FULL + 8 * (b ^ 1), ((lc + 1) >> 1) & 1, flag, geo.err)))
+                    if (!(ok = uwait(sb + L::B_PREP, (lc + 1) & 1, flag, geo.err) &&
+                               uwait(sb + L::B_FULL + 8 * (b ^ 1), ((lc + 1) >> 1) & 1, flag, geo.err)))
                         break;
                     umma::fence_after();
                     issue_pw(lc + 1);
                 }
             }
-            umma::commit(sb + L::B_DONE);
+            if (l0) umma::commit(sb + L::B_DONE);
             umma::mbar_wait(sb + L::B_DONE, 0, 4000000L);
         }
     } else if (warp >= 12) {
@@ -1052,6 +1057,11 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
                     st_v4(sb + L::AKG + umma::off(r, c0 + c * 8, 0), wk[0], wk[1], wk[2], wk[3]);
                 }
             }
+            if (valid < C && at >= valid && at < C) {
+                // P rows past the end of the sequence belong to other tokens: zero them (P^T dO sums rows)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) st_v4(st + L::ST_P + umma::off(at, c * 8, 0), 0u, 0u, 0u, 0u);
+            }
             {
                 // Q~ = diag(scale rq e^G) Q in place: thread -> row at & 63, key half at >> 6
                 const int r = at & 63;
@@ -1071,11 +1081,6 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
                     }
                     st_v4(blk + umma::off(r, c * 8, 0), o4[0], o4[1], o4[2], o4[3]);
                 }
-            }
-            if (valid < C && at >= valid && at < C) {
-                // P rows past the end of the sequence belong to other tokens: zero them (P^T dO sums rows)
-#pragma unroll
-                for (int c = 0; c < 8; ++c) st_v4(st + L::ST_P + umma::off(at, c * 8, 0), 0u, 0u, 0u, 0u);
             }
             umma::fence_async_smem();
             __syncwarp();
