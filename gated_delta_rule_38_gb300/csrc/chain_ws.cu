@@ -811,7 +811,11 @@ struct RLay {
     static constexpr uint32_t B_FULL = BAR, B_EMPTY = BAR + 16, B_PREP = BAR + 32, B_EPIW = BAR + 40,
                               B_MPW = BAR + 48, B_MA = BAR + 56, B_EPIA = BAR + 64, B_MB = BAR + 72,
                               B_EPIB = BAR + 80, B_DONE = BAR + 88;
-    static constexpr uint32_t SLOT = BAR + 96, FLAG = SLOT + 4, USED = FLAG + 12;
+    // the preparation is released in two steps: B_PREP (A diag(beta e^G rk) and P's rows past the end: P^T dO
+    // and W may go) and B_PREPQ + 8 (c & 1) (Q~ of chunk step c in place: Q~^T dO may go).  B_PREPQ is a ring of
+    // two so that the preparation, which runs ahead, can never complete a phase its waiter has not yet seen.
+    static constexpr uint32_t B_PREPQ = BAR + 96;
+    static constexpr uint32_t SLOT = BAR + 112, FLAG = SLOT + 4, USED = FLAG + 12;
     static constexpr uint32_t BYTES = USED + 1024;
     static constexpr uint32_t T_W = 0, T_E = 128, T_P = 256, T_Y = 384;
 };
@@ -857,6 +861,8 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
         umma::mbar_init(sb + L::B_EMPTY, 1);
         umma::mbar_init(sb + L::B_EMPTY + 8, 1);
         umma::mbar_init(sb + L::B_PREP, 4);
+        umma::mbar_init(sb + L::B_PREPQ, 4);
+        umma::mbar_init(sb + L::B_PREPQ + 8, 4);
         umma::mbar_init(sb + L::B_EPIW, 2);
         umma::mbar_init(sb + L::B_MPW, 1);
         umma::mbar_init(sb + L::B_MA, 2);  // the commit, and the issuing thread's own arrival
@@ -951,7 +957,9 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
                 }
                 if (l0) umma::commit(sb + L::B_MA);
                 if (l0) mbar_arrive(sb + L::B_MA);
-                // Q~^T dO, the base that round B adds to
+                // Q~^T dO, the base that round B adds to (Q~ of this chunk step in place)
+                if (!(ok = uwait(sb + L::B_PREPQ + 8 * b, (lc >> 1) & 1, flag, geo.err))) break;
+                umma::fence_after();
                 {
                     const uint64_t aq = umma::desc(st + L::ST_Q0, 8192, 1024), bdo = umma::desc(st + L::ST_DO, 8192, 1024);
 #pragma unroll
@@ -1062,6 +1070,9 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
 #pragma unroll
                 for (int c = 0; c < 8; ++c) st_v4(st + L::ST_P + umma::off(at, c * 8, 0), 0u, 0u, 0u, 0u);
             }
+            umma::fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sb + L::B_PREP);  // P^T dO and W need only these
             {
                 // Q~ = diag(scale rq e^G) Q in place: thread -> row at & 63, key half at >> 6
                 const int r = at & 63;
@@ -1084,7 +1095,7 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
             }
             umma::fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(sb + L::B_PREP);
+            if (lane == 0) mbar_arrive(sb + L::B_PREPQ + 8 * (lc & 1));
         }
     } else if (warp >= 4) {
         // ------------------------------------------------------------ state gradient (256 threads)
