@@ -135,13 +135,11 @@ __device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile 
     return false;
 }
 
-// Warp-uniform wait: lane 0 polls, the warp agrees on the outcome and synchronises its memory view.
+// Warp-uniform wait: every lane polls and the warp agrees on the outcome.  (Lane 0 polling alone while
+// the other lanes waited in a shuffle passed the phases markedly later: the forward chain ran 19 us slower.)
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *flag, unsigned *err, int lane) {
-    int ok = 0;
-    if (lane == 0) ok = wait_phase(bar, parity, flag, err) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
+    (void)lane;
+    return __all_sync(0xffffffffu, wait_phase(bar, parity, flag, err));
 }
 
 // Named-barrier arrival without waiting, and arrival with waiting, over `nthreads` threads.
@@ -196,8 +194,8 @@ struct BoxStore {
 };
 
 // Warp-uniform waits for the roles whose work one lane issues (TMA producer, MMA issuer): the whole warp
-// runs the role's loop and lane 0 alone issues, so no lane of the warp sits at the block's final barrier
-// while lane 0 works.
+// runs the role's loop and polls, and lane 0 alone issues, so no lane of the warp sits at a barrier or a
+// shuffle while lane 0 works (a lane working alone in a diverged warp was seen to make slow progress).
 __device__ __forceinline__ bool uwait(uint32_t bar, uint32_t parity, volatile int *flag, unsigned *err) {
     return __all_sync(0xffffffffu, wait_phase(bar, parity, flag, err));
 }
