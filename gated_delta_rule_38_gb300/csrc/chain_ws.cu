@@ -72,7 +72,7 @@ struct Lay {
     static constexpr uint32_t OST = F + 4 * NF * 256;             // output rows of a full chunk [64][BV]
     static constexpr uint32_t BAR = OST + (WRITE_O ? BV * 128 : 0);
     // barriers
-    static constexpr uint32_t B_FULL = BAR, B_EMPTY = BAR + 16, B_PREP = BAR + 32, B_EPIW = BAR + 40,
+    static constexpr uint32_t B_FULL = BAR, B_EMPTY = BAR + 16, B_PREP = BAR + 32,
                               B_MPW = BAR + 48, B_MA = BAR + 56, B_EPIA = BAR + 64, B_MB = BAR + 72,
                               B_EPIB = BAR + 80, B_MO = BAR + 88, B_OFREE = BAR + 104, B_DONE = BAR + 120,
                               B_MPU = BAR + 128;
@@ -267,13 +267,12 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
         umma::mbar_init(sb + L::B_EMPTYL, 1);
         umma::mbar_init(sb + L::B_EMPTYL + 8, 1);
         umma::mbar_init(sb + L::B_PREP, 4);
-        umma::mbar_init(sb + L::B_EPIW, 2);
         umma::mbar_init(sb + L::B_MPW, 1);
         umma::mbar_init(sb + L::B_MPU, 1);
         umma::mbar_init(sb + L::B_MA, 2);
         umma::mbar_init(sb + L::B_EPIA, 4);
         umma::mbar_init(sb + L::B_MB, 1);
-        umma::mbar_init(sb + L::B_EPIB, 8);
+        umma::mbar_init(sb + L::B_EPIB, 10);  // the 8 state warps and the 2 -W warps: round A's operands
         umma::mbar_init(sb + L::B_MO, 1);
         umma::mbar_init(sb + L::B_MO + 8, 1);
         umma::mbar_init(sb + L::B_OFREE, 2);
@@ -379,9 +378,8 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                 const int b = lc & 1;
                 const uint32_t st = sb + b * L::ST_BYTES;
                 const uint32_t tD = b ? L::T_D1 : L::T_D0;
-                // round A: needs -W (rows above Q) and the state tile
-                if (!(ok = uwait(sb + L::B_EPIW, lc & 1, flag, geo.err) &&
-                           uwait(sb + L::B_EPIB, lc & 1, flag, geo.err)))
+                // round A: needs -W (rows above Q) and the state tile, both announced on B_EPIB (one barrier to pass)
+                if (!(ok = uwait(sb + L::B_EPIB, lc & 1, flag, geo.err)))
                     break;
                 umma::fence_after();
                 {
@@ -762,7 +760,7 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
             umma::fence_before();
             umma::fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(sb + L::B_EPIW);
+            if (lane == 0) mbar_arrive(sb + L::B_EPIB);  // (-W of this chunk: the other half of round A's inputs)
             if (WRITE_O && lc > 0) ok = out_rows(lc - 1);
         }
         if (WRITE_O && ok && nc > 0) out_rows(nc - 1);
@@ -806,7 +804,7 @@ struct RLay {
     static constexpr uint32_t H = DL + 16384;     // dh' [128 d][128]: two 16 KB blocks
     static constexpr uint32_t F = H + 32768;
     static constexpr uint32_t BAR = F + 4 * NF * 256;
-    static constexpr uint32_t B_FULL = BAR, B_EMPTY = BAR + 16, B_PREP = BAR + 32, B_EPIW = BAR + 40,
+    static constexpr uint32_t B_FULL = BAR, B_EMPTY = BAR + 16, B_PREP = BAR + 32,
                               B_MPW = BAR + 48, B_MA = BAR + 56, B_EPIA = BAR + 64, B_MB = BAR + 72,
                               B_EPIB = BAR + 80, B_DONE = BAR + 88;
     // the preparation is released in two steps: B_PREP (A diag(beta e^G rk) and P's rows past the end: P^T dO
@@ -861,10 +859,9 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
         umma::mbar_init(sb + L::B_PREP, 4);
         umma::mbar_init(sb + L::B_PREPQ, 4);
         umma::mbar_init(sb + L::B_PREPQ + 8, 4);
-        umma::mbar_init(sb + L::B_EPIW, 2);
         umma::mbar_init(sb + L::B_MPW, 1);
         umma::mbar_init(sb + L::B_MA, 2);  // the commit, and the issuing thread's own arrival
-        umma::mbar_init(sb + L::B_EPIA, 4);
+        umma::mbar_init(sb + L::B_EPIA, 6);  // the 4 dDelta-row warps and the 2 -W warps: round B's operands
         umma::mbar_init(sb + L::B_MB, 1);
         umma::mbar_init(sb + L::B_EPIB, 8);
         umma::mbar_init(sb + L::B_DONE, 1);
@@ -963,9 +960,8 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) if (l0) umma::mma(tmem + L::T_Y, aq + ks * 128, bdo + ks * 128, id_mn, ks > 0);
                 }
-                // round B: needs dDelta and -W
-                if (!(ok = uwait(sb + L::B_EPIA, lc & 1, flag, geo.err) &&
-                           uwait(sb + L::B_EPIW, lc & 1, flag, geo.err)))
+                // round B: needs dDelta and -W, both announced on B_EPIA (one barrier to pass)
+                if (!(ok = uwait(sb + L::B_EPIA, lc & 1, flag, geo.err)))
                     break;
                 umma::fence_after();
 #pragma unroll
@@ -1216,7 +1212,7 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
             umma::fence_before();
             umma::fence_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(sb + L::B_EPIW);
+            if (lane == 0) mbar_arrive(sb + L::B_EPIA);
         }
     }
 
