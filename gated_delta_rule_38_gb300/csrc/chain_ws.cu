@@ -24,12 +24,13 @@
 // WY/UT representation, PR #998 "[GDN] Add FlashQLA backend dispatch").
 //
 // Warp roles (one CTA per SM):
-//   warp 0            lane 0 issues every MMA (single thread; the next chunk's products are issued in
+//   warp 0            lane 0 issues every MMA but round B's X (the next chunk's products are issued in
 //                     small groups around round B so that round B never waits behind them)
 //   warp 1            lane 0 issues the TMA tile loads into a two-stage ring
 //   warps 2,3         TMEM lanes 64..127: the -W epilogue and the output rows
 //   warps 4..11       the state: TMEM lane 32*(w%4)+l, value columns of half (w-4)/4 of the slice;
-//                     warps 4,5,8,9 also move Delta (lanes 0..63) into shared memory
+//                     warps 4,5,8,9 also move Delta (lanes 0..63) into shared memory, and warp 4 then issues
+//                     round B's X product
 //   warps 12..15      per-chunk preparation (one warp per scheduler): gate factors, scaled copies of A
 // Hand-offs go through mbarriers whose phases each complete once per chunk; every wait is
 // bounded and gives up early once another role has raised the block's error flag.
@@ -264,8 +265,9 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
         umma::mbar_init(sb + L::B_EMPTY + 8, 1);
         umma::mbar_init(sb + L::B_FULLL, 1);
         umma::mbar_init(sb + L::B_FULLL + 8, 1);
-        umma::mbar_init(sb + L::B_EMPTYL, 1);
-        umma::mbar_init(sb + L::B_EMPTYL + 8, 1);
+        // (k and P: released by the MMA warp after the output product and by warp 4 after X)
+        umma::mbar_init(sb + L::B_EMPTYL, 2);
+        umma::mbar_init(sb + L::B_EMPTYL + 8, 2);
         umma::mbar_init(sb + L::B_PREP, 4);
         umma::mbar_init(sb + L::B_MPW, 1);
         umma::mbar_init(sb + L::B_MPU, 1);
@@ -348,7 +350,7 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
             const uint32_t id_mn = umma::idesc(128, BV, bf16, true, true);    // MN-major A and B
             const uint64_t dZAKG = umma::desc(sb + L::Z, 16, 1024), dABZ = umma::desc(sb + L::AB, 16, 1024);
             const uint64_t dH = umma::desc(sb + L::H, 16384, 1024);
-            const uint64_t dDL = umma::desc(sb + L::DL, 8192, 1024), dDT = umma::desc(sb + L::DT, 8192, 1024);
+            const uint64_t dDL = umma::desc(sb + L::DL, 8192, 1024);
             auto issue_w = [&](int lc) {  // W of chunk lc
                 const uint32_t st = sb + (lc & 1) * L::ST_BYTES;
                 const uint64_t bk = umma::desc(st + L::ST_K0, L::LBO_K, 1024);
@@ -398,14 +400,9 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                 bool b_done = false, w_done = !next, u_done = !next;
                 for (long it = 0; !(b_done && w_done && u_done); ++it) {
                     if (!b_done && utest(sb + L::B_EPIA, lc & 1)) {
+                        // round B's output product (its X product is issued by the Delta-row warps themselves)
                         umma::fence_after();
-                        const uint64_t akt = umma::desc(st + L::ST_K0, L::LBO_K, 1024);
                         const uint64_t ap = umma::desc(st + L::ST_A, 16, 1024);
-                        // X first, with its own commit: the state epilogue waits for X alone, not for the output
-                        // product issued after it
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) if (l0) umma::mma(tmem + L::T_X, akt + ks * 128, dDT + ks * 128, id_mn, ks > 0);
-                        if (l0) umma::commit(sb + L::B_MB);
                         if (WRITE_O) {
                             // P Delta into its own columns: the output epilogue scales the Q h rows alone
                             const uint32_t tPD = b ? L::T_PD1 : L::T_PD0;
@@ -649,6 +646,24 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                 umma::fence_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(sb + L::B_EPIA);
+                // round B's X = K^T (diag(ck) Delta) goes in from here, not from the MMA warp: the four Delta-row
+                // warps meet at a hardware barrier and warp 4 issues it, which spares the state's critical path
+                // the MMA warp's late view of B_EPIA
+                asm volatile("bar.sync 3, 128;\n" ::: "memory");
+                if (warp == 4) {
+                    if (lane == 0) {
+                        umma::fence_after();
+                        const uint32_t stx = sb + (lc & 1) * L::ST_BYTES;
+                        const uint64_t akt = umma::desc(stx + L::ST_K0, L::LBO_K, 1024);
+                        const uint64_t dDTx = umma::desc(sb + L::DT, 8192, 1024);
+                        const uint32_t idx = umma::idesc(128, BV, IsBf16<T>::value, true, true);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) umma::mma(tmem + L::T_X, akt + ks * 128, dDTx + ks * 128, idx, ks > 0);
+                        umma::commit(sb + L::B_MB);
+                        umma::commit(sb + L::B_EMPTYL + 8 * (lc & 1));
+                    }
+                    __syncwarp();
+                }
                 if (p.tma_delta)
                     box.store(&p.tdl, v0 + bx, q4 * 32, (row0 + lc) * Hv + j, sb + L::DL + (bx >> 6) * 8192 + q4 * 4096);
             }
