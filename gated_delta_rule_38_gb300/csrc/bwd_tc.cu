@@ -157,6 +157,8 @@ __device__ __forceinline__ void row_norms64(uint32_t base, int warp, int lane, f
 
 template <typename T>
 __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __grid_constant__ BcP p) {
+    griddep_launch_next();
+    griddep_wait();
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -868,8 +870,7 @@ cudaError_t bwd_chunk_tc_t(const Args &a, const BcP &p, cudaStream_t s) {
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const long items = (long)a.max_chunks * a.Hq;
     const unsigned grid = (unsigned)(items < sms ? items : sms);  // one persistent CTA per SM
-    kern<<<grid, NT, S_BYTES, s>>>(make_geo(a), p);
-    return cudaGetLastError();
+    return launch_overlapped(kern, dim3(grid), dim3(NT), S_BYTES, s, make_geo(a), p);
 }
 
 }  // namespace

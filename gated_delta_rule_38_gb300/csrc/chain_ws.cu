@@ -789,6 +789,8 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
 
 template <typename T, int BV, bool WRITE_O>
 __global__ void __launch_bounds__(WS_NT, 1) chain_ws_kernel(Geo geo, const __grid_constant__ WsP p) {
+    griddep_launch_next();
+    griddep_wait();
     ws_fwd_body<T, BV, WRITE_O>(geo, p, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
@@ -1238,6 +1240,8 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
 
 template <typename T, int BV>
 __global__ void __launch_bounds__(WS_NT, 1) chain_rev_kernel(Geo geo, const __grid_constant__ RevP p) {
+    griddep_launch_next();
+    griddep_wait();
     ws_rev_body<T, BV>(geo, p, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
@@ -1270,8 +1274,7 @@ cudaError_t chain_rev_t(const Args &a, const RevP &p, cudaStream_t s) {
     auto kern = chain_rev_kernel<T, BV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, RLay::BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(DV / BV, a.Hv, a.N), WS_NT, RLay::BYTES, s>>>(make_geo(a), p);
-    return cudaGetLastError();
+    return launch_overlapped(kern, dim3(DV / BV, a.Hv, a.N), dim3(WS_NT), RLay::BYTES, s, make_geo(a), p);
 }
 
 template <typename T, int BV, bool WRITE_O>
@@ -1280,8 +1283,7 @@ cudaError_t chain_ws_t(const Args &a, const WsP &p, cudaStream_t s) {
     const uint32_t bytes = Lay<BV, WRITE_O>::BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(DV / BV, a.Hv, a.N), WS_NT, bytes, s>>>(make_geo(a), p);
-    return cudaGetLastError();
+    return launch_overlapped(kern, dim3(DV / BV, a.Hv, a.N), dim3(WS_NT), bytes, s, make_geo(a), p);
 }
 
 template <typename T>

@@ -49,6 +49,13 @@ template <> struct Elt<__half> {
     }
 };
 
+// Programmatic dependent launch (kernels launched by launch_overlapped): the next kernel in the stream may
+// start launching once every block of this one has called griddep_launch_next; griddep_wait returns once
+// the previous kernel has completed and its memory is visible, so it precedes every global memory access.
+// Outside such a launch both are no-ops.
+__device__ __forceinline__ void griddep_launch_next() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 // Gate-like per-token scalar (g, beta): the element type or fp32.
 template <typename T>
 __device__ __forceinline__ float load_gate(const void *p, long long i, bool f32) {

@@ -63,6 +63,8 @@ struct WyArgs {
 
 template <typename T>
 __global__ void __launch_bounds__(128, 4) wy_fwd_kernel(Geo geo, const WyArgs w) {
+    griddep_launch_next();
+    griddep_wait();
     extern __shared__ __align__(1024) unsigned char smem[];
     T *sk = reinterpret_cast<T *>(smem);
     T *sq = reinterpret_cast<T *>(smem + C * DK * 2);
@@ -359,8 +361,7 @@ static cudaError_t wy_fwd_t(const Args &a, const WyArgs &w, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, WY_SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)a.max_chunks, a.Hv);
-    kern<<<grid, 128, WY_SMEM, s>>>(make_geo(a), w);
-    return cudaGetLastError();
+    return launch_overlapped(kern, grid, dim3(128), WY_SMEM, s, make_geo(a), w);
 }
 
 cudaError_t launch_wy_fwd(const Args &a, const void *q, const void *k, const void *g, const void *beta, float *g_cs,

@@ -31,6 +31,25 @@ struct SegWs {
     float *start, *end0, *end1;
 };
 
+// Launch with programmatic stream serialisation: the kernel may begin launching while the previous kernel in
+// the stream finishes (its blocks then wait in griddep_wait, before any global memory access, until that
+// kernel is complete), which hides the launch gap between the step's kernels.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 cudaError_t launch_prep_chunks(const int32_t *cu, int N, int T, int chunk, int32_t *idx, int64_t max_chunks,
                                int32_t *off, int32_t *total, unsigned *err, cudaStream_t s);
 
