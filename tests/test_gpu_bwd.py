@@ -140,3 +140,25 @@ def test_autograd_function():
 def test_full_size_sampled_heads(name, heads, saved):
     w = WORKLOADS[name]
     check_bwd(w, kernel_l2=not w.host_l2, heads=heads, saved=saved)
+
+
+def test_back_to_back_steps_bit_identical():
+    """Forward + backward steps issued back to back on one stream, with no host synchronisation between
+    them (each kernel may begin launching while its predecessor finishes), give bit-identical results:
+    every kernel waits for its predecessor's results before touching global memory."""
+    import gated_delta_rule_38_gb300 as gdr
+    w = custom(B=2, T=300, Hq=2, Hv=2, host_l2=False)
+    d = to_dev(make_inputs(w))
+    runs = []
+    for _ in range(3):
+        sv = gdr.saved_buffer(d["q"], d["v"], d["g"], use_qk_l2norm_in_kernel=True)
+        gcs, A, o, _, fin = gdr.chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                                           initial_state=d["h0"], use_qk_l2norm_in_kernel=True,
+                                                           saved=sv)
+        grads = gdr.chunk_gated_delta_rule_bwd(d["q"], d["k"], d["v"], gcs, d["beta"], A, d["do"], dht=d["dht"],
+                                               initial_state=d["h0"], use_qk_l2norm_in_kernel=True, saved=sv)
+        runs.append([o, fin] + [t for t in grads if t is not None])
+    torch.cuda.synchronize()
+    for other in runs[1:]:
+        for a, b in zip(runs[0], other):
+            assert torch.equal(a, b)
