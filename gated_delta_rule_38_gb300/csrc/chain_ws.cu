@@ -986,8 +986,8 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
                 if (l0) umma::commit(sb + L::B_MB);
                 if (l0) umma::commit(sb + L::B_EMPTY + 8 * b);
                 if (lc + 1 < nc) {
-                    if (!(ok = uwait(sb + L::B_PREP, (lc + 1) & 1, flag, geo.err) &&
-                               uwait(sb + L::B_FULL + 8 * (b ^ 1), ((lc + 1) >> 1) & 1, flag, geo.err)))
+                    // (B_PREP implies the stage's tiles: the preparation waited for them before its arrival)
+                    if (!(ok = uwait(sb + L::B_PREP, (lc + 1) & 1, flag, geo.err)))
                         break;
                     umma::fence_after();
                     issue_pw(lc + 1);
