@@ -32,7 +32,8 @@ from gated_delta_rule_38_gb300.inputs import WORKLOADS, make_inputs  # noqa: E40
 METRIC = "GDN fwd+bwd tokens/s & TFLOP/s (H=32,K=V=128,bf16) vs roofline, 1xGB300"
 # DRAM bytes (read + write) per launch on the dense workload from one ncu capture of each kernel as it
 # stands (profiles/*_dense_B2_T4096_H32.md); an entry must be removed when its kernel changes.
-NCU_TRAFFIC = {"wy_fwd": 172.6e6, "chain_fwd": 496.5e6, "chunk_p": 151.4e6, "bwd_chunk": 884.1e6}
+NCU_TRAFFIC = {"wy_fwd": 172.6e6, "chain_fwd": 496.5e6, "chain_rev": 437.7e6, "chunk_p": 151.4e6,
+               "bwd_chunk": 884.1e6}
 C = 64
 L2_BYTES = 129 * 2 ** 20
 
