@@ -24,16 +24,18 @@
 // WY/UT representation, PR #998 "[GDN] Add FlashQLA backend dispatch").
 //
 // Warp roles (one CTA per SM):
-//   warp 0            lane 0 issues every MMA but round B's X (the next chunk's products are issued in
-//                     small groups around round B so that round B never waits behind them)
-//   warp 1            lane 0 issues the TMA tile loads into a two-stage ring
+//   warp 0            the MMA warp: the whole warp runs the loop and polls, lane 0 issues every MMA but
+//                     round B's X (the next chunk's products go in small groups around round B so that
+//                     round B never waits behind them)
+//   warp 1            the TMA warp, likewise: tile loads into a two-stage ring, and an L2 prefetch of the
+//                     next chunk's boxes
 //   warps 2,3         TMEM lanes 64..127: the -W epilogue and the output rows
 //   warps 4..11       the state: TMEM lane 32*(w%4)+l, value columns of half (w-4)/4 of the slice;
 //                     warps 4,5,8,9 also move Delta (lanes 0..63) into shared memory, and warp 4 then issues
 //                     round B's X product
 //   warps 12..15      per-chunk preparation (one warp per scheduler): gate factors, scaled copies of A
-// Hand-offs go through mbarriers whose phases each complete once per chunk; every wait is
-// bounded and gives up early once another role has raised the block's error flag.
+// Hand-offs go through mbarriers whose phases each complete once per chunk (every lane of a waiting warp
+// polls); every wait is bounded and gives up early once another role has raised the block's error flag.
 #include <cuda_runtime.h>
 
 #include <cuda.h>
@@ -797,16 +799,17 @@ __global__ void __launch_bounds__(WS_NT, 1) chain_ws_kernel(Geo geo, const __gri
 // ============================================================================ reverse chain
 //
 // The gradient of the state, dh [K x V], runs the chunks backwards; its value columns are independent,
-// so one CTA of 512 threads owns one (sequence, value head) with all 128 columns (the warp roles of the
-// forward).  With dh' the gradient after chunk c, P = scale (q^ k^T o Gamma) (lower), Q~ = diag(scale rq e^G) Q
-// and W = A diag(beta e^G rk) K:
+// so one CTA of 512 threads owns one (sequence, value head, BV-wide slice of the value columns): BV = 64
+// (two CTAs per head) when the forward's states are at hand and the chain runs alone, BV = 128 beside the
+// forward recompute.  The warp roles are the forward's.  With dh' the gradient after chunk c,
+// P = scale (q^ k^T o Gamma) (lower), Q~ = diag(scale rq e^G) Q and W = A diag(beta e^G rk) K:
 //
 //   dDelta = diag(rk e^{Gl-G}) (K dh') + P^T dO                     [64 x V]
 //   dh     = e^{Gl} dh' + Q~^T dO - W^T dDelta                        [K x V]
 //
 //   state-independent:  P^T dO -> T_P, Q~^T dO -> T_Y (the base of round B), W -> T_W (the -W epilogue)
-//   round A:  E = [K ; .] dh'                  (lanes 0..63)           M=128, N=128, K=128
-//   round B:  T_Y += (-W)^T dDelta                                     M=128, N=128, K=64
+//   round A:  E = [K ; .] dh'                  (lanes 0..63)           M=128, N=BV, K=128
+//   round B:  T_Y += (-W)^T dDelta                                     M=128, N=BV, K=64
 // It stores dh' of every chunk (the gradient after the chunk) and dDelta for the per-chunk gradients;
 // the last dh is dh0.
 
