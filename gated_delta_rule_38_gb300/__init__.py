@@ -65,9 +65,14 @@ def problem(q, v, g, scale=None, cu_seqlens=None, use_qk_l2norm_in_kernel=False,
     return p
 
 
-def workspace_bytes(p: _lib.Problem, backward: bool) -> int:
+def workspace_bytes(p: _lib.Problem, backward: bool, saved=None) -> int:
+    """Workspace bytes of the forward or backward (smaller with a saved buffer, which holds some parts)."""
     lib = _lib.load()
     n = ctypes.c_size_t(0)
+    if saved is not None:
+        _lib.check(lib.gdr_saved_workspace_size(ctypes.byref(p), int(backward), ctypes.byref(n)),
+                   "gdr_saved_workspace_size")
+        return int(n.value)
     fn = lib.gdr_bwd_workspace_size if backward else lib.gdr_fwd_workspace_size
     _lib.check(fn(ctypes.byref(p), ctypes.byref(n)), fn.__name__)
     return int(n.value)
@@ -125,7 +130,7 @@ def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
     if output_h:
         rows = int(lib.gdr_max_chunks(ctypes.byref(p)))
         h = torch.empty((rows, Hv) + _state_shape(p, state_v_first)[2:], dtype=q.dtype, device=dev)
-    nbytes = workspace_bytes(p, False)
+    nbytes = workspace_bytes(p, False, saved)
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
     h0 = None if initial_state is None else initial_state.to(torch.float32).contiguous()
     st = lib.gdr_fwd_ex(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(o),
@@ -156,7 +161,7 @@ def chunk_gated_delta_rule_bwd(q, k, v, g, beta, A, do, dht=None, scale=None, in
     h0 = None if initial_state is None else initial_state.to(torch.float32).contiguous()
     dh0 = torch.empty(_state_shape(p, state_v_first), dtype=torch.float32, device=dev) if h0 is not None else None
     dht_ = None if dht is None else dht.to(torch.float32).contiguous()
-    nbytes = workspace_bytes(p, True)
+    nbytes = workspace_bytes(p, True, saved)
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
     st = lib.gdr_bwd_ex(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A), _ptr(do),
                         _ptr(dht_), _ptr(h0), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(db), _ptr(dh0), _ptr(ws),

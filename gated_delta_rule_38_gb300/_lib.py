@@ -27,7 +27,8 @@ STATUS_NAMES = {
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ["gdr_max_chunks", "gdr_prepare_chunks", "gdr_fwd_workspace_size", "gdr_bwd_workspace_size",
            "gdr_fwd", "gdr_bwd", "gdr_get_error", "gdr_status_string", "gdr_version", "gdr_profile_enable",
-           "gdr_profile_read", "gdr_fwd_noalloc", "gdr_saved_bytes", "gdr_fwd_ex", "gdr_bwd_ex"]
+           "gdr_profile_read", "gdr_fwd_noalloc", "gdr_saved_bytes", "gdr_saved_workspace_size", "gdr_fwd_ex",
+           "gdr_bwd_ex"]
 
 
 class Problem(ctypes.Structure):
@@ -78,6 +79,8 @@ def load() -> ctypes.CDLL:
         lib.gdr_bwd.restype = i32
         lib.gdr_saved_bytes.argtypes = [PP, ctypes.POINTER(ctypes.c_size_t)]
         lib.gdr_saved_bytes.restype = i32
+        lib.gdr_saved_workspace_size.argtypes = [PP, i32, ctypes.POINTER(ctypes.c_size_t)]
+        lib.gdr_saved_workspace_size.restype = i32
         lib.gdr_fwd_ex.argtypes = [PP] + [P] * 12 + [ctypes.c_size_t, P, P]
         lib.gdr_fwd_ex.restype = i32
         lib.gdr_bwd_ex.argtypes = [PP] + [P] * 16 + [ctypes.c_size_t, P, P]

@@ -179,8 +179,10 @@ struct Layout {
     size_t bytes = 0;
 };
 
-// Workspace: [varlen chunk tables][fwd: g_cumsum, A scratch | bwd: states, state gradients].
-Layout layout_of(const gdr_problem *p, bool bwd) {
+// Workspace: [varlen chunk tables][fwd: g_cumsum, A scratch | bwd: states, state gradients].  With a saved
+// buffer (`kept`, unsplit problems) the parts that the buffer holds instead are left out: P and the norms
+// in both directions, the states and Delta in the backward.
+Layout layout_of(const gdr_problem *p, bool bwd, bool kept = false) {
     Layout L;
     size_t at = 0;
     const int64_t mc = max_chunks_of(p);
@@ -194,12 +196,13 @@ Layout layout_of(const gdr_problem *p, bool bwd) {
     }
     const size_t tok = (size_t)p->B * p->T;
     L.nseg = choose_nseg(p);
+    kept = kept && L.nseg == 1;
     if (!bwd) {
         L.gcs = at;
         at = round_up(at + tok * p->Hv * sizeof(float), 256);
         L.A = at;
         at = round_up(at + tok * p->Hv * C * esize(p->dtype), 256);
-        if (L.nseg == 1) {
+        if (L.nseg == 1 && !kept) {
             // the decayed causal attention block and the inverse q/k norms for the unsplit recurrence
             L.P = at;
             at = round_up(at + tok * p->Hv * C * esize(p->dtype), 256);
@@ -212,16 +215,20 @@ Layout layout_of(const gdr_problem *p, bool bwd) {
         }
     } else {
         const size_t st = (size_t)mc * p->Hv * DK * DV * esize(p->dtype);
-        L.h = at;
-        at = round_up(at + st, 256);
+        if (!kept) {
+            L.h = at;
+            at = round_up(at + st, 256);
+        }
         L.dhn = at;
         at = round_up(at + st, 256);
         const size_t dsz = (size_t)mc * p->Hv * C * DV * esize(p->dtype);
-        L.delta = at;
-        at = round_up(at + dsz, 256);
+        if (!kept) {
+            L.delta = at;
+            at = round_up(at + dsz, 256);
+        }
         L.ddelta = at;
         at = round_up(at + dsz, 256);
-        if (L.nseg == 1) {
+        if (L.nseg == 1 && !kept) {
             L.P = at;
             at = round_up(at + tok * p->Hv * C * esize(p->dtype), 256);
             if (p->flags & GDR_L2NORM_QK) {
@@ -416,6 +423,14 @@ gdr_status gdr_bwd_workspace_size(const gdr_problem *p, size_t *bytes) {
     return GDR_OK;
 }
 
+gdr_status gdr_saved_workspace_size(const gdr_problem *p, int backward, size_t *bytes) {
+    gdr_status st = check_problem(p);
+    if (st != GDR_OK) return st;
+    if (!bytes) return GDR_ERR_NULL;
+    *bytes = layout_of(p, backward != 0, true).bytes;
+    return GDR_OK;
+}
+
 gdr_status gdr_saved_bytes(const gdr_problem *p, size_t *bytes) {
     if (!bytes) return GDR_ERR_NULL;
     gdr_status st = check_problem(p);
@@ -442,7 +457,7 @@ gdr_status gdr_fwd_ex(const gdr_problem *p, const void *q, const void *k, const 
         if (x && !aligned16(x)) return GDR_ERR_ALIGN;
     // with a saved buffer the states go there (one copy of them per call)
     if (h && saved && saved_layout_of(p).bytes) return GDR_ERR_UNSUPPORTED;
-    const Layout L = layout_of(p, false);
+    const Layout L = layout_of(p, false, saved != nullptr);
     if ((st = check_ws(L, workspace, workspace_bytes)) != GDR_OK) return st;
     unsigned *err = nullptr;
     if ((st = device_state(&err)) != GDR_OK) return st;
@@ -494,7 +509,7 @@ gdr_status gdr_bwd_ex(const gdr_problem *p, const void *q, const void *k, const 
     const void *ptrs[] = {q, k, v, g_cumsum, beta, A, dout, dht, h0, dq, dk, dv, dg, dbeta, dh0, p->cu_seqlens, saved};
     for (const void *x : ptrs)
         if (x && !aligned16(x)) return GDR_ERR_ALIGN;
-    const Layout L = layout_of(p, true);
+    const Layout L = layout_of(p, true, saved != nullptr);
     if ((st = check_ws(L, workspace, workspace_bytes)) != GDR_OK) return st;
     unsigned *err = nullptr;
     if ((st = device_state(&err)) != GDR_OK) return st;

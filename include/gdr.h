@@ -171,6 +171,12 @@ gdr_status gdr_bwd(const gdr_problem *p, const void *q, const void *k, const voi
  *   Other arguments, layouts and errors as gdr_fwd / gdr_bwd.
  */
 gdr_status gdr_saved_bytes(const gdr_problem *p, size_t *bytes);
+/* Workspace bytes that gdr_fwd_ex (backward == 0) or gdr_bwd_ex (backward != 0) needs
+ * when it is given a saved buffer (host-only): the parts that the buffer holds instead
+ * (P and the norms; in the backward also the states and Delta) are left out, so this is
+ * at most gdr_fwd_workspace_size / gdr_bwd_workspace_size (equal when the problem runs
+ * the intra-GPU split).  Errors as gdr_fwd_workspace_size. */
+gdr_status gdr_saved_workspace_size(const gdr_problem *p, int backward, size_t *bytes);
 gdr_status gdr_fwd_ex(const gdr_problem *p, const void *q, const void *k, const void *v,
                       const void *g, const void *beta, const float *h0, void *o,
                       float *final_state, float *g_cumsum, void *A, void *h, void *workspace,

@@ -147,3 +147,24 @@ def test_binding_rejects_states_with_saved():
     g = torch.zeros(1, 64, 1)
     with pytest.raises(ValueError):
         gdr.chunk_gated_delta_rule_fwd(x, x, x, g, g, output_h=True, saved=torch.zeros(16, dtype=torch.uint8))
+
+
+def test_saved_workspace_sizes(lib):
+    """With a saved buffer the workspaces leave out what the buffer holds (P and norms; states and Delta)."""
+    p = prob(B=2, T=4096, Hq=32, Hv=32, flags=_lib.GDR_L2NORM_QK)
+    n, m = ctypes.c_size_t(), ctypes.c_size_t()
+    tok, rows = 2 * 4096 * 32, 128 * 32
+    for backward in (0, 1):
+        full = lib.gdr_bwd_workspace_size if backward else lib.gdr_fwd_workspace_size
+        assert full(ctypes.byref(p), ctypes.byref(n)) == 0
+        assert lib.gdr_saved_workspace_size(ctypes.byref(p), backward, ctypes.byref(m)) == 0
+        kept = tok * 64 * 2 + 2 * tok * 4 + (rows * 128 * 128 * 2 + rows * 64 * 128 * 2 if backward else 0)
+        assert n.value - m.value == kept
+    # the split path keeps nothing: the sizes agree
+    ps = prob(B=1, T=65536, Hq=16, Hv=16, num_segments=4)
+    for backward in (0, 1):
+        full = lib.gdr_bwd_workspace_size if backward else lib.gdr_fwd_workspace_size
+        assert full(ctypes.byref(ps), ctypes.byref(n)) == 0
+        assert lib.gdr_saved_workspace_size(ctypes.byref(ps), backward, ctypes.byref(m)) == 0
+        assert n.value == m.value
+    assert lib.gdr_saved_workspace_size(ctypes.byref(prob(K=64)), 1, ctypes.byref(m)) == 2
