@@ -345,6 +345,86 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_decode(args):
+    """Recurrent decode: one token for each of 256 rows x 32 heads from resident fp32 states (the state cache
+    of autoregressive inference), updated in place.  HBM-bound on the states (64 KB per row and head, read and
+    written every step); the 537 MB of states exceed L2, so no flush is needed between steps."""
+    import gated_delta_rule_38_gb300 as gdr
+    from gated_delta_rule_38_gb300.inputs import custom
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    w = custom(name="decode", B=256, T=1, Hq=32, Hv=32, host_l2=False)
+    x = make_inputs(w)
+    d = {k: (v.to(dev) if v is not None else None) for k, v in x.items()}
+    state = d["h0"].clone()
+
+    def step(dd):
+        return gdr.recurrent_gated_delta_rule(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], initial_state=state,
+                                              use_qk_l2norm_in_kernel=True, inplace=True)[0]
+
+    for _ in range(args.warmup):
+        step(d)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with Clocks(0) as clk:
+        for i in range(args.steps):
+            evs[i][0].record(stream)
+            step(d)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    # end to end: the step's token inputs from pinned host memory and its output back (the states stay resident)
+    names = ["q", "k", "v", "g", "beta"]
+    hin = {k: x[k].pin_memory() for k in names}
+    hout = torch.empty(d["v"].shape, dtype=d["v"].dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in hin.values())
+    d2h = hout.numel() * hout.element_size()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        dd = {k: hin[k].to(dev, non_blocking=True) for k in names}
+        hout.copy_(step(dd), non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / args.steps
+    tokens = w.B * w.T
+    sbytes = w.B * w.Hv * 128 * 128 * 4
+    tok_bytes = tokens * (2 * w.Hq * 128 * 2 + 2 * w.Hv * 128 * 2 + 2 * w.Hv * 2)
+    algo = 2 * sbytes + tok_bytes
+    hbm, _, _, src = peaks()
+    achieved = algo / (ms * 1e-3) / 1e9
+    line = {
+        "metric": "GDN recurrent decode tokens/s (B=256 rows, T=1, H=32, K=V=128, fp32 state), 1xGB300",
+        "value": round(tokens / (ms * 1e-3), 1), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "decode B=256 T=1 Hq=Hv=32 K=V=128 l2norm-in-kernel, fp32 states resident and "
+                               "updated in place", "l2": "states (537 MB) larger than L2: no flush"},
+        "roofline": {"kernel": "decode", "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None, "peak_source": src,
+                     "algorithmic_bytes": int(algo)},
+        "e2e": {"value": round(tokens / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        pb = oracle.Problem(B=w.B, T=w.T, Hq=w.Hq, Hv=w.Hv, l2norm=True)
+        heads = [0, 1]
+        t0 = time.perf_counter()
+        oracle.fwd(pb, x["q"], x["k"], x["v"], x["g"], x["beta"], h0=x["h0"], heads=heads,
+                   nthreads=oracle.max_threads())
+        dt = time.perf_counter() - t0
+        all_heads_s = dt * w.Hv / len(heads)  # the sample's time scaled to every head
+        line["cpu_baseline"] = {"value": round(tokens / all_heads_s, 1), "unit": "tokens/s",
+                                "cores": oracle.max_threads(), "kind": "oracle",
+                                "sample": "all %d rows on %d of %d value heads (%.2f s); tokens/s scaled to all heads"
+                                          % (w.B, len(heads), w.Hv, dt)}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -354,8 +434,11 @@ def main():
     ap.add_argument("--workload", default="dense", choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode", action="store_true", help="time the recurrent decode instead of the training step")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.decode and args.impl == "ours":
+        run_decode(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -24,7 +24,7 @@ import torch
 from . import _lib
 
 __all__ = ["chunk_gated_delta_rule", "chunk_gated_delta_rule_fwd", "chunk_gated_delta_rule_bwd", "saved_buffer",
-           "prepare_chunks", "GdrError", "problem", "workspace_bytes"]
+           "recurrent_gated_delta_rule", "prepare_chunks", "GdrError", "problem", "workspace_bytes"]
 
 GdrError = _lib.GdrError
 
@@ -137,6 +137,32 @@ def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
                         _ptr(fin), _ptr(gcs), _ptr(A), _ptr(h), _ptr(ws), nbytes, _ptr(saved), _stream(dev))
     _lib.check(st, "gdr_fwd_ex")
     return gcs, A, o, h, fin
+
+
+def recurrent_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, use_qk_l2norm_in_kernel=False,
+                               state_v_first=False, inplace=False, out=None):
+    """Recurrent decode: the T tokens of every row applied one by one to its cached fp32 state.
+
+    Returns (o, final_state).  ``initial_state`` [B,Hv,K,V] fp32 ([B,Hv,V,K] with state_v_first) or None
+    (zero states); with ``inplace`` the final state is written into ``initial_state`` itself (contiguous
+    fp32).  Same recurrence as chunk_gated_delta_rule over the same tokens; meant for T = 1 or a few.
+    """
+    lib = _lib.load()
+    p = problem(q, v, g, scale, None, use_qk_l2norm_in_kernel, state_v_first, 0)
+    dev = q.device
+    B, T, Hv, V = v.shape
+    o = out if out is not None else torch.empty_like(v)
+    if inplace:
+        if initial_state is None or initial_state.dtype != torch.float32 or not initial_state.is_contiguous():
+            raise ValueError("inplace needs a contiguous fp32 initial_state")
+        h0 = fin = initial_state
+    else:
+        h0 = None if initial_state is None else initial_state.to(torch.float32).contiguous()
+        fin = torch.empty(_state_shape(p, state_v_first), dtype=torch.float32, device=dev)
+    st = lib.gdr_decode(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(fin),
+                        _ptr(o), _stream(dev))
+    _lib.check(st, "gdr_decode")
+    return o, fin
 
 
 def chunk_gated_delta_rule_bwd(q, k, v, g, beta, A, do, dht=None, scale=None, initial_state=None,

@@ -28,7 +28,7 @@ STATUS_NAMES = {
 EXPORTS = ["gdr_max_chunks", "gdr_prepare_chunks", "gdr_fwd_workspace_size", "gdr_bwd_workspace_size",
            "gdr_fwd", "gdr_bwd", "gdr_get_error", "gdr_status_string", "gdr_version", "gdr_profile_enable",
            "gdr_profile_read", "gdr_fwd_noalloc", "gdr_saved_bytes", "gdr_saved_workspace_size", "gdr_fwd_ex",
-           "gdr_bwd_ex"]
+           "gdr_bwd_ex", "gdr_decode"]
 
 
 class Problem(ctypes.Structure):
@@ -81,6 +81,8 @@ def load() -> ctypes.CDLL:
         lib.gdr_saved_bytes.restype = i32
         lib.gdr_saved_workspace_size.argtypes = [PP, i32, ctypes.POINTER(ctypes.c_size_t)]
         lib.gdr_saved_workspace_size.restype = i32
+        lib.gdr_decode.argtypes = [PP] + [P] * 9
+        lib.gdr_decode.restype = i32
         lib.gdr_fwd_ex.argtypes = [PP] + [P] * 12 + [ctypes.c_size_t, P, P]
         lib.gdr_fwd_ex.restype = i32
         lib.gdr_bwd_ex.argtypes = [PP] + [P] * 16 + [ctypes.c_size_t, P, P]

@@ -560,6 +560,21 @@ gdr_status gdr_bwd_ex(const gdr_problem *p, const void *q, const void *k, const 
     });
 }
 
+gdr_status gdr_decode(const gdr_problem *p, const void *q, const void *k, const void *v, const void *g,
+                      const void *beta, const float *state_in, float *state_out, void *o, void *stream) {
+    gdr_status st = check_problem(p);
+    if (st != GDR_OK) return st;
+    if (p->cu_seqlens) return GDR_ERR_UNSUPPORTED;  // dense rows only (each row its own cached state)
+    if (!state_out || (p->T > 0 && (!q || !k || !v || !g || !beta || !o))) return GDR_ERR_NULL;
+    const void *ptrs[] = {q, k, v, g, beta, state_in, state_out, o};
+    for (const void *x : ptrs)
+        if (x && !aligned16(x)) return GDR_ERR_ALIGN;
+    unsigned *err = nullptr;
+    if ((st = device_state(&err)) != GDR_OK) return st;
+    const Args a = make_args(p, err);
+    return cuda_status(launch_decode(a, q, k, v, g, beta, state_in, state_out, o, static_cast<cudaStream_t>(stream)));
+}
+
 gdr_status gdr_get_error(void *stream) {
     unsigned *err = nullptr;
     gdr_status st = device_state(&err);

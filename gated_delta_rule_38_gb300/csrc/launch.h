@@ -50,6 +50,11 @@ cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// Recurrent decode: T tokens of B sequences applied one by one to the fp32 states (state_in may be null
+// for zero states and may alias state_out); o [B,T,Hv,V].
+cudaError_t launch_decode(const Args &a, const void *q, const void *k, const void *v, const void *g,
+                          const void *beta, const float *state_in, float *state_out, void *o, cudaStream_t s);
+
 cudaError_t launch_prep_chunks(const int32_t *cu, int N, int T, int chunk, int32_t *idx, int64_t max_chunks,
                                int32_t *off, int32_t *total, unsigned *err, cudaStream_t s);
 

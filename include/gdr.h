@@ -210,6 +210,27 @@ gdr_status gdr_bwd_ex(const gdr_problem *p, const void *q, const void *k, const 
 gdr_status gdr_fwd_noalloc(const gdr_problem *p, const void *q, const void *k, const void *v, const void *g,
                            const void *beta, const float *h0, void *o, float *final_state, void *stream);
 
+/*
+ * Recurrent decode (autoregressive inference from a cached state; the pages name
+ * it in the FlashQLA skill page's inference section, whose text is cut off).  Each
+ * of the T tokens of every row is applied in turn to the row's fp32 state, with
+ * the recurrence the chunked forward computes in blocks: per token,
+ *   S <- e^{g} S (I - beta k k^T) + beta v k^T,   o = scale S q
+ * (FlashQLA skill page, "Core API"), k and q L2-normalised per token with
+ * GDR_L2NORM_QK.  gdr_fwd over the same tokens gives the same o and final state up
+ * to rounding.  Meant for T = 1 (one generated token) or a few tokens.
+ *   in : q, k [B,T,Hq,K]; v [B,T,Hv,V]; g (the raw log-gate, as gdr_fwd's g) and
+ *        beta [B,T,Hv]; state_in [B,Hv,K,V] fp32 ([B,Hv,V,K] with GDR_STATE_V_FIRST)
+ *        or NULL (zero states)
+ *   out: o [B,T,Hv,V] (dtype); state_out, same layout as state_in (may be state_in
+ *        itself: the update runs in place).  With T = 0 only state_out is required
+ *        (it receives state_in, or zeros).
+ *   p: dense rows only (cu_seqlens != NULL returns GDR_ERR_UNSUPPORTED);
+ *      num_segments is ignored.  Other checks and errors as gdr_fwd.
+ */
+gdr_status gdr_decode(const gdr_problem *p, const void *q, const void *k, const void *v, const void *g,
+                      const void *beta, const float *state_in, float *state_out, void *o, void *stream);
+
 /* Synchronises `stream`, then returns and clears the device error word of the
  * current device (GDR_OK when no kernel latched an error), or GDR_ERR_CUDA when
  * the stream reports a CUDA error. */
