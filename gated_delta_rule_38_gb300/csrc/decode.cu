@@ -7,9 +7,10 @@
 //   h <- e^{g} h + k (beta (v - e^{g} u))^T
 //   o  = scale h^T q
 //
-// One CTA of 128 threads per (sequence, value head): thread v holds column v of h in 128 fp32 registers,
-// so u and o are dot products inside a thread and every state row moves as one coalesced 512-byte access
-// (the [V][K] layout: one contiguous 512-byte column per thread).  The kernel is bound by HBM: 64 KB of
+// One CTA of 256 threads per (sequence, value head): threads v and v + 128 hold the two 64-row halves of
+// column v of h in fp32 registers, so u and o are dot products inside a thread plus one sum of two
+// halves, and every state row moves as one coalesced 512-byte access per half-block of threads (the
+// [V][K] layout: one contiguous 256-byte half column per thread).  The kernel is bound by HBM: 64 KB of
 // state read and 64 KB written per (sequence, head), plus 1 KB of token data per token.
 #include <cuda_runtime.h>
 
@@ -31,43 +32,48 @@ struct DecArgs {
     bool gate_f32, l2norm, v_first;
 };
 
-// Sum over the 128 threads of the block (fixed order: warp butterflies, then the four warp sums).
+// Sum over the 256 threads of the block (fixed order: warp butterflies, then the eight warp sums).
 __device__ __forceinline__ float block_sum(float x, float *red, int lane, int warp) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     if (lane == 0) red[warp] = x;
     __syncthreads();
-    const float s = (red[0] + red[1]) + (red[2] + red[3]);
+    const float s = ((red[0] + red[1]) + (red[2] + red[3])) + ((red[4] + red[5]) + (red[6] + red[7]));
     __syncthreads();
     return s;
 }
 
+// Two threads per value column: thread t holds rows 64 (t / 128) .. +63 of column t % 128 (64 registers, so
+// two CTAs of eight warps fit on an SM), and the two halves of each dot product meet in shared memory.
 template <typename T>
-__global__ void __launch_bounds__(DN) decode_kernel(const DecArgs a) {
+__global__ void __launch_bounds__(2 * DN) decode_kernel(const DecArgs a) {
+    constexpr int HR = DN / 2;  // state rows per thread
     __shared__ __align__(16) float sq[DN];
     __shared__ __align__(16) float sk[DN];
-    __shared__ float red[4];
-    const int j = blockIdx.x, n = blockIdx.y, v = threadIdx.x;
-    const int lane = v & 31, warp = v >> 5;
+    __shared__ float pu[2][DN], po[2][DN];  // the two halves' partial dot products
+    __shared__ float red[8];
+    const int j = blockIdx.x, n = blockIdx.y, tid = threadIdx.x;
+    const int v = tid & (DN - 1), half = tid >> 7, d0 = half * HR;
+    const int lane = tid & 31, warp = tid >> 5;
     const int hq = j / (a.Hv / a.Hq);
     const size_t sbase = ((size_t)n * a.Hv + j) * DN * DN;
 
-    float h[DN];  // column v of h: h[d] = h_{d,v}
+    float h[HR];  // h[i] = h_{d0+i, v}
     if (a.state_in) {
         if (a.v_first) {
-            const float4 *col = reinterpret_cast<const float4 *>(a.state_in + sbase + (size_t)v * DN);
+            const float4 *col = reinterpret_cast<const float4 *>(a.state_in + sbase + (size_t)v * DN + d0);
 #pragma unroll
-            for (int i = 0; i < DN / 4; ++i) {
+            for (int i = 0; i < HR / 4; ++i) {
                 const float4 x = col[i];
                 h[4 * i] = x.x, h[4 * i + 1] = x.y, h[4 * i + 2] = x.z, h[4 * i + 3] = x.w;
             }
         } else {
 #pragma unroll
-            for (int d = 0; d < DN; ++d) h[d] = a.state_in[sbase + (size_t)d * DN + v];
+            for (int i = 0; i < HR; ++i) h[i] = a.state_in[sbase + (size_t)(d0 + i) * DN + v];
         }
     } else {
 #pragma unroll
-        for (int d = 0; d < DN; ++d) h[d] = 0.f;
+        for (int i = 0; i < HR; ++i) h[i] = 0.f;
     }
 
     const T *q = static_cast<const T *>(a.q);
@@ -77,7 +83,9 @@ __global__ void __launch_bounds__(DN) decode_kernel(const DecArgs a) {
     for (int t = 0; t < a.T; ++t) {
         const long long tk = ((long long)n * a.T + t) * a.Hq + hq;  // token row of q, k
         const long long tv = ((long long)n * a.T + t) * a.Hv + j;   // token row of v, g, beta, o
-        const float qe = Elt<T>::to_f(q[tk * DN + v]), ke = Elt<T>::to_f(k[tk * DN + v]);
+        // the first half's threads bring q and k (element v); both halves need v, g and beta
+        const float qe = half == 0 ? Elt<T>::to_f(q[tk * DN + v]) : 0.f;
+        const float ke = half == 0 ? Elt<T>::to_f(k[tk * DN + v]) : 0.f;
         const float ve = Elt<T>::to_f(vv[tv * DN + v]);
         const float gt = load_gate<T>(a.g, tv, a.gate_f32), bt = load_gate<T>(a.beta, tv, a.gate_f32);
         float rq = 1.f, rk = 1.f;
@@ -85,25 +93,30 @@ __global__ void __launch_bounds__(DN) decode_kernel(const DecArgs a) {
             rq = 1.0f / sqrtf(block_sum(qe * qe, red, lane, warp) + L2_EPS);
             rk = 1.0f / sqrtf(block_sum(ke * ke, red, lane, warp) + L2_EPS);
         }
-        sq[v] = qe * rq;
-        sk[v] = ke * rk;
+        if (half == 0) {
+            sq[v] = qe * rq;
+            sk[v] = ke * rk;
+        }
         __syncthreads();
-        const float4 *k4 = reinterpret_cast<const float4 *>(sk);
-        const float4 *q4 = reinterpret_cast<const float4 *>(sq);
+        const float4 *k4 = reinterpret_cast<const float4 *>(sk + d0);
+        const float4 *q4 = reinterpret_cast<const float4 *>(sq + d0);
         float u = 0.f;
 #pragma unroll
-        for (int i = 0; i < DN / 4; ++i) {
+        for (int i = 0; i < HR / 4; ++i) {
             const float4 kk = k4[i];
             u = fmaf(h[4 * i], kk.x, u);
             u = fmaf(h[4 * i + 1], kk.y, u);
             u = fmaf(h[4 * i + 2], kk.z, u);
             u = fmaf(h[4 * i + 3], kk.w, u);
         }
+        pu[half][v] = u;
+        __syncthreads();
+        u = pu[0][v] + pu[1][v];  // h^T k, both halves in a fixed order
         const float e = __expf(gt);
         const float w = bt * (ve - e * u);
         float ov = 0.f;
 #pragma unroll
-        for (int i = 0; i < DN / 4; ++i) {
+        for (int i = 0; i < HR / 4; ++i) {
             const float4 kk = k4[i], qq = q4[i];
             h[4 * i] = fmaf(e, h[4 * i], kk.x * w);
             h[4 * i + 1] = fmaf(e, h[4 * i + 1], kk.y * w);
@@ -114,23 +127,25 @@ __global__ void __launch_bounds__(DN) decode_kernel(const DecArgs a) {
             ov = fmaf(h[4 * i + 2], qq.z, ov);
             ov = fmaf(h[4 * i + 3], qq.w, ov);
         }
-        o[tv * DN + v] = Elt<T>::from_f(a.scale * ov);
-        __syncthreads();  // sq, sk are rewritten by the next token
+        po[half][v] = ov;
+        __syncthreads();
+        if (half == 0) o[tv * DN + v] = Elt<T>::from_f(a.scale * (po[0][v] + po[1][v]));
+        __syncthreads();  // sq, sk, pu, po are rewritten by the next token
     }
 
     if (a.v_first) {
-        float4 *col = reinterpret_cast<float4 *>(a.state_out + sbase + (size_t)v * DN);
+        float4 *col = reinterpret_cast<float4 *>(a.state_out + sbase + (size_t)v * DN + d0);
 #pragma unroll
-        for (int i = 0; i < DN / 4; ++i) col[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+        for (int i = 0; i < HR / 4; ++i) col[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
     } else {
 #pragma unroll
-        for (int d = 0; d < DN; ++d) a.state_out[sbase + (size_t)d * DN + v] = h[d];
+        for (int i = 0; i < HR; ++i) a.state_out[sbase + (size_t)(d0 + i) * DN + v] = h[i];
     }
 }
 
 template <typename T>
 cudaError_t decode_t(const DecArgs &d, cudaStream_t s) {
-    decode_kernel<T><<<dim3(d.Hv, d.B), DN, 0, s>>>(d);
+    decode_kernel<T><<<dim3(d.Hv, d.B), 2 * DN, 0, s>>>(d);
     return cudaGetLastError();
 }
 
