@@ -2,13 +2,17 @@
 
 One step = one training pass of the whole hot path over one batch: the
 forward (gate cumsum, WY matrix, state recurrence and output, saving g_cumsum
-and A) followed by the backward (state recompute, reverse state-gradient
-chain, per-chunk gradients), on synthetic seeded inputs of the dense prefill
-workload B=2, T=4096, H_q=H_v=32, K=V=128, bf16, q/k L2-normalised in the
-kernels.
+and A, and handing its states to the backward) followed by the backward
+(reverse state-gradient chain, per-chunk gradients), on synthetic seeded
+inputs of the dense prefill workload B=2, T=4096, H_q=H_v=32, K=V=128, bf16,
+q/k L2-normalised in the kernels.
 
-Prints one JSON line.  --impl reference times the fp64 CPU oracle instead
-(a bounded sample of the same workload on the host cores).
+Prints one JSON line: the headline (tokens/s of exactly --steps timed steps),
+each direction's time, throughput and roofline fraction (inference forward,
+training forward, backward), the same per direction for the varlen, GVA and
+long workloads, per-kernel times, the end-to-end figure through host memory,
+the clocks under load and the fp64 oracle on the host cores.
+--impl reference times the oracle alone (a bounded sample of the workload).
 """
 
 from __future__ import annotations
@@ -30,12 +34,16 @@ import torch  # noqa: E402
 from gated_delta_rule_38_gb300.inputs import WORKLOADS, make_inputs  # noqa: E402
 
 METRIC = "GDN fwd+bwd tokens/s & TFLOP/s (H=32,K=V=128,bf16) vs roofline, 1xGB300"
-# DRAM bytes (read + write) per launch on the dense workload from one ncu capture of each kernel as it
-# stands (profiles/*_dense_B2_T4096_H32.md); an entry must be removed when its kernel changes.
-NCU_TRAFFIC = {"wy_fwd": 172.6e6, "chain_fwd": 496.5e6, "chain_rev": 437.7e6, "chunk_p": 151.4e6,
-               "bwd_chunk": 884.1e6}
 C = 64
 L2_BYTES = 129 * 2 ** 20
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic_dense_B2_T4096_H32.json")
+WORKLOAD_TEXT = {
+    "dense": "dense prefill B=2 T=4096 Hq=32 Hv=32 K=V=128 l2norm-in-kernel",
+    "varlen": "varlen packed T=5311 lengths [512,1024,768,3000,7] H=32 K=V=128, initial and final states",
+    "gva": "GVA B=4 T=8192 Hq=16 Hv=32 K=V=128 fp16, initial and final states",
+    "long": "long single sequence B=1 T=65536 H=16 K=V=128, slow decay, intra-GPU sequence split",
+    "tiny": "tiny B=1 T=256 H=2 K=V=128",
+}
 
 
 def peaks():
@@ -47,12 +55,14 @@ def peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def work(w, backward=True):
-    """Algorithmic FLOPs and bytes of one step (forward saving A and g_cumsum, plus backward).
+def work(w):
+    """Algorithmic FLOPs and bytes of each direction of one pass over workload ``w``.
 
-    FLOPs per token and value head (multiply-add = 2, C = 64, K = V = 128):
-    forward Hq/Hv * 4CK + 2C(K+2V) + 6KV; backward twice the forward plus 4C^2.
-    Bytes: every tensor the pass must read or write once.
+    FLOPs per token and value head (multiply-add = 2, C = 64, K = V = 128): forward Hq/Hv * 4CK + 2C(K+2V) +
+    6KV; backward twice the forward plus 4C^2.  Bytes: every tensor the direction must read or write once --
+    forward-only (inference): q, k, v, g, beta in, o out (and the initial / final states when used); the
+    training forward adds A (input dtype) and g_cumsum (fp32) out; the backward reads q, k, v, g_cumsum, beta,
+    A, do (and h0, dht) and writes dq, dk, dv, dg, dbeta (and dh0).
     """
     K = V = 128
     tok = w.tokens
@@ -64,17 +74,59 @@ def work(w, backward=True):
     qk = 2 * tok * w.Hq * K * e
     vv = tok * w.Hv * V * e
     gb = 2 * tok * w.Hv * e
-    fwd_b = qk + vv + gb + vv + tok * w.Hv * (C * e + 4)  # in; o; A and g_cumsum out
-    if w.has_h0:
-        fwd_b += st
-    if w.final_state:
-        fwd_b += st
-    bwd_b = qk + vv + tok * w.Hv * (4 + e + C * e) + vv + qk + vv + gb  # q,k,v,g_cs,beta,A,do in; grads out
+    fwd_only_b = qk + vv + gb + vv + (st if w.has_h0 else 0) + (st if w.final_state else 0)
+    train_fwd_b = fwd_only_b + tok * w.Hv * (C * e + 4)
+    bwd_b = qk + vv + tok * w.Hv * (4 + e + C * e) + vv + qk + vv + gb
     if w.has_h0:
         bwd_b += 2 * st
     if w.final_state:
         bwd_b += st
-    return (fwd_f, fwd_b, bwd_f, bwd_b) if backward else (fwd_f, fwd_b, 0, 0)
+    return {"fwd_flops": fwd_f, "fwd_only_bytes": fwd_only_b, "train_fwd_bytes": train_fwd_b, "bwd_flops": bwd_f,
+            "bwd_bytes": bwd_b, "parts": {"qk": qk, "v": vv, "gates": gb, "A_gcs": tok * w.Hv * (C * e + 4),
+                                          "gcs_beta_A": tok * w.Hv * (4 + e + C * e), "state": st}}
+
+
+def kernel_bytes(name, w, wk):
+    """Algorithmic bytes of one launch of a kernel: the tensors of the direction's list that the kernel
+    itself must read or write (intermediates it exchanges with another kernel are not counted)."""
+    p = wk["parts"]
+    st_in = p["state"] if w.has_h0 else 0
+    st_out = p["state"] if w.final_state else 0
+    table = {
+        # q, k, g, beta in; A and g_cumsum out
+        "wy_fwd": p["qk"] + p["gates"] + p["A_gcs"],
+        # q, k, v, beta, g_cumsum, A in; o out (initial / final states)
+        "chain_fwd": p["qk"] + 2 * p["v"] + p["gcs_beta_A"] + st_in + st_out,
+        # q, k, do, g_cumsum, beta, A in (dht in, dh0 out)
+        "chain_rev": p["qk"] + p["v"] + p["gcs_beta_A"] + st_out + (p["state"] if w.has_h0 else 0),
+        # every input of the backward in, every gradient out
+        "bwd_chunk": wk["bwd_bytes"],
+    }
+    return table.get(name)
+
+
+def recorded_traffic(name):
+    """DRAM bytes (read + write) of one launch of a kernel on the dense workload, from the committed ncu
+    record, or None when the record is missing or the kernel's sources changed since it was taken."""
+    import hashlib
+    try:
+        rec = json.load(open(TRAFFIC_FILE))["kernels"][name]
+    except Exception:
+        return None
+    h = hashlib.sha256()
+    for f in rec["sources"]:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return float(rec["dram_bytes"]) if h.hexdigest()[:16] == rec["sources_sha16"] else None
+
+
+def direction_report(ms, flops, nbytes, tokens, hbm, tflops):
+    """Throughput and roofline fraction of one direction (roofline = the slower of bytes at HBM bandwidth and
+    FLOPs at dense bf16 tensor peak)."""
+    rl_us = max(nbytes / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
+    return {"us": round(ms * 1e3, 2), "tokens_per_s": round(tokens / (ms * 1e-3), 1),
+            "tflops": round(flops / (ms * 1e-3) / 1e12, 2), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "roofline_us": round(rl_us, 2), "roofline_frac": round(rl_us / (ms * 1e3), 4),
+            "algorithmic_bytes": int(nbytes), "algorithmic_flops": int(flops)}
 
 
 def rank_seed(rank: int) -> int:
@@ -99,8 +151,9 @@ def job_throughput(tokens_per_rank: int, world: int, seconds: float) -> float:
 class Clocks:
     """nvidia-smi sampler running during the timed region."""
 
-    def __init__(self, index=0):
+    def __init__(self, index=0, interval_ms=50):
         self.index = index
+        self.interval_ms = interval_ms
         self.rows = []
         self.proc = None
 
@@ -110,7 +163,7 @@ class Clocks:
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + q,
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -143,6 +196,74 @@ class Clocks:
                 "samples": len(self.rows)}
 
 
+def _inputs_on(w, seed, dev):
+    x = make_inputs(w, seed=seed)
+    d = {k: (v.to(dev) if v is not None else None) for k, v in x.items()}
+    cu = None if w.cu_seqlens is None else torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
+    return x, d, cu
+
+
+def _make_step(gdr, w, cu, saved):
+    l2 = not w.host_l2
+
+    def fwd(dd, save=True):
+        if not save:
+            return gdr.chunk_gated_delta_rule_fwd(
+                dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], initial_state=dd["h0"],
+                output_final_state=w.final_state, cu_seqlens=cu, use_qk_l2norm_in_kernel=l2,
+                save_for_backward=False)
+        return gdr.chunk_gated_delta_rule_fwd(
+            dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], initial_state=dd["h0"],
+            output_final_state=w.final_state, cu_seqlens=cu, use_qk_l2norm_in_kernel=l2, saved=saved)
+
+    def bwd(dd, f):
+        gcs, A = f[0], f[1]
+        return gdr.chunk_gated_delta_rule_bwd(
+            dd["q"], dd["k"], dd["v"], gcs, dd["beta"], A, dd["do"], dht=dd["dht"], initial_state=dd["h0"],
+            cu_seqlens=cu, use_qk_l2norm_in_kernel=l2, saved=saved)
+
+    def step(dd):
+        f = fwd(dd)
+        return f[2], bwd(dd, f)
+
+    return fwd, bwd, step
+
+
+def _direction_times(fwd, bwd, d, steps, flush, stream):
+    """Mean device ms of the training forward, the backward, and an inference forward (no saving), each step
+    timed with CUDA events on the launching stream and the L2 flushed before it."""
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        f = fwd(d)
+        ev[i][1].record(stream)
+        bwd(d, f)
+        ev[i][2].record(stream)
+    inf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        inf[i][0].record(stream)
+        fwd(d, save=False)
+        inf[i][1].record(stream)
+    torch.cuda.synchronize()
+    tf = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    tb = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+    ti = sum(a.elapsed_time(b) for a, b in inf) / steps
+    return tf, tb, ti
+
+
+def _directions(w, tf, tb, ti, hbm, tflops):
+    wk = work(w)
+    return {
+        "fwd_only": direction_report(ti, wk["fwd_flops"], wk["fwd_only_bytes"], w.tokens, hbm, tflops),
+        "train_fwd": direction_report(tf, wk["fwd_flops"], wk["train_fwd_bytes"], w.tokens, hbm, tflops),
+        "bwd": direction_report(tb, wk["bwd_flops"], wk["bwd_bytes"], w.tokens, hbm, tflops),
+        "fwd_bwd": direction_report(tf + tb, wk["fwd_flops"] + wk["bwd_flops"],
+                                    wk["train_fwd_bytes"] + wk["bwd_bytes"], w.tokens, hbm, tflops),
+    }
+
+
 def run_ours(args):
     import gated_delta_rule_38_gb300 as gdr
     from gated_delta_rule_38_gb300 import _lib
@@ -156,45 +277,50 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     w = WORKLOADS[args.workload]
-    l2 = not w.host_l2
-    x = make_inputs(w, seed=rank_seed(rank))  # every rank: its own batch (weak scaling, no collective)
     dev = torch.device("cuda", local)
-    d = {k: (v.to(dev) if v is not None else None) for k, v in x.items()}
-    cu = None if w.cu_seqlens is None else torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
+    x, d, cu = _inputs_on(w, rank_seed(rank), dev)  # every rank: its own batch (weak scaling, no collective)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-
-    # the forward hands its decayed causal blocks and q/k norms to the backward (one buffer, reused by the steps)
-    saved = gdr.saved_buffer(d["q"], d["v"], d["g"], cu_seqlens=cu, use_qk_l2norm_in_kernel=l2)
-
-    def step(dd):
-        gcs, A, o, _, fin = gdr.chunk_gated_delta_rule_fwd(
-            dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], initial_state=dd["h0"],
-            output_final_state=w.final_state, cu_seqlens=cu, use_qk_l2norm_in_kernel=l2, saved=saved)
-        grads = gdr.chunk_gated_delta_rule_bwd(
-            dd["q"], dd["k"], dd["v"], gcs, dd["beta"], A, dd["do"], dht=dd["dht"], initial_state=dd["h0"],
-            cu_seqlens=cu, use_qk_l2norm_in_kernel=l2, saved=saved)
-        return o, grads
+    # the forward hands P, the q/k norms, its states and Delta to the backward (one buffer, reused by the steps)
+    saved = gdr.saved_buffer(d["q"], d["v"], d["g"], cu_seqlens=cu, use_qk_l2norm_in_kernel=not w.host_l2)
+    fwd, bwd, step = _make_step(gdr, w, cu, saved)
+    hbm, tf_burst, tf_sus, src = peaks()
 
     for _ in range(args.warmup):
         step(d)
     torch.cuda.synchronize()
 
-    # ---- device-resident timing: per step events, L2 flushed between steps (outside the events).  The
-    # library's per-kernel event profiler stays off here (its event pairs would sit between the step's
-    # kernels); a second pass of the same steps with it on gives the per-kernel times and the launch count.
+    # ---- the headline: exactly K training steps, device time per step from CUDA events on the launching
+    # stream, the L2 flushed between steps (outside the events).  The clock sampler runs from a loaded
+    # stretch of steps just before the timed ones until they end, so it sees the GPU under this load.
     stream = torch.cuda.current_stream(dev)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
     with Clocks(local) as clk:
+        t_load = time.perf_counter()
+        n_load = 0
+        while time.perf_counter() - t_load < args.load_seconds:
+            for _ in range(20):
+                flush.zero_()
+                step(d)
+            n_load += 20
+            torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
         for i in range(args.steps):
             flush.zero_()
             evs[i][0].record(stream)
             step(d)
             evs[i][1].record(stream)
         torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
     ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / args.steps, dist, dev)
+
+    # ---- per direction (events between the forward and the backward), and the inference forward
+    tf, tb, ti = _direction_times(fwd, bwd, d, args.steps, flush, stream)
+    tf, tb, ti = (max_over_ranks(t, dist, dev) for t in (tf, tb, ti))
+
+    # ---- per kernel: the library's own event pairs around each launch, in a pass of its own
     _lib.profile_enable(True)
     for i in range(args.steps):
         flush.zero_()
@@ -245,45 +371,67 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, dist, dev)
 
-    fwd_f, fwd_b, bwd_f, bwd_b = work(w)
-    hbm, tf_burst, tf_sus, src = peaks()
+    wk = work(w)
     tokens = w.tokens * world
     value = job_throughput(w.tokens, world, ms * 1e-3)
-    # dominant kernel by measured time share
+    directions = _directions(w, tf, tb, ti, hbm, tf_sus)
+    # dominant kernel by measured time share; its algorithmic bytes are the direction's tensors it must move
     tot = sum(v[1] for v in prof.values()) or 1.0
     name, (cnt, kms) = max(prof.items(), key=lambda kv: kv[1][1])
     per_launch_ms = kms / cnt
-    kernel_bytes = {
-        # algorithmic bytes one launch of each kernel must move: the per-chunk gradient kernel reads every
-        # input of the backward and writes every gradient; the forward recurrence reads the forward's inputs
-        # and writes o
-        "bwd_chunk": bwd_b, "chain_fwd": fwd_b, "chain_bwd": bwd_b * 0.5, "chain_fwd_recompute": fwd_b,
-        "chain_pair": bwd_b * 0.5, "chain_rev": bwd_b * 0.5, "wy_fwd": fwd_b * 0.4, "chunk_p": fwd_b * 0.4,
-    }
-    kb = kernel_bytes.get(name, fwd_b + bwd_b)
-    achieved = kb / (per_launch_ms * 1e-3) / 1e9
-    traffic = NCU_TRAFFIC.get(name) if args.workload == "dense" else None
-    roofline = {"kernel": name, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(achieved / hbm, 4), "traffic": traffic, "peak_source": src,
-                "share": round(kms / tot, 3), "algorithmic_bytes": int(kb)}
-    rl_us = max((fwd_b + bwd_b) / (hbm * 1e9), (fwd_f + bwd_f) / (tf_sus * 1e12)) * 1e6
+    kb = kernel_bytes(name, w, wk)
+    roofline = {"kernel": name, "bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s", "frac": None,
+                "traffic": recorded_traffic(name) if args.workload == "dense" else None,
+                "peak_source": src, "share": round(kms / tot, 3), "algorithmic_bytes": kb,
+                "launch_ms": round(per_launch_ms, 4)}
+    if kb:
+        achieved = kb / (per_launch_ms * 1e-3) / 1e9
+        roofline["achieved"] = round(achieved, 1)
+        roofline["frac"] = round(achieved / hbm, 4)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "fp16", "data": "synthetic",
-        "config": {"workload": "dense prefill B=%d T=%d Hq=%d Hv=%d K=V=128 l2norm-in-kernel" % (
-            w.B, w.T, w.Hq, w.Hv) if args.workload == "dense" else args.workload,
-            "B": w.B, "T": w.T, "Hq": w.Hq, "Hv": w.Hv, "chunk": C,
-            "l2": "flushed between steps (256 MiB write outside the timed events)", "parallelism": "replicas"},
-        "tflops": round((fwd_f + bwd_f) / (ms * 1e-3) / 1e12, 2),
-        "step_roofline_us": round(rl_us, 2), "step_roofline_frac": round(rl_us / (ms * 1e3), 4),
+        "config": {"workload": WORKLOAD_TEXT.get(args.workload, args.workload),
+                   "B": w.B, "T": w.T, "Hq": w.Hq, "Hv": w.Hv, "chunk": C,
+                   "l2": "flushed between steps (256 MiB write outside the timed events)", "parallelism": "replicas"},
+        "tflops": round((wk["fwd_flops"] + wk["bwd_flops"]) / (ms * 1e-3) / 1e12, 2),
+        "directions": directions,
         "kernels_ms_per_step": {k: round(v[1] / args.steps, 4) for k, v in prof.items()},
         "roofline": roofline,
         "e2e": {"value": round(tokens / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(sum(v[0] for v in prof.values())),
-        "clocks": clk.summary(),
+        "clocks": dict(clk.summary(), load_steps_before_timed=n_load),
     }
+    # the other workloads, each direction on its own (one GPU only: the per-workload report is a 1-GPU one)
+    if world == 1 and not args.headline_only:
+        del saved, bufs, hout
+        configs = {}
+        for other in ("varlen", "gva", "long"):
+            if other == args.workload:
+                continue
+            wo = WORKLOADS[other]
+            xo, do_, cuo = _inputs_on(wo, 42, dev)
+            svo = gdr.saved_buffer(do_["q"], do_["v"], do_["g"], cu_seqlens=cuo,
+                                   use_qk_l2norm_in_kernel=not wo.host_l2)
+            fo, bo, so = _make_step(gdr, wo, cuo, svo)
+            for _ in range(max(3, args.warmup)):
+                so(do_)
+            torch.cuda.synchronize()
+            n = max(3, min(args.steps, 50))
+            a, b, c = _direction_times(fo, bo, do_, n, flush, stream)
+            _lib.profile_enable(True)
+            so(do_)
+            torch.cuda.synchronize()
+            _lib.profile_enable(False)
+            kp = _lib.profile_read()
+            configs[other] = {"workload": WORKLOAD_TEXT[other], "steps": n,
+                              "directions": _directions(wo, a, b, c, hbm, tf_sus),
+                              "kernels_ms": {k: round(v[1], 4) for k, v in kp.items()}}
+            del xo, do_, cuo, svo, fo, bo, so
+            torch.cuda.empty_cache()
+        line["configs"] = configs
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     if rank == 0:
@@ -292,55 +440,69 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def cpu_baseline(w, budget_s):
-    """The fp64 oracle on a bounded sample of the workload (whole sequences, a subset of heads)."""
+def _oracle_sample(w, x, nh, nthreads):
+    """fwd + bwd of the oracle over every token of ``w`` on its first ``nh`` value heads; returns seconds."""
     import oracle
-    nthreads = oracle.max_threads()
-    x = make_inputs(w)
     pb = oracle.Problem(B=w.B, T=w.T, Hq=w.Hq, Hv=w.Hv, l2norm=not w.host_l2, cu_seqlens=w.cu_seqlens)
-    heads = [0]
+    heads = list(range(nh))
     t0 = time.perf_counter()
     oracle.fwd(pb, x["q"], x["k"], x["v"], x["g"], x["beta"], h0=x["h0"], heads=heads, nthreads=nthreads)
     oracle.bwd(pb, x["q"], x["k"], x["v"], x["g"], x["beta"], x["do"], h0=x["h0"], dht=x["dht"], heads=heads,
                nthreads=nthreads)
-    dt = time.perf_counter() - t0
-    nh = 1
-    # grow the sample (more heads) while it stays inside the budget
+    return time.perf_counter() - t0
+
+
+def _first_heads(w, nthreads):
+    """Fewest value heads whose (sequence, head) pairs keep every oracle thread busy (it parallelises over
+    those pairs)."""
+    return min(w.Hv, max(1, -(-nthreads // max(1, w.num_seqs))))
+
+
+def cpu_baseline(w, budget_s):
+    """The fp64 oracle on a bounded sample of the workload (every token, a subset of the value heads large
+    enough to occupy every thread), grown while it stays inside the budget."""
+    import oracle
+    nthreads = oracle.max_threads()
+    x = make_inputs(w)
+    nh = _first_heads(w, nthreads)
+    dt = _oracle_sample(w, x, nh, nthreads)
     while dt * 2.2 < budget_s and nh * 2 <= w.Hv:
         nh *= 2
-        heads = list(range(nh))
-        t0 = time.perf_counter()
-        oracle.fwd(pb, x["q"], x["k"], x["v"], x["g"], x["beta"], h0=x["h0"], heads=heads, nthreads=nthreads)
-        oracle.bwd(pb, x["q"], x["k"], x["v"], x["g"], x["beta"], x["do"], h0=x["h0"], dht=x["dht"],
-                   heads=heads, nthreads=nthreads)
-        dt = time.perf_counter() - t0
-    token_heads = w.tokens * nh
-    return {"value": round(token_heads / w.Hv / dt, 1), "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
-            "sample": "fwd+bwd of all %d tokens on %d of %d value heads (%.1f s); tokens/s scaled to all heads"
-                      % (w.tokens, nh, w.Hv, dt)}
+        dt = _oracle_sample(w, x, nh, nthreads)
+    return {"value": round(w.tokens * nh / w.Hv / dt, 1), "unit": "tokens/s", "cores": nthreads,
+            "host_cpus": os.cpu_count(), "kind": "oracle",
+            "sample": "fwd+bwd of all %d tokens on %d of %d value heads (%.2f s, %d threads); tokens/s scaled to "
+                      "all heads" % (w.tokens, nh, w.Hv, dt, nthreads)}
 
 
 def run_reference(args):
-    """The oracle as the reference arm: fp64 CPU, bounded sample, on rank 0 only."""
+    """The oracle as the reference arm: fp64 CPU on the host cores, rank 0 only.  Each step is a timed sample
+    of the workload: fwd + bwd of every token on as many value heads as keep every oracle thread busy."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    import oracle
     w = WORKLOADS[args.workload]
-    samples = []
+    nthreads = oracle.max_threads()
+    x = make_inputs(w)
+    nh = _first_heads(w, nthreads)
+    times = []
     for i in range(args.warmup + args.steps):
-        cb = cpu_baseline(w, args.cpu_seconds / max(1, args.steps))
+        dt = _oracle_sample(w, x, nh, nthreads)
         if i >= args.warmup:
-            samples.append(cb)
-    v = sum(s["value"] for s in samples) / len(samples)
-    tokens = w.tokens
+            times.append(dt)
+    t = sum(times) / len(times)
+    v = w.tokens * nh / w.Hv / t
+    sample = ("each step: fwd+bwd of all %d tokens on %d of %d value heads (%d threads, %d host CPUs); "
+              "tokens/s scaled to all heads" % (w.tokens, nh, w.Hv, nthreads, os.cpu_count()))
     line = {"metric": METRIC, "impl": "reference", "value": round(v, 1), "unit": "tokens/s",
             "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(tokens / v * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": round(t * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "dense prefill B=%d T=%d Hq=%d Hv=%d K=V=128 l2norm-in-kernel" % (
-                w.B, w.T, w.Hq, w.Hv) if args.workload == "dense" else args.workload},
-            "cpu_baseline": {"value": round(v, 1), "unit": "tokens/s", "kind": "oracle",
-                             "cores": samples[-1]["cores"], "sample": samples[-1]["sample"]},
+            "config": {"workload": WORKLOAD_TEXT.get(args.workload, args.workload),
+                       "step": "a timed sample: %d of %d value heads" % (nh, w.Hv)},
+            "cpu_baseline": {"value": round(v, 1), "unit": "tokens/s", "kind": "oracle", "cores": nthreads,
+                             "host_cpus": os.cpu_count(), "sample": sample},
             "e2e": {"value": round(v, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -434,6 +596,9 @@ def main():
     ap.add_argument("--workload", default="dense", choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--load-seconds", type=float, default=1.0,
+                    help="loaded stretch of steps before the timed ones, inside the clock sampler's window")
+    ap.add_argument("--headline-only", action="store_true", help="skip the per-workload direction report")
     ap.add_argument("--decode", action="store_true", help="time the recurrent decode instead of the training step")
     args = ap.parse_args()
     if args.decode and args.impl == "ours":

@@ -200,13 +200,16 @@ def prepare_chunks(cu_seqlens: torch.Tensor, chunk_size: int = _lib.GDR_CHUNK, t
     """Chunk tables of a packed batch, computed on the GPU.
 
     Returns (chunk_indices [max_chunks,2] int32, chunk_offsets [N+1] int32, total_chunks int32 [1]);
-    rows of chunk_indices past total_chunks are zero.
+    rows of chunk_indices past total_chunks are zero.  Without ``total_tokens`` the table is sized from
+    ``cu_seqlens[-1]``, read back to the host once (a synchronisation); passing it avoids that read.
     """
     lib = _lib.load()
     cu = _cu(cu_seqlens)
     N = cu.numel() - 1
     T = int(total_tokens)
-    bound = ((T if T >= 0 else 0) + N * (chunk_size - 1)) // chunk_size
+    if T < 0:
+        T = int(cu[-1].item())
+    bound = (max(T, 0) + N * (chunk_size - 1)) // chunk_size
     max_chunks = max(bound, 1)
     idx = torch.zeros((max_chunks, 2), dtype=torch.int32, device=cu.device)
     off = torch.empty((N + 1,), dtype=torch.int32, device=cu.device)

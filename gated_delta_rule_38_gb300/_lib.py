@@ -28,7 +28,7 @@ STATUS_NAMES = {
 EXPORTS = ["gdr_max_chunks", "gdr_prepare_chunks", "gdr_fwd_workspace_size", "gdr_bwd_workspace_size",
            "gdr_fwd", "gdr_bwd", "gdr_get_error", "gdr_status_string", "gdr_version", "gdr_profile_enable",
            "gdr_profile_read", "gdr_fwd_noalloc", "gdr_saved_bytes", "gdr_saved_workspace_size", "gdr_fwd_ex",
-           "gdr_bwd_ex", "gdr_decode"]
+           "gdr_bwd_ex", "gdr_decode", "gdr_debug_set_wait_polls"]
 
 
 class Problem(ctypes.Structure):
@@ -98,6 +98,8 @@ def load() -> ctypes.CDLL:
         lib.gdr_profile_read.argtypes = [i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_longlong),
                                          ctypes.POINTER(ctypes.c_double)]
         lib.gdr_profile_read.restype = i32
+        lib.gdr_debug_set_wait_polls.argtypes = [ctypes.c_longlong]
+        lib.gdr_debug_set_wait_polls.restype = i32
         lib.gdr_version.argtypes = []
         lib.gdr_version.restype = i32
         _lib = lib

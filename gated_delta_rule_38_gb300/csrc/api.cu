@@ -17,8 +17,10 @@ __device__ unsigned int g_gdr_error_word = 0;
 
 // ---------------------------------------------------------------- chunk tables
 
-// One CTA.  Validates cu_seqlens, then an exclusive scan of ceil(len/chunk)
-// gives the offsets; each sequence's rows of the chunk table follow.
+// One CTA.  Validates cu_seqlens and checks that the table has room for every
+// chunk (both before anything is written), then an exclusive scan of
+// ceil(len/chunk) gives the offsets; each sequence's rows of the chunk table
+// follow.
 __global__ void __launch_bounds__(1024) prep_chunks_kernel(const int32_t *__restrict__ cu, int N, int T, int chunk,
                                                            int32_t *__restrict__ idx, long long max_chunks,
                                                            int32_t *__restrict__ off, int32_t *__restrict__ total,
@@ -26,19 +28,26 @@ __global__ void __launch_bounds__(1024) prep_chunks_kernel(const int32_t *__rest
     __shared__ int s_bad;
     __shared__ int s_warp[32];
     __shared__ long long s_carry;
+    __shared__ unsigned long long s_need;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
     if (tid == 0) {
         s_bad = (cu[0] != 0 || (T >= 0 && cu[N] != T)) ? 1 : 0;
         s_carry = 0;
+        s_need = 0;
     }
     __syncthreads();
-    for (int n = tid; n < N; n += blockDim.x)
-        if (cu[n + 1] < cu[n]) atomicOr(&s_bad, 1);
+    unsigned long long need = 0;
+    for (int n = tid; n < N; n += blockDim.x) {
+        const int a = cu[n], b = cu[n + 1];
+        if (b < a) atomicOr(&s_bad, 1);
+        else need += (unsigned long long)((b - a + chunk - 1) / chunk);
+    }
+    if (need) atomicAdd(&s_need, need);
     __syncthreads();
-    if (s_bad) {
+    if (s_bad || (long long)s_need > max_chunks) {
         if (tid == 0) {
             *total = 0;
-            raise_error(err, GDR_ERR_CUSEQLENS);
+            raise_error(err, s_bad ? GDR_ERR_CUSEQLENS : GDR_ERR_SHAPE);
         }
         return;
     }
@@ -97,6 +106,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
+long long g_wait_polls = 0;  // gdr_debug_set_wait_polls (0: every wait keeps its own bound)
 int g_dev_ok[kMaxDevices];           // 0 unknown, 1 ok, 2 wrong arch
 unsigned *g_err_ptr[kMaxDevices];    // device address of the error word
 
@@ -301,6 +311,10 @@ Args make_args(const gdr_problem *p, unsigned *err) {
     a.cidx = a.coff = a.ctotal = nullptr;
     a.max_chunks = max_chunks_of(p);
     a.err = err;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        a.wait_polls = g_wait_polls;
+    }
     return a;
 }
 
@@ -565,6 +579,7 @@ gdr_status gdr_decode(const gdr_problem *p, const void *q, const void *k, const 
     gdr_status st = check_problem(p);
     if (st != GDR_OK) return st;
     if (p->cu_seqlens) return GDR_ERR_UNSUPPORTED;  // dense rows only (each row its own cached state)
+    if ((long long)p->B * p->Hv > 0x7fffffffLL) return GDR_ERR_SHAPE;  // one block per (row, head)
     if (!state_out || (p->T > 0 && (!q || !k || !v || !g || !beta || !o))) return GDR_ERR_NULL;
     const void *ptrs[] = {q, k, v, g, beta, state_in, state_out, o};
     for (const void *x : ptrs)
@@ -607,6 +622,13 @@ const char *gdr_status_string(gdr_status s) {
 }
 
 int gdr_version(void) { return 100; }
+
+gdr_status gdr_debug_set_wait_polls(long long polls) {
+    if (polls < 0) return GDR_ERR_SHAPE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_wait_polls = polls;
+    return GDR_OK;
+}
 
 gdr_status gdr_profile_enable(int on) {
     std::lock_guard<std::mutex> lk(g_prof.mu);

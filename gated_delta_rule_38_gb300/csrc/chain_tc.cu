@@ -822,17 +822,6 @@ __global__ void __launch_bounds__(NT, 1) chain_bwd_tc_kernel(Geo geo, const __gr
     chain_bwd_body<T, AFFINE>(geo, p, blockIdx.x, blockIdx.y, blockIdx.z);
 }
 
-// The backward's two chains are independent: blocks z < N recompute the forward states,
-// blocks z >= N run the reverse state-gradient chain, side by side on the GPU.
-template <typename T>
-__global__ void __launch_bounds__(NT, 1) chain_pair_kernel(Geo geo, const __grid_constant__ TcP pf,
-                                                           const __grid_constant__ TcBwdP pb) {
-    if ((int)blockIdx.z < geo.N)
-        chain_fwd_body<T, false, false>(geo, pf, blockIdx.x, blockIdx.y, blockIdx.z);
-    else
-        chain_bwd_body<T, false>(geo, pb, blockIdx.x, blockIdx.y, blockIdx.z - geo.N);
-}
-
 template <typename T>
 cudaError_t chain_bwd_tc_t(const Args &a, const TcBwdP &p, bool affine, cudaStream_t s) {
     auto kern = affine ? chain_bwd_tc_kernel<T, true> : chain_bwd_tc_kernel<T, false>;
@@ -972,16 +961,6 @@ TcP fwd_params(const Args &a, const void *q, const void *k, const void *v, const
     return p;
 }
 
-template <typename T>
-cudaError_t chain_pair_t(const Args &a, const TcP &pf, const TcBwdP &pb, cudaStream_t s) {
-    auto kern = chain_pair_kernel<T>;
-    const uint32_t smem = SMEM_BYTES > B_SMEM_BYTES ? SMEM_BYTES : B_SMEM_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    kern<<<dim3(1, a.Hv, 2 * a.N), NT, smem, s>>>(make_geo(a), pf, pb);
-    return cudaGetLastError();
-}
-
 }  // namespace
 
 cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
@@ -1017,16 +996,6 @@ cudaError_t launch_chain_fwd(const Args &a, const void *q, const void *k, const 
     }
     return a.bf16 ? chain_fwd_tc_t<__nv_bfloat16>(a, p, o != nullptr, false, s)
                   : chain_fwd_tc_t<__half>(a, p, o != nullptr, false, s);
-}
-
-cudaError_t launch_chain_pair(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
-                              const void *beta, const void *A, const float *h0, void *h, void *delta, const void *dout,
-                              const float *dht, void *dhn, void *ddelta, float *dh0, cudaStream_t s) {
-    SegWs none{1, nullptr, nullptr, nullptr};
-    const TcP pf = fwd_params(a, q, k, v, g_cs, beta, A, h0, nullptr, nullptr, h, false, delta, none);
-    const TcBwdP pb = bwd_params(a, q, k, g_cs, beta, A, dout, dht, dhn, ddelta, dh0, none);
-    if (pf.nseg < 1 || pb.nseg < 1) return cudaErrorInvalidValue;
-    return a.bf16 ? chain_pair_t<__nv_bfloat16>(a, pf, pb, s) : chain_pair_t<__half>(a, pf, pb, s);
 }
 
 }  // namespace gdr

@@ -51,6 +51,7 @@ struct PpP {
     bool l2norm;
     float scale;
     int nslots;
+    long polls;  // bound of the two waits of the item loop
 };
 
 template <typename T>
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(PT, 2) chunk_p_tc_kernel(Geo geo, const __grid
     while (cur.y >= 0) {
         const uint32_t st = sb + (uint32_t)stage * ST_BYTES;
         if (tid == 0) {
-            if (umma::mbar_spin(full0 + 8u * (uint32_t)stage, (fph >> stage) & 1u)) {
+            if (umma::mbar_spin(full0 + 8u * (uint32_t)stage, (fph >> stage) & 1u, p.polls)) {
                 fph ^= 1u << stage;
                 seen[stage] += 1;
             } else {
@@ -180,7 +181,7 @@ __global__ void __launch_bounds__(PT, 2) chunk_p_tc_kernel(Geo geo, const __grid
             (half ? nk : nq)[r] = 1.f;
         }
         if (tid == 0) {
-            if (umma::mbar_spin(mbar, mph)) {
+            if (umma::mbar_spin(mbar, mph, p.polls)) {
                 mph ^= 1u;
                 mma_out = false;
             } else {
@@ -310,6 +311,7 @@ cudaError_t launch_chunk_p_tc(const Args &a, const void *q, const void *k, const
     p.l2norm = a.l2norm;
     p.scale = a.scale;
     p.nslots = (int)a.max_chunks;
+    p.polls = a.wait_polls > 0 ? (long)a.wait_polls : 200000000L;
     return a.bf16 ? chunk_p_tc_t<__nv_bfloat16>(a, p, s) : chunk_p_tc_t<__half>(a, p, s);
 }
 

@@ -52,7 +52,8 @@ __global__ void __launch_bounds__(2 * DN) decode_kernel(const DecArgs a) {
     __shared__ __align__(16) float sk[DN];
     __shared__ float pu[2][DN], po[2][DN];  // the two halves' partial dot products
     __shared__ float red[8];
-    const int j = blockIdx.x, n = blockIdx.y, tid = threadIdx.x;
+    // one flat grid dimension (x allows 2^31 - 1 blocks): block b = (row n, value head j)
+    const int j = (int)(blockIdx.x % (unsigned)a.Hv), n = (int)(blockIdx.x / (unsigned)a.Hv), tid = threadIdx.x;
     const int v = tid & (DN - 1), half = tid >> 7, d0 = half * HR;
     const int lane = tid & 31, warp = tid >> 5;
     const int hq = j / (a.Hv / a.Hq);
@@ -145,7 +146,8 @@ __global__ void __launch_bounds__(2 * DN) decode_kernel(const DecArgs a) {
 
 template <typename T>
 cudaError_t decode_t(const DecArgs &d, cudaStream_t s) {
-    decode_kernel<T><<<dim3(d.Hv, d.B), 2 * DN, 0, s>>>(d);
+    if (d.B == 0) return cudaSuccess;
+    decode_kernel<T><<<dim3((unsigned)((long long)d.Hv * d.B)), 2 * DN, 0, s>>>(d);
     return cudaGetLastError();
 }
 

@@ -22,6 +22,7 @@ struct Args {
     const int32_t *ctotal;   // device total chunks (varlen)
     int64_t max_chunks;
     unsigned *err;           // device error word
+    long long wait_polls;    // > 0: poll budget of the waits that honour it (test support); 0 = default
 };
 
 // Workspace of the intra-GPU sequence split (nseg segments per sequence; nseg == 1: no split):
@@ -97,11 +98,6 @@ cudaError_t launch_chain_rev(const Args &a, const void *q, const void *k, const 
 cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
                              const void *A, const void *dout, const float *dht, void *dhn, void *ddelta, float *dh0,
                              const SegWs &sw, cudaStream_t s);
-// Backward, no sequence split: both chains above (forward recompute without output, reverse chain) in
-// one launch, side by side.
-cudaError_t launch_chain_pair(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
-                              const void *beta, const void *A, const float *h0, void *h, void *delta, const void *dout,
-                              const float *dht, void *dhn, void *ddelta, float *dh0, cudaStream_t s);
 // Backward: per-chunk gradients (dq, dk, dv, dg, dbeta).
 cudaError_t launch_bwd_chunk_tc(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
                                 const void *beta, const void *A, const void *dout, const void *h, const void *dhn,

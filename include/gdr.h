@@ -104,7 +104,10 @@ int64_t gdr_max_chunks(const gdr_problem *p);
  * skip that check.  A malformed cu_seqlens latches GDR_ERR_CUSEQLENS in the
  * device error word (see gdr_get_error) and writes total_chunks = 0.
  * Returns GDR_ERR_SHAPE when max_chunks is smaller than the bound
- * (total_tokens + num_seqs*(chunk_size-1)) / chunk_size.
+ * (total_tokens + num_seqs*(chunk_size-1)) / chunk_size.  The kernel also
+ * counts the chunks before it writes anything: when they exceed max_chunks
+ * (possible with total_tokens = -1) it writes nothing but total_chunks = 0 and
+ * latches GDR_ERR_SHAPE in the device error word.
  */
 gdr_status gdr_prepare_chunks(const int32_t *cu_seqlens, int num_seqs, int total_tokens,
                               int chunk_size, int32_t *chunk_indices, int64_t max_chunks,
@@ -251,6 +254,19 @@ const char *gdr_status_string(gdr_status s);
  */
 gdr_status gdr_profile_enable(int on);
 int gdr_profile_read(int max, const char **names, long long *launches, double *ms);
+
+/*
+ * Test support for the bounded device-side waits (no counterpart on the pages).
+ * polls > 0 caps the number of polls of each wait in the item loop of the
+ * backward's decayed-block kernel (the one gdr_bwd / gdr_bwd_ex launch without a
+ * saved buffer) at `polls`; with a handful of polls the first wait gives up
+ * before its tile loads land.  The kernel then latches GDR_ERR_TIMEOUT in the
+ * device error word, lets the loads and the MMA it issued finish (with its own
+ * fixed bound), frees its tensor memory and returns; the results of that call
+ * are undefined.  polls = 0 restores the normal bound.  Process-wide setting,
+ * read by every later call; returns GDR_ERR_SHAPE for polls < 0.
+ */
+gdr_status gdr_debug_set_wait_polls(long long polls);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int gdr_version(void);

@@ -62,18 +62,74 @@ def test_no_alloc_forward_matches_workspace_forward_twice():
     _run_both(lib, w2, _inputs(2, w2), cu, False)
 
 
-def test_no_alloc_rejects_problems_beyond_its_scratch():
-    """A forward whose workspace exceeds the built-in scratch is refused on the host."""
-    from gated_delta_rule_38_gb300 import build as gbuild
-    gbuild.build()
-    lib = _lib.load()
+def _big_problem():
+    """A forward whose workspace (about 70 MB: 262,144 token-heads x 268 bytes) exceeds the 64 MiB scratch."""
     p = _lib.Problem()
-    p.B, p.T, p.Hq, p.Hv, p.K, p.V = 1, 1 << 20, 1, 16, 128, 128
+    p.B, p.T, p.Hq, p.Hv, p.K, p.V = 1, 16384, 16, 16, 128, 128
     p.dtype = p.gate_dtype = _lib.GDR_BF16
     p.scale = 128 ** -0.5
     p.cu_seqlens = None
     p.num_seqs = 0
     p.flags = 0
     p.num_segments = 1
+    return p
+
+
+def test_no_alloc_rejects_problems_beyond_its_scratch_without_gpu():
+    """A forward whose workspace exceeds the built-in scratch is refused on the host (made-up addresses,
+    so only on a machine without a GPU)."""
+    if torch.cuda.is_available():
+        pytest.skip("the GPU variant below uses real buffers")
+    from gated_delta_rule_38_gb300 import build as gbuild
+    gbuild.build()
+    lib = _lib.load()
+    p = _big_problem()
     P = ctypes.c_void_p(0x100000)
     assert lib.gdr_fwd_noalloc(ctypes.byref(p), P, P, P, P, P, None, P, None, None) == 7
+
+
+@pytest.mark.gpu
+def test_no_alloc_rejects_problems_beyond_its_scratch():
+    """The same refusal with real buffers of the problem's sizes."""
+    lib = _lib.load()
+    p = _big_problem()
+    x = torch.zeros(1, 16384, 16, 128, dtype=torch.bfloat16, device="cuda")
+    gb = torch.zeros(1, 16384, 16, dtype=torch.bfloat16, device="cuda")
+    o = torch.empty_like(x)
+    assert lib.gdr_fwd_noalloc(ctypes.byref(p), _p(x), _p(x), _p(x), _p(gb), _p(gb), None, _p(o), None,
+                               _stream()) == 7
+
+
+@pytest.mark.gpu
+def test_no_alloc_allocates_nothing_and_runs_the_split_layout():
+    """After a first (set-up) call, further calls leave the device's free memory unchanged; a problem that
+    runs the intra-GPU sequence split (two segments: its own workspace layout) still fits the scratch."""
+    lib = _lib.load()
+    w = custom(B=1, T=1000, Hq=2, Hv=2)
+    x = _inputs(3, w)
+    pb = gdr.problem(x["q"], x["v"], x["g"], None, None, False, num_segments=2)
+    nbytes = gdr.workspace_bytes(pb, False)
+    assert 0 < nbytes <= 64 << 20
+    o_ref = torch.empty_like(x["v"])
+    fin_ref = torch.empty(x["h0"].shape, dtype=torch.float32, device="cuda")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    st = lib.gdr_fwd(ctypes.byref(pb), _p(x["q"]), _p(x["k"]), _p(x["v"]), _p(x["g"]), _p(x["beta"]),
+                     _p(x["h0"]), _p(o_ref), _p(fin_ref), None, None, None, _p(ws), nbytes, _stream())
+    assert st == 0
+    o = torch.empty_like(x["v"])
+    fin = torch.empty_like(fin_ref)
+
+    def call():
+        s = lib.gdr_fwd_noalloc(ctypes.byref(pb), _p(x["q"]), _p(x["k"]), _p(x["v"]), _p(x["g"]), _p(x["beta"]),
+                                _p(x["h0"]), _p(o), _p(fin), _stream())
+        assert s == 0, _lib.status_string(s)
+        torch.cuda.synchronize()
+
+    call()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        call()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    assert rel_l2(np64(o), np64(o_ref)) <= TOL
+    assert rel_l2(np64(fin), np64(fin_ref)) <= TOL
