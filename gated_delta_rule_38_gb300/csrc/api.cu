@@ -106,7 +106,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-long long g_wait_polls = 0;  // gdr_debug_set_wait_polls (0: every wait keeps its own bound)
+long long g_wait_polls = -1;  // gdr_debug_set_wait_polls (< 0: every wait keeps its own bound)
 int g_dev_ok[kMaxDevices];           // 0 unknown, 1 ok, 2 wrong arch
 unsigned *g_err_ptr[kMaxDevices];    // device address of the error word
 
@@ -624,9 +624,8 @@ const char *gdr_status_string(gdr_status s) {
 int gdr_version(void) { return 100; }
 
 gdr_status gdr_debug_set_wait_polls(long long polls) {
-    if (polls < 0) return GDR_ERR_SHAPE;
     std::lock_guard<std::mutex> lk(g_mu);
-    g_wait_polls = polls;
+    g_wait_polls = polls < 0 ? -1 : polls;
     return GDR_OK;
 }
 

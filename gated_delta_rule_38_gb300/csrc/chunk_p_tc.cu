@@ -311,7 +311,7 @@ cudaError_t launch_chunk_p_tc(const Args &a, const void *q, const void *k, const
     p.l2norm = a.l2norm;
     p.scale = a.scale;
     p.nslots = (int)a.max_chunks;
-    p.polls = a.wait_polls > 0 ? (long)a.wait_polls : 200000000L;
+    p.polls = a.wait_polls >= 0 ? (long)a.wait_polls : 200000000L;
     return a.bf16 ? chunk_p_tc_t<__nv_bfloat16>(a, p, s) : chunk_p_tc_t<__half>(a, p, s);
 }
 

@@ -22,7 +22,7 @@ struct Args {
     const int32_t *ctotal;   // device total chunks (varlen)
     int64_t max_chunks;
     unsigned *err;           // device error word
-    long long wait_polls;    // > 0: poll budget of the waits that honour it (test support); 0 = default
+    long long wait_polls;    // >= 0: poll budget of the waits that honour it (test support); < 0 = default
 };
 
 // Workspace of the intra-GPU sequence split (nseg segments per sequence; nseg == 1: no split):

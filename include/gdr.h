@@ -257,14 +257,14 @@ int gdr_profile_read(int max, const char **names, long long *launches, double *m
 
 /*
  * Test support for the bounded device-side waits (no counterpart on the pages).
- * polls > 0 caps the number of polls of each wait in the item loop of the
+ * polls >= 0 caps the number of polls of each wait in the item loop of the
  * backward's decayed-block kernel (the one gdr_bwd / gdr_bwd_ex launch without a
- * saved buffer) at `polls`; with a handful of polls the first wait gives up
- * before its tile loads land.  The kernel then latches GDR_ERR_TIMEOUT in the
- * device error word, lets the loads and the MMA it issued finish (with its own
- * fixed bound), frees its tensor memory and returns; the results of that call
- * are undefined.  polls = 0 restores the normal bound.  Process-wide setting,
- * read by every later call; returns GDR_ERR_SHAPE for polls < 0.
+ * saved buffer) at `polls`; with polls = 0 the first wait gives up without
+ * looking, before its tile loads can land.  The kernel then latches
+ * GDR_ERR_TIMEOUT in the device error word, lets the loads and the MMA it issued
+ * finish (with its own fixed bound), frees its tensor memory and returns; the
+ * results of that call are undefined.  polls < 0 restores the normal bound.
+ * Process-wide setting, read by every later call.
  */
 gdr_status gdr_debug_set_wait_polls(long long polls);
 
