@@ -22,7 +22,11 @@ Contents
   as plain Python loops.
 
 Readings where the pages are silent (each is listed in the design notes):
-the log-gate ``g`` is used as ``exp(g)`` with no activation; the L2 norm is
+the log-gate ``g`` is used as ``exp(g)`` with no activation unless one of the
+activation options is set (``gate_in_kernel``: g = logsigmoid(raw), the log of
+the sigmoid decay in (0, 1) that the skill page's module example applies;
+``beta_sigmoid``: beta = sigmoid(raw); ``neg_eigval``: beta doubled, so that the
+eigenvalue 1 - beta of the transition along k spans (-1, 1)); the L2 norm is
 ``x / sqrt(sum x^2 + 1e-6)``; the chunk size is 64; ``g_cumsum`` is the
 chunk-local inclusive cumulative sum reset at every chunk and sequence start;
 ``A`` is stored per token as row ``t mod 64`` of its chunk's inverse;
@@ -97,6 +101,11 @@ class Problem:
     state_v_first: bool = False
     cu_seqlens: Optional[List[int]] = None
     chunk: int = CHUNK
+    # activations applied to the raw per-token scalars before the recurrence (the options the FlashQLA
+    # backend's verifier names: use_gate_in_kernel, use_beta_sigmoid_in_kernel, allow_neg_eigval)
+    gate_in_kernel: bool = False   # g <- logsigmoid(g): the log of a sigmoid decay in (0, 1)
+    beta_sigmoid: bool = False     # beta <- sigmoid(beta)
+    neg_eigval: bool = False       # beta <- 2 beta: the transition's eigenvalue along k spans (-1, 1)
 
     def __post_init__(self):
         if self.scale is None:
@@ -130,6 +139,42 @@ def _f64(a) -> Optional[np.ndarray]:
     return np.ascontiguousarray(a, dtype=np.float64)
 
 
+def _sigmoid(x: np.ndarray) -> np.ndarray:
+    """1 / (1 + e^{-x}), evaluated without overflow for either sign of x."""
+    e = np.exp(-np.abs(x))
+    return np.where(x >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
+
+
+def _logsigmoid(x: np.ndarray) -> np.ndarray:
+    """log(1 / (1 + e^{-x})) = min(x, 0) - log(1 + e^{-|x|})."""
+    return np.minimum(x, 0.0) - np.log1p(np.exp(-np.abs(x)))
+
+
+def activate(pb: Problem, g, beta):
+    """The gate and beta the recurrence uses, from the raw inputs (fp64); unchanged without the options."""
+    g, beta = _f64(g), _f64(beta)
+    if pb.gate_in_kernel:
+        g = _logsigmoid(g)
+    if pb.beta_sigmoid:
+        beta = _sigmoid(beta)
+    if pb.neg_eigval:
+        beta = 2.0 * beta
+    return g, beta
+
+
+def activate_grads(pb: Problem, g_raw, beta_raw, dg, dbeta):
+    """Chain rule through ``activate``: gradients w.r.t. the raw g and beta from those w.r.t. the used ones.
+    d logsigmoid(x)/dx = sigmoid(-x); d sigmoid(x)/dx = sigmoid(x) sigmoid(-x)."""
+    if pb.gate_in_kernel:
+        dg = dg * _sigmoid(-_f64(g_raw)).reshape(dg.shape)
+    if pb.neg_eigval:
+        dbeta = 2.0 * dbeta
+    if pb.beta_sigmoid:
+        b = _f64(beta_raw).reshape(dbeta.shape)
+        dbeta = dbeta * _sigmoid(b) * _sigmoid(-b)
+    return dg, dbeta
+
+
 def _chunk_base(pb: Problem) -> np.ndarray:
     base, acc = [], 0
     for _, ln in pb.seq_bounds():
@@ -147,6 +192,7 @@ def fwd(pb: Problem, q, k, v, g, beta, h0=None, heads=None, want_h=False, want_d
     evaluate (outputs of the other heads are NaN).
     """
     lib = _load()
+    g, beta = activate(pb, g, beta)
     q, k, v, g, beta, h0 = (_f64(x) for x in (q, k, v, g, beta, h0))
     Ttot = pb.total_tokens
     N = pb.num_seqs
@@ -188,6 +234,8 @@ def bwd(pb: Problem, q, k, v, g, beta, do, h0=None, dht=None, heads=None, nthrea
     exact when every v-head of its group is selected).
     """
     lib = _load()
+    g_raw, beta_raw = g, beta
+    g, beta = activate(pb, g, beta)
     q, k, v, g, beta, h0, do, dht = (_f64(x) for x in (q, k, v, g, beta, h0, do, dht))
     Ttot = pb.total_tokens
     N = pb.num_seqs
@@ -212,6 +260,7 @@ def bwd(pb: Problem, q, k, v, g, beta, do, h0=None, dht=None, heads=None, nthrea
                             _ptr(dh0), int(nthreads))
     if rc != 0:
         raise RuntimeError("oracle bwd failed with code %d" % rc)
+    dg, db = activate_grads(pb, g_raw, beta_raw, dg, db)
     lead = (pb.B, pb.T) if pb.cu_seqlens is None else (1, Ttot)
     return {"dq": dq.reshape(lead + (pb.Hq, pb.K)), "dk": dk.reshape(lead + (pb.Hq, pb.K)),
             "dv": dv.reshape(lead + (pb.Hv, pb.V)), "dg": dg.reshape(lead + (pb.Hv,)),
@@ -232,7 +281,7 @@ def g_cumsum(pb: Problem, g) -> np.ndarray:
     Returns [B,T,Hv] (or [1,Ttot,Hv]) fp64.  Restarts at every chunk start and
     at every sequence start (reading of the "processed gate tensor").
     """
-    g = _f64(g).reshape(pb.total_tokens, pb.Hv)
+    g = activate(pb, g, np.zeros(1))[0].reshape(pb.total_tokens, pb.Hv)
     out = np.zeros_like(g)
     for s0, L in pb.seq_bounds():
         for c0 in range(0, L, pb.chunk):
@@ -254,7 +303,7 @@ def wy_matrix(pb: Problem, k, g, beta) -> np.ndarray:
     kk = _f64(k).reshape(pb.total_tokens, pb.Hq, pb.K)
     if pb.l2norm:
         kk = _l2n(kk)
-    bb = _f64(beta).reshape(pb.total_tokens, pb.Hv)
+    bb = activate(pb, np.zeros(1), beta)[1].reshape(pb.total_tokens, pb.Hv)
     G = g_cumsum(pb, g).reshape(pb.total_tokens, pb.Hv)
     grp = pb.Hv // pb.Hq
     out = np.zeros((pb.total_tokens, pb.Hv, pb.chunk))

@@ -375,3 +375,79 @@ def test_gate_gradient_identity():
         s = slice(cu[n], cu[n + 1])
         ident = np.flip(np.cumsum(np.flip(D[0, s], 0), 0), 0) + (dht[n] * f["final_state"][n]).sum((-1, -2))
         np.testing.assert_allclose(ident, r["dg"][0, s], rtol=1e-10, atol=1e-12)
+
+
+# ---------------------------------------------------------------- activation options
+
+ACT = dict(gate_in_kernel=True, beta_sigmoid=True, neg_eigval=True)
+
+
+def test_activations_equal_library_routines():
+    """With the options set, the oracle equals the plain recurrence on inputs activated by scipy's own
+    logistic routines (an implementation other than the oracle's)."""
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(21)
+    base = dict(B=2, T=11, Hq=1, Hv=2, K=4, V=4, scale=0.7, chunk=4)
+    x = small_inputs(rng, Problem(**base))
+    graw = 3.0 * rnd(rng, *x["g"].shape)          # raw gate logits, both signs, some large
+    braw = 3.0 * rnd(rng, *x["beta"].shape)
+    for opts in (dict(gate_in_kernel=True), dict(beta_sigmoid=True), dict(neg_eigval=True), ACT):
+        pa = Problem(**base, **opts)
+        ga = special.log_expit(graw) if opts.get("gate_in_kernel") else graw
+        ba = special.expit(braw) if opts.get("beta_sigmoid") else braw
+        if opts.get("neg_eigval"):
+            ba = 2.0 * ba
+        got = oracle.fwd(pa, x["q"], x["k"], x["v"], graw, braw, h0=x["h0"])
+        want = oracle.fwd(Problem(**base), x["q"], x["k"], x["v"], ga, ba, h0=x["h0"])
+        for key in ("o", "final_state"):
+            assert np.allclose(got[key], want[key], rtol=1e-13, atol=1e-13), (opts, key)
+
+
+def test_negative_eigenvalue_reflects_the_key_direction():
+    """beta = 2 (raw beta = 1 doubled), g = 0, v = 0: the step is the Householder reflection I - 2 k k^T of
+    the state, so a state k u^T becomes -k u^T (eigenvalue -1 along k) and directions orthogonal to k stay."""
+    K = V = 4
+    pb = Problem(B=1, T=1, Hq=1, Hv=1, K=K, V=V, scale=1.0, neg_eigval=True)
+    k = np.zeros((1, 1, 1, K)); k[..., 1] = 1.0
+    u = np.array([0.5, -1.0, 2.0, 0.25])
+    w = np.array([0.0, 0.0, 3.0, 0.0])            # orthogonal to k
+    h0 = (np.outer(k[0, 0, 0], u) + np.outer(np.array([1.0, 0, 0, 0]), w))[None, None]
+    out = oracle.fwd(pb, np.zeros((1, 1, 1, K)), k, np.zeros((1, 1, 1, V)), np.zeros((1, 1, 1)),
+                     np.ones((1, 1, 1)), h0=h0)
+    want = -np.outer(k[0, 0, 0], u) + np.outer(np.array([1.0, 0, 0, 0]), w)
+    assert np.allclose(out["final_state"][0, 0], want, atol=1e-15)
+
+
+@pytest.mark.parametrize("opts", [dict(gate_in_kernel=True), dict(beta_sigmoid=True), ACT],
+                         ids=["gate", "beta_sigmoid", "all"])
+def test_activation_gradients_match_finite_differences(opts):
+    """Gradients w.r.t. the raw gate and beta (chain rule through the activations) against central
+    differences of the whole forward."""
+    rng = np.random.default_rng(22)
+    pb = Problem(B=1, T=7, Hq=1, Hv=2, K=4, V=4, scale=0.8, l2norm=True, cu_seqlens=[0, 3, 7], chunk=3, **opts)
+    x = small_inputs(rng, pb)
+    x["g"] = 2.0 * rnd(rng, *x["g"].shape)
+    x["beta"] = 2.0 * rnd(rng, *x["beta"].shape)
+    out = oracle.fwd(pb, **x)
+    Ro = rnd(rng, *out["o"].shape)
+    Rh = rnd(rng, *out["final_state"].shape)
+
+    def loss(xx):
+        r = oracle.fwd(pb, **xx)
+        return float(np.sum(r["o"] * Ro) + np.sum(r["final_state"] * Rh))
+
+    grads = oracle.bwd(pb, **x, do=Ro, dht=Rh)
+    eps = 1e-6
+    for name, gname in (("g", "dg"), ("beta", "dbeta"), ("k", "dk")):
+        base = x[name]
+        num = np.zeros_like(base)
+        it = np.nditer(base, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            xp = {kk: (vv.copy() if kk == name else vv) for kk, vv in x.items()}
+            xm = {kk: (vv.copy() if kk == name else vv) for kk, vv in x.items()}
+            xp[name][idx] += eps
+            xm[name][idx] -= eps
+            num[idx] = (loss(xp) - loss(xm)) / (2 * eps)
+        err = np.max(np.abs(grads[gname] - num)) / max(1e-3, np.max(np.abs(num)))
+        assert err < 1e-6, (name, err)
