@@ -40,7 +40,8 @@ def _stream(device) -> ctypes.c_void_p:
 
 
 def problem(q, v, g, scale=None, cu_seqlens=None, use_qk_l2norm_in_kernel=False, state_v_first=False,
-            num_segments=0, extra_flags=0) -> _lib.Problem:
+            num_segments=0, extra_flags=0, use_gate_in_kernel=False, use_beta_sigmoid_in_kernel=False,
+            allow_neg_eigval=False) -> _lib.Problem:
     """The gdr_problem struct describing a call with these tensors."""
     B, T, Hq, K = q.shape
     Hv, V = v.shape[2], v.shape[3]
@@ -49,6 +50,12 @@ def problem(q, v, g, scale=None, cu_seqlens=None, use_qk_l2norm_in_kernel=False,
         flags |= _lib.GDR_L2NORM_QK
     if state_v_first:
         flags |= _lib.GDR_STATE_V_FIRST
+    if use_gate_in_kernel:
+        flags |= _lib.GDR_GATE_IN_KERNEL
+    if use_beta_sigmoid_in_kernel:
+        flags |= _lib.GDR_BETA_SIGMOID_IN_KERNEL
+    if allow_neg_eigval:
+        flags |= _lib.GDR_ALLOW_NEG_EIGVAL
     p = _lib.Problem()
     p.B, p.T, p.Hq, p.Hv, p.K, p.V = B, T, Hq, Hv, K, V
     p.dtype = _DT.get(q.dtype, 99)
@@ -92,12 +99,13 @@ def _cu(cu_seqlens):
 
 
 def saved_buffer(q, v, g, scale=None, cu_seqlens=None, use_qk_l2norm_in_kernel=False, state_v_first=False,
-                 num_segments=0):
+                 num_segments=0, **act):
     """A device buffer for what the forward keeps for the backward (``saved=`` of the forward and backward
-    below): the decayed causal blocks, the q/k norms, the state before every chunk and Delta of every chunk.
-    None when the problem keeps nothing (the intra-GPU split path)."""
+    below): the decayed causal blocks, the q/k norms, the state before every chunk and Delta of every chunk,
+    and with ``use_gate_in_kernel`` the gate activation's derivative.  None when the problem keeps nothing
+    (the intra-GPU split path without the in-kernel gate).  ``act``: the activation options."""
     lib = _lib.load()
-    p = problem(q, v, g, scale, _cu(cu_seqlens), use_qk_l2norm_in_kernel, state_v_first, num_segments)
+    p = problem(q, v, g, scale, _cu(cu_seqlens), use_qk_l2norm_in_kernel, state_v_first, num_segments, **act)
     n = ctypes.c_size_t(0)
     _lib.check(lib.gdr_saved_bytes(ctypes.byref(p), ctypes.byref(n)), "gdr_saved_bytes")
     return torch.empty(int(n.value), dtype=torch.uint8, device=q.device) if n.value else None
@@ -105,19 +113,24 @@ def saved_buffer(q, v, g, scale=None, cu_seqlens=None, use_qk_l2norm_in_kernel=F
 
 def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=True,
                                cu_seqlens=None, use_qk_l2norm_in_kernel=False, state_v_first=False,
-                               num_segments=0, output_h=False, save_for_backward=True, out=None, saved=None):
+                               num_segments=0, output_h=False, save_for_backward=True, out=None, saved=None,
+                               use_gate_in_kernel=False, use_beta_sigmoid_in_kernel=False, allow_neg_eigval=False):
     """Forward.  Returns (g_cumsum, A, o, h, final_state); h is None unless output_h.
 
     g_cumsum and A are None when save_for_backward is False.  For packed
     batches h has gdr_max_chunks rows; rows past the true chunk count are unused.
     ``saved`` (from saved_buffer) receives the decayed causal blocks, q/k norms, states and Delta for the
-    backward; it excludes ``output_h`` (the states then live in ``saved``).
+    backward; it excludes ``output_h`` (the states then live in ``saved``).  With ``use_gate_in_kernel`` g
+    holds raw gate logits (the recurrence uses logsigmoid(g)); with ``use_beta_sigmoid_in_kernel`` beta holds
+    raw logits (sigmoid(beta)); ``allow_neg_eigval`` doubles beta.
     """
     if output_h and saved is not None:
         raise ValueError("output_h and saved are exclusive: with saved, the states are kept in the saved buffer")
     lib = _lib.load()
     cu = _cu(cu_seqlens)
-    p = problem(q, v, g, scale, cu, use_qk_l2norm_in_kernel, state_v_first, num_segments)
+    p = problem(q, v, g, scale, cu, use_qk_l2norm_in_kernel, state_v_first, num_segments,
+                use_gate_in_kernel=use_gate_in_kernel, use_beta_sigmoid_in_kernel=use_beta_sigmoid_in_kernel,
+                allow_neg_eigval=allow_neg_eigval)
     dev = q.device
     B, T, Hv, V = v.shape
     o = out if out is not None else torch.empty_like(v)
@@ -140,7 +153,8 @@ def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
 
 
 def recurrent_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, use_qk_l2norm_in_kernel=False,
-                               state_v_first=False, inplace=False, out=None):
+                               state_v_first=False, inplace=False, out=None, use_gate_in_kernel=False,
+                               use_beta_sigmoid_in_kernel=False, allow_neg_eigval=False):
     """Recurrent decode: the T tokens of every row applied one by one to its cached fp32 state.
 
     Returns (o, final_state).  ``initial_state`` [B,Hv,K,V] fp32 ([B,Hv,V,K] with state_v_first) or None
@@ -148,7 +162,9 @@ def recurrent_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None,
     fp32).  Same recurrence as chunk_gated_delta_rule over the same tokens; meant for T = 1 or a few.
     """
     lib = _lib.load()
-    p = problem(q, v, g, scale, None, use_qk_l2norm_in_kernel, state_v_first, 0)
+    p = problem(q, v, g, scale, None, use_qk_l2norm_in_kernel, state_v_first, 0,
+                use_gate_in_kernel=use_gate_in_kernel, use_beta_sigmoid_in_kernel=use_beta_sigmoid_in_kernel,
+                allow_neg_eigval=allow_neg_eigval)
     dev = q.device
     B, T, Hv, V = v.shape
     o = out if out is not None else torch.empty_like(v)
@@ -167,17 +183,22 @@ def recurrent_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None,
 
 def chunk_gated_delta_rule_bwd(q, k, v, g, beta, A, do, dht=None, scale=None, initial_state=None,
                                cu_seqlens=None, use_qk_l2norm_in_kernel=False, state_v_first=False,
-                               num_segments=0, gate_dtype=None, saved=None):
+                               num_segments=0, gate_dtype=None, saved=None, use_gate_in_kernel=False,
+                               use_beta_sigmoid_in_kernel=False, allow_neg_eigval=False):
     """Backward.  ``g`` is the forward's g_cumsum (fp32).  Returns (dq, dk, dv, dbeta, dg, dh0).
 
     dg and dbeta take beta's dtype (or ``gate_dtype``); dh0 is None without an initial state.
     ``saved`` is the buffer the forward filled for the same problem and inputs (the backward then skips
-    recomputing the decayed causal blocks, the states and Delta); None recomputes them.
+    recomputing the decayed causal blocks, the states and Delta); None recomputes them.  With the activation
+    options, beta is the raw beta and dg, dbeta are gradients w.r.t. the raw inputs; ``use_gate_in_kernel``
+    needs ``saved``.
     """
     lib = _lib.load()
     cu = _cu(cu_seqlens)
     gd = gate_dtype or beta.dtype
-    p = problem(q, v, torch.empty(0, dtype=gd), scale, cu, use_qk_l2norm_in_kernel, state_v_first, num_segments)
+    p = problem(q, v, torch.empty(0, dtype=gd), scale, cu, use_qk_l2norm_in_kernel, state_v_first, num_segments,
+                use_gate_in_kernel=use_gate_in_kernel, use_beta_sigmoid_in_kernel=use_beta_sigmoid_in_kernel,
+                allow_neg_eigval=allow_neg_eigval)
     dev = q.device
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
@@ -228,30 +249,34 @@ def get_error(device=None) -> int:
 class _GDR(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, g, beta, scale, initial_state, output_final_state, cu_seqlens,
-                use_qk_l2norm_in_kernel, state_v_first, num_segments):
+                use_qk_l2norm_in_kernel, state_v_first, num_segments, act):
         saved = saved_buffer(q, v, g, scale=scale, cu_seqlens=cu_seqlens,
                              use_qk_l2norm_in_kernel=use_qk_l2norm_in_kernel, state_v_first=state_v_first,
-                             num_segments=num_segments)
+                             num_segments=num_segments, **act)
         gcs, A, o, _, fin = chunk_gated_delta_rule_fwd(
             q, k, v, g, beta, scale=scale, initial_state=initial_state, output_final_state=output_final_state,
             cu_seqlens=cu_seqlens, use_qk_l2norm_in_kernel=use_qk_l2norm_in_kernel, state_v_first=state_v_first,
-            num_segments=num_segments, saved=saved)
+            num_segments=num_segments, saved=saved, **act)
         ctx.save_for_backward(q, k, v, gcs, beta, A, initial_state, cu_seqlens, saved)
-        ctx.opts = (scale, use_qk_l2norm_in_kernel, state_v_first, num_segments, g.dtype)
+        ctx.opts = (scale, use_qk_l2norm_in_kernel, state_v_first, num_segments, g.dtype, act)
         return o, fin
 
     @staticmethod
     def backward(ctx, do, dht):
         q, k, v, gcs, beta, A, h0, cu, saved = ctx.saved_tensors
-        scale, l2, vf, nseg, gdt = ctx.opts
+        scale, l2, vf, nseg, gdt, act = ctx.opts
         dq, dk, dv, db, dg, dh0 = chunk_gated_delta_rule_bwd(
             q, k, v, gcs, beta, A, do.contiguous(), dht=dht, scale=scale, initial_state=h0, cu_seqlens=cu,
-            use_qk_l2norm_in_kernel=l2, state_v_first=vf, num_segments=nseg, gate_dtype=gdt, saved=saved)
-        return dq, dk, dv, dg, db, None, dh0, None, None, None, None, None
+            use_qk_l2norm_in_kernel=l2, state_v_first=vf, num_segments=nseg, gate_dtype=gdt, saved=saved, **act)
+        return dq, dk, dv, dg, db, None, dh0, None, None, None, None, None, None
 
 
 def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, output_final_state=False,
-                           cu_seqlens=None, use_qk_l2norm_in_kernel=False, state_v_first=False, num_segments=0):
-    """Differentiable op: returns (o, final_state or None)."""
+                           cu_seqlens=None, use_qk_l2norm_in_kernel=False, state_v_first=False, num_segments=0,
+                           use_gate_in_kernel=False, use_beta_sigmoid_in_kernel=False, allow_neg_eigval=False):
+    """Differentiable op: returns (o, final_state or None).  The activation options: see
+    chunk_gated_delta_rule_fwd (gradients are w.r.t. the raw g and beta)."""
+    act = dict(use_gate_in_kernel=use_gate_in_kernel, use_beta_sigmoid_in_kernel=use_beta_sigmoid_in_kernel,
+               allow_neg_eigval=allow_neg_eigval)
     return _GDR.apply(q, k, v, g, beta, scale, initial_state, output_final_state, cu_seqlens,
-                      use_qk_l2norm_in_kernel, state_v_first, num_segments)
+                      use_qk_l2norm_in_kernel, state_v_first, num_segments, act)

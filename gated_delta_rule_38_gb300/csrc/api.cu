@@ -133,6 +133,9 @@ gdr_status device_state(unsigned **err) {
     return GDR_OK;
 }
 
+// the gate / beta activation options
+constexpr unsigned kActFlags = GDR_GATE_IN_KERNEL | GDR_BETA_SIGMOID_IN_KERNEL | GDR_ALLOW_NEG_EIGVAL;
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline size_t esize(gdr_dtype d) { return d == GDR_FP32 ? 4 : 2; }
@@ -145,8 +148,8 @@ gdr_status check_problem(const gdr_problem *p) {
     if (p->num_segments < 0) return GDR_ERR_SHAPE;
     if (p->dtype != GDR_BF16 && p->dtype != GDR_FP16) return GDR_ERR_DTYPE;
     if (p->gate_dtype != p->dtype && p->gate_dtype != GDR_FP32) return GDR_ERR_DTYPE;
-    const unsigned rejected = GDR_GATE_IN_KERNEL | GDR_BETA_SIGMOID_IN_KERNEL | GDR_ALLOW_NEG_EIGVAL | GDR_INTER_CARD_CP;
-    const unsigned known = GDR_L2NORM_QK | GDR_STATE_V_FIRST;
+    const unsigned rejected = GDR_INTER_CARD_CP;
+    const unsigned known = GDR_L2NORM_QK | GDR_STATE_V_FIRST | kActFlags;
     if ((p->flags & rejected) || (p->flags & ~(known | rejected))) return GDR_ERR_UNSUPPORTED;
     return GDR_OK;
 }
@@ -184,6 +187,7 @@ int choose_nseg(const gdr_problem *p) {
 
 struct Layout {
     size_t idx = 0, off = 0, total = 0, gcs = 0, A = 0, P = 0, rq = 0, rk = 0, h = 0, dhn = 0, delta = 0, ddelta = 0;
+    size_t geff = 0, beff = 0, dgeff = 0, dbeff = 0;  // activated gate / beta and their gradients (fp32)
     size_t seg[3] = {0, 0, 0};
     int nseg = 1;
     size_t bytes = 0;
@@ -207,6 +211,23 @@ Layout layout_of(const gdr_problem *p, bool bwd, bool kept = false) {
     const size_t tok = (size_t)p->B * p->T;
     L.nseg = choose_nseg(p);
     kept = kept && L.nseg == 1;
+    if (p->flags & kActFlags) {
+        // fp32 activated gates for the forward; activated beta and the gradients w.r.t. the activated g and
+        // beta for the backward
+        const size_t sz = tok * p->Hv * sizeof(float);
+        if (!bwd) {
+            L.geff = at;
+            at = round_up(at + sz, 256);
+        }
+        L.beff = at;
+        at = round_up(at + sz, 256);
+        if (bwd) {
+            L.dgeff = at;
+            at = round_up(at + sz, 256);
+            L.dbeff = at;
+            at = round_up(at + sz, 256);
+        }
+    }
     if (!bwd) {
         L.gcs = at;
         at = round_up(at + tok * p->Hv * sizeof(float), 256);
@@ -260,18 +281,26 @@ Layout layout_of(const gdr_problem *p, bool bwd, bool kept = false) {
     return L;
 }
 
-// The forward's decayed causal blocks and inverse q/k norms, kept for the backward (gdr_fwd_ex / gdr_bwd_ex):
-// [P: tokens x Hv x 64 (dtype)][rq: tokens x Hv fp32][rk: tokens x Hv fp32], 256-byte aligned parts; empty
-// when the problem runs the intra-GPU split (that path uses no P).
+// What the forward keeps for the backward (gdr_fwd_ex / gdr_bwd_ex), 256-byte aligned parts: without the
+// intra-GPU split ("blocks") the decayed causal blocks P [tokens x Hv x 64 (dtype)], the inverse q/k norms
+// rq, rk [tokens x Hv fp32], the states h and Delta of every chunk; with GDR_GATE_IN_KERNEL also sigmoid(-x)
+// of the raw gate [tokens x Hv fp32] (the derivative of the gate activation).  Empty otherwise.
 struct SavedLayout {
-    size_t P = 0, rq = 0, rk = 0, h = 0, delta = 0, bytes = 0;
+    size_t P = 0, rq = 0, rk = 0, h = 0, delta = 0, gate = 0, bytes = 0;
+    bool blocks = false;
 };
 SavedLayout saved_layout_of(const gdr_problem *p) {
     SavedLayout S;
-    if (choose_nseg(p) != 1) return S;
     const size_t tok = (size_t)p->B * p->T;
-    const size_t mc = (size_t)max_chunks_of(p);
     size_t at = 0;
+    if (p->flags & GDR_GATE_IN_KERNEL) {
+        S.gate = at;
+        at = round_up(at + tok * p->Hv * sizeof(float), 256);
+    }
+    S.bytes = at;
+    if (choose_nseg(p) != 1) return S;
+    S.blocks = true;
+    const size_t mc = (size_t)max_chunks_of(p);
     S.P = at;
     at = round_up(at + tok * p->Hv * C * esize(p->dtype), 256);
     S.rq = at;
@@ -311,6 +340,7 @@ Args make_args(const gdr_problem *p, unsigned *err) {
     a.cidx = a.coff = a.ctotal = nullptr;
     a.max_chunks = max_chunks_of(p);
     a.err = err;
+    a.flags = p->flags;
     {
         std::lock_guard<std::mutex> lk(g_mu);
         a.wait_polls = g_wait_polls;
@@ -330,11 +360,11 @@ gdr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_E
 // ---- per-kernel timing: event pairs recorded around each launch while enabled
 enum KernelId {
     K_PREP = 0, K_WY_FWD, K_CHAIN_FWD, K_CHAIN_FWD_RECOMPUTE, K_CHAIN_BWD, K_CHAIN_PAIR, K_BWD_CHUNK, K_CHUNK_P,
-    K_CHAIN_REV, K_COUNT
+    K_CHAIN_REV, K_GATE_ACT, K_COUNT
 };
 const char *const kKernelNames[K_COUNT] = {"prep_chunks", "wy_fwd",     "chain_fwd", "chain_fwd_recompute",
                                            "chain_bwd",   "chain_pair", "bwd_chunk", "chunk_p",
-                                           "chain_rev"};
+                                           "chain_rev",   "gate_act"};
 struct Pending {
     int id;
     cudaEvent_t a, b;
@@ -470,7 +500,7 @@ gdr_status gdr_fwd_ex(const gdr_problem *p, const void *q, const void *k, const 
     for (const void *x : ptrs)
         if (x && !aligned16(x)) return GDR_ERR_ALIGN;
     // with a saved buffer the states go there (one copy of them per call)
-    if (h && saved && saved_layout_of(p).bytes) return GDR_ERR_UNSUPPORTED;
+    if (h && saved && saved_layout_of(p).blocks) return GDR_ERR_UNSUPPORTED;
     const Layout L = layout_of(p, false, saved != nullptr);
     if ((st = check_ws(L, workspace, workspace_bytes)) != GDR_OK) return st;
     unsigned *err = nullptr;
@@ -479,12 +509,23 @@ gdr_status gdr_fwd_ex(const gdr_problem *p, const void *q, const void *k, const 
     char *ws = static_cast<char *>(workspace);
     Args a = make_args(p, err);
     if ((st = tables(p, a, ws, L, s)) != GDR_OK) return st;
+    const SavedLayout S = saved_layout_of(p);
+    if (p->flags & kActFlags) {
+        // the activated gate and beta (fp32) replace the raw ones for the rest of the pass
+        float *ge = reinterpret_cast<float *>(ws + L.geff), *be = reinterpret_cast<float *>(ws + L.beff);
+        float *sg = (saved && (p->flags & GDR_GATE_IN_KERNEL)) ? reinterpret_cast<float *>(static_cast<char *>(saved) + S.gate)
+                                                                : nullptr;
+        if ((st = timed(K_GATE_ACT, s, [&] { return launch_gate_act_fwd(a, g, beta, p->flags, ge, be, sg, s); })) != GDR_OK)
+            return st;
+        g = ge;
+        beta = be;
+        a.gate_f32 = true;
+    }
     float *gcs = g_cumsum ? g_cumsum : reinterpret_cast<float *>(ws + L.gcs);
     void *Aw = A ? A : static_cast<void *>(ws + L.A);
     const SegWs sw = seg_ws(L, ws);
     // P and the norms go to the caller's saved buffer when one is given (the backward then skips its P pass)
-    const SavedLayout S = saved_layout_of(p);
-    char *sv = (saved && S.bytes) ? static_cast<char *>(saved) : nullptr;
+    char *sv = (saved && S.blocks) ? static_cast<char *>(saved) : nullptr;
     void *Pw = sw.nseg == 1 ? static_cast<void *>(sv ? sv + S.P : ws + L.P) : nullptr;
     float *rqw = (sw.nseg == 1 && a.l2norm) ? reinterpret_cast<float *>(sv ? sv + S.rq : ws + L.rq) : nullptr;
     float *rkw = (sw.nseg == 1 && a.l2norm) ? reinterpret_cast<float *>(sv ? sv + S.rk : ws + L.rk) : nullptr;
@@ -523,6 +564,8 @@ gdr_status gdr_bwd_ex(const gdr_problem *p, const void *q, const void *k, const 
     const void *ptrs[] = {q, k, v, g_cumsum, beta, A, dout, dht, h0, dq, dk, dv, dg, dbeta, dh0, p->cu_seqlens, saved};
     for (const void *x : ptrs)
         if (x && !aligned16(x)) return GDR_ERR_ALIGN;
+    // the gate activation's derivative comes from the forward's saved buffer
+    if ((p->flags & GDR_GATE_IN_KERNEL) && !saved) return GDR_ERR_UNSUPPORTED;
     const Layout L = layout_of(p, true, saved != nullptr);
     if ((st = check_ws(L, workspace, workspace_bytes)) != GDR_OK) return st;
     unsigned *err = nullptr;
@@ -531,14 +574,27 @@ gdr_status gdr_bwd_ex(const gdr_problem *p, const void *q, const void *k, const 
     char *ws = static_cast<char *>(workspace);
     Args a = make_args(p, err);
     if ((st = tables(p, a, ws, L, s)) != GDR_OK) return st;
+    const Args a_raw = a;
+    const SavedLayout S = saved_layout_of(p);
+    void *dg_out = dg, *dbeta_out = dbeta;
+    const void *beta_raw = beta;
+    if (p->flags & kActFlags) {
+        // the pass runs on the activated beta and yields the gradients w.r.t. the activated g and beta (fp32)
+        float *be = reinterpret_cast<float *>(ws + L.beff);
+        if ((st = timed(K_GATE_ACT, s, [&] { return launch_gate_act_beta(a, beta, p->flags, be, s); })) != GDR_OK)
+            return st;
+        beta = be;
+        dg = ws + L.dgeff;
+        dbeta = ws + L.dbeff;
+        a.gate_f32 = true;
+    }
     void *hw = ws + L.h, *dhw = ws + L.dhn, *dlw = ws + L.delta, *ddlw = ws + L.ddelta;
     // states and Delta of every chunk (recomputed), the reverse state-gradient chain, then every
     // chunk's gradients in parallel
     const SegWs sw = seg_ws(L, ws);
     if (sw.nseg == 1) {
         // P and the norms: from the forward's saved buffer when given, else recomputed from g_cumsum
-        const SavedLayout S = saved_layout_of(p);
-        const char *sv = (saved && S.bytes) ? static_cast<const char *>(saved) : nullptr;
+        const char *sv = (saved && S.blocks) ? static_cast<const char *>(saved) : nullptr;
         void *Pw = sv ? const_cast<char *>(sv + S.P) : ws + L.P;
         float *rqw = a.l2norm ? reinterpret_cast<float *>(sv ? const_cast<char *>(sv + S.rq) : ws + L.rq) : nullptr;
         float *rkw = a.l2norm ? reinterpret_cast<float *>(sv ? const_cast<char *>(sv + S.rk) : ws + L.rk) : nullptr;
@@ -569,8 +625,19 @@ gdr_status gdr_bwd_ex(const gdr_problem *p, const void *q, const void *k, const 
                 })) != GDR_OK) {
         return st;
     }
-    return timed(K_BWD_CHUNK, s, [&] {
-        return launch_bwd_chunk_tc(a, q, k, v, g_cumsum, beta, A, dout, hw, dhw, dlw, ddlw, dq, dk, dv, dg, dbeta, s);
+    if ((st = timed(K_BWD_CHUNK, s, [&] {
+             return launch_bwd_chunk_tc(a, q, k, v, g_cumsum, beta, A, dout, hw, dhw, dlw, ddlw, dq, dk, dv, dg, dbeta,
+                                        s);
+         })) != GDR_OK)
+        return st;
+    if (!(p->flags & kActFlags)) return GDR_OK;
+    // gradients w.r.t. the raw gate and beta
+    const float *sg = (p->flags & GDR_GATE_IN_KERNEL)
+                          ? reinterpret_cast<const float *>(static_cast<const char *>(saved) + S.gate)
+                          : nullptr;
+    return timed(K_GATE_ACT, s, [&] {
+        return launch_gate_act_bwd(a_raw, static_cast<const float *>(dg), static_cast<const float *>(dbeta), sg,
+                                   beta_raw, p->flags, dg_out, dbeta_out, s);
     });
 }
 

@@ -466,6 +466,25 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                 f(F_IQ + (tid >> 6), tid & 63) = 1.f;  // F_IQ, F_IK, F_MQ, F_MK
             }
         }
+        if (upper) {
+            // <dH', h> over the whole state (both tiles share one layout, so equal offsets hold equal elements),
+            // on the upper-lane warps while round 1 runs (it reads only the loaded tiles); consecutive threads
+            // read consecutive 8-byte words (no bank conflicts)
+            const int ut = uw * 32 + lane;
+            float hd = 0.f;
+#pragma unroll 4
+            for (int u = 0; u < (DK * DV * 2 / 8) / (NT / 2); ++u) {
+                const uint32_t o = (uint32_t)(u * (NT / 2) + ut) * 8u;
+                const uint2 a = *reinterpret_cast<const uint2 *>(smem + S_H + o);
+                const uint2 b = *reinterpret_cast<const uint2 *>(smem + S_DH + o);
+                const float2 a0 = Elt<T>::unpack(a.x), a1 = Elt<T>::unpack(a.y);
+                const float2 b0 = Elt<T>::unpack(b.x), b1 = Elt<T>::unpack(b.y);
+                hd += a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, o);
+            if (lane == 0) f(F_HD, uw) = hd;
+        }
         if (!wait_mma()) {
             ok = false;
             break;
@@ -532,25 +551,6 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                 store16<T>(sb + wblk, r, (qc & 1) * 32 + c, x);
             }
             f(F_Z0 + qc, r) = z * f(F_IK, r);
-        }
-        if (upper) {
-            // <dH', h> over the whole state (both tiles share one layout, so equal offsets hold equal elements),
-            // on the upper-lane warps, whose round-1 epilogue is the shorter one; consecutive threads read
-            // consecutive 8-byte words (no bank conflicts)
-            const int ut = uw * 32 + lane;
-            float hd = 0.f;
-#pragma unroll 4
-            for (int u = 0; u < (DK * DV * 2 / 8) / (NT / 2); ++u) {
-                const uint32_t o = (uint32_t)(u * (NT / 2) + ut) * 8u;
-                const uint2 a = *reinterpret_cast<const uint2 *>(smem + S_H + o);
-                const uint2 b = *reinterpret_cast<const uint2 *>(smem + S_DH + o);
-                const float2 a0 = Elt<T>::unpack(a.x), a1 = Elt<T>::unpack(a.y);
-                const float2 b0 = Elt<T>::unpack(b.x), b1 = Elt<T>::unpack(b.y);
-                hd += a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, o);
-            if (lane == 0) f(F_HD, uw) = hd;
         }
         sync_tc();
 

@@ -331,6 +331,20 @@ inline Geo make_geo(const Args &a) {
     return g;
 }
 
+// Activations of the raw per-token gate and beta (GDR_GATE_IN_KERNEL, GDR_BETA_SIGMOID_IN_KERNEL,
+// GDR_ALLOW_NEG_EIGVAL): g = logsigmoid(x) = min(x, 0) - log(1 + e^{-|x|}); beta = sigmoid(b), doubled when
+// negative eigenvalues are allowed.
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + expf(-x)); }
+__device__ __forceinline__ float logsigmoid_f(float x) { return fminf(x, 0.f) - log1pf(expf(-fabsf(x))); }
+__device__ __forceinline__ float gate_of(float x, unsigned flags) {
+    return (flags & GDR_GATE_IN_KERNEL) ? logsigmoid_f(x) : x;
+}
+__device__ __forceinline__ float beta_of(float b, unsigned flags) {
+    if (flags & GDR_BETA_SIGMOID_IN_KERNEL) b = sigmoid_f(b);
+    if (flags & GDR_ALLOW_NEG_EIGVAL) b *= 2.f;
+    return b;
+}
+
 // Latch an error code in the device error word (the first code wins).
 __device__ __forceinline__ void raise_error(unsigned *err, unsigned code) {
     if (err) atomicCAS(err, 0u, code);

@@ -3,6 +3,8 @@
 // recurrence S_t = e^{g_t} S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T, o_t = scale S_t q_t), with
 // h = S^T [K x V] and k, q optionally L2-normalised:
 //
+// (g and beta after the optional activations of GDR_GATE_IN_KERNEL / GDR_BETA_SIGMOID_IN_KERNEL /
+// GDR_ALLOW_NEG_EIGVAL)
 //   u  = h^T k                         (V-vector)
 //   h <- e^{g} h + k (beta (v - e^{g} u))^T
 //   o  = scale h^T q
@@ -30,6 +32,7 @@ struct DecArgs {
     int B, T, Hq, Hv;
     float scale;
     bool gate_f32, l2norm, v_first;
+    unsigned flags;  // gate / beta activations
 };
 
 // Sum over the 256 threads of the block (fixed order: warp butterflies, then the eight warp sums).
@@ -88,7 +91,8 @@ __global__ void __launch_bounds__(2 * DN) decode_kernel(const DecArgs a) {
         const float qe = half == 0 ? Elt<T>::to_f(q[tk * DN + v]) : 0.f;
         const float ke = half == 0 ? Elt<T>::to_f(k[tk * DN + v]) : 0.f;
         const float ve = Elt<T>::to_f(vv[tv * DN + v]);
-        const float gt = load_gate<T>(a.g, tv, a.gate_f32), bt = load_gate<T>(a.beta, tv, a.gate_f32);
+        const float gt = gate_of(load_gate<T>(a.g, tv, a.gate_f32), a.flags);
+        const float bt = beta_of(load_gate<T>(a.beta, tv, a.gate_f32), a.flags);
         float rq = 1.f, rk = 1.f;
         if (a.l2norm) {
             rq = 1.0f / sqrtf(block_sum(qe * qe, red, lane, warp) + L2_EPS);
@@ -172,6 +176,7 @@ cudaError_t launch_decode(const Args &a, const void *q, const void *k, const voi
     d.gate_f32 = a.gate_f32;
     d.l2norm = a.l2norm;
     d.v_first = a.v_first;
+    d.flags = a.flags;
     return a.bf16 ? decode_t<__nv_bfloat16>(d, s) : decode_t<__half>(d, s);
 }
 

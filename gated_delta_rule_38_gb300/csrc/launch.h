@@ -23,6 +23,7 @@ struct Args {
     int64_t max_chunks;
     unsigned *err;           // device error word
     long long wait_polls;    // >= 0: poll budget of the waits that honour it (test support); < 0 = default
+    unsigned flags;          // the problem's GDR_* flags
 };
 
 // Workspace of the intra-GPU sequence split (nseg segments per sequence; nseg == 1: no split):
@@ -55,6 +56,16 @@ cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 // for zero states and may alias state_out); o [B,T,Hv,V].
 cudaError_t launch_decode(const Args &a, const void *q, const void *k, const void *v, const void *g,
                           const void *beta, const float *state_in, float *state_out, void *o, cudaStream_t s);
+
+// Gate and beta activations (GDR_GATE_IN_KERNEL, GDR_BETA_SIGMOID_IN_KERNEL, GDR_ALLOW_NEG_EIGVAL) over the
+// [tokens, Hv] scalars: the forward's activated g, beta (fp32) and sigmoid(-x) (sg, nullable); the backward's
+// activated beta; and the backward's gradients w.r.t. the raw g and beta (in the gate dtype) from those w.r.t.
+// the activated ones.  a.gate_f32 describes the raw tensors.
+cudaError_t launch_gate_act_fwd(const Args &a, const void *g, const void *beta, unsigned flags, float *geff,
+                                float *beff, float *sg, cudaStream_t s);
+cudaError_t launch_gate_act_beta(const Args &a, const void *beta, unsigned flags, float *beff, cudaStream_t s);
+cudaError_t launch_gate_act_bwd(const Args &a, const float *dgeff, const float *dbeff, const float *sg,
+                                const void *beta, unsigned flags, void *dg, void *dbeta, cudaStream_t s);
 
 cudaError_t launch_prep_chunks(const int32_t *cu, int N, int T, int chunk, int32_t *idx, int64_t max_chunks,
                                int32_t *off, int32_t *total, unsigned *err, cudaStream_t s);

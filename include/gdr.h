@@ -47,8 +47,8 @@ typedef enum gdr_status {
     GDR_ERR_NULL = 1,        /* a required pointer is NULL */
     GDR_ERR_SHAPE = 2,       /* K or V != 128, Hv % Hq != 0, B != 1 with cu_seqlens, negative sizes */
     GDR_ERR_DTYPE = 3,       /* fp32 or unknown q/k/v dtype, bad gate dtype */
-    GDR_ERR_UNSUPPORTED = 4, /* a rejected option (gate/beta activation in kernel, negative
-                                eigenvalues, multi-GPU sequence split) */
+    GDR_ERR_UNSUPPORTED = 4, /* a rejected option (multi-GPU sequence split), or an in-kernel gate
+                                backward without the forward's saved buffer */
     GDR_ERR_DEVICE = 5,      /* current device is not compute capability 10.3 */
     GDR_ERR_ALIGN = 6,       /* a tensor pointer is not 16-byte aligned */
     GDR_ERR_WORKSPACE = 7,   /* workspace NULL or smaller than the size query returns */
@@ -63,11 +63,23 @@ typedef enum gdr_dtype { GDR_BF16 = 0, GDR_FP16 = 1, GDR_FP32 = 2 } gdr_dtype;
 /* gdr_problem.flags */
 #define GDR_L2NORM_QK              (1u << 0)  /* use_qk_l2norm_in_kernel */
 #define GDR_STATE_V_FIRST          (1u << 1)  /* state tensors stored [..,V,K] */
-/* Options that the FlashQLA backend's verifier rejects (PR #998, review of the
- * verifier); requesting one returns GDR_ERR_UNSUPPORTED. */
+/* Activations of the raw per-token scalars inside the library (the options named by
+ * the FlashQLA backend's verifier, PR #998; the pages do not define them, this is the
+ * library's reading):
+ *   GDR_GATE_IN_KERNEL:         g holds raw gate logits x; the recurrence uses
+ *                               logsigmoid(x), the log of a sigmoid decay in (0, 1)
+ *   GDR_BETA_SIGMOID_IN_KERNEL: beta holds raw logits b; the recurrence uses sigmoid(b)
+ *   GDR_ALLOW_NEG_EIGVAL:       beta is doubled, so the eigenvalue 1 - beta of the
+ *                               transition along k spans (-1, 1)
+ * g_cumsum (forward output, backward input) is the cumsum of the activated gate; dg and
+ * dbeta are gradients w.r.t. the raw inputs.  The backward of GDR_GATE_IN_KERNEL needs
+ * the forward's saved buffer (gdr_fwd_ex / gdr_bwd_ex), which holds the activation's
+ * derivative; without it the backward returns GDR_ERR_UNSUPPORTED. */
 #define GDR_GATE_IN_KERNEL         (1u << 8)
 #define GDR_BETA_SIGMOID_IN_KERNEL (1u << 9)
 #define GDR_ALLOW_NEG_EIGVAL       (1u << 10)
+/* A sequence split across GPUs (rejected as the FlashQLA backend's verifier rejects
+ * it): GDR_ERR_UNSUPPORTED. */
 #define GDR_INTER_CARD_CP          (1u << 11)
 
 #define GDR_CHUNK 64
@@ -163,8 +175,9 @@ gdr_status gdr_bwd(const gdr_problem *p, const void *q, const void *k, const voi
  * rounding (the same quantities, computed by other kernels).  The buffer costs
  * memory: for B x T tokens and Hv heads about B*T*Hv*(128 + 8 + 2*128*128/64 + 2*128)
  * bytes at 16-bit data, i.e. about 0.9 KB per token and head.
- *   gdr_saved_bytes: bytes of the saved buffer for problem p (host-only; 0 when p
- *     runs the intra-GPU sequence split, which uses no P -- the buffer is then unused).
+ *   gdr_saved_bytes: bytes of the saved buffer for problem p (host-only; when p runs
+ *     the intra-GPU sequence split, which uses no P, only the in-kernel gate's part, so 0
+ *     without GDR_GATE_IN_KERNEL -- the buffer is then unused).
  *   saved: DEVICE buffer of at least gdr_saved_bytes bytes, 256-byte aligned, owned by
  *     the caller; NULL gives gdr_fwd / gdr_bwd exactly.  gdr_fwd_ex writes it;
  *     gdr_bwd_ex reads it and must get the buffer written by gdr_fwd_ex for the same

@@ -76,8 +76,7 @@ def fwd_call(lib, p, ptr=0x100000, ws=0x200000, ws_bytes=1 << 40, **over):
 @pytest.mark.parametrize("field,value,status", [
     ("K", 64, 2), ("V", 64, 2), ("Hv", 6, 2), ("T", -1, 2), ("B", 0, 2),
     ("dtype", _lib.GDR_FP32, 3), ("gate_dtype", _lib.GDR_FP16, 3),
-    ("flags", _lib.GDR_GATE_IN_KERNEL, 4), ("flags", _lib.GDR_BETA_SIGMOID_IN_KERNEL, 4),
-    ("flags", _lib.GDR_ALLOW_NEG_EIGVAL, 4), ("flags", _lib.GDR_INTER_CARD_CP, 4), ("flags", 1 << 20, 4),
+    ("flags", _lib.GDR_INTER_CARD_CP, 4), ("flags", 1 << 20, 4),
 ])
 def test_verifier_rejections(lib, fake_ptrs, field, value, status):
     p = prob(**{field: value})
@@ -208,3 +207,18 @@ def test_decode_host_checks(lib, fake_ptrs):
         has_gpu = False
     if not has_gpu:
         assert dec(prob(T=0), q=None, o=None) in (5, 10)
+
+
+def test_activation_options_are_accepted_and_the_gate_backward_needs_saved(lib, fake_ptrs):
+    """The gate / beta activation options pass the host checks; the in-kernel gate's backward without the
+    forward's saved buffer is refused (the activation's derivative lives there)."""
+    n = ctypes.c_size_t()
+    act = _lib.GDR_GATE_IN_KERNEL | _lib.GDR_BETA_SIGMOID_IN_KERNEL | _lib.GDR_ALLOW_NEG_EIGVAL
+    p = prob(flags=act)
+    assert lib.gdr_fwd_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0
+    assert lib.gdr_saved_bytes(ctypes.byref(p), ctypes.byref(n)) == 0 and n.value > 0
+    ps = prob(B=1, T=65536, Hq=16, Hv=16, num_segments=4, flags=_lib.GDR_GATE_IN_KERNEL)
+    assert lib.gdr_saved_bytes(ctypes.byref(ps), ctypes.byref(n)) == 0 and n.value == 65536 * 16 * 4
+    P = 0x100000
+    st = lib.gdr_bwd(ctypes.byref(p), P, P, P, P, P, P, P, None, None, P, P, P, P, P, None, 0x200000, 1 << 40, None)
+    assert st == 4
