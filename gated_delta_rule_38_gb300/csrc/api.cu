@@ -142,7 +142,7 @@ inline size_t esize(gdr_dtype d) { return d == GDR_FP32 ? 4 : 2; }
 
 gdr_status check_problem(const gdr_problem *p) {
     if (!p) return GDR_ERR_NULL;
-    if (p->K != DK || p->V != DV) return GDR_ERR_SHAPE;
+    if (p->K < 8 || p->K > DK || p->K % 8 || p->V < 8 || p->V > DV || p->V % 8) return GDR_ERR_SHAPE;
     if (p->B < 1 || p->T < 0 || p->Hq < 1 || p->Hv < 1 || p->Hv % p->Hq != 0) return GDR_ERR_SHAPE;
     if (p->cu_seqlens && (p->B != 1 || p->num_seqs < 1)) return GDR_ERR_SHAPE;
     if (p->num_segments < 0) return GDR_ERR_SHAPE;
@@ -315,6 +315,50 @@ SavedLayout saved_layout_of(const gdr_problem *p) {
     return S;
 }
 
+// Head dimensions below 128: the problem runs on zero-padded copies (pad.cu) through the K = V = 128 path.
+bool is_padded(const gdr_problem *p) { return p->K != DK || p->V != DV; }
+gdr_problem padded_problem(const gdr_problem *p) {
+    gdr_problem q = *p;
+    q.K = DK;
+    q.V = DV;
+    return q;
+}
+// Workspace of a padded call: [padded copies][the K = V = 128 call's own workspace].
+struct PadLayout {
+    size_t q = 0, k = 0, v = 0, o = 0, dout = 0, dq = 0, dk = 0, dv = 0, h0 = 0, fin = 0, dht = 0, dh0 = 0;
+    size_t inner = 0, bytes = 0;
+};
+PadLayout pad_layout_of(const gdr_problem *p, bool bwd, bool kept) {
+    PadLayout P;
+    const size_t tok = (size_t)p->B * p->T, e = esize(p->dtype);
+    const size_t qk = tok * p->Hq * DK * e, vv = tok * p->Hv * DV * e;
+    const size_t st = (size_t)num_seqs(p) * p->Hv * DK * DV * sizeof(float);
+    size_t at = 0;
+    auto take = [&](size_t &off, size_t n) {
+        off = at;
+        at = round_up(at + n, 256);
+    };
+    take(P.q, qk);
+    take(P.k, qk);
+    take(P.v, vv);
+    take(P.h0, st);
+    if (!bwd) {
+        take(P.o, vv);
+        take(P.fin, st);
+    } else {
+        take(P.dout, vv);
+        take(P.dq, qk);
+        take(P.dk, qk);
+        take(P.dv, vv);
+        take(P.dht, st);
+        take(P.dh0, st);
+    }
+    P.inner = at;
+    const gdr_problem p128 = padded_problem(p);
+    P.bytes = at + layout_of(&p128, bwd, kept).bytes;
+    return P;
+}
+
 SegWs seg_ws(const Layout &L, char *ws) {
     SegWs sw;
     sw.nseg = L.nseg;
@@ -330,6 +374,8 @@ Args make_args(const gdr_problem *p, unsigned *err) {
     a.T = p->T;
     a.Hq = p->Hq;
     a.Hv = p->Hv;
+    a.K = p->K;
+    a.V = p->V;
     a.N = num_seqs(p);
     a.bf16 = p->dtype == GDR_BF16;
     a.gate_f32 = p->gate_dtype == GDR_FP32;
@@ -360,11 +406,11 @@ gdr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_E
 // ---- per-kernel timing: event pairs recorded around each launch while enabled
 enum KernelId {
     K_PREP = 0, K_WY_FWD, K_CHAIN_FWD, K_CHAIN_FWD_RECOMPUTE, K_CHAIN_BWD, K_CHAIN_PAIR, K_BWD_CHUNK, K_CHUNK_P,
-    K_CHAIN_REV, K_GATE_ACT, K_COUNT
+    K_CHAIN_REV, K_GATE_ACT, K_PAD, K_COUNT
 };
 const char *const kKernelNames[K_COUNT] = {"prep_chunks", "wy_fwd",     "chain_fwd", "chain_fwd_recompute",
                                            "chain_bwd",   "chain_pair", "bwd_chunk", "chunk_p",
-                                           "chain_rev",   "gate_act"};
+                                           "chain_rev",   "gate_act",   "pad"};
 struct Pending {
     int id;
     cudaEvent_t a, b;
@@ -455,7 +501,7 @@ gdr_status gdr_fwd_workspace_size(const gdr_problem *p, size_t *bytes) {
     gdr_status st = check_problem(p);
     if (st != GDR_OK) return st;
     if (!bytes) return GDR_ERR_NULL;
-    *bytes = layout_of(p, false).bytes;
+    *bytes = is_padded(p) ? pad_layout_of(p, false, false).bytes : layout_of(p, false).bytes;
     return GDR_OK;
 }
 
@@ -463,7 +509,7 @@ gdr_status gdr_bwd_workspace_size(const gdr_problem *p, size_t *bytes) {
     gdr_status st = check_problem(p);
     if (st != GDR_OK) return st;
     if (!bytes) return GDR_ERR_NULL;
-    *bytes = layout_of(p, true).bytes;
+    *bytes = is_padded(p) ? pad_layout_of(p, true, false).bytes : layout_of(p, true).bytes;
     return GDR_OK;
 }
 
@@ -471,7 +517,7 @@ gdr_status gdr_saved_workspace_size(const gdr_problem *p, int backward, size_t *
     gdr_status st = check_problem(p);
     if (st != GDR_OK) return st;
     if (!bytes) return GDR_ERR_NULL;
-    *bytes = layout_of(p, backward != 0, true).bytes;
+    *bytes = is_padded(p) ? pad_layout_of(p, backward != 0, true).bytes : layout_of(p, backward != 0, true).bytes;
     return GDR_OK;
 }
 
@@ -479,7 +525,8 @@ gdr_status gdr_saved_bytes(const gdr_problem *p, size_t *bytes) {
     if (!bytes) return GDR_ERR_NULL;
     gdr_status st = check_problem(p);
     if (st != GDR_OK) return st;
-    *bytes = saved_layout_of(p).bytes;
+    const gdr_problem p128 = padded_problem(p);
+    *bytes = saved_layout_of(&p128).bytes;
     return GDR_OK;
 }
 
@@ -499,6 +546,40 @@ gdr_status gdr_fwd_ex(const gdr_problem *p, const void *q, const void *k, const 
     const void *ptrs[] = {q, k, v, g, beta, h0, o, final_state, g_cumsum, A, h, p->cu_seqlens, saved};
     for (const void *x : ptrs)
         if (x && !aligned16(x)) return GDR_ERR_ALIGN;
+    if (is_padded(p)) {
+        // zero-padded copies through the K = V = 128 path (the per-chunk states h are not offered here)
+        if (h) return GDR_ERR_UNSUPPORTED;
+        const PadLayout P = pad_layout_of(p, false, saved != nullptr);
+        if (!workspace || workspace_bytes < P.bytes) return GDR_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u) return GDR_ERR_ALIGN;
+        unsigned *err = nullptr;
+        if ((st = device_state(&err)) != GDR_OK) return st;
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        char *ws = static_cast<char *>(workspace);
+        const long long tok = (long long)p->B * p->T, nh = (long long)num_seqs(p) * p->Hv;
+        const bool vf = (p->flags & GDR_STATE_V_FIRST) != 0;
+        const int R = vf ? p->V : p->K, Cc = vf ? p->K : p->V;
+        if ((st = timed(K_PAD, s, [&] {
+                 cudaError_t e = launch_pad_rows(q, ws + P.q, tok * p->Hq, p->K, s);
+                 if (e == cudaSuccess) e = launch_pad_rows(k, ws + P.k, tok * p->Hq, p->K, s);
+                 if (e == cudaSuccess) e = launch_pad_rows(v, ws + P.v, tok * p->Hv, p->V, s);
+                 if (e == cudaSuccess && h0) e = launch_pad_state(h0, reinterpret_cast<float *>(ws + P.h0), nh, R, Cc, s);
+                 return e;
+             })) != GDR_OK)
+            return st;
+        const gdr_problem p128 = padded_problem(p);
+        if ((st = gdr_fwd_ex(&p128, ws + P.q, ws + P.k, ws + P.v, g, beta,
+                             h0 ? reinterpret_cast<const float *>(ws + P.h0) : nullptr, ws + P.o,
+                             final_state ? reinterpret_cast<float *>(ws + P.fin) : nullptr, g_cumsum, A, nullptr,
+                             ws + P.inner, workspace_bytes - P.inner, saved, stream)) != GDR_OK)
+            return st;
+        return timed(K_PAD, s, [&] {
+            cudaError_t e = launch_unpad_rows(ws + P.o, o, tok * p->Hv, p->V, s);
+            if (e == cudaSuccess && final_state)
+                e = launch_unpad_state(reinterpret_cast<const float *>(ws + P.fin), final_state, nh, R, Cc, s);
+            return e;
+        });
+    }
     // with a saved buffer the states go there (one copy of them per call)
     if (h && saved && saved_layout_of(p).blocks) return GDR_ERR_UNSUPPORTED;
     const Layout L = layout_of(p, false, saved != nullptr);
@@ -566,6 +647,44 @@ gdr_status gdr_bwd_ex(const gdr_problem *p, const void *q, const void *k, const 
         if (x && !aligned16(x)) return GDR_ERR_ALIGN;
     // the gate activation's derivative comes from the forward's saved buffer
     if ((p->flags & GDR_GATE_IN_KERNEL) && !saved) return GDR_ERR_UNSUPPORTED;
+    if (is_padded(p)) {
+        const PadLayout P = pad_layout_of(p, true, saved != nullptr);
+        if (!workspace || workspace_bytes < P.bytes) return GDR_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u) return GDR_ERR_ALIGN;
+        unsigned *err = nullptr;
+        if ((st = device_state(&err)) != GDR_OK) return st;
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        char *ws = static_cast<char *>(workspace);
+        const long long tok = (long long)p->B * p->T, nh = (long long)num_seqs(p) * p->Hv;
+        const bool vf = (p->flags & GDR_STATE_V_FIRST) != 0;
+        const int R = vf ? p->V : p->K, Cc = vf ? p->K : p->V;
+        if ((st = timed(K_PAD, s, [&] {
+                 cudaError_t e = launch_pad_rows(q, ws + P.q, tok * p->Hq, p->K, s);
+                 if (e == cudaSuccess) e = launch_pad_rows(k, ws + P.k, tok * p->Hq, p->K, s);
+                 if (e == cudaSuccess) e = launch_pad_rows(v, ws + P.v, tok * p->Hv, p->V, s);
+                 if (e == cudaSuccess) e = launch_pad_rows(dout, ws + P.dout, tok * p->Hv, p->V, s);
+                 if (e == cudaSuccess && h0) e = launch_pad_state(h0, reinterpret_cast<float *>(ws + P.h0), nh, R, Cc, s);
+                 if (e == cudaSuccess && dht)
+                     e = launch_pad_state(dht, reinterpret_cast<float *>(ws + P.dht), nh, R, Cc, s);
+                 return e;
+             })) != GDR_OK)
+            return st;
+        const gdr_problem p128 = padded_problem(p);
+        if ((st = gdr_bwd_ex(&p128, ws + P.q, ws + P.k, ws + P.v, g_cumsum, beta, A, ws + P.dout,
+                             dht ? reinterpret_cast<const float *>(ws + P.dht) : nullptr,
+                             h0 ? reinterpret_cast<const float *>(ws + P.h0) : nullptr, ws + P.dq, ws + P.dk,
+                             ws + P.dv, dg, dbeta, dh0 ? reinterpret_cast<float *>(ws + P.dh0) : nullptr,
+                             ws + P.inner, workspace_bytes - P.inner, saved, stream)) != GDR_OK)
+            return st;
+        return timed(K_PAD, s, [&] {
+            cudaError_t e = launch_unpad_rows(ws + P.dq, dq, tok * p->Hq, p->K, s);
+            if (e == cudaSuccess) e = launch_unpad_rows(ws + P.dk, dk, tok * p->Hq, p->K, s);
+            if (e == cudaSuccess) e = launch_unpad_rows(ws + P.dv, dv, tok * p->Hv, p->V, s);
+            if (e == cudaSuccess && dh0)
+                e = launch_unpad_state(reinterpret_cast<const float *>(ws + P.dh0), dh0, nh, R, Cc, s);
+            return e;
+        });
+    }
     const Layout L = layout_of(p, true, saved != nullptr);
     if ((st = check_ws(L, workspace, workspace_bytes)) != GDR_OK) return st;
     unsigned *err = nullptr;

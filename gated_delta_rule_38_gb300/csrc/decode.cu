@@ -9,6 +9,8 @@
 //   h <- e^{g} h + k (beta (v - e^{g} u))^T
 //   o  = scale h^T q
 //
+// Head dims K, V <= 128: threads of columns v >= V and state rows d >= K hold zeros (exact: zero key
+// coordinates and zero value columns stay zero through the update).
 // One CTA of 256 threads per (sequence, value head): threads v and v + 128 hold the two 64-row halves of
 // column v of h in fp32 registers, so u and o are dot products inside a thread plus one sum of two
 // halves, and every state row moves as one coalesced 512-byte access per half-block of threads (the
@@ -22,7 +24,7 @@
 namespace gdr {
 namespace {
 
-constexpr int DN = 128;  // K = V = 128: one thread per value column, one key row per state element
+constexpr int DN = 128;  // the largest head dim: one thread per value column, one key row per state element
 
 struct DecArgs {
     const void *q, *k, *v, *g, *beta;
@@ -30,6 +32,7 @@ struct DecArgs {
     float *state_out;       // may alias state_in
     void *o;
     int B, T, Hq, Hv;
+    int K, V;  // head dims (<= 128): threads v >= V and state rows d >= K carry zeros
     float scale;
     bool gate_f32, l2norm, v_first;
     unsigned flags;  // gate / beta activations
@@ -60,20 +63,22 @@ __global__ void __launch_bounds__(2 * DN) decode_kernel(const DecArgs a) {
     const int v = tid & (DN - 1), half = tid >> 7, d0 = half * HR;
     const int lane = tid & 31, warp = tid >> 5;
     const int hq = j / (a.Hv / a.Hq);
-    const size_t sbase = ((size_t)n * a.Hv + j) * DN * DN;
+    const int K = a.K, V = a.V;
+    const bool vc = v < V;  // this thread's value column exists
+    const size_t sbase = ((size_t)n * a.Hv + j) * K * V;
 
-    float h[HR];  // h[i] = h_{d0+i, v}
+    float h[HR];  // h[i] = h_{d0+i, v} (zero for rows d0+i >= K or columns v >= V)
     if (a.state_in) {
         if (a.v_first) {
-            const float4 *col = reinterpret_cast<const float4 *>(a.state_in + sbase + (size_t)v * DN + d0);
+            const float4 *col = reinterpret_cast<const float4 *>(a.state_in + sbase + (size_t)v * K + d0);
 #pragma unroll
             for (int i = 0; i < HR / 4; ++i) {
-                const float4 x = col[i];
+                const float4 x = (vc && d0 + 4 * i < K) ? col[i] : make_float4(0.f, 0.f, 0.f, 0.f);
                 h[4 * i] = x.x, h[4 * i + 1] = x.y, h[4 * i + 2] = x.z, h[4 * i + 3] = x.w;
             }
         } else {
 #pragma unroll
-            for (int i = 0; i < HR; ++i) h[i] = a.state_in[sbase + (size_t)(d0 + i) * DN + v];
+            for (int i = 0; i < HR; ++i) h[i] = (vc && d0 + i < K) ? a.state_in[sbase + (size_t)(d0 + i) * V + v] : 0.f;
         }
     } else {
 #pragma unroll
@@ -88,9 +93,9 @@ __global__ void __launch_bounds__(2 * DN) decode_kernel(const DecArgs a) {
         const long long tk = ((long long)n * a.T + t) * a.Hq + hq;  // token row of q, k
         const long long tv = ((long long)n * a.T + t) * a.Hv + j;   // token row of v, g, beta, o
         // the first half's threads bring q and k (element v); both halves need v, g and beta
-        const float qe = half == 0 ? Elt<T>::to_f(q[tk * DN + v]) : 0.f;
-        const float ke = half == 0 ? Elt<T>::to_f(k[tk * DN + v]) : 0.f;
-        const float ve = Elt<T>::to_f(vv[tv * DN + v]);
+        const float qe = (half == 0 && v < K) ? Elt<T>::to_f(q[tk * K + v]) : 0.f;
+        const float ke = (half == 0 && v < K) ? Elt<T>::to_f(k[tk * K + v]) : 0.f;
+        const float ve = vc ? Elt<T>::to_f(vv[tv * V + v]) : 0.f;
         const float gt = gate_of(load_gate<T>(a.g, tv, a.gate_f32), a.flags);
         const float bt = beta_of(load_gate<T>(a.beta, tv, a.gate_f32), a.flags);
         float rq = 1.f, rk = 1.f;
@@ -134,17 +139,20 @@ __global__ void __launch_bounds__(2 * DN) decode_kernel(const DecArgs a) {
         }
         po[half][v] = ov;
         __syncthreads();
-        if (half == 0) o[tv * DN + v] = Elt<T>::from_f(a.scale * (po[0][v] + po[1][v]));
+        if (half == 0 && vc) o[tv * V + v] = Elt<T>::from_f(a.scale * (po[0][v] + po[1][v]));
         __syncthreads();  // sq, sk, pu, po are rewritten by the next token
     }
 
+    if (!vc) return;
     if (a.v_first) {
-        float4 *col = reinterpret_cast<float4 *>(a.state_out + sbase + (size_t)v * DN + d0);
+        float4 *col = reinterpret_cast<float4 *>(a.state_out + sbase + (size_t)v * K + d0);
 #pragma unroll
-        for (int i = 0; i < HR / 4; ++i) col[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+        for (int i = 0; i < HR / 4; ++i)
+            if (d0 + 4 * i < K) col[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
     } else {
 #pragma unroll
-        for (int i = 0; i < HR; ++i) a.state_out[sbase + (size_t)(d0 + i) * DN + v] = h[i];
+        for (int i = 0; i < HR; ++i)
+            if (d0 + i < K) a.state_out[sbase + (size_t)(d0 + i) * V + v] = h[i];
     }
 }
 
@@ -172,6 +180,8 @@ cudaError_t launch_decode(const Args &a, const void *q, const void *k, const voi
     d.T = a.T;
     d.Hq = a.Hq;
     d.Hv = a.Hv;
+    d.K = a.K;
+    d.V = a.V;
     d.scale = a.scale;
     d.gate_f32 = a.gate_f32;
     d.l2norm = a.l2norm;

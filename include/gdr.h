@@ -23,7 +23,12 @@
  *   dg,dbeta [B,T,Hv]; A [B,T,Hv,64]; states [B,Hv,K,V].
  *   Packed variable-length batches (cu_seqlens != NULL): the same with B = 1
  *   and T = total tokens; states are [N,Hv,K,V] for the N sequences.
- * - K = V = 128 (GDR_ERR_SHAPE otherwise); Hv % Hq == 0.
+ * - 8 <= K, V <= 128 and multiples of 8 (GDR_ERR_SHAPE otherwise); Hv % Hq == 0.
+ *   The chunked kernels are built for K = V = 128; smaller head dims run on
+ *   zero-padded copies in the workspace (exact: zero coordinates stay zero), so
+ *   they cost about what K = V = 128 costs, and the optional per-chunk states h
+ *   are not offered for them (GDR_ERR_UNSUPPORTED).  The decode handles them
+ *   directly.
  * - dtype (q,k,v,o,A,h,dq,dk,dv) is bf16 or fp16 (fp32 -> GDR_ERR_DTYPE);
  *   gate_dtype (g,beta,dg,dbeta) is dtype or fp32.  States, final_state,
  *   initial_state, dht, dh0 and g_cumsum are fp32.
@@ -45,7 +50,7 @@ extern "C" {
 typedef enum gdr_status {
     GDR_OK = 0,
     GDR_ERR_NULL = 1,        /* a required pointer is NULL */
-    GDR_ERR_SHAPE = 2,       /* K or V != 128, Hv % Hq != 0, B != 1 with cu_seqlens, negative sizes */
+    GDR_ERR_SHAPE = 2,       /* K or V not in 8..128 step 8, Hv % Hq != 0, B != 1 with cu_seqlens, negative sizes */
     GDR_ERR_DTYPE = 3,       /* fp32 or unknown q/k/v dtype, bad gate dtype */
     GDR_ERR_UNSUPPORTED = 4, /* a rejected option (multi-GPU sequence split), or an in-kernel gate
                                 backward without the forward's saved buffer */
@@ -87,7 +92,7 @@ typedef enum gdr_dtype { GDR_BF16 = 0, GDR_FP16 = 1, GDR_FP32 = 2 } gdr_dtype;
 typedef struct gdr_problem {
     int B, T;                  /* batch rows and tokens per row (packed: B = 1, T = total) */
     int Hq, Hv;                /* q/k heads and value heads, Hv % Hq == 0 */
-    int K, V;                  /* head dims, both 128 */
+    int K, V;                  /* head dims, 8..128 in steps of 8 (128 is the native size) */
     gdr_dtype dtype;           /* q, k, v (and o, A, h, dq, dk, dv) */
     gdr_dtype gate_dtype;      /* g, beta (and dg, dbeta): dtype or GDR_FP32 */
     float scale;               /* output scale (K^-0.5 is the usual choice) */

@@ -74,7 +74,7 @@ def fwd_call(lib, p, ptr=0x100000, ws=0x200000, ws_bytes=1 << 40, **over):
 
 
 @pytest.mark.parametrize("field,value,status", [
-    ("K", 64, 2), ("V", 64, 2), ("Hv", 6, 2), ("T", -1, 2), ("B", 0, 2),
+    ("K", 60, 2), ("K", 256, 2), ("V", 4, 2), ("V", 0, 2), ("Hv", 6, 2), ("T", -1, 2), ("B", 0, 2),
     ("dtype", _lib.GDR_FP32, 3), ("gate_dtype", _lib.GDR_FP16, 3),
     ("flags", _lib.GDR_INTER_CARD_CP, 4), ("flags", 1 << 20, 4),
 ])
@@ -182,7 +182,7 @@ def test_saved_workspace_sizes(lib):
         assert full(ctypes.byref(ps), ctypes.byref(n)) == 0
         assert lib.gdr_saved_workspace_size(ctypes.byref(ps), backward, ctypes.byref(m)) == 0
         assert n.value == m.value
-    assert lib.gdr_saved_workspace_size(ctypes.byref(prob(K=64)), 1, ctypes.byref(m)) == 2
+    assert lib.gdr_saved_workspace_size(ctypes.byref(prob(K=60)), 1, ctypes.byref(m)) == 2
 
 
 def test_decode_host_checks(lib, fake_ptrs):
@@ -193,7 +193,7 @@ def test_decode_host_checks(lib, fake_ptrs):
         return lib.gdr_decode(ctypes.byref(p), q, P, P, P, P, None, out, o, None)
 
     assert dec(prob(T=1, cu_seqlens=P, B=1, num_seqs=2)) == 4   # packed rows: not a decode layout
-    assert dec(prob(T=1, K=64)) == 2
+    assert dec(prob(T=1, K=72, V=256)) == 2
     assert dec(prob(T=1), out=None) == 1
     assert dec(prob(T=1), o=None) == 1
     assert dec(prob(T=1), q=0x100008) == 6
@@ -222,3 +222,16 @@ def test_activation_options_are_accepted_and_the_gate_backward_needs_saved(lib, 
     P = 0x100000
     st = lib.gdr_bwd(ctypes.byref(p), P, P, P, P, P, P, P, None, None, P, P, P, P, P, None, 0x200000, 1 << 40, None)
     assert st == 4
+
+
+def test_smaller_head_dims_run_padded(lib):
+    """K or V below 128 are accepted; their workspaces hold zero-padded copies on top of the 128-wide ones."""
+    n, m = ctypes.c_size_t(), ctypes.c_size_t()
+    p128 = prob(B=2, T=256, Hq=4, Hv=4)
+    p64 = prob(B=2, T=256, Hq=4, Hv=4, K=64, V=64)
+    for backward, fn in ((0, lib.gdr_fwd_workspace_size), (1, lib.gdr_bwd_workspace_size)):
+        assert fn(ctypes.byref(p128), ctypes.byref(n)) == 0
+        assert fn(ctypes.byref(p64), ctypes.byref(m)) == 0
+        assert m.value > n.value
+    assert lib.gdr_saved_bytes(ctypes.byref(p64), ctypes.byref(m)) == 0
+    assert lib.gdr_saved_bytes(ctypes.byref(p128), ctypes.byref(n)) == 0 and m.value == n.value
