@@ -51,7 +51,8 @@ __device__ __forceinline__ float block_sum(float x, float *red, int lane, int wa
 
 // Two threads per value column: thread t holds rows 64 (t / 128) .. +63 of column t % 128 (64 registers, so
 // two CTAs of eight warps fit on an SM), and the two halves of each dot product meet in shared memory.
-template <typename T>
+// FULL: K = V = 128 (every mask below is compile-time true); otherwise the masks of smaller head dims.
+template <typename T, bool FULL>
 __global__ void __launch_bounds__(2 * DN) decode_kernel(const DecArgs a) {
     constexpr int HR = DN / 2;  // state rows per thread
     __shared__ __align__(16) float sq[DN];
@@ -63,8 +64,8 @@ __global__ void __launch_bounds__(2 * DN) decode_kernel(const DecArgs a) {
     const int v = tid & (DN - 1), half = tid >> 7, d0 = half * HR;
     const int lane = tid & 31, warp = tid >> 5;
     const int hq = j / (a.Hv / a.Hq);
-    const int K = a.K, V = a.V;
-    const bool vc = v < V;  // this thread's value column exists
+    const int K = FULL ? DN : a.K, V = FULL ? DN : a.V;
+    const bool vc = FULL || v < V;  // this thread's value column exists
     const size_t sbase = ((size_t)n * a.Hv + j) * K * V;
 
     float h[HR];  // h[i] = h_{d0+i, v} (zero for rows d0+i >= K or columns v >= V)
@@ -73,12 +74,13 @@ __global__ void __launch_bounds__(2 * DN) decode_kernel(const DecArgs a) {
             const float4 *col = reinterpret_cast<const float4 *>(a.state_in + sbase + (size_t)v * K + d0);
 #pragma unroll
             for (int i = 0; i < HR / 4; ++i) {
-                const float4 x = (vc && d0 + 4 * i < K) ? col[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 x = (vc && (FULL || d0 + 4 * i < K)) ? col[i] : make_float4(0.f, 0.f, 0.f, 0.f);
                 h[4 * i] = x.x, h[4 * i + 1] = x.y, h[4 * i + 2] = x.z, h[4 * i + 3] = x.w;
             }
         } else {
 #pragma unroll
-            for (int i = 0; i < HR; ++i) h[i] = (vc && d0 + i < K) ? a.state_in[sbase + (size_t)(d0 + i) * V + v] : 0.f;
+            for (int i = 0; i < HR; ++i)
+                h[i] = (vc && (FULL || d0 + i < K)) ? a.state_in[sbase + (size_t)(d0 + i) * V + v] : 0.f;
         }
     } else {
 #pragma unroll
@@ -93,8 +95,8 @@ __global__ void __launch_bounds__(2 * DN) decode_kernel(const DecArgs a) {
         const long long tk = ((long long)n * a.T + t) * a.Hq + hq;  // token row of q, k
         const long long tv = ((long long)n * a.T + t) * a.Hv + j;   // token row of v, g, beta, o
         // the first half's threads bring q and k (element v); both halves need v, g and beta
-        const float qe = (half == 0 && v < K) ? Elt<T>::to_f(q[tk * K + v]) : 0.f;
-        const float ke = (half == 0 && v < K) ? Elt<T>::to_f(k[tk * K + v]) : 0.f;
+        const float qe = (half == 0 && (FULL || v < K)) ? Elt<T>::to_f(q[tk * K + v]) : 0.f;
+        const float ke = (half == 0 && (FULL || v < K)) ? Elt<T>::to_f(k[tk * K + v]) : 0.f;
         const float ve = vc ? Elt<T>::to_f(vv[tv * V + v]) : 0.f;
         const float gt = gate_of(load_gate<T>(a.g, tv, a.gate_f32), a.flags);
         const float bt = beta_of(load_gate<T>(a.beta, tv, a.gate_f32), a.flags);
@@ -148,18 +150,22 @@ __global__ void __launch_bounds__(2 * DN) decode_kernel(const DecArgs a) {
         float4 *col = reinterpret_cast<float4 *>(a.state_out + sbase + (size_t)v * K + d0);
 #pragma unroll
         for (int i = 0; i < HR / 4; ++i)
-            if (d0 + 4 * i < K) col[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+            if (FULL || d0 + 4 * i < K) col[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
     } else {
 #pragma unroll
         for (int i = 0; i < HR; ++i)
-            if (d0 + i < K) a.state_out[sbase + (size_t)(d0 + i) * V + v] = h[i];
+            if (FULL || d0 + i < K) a.state_out[sbase + (size_t)(d0 + i) * V + v] = h[i];
     }
 }
 
 template <typename T>
 cudaError_t decode_t(const DecArgs &d, cudaStream_t s) {
     if (d.B == 0) return cudaSuccess;
-    decode_kernel<T><<<dim3((unsigned)((long long)d.Hv * d.B)), 2 * DN, 0, s>>>(d);
+    const dim3 grid((unsigned)((long long)d.Hv * d.B));
+    if (d.K == DN && d.V == DN)
+        decode_kernel<T, true><<<grid, 2 * DN, 0, s>>>(d);
+    else
+        decode_kernel<T, false><<<grid, 2 * DN, 0, s>>>(d);
     return cudaGetLastError();
 }
 
