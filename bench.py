@@ -9,8 +9,8 @@ q/k L2-normalised in the kernels.
 
 Prints one JSON line: the headline (tokens/s of exactly --steps timed steps),
 each direction's time, throughput and roofline fraction (inference forward,
-training forward, backward), the same per direction for the varlen, GVA and
-long workloads, per-kernel times, the end-to-end figure through host memory,
+training forward, backward), the same per direction for the varlen, GVA,
+long, activated-gate and head-dimension-64 workloads, per-kernel times, the end-to-end figure through host memory,
 the clocks under load and the fp64 oracle on the host cores.
 --impl reference times the oracle alone (a bounded sample of the workload).
 """
@@ -43,6 +43,10 @@ WORKLOAD_TEXT = {
     "gva": "GVA B=4 T=8192 Hq=16 Hv=32 K=V=128 fp16, initial and final states",
     "long": "long single sequence B=1 T=65536 H=16 K=V=128, slow decay, intra-GPU sequence split",
     "tiny": "tiny B=1 T=256 H=2 K=V=128",
+    "dense_act": "dense prefill B=2 T=4096 H=32 K=V=128 l2norm-in-kernel, raw gate and beta logits activated in "
+                 "the kernels (logsigmoid gate, sigmoid beta, negative eigenvalues allowed)",
+    "dense_hd64": "dense prefill B=2 T=4096 H=32 K=V=64 l2norm-in-kernel (run zero-padded to 128 in the chunked "
+                  "kernels; bytes and FLOPs counted at 64)",
 }
 
 
@@ -58,13 +62,13 @@ def peaks():
 def work(w):
     """Algorithmic FLOPs and bytes of each direction of one pass over workload ``w``.
 
-    FLOPs per token and value head (multiply-add = 2, C = 64, K = V = 128): forward Hq/Hv * 4CK + 2C(K+2V) +
+    FLOPs per token and value head (multiply-add = 2, C = 64, the workload's K and V): forward Hq/Hv * 4CK + 2C(K+2V) +
     6KV; backward twice the forward plus 4C^2.  Bytes: every tensor the direction must read or write once --
     forward-only (inference): q, k, v, g, beta in, o out (and the initial / final states when used); the
     training forward adds A (input dtype) and g_cumsum (fp32) out; the backward reads q, k, v, g_cumsum, beta,
     A, do (and h0, dht) and writes dq, dk, dv, dg, dbeta (and dh0).
     """
-    K = V = 128
+    K, V = w.K, w.V
     tok = w.tokens
     e = 2
     fwd_f = tok * (w.Hq * 4 * C * K + w.Hv * (2 * C * (K + 2 * V) + 6 * K * V))
@@ -203,24 +207,38 @@ def _inputs_on(w, seed, dev):
     return x, d, cu
 
 
+def act_options(w):
+    """The library's activation options for a workload whose gate and beta are raw logits."""
+    if not w.activations:
+        return {}
+    return dict(use_gate_in_kernel=True, use_beta_sigmoid_in_kernel=True, allow_neg_eigval=True)
+
+
+def saved_for(gdr, w, d, cu):
+    """The forward-to-backward buffer of workload ``w`` (reused by every step)."""
+    return gdr.saved_buffer(d["q"], d["v"], d["g"], cu_seqlens=cu, use_qk_l2norm_in_kernel=not w.host_l2,
+                            **act_options(w))
+
+
 def _make_step(gdr, w, cu, saved):
     l2 = not w.host_l2
+    act = act_options(w)
 
     def fwd(dd, save=True):
         if not save:
             return gdr.chunk_gated_delta_rule_fwd(
                 dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], initial_state=dd["h0"],
                 output_final_state=w.final_state, cu_seqlens=cu, use_qk_l2norm_in_kernel=l2,
-                save_for_backward=False)
+                save_for_backward=False, **act)
         return gdr.chunk_gated_delta_rule_fwd(
             dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], initial_state=dd["h0"],
-            output_final_state=w.final_state, cu_seqlens=cu, use_qk_l2norm_in_kernel=l2, saved=saved)
+            output_final_state=w.final_state, cu_seqlens=cu, use_qk_l2norm_in_kernel=l2, saved=saved, **act)
 
     def bwd(dd, f):
         gcs, A = f[0], f[1]
         return gdr.chunk_gated_delta_rule_bwd(
             dd["q"], dd["k"], dd["v"], gcs, dd["beta"], A, dd["do"], dht=dd["dht"], initial_state=dd["h0"],
-            cu_seqlens=cu, use_qk_l2norm_in_kernel=l2, saved=saved)
+            cu_seqlens=cu, use_qk_l2norm_in_kernel=l2, saved=saved, **act)
 
     def step(dd):
         f = fwd(dd)
@@ -281,7 +299,7 @@ def run_ours(args):
     x, d, cu = _inputs_on(w, rank_seed(rank), dev)  # every rank: its own batch (weak scaling, no collective)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     # the forward hands P, the q/k norms, its states and Delta to the backward (one buffer, reused by the steps)
-    saved = gdr.saved_buffer(d["q"], d["v"], d["g"], cu_seqlens=cu, use_qk_l2norm_in_kernel=not w.host_l2)
+    saved = saved_for(gdr, w, d, cu)
     fwd, bwd, step = _make_step(gdr, w, cu, saved)
     hbm, tf_burst, tf_sus, src = peaks()
 
@@ -393,7 +411,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "fp16", "data": "synthetic",
         "config": {"workload": WORKLOAD_TEXT.get(args.workload, args.workload),
-                   "B": w.B, "T": w.T, "Hq": w.Hq, "Hv": w.Hv, "chunk": C,
+                   "B": w.B, "T": w.T, "Hq": w.Hq, "Hv": w.Hv, "K": w.K, "V": w.V, "chunk": C,
                    "l2": "flushed between steps (256 MiB write outside the timed events)", "parallelism": "replicas"},
         "tflops": round((wk["fwd_flops"] + wk["bwd_flops"]) / (ms * 1e-3) / 1e12, 2),
         "directions": directions,
@@ -408,13 +426,12 @@ def run_ours(args):
     if world == 1 and not args.headline_only:
         del saved, bufs, hout
         configs = {}
-        for other in ("varlen", "gva", "long"):
+        for other in ("varlen", "gva", "long", "dense_act", "dense_hd64"):
             if other == args.workload:
                 continue
             wo = WORKLOADS[other]
             xo, do_, cuo = _inputs_on(wo, 42, dev)
-            svo = gdr.saved_buffer(do_["q"], do_["v"], do_["g"], cu_seqlens=cuo,
-                                   use_qk_l2norm_in_kernel=not wo.host_l2)
+            svo = saved_for(gdr, wo, do_, cuo)
             fo, bo, so = _make_step(gdr, wo, cuo, svo)
             for _ in range(max(3, args.warmup)):
                 so(do_)
@@ -443,7 +460,9 @@ def run_ours(args):
 def _oracle_sample(w, x, nh, nthreads):
     """fwd + bwd of the oracle over every token of ``w`` on its first ``nh`` value heads; returns seconds."""
     import oracle
-    pb = oracle.Problem(B=w.B, T=w.T, Hq=w.Hq, Hv=w.Hv, l2norm=not w.host_l2, cu_seqlens=w.cu_seqlens)
+    pb = oracle.Problem(B=w.B, T=w.T, Hq=w.Hq, Hv=w.Hv, K=w.K, V=w.V, l2norm=not w.host_l2,
+                        state_v_first=w.state_v_first, cu_seqlens=w.cu_seqlens, gate_in_kernel=w.activations,
+                        beta_sigmoid=w.activations, neg_eigval=w.activations)
     heads = list(range(nh))
     t0 = time.perf_counter()
     oracle.fwd(pb, x["q"], x["k"], x["v"], x["g"], x["beta"], h0=x["h0"], heads=heads, nthreads=nthreads)

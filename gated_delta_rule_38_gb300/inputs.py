@@ -13,6 +13,9 @@ dtype; the oracle reads the cast values):
   L2-norm option is then off), otherwise the kernel normalises them.
 * v ~ N(0, 1).
 * g = logsigmoid(N(mu_g, 1)) (a log-space decay <= 0); beta = sigmoid(N(0, 1)).
+  For the workloads marked ``activations`` the same draws are handed over
+  raw (g = N(mu_g, 1), beta = N(0, 1): the logits before the activations),
+  and they run with the in-kernel gate and beta activations.
 * h0 = 0.1 N(0, 1) in fp32 when the workload has an initial state.
 * do ~ N(0, 1); dht = 0.1 N(0, 1) in fp32 when the final state is an output.
 """
@@ -41,6 +44,7 @@ class Workload:
     state_v_first: bool = False
     mu_g: float = 0.0
     seq_lens: Optional[tuple] = None   # varlen: packed lengths (B must be 1)
+    activations: bool = False     # g, beta drawn as raw logits; run with the in-kernel activations
 
     @property
     def cu_seqlens(self) -> Optional[List[int]]:
@@ -60,8 +64,10 @@ class Workload:
         return self.B * self.T
 
 
-# The five workloads: a tiny correctness case, dense prefill, a packed
-# variable-length batch, grouped value attention and one long sequence.
+# The workloads: a tiny correctness case, dense prefill, a packed
+# variable-length batch, grouped value attention and one long sequence; and
+# two variants of dense prefill, one with raw gate / beta logits activated in
+# the kernels and one with head dimension 64.
 WORKLOADS: Dict[str, Workload] = {
     "tiny": Workload("tiny", B=1, T=256, Hq=2, Hv=2),
     "dense": Workload("dense", B=2, T=4096, Hq=32, Hv=32, host_l2=False, has_h0=False,
@@ -69,6 +75,10 @@ WORKLOADS: Dict[str, Workload] = {
     "varlen": Workload("varlen", B=1, T=5311, Hq=32, Hv=32, seq_lens=(512, 1024, 768, 3000, 7)),
     "gva": Workload("gva", B=4, T=8192, Hq=16, Hv=32, dtype=torch.float16),
     "long": Workload("long", B=1, T=65536, Hq=16, Hv=16, mu_g=2.0),
+    "dense_act": Workload("dense_act", B=2, T=4096, Hq=32, Hv=32, host_l2=False, has_h0=False,
+                          final_state=False, activations=True),
+    "dense_hd64": Workload("dense_hd64", B=2, T=4096, Hq=32, Hv=32, K=64, V=64, host_l2=False, has_h0=False,
+                           final_state=False),
 }
 
 
@@ -101,8 +111,11 @@ def make_inputs(w: Workload, seed: int = 42) -> Dict[str, torch.Tensor]:
         q = q / q.norm(dim=-1, keepdim=True)
         k = k / k.norm(dim=-1, keepdim=True)
     v = randn(B, T, w.Hv, w.V)
-    g = torch.nn.functional.logsigmoid(randn(B, T, w.Hv) + w.mu_g)
-    beta = torch.sigmoid(randn(B, T, w.Hv))
+    g = randn(B, T, w.Hv) + w.mu_g
+    beta = randn(B, T, w.Hv)
+    if not w.activations:
+        g = torch.nn.functional.logsigmoid(g)
+        beta = torch.sigmoid(beta)
     N = w.num_seqs
     sshape = (N, w.Hv, w.V, w.K) if w.state_v_first else (N, w.Hv, w.K, w.V)
     h0 = 0.1 * randn(*sshape) if w.has_h0 else None

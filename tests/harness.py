@@ -27,9 +27,17 @@ def np64(t) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
+def act_options(w: Workload) -> dict:
+    """The library's activation options for a workload whose gate and beta are raw logits."""
+    if not w.activations:
+        return {}
+    return dict(use_gate_in_kernel=True, use_beta_sigmoid_in_kernel=True, allow_neg_eigval=True)
+
+
 def oracle_problem(w: Workload, kernel_l2: bool) -> oracle.Problem:
     return oracle.Problem(B=w.B, T=w.T, Hq=w.Hq, Hv=w.Hv, K=w.K, V=w.V, l2norm=kernel_l2,
-                          state_v_first=w.state_v_first, cu_seqlens=w.cu_seqlens)
+                          state_v_first=w.state_v_first, cu_seqlens=w.cu_seqlens, gate_in_kernel=w.activations,
+                          beta_sigmoid=w.activations, neg_eigval=w.activations)
 
 
 def to_dev(x, dev="cuda"):
@@ -48,7 +56,7 @@ def gpu_fwd(w: Workload, d, kernel_l2: bool, output_h=False, num_segments=0, gat
     return gdr.chunk_gated_delta_rule_fwd(
         d["q"], d["k"], d["v"], g, beta, initial_state=d["h0"], output_final_state=w.final_state,
         cu_seqlens=cu_tensor(w), use_qk_l2norm_in_kernel=kernel_l2, state_v_first=w.state_v_first,
-        num_segments=num_segments, output_h=output_h, saved=saved)
+        num_segments=num_segments, output_h=output_h, saved=saved, **act_options(w))
 
 
 def gpu_bwd(w: Workload, d, gcs, A, kernel_l2: bool, num_segments=0, gate_f32=False, saved=None):
@@ -57,7 +65,7 @@ def gpu_bwd(w: Workload, d, gcs, A, kernel_l2: bool, num_segments=0, gate_f32=Fa
     return gdr.chunk_gated_delta_rule_bwd(
         d["q"], d["k"], d["v"], gcs, beta, A, d["do"], dht=d["dht"], initial_state=d["h0"],
         cu_seqlens=cu_tensor(w), use_qk_l2norm_in_kernel=kernel_l2, state_v_first=w.state_v_first,
-        num_segments=num_segments, saved=saved)
+        num_segments=num_segments, saved=saved, **act_options(w))
 
 
 def gpu_saved(w: Workload, d, kernel_l2: bool, num_segments=0, gate_f32=False):
@@ -65,4 +73,4 @@ def gpu_saved(w: Workload, d, kernel_l2: bool, num_segments=0, gate_f32=False):
     import gated_delta_rule_38_gb300 as gdr
     g = d["g"].float() if gate_f32 else d["g"]
     return gdr.saved_buffer(d["q"], d["v"], g, cu_seqlens=cu_tensor(w), use_qk_l2norm_in_kernel=kernel_l2,
-                            state_v_first=w.state_v_first, num_segments=num_segments)
+                            state_v_first=w.state_v_first, num_segments=num_segments, **act_options(w))
