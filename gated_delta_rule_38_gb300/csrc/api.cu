@@ -315,7 +315,10 @@ SavedLayout saved_layout_of(const gdr_problem *p) {
     return S;
 }
 
-// Head dimensions below 128: the problem runs on zero-padded copies (pad.cu) through the K = V = 128 path.
+// Head dimensions below 128 run through the K = V = 128 path: the kernels read the token tensors through TMA
+// boxes that load zeros past K / V (so their 128-wide tiles see zero-padded rows) and clip their stores there;
+// the fp32 states, which the kernels address directly, are copied to and from zero-padded 128 x 128 blocks
+// (pad.cu).  Zero padding is exact for this recurrence (pad.cu).
 bool is_padded(const gdr_problem *p) { return p->K != DK || p->V != DV; }
 gdr_problem padded_problem(const gdr_problem *p) {
     gdr_problem q = *p;
@@ -323,33 +326,23 @@ gdr_problem padded_problem(const gdr_problem *p) {
     q.V = DV;
     return q;
 }
-// Workspace of a padded call: [padded copies][the K = V = 128 call's own workspace].
+// Workspace of a call with small head dims: [padded states][the K = V = 128 call's own workspace].
 struct PadLayout {
-    size_t q = 0, k = 0, v = 0, o = 0, dout = 0, dq = 0, dk = 0, dv = 0, h0 = 0, fin = 0, dht = 0, dh0 = 0;
+    size_t h0 = 0, fin = 0, dht = 0, dh0 = 0;
     size_t inner = 0, bytes = 0;
 };
 PadLayout pad_layout_of(const gdr_problem *p, bool bwd, bool kept) {
     PadLayout P;
-    const size_t tok = (size_t)p->B * p->T, e = esize(p->dtype);
-    const size_t qk = tok * p->Hq * DK * e, vv = tok * p->Hv * DV * e;
     const size_t st = (size_t)num_seqs(p) * p->Hv * DK * DV * sizeof(float);
     size_t at = 0;
     auto take = [&](size_t &off, size_t n) {
         off = at;
         at = round_up(at + n, 256);
     };
-    take(P.q, qk);
-    take(P.k, qk);
-    take(P.v, vv);
     take(P.h0, st);
     if (!bwd) {
-        take(P.o, vv);
         take(P.fin, st);
     } else {
-        take(P.dout, vv);
-        take(P.dq, qk);
-        take(P.dk, qk);
-        take(P.dv, vv);
         take(P.dht, st);
         take(P.dh0, st);
     }
@@ -537,6 +530,15 @@ gdr_status gdr_fwd(const gdr_problem *p, const void *q, const void *k, const voi
                       stream);
 }
 
+static gdr_status fwd_core(const gdr_problem *p, int tk, int tv, const void *q, const void *k, const void *v,
+                           const void *g, const void *beta, const float *h0, void *o, float *final_state,
+                           float *g_cumsum, void *A, void *h, void *workspace, size_t workspace_bytes, void *saved,
+                           void *stream);
+static gdr_status bwd_core(const gdr_problem *p, int tk, int tv, const void *q, const void *k, const void *v,
+                           const float *g_cumsum, const void *beta, const void *A, const void *dout, const float *dht,
+                           const float *h0, void *dq, void *dk, void *dv, void *dg, void *dbeta, float *dh0,
+                           void *workspace, size_t workspace_bytes, const void *saved, void *stream);
+
 gdr_status gdr_fwd_ex(const gdr_problem *p, const void *q, const void *k, const void *v, const void *g,
                       const void *beta, const float *h0, void *o, float *final_state, float *g_cumsum, void *A,
                       void *h, void *workspace, size_t workspace_bytes, void *saved, void *stream) {
@@ -547,7 +549,8 @@ gdr_status gdr_fwd_ex(const gdr_problem *p, const void *q, const void *k, const 
     for (const void *x : ptrs)
         if (x && !aligned16(x)) return GDR_ERR_ALIGN;
     if (is_padded(p)) {
-        // zero-padded copies through the K = V = 128 path (the per-chunk states h are not offered here)
+        // the K = V = 128 path on the caller's token tensors, with zero-padded states (the per-chunk states h
+        // are not offered here)
         if (h) return GDR_ERR_UNSUPPORTED;
         const PadLayout P = pad_layout_of(p, false, saved != nullptr);
         if (!workspace || workspace_bytes < P.bytes) return GDR_ERR_WORKSPACE;
@@ -556,30 +559,34 @@ gdr_status gdr_fwd_ex(const gdr_problem *p, const void *q, const void *k, const 
         if ((st = device_state(&err)) != GDR_OK) return st;
         cudaStream_t s = static_cast<cudaStream_t>(stream);
         char *ws = static_cast<char *>(workspace);
-        const long long tok = (long long)p->B * p->T, nh = (long long)num_seqs(p) * p->Hv;
+        const long long nh = (long long)num_seqs(p) * p->Hv;
         const bool vf = (p->flags & GDR_STATE_V_FIRST) != 0;
         const int R = vf ? p->V : p->K, Cc = vf ? p->K : p->V;
-        if ((st = timed(K_PAD, s, [&] {
-                 cudaError_t e = launch_pad_rows(q, ws + P.q, tok * p->Hq, p->K, s);
-                 if (e == cudaSuccess) e = launch_pad_rows(k, ws + P.k, tok * p->Hq, p->K, s);
-                 if (e == cudaSuccess) e = launch_pad_rows(v, ws + P.v, tok * p->Hv, p->V, s);
-                 if (e == cudaSuccess && h0) e = launch_pad_state(h0, reinterpret_cast<float *>(ws + P.h0), nh, R, Cc, s);
-                 return e;
-             })) != GDR_OK)
+        if (h0 && (st = timed(K_PAD, s, [&] {
+                       return launch_pad_state(h0, reinterpret_cast<float *>(ws + P.h0), nh, R, Cc, s);
+                   })) != GDR_OK)
             return st;
         const gdr_problem p128 = padded_problem(p);
-        if ((st = gdr_fwd_ex(&p128, ws + P.q, ws + P.k, ws + P.v, g, beta,
-                             h0 ? reinterpret_cast<const float *>(ws + P.h0) : nullptr, ws + P.o,
-                             final_state ? reinterpret_cast<float *>(ws + P.fin) : nullptr, g_cumsum, A, nullptr,
-                             ws + P.inner, workspace_bytes - P.inner, saved, stream)) != GDR_OK)
+        if ((st = fwd_core(&p128, p->K, p->V, q, k, v, g, beta, h0 ? reinterpret_cast<const float *>(ws + P.h0) : nullptr,
+                           o, final_state ? reinterpret_cast<float *>(ws + P.fin) : nullptr, g_cumsum, A, nullptr,
+                           ws + P.inner, workspace_bytes - P.inner, saved, stream)) != GDR_OK)
             return st;
+        if (!final_state) return GDR_OK;
         return timed(K_PAD, s, [&] {
-            cudaError_t e = launch_unpad_rows(ws + P.o, o, tok * p->Hv, p->V, s);
-            if (e == cudaSuccess && final_state)
-                e = launch_unpad_state(reinterpret_cast<const float *>(ws + P.fin), final_state, nh, R, Cc, s);
-            return e;
+            return launch_unpad_state(reinterpret_cast<const float *>(ws + P.fin), final_state, nh, R, Cc, s);
         });
     }
+    return fwd_core(p, p->K, p->V, q, k, v, g, beta, h0, o, final_state, g_cumsum, A, h, workspace, workspace_bytes,
+                    saved, stream);
+}
+
+// The K = V = 128 forward; tk, tv: the head dims of the token tensors (below 128 they are read through boxes that
+// load zeros past them, and o is stored clipped to tv columns).
+static gdr_status fwd_core(const gdr_problem *p, int tk, int tv, const void *q, const void *k, const void *v,
+                           const void *g, const void *beta, const float *h0, void *o, float *final_state,
+                           float *g_cumsum, void *A, void *h, void *workspace, size_t workspace_bytes, void *saved,
+                           void *stream) {
+    gdr_status st;
     // with a saved buffer the states go there (one copy of them per call)
     if (h && saved && saved_layout_of(p).blocks) return GDR_ERR_UNSUPPORTED;
     const Layout L = layout_of(p, false, saved != nullptr);
@@ -589,6 +596,8 @@ gdr_status gdr_fwd_ex(const gdr_problem *p, const void *q, const void *k, const 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
     Args a = make_args(p, err);
+    a.K = tk;
+    a.V = tv;
     if ((st = tables(p, a, ws, L, s)) != GDR_OK) return st;
     const SavedLayout S = saved_layout_of(p);
     if (p->flags & kActFlags) {
@@ -648,6 +657,7 @@ gdr_status gdr_bwd_ex(const gdr_problem *p, const void *q, const void *k, const 
     // the gate activation's derivative comes from the forward's saved buffer
     if ((p->flags & GDR_GATE_IN_KERNEL) && !saved) return GDR_ERR_UNSUPPORTED;
     if (is_padded(p)) {
+        // the K = V = 128 path on the caller's token tensors, with zero-padded states
         const PadLayout P = pad_layout_of(p, true, saved != nullptr);
         if (!workspace || workspace_bytes < P.bytes) return GDR_ERR_WORKSPACE;
         if (reinterpret_cast<uintptr_t>(workspace) & 255u) return GDR_ERR_ALIGN;
@@ -655,36 +665,40 @@ gdr_status gdr_bwd_ex(const gdr_problem *p, const void *q, const void *k, const 
         if ((st = device_state(&err)) != GDR_OK) return st;
         cudaStream_t s = static_cast<cudaStream_t>(stream);
         char *ws = static_cast<char *>(workspace);
-        const long long tok = (long long)p->B * p->T, nh = (long long)num_seqs(p) * p->Hv;
+        const long long nh = (long long)num_seqs(p) * p->Hv;
         const bool vf = (p->flags & GDR_STATE_V_FIRST) != 0;
         const int R = vf ? p->V : p->K, Cc = vf ? p->K : p->V;
-        if ((st = timed(K_PAD, s, [&] {
-                 cudaError_t e = launch_pad_rows(q, ws + P.q, tok * p->Hq, p->K, s);
-                 if (e == cudaSuccess) e = launch_pad_rows(k, ws + P.k, tok * p->Hq, p->K, s);
-                 if (e == cudaSuccess) e = launch_pad_rows(v, ws + P.v, tok * p->Hv, p->V, s);
-                 if (e == cudaSuccess) e = launch_pad_rows(dout, ws + P.dout, tok * p->Hv, p->V, s);
-                 if (e == cudaSuccess && h0) e = launch_pad_state(h0, reinterpret_cast<float *>(ws + P.h0), nh, R, Cc, s);
-                 if (e == cudaSuccess && dht)
-                     e = launch_pad_state(dht, reinterpret_cast<float *>(ws + P.dht), nh, R, Cc, s);
-                 return e;
-             })) != GDR_OK)
+        if ((h0 || dht) && (st = timed(K_PAD, s, [&] {
+                                cudaError_t e = cudaSuccess;
+                                if (h0) e = launch_pad_state(h0, reinterpret_cast<float *>(ws + P.h0), nh, R, Cc, s);
+                                if (e == cudaSuccess && dht)
+                                    e = launch_pad_state(dht, reinterpret_cast<float *>(ws + P.dht), nh, R, Cc, s);
+                                return e;
+                            })) != GDR_OK)
             return st;
         const gdr_problem p128 = padded_problem(p);
-        if ((st = gdr_bwd_ex(&p128, ws + P.q, ws + P.k, ws + P.v, g_cumsum, beta, A, ws + P.dout,
-                             dht ? reinterpret_cast<const float *>(ws + P.dht) : nullptr,
-                             h0 ? reinterpret_cast<const float *>(ws + P.h0) : nullptr, ws + P.dq, ws + P.dk,
-                             ws + P.dv, dg, dbeta, dh0 ? reinterpret_cast<float *>(ws + P.dh0) : nullptr,
-                             ws + P.inner, workspace_bytes - P.inner, saved, stream)) != GDR_OK)
+        if ((st = bwd_core(&p128, p->K, p->V, q, k, v, g_cumsum, beta, A, dout,
+                           dht ? reinterpret_cast<const float *>(ws + P.dht) : nullptr,
+                           h0 ? reinterpret_cast<const float *>(ws + P.h0) : nullptr, dq, dk, dv, dg, dbeta,
+                           dh0 ? reinterpret_cast<float *>(ws + P.dh0) : nullptr, ws + P.inner,
+                           workspace_bytes - P.inner, saved, stream)) != GDR_OK)
             return st;
+        if (!dh0) return GDR_OK;
         return timed(K_PAD, s, [&] {
-            cudaError_t e = launch_unpad_rows(ws + P.dq, dq, tok * p->Hq, p->K, s);
-            if (e == cudaSuccess) e = launch_unpad_rows(ws + P.dk, dk, tok * p->Hq, p->K, s);
-            if (e == cudaSuccess) e = launch_unpad_rows(ws + P.dv, dv, tok * p->Hv, p->V, s);
-            if (e == cudaSuccess && dh0)
-                e = launch_unpad_state(reinterpret_cast<const float *>(ws + P.dh0), dh0, nh, R, Cc, s);
-            return e;
+            return launch_unpad_state(reinterpret_cast<const float *>(ws + P.dh0), dh0, nh, R, Cc, s);
         });
     }
+    return bwd_core(p, p->K, p->V, q, k, v, g_cumsum, beta, A, dout, dht, h0, dq, dk, dv, dg, dbeta, dh0, workspace,
+                    workspace_bytes, saved, stream);
+}
+
+// The K = V = 128 backward; tk, tv: the head dims of the token tensors (below 128 they are read through boxes that
+// load zeros past them, and dq, dk, dv are stored clipped to them).
+static gdr_status bwd_core(const gdr_problem *p, int tk, int tv, const void *q, const void *k, const void *v,
+                           const float *g_cumsum, const void *beta, const void *A, const void *dout, const float *dht,
+                           const float *h0, void *dq, void *dk, void *dv, void *dg, void *dbeta, float *dh0,
+                           void *workspace, size_t workspace_bytes, const void *saved, void *stream) {
+    gdr_status st;
     const Layout L = layout_of(p, true, saved != nullptr);
     if ((st = check_ws(L, workspace, workspace_bytes)) != GDR_OK) return st;
     unsigned *err = nullptr;
@@ -692,6 +706,8 @@ gdr_status gdr_bwd_ex(const gdr_problem *p, const void *q, const void *k, const 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char *ws = static_cast<char *>(workspace);
     Args a = make_args(p, err);
+    a.K = tk;
+    a.V = tv;
     if ((st = tables(p, a, ws, L, s)) != GDR_OK) return st;
     const Args a_raw = a;
     const SavedLayout S = saved_layout_of(p);
@@ -793,7 +809,7 @@ const char *gdr_status_string(gdr_status s) {
     switch (s) {
         case GDR_OK: return "ok";
         case GDR_ERR_NULL: return "a required pointer is NULL";
-        case GDR_ERR_SHAPE: return "unsupported shape (K and V must be 128, Hv % Hq == 0, B == 1 with cu_seqlens)";
+        case GDR_ERR_SHAPE: return "unsupported shape (K and V multiples of 8 in [8, 128], Hv % Hq == 0, B == 1 with cu_seqlens)";
         case GDR_ERR_DTYPE: return "unsupported dtype (q/k/v must be bf16 or fp16; gates the same or fp32)";
         case GDR_ERR_UNSUPPORTED: return "unsupported option";
         case GDR_ERR_DEVICE: return "the current device is not compute capability 10.3 (sm_103a)";

@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
         if (!staged && r >= valid_) return;
         const float inv = p.l2norm ? f(upper ? F_IK : F_IQ, r) : 1.f;
         const float dot = p.l2norm ? inv * inv * ((dp[L] + dp[128 + L]) + (dp[256 + L] + dp[384 + L])) : 0.f;
-        T *dst = static_cast<T *>(upper ? p.dk : p.dq) + ((tok0_ + r) * Hq + hq_) * DK + qc * 32;
+        T *dst = static_cast<T *>(upper ? p.dk : p.dq) + ((tok0_ + r) * Hq + hq_) * geo.K + qc * 32;
         const uint32_t stg = sb + (upper ? ((qc >> 1) ? S_DW1 : S_DS) : ((qc >> 1) ? S_DW0 : S_X));
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                                      (acc[c * 8 + 2 * e + 1] - xv[2 * e + 1] * dot) * inv);
             if (staged)
                 umma::st_shared_v4(stg + umma::off(r, xc + c * 8, 0), o4[0], o4[1], o4[2], o4[3]);
-            else
+            else if (qc * 32 + c * 8 < geo.K)
                 *reinterpret_cast<uint4 *>(dst + c * 8) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
         }
     };
@@ -579,7 +579,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             float vd = 0.f, kd = 0.f;
             // dDelta-side: ddelta = A^T dDelta (columns 0..127), A^T dW (128..255)
             const float br = f(F_B, r);
-            T *dvrow = static_cast<T *>(p.dv) + ((tok0 + r) * Hv + j) * DV + qc * 32;
+            T *dvrow = static_cast<T *>(p.dv) + ((tok0 + r) * Hv + j) * geo.V + qc * 32;
 #pragma unroll
             for (int c = 0; c < 32; c += 16) {
                 float x[16], y[16], vv[16], kv[16];
@@ -602,8 +602,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                     umma::st_shared_v4(stg + umma::off(r, col, 0), w[0], w[1], w[2], w[3]);
                     umma::st_shared_v4(stg + umma::off(r, col + 8, 0), w[4], w[5], w[6], w[7]);
                 } else if (r < valid) {
-                    *reinterpret_cast<uint4 *>(dvrow + c) = make_uint4(w[0], w[1], w[2], w[3]);
-                    *reinterpret_cast<uint4 *>(dvrow + c + 8) = make_uint4(w[4], w[5], w[6], w[7]);
+                    if (qc * 32 + c < geo.V) *reinterpret_cast<uint4 *>(dvrow + c) = make_uint4(w[0], w[1], w[2], w[3]);
+                    if (qc * 32 + c + 8 < geo.V)
+                        *reinterpret_cast<uint4 *>(dvrow + c + 8) = make_uint4(w[4], w[5], w[6], w[7]);
                 }
             }
             f(F_VD0 + qc, r) = vd;
@@ -613,7 +614,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
                 asm volatile("bar.sync 2, 256;\n" ::: "memory");  // the eight lower-lane warps
                 if (tid == ST) {
                     tma::store3d(&p.tdv, 0, j, (int)tok0, sb + S_DW0);
-                    tma::store3d(&p.tdv, 64, j, (int)tok0, sb + S_DW1);
+                    if (geo.V > 64) tma::store3d(&p.tdv, 64, j, (int)tok0, sb + S_DW1);
                     tma::commit_group();
                 }
             }
@@ -767,7 +768,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
             if (tid == ST) {
                 if (valid == C) {
                     tma::store3d(&p.tdq, 0, hq, (int)tok0, sb + S_X);
-                    tma::store3d(&p.tdq, 64, hq, (int)tok0, sb + S_DW0);
+                    if (geo.K > 64) tma::store3d(&p.tdq, 64, hq, (int)tok0, sb + S_DW0);
                     tma::commit_group();
                 }
                 if (wn >= 0) issue(nxt, jn, 5);  // the q tile has been read for the last time
@@ -841,7 +842,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
         __syncthreads();
         if (tid == ST && last_head && valid == C) {
             tma::store3d(&p.tdk, 0, hq, (int)tok0, sb + S_DS);
-            tma::store3d(&p.tdk, 64, hq, (int)tok0, sb + S_DW1);
+            if (geo.K > 64) tma::store3d(&p.tdk, 64, hq, (int)tok0, sb + S_DW1);
             tma::commit_group();
         }
         if (wn < 0) break;
@@ -882,18 +883,15 @@ cudaError_t launch_bwd_chunk_tc(const Args &a, const void *q, const void *k, con
     BcP p;
     const uint64_t tokens = (uint64_t)a.B * (uint64_t)a.T, rows = (uint64_t)a.max_chunks * a.Hv;
     const bool bf = a.bf16;
-    if (!make_tmap_3d(&p.tq, q, bf, DK, a.Hq, tokens, DK * 2, (uint64_t)a.Hq * DK * 2, 64, 1, 64) ||
-        !make_tmap_3d(&p.tk, k, bf, DK, a.Hq, tokens, DK * 2, (uint64_t)a.Hq * DK * 2, 64, 1, 64) ||
-        !make_tmap_3d(&p.tdo, dout, bf, DV, a.Hv, tokens, DV * 2, (uint64_t)a.Hv * DV * 2, 64, 1, 64) ||
-        !make_tmap_3d(&p.tv, v, bf, DV, a.Hv, tokens, DV * 2, (uint64_t)a.Hv * DV * 2, 64, 1, 64) ||
+    if (!make_token_map(&p.tq, q, bf, a.K, a.Hq, tokens, 64) || !make_token_map(&p.tk, k, bf, a.K, a.Hq, tokens, 64) ||
+        !make_token_map(&p.tdo, dout, bf, a.V, a.Hv, tokens, 64) || !make_token_map(&p.tv, v, bf, a.V, a.Hv, tokens, 64) ||
         !make_tmap_3d(&p.ta, A, bf, C, a.Hv, tokens, C * 2, (uint64_t)a.Hv * C * 2, 64, 1, 64) ||
         !make_tmap_3d(&p.th, h, bf, DV, DK, rows, DV * 2, (uint64_t)DK * DV * 2, 64, 128, 1) ||
         !make_tmap_3d(&p.tdh, dhn, bf, DV, DK, rows, DV * 2, (uint64_t)DK * DV * 2, 64, 128, 1) ||
         !make_tmap_3d(&p.td, delta, bf, DV, C, rows, DV * 2, (uint64_t)C * DV * 2, 64, 64, 1) ||
         !make_tmap_3d(&p.tdd, ddelta, bf, DV, C, rows, DV * 2, (uint64_t)C * DV * 2, 64, 64, 1) ||
-        !make_tmap_3d(&p.tdq, dq, bf, DK, a.Hq, tokens, DK * 2, (uint64_t)a.Hq * DK * 2, 64, 1, 64) ||
-        !make_tmap_3d(&p.tdk, dk, bf, DK, a.Hq, tokens, DK * 2, (uint64_t)a.Hq * DK * 2, 64, 1, 64) ||
-        !make_tmap_3d(&p.tdv, dv, bf, DV, a.Hv, tokens, DV * 2, (uint64_t)a.Hv * DV * 2, 64, 1, 64))
+        !make_token_map(&p.tdq, dq, bf, a.K, a.Hq, tokens, 64) || !make_token_map(&p.tdk, dk, bf, a.K, a.Hq, tokens, 64) ||
+        !make_token_map(&p.tdv, dv, bf, a.V, a.Hv, tokens, 64))
         return cudaErrorInvalidValue;
     p.q = q;
     p.k = k;

@@ -440,8 +440,8 @@ __device__ __forceinline__ void chain_fwd_body(const Geo &geo, const TcP &p, con
                 for (int u = 0; u < 16; ++u) S[c + u] = eg * S[c + u] + x[u];
             }
             if (WRITE_O) {
-                T *o = static_cast<T *>(p.o) + ((tok0 + (long long)i * C + qq * EW) * Hv + j) * DV + e;
-                const long long ostride = (long long)Hv * DV;
+                T *o = static_cast<T *>(p.o) + ((tok0 + (long long)i * C + qq * EW) * Hv + j) * geo.V + e;
+                const long long ostride = (long long)Hv * geo.V;
 #pragma unroll
                 for (int c = 0; c < EW; c += 16) {
                     float x1[16], x2[16];
@@ -451,7 +451,8 @@ __device__ __forceinline__ void chain_fwd_body(const Geo &geo, const TcP &p, con
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
                         const int r = qq * EW + c + u;
-                        if (r < valid) o[(c + u) * ostride] = Elt<T>::from_f(p.scale * (fEG[r] * x1[u] + x2[u]));
+                        if (r < valid && e < geo.V)
+                            o[(c + u) * ostride] = Elt<T>::from_f(p.scale * (fEG[r] * x1[u] + x2[u]));
                     }
                 }
             }
@@ -897,16 +898,14 @@ namespace {
 
 // [tokens][heads][cols] map with 64 x 1 x 64 boxes
 bool tile_map(CUtensorMap *m, const void *base, const Args &a, int heads, int cols) {
-    const uint64_t tokens = (uint64_t)a.B * (uint64_t)a.T;
-    return make_tmap_3d(m, base, a.bf16, (uint64_t)cols, (uint64_t)heads, tokens, (uint64_t)cols * 2,
-                        (uint64_t)heads * cols * 2, 64, 1, 64);
+    return make_token_map(m, base, a.bf16, cols, heads, (uint64_t)a.B * (uint64_t)a.T, 64);
 }
 
 TcBwdP bwd_params(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta, const void *A,
                   const void *dout, const float *dht, void *dhn, void *ddelta, float *dh0, const SegWs &sw) {
     TcBwdP p;
     p.nseg = -1;  // marks a failed tensor-map encoding
-    if (!tile_map(&p.tq, q, a, a.Hq, DK) || !tile_map(&p.tk, k, a, a.Hq, DK) || !tile_map(&p.tdo, dout, a, a.Hv, DV) ||
+    if (!tile_map(&p.tq, q, a, a.Hq, a.K) || !tile_map(&p.tk, k, a, a.Hq, a.K) || !tile_map(&p.tdo, dout, a, a.Hv, a.V) ||
         !tile_map(&p.ta, A, a, a.Hv, C))
         return p;
     p.q = q;
@@ -935,7 +934,7 @@ TcP fwd_params(const Args &a, const void *q, const void *k, const void *v, const
                const SegWs &sw) {
     TcP p;
     p.nseg = -1;  // marks a failed tensor-map encoding
-    if (!tile_map(&p.tq, q, a, a.Hq, DK) || !tile_map(&p.tk, k, a, a.Hq, DK) || !tile_map(&p.tv, v, a, a.Hv, DV) ||
+    if (!tile_map(&p.tq, q, a, a.Hq, a.K) || !tile_map(&p.tk, k, a, a.Hq, a.K) || !tile_map(&p.tv, v, a, a.Hv, a.V) ||
         !tile_map(&p.ta, A, a, a.Hv, C))
         return p;
     p.q = q;

@@ -709,7 +709,7 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
             umma::fence_after();
             const uint32_t tD = b ? L::T_D1 : L::T_D0, tPD = b ? L::T_PD1 : L::T_PD0;
             const float cq = fa(lc, FCQ)[r];  // scale rq e^G of this row (0 past the end)
-            T *orow = static_cast<T *>(p.o) + ((tok0 + (long long)lc * C + r) * Hv + j) * DV + v0;
+            T *orow = static_cast<T *>(p.o) + ((tok0 + (long long)lc * C + r) * Hv + j) * geo.V + v0;
             // a full chunk's rows leave through the staging tile, this warp's 32 rows as one TMA box (scattered
             // row stores would crowd the memory instruction queue of the schedulers the state warps share);
             // a ragged chunk's rows are stored directly (its tail rows belong to the next sequence)
@@ -735,8 +735,8 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                     st_v4(ost + (uint32_t)(c >> 6) * 8192u + umma::off(r, (c & 63), 0), w0, w1, w2, w3);
                     st_v4(ost + (uint32_t)(c >> 6) * 8192u + umma::off(r, (c & 63) + 8, 0), w4, w5, w6, w7);
                 } else if (r < valid) {
-                    *reinterpret_cast<uint4 *>(orow + c) = make_uint4(w0, w1, w2, w3);
-                    *reinterpret_cast<uint4 *>(orow + c + 8) = make_uint4(w4, w5, w6, w7);
+                    if (v0 + c < geo.V) *reinterpret_cast<uint4 *>(orow + c) = make_uint4(w0, w1, w2, w3);
+                    if (v0 + c + 8 < geo.V) *reinterpret_cast<uint4 *>(orow + c + 8) = make_uint4(w4, w5, w6, w7);
                 }
             }
             umma::fence_before();
@@ -748,7 +748,8 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                     const int t0 = (int)(tok0 + (long long)lc * C) + (warp - 2) * 32;
 #pragma unroll
                     for (int cb = 0; cb < BV; cb += 64)
-                        tma::store3d(&p.to, v0 + cb, j, t0, ost + (uint32_t)(cb >> 6) * 8192u + (warp - 2) * 4096);
+                        if (v0 + cb < geo.V)
+                            tma::store3d(&p.to, v0 + cb, j, t0, ost + (uint32_t)(cb >> 6) * 8192u + (warp - 2) * 4096);
                     tma::commit_group();
                 }
             }
@@ -1260,9 +1261,7 @@ __global__ void __launch_bounds__(WS_NT, 1) chain_ws_pair_kernel(Geo geo, const 
 }
 
 bool ws_map(CUtensorMap *m, const void *base, const Args &a, int heads, int cols) {
-    const uint64_t tokens = (uint64_t)a.B * (uint64_t)a.T;
-    return make_tmap_3d(m, base, a.bf16, (uint64_t)cols, (uint64_t)heads, tokens, (uint64_t)cols * 2,
-                        (uint64_t)heads * cols * 2, 64, 1, 64);
+    return make_token_map(m, base, a.bf16, cols, heads, (uint64_t)a.B * (uint64_t)a.T, 64);
 }
 
 // Per-chunk tiles [rows x Hv][rows_per][128 columns] (states, Delta and their gradients), 64 x 32 boxes.
@@ -1307,9 +1306,9 @@ cudaError_t launch_chain_ws_pair(const Args &a, const void *q, const void *k, co
                                  void *dhn, void *ddelta, float *dh0, cudaStream_t s) {
     WsP pf;
     RevP pb;
-    if (!ws_map(&pf.tq, q, a, a.Hq, DK) || !ws_map(&pf.tk, k, a, a.Hq, DK) || !ws_map(&pf.tv, v, a, a.Hv, DV) ||
-        !ws_map(&pf.ta, A, a, a.Hv, C) || !ws_map(&pb.tq, q, a, a.Hq, DK) || !ws_map(&pb.tk, k, a, a.Hq, DK) ||
-        !ws_map(&pb.tdo, dout, a, a.Hv, DV) || !ws_map(&pb.tp, P, a, a.Hv, C) || !ws_map(&pb.ta, A, a, a.Hv, C))
+    if (!ws_map(&pf.tq, q, a, a.Hq, a.K) || !ws_map(&pf.tk, k, a, a.Hq, a.K) || !ws_map(&pf.tv, v, a, a.Hv, a.V) ||
+        !ws_map(&pf.ta, A, a, a.Hv, C) || !ws_map(&pb.tq, q, a, a.Hq, a.K) || !ws_map(&pb.tk, k, a, a.Hq, a.K) ||
+        !ws_map(&pb.tdo, dout, a, a.Hv, a.V) || !ws_map(&pb.tp, P, a, a.Hv, C) || !ws_map(&pb.ta, A, a, a.Hv, C))
         return cudaErrorInvalidValue;
     pf.tp = pb.tp;
     pf.tma_h = h != nullptr;
@@ -1351,7 +1350,7 @@ cudaError_t launch_chain_rev(const Args &a, const void *q, const void *k, const 
                              const void *A, const void *P, const float *rq, const float *rk, const void *dout,
                              const float *dht, void *dhn, void *ddelta, float *dh0, cudaStream_t s) {
     RevP pb;
-    if (!ws_map(&pb.tq, q, a, a.Hq, DK) || !ws_map(&pb.tk, k, a, a.Hq, DK) || !ws_map(&pb.tdo, dout, a, a.Hv, DV) ||
+    if (!ws_map(&pb.tq, q, a, a.Hq, a.K) || !ws_map(&pb.tk, k, a, a.Hq, a.K) || !ws_map(&pb.tdo, dout, a, a.Hv, a.V) ||
         !ws_map(&pb.tp, P, a, a.Hv, C) || !ws_map(&pb.ta, A, a, a.Hv, C) ||
         (dhn && !box_map(&pb.tdh, dhn, a, DK)) || (ddelta && !box_map(&pb.tdd, ddelta, a, C)))
         return cudaErrorInvalidValue;
@@ -1376,9 +1375,9 @@ cudaError_t launch_chain_ws(const Args &a, const void *q, const void *k, const v
                             bool h_vfirst, void *delta, cudaStream_t s) {
     WsP p;
     const uint64_t tokens = (uint64_t)a.B * (uint64_t)a.T;
-    if (!ws_map(&p.tq, q, a, a.Hq, DK) || !ws_map(&p.tk, k, a, a.Hq, DK) || !ws_map(&p.tv, v, a, a.Hv, DV) ||
+    if (!ws_map(&p.tq, q, a, a.Hq, a.K) || !ws_map(&p.tk, k, a, a.Hq, a.K) || !ws_map(&p.tv, v, a, a.Hv, a.V) ||
         !ws_map(&p.ta, A, a, a.Hv, C) || (o && !ws_map(&p.tp, P, a, a.Hv, C)) ||
-        (o && !make_tmap_3d(&p.to, o, a.bf16, DV, a.Hv, tokens, DV * 2, (uint64_t)a.Hv * DV * 2, 64, 1, 32)))
+        (o && !make_token_map(&p.to, o, a.bf16, a.V, a.Hv, tokens, 32)))
         return cudaErrorInvalidValue;
     p.g_cs = g_cs;
     p.rq = rq;

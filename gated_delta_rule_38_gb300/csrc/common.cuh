@@ -278,6 +278,7 @@ __device__ __forceinline__ void load_rows_async(const Tile &t, const T *src, lon
 
 struct Geo {
     int B, T, Hq, Hv, N;
+    int K, V;                 // head dims of the token tensors (the tiles are 128 wide; columns >= K / V are zero)
     const int32_t *cu;        // nullptr = dense
     const int32_t *cidx;      // varlen chunk table [*,2]
     const int32_t *coff;      // varlen chunk offsets [N+1]
@@ -323,6 +324,8 @@ inline Geo make_geo(const Args &a) {
     g.Hq = a.Hq;
     g.Hv = a.Hv;
     g.N = a.N;
+    g.K = a.K;
+    g.V = a.V;
     g.cu = a.cu;
     g.cidx = a.cidx;
     g.coff = a.coff;

@@ -11,7 +11,8 @@ namespace gdr {
 // Everything a kernel needs to address one problem's tensors.
 struct Args {
     int B, T, Hq, Hv, N;
-    int K, V;         // head dims (the chunked kernels run with 128 / 128; the decode takes any <= 128)
+    int K, V;         // head dims of the token tensors (the chunked kernels' tiles are 128 wide and load zeros past
+                      // them; the decode takes any <= 128)
     bool bf16;        // element type of q,k,v,... (else fp16)
     bool gate_f32;    // g, beta (dg, dbeta) are fp32
     bool l2norm;
@@ -68,10 +69,8 @@ cudaError_t launch_gate_act_beta(const Args &a, const void *beta, unsigned flags
 cudaError_t launch_gate_act_bwd(const Args &a, const float *dgeff, const float *dbeff, const float *sg,
                                 const void *beta, unsigned flags, void *dg, void *dbeta, cudaStream_t s);
 
-// Zero padding of head dimensions below 128 (pad.cu): token tensors [rows, D] <-> [rows, 128] (16-bit, D a
-// multiple of 8), fp32 states [nh, R, Cc] <-> [nh, 128, 128] (Cc a multiple of 4).
-cudaError_t launch_pad_rows(const void *src, void *dst, long long rows, int D, cudaStream_t s);
-cudaError_t launch_unpad_rows(const void *src, void *dst, long long rows, int D, cudaStream_t s);
+// Zero padding of head dimensions below 128 (pad.cu): fp32 states [nh, R, Cc] <-> [nh, 128, 128] (Cc a
+// multiple of 4).
 cudaError_t launch_pad_state(const float *src, float *dst, long long nh, int R, int Cc, cudaStream_t s);
 cudaError_t launch_unpad_state(const float *src, float *dst, long long nh, int R, int Cc, cudaStream_t s);
 

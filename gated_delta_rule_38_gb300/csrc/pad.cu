@@ -1,9 +1,9 @@
-// Head dimensions below 128: the chunked kernels are written for K = V = 128, so problems with smaller K or V
-// run on zero-padded copies.  Padding is exact for this recurrence: zero key coordinates leave k.k, q.k and
-// the L2 norms unchanged and keep the state's padded rows zero; zero value coordinates keep its padded columns
-// zero; so the padded outputs hold the true ones in their leading K / V coordinates and zeros elsewhere.
-// These kernels copy token tensors [rows, D] <-> [rows, 128] (16-bit elements, D a multiple of 8) and state
-// tensors [NH, R, Cc] <-> [NH, 128, 128] (fp32, Cc a multiple of 4), zero-filling on the way in.
+// Head dimensions below 128: the chunked kernels are written for K = V = 128 and run smaller problems as if
+// zero-padded.  Padding is exact for this recurrence: zero key coordinates leave k.k, q.k and the L2 norms
+// unchanged and keep the state's padded rows zero; zero value coordinates keep its padded columns zero; so
+// the padded outputs hold the true ones in their leading K / V coordinates and zeros elsewhere.  The token
+// tensors need no copies (the kernels' TMA boxes load zeros past K / V); these kernels copy the fp32 state
+// tensors [NH, R, Cc] <-> [NH, 128, 128] (Cc a multiple of 4), zero-filling on the way in.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -15,27 +15,6 @@ namespace {
 inline unsigned grid_for(long long n) {
     const long long b = (n + 255) / 256;
     return (unsigned)(b < 8192 ? (b > 0 ? b : 1) : 8192);
-}
-
-// One thread per 16-byte group of the padded row (16 per row).
-__global__ void pad_rows_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst, long long rows, int d8) {
-    griddep_wait();
-    const long long n = rows * 16;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-        const long long r = i >> 4;
-        const int c = (int)(i & 15);
-        dst[i] = c < d8 ? src[r * d8 + c] : make_uint4(0u, 0u, 0u, 0u);
-    }
-}
-
-__global__ void unpad_rows_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst, long long rows, int d8) {
-    griddep_wait();
-    const long long n = rows * d8;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-        const long long r = i / d8;
-        const int c = (int)(i - r * d8);
-        dst[i] = src[r * 16 + c];
-    }
 }
 
 // fp32 states: one thread per float4 of the padded [128][128] matrix.
@@ -62,20 +41,6 @@ __global__ void unpad_state_kernel(const float4 *__restrict__ src, float4 *__res
 }
 
 }  // namespace
-
-cudaError_t launch_pad_rows(const void *src, void *dst, long long rows, int D, cudaStream_t s) {
-    if (rows == 0) return cudaSuccess;
-    pad_rows_kernel<<<grid_for(rows * 16), 256, 0, s>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst),
-                                                         rows, D / 8);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_unpad_rows(const void *src, void *dst, long long rows, int D, cudaStream_t s) {
-    if (rows == 0) return cudaSuccess;
-    unpad_rows_kernel<<<grid_for(rows * (D / 8)), 256, 0, s>>>(static_cast<const uint4 *>(src),
-                                                                static_cast<uint4 *>(dst), rows, D / 8);
-    return cudaGetLastError();
-}
 
 cudaError_t launch_pad_state(const float *src, float *dst, long long nh, int R, int Cc, cudaStream_t s) {
     if (nh == 0) return cudaSuccess;

@@ -12,4 +12,13 @@ namespace gdr {
 bool make_tmap_3d(CUtensorMap *map, const void *base, bool bf16, uint64_t dim0, uint64_t dim1, uint64_t dim2,
                   uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1, uint32_t box2);
 
+// A token tensor [tokens][heads][cols] (16-bit, cols a multiple of 8) read or written in boxes of 64 columns x
+// 1 head x box_tok tokens.  Head dimensions below 128 are described with their own column count, so boxes at
+// columns >= cols load zeros (the kernels' tiles are 128 columns wide) and stores clip there.
+inline bool make_token_map(CUtensorMap *map, const void *base, bool bf16, int cols, int heads, uint64_t tokens,
+                           uint32_t box_tok) {
+    return make_tmap_3d(map, base, bf16, (uint64_t)cols, (uint64_t)heads, tokens, (uint64_t)cols * 2,
+                        (uint64_t)heads * cols * 2, 64, 1, box_tok);
+}
+
 }  // namespace gdr

@@ -467,8 +467,7 @@ cudaError_t launch_wy_fwd(const Args &a, const void *q, const void *k, const voi
     WyP p;
     const uint64_t tokens = (uint64_t)a.B * (uint64_t)a.T;
     const bool bf = a.bf16;
-    if (!make_tmap_3d(&p.tq, q, bf, DK, a.Hq, tokens, DK * 2, (uint64_t)a.Hq * DK * 2, 64, 1, 64) ||
-        !make_tmap_3d(&p.tk, k, bf, DK, a.Hq, tokens, DK * 2, (uint64_t)a.Hq * DK * 2, 64, 1, 64))
+    if (!make_token_map(&p.tq, q, bf, a.K, a.Hq, tokens, 64) || !make_token_map(&p.tk, k, bf, a.K, a.Hq, tokens, 64))
         return cudaErrorInvalidValue;
     if (P && !make_tmap_3d(&p.tp, P, bf, C, a.Hv, tokens, C * 2, (uint64_t)a.Hv * C * 2, 64, 1, 64))
         return cudaErrorInvalidValue;

@@ -24,11 +24,13 @@
  *   Packed variable-length batches (cu_seqlens != NULL): the same with B = 1
  *   and T = total tokens; states are [N,Hv,K,V] for the N sequences.
  * - 8 <= K, V <= 128 and multiples of 8 (GDR_ERR_SHAPE otherwise); Hv % Hq == 0.
- *   The chunked kernels are built for K = V = 128; smaller head dims run on
- *   zero-padded copies in the workspace (exact: zero coordinates stay zero), so
- *   they cost about what K = V = 128 costs, and the optional per-chunk states h
- *   are not offered for them (GDR_ERR_UNSUPPORTED).  The decode handles them
- *   directly.
+ *   The chunked kernels are built for K = V = 128; smaller head dims run as if
+ *   zero-padded (exact: zero coordinates stay zero): the token tensors are read
+ *   in place through tiles that load zeros past K / V and written clipped to
+ *   them, and only the fp32 states are copied to zero-padded 128 x 128 blocks
+ *   in the workspace.  They cost about what K = V = 128 costs, and the optional
+ *   per-chunk states h are not offered for them (GDR_ERR_UNSUPPORTED).  The
+ *   decode handles them directly.
  * - dtype (q,k,v,o,A,h,dq,dk,dv) is bf16 or fp16 (fp32 -> GDR_ERR_DTYPE);
  *   gate_dtype (g,beta,dg,dbeta) is dtype or fp32.  States, final_state,
  *   initial_state, dht, dh0 and g_cumsum are fp32.
