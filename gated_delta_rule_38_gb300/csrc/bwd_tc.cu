@@ -66,9 +66,10 @@ template <typename T> struct IsBf16 { static constexpr bool value = false; };
 template <> struct IsBf16<__nv_bfloat16> { static constexpr bool value = true; };
 
 struct BcP {
-    // TMA maps: q, k [tokens][Hq][128]; dO, v [tokens][Hv][128]; A [tokens][Hv][64];
+    // TMA maps: q, k [tokens][Hq][K]; dO, v [tokens][Hv][V]; A [tokens][Hv][64];
     // states h, dH' [rows*Hv][128][128]; Delta, dDelta [rows*Hv][64][128]
-    // outputs dq, dk [tokens][Hq][128], dv [tokens][Hv][128] (full chunks leave by TMA stores)
+    // outputs dq, dk [tokens][Hq][K], dv [tokens][Hv][V] (full chunks leave by TMA stores)
+    // (K, V below 128: the 128-wide tiles load zeros past them and the stores are clipped)
     CUtensorMap tq, tk, tdo, tv, ta, th, tdh, td, tdd, tdq, tdk, tdv;
     const void *q, *k, *v, *A, *beta, *dout, *h, *dhn, *delta, *ddelta;
     const float *g_cs;
@@ -126,7 +127,6 @@ template <> __device__ __forceinline__ float bits_to_f<__half>(uint32_t b) {
     return __half2float(__ushort_as_half((unsigned short)b));
 }
 
-// In-place L2 normalisation of 64 rows of a [64 x 128] swizzled tile (blocks 16 KB apart).
 // Row norms of the 64 rows of a [64 x 128] swizzled tile (blocks 16 KB apart), read only: eight warps per tile,
 // four lanes per row; lane quarter qq takes 16-byte chunks 2qq, 2qq+1 of each 64-column block, so the eight
 // lanes of a quarter-warp access hit eight distinct bank groups.  n_out[r] = 1 / sqrt(|x_r|^2 + eps) (the

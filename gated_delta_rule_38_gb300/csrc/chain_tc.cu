@@ -46,7 +46,7 @@ constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack for aligning the bas
 constexpr uint32_t T_QK = 0, T_W = 64, T_U = 128, T_O1 = 192, T_O2 = 256, T_X = 320, T_COLS = 512;
 
 struct TcP {
-    CUtensorMap tq, tk, tv, ta;  // TMA maps of q, k ([tokens][Hq][128]), v ([tokens][Hv][128]), A ([tokens][Hv][64])
+    CUtensorMap tq, tk, tv, ta;  // TMA maps of q, k ([tokens][Hq][K]), v ([tokens][Hv][V]), A ([tokens][Hv][64])
     const void *q, *k, *v, *A, *beta;
     const float *g_cs, *h0;
     void *o, *h;

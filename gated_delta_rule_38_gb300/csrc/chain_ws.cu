@@ -107,7 +107,7 @@ struct WsP {
     // bf16 tiles in shared memory: each state warp stores its own 32-row x 64-column box
     bool tma_h, tma_delta;
     CUtensorMap th, tdl;  // h [rows*Hv][128][128], Delta [rows*Hv][64][128]; boxes 64 x 32 x 1
-    CUtensorMap to;       // o [tokens][Hv][128], boxes 64 x 1 x 32 (full chunks' output rows)
+    CUtensorMap to;       // o [tokens][Hv][V], boxes 64 x 1 x 32 (full chunks' output rows)
 };
 
 // One non-blocking test (the MMA thread polls several barriers in turn).

@@ -44,7 +44,7 @@ constexpr uint32_t TILE_BYTES = 49152;  // bytes one item's loads bring in
 constexpr int PR = 64;  // the producer thread (warp 2: its rows 0..31 x columns 32..63 of P are all zero)
 
 struct PpP {
-    CUtensorMap tq, tk, tp;  // q, k [tokens][Hq][128]; P [tokens][Hv][64]; boxes 64 x 1 x 64
+    CUtensorMap tq, tk, tp;  // q, k [tokens][Hq][K]; P [tokens][Hv][64]; boxes 64 x 1 x 64
     const float *g_cs;
     void *P;
     float *rq, *rk;

@@ -60,7 +60,7 @@ constexpr uint32_t TILE_BYTES = ST_BYTES;
 constexpr float LOG2E = 1.4426950408889634f;
 
 struct WyP {
-    CUtensorMap tq, tk, tp;      // q, k [tokens][Hq][128]; P [tokens][Hv][64]; boxes 64 x 1 x 64
+    CUtensorMap tq, tk, tp;      // q, k [tokens][Hq][K]; P [tokens][Hv][64]; boxes 64 x 1 x 64
     const void *g, *beta;        // raw log-gate and beta [tokens][Hv] (element type or fp32)
     float *g_cs;                 // out: [tokens][Hv]
     void *P, *A;                 // out: [tokens][Hv][64] (P may be null)
