@@ -846,55 +846,120 @@ cudaError_t chain_fwd_tc_t(const Args &a, const TcP &p, bool write_o, bool affin
 
 // Segment start states: S_0 = init (API state layout, or zero), S_{s+1} = S_s P_s + Q_s in fp32,
 // walking segments forward (or backward when reverse), with P = seg_end1, Q = seg_end0 (S-form).
-// One block per (16-row slice of the value index, head, sequence).
-__global__ void __launch_bounds__(256) seg_scan_kernel(int Hv, int nseg, bool reverse, const float *__restrict__ init,
-                                                       bool v_first, const float *__restrict__ P,
-                                                       const float *__restrict__ Q, float *__restrict__ out) {
-    __shared__ float sS[16][DK];
+// One block of four warps per (16-row slice of the value index, head, sequence); warp w owns rows 4w..4w+3,
+// lane l the columns 4l..4l+3, so each row of P_s is read from shared memory once per warp, conflict-free,
+// and feeds 16 products per thread.  The walk is serial over the segments, so each segment's P_s (64 KB)
+// and this block's 16 rows of Q_s (8 KB) come in by bulk async copies into a two-slot shared-memory ring
+// while the previous segment is applied: the block waits on memory about once, not once per segment.
+// Waits are bounded; on expiry the block latches GDR_ERR_TIMEOUT and stops after its copies in flight
+// have landed.
+constexpr int SCAN_NT = 128;
+constexpr uint32_t SCAN_P = DK * DK * 4, SCAN_Q = 16 * DK * 4, SCAN_SLOT = SCAN_P + SCAN_Q;
+constexpr int SCAN_LD = DK + 4;  // row stride of the state rows in shared memory (16-byte aligned rows)
+constexpr uint32_t SCAN_S = 2 * SCAN_SLOT, SCAN_BAR = SCAN_S + 16 * SCAN_LD * 4, SCAN_BYTES = SCAN_BAR + 16;
+__global__ void __launch_bounds__(SCAN_NT) seg_scan_kernel(int Hv, int nseg, bool reverse, const float *__restrict__ init,
+                                                           bool v_first, const float *__restrict__ P,
+                                                           const float *__restrict__ Q, float *__restrict__ out,
+                                                           unsigned *err, long polls) {
+    extern __shared__ __align__(128) unsigned char scan_smem[];
+    float *sS = reinterpret_cast<float *>(scan_smem + SCAN_S);  // [16][SCAN_LD]
+    const uint32_t sb = smem_u32(scan_smem), bar = sb + SCAN_BAR;
     const int blk = blockIdx.x, j = blockIdx.y, n = blockIdx.z;
-    const int tid = threadIdx.x, rr = tid >> 4, cb = (tid & 15) * 8;
-    const int e = blk * 16 + rr;
+    const int tid = threadIdx.x, r0 = (tid >> 5) * 4, c0 = (tid & 31) * 4;
     const long long st_base = ((long long)n * Hv + j) * DK * DV;
-    for (int i = 0; i < 8; ++i) {
-        const int d = cb + i;
-        sS[rr][d] = init ? init[st_base + (v_first ? (long long)e * DK + d : (long long)d * DV + e)] : 0.f;
+    auto seg_base = [&](int t) -> long long {
+        const int sg = reverse ? nseg - 1 - t : t;
+        return (((long long)n * Hv + j) * nseg + sg) * DK * DV;
+    };
+    // segment t's P and Q rows into slot t & 1 (thread 0)
+    auto fetch = [&](int t) {
+        const uint32_t slot = sb + (uint32_t)(t & 1) * SCAN_SLOT, b = bar + 8 * (t & 1);
+        const long long sbase = seg_base(t);
+        tma::expect_tx(b, SCAN_SLOT);
+        for (int i = 0; i < 4; ++i)
+            tma::load1d(slot + i * (SCAN_P / 4), P + sbase + i * (DK * DK / 4), SCAN_P / 4, b);
+        tma::load1d(slot + SCAN_P, Q + sbase + (long long)blk * 16 * DK, SCAN_Q, b);
+    };
+    const int steps = nseg - 1;  // segments whose P and Q are applied
+    if (tid == 0) {
+        umma::mbar_init(bar, 1);
+        umma::mbar_init(bar + 8, 1);
+        umma::fence_mbar_init();
+    }
+    for (int r = 0; r < 4; ++r) {
+        const int e = blk * 16 + r0 + r;
+        for (int c = 0; c < 4; ++c) {
+            const int d = c0 + c;
+            sS[(r0 + r) * SCAN_LD + d] = init ? init[st_base + (v_first ? (long long)e * DK + d : (long long)d * DV + e)] : 0.f;
+        }
     }
     __syncthreads();
+    if (tid == 0 && steps > 0) fetch(0);
+    int issued = steps > 0 ? 1 : 0;
+    bool ok = true;
     for (int t = 0; t < nseg; ++t) {
-        const int sg = reverse ? nseg - 1 - t : t;
-        const long long sbase = (((long long)n * Hv + j) * nseg + sg) * DK * DV;
-        float acc[8];
+        const long long sbase = seg_base(t);
+        float4 y[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            acc[i] = sS[rr][cb + i];
-            out[sbase + (long long)e * DK + cb + i] = acc[i];
+        for (int r = 0; r < 4; ++r) {
+            y[r] = *reinterpret_cast<const float4 *>(sS + (r0 + r) * SCAN_LD + c0);
+            *reinterpret_cast<float4 *>(out + sbase + (long long)(blk * 16 + r0 + r) * DK + c0) = y[r];
         }
-        if (t + 1 == nseg) break;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = Q[sbase + (long long)e * DK + cb + i];
-        for (int d2 = 0; d2 < DK; ++d2) {
-            const float a = sS[rr][d2];
-            const float4 p0 = *reinterpret_cast<const float4 *>(P + sbase + (long long)d2 * DK + cb);
-            const float4 p1 = *reinterpret_cast<const float4 *>(P + sbase + (long long)d2 * DK + cb + 4);
-            acc[0] += a * p0.x;
-            acc[1] += a * p0.y;
-            acc[2] += a * p0.z;
-            acc[3] += a * p0.w;
-            acc[4] += a * p1.x;
-            acc[5] += a * p1.y;
-            acc[6] += a * p1.z;
-            acc[7] += a * p1.w;
+        if (t >= steps) break;
+        // the next segment's copies go into the other slot, which segment t - 1 has finished with
+        if (tid == 0 && t + 1 < steps) {
+            fetch(t + 1);
+            ++issued;
         }
-        __syncthreads();
+        const bool got = umma::mbar_wait(bar + 8 * (t & 1), (t >> 1) & 1, polls);
+        if (__syncthreads_or(!got)) {
+            if (tid == 0) raise_error(err, GDR_ERR_TIMEOUT);
+            ok = false;
+            break;
+        }
+        const float *sP = reinterpret_cast<const float *>(scan_smem + (t & 1) * SCAN_SLOT);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) sS[rr][cb + i] = acc[i];
+        for (int r = 0; r < 4; ++r) y[r] = *reinterpret_cast<const float4 *>(sP + DK * DK + (r0 + r) * DK + c0);
+#pragma unroll 2
+        for (int d = 0; d < DK; d += 4) {
+            float4 sv[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) sv[r] = *reinterpret_cast<const float4 *>(sS + (r0 + r) * SCAN_LD + d);
+#pragma unroll
+            for (int dd = 0; dd < 4; ++dd) {
+                const float4 pv = *reinterpret_cast<const float4 *>(sP + (d + dd) * DK + c0);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const float a = dd == 0 ? sv[r].x : dd == 1 ? sv[r].y : dd == 2 ? sv[r].z : sv[r].w;
+                    y[r].x += a * pv.x;
+                    y[r].y += a * pv.y;
+                    y[r].z += a * pv.z;
+                    y[r].w += a * pv.w;
+                }
+            }
+        }
+        __syncthreads();  // every thread has read S_t and this slot
+#pragma unroll
+        for (int r = 0; r < 4; ++r) *reinterpret_cast<float4 *>(sS + (r0 + r) * SCAN_LD + c0) = y[r];
         __syncthreads();
     }
+    // copies still in flight land before the block exits (bounded)
+    if (!ok && tid == 0)
+        for (int t = 0; t < issued; ++t) umma::mbar_wait(bar + 8 * (t & 1), (t >> 1) & 1, 4000000L);
 }
 
 }  // namespace
 
 namespace {
+
+cudaError_t launch_seg_scan(const Args &a, const SegWs &sw, bool reverse, const float *init, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SCAN_BYTES);
+    if (e != cudaSuccess) return e;
+    seg_scan_kernel<<<dim3(DV / 16, a.Hv, a.N), SCAN_NT, SCAN_BYTES, s>>>(
+        a.Hv, sw.nseg, reverse, init, a.v_first, sw.end1, sw.end0, sw.start, a.err,
+        a.wait_polls >= 0 ? (long)a.wait_polls : 200000000L);
+    return cudaGetLastError();
+}
 
 // [tokens][heads][cols] map with 64 x 1 x 64 boxes
 bool tile_map(CUtensorMap *m, const void *base, const Args &a, int heads, int cols) {
@@ -971,9 +1036,7 @@ cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const 
     if (sw.nseg > 1) {
         e = a.bf16 ? chain_bwd_tc_t<__nv_bfloat16>(a, p, true, s) : chain_bwd_tc_t<__half>(a, p, true, s);
         if (e != cudaSuccess) return e;
-        seg_scan_kernel<<<dim3(DV / 16, a.Hv, a.N), 256, 0, s>>>(a.Hv, sw.nseg, true, dht, a.v_first, sw.end1,
-                                                                 sw.end0, sw.start);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_seg_scan(a, sw, true, dht, s)) != cudaSuccess) return e;
         p.seg_start = sw.start;
     }
     return a.bf16 ? chain_bwd_tc_t<__nv_bfloat16>(a, p, false, s) : chain_bwd_tc_t<__half>(a, p, false, s);
@@ -988,9 +1051,7 @@ cudaError_t launch_chain_fwd(const Args &a, const void *q, const void *k, const 
     if (sw.nseg > 1) {
         e = a.bf16 ? chain_fwd_tc_t<__nv_bfloat16>(a, p, false, true, s) : chain_fwd_tc_t<__half>(a, p, false, true, s);
         if (e != cudaSuccess) return e;
-        seg_scan_kernel<<<dim3(DV / 16, a.Hv, a.N), 256, 0, s>>>(a.Hv, sw.nseg, false, h0, a.v_first, sw.end1, sw.end0,
-                                                                 sw.start);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_seg_scan(a, sw, false, h0, s)) != cudaSuccess) return e;
         p.seg_start = sw.start;
     }
     return a.bf16 ? chain_fwd_tc_t<__nv_bfloat16>(a, p, o != nullptr, false, s)

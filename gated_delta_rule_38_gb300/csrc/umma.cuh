@@ -168,6 +168,14 @@ __device__ __forceinline__ void wait_read() { asm volatile("cp.async.bulk.wait_g
 __device__ __forceinline__ void wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;\n" ::: "memory"); }
 __device__ __forceinline__ void wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 
+// Plain (untiled) bulk copy of `bytes` contiguous bytes from global into shared memory, completion counted in
+// bytes on `mbar`.  Both addresses 16-byte aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void load1d(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(mbar)
+                 : "memory");
+}
+
 // One arrival that also announces `bytes` of transactions on the barrier's current phase.
 __device__ __forceinline__ void expect_tx(uint32_t mbar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(mbar), "r"(bytes) : "memory");
