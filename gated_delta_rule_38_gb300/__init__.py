@@ -102,8 +102,7 @@ def saved_buffer(q, v, g, scale=None, cu_seqlens=None, use_qk_l2norm_in_kernel=F
                  num_segments=0, **act):
     """A device buffer for what the forward keeps for the backward (``saved=`` of the forward and backward
     below): the decayed causal blocks, the q/k norms, the state before every chunk and Delta of every chunk,
-    and with ``use_gate_in_kernel`` the gate activation's derivative.  None when the problem keeps nothing
-    (the intra-GPU split path without the in-kernel gate).  ``act``: the activation options."""
+    and with ``use_gate_in_kernel`` the gate activation's derivative.  ``act``: the activation options."""
     lib = _lib.load()
     p = problem(q, v, g, scale, _cu(cu_seqlens), use_qk_l2norm_in_kernel, state_v_first, num_segments, **act)
     n = ctypes.c_size_t(0)

@@ -162,22 +162,27 @@ int64_t max_chunks_of(const gdr_problem *p) {
 }
 
 // Segments per sequence for the intra-GPU sequence split.  Every chain CTA occupies one SM, so with
-// S segments the affine pass runs ceil(2 S streams / SMs) waves and the full pass ceil(S streams / SMs)
-// waves, each over ceil(chunks / S) chunks (an affine chunk costs about 0.7 of a full one), plus a
-// scan whose cost grows with S.  The automatic choice minimises that estimate; S = 1 means no split.
-// Host-only (the workspace size must not depend on the device).
+// S segments the affine passes and the full passes each run ceil(2 S streams / SMs) waves over
+// ceil(chunks / S) chunks, plus a scan whose cost grows with S.  The automatic choice minimises that
+// estimate against the unsplit chains; S = 1 means no split.  Host-only (the workspace size must not
+// depend on the device).
 constexpr int64_t kSplitSMs = 152;
 int choose_nseg(const gdr_problem *p) {
     const int64_t streams = std::max<int64_t>(1, (int64_t)num_seqs(p) * p->Hv);
     const int64_t maxc = std::max<int64_t>(1, ((int64_t)p->T + C - 1) / C);
     if (p->num_segments > 0) return (int)std::max<int64_t>(1, std::min<int64_t>({p->num_segments, maxc, 64}));
     auto waves = [&](int64_t ctas) { return (ctas + kSplitSMs - 1) / kSplitSMs; };
-    double best = (double)waves(streams) * (double)maxc;
+    // Time in units of one step of the warp-specialised chains (one chunk of one 64-column slice; both run
+    // one CTA per SM).  Unsplit: every (sequence, head) walks its chunks in two slices.  Split into s
+    // segments: the segment-affine passes (two CTAs per segment and head, about 2.1 units per chunk over
+    // the forward and reverse chains), the segments' full passes (two slices each), the scan and the two
+    // extra launches.
+    double best = (double)waves(2 * streams) * (double)maxc;
     int best_s = 1;
     for (int64_t s = 2; s <= std::min<int64_t>(64, maxc); ++s) {
         const double per = (double)((maxc + s - 1) / s);
-        const double cost = per * (0.7 * (double)waves(2 * s * streams) + (double)waves(s * streams)) + 2.0 * (double)s;
-        if (cost < 0.9 * best) {
+        const double cost = per * 3.1 * (double)waves(2 * s * streams) + 1.5 * (double)s + 8.0;
+        if (cost < 0.95 * best) {
             best = cost;
             best_s = (int)s;
         }
@@ -194,8 +199,8 @@ struct Layout {
 };
 
 // Workspace: [varlen chunk tables][fwd: g_cumsum, A scratch | bwd: states, state gradients].  With a saved
-// buffer (`kept`, unsplit problems) the parts that the buffer holds instead are left out: P and the norms
-// in both directions, the states and Delta in the backward.
+// buffer (`kept`) the parts that the buffer holds instead are left out: P and the norms in both directions,
+// the states and Delta in the backward.
 Layout layout_of(const gdr_problem *p, bool bwd, bool kept = false) {
     Layout L;
     size_t at = 0;
@@ -210,7 +215,6 @@ Layout layout_of(const gdr_problem *p, bool bwd, bool kept = false) {
     }
     const size_t tok = (size_t)p->B * p->T;
     L.nseg = choose_nseg(p);
-    kept = kept && L.nseg == 1;
     if (p->flags & kActFlags) {
         // fp32 activated gates for the forward; activated beta and the gradients w.r.t. the activated g and
         // beta for the backward
@@ -233,8 +237,8 @@ Layout layout_of(const gdr_problem *p, bool bwd, bool kept = false) {
         at = round_up(at + tok * p->Hv * sizeof(float), 256);
         L.A = at;
         at = round_up(at + tok * p->Hv * C * esize(p->dtype), 256);
-        if (L.nseg == 1 && !kept) {
-            // the decayed causal attention block and the inverse q/k norms for the unsplit recurrence
+        if (!kept) {
+            // the decayed causal attention block and the inverse q/k norms for the output
             L.P = at;
             at = round_up(at + tok * p->Hv * C * esize(p->dtype), 256);
             if (p->flags & GDR_L2NORM_QK) {
@@ -281,10 +285,10 @@ Layout layout_of(const gdr_problem *p, bool bwd, bool kept = false) {
     return L;
 }
 
-// What the forward keeps for the backward (gdr_fwd_ex / gdr_bwd_ex), 256-byte aligned parts: without the
-// intra-GPU split ("blocks") the decayed causal blocks P [tokens x Hv x 64 (dtype)], the inverse q/k norms
-// rq, rk [tokens x Hv fp32], the states h and Delta of every chunk; with GDR_GATE_IN_KERNEL also sigmoid(-x)
-// of the raw gate [tokens x Hv fp32] (the derivative of the gate activation).  Empty otherwise.
+// What the forward keeps for the backward (gdr_fwd_ex / gdr_bwd_ex), 256-byte aligned parts: the decayed
+// causal blocks P [tokens x Hv x 64 (dtype)], the inverse q/k norms rq, rk [tokens x Hv fp32], the states h
+// and Delta of every chunk ("blocks"), and with GDR_GATE_IN_KERNEL first sigmoid(-x) of the raw gate
+// [tokens x Hv fp32] (the derivative of the gate activation).
 struct SavedLayout {
     size_t P = 0, rq = 0, rk = 0, h = 0, delta = 0, gate = 0, bytes = 0;
     bool blocks = false;
@@ -297,8 +301,6 @@ SavedLayout saved_layout_of(const gdr_problem *p) {
         S.gate = at;
         at = round_up(at + tok * p->Hv * sizeof(float), 256);
     }
-    S.bytes = at;
-    if (choose_nseg(p) != 1) return S;
     S.blocks = true;
     const size_t mc = (size_t)max_chunks_of(p);
     S.P = at;
@@ -616,22 +618,24 @@ static gdr_status fwd_core(const gdr_problem *p, int tk, int tv, const void *q, 
     const SegWs sw = seg_ws(L, ws);
     // P and the norms go to the caller's saved buffer when one is given (the backward then skips its P pass)
     char *sv = (saved && S.blocks) ? static_cast<char *>(saved) : nullptr;
-    void *Pw = sw.nseg == 1 ? static_cast<void *>(sv ? sv + S.P : ws + L.P) : nullptr;
-    float *rqw = (sw.nseg == 1 && a.l2norm) ? reinterpret_cast<float *>(sv ? sv + S.rq : ws + L.rq) : nullptr;
-    float *rkw = (sw.nseg == 1 && a.l2norm) ? reinterpret_cast<float *>(sv ? sv + S.rk : ws + L.rk) : nullptr;
+    void *Pw = sv ? sv + S.P : ws + L.P;
+    float *rqw = a.l2norm ? reinterpret_cast<float *>(sv ? sv + S.rq : ws + L.rq) : nullptr;
+    float *rkw = a.l2norm ? reinterpret_cast<float *>(sv ? sv + S.rk : ws + L.rk) : nullptr;
     // ... and the state before every chunk and Delta of every chunk (the backward then runs no forward recompute)
     void *hs = sv ? static_cast<void *>(sv + S.h) : h;
     void *dls = sv ? static_cast<void *>(sv + S.delta) : nullptr;
     if ((st = timed(K_WY_FWD, s, [&] { return launch_wy_fwd(a, q, k, g, beta, gcs, Aw, Pw, rqw, rkw, s); })) !=
         GDR_OK)
         return st;
-    if (sw.nseg == 1)
-        return timed(K_CHAIN_FWD, s, [&] {
-            return launch_chain_ws(a, q, k, v, gcs, beta, Aw, Pw, rqw, rkw, h0, nullptr, o, final_state, hs,
-                                   sv ? false : a.v_first, dls, s);
-        });
+    // the intra-GPU split: the segment-affine passes and the scan give every segment's start state, then the
+    // same warp-specialised recurrence runs every segment from its start
     return timed(K_CHAIN_FWD, s, [&] {
-        return launch_chain_fwd(a, q, k, v, gcs, beta, Aw, h0, o, final_state, h, true, nullptr, sw, s);
+        if (sw.nseg > 1) {
+            const cudaError_t e = launch_chain_fwd_affine(a, q, k, v, gcs, beta, Aw, h0, sw, s);
+            if (e != cudaSuccess) return e;
+        }
+        return launch_chain_ws(a, q, k, v, gcs, beta, Aw, Pw, rqw, rkw, h0, sw.nseg > 1 ? sw.start : nullptr, sw.nseg,
+                               o, final_state, hs, sv ? false : a.v_first, dls, s);
     });
 }
 
@@ -724,33 +728,40 @@ static gdr_status bwd_core(const gdr_problem *p, int tk, int tv, const void *q, 
         a.gate_f32 = true;
     }
     void *hw = ws + L.h, *dhw = ws + L.dhn, *dlw = ws + L.delta, *ddlw = ws + L.ddelta;
-    // states and Delta of every chunk (recomputed), the reverse state-gradient chain, then every
-    // chunk's gradients in parallel
+    // states and Delta of every chunk (the forward's, or recomputed), the reverse state-gradient chain, then
+    // every chunk's gradients in parallel
     const SegWs sw = seg_ws(L, ws);
-    if (sw.nseg == 1) {
-        // P and the norms: from the forward's saved buffer when given, else recomputed from g_cumsum
-        const char *sv = (saved && S.blocks) ? static_cast<const char *>(saved) : nullptr;
-        void *Pw = sv ? const_cast<char *>(sv + S.P) : ws + L.P;
-        float *rqw = a.l2norm ? reinterpret_cast<float *>(sv ? const_cast<char *>(sv + S.rq) : ws + L.rq) : nullptr;
-        float *rkw = a.l2norm ? reinterpret_cast<float *>(sv ? const_cast<char *>(sv + S.rk) : ws + L.rk) : nullptr;
-        if (sv) {
-            // the states and Delta are the forward's: the reverse chain alone, in 64-column slices
-            hw = const_cast<char *>(sv + S.h);
-            dlw = const_cast<char *>(sv + S.delta);
-            if ((st = timed(K_CHAIN_REV, s, [&] {
-                     return launch_chain_rev(a, q, k, g_cumsum, beta, A, Pw, rqw, rkw, dout, dht, dhw, ddlw, dh0, s);
-                 })) != GDR_OK)
-                return st;
-        } else {
-            if ((st = timed(K_CHUNK_P, s, [&] { return launch_chunk_p_tc(a, q, k, g_cumsum, Pw, rqw, rkw, s); })) !=
-                GDR_OK)
-                return st;
-            if ((st = timed(K_CHAIN_PAIR, s, [&] {
-                     return launch_chain_ws_pair(a, q, k, v, g_cumsum, beta, A, Pw, rqw, rkw, h0, hw, dlw, dout, dht,
-                                                 dhw, ddlw, dh0, s);
-                 })) != GDR_OK)
-                return st;
-        }
+    const char *sv = (saved && S.blocks) ? static_cast<const char *>(saved) : nullptr;
+    if (sv) {
+        // the states, Delta, P and the norms are the forward's: the reverse chain alone, in 64-column slices
+        // (with the intra-GPU split: after the reverse segment-affine passes and the scan, every segment from
+        // the gradient at its end)
+        void *Pw = const_cast<char *>(sv + S.P);
+        float *rqw = a.l2norm ? reinterpret_cast<float *>(const_cast<char *>(sv + S.rq)) : nullptr;
+        float *rkw = a.l2norm ? reinterpret_cast<float *>(const_cast<char *>(sv + S.rk)) : nullptr;
+        hw = const_cast<char *>(sv + S.h);
+        dlw = const_cast<char *>(sv + S.delta);
+        if ((st = timed(sw.nseg > 1 ? K_CHAIN_BWD : K_CHAIN_REV, s, [&] {
+                 if (sw.nseg > 1) {
+                     const cudaError_t e = launch_chain_bwd_affine(a, q, k, g_cumsum, beta, A, dout, dht, sw, s);
+                     if (e != cudaSuccess) return e;
+                 }
+                 return launch_chain_rev(a, q, k, g_cumsum, beta, A, Pw, rqw, rkw, dout, dht,
+                                         sw.nseg > 1 ? sw.start : nullptr, sw.nseg, dhw, ddlw, dh0, s);
+             })) != GDR_OK)
+            return st;
+    } else if (sw.nseg == 1) {
+        // P and the norms recomputed from g_cumsum
+        void *Pw = ws + L.P;
+        float *rqw = a.l2norm ? reinterpret_cast<float *>(ws + L.rq) : nullptr;
+        float *rkw = a.l2norm ? reinterpret_cast<float *>(ws + L.rk) : nullptr;
+        if ((st = timed(K_CHUNK_P, s, [&] { return launch_chunk_p_tc(a, q, k, g_cumsum, Pw, rqw, rkw, s); })) != GDR_OK)
+            return st;
+        if ((st = timed(K_CHAIN_PAIR, s, [&] {
+                 return launch_chain_ws_pair(a, q, k, v, g_cumsum, beta, A, Pw, rqw, rkw, h0, hw, dlw, dout, dht, dhw,
+                                             ddlw, dh0, s);
+             })) != GDR_OK)
+            return st;
     } else if ((st = timed(K_CHAIN_FWD_RECOMPUTE, s, [&] {
              return launch_chain_fwd(a, q, k, v, g_cumsum, beta, A, h0, nullptr, nullptr, hw, false, dlw, sw, s);
          })) != GDR_OK) {

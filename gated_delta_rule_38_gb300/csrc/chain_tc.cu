@@ -1027,6 +1027,16 @@ TcP fwd_params(const Args &a, const void *q, const void *k, const void *v, const
 
 }  // namespace
 
+cudaError_t launch_chain_bwd_affine(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
+                                    const void *A, const void *dout, const float *dht, const SegWs &sw, cudaStream_t s) {
+    if (sw.nseg < 2) return cudaErrorInvalidValue;
+    TcBwdP p = bwd_params(a, q, k, g_cs, beta, A, dout, dht, nullptr, nullptr, nullptr, sw);
+    if (p.nseg < 1) return cudaErrorInvalidValue;
+    cudaError_t e = a.bf16 ? chain_bwd_tc_t<__nv_bfloat16>(a, p, true, s) : chain_bwd_tc_t<__half>(a, p, true, s);
+    if (e != cudaSuccess) return e;
+    return launch_seg_scan(a, sw, true, dht, s);
+}
+
 cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
                              const void *A, const void *dout, const float *dht, void *dhn, void *ddelta, float *dh0,
                              const SegWs &sw, cudaStream_t s) {
@@ -1034,12 +1044,21 @@ cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const 
     if (p.nseg < 1) return cudaErrorInvalidValue;
     cudaError_t e;
     if (sw.nseg > 1) {
-        e = a.bf16 ? chain_bwd_tc_t<__nv_bfloat16>(a, p, true, s) : chain_bwd_tc_t<__half>(a, p, true, s);
-        if (e != cudaSuccess) return e;
-        if ((e = launch_seg_scan(a, sw, true, dht, s)) != cudaSuccess) return e;
+        if ((e = launch_chain_bwd_affine(a, q, k, g_cs, beta, A, dout, dht, sw, s)) != cudaSuccess) return e;
         p.seg_start = sw.start;
     }
     return a.bf16 ? chain_bwd_tc_t<__nv_bfloat16>(a, p, false, s) : chain_bwd_tc_t<__half>(a, p, false, s);
+}
+
+cudaError_t launch_chain_fwd_affine(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
+                                    const void *beta, const void *A, const float *h0, const SegWs &sw, cudaStream_t s) {
+    if (sw.nseg < 2) return cudaErrorInvalidValue;
+    TcP p = fwd_params(a, q, k, v, g_cs, beta, A, h0, nullptr, nullptr, nullptr, false, nullptr, sw);
+    if (p.nseg < 1) return cudaErrorInvalidValue;
+    cudaError_t e =
+        a.bf16 ? chain_fwd_tc_t<__nv_bfloat16>(a, p, false, true, s) : chain_fwd_tc_t<__half>(a, p, false, true, s);
+    if (e != cudaSuccess) return e;
+    return launch_seg_scan(a, sw, false, h0, s);
 }
 
 cudaError_t launch_chain_fwd(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
@@ -1049,9 +1068,7 @@ cudaError_t launch_chain_fwd(const Args &a, const void *q, const void *k, const 
     if (p.nseg < 1) return cudaErrorInvalidValue;
     cudaError_t e;
     if (sw.nseg > 1) {
-        e = a.bf16 ? chain_fwd_tc_t<__nv_bfloat16>(a, p, false, true, s) : chain_fwd_tc_t<__half>(a, p, false, true, s);
-        if (e != cudaSuccess) return e;
-        if ((e = launch_seg_scan(a, sw, false, h0, s)) != cudaSuccess) return e;
+        if ((e = launch_chain_fwd_affine(a, q, k, v, g_cs, beta, A, h0, sw, s)) != cudaSuccess) return e;
         p.seg_start = sw.start;
     }
     return a.bf16 ? chain_fwd_tc_t<__nv_bfloat16>(a, p, o != nullptr, false, s)

@@ -100,7 +100,8 @@ struct WsP {
     float *fin;
     void *h;       // optional: state before every chunk, [rows,Hv,K,V] (or [..,V,K] with h_vfirst)
     void *delta;   // optional: Delta of every chunk, [rows,Hv,64,V]
-    const float *seg_start;  // optional start states, transposed [N,Hv,V,K] fp32 (replaces h0)
+    const float *seg_start;  // optional start states, transposed [N,Hv,nseg,V,K] fp32 (replaces h0)
+    int nseg;                // segments per sequence (the intra-GPU split; 1 = none): grid z = N x nseg
     bool gate_f32, l2norm, v_first, h_vfirst;
     float scale;
     // with all 128 value columns in one CTA and the [K,V] layout, h and Delta leave by TMA store from the
@@ -241,8 +242,20 @@ __device__ __forceinline__ uint16_t to_bits(float x) {
     return *reinterpret_cast<const uint16_t *>(&h);
 }
 
+// The intra-GPU split: block z of a launch over N x nseg is segment z % nseg of sequence z / nseg, the
+// sequence's whole chunks [cb, cb + sl) with sl = ceil(chunks / nseg) (the affine passes' segments); the
+// sequence's first token, length and first chunk row move to the segment's (an empty segment has length 0).
+__device__ __forceinline__ void seg_range(int nseg, int seg, long long &tok0, int &len, int &row0) {
+    if (nseg <= 1) return;
+    const int nc_all = (len + C - 1) / C, sl = (nc_all + nseg - 1) / nseg;
+    const int cb = min(nc_all, seg * sl), ce = min(nc_all, cb + sl);
+    tok0 += (long long)cb * C;
+    row0 += cb;
+    len = ce > cb ? min(len - cb * C, (ce - cb) * C) : 0;
+}
+
 template <typename T, int BV, bool WRITE_O>
-__device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const int vh, const int j, const int n) {
+__device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const int vh, const int j, const int nz) {
     using L = Lay<BV, WRITE_O>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem =
@@ -252,9 +265,11 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
     const int Hv = geo.Hv, Hq = geo.Hq, hq = j / (Hv / Hq);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr bool bf16 = IsBf16<T>::value;
+    const int nseg = p.nseg > 1 ? p.nseg : 1, n = nz / nseg, seg = nz - n * nseg;
     long long tok0;
     int len, row0;
     geo.seq(n, tok0, len, row0);
+    seg_range(nseg, seg, tok0, len, row0);
     const int nc = (len + C - 1) / C;
     volatile int *flag = reinterpret_cast<volatile int *>(smem + L::FLAG);
     float *F = reinterpret_cast<float *>(smem + L::F);
@@ -549,12 +564,13 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
         constexpr int HW = BV / 2;     // value columns per thread
         const int cb0 = cg * HW;
         const long long st_base = ((long long)n * Hv + j) * DK * DV;
+        const long long seg_base = (((long long)n * Hv + j) * nseg + seg) * DK * DV;
         float hS[HW];
 #pragma unroll
         for (int i = 0; i < HW; ++i) {
             const int e = v0 + cb0 + i;
             if (p.seg_start)
-                hS[i] = p.seg_start[st_base + (long long)e * DK + d];
+                hS[i] = p.seg_start[seg_base + (long long)e * DK + d];
             else if (p.h0)
                 hS[i] = p.h0[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)];
             else
@@ -691,7 +707,7 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
             write_h(lc + 1);
         }
         if (lane == 0 && (p.tma_h || p.tma_delta)) tma::wait_all();  // the stored boxes are complete (issuers)
-        if (!*flag && p.fin) {
+        if (!*flag && p.fin && seg == nseg - 1) {
 #pragma unroll
             for (int i = 0; i < HW; ++i) {
                 const int e = v0 + cb0 + i;
@@ -841,6 +857,8 @@ static_assert(RLay::BYTES <= 232448, "shared memory");
 struct RevP {
     CUtensorMap tq, tk, tdo, tp, ta;  // [tokens][heads][cols] maps, boxes 64 x 1 x 64
     const float *g_cs, *rq, *rk, *dht;
+    const float *seg_start;  // optional end-of-segment gradients, transposed [N,Hv,nseg,V,K] fp32 (replaces dht)
+    int nseg;                // segments per sequence (1 = none): grid z = N x nseg
     const void *beta;
     void *dhn;     // [rows,Hv,K,V]: the gradient after every chunk
     void *ddelta;  // [rows,Hv,64,V]
@@ -853,7 +871,7 @@ struct RevP {
 };
 
 template <typename T, int BV>
-__device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const int vh, const int j, const int n) {
+__device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const int vh, const int j, const int nz) {
     using L = RLay;
     const int v0 = vh * BV;  // this block's value columns v0 .. v0+BV-1
     extern __shared__ unsigned char smem_raw[];
@@ -863,9 +881,11 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
     const int Hv = geo.Hv, Hq = geo.Hq, hq = j / (Hv / Hq);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr bool bf16 = IsBf16<T>::value;
+    const int nseg = p.nseg > 1 ? p.nseg : 1, n = nz / nseg, seg = nz - n * nseg;
     long long tok0;
     int len, row0;
     geo.seq(n, tok0, len, row0);
+    seg_range(nseg, seg, tok0, len, row0);
     const int nc = (len + C - 1) / C;
     auto chunk_of = [&](int lc) { return nc - 1 - lc; };
     volatile int *flag = reinterpret_cast<volatile int *>(smem + L::FLAG);
@@ -1119,11 +1139,15 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
         constexpr int HW = BV / 2;  // value columns per thread
         const int cb0 = cg * HW;
         const long long st_base = ((long long)n * Hv + j) * DK * DV;
+        const long long seg_base = (((long long)n * Hv + j) * nseg + seg) * DK * DV;
         float hS[HW];
 #pragma unroll
         for (int i = 0; i < HW; ++i) {
             const int e = v0 + cb0 + i;
-            hS[i] = p.dht ? p.dht[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] : 0.f;
+            if (p.seg_start)
+                hS[i] = p.seg_start[seg_base + (long long)e * DK + d];
+            else
+                hS[i] = p.dht ? p.dht[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)] : 0.f;
         }
         const BoxStore<BV> box{q4, cg, lane};
         const int bx = cb0 & ~63;  // first column of the stored box that holds this warp's columns
@@ -1205,7 +1229,7 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
             write_h(lc + 1);
         }
         if (lane == 0 && (p.dhn || p.ddelta)) tma::wait_all();  // the stored boxes are complete
-        if (!*flag && p.dh0) {
+        if (!*flag && p.dh0 && seg == 0) {
 #pragma unroll
             for (int i = 0; i < HW; ++i) {
                 const int e = v0 + cb0 + i;
@@ -1276,7 +1300,8 @@ cudaError_t chain_rev_t(const Args &a, const RevP &p, cudaStream_t s) {
     auto kern = chain_rev_kernel<T, BV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, RLay::BYTES);
     if (e != cudaSuccess) return e;
-    return launch_overlapped(kern, dim3(DV / BV, a.Hv, a.N), dim3(WS_NT), RLay::BYTES, s, make_geo(a), p);
+    return launch_overlapped(kern, dim3(DV / BV, a.Hv, a.N * (p.nseg > 1 ? p.nseg : 1)), dim3(WS_NT), RLay::BYTES, s,
+                             make_geo(a), p);
 }
 
 template <typename T, int BV, bool WRITE_O>
@@ -1285,7 +1310,8 @@ cudaError_t chain_ws_t(const Args &a, const WsP &p, cudaStream_t s) {
     const uint32_t bytes = Lay<BV, WRITE_O>::BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    return launch_overlapped(kern, dim3(DV / BV, a.Hv, a.N), dim3(WS_NT), bytes, s, make_geo(a), p);
+    return launch_overlapped(kern, dim3(DV / BV, a.Hv, a.N * (p.nseg > 1 ? p.nseg : 1)), dim3(WS_NT), bytes, s,
+                             make_geo(a), p);
 }
 
 template <typename T>
@@ -1326,6 +1352,7 @@ cudaError_t launch_chain_ws_pair(const Args &a, const void *q, const void *k, co
     pf.h = h;
     pf.delta = delta;
     pf.seg_start = nullptr;
+    pf.nseg = 1;
     pf.gate_f32 = a.gate_f32;
     pf.l2norm = a.l2norm;
     pf.v_first = a.v_first;
@@ -1335,6 +1362,8 @@ cudaError_t launch_chain_ws_pair(const Args &a, const void *q, const void *k, co
     pb.rq = rq;
     pb.rk = rk;
     pb.dht = dht;
+    pb.seg_start = nullptr;
+    pb.nseg = 1;
     pb.beta = beta;
     pb.dhn = dhn;
     pb.ddelta = ddelta;
@@ -1348,7 +1377,8 @@ cudaError_t launch_chain_ws_pair(const Args &a, const void *q, const void *k, co
 
 cudaError_t launch_chain_rev(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
                              const void *A, const void *P, const float *rq, const float *rk, const void *dout,
-                             const float *dht, void *dhn, void *ddelta, float *dh0, cudaStream_t s) {
+                             const float *dht, const float *seg_start, int nseg, void *dhn, void *ddelta, float *dh0,
+                             cudaStream_t s) {
     RevP pb;
     if (!ws_map(&pb.tq, q, a, a.Hq, a.K) || !ws_map(&pb.tk, k, a, a.Hq, a.K) || !ws_map(&pb.tdo, dout, a, a.Hv, a.V) ||
         !ws_map(&pb.tp, P, a, a.Hv, C) || !ws_map(&pb.ta, A, a, a.Hv, C) ||
@@ -1358,6 +1388,8 @@ cudaError_t launch_chain_rev(const Args &a, const void *q, const void *k, const 
     pb.rq = rq;
     pb.rk = rk;
     pb.dht = dht;
+    pb.seg_start = seg_start;
+    pb.nseg = nseg;
     pb.beta = beta;
     pb.dhn = dhn;
     pb.ddelta = ddelta;
@@ -1371,7 +1403,7 @@ cudaError_t launch_chain_rev(const Args &a, const void *q, const void *k, const 
 
 cudaError_t launch_chain_ws(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
                             const void *beta, const void *A, const void *P, const float *rq, const float *rk,
-                            const float *h0, const float *seg_start, void *o, float *final_state, void *h,
+                            const float *h0, const float *seg_start, int nseg, void *o, float *final_state, void *h,
                             bool h_vfirst, void *delta, cudaStream_t s) {
     WsP p;
     const uint64_t tokens = (uint64_t)a.B * (uint64_t)a.T;
@@ -1389,6 +1421,7 @@ cudaError_t launch_chain_ws(const Args &a, const void *q, const void *k, const v
     p.h = h;
     p.delta = delta;
     p.seg_start = seg_start;
+    p.nseg = nseg;
     p.gate_f32 = a.gate_f32;
     p.l2norm = a.l2norm;
     p.v_first = a.v_first;

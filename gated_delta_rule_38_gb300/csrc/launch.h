@@ -90,15 +90,22 @@ cudaError_t launch_chunk_p_tc(const Args &a, const void *q, const void *k, const
 cudaError_t launch_chain_fwd(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
                              const void *beta, const void *A, const float *h0, void *o, float *final_state, void *h,
                              bool h_api_layout, void *delta, const SegWs &sw, cudaStream_t s);
-// Forward recurrence, warp-specialised (one CTA per value-column slice); no sequence split.
-// o != nullptr: output rows; h: state before every chunk ([rows,Hv,K,V], or [..,V,K] when
-// h_vfirst); delta: Delta of every chunk; seg_start: transposed fp32 start states replacing h0.
-// P, rq, rk: from launch_wy_fwd / launch_chunk_p_tc (P is read only when o != nullptr; rq, rk only with
-// in-kernel L2 normalisation).
+// Forward recurrence, warp-specialised (one CTA per value-column slice, and per segment of the intra-GPU
+// split when nseg > 1).  o != nullptr: output rows; h: state before every chunk ([rows,Hv,K,V], or [..,V,K]
+// when h_vfirst); delta: Delta of every chunk; seg_start: transposed fp32 start states [N,Hv,nseg,V,K]
+// replacing h0 (from launch_chain_fwd_affine).  P, rq, rk: from launch_wy_fwd / launch_chunk_p_tc (P is read
+// only when o != nullptr; rq, rk only with in-kernel L2 normalisation).
 cudaError_t launch_chain_ws(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
                             const void *beta, const void *A, const void *P, const float *rq, const float *rk,
-                            const float *h0, const float *seg_start, void *o, float *final_state, void *h,
+                            const float *h0, const float *seg_start, int nseg, void *o, float *final_state, void *h,
                             bool h_vfirst, void *delta, cudaStream_t s);
+// The intra-GPU split's first two steps (sw.nseg > 1): the segment-affine passes and the scan, leaving the
+// start state of every segment in sw.start (forward: from h0; reverse: the gradient at every segment's end,
+// from dht).
+cudaError_t launch_chain_fwd_affine(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
+                                    const void *beta, const void *A, const float *h0, const SegWs &sw, cudaStream_t s);
+cudaError_t launch_chain_bwd_affine(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
+                                    const void *A, const void *dout, const float *dht, const SegWs &sw, cudaStream_t s);
 // Backward without a sequence split, warp-specialised: the forward recompute (states h and Delta of every
 // chunk, no output) and the reverse chain (dH' and dDelta of every chunk, dh0) in one launch, one CTA each
 // per (sequence, value head).  P, rq, rk from launch_chunk_p_tc.
@@ -106,12 +113,14 @@ cudaError_t launch_chain_ws_pair(const Args &a, const void *q, const void *k, co
                                  const void *beta, const void *A, const void *P, const float *rq, const float *rk,
                                  const float *h0, void *h, void *delta, const void *dout, const float *dht,
                                  void *dhn, void *ddelta, float *dh0, cudaStream_t s);
-// Backward without a sequence split, the reverse chain alone (dH' and dDelta of every chunk, dh0), warp-
-// specialised, one CTA per (sequence, value head, 64-column slice); for callers that hold the forward's
-// states and Delta.  P, rq, rk as for launch_chain_ws_pair.
+// The reverse chain alone (dH' and dDelta of every chunk, dh0), warp-specialised, one CTA per (sequence,
+// value head, 64-column slice, and segment when nseg > 1); for callers that hold the forward's states and
+// Delta.  seg_start: the gradients at the segments' ends [N,Hv,nseg,V,K] (from launch_chain_bwd_affine),
+// replacing dht.  P, rq, rk as for launch_chain_ws_pair.
 cudaError_t launch_chain_rev(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
                              const void *A, const void *P, const float *rq, const float *rk, const void *dout,
-                             const float *dht, void *dhn, void *ddelta, float *dh0, cudaStream_t s);
+                             const float *dht, const float *seg_start, int nseg, void *dhn, void *ddelta, float *dh0,
+                             cudaStream_t s);
 // Backward: reverse state-gradient chain (dH' and dDelta of every chunk, dh0).
 cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
                              const void *A, const void *dout, const float *dht, void *dhn, void *ddelta, float *dh0,

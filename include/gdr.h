@@ -178,13 +178,13 @@ gdr_status gdr_bwd(const gdr_problem *p, const void *q, const void *k, const voi
  * recompute (no counterpart on the pages: an addition of this library): the decayed
  * causal blocks P = scale (q^ k^T o exp(G_r - G_s)) (s <= r), the inverse q/k norms,
  * the state before every chunk and Delta = U - W h of every chunk.  The backward then
- * runs the reverse state-gradient chain alone.  Results equal gdr_fwd / gdr_bwd up to
- * rounding (the same quantities, computed by other kernels).  The buffer costs
- * memory: for B x T tokens and Hv heads about B*T*Hv*(128 + 8 + 2*128*128/64 + 2*128)
- * bytes at 16-bit data, i.e. about 0.9 KB per token and head.
- *   gdr_saved_bytes: bytes of the saved buffer for problem p (host-only; when p runs
- *     the intra-GPU sequence split, which uses no P, only the in-kernel gate's part, so 0
- *     without GDR_GATE_IN_KERNEL -- the buffer is then unused).
+ * runs the reverse state-gradient chain alone (with the intra-GPU sequence split: the
+ * reverse segment passes and that chain; the forward recompute is skipped).  Results
+ * equal gdr_fwd / gdr_bwd up to rounding (the same quantities, computed by other
+ * kernels).  The buffer costs memory: for B x T tokens and Hv heads about
+ * B*T*Hv*(128 + 8 + 2*128*128/64 + 2*128) bytes at 16-bit data, i.e. about 0.9 KB per
+ * token and head.
+ *   gdr_saved_bytes: bytes of the saved buffer for problem p (host-only).
  *   saved: DEVICE buffer of at least gdr_saved_bytes bytes, 256-byte aligned, owned by
  *     the caller; NULL gives gdr_fwd / gdr_bwd exactly.  gdr_fwd_ex writes it;
  *     gdr_bwd_ex reads it and must get the buffer written by gdr_fwd_ex for the same
@@ -197,8 +197,8 @@ gdr_status gdr_saved_bytes(const gdr_problem *p, size_t *bytes);
 /* Workspace bytes that gdr_fwd_ex (backward == 0) or gdr_bwd_ex (backward != 0) needs
  * when it is given a saved buffer (host-only): the parts that the buffer holds instead
  * (P and the norms; in the backward also the states and Delta) are left out, so this is
- * at most gdr_fwd_workspace_size / gdr_bwd_workspace_size (equal when the problem runs
- * the intra-GPU split).  Errors as gdr_fwd_workspace_size. */
+ * at most gdr_fwd_workspace_size / gdr_bwd_workspace_size.  Errors as
+ * gdr_fwd_workspace_size. */
 gdr_status gdr_saved_workspace_size(const gdr_problem *p, int backward, size_t *bytes);
 gdr_status gdr_fwd_ex(const gdr_problem *p, const void *q, const void *k, const void *v,
                       const void *g, const void *beta, const float *h0, void *o,

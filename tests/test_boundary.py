@@ -144,15 +144,13 @@ def test_saved_buffer_size_and_exclusive_states(lib, fake_ptrs):
     P = 0x100000
     st = lib.gdr_fwd_ex(ctypes.byref(p), P, P, P, P, P, None, P, None, None, None, P, 0x200000, 1 << 40, P, None)
     assert st == 4
-    # the split path keeps nothing, so there the two do not clash (the call goes on to the device checks:
-    # only without a GPU, since the pointers here are not device memory)
+    # the intra-GPU split keeps the same parts (its forward stores the states for its backward too)
     ps = prob(B=1, T=65536, Hq=16, Hv=16, num_segments=4)
-    assert lib.gdr_saved_bytes(ctypes.byref(ps), ctypes.byref(n)) == 0 and n.value == 0
-    import torch
-    if not torch.cuda.is_available():
-        st = lib.gdr_fwd_ex(ctypes.byref(ps), P, P, P, P, P, None, P, None, None, None, P, 0x200000, 1 << 40, P,
-                            None)
-        assert st in (5, 10)
+    assert lib.gdr_saved_bytes(ctypes.byref(ps), ctypes.byref(n)) == 0
+    tok, rows = 65536 * 16, 1024 * 16
+    assert n.value == tok * 64 * 2 + 2 * tok * 4 + rows * 128 * 128 * 2 + rows * 64 * 128 * 2
+    st = lib.gdr_fwd_ex(ctypes.byref(ps), P, P, P, P, P, None, P, None, None, None, P, 0x200000, 1 << 40, P, None)
+    assert st == 4
 
 
 def test_binding_rejects_states_with_saved():
@@ -175,13 +173,16 @@ def test_saved_workspace_sizes(lib):
         assert lib.gdr_saved_workspace_size(ctypes.byref(p), backward, ctypes.byref(m)) == 0
         kept = tok * 64 * 2 + 2 * tok * 4 + (rows * 128 * 128 * 2 + rows * 64 * 128 * 2 if backward else 0)
         assert n.value - m.value == kept
-    # the split path keeps nothing: the sizes agree
+    # the intra-GPU split (no in-kernel L2 norm): the forward leaves out P; the backward, whose recompute
+    # without the buffer needs no P, leaves out the states and Delta
     ps = prob(B=1, T=65536, Hq=16, Hv=16, num_segments=4)
+    tok, rows = 65536 * 16, 1024 * 16
     for backward in (0, 1):
         full = lib.gdr_bwd_workspace_size if backward else lib.gdr_fwd_workspace_size
         assert full(ctypes.byref(ps), ctypes.byref(n)) == 0
         assert lib.gdr_saved_workspace_size(ctypes.byref(ps), backward, ctypes.byref(m)) == 0
-        assert n.value == m.value
+        kept = rows * 128 * 128 * 2 + rows * 64 * 128 * 2 if backward else tok * 64 * 2
+        assert n.value - m.value == kept
     assert lib.gdr_saved_workspace_size(ctypes.byref(prob(K=60)), 1, ctypes.byref(m)) == 2
 
 
@@ -217,8 +218,11 @@ def test_activation_options_are_accepted_and_the_gate_backward_needs_saved(lib, 
     p = prob(flags=act)
     assert lib.gdr_fwd_workspace_size(ctypes.byref(p), ctypes.byref(n)) == 0
     assert lib.gdr_saved_bytes(ctypes.byref(p), ctypes.byref(n)) == 0 and n.value > 0
+    # the gate activation's derivative (tokens x Hv fp32) comes first, then the parts of the plain buffer
     ps = prob(B=1, T=65536, Hq=16, Hv=16, num_segments=4, flags=_lib.GDR_GATE_IN_KERNEL)
-    assert lib.gdr_saved_bytes(ctypes.byref(ps), ctypes.byref(n)) == 0 and n.value == 65536 * 16 * 4
+    m = ctypes.c_size_t()
+    assert lib.gdr_saved_bytes(ctypes.byref(prob(B=1, T=65536, Hq=16, Hv=16, num_segments=4)), ctypes.byref(m)) == 0
+    assert lib.gdr_saved_bytes(ctypes.byref(ps), ctypes.byref(n)) == 0 and n.value == m.value + 65536 * 16 * 4
     P = 0x100000
     st = lib.gdr_bwd(ctypes.byref(p), P, P, P, P, P, P, P, None, None, P, P, P, P, P, None, 0x200000, 1 << 40, None)
     assert st == 4

@@ -107,7 +107,7 @@ def test_beta_options_without_saved_buffer(act):
 
 
 def test_all_options_split_path():
-    """The intra-GPU sequence split keeps only the gate activation's part in the saved buffer."""
+    """The intra-GPU sequence split with the saved buffer (the forward keeps its states for the backward)."""
     check(custom(B=1, T=700, Hq=1, Hv=2, host_l2=False), True, ALL, seed=37, num_segments=3)
 
 

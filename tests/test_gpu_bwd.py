@@ -137,7 +137,7 @@ def test_autograd_function():
 # and without the buffer (forward recompute beside the reverse chain); the long sequence runs the split path;
 # the dense variants with in-kernel activations and with head dimension 64 run as the benchmark times them
 @pytest.mark.parametrize("name,saved", [("dense", True), ("dense", False), ("varlen", True), ("gva", True),
-                                        ("long", False), ("dense_act", True), ("dense_hd64", True)])
+                                        ("long", False), ("long", True), ("dense_act", True), ("dense_hd64", True)])
 def test_full_size_all_heads(name, saved):
     w = WORKLOADS[name]
     check_bwd(w, kernel_l2=not w.host_l2, saved=saved)
