@@ -172,16 +172,18 @@ int choose_nseg(const gdr_problem *p) {
     const int64_t maxc = std::max<int64_t>(1, ((int64_t)p->T + C - 1) / C);
     if (p->num_segments > 0) return (int)std::max<int64_t>(1, std::min<int64_t>({p->num_segments, maxc, 64}));
     auto waves = [&](int64_t ctas) { return (ctas + kSplitSMs - 1) / kSplitSMs; };
-    // Time in units of one step of the warp-specialised chains (one chunk of one 64-column slice; both run
-    // one CTA per SM).  Unsplit: every (sequence, head) walks its chunks in two slices.  Split into s
-    // segments: the segment-affine passes (two CTAs per segment and head, about 2.1 units per chunk over
-    // the forward and reverse chains), the segments' full passes (two slices each), the scan and the two
-    // extra launches.
-    double best = (double)waves(2 * streams) * (double)maxc;
+    // Time of the forward and reverse chains in units of one step of the warp-specialised chains (one chunk
+    // of one 64-column slice; every chain CTA runs alone on an SM).  Unsplit: every (sequence, head) walks
+    // its chunks in two slices, in both directions.  Split into s segments: the forward's segment-affine
+    // pass (two CTAs per segment and head, 1.7 units per chunk), the reverse one (its zero-start half alone,
+    // 2.5 units per chunk: the transfer matrices are the forward's, transposed), the full passes (two slices
+    // per segment and head), the scans and the extra launches.
+    double best = 2.0 * (double)waves(2 * streams) * (double)maxc;
     int best_s = 1;
     for (int64_t s = 2; s <= std::min<int64_t>(64, maxc); ++s) {
         const double per = (double)((maxc + s - 1) / s);
-        const double cost = per * 3.1 * (double)waves(2 * s * streams) + 1.5 * (double)s + 8.0;
+        const double w2 = (double)waves(2 * s * streams), w1 = (double)waves(s * streams);
+        const double cost = per * (3.7 * w2 + 2.5 * w1) + 3.0 * (double)s + 16.0;
         if (cost < 0.95 * best) {
             best = cost;
             best_s = (int)s;
@@ -287,10 +289,11 @@ Layout layout_of(const gdr_problem *p, bool bwd, bool kept = false) {
 
 // What the forward keeps for the backward (gdr_fwd_ex / gdr_bwd_ex), 256-byte aligned parts: the decayed
 // causal blocks P [tokens x Hv x 64 (dtype)], the inverse q/k norms rq, rk [tokens x Hv fp32], the states h
-// and Delta of every chunk ("blocks"), and with GDR_GATE_IN_KERNEL first sigmoid(-x) of the raw gate
+// and Delta of every chunk ("blocks"), with the intra-GPU split the segments' transfer matrices
+// [N x Hv x segments x 128 x 128 fp32], and with GDR_GATE_IN_KERNEL first sigmoid(-x) of the raw gate
 // [tokens x Hv fp32] (the derivative of the gate activation).
 struct SavedLayout {
-    size_t P = 0, rq = 0, rk = 0, h = 0, delta = 0, gate = 0, bytes = 0;
+    size_t P = 0, rq = 0, rk = 0, h = 0, delta = 0, gate = 0, segp = 0, bytes = 0;
     bool blocks = false;
 };
 SavedLayout saved_layout_of(const gdr_problem *p) {
@@ -313,6 +316,12 @@ SavedLayout saved_layout_of(const gdr_problem *p) {
     at = round_up(at + mc * p->Hv * DK * DV * esize(p->dtype), 256);
     S.delta = at;
     at = round_up(at + mc * p->Hv * C * DV * esize(p->dtype), 256);
+    const int nseg = choose_nseg(p);
+    if (nseg > 1) {
+        // the intra-GPU split's segment transfer matrices (the identity-start affine pass of the forward)
+        S.segp = at;
+        at = round_up(at + (size_t)num_seqs(p) * p->Hv * nseg * DK * DV * sizeof(float), 256);
+    }
     S.bytes = at;
     return S;
 }
@@ -615,9 +624,11 @@ static gdr_status fwd_core(const gdr_problem *p, int tk, int tv, const void *q, 
     }
     float *gcs = g_cumsum ? g_cumsum : reinterpret_cast<float *>(ws + L.gcs);
     void *Aw = A ? A : static_cast<void *>(ws + L.A);
-    const SegWs sw = seg_ws(L, ws);
+    SegWs sw = seg_ws(L, ws);
     // P and the norms go to the caller's saved buffer when one is given (the backward then skips its P pass)
     char *sv = (saved && S.blocks) ? static_cast<char *>(saved) : nullptr;
+    // ... and so do the split's segment transfer matrices (the backward's transfer matrices are their transposes)
+    if (sv && sw.nseg > 1) sw.end1 = reinterpret_cast<float *>(sv + S.segp);
     void *Pw = sv ? sv + S.P : ws + L.P;
     float *rqw = a.l2norm ? reinterpret_cast<float *>(sv ? sv + S.rq : ws + L.rq) : nullptr;
     float *rkw = a.l2norm ? reinterpret_cast<float *>(sv ? sv + S.rk : ws + L.rk) : nullptr;
@@ -743,7 +754,8 @@ static gdr_status bwd_core(const gdr_problem *p, int tk, int tv, const void *q, 
         dlw = const_cast<char *>(sv + S.delta);
         if ((st = timed(sw.nseg > 1 ? K_CHAIN_BWD : K_CHAIN_REV, s, [&] {
                  if (sw.nseg > 1) {
-                     const cudaError_t e = launch_chain_bwd_affine(a, q, k, g_cumsum, beta, A, dout, dht, sw, s);
+                     const cudaError_t e = launch_chain_bwd_affine(
+                         a, q, k, g_cumsum, beta, A, dout, dht, reinterpret_cast<const float *>(sv + S.segp), sw, s);
                      if (e != cudaSuccess) return e;
                  }
                  return launch_chain_rev(a, q, k, g_cumsum, beta, A, Pw, rqw, rkw, dout, dht,

@@ -104,8 +104,11 @@ cudaError_t launch_chain_ws(const Args &a, const void *q, const void *k, const v
 // from dht).
 cudaError_t launch_chain_fwd_affine(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
                                     const void *beta, const void *A, const float *h0, const SegWs &sw, cudaStream_t s);
+// fwd_transfer (nullable): the forward's identity-start end states [N,Hv,nseg,V,K] (its sw.end1); the
+// reverse pass then runs its zero-start half alone and takes the transposes as its transfer matrices.
 cudaError_t launch_chain_bwd_affine(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
-                                    const void *A, const void *dout, const float *dht, const SegWs &sw, cudaStream_t s);
+                                    const void *A, const void *dout, const float *dht, const float *fwd_transfer,
+                                    const SegWs &sw, cudaStream_t s);
 // Backward without a sequence split, warp-specialised: the forward recompute (states h and Delta of every
 // chunk, no output) and the reverse chain (dH' and dDelta of every chunk, dh0) in one launch, one CTA each
 // per (sequence, value head).  P, rq, rk from launch_chunk_p_tc.

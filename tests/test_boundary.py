@@ -144,11 +144,12 @@ def test_saved_buffer_size_and_exclusive_states(lib, fake_ptrs):
     P = 0x100000
     st = lib.gdr_fwd_ex(ctypes.byref(p), P, P, P, P, P, None, P, None, None, None, P, 0x200000, 1 << 40, P, None)
     assert st == 4
-    # the intra-GPU split keeps the same parts (its forward stores the states for its backward too)
+    # the intra-GPU split keeps the same parts (its forward stores the states for its backward too) and the
+    # segments' transfer matrices (1 sequence x 16 heads x 4 segments x 128 x 128 fp32)
     ps = prob(B=1, T=65536, Hq=16, Hv=16, num_segments=4)
     assert lib.gdr_saved_bytes(ctypes.byref(ps), ctypes.byref(n)) == 0
     tok, rows = 65536 * 16, 1024 * 16
-    assert n.value == tok * 64 * 2 + 2 * tok * 4 + rows * 128 * 128 * 2 + rows * 64 * 128 * 2
+    assert n.value == tok * 64 * 2 + 2 * tok * 4 + rows * 128 * 128 * 2 + rows * 64 * 128 * 2 + 16 * 4 * 128 * 128 * 4
     st = lib.gdr_fwd_ex(ctypes.byref(ps), P, P, P, P, P, None, P, None, None, None, P, 0x200000, 1 << 40, P, None)
     assert st == 4
 
