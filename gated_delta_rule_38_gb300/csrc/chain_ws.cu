@@ -1294,14 +1294,27 @@ bool box_map(CUtensorMap *m, void *base, const Args &a, uint64_t rows_per) {
     return make_tmap_3d(m, base, a.bf16, DV, rows_per, srows, DV * 2, rows_per * DV * 2, 64, 32, 1);
 }
 
-template <typename T>
-cudaError_t chain_rev_t(const Args &a, const RevP &p, cudaStream_t s) {
-    constexpr int BV = 64;
+// 64-column slices (two CTAs per chain, the shorter chunk step) unless they would take more waves of one
+// CTA per SM than whole-width CTAs do, for batches of equal-length sequences (a packed batch's time is its
+// longest sequence's chain, which the shorter step serves better).
+template <typename T, int BV>
+cudaError_t chain_rev_launch(const Args &a, const RevP &p, int chains, cudaStream_t s) {
     auto kern = chain_rev_kernel<T, BV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, RLay::BYTES);
     if (e != cudaSuccess) return e;
-    return launch_overlapped(kern, dim3(DV / BV, a.Hv, a.N * (p.nseg > 1 ? p.nseg : 1)), dim3(WS_NT), RLay::BYTES, s,
-                             make_geo(a), p);
+    return launch_overlapped(kern, dim3(DV / BV, a.Hv, chains), dim3(WS_NT), RLay::BYTES, s, make_geo(a), p);
+}
+
+template <typename T>
+cudaError_t chain_rev_t(const Args &a, const RevP &p, cudaStream_t s) {
+    const int chains = a.N * (p.nseg > 1 ? p.nseg : 1);
+    int dev = 0, sms = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const long long ctas = (long long)chains * a.Hv;
+    const bool wide = a.cu == nullptr && sms > 0 && (2 * ctas + sms - 1) / sms > (ctas + sms - 1) / sms;
+    return wide ? chain_rev_launch<T, 128>(a, p, chains, s) : chain_rev_launch<T, 64>(a, p, chains, s);
 }
 
 template <typename T, int BV, bool WRITE_O>
