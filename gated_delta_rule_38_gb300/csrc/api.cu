@@ -20,15 +20,19 @@ __device__ unsigned int g_gdr_error_word = 0;
 // One CTA.  Validates cu_seqlens and checks that the table has room for every
 // chunk (both before anything is written), then an exclusive scan of
 // ceil(len/chunk) gives the offsets; each sequence's rows of the chunk table
-// follow.
+// follow.  `order` (nullable, N entries): the sequences longest first (ties by
+// index), for the chains to start the longest ones first; the identity when
+// N > kOrderMax.
+constexpr int kOrderMax = 2048;
 __global__ void __launch_bounds__(1024) prep_chunks_kernel(const int32_t *__restrict__ cu, int N, int T, int chunk,
                                                            int32_t *__restrict__ idx, long long max_chunks,
                                                            int32_t *__restrict__ off, int32_t *__restrict__ total,
-                                                           unsigned *err) {
+                                                           int32_t *__restrict__ order, unsigned *err) {
     __shared__ int s_bad;
     __shared__ int s_warp[32];
     __shared__ long long s_carry;
     __shared__ unsigned long long s_need;
+    __shared__ int s_len[kOrderMax];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
     if (tid == 0) {
         s_bad = (cu[0] != 0 || (T >= 0 && cu[N] != T)) ? 1 : 0;
@@ -92,11 +96,28 @@ __global__ void __launch_bounds__(1024) prep_chunks_kernel(const int32_t *__rest
         off[N] = (int32_t)s_carry;
         *total = (int32_t)s_carry;
     }
+    if (order) {
+        if (N > kOrderMax) {
+            for (int n = tid; n < N; n += blockDim.x) order[n] = n;
+            return;
+        }
+        for (int n = tid; n < N; n += blockDim.x) s_len[n] = cu[n + 1] - cu[n];
+        __syncthreads();
+        for (int n = tid; n < N; n += blockDim.x) {
+            const int ln = s_len[n];
+            int rank = 0;
+            for (int m = 0; m < N; ++m) {
+                const int lm = s_len[m];
+                rank += (lm > ln || (lm == ln && m < n)) ? 1 : 0;
+            }
+            order[rank] = n;
+        }
+    }
 }
 
 cudaError_t launch_prep_chunks(const int32_t *cu, int N, int T, int chunk, int32_t *idx, int64_t max_chunks,
-                               int32_t *off, int32_t *total, unsigned *err, cudaStream_t s) {
-    prep_chunks_kernel<<<1, 1024, 0, s>>>(cu, N, T, chunk, idx, (long long)max_chunks, off, total, err);
+                               int32_t *off, int32_t *total, int32_t *order, unsigned *err, cudaStream_t s) {
+    prep_chunks_kernel<<<1, 1024, 0, s>>>(cu, N, T, chunk, idx, (long long)max_chunks, off, total, order, err);
     return cudaGetLastError();
 }
 
@@ -193,7 +214,7 @@ int choose_nseg(const gdr_problem *p) {
 }
 
 struct Layout {
-    size_t idx = 0, off = 0, total = 0, gcs = 0, A = 0, P = 0, rq = 0, rk = 0, h = 0, dhn = 0, delta = 0, ddelta = 0;
+    size_t idx = 0, off = 0, total = 0, order = 0, gcs = 0, A = 0, P = 0, rq = 0, rk = 0, h = 0, dhn = 0, delta = 0, ddelta = 0;
     size_t geff = 0, beff = 0, dgeff = 0, dbeff = 0;  // activated gate / beta and their gradients (fp32)
     size_t seg[3] = {0, 0, 0};
     int nseg = 1;
@@ -214,6 +235,8 @@ Layout layout_of(const gdr_problem *p, bool bwd, bool kept = false) {
         at = round_up(at + (size_t)(p->num_seqs + 1) * sizeof(int32_t), 256);
         L.total = at;
         at = round_up(at + sizeof(int32_t), 256);
+        L.order = at;
+        at = round_up(at + (size_t)p->num_seqs * sizeof(int32_t), 256);
     }
     const size_t tok = (size_t)p->B * p->T;
     L.nseg = choose_nseg(p);
@@ -387,7 +410,7 @@ Args make_args(const gdr_problem *p, unsigned *err) {
     a.v_first = (p->flags & GDR_STATE_V_FIRST) != 0;
     a.scale = p->scale;
     a.cu = p->cu_seqlens;
-    a.cidx = a.coff = a.ctotal = nullptr;
+    a.cidx = a.coff = a.ctotal = a.sorder = nullptr;
     a.max_chunks = max_chunks_of(p);
     a.err = err;
     a.flags = p->flags;
@@ -466,9 +489,11 @@ gdr_status tables(const gdr_problem *p, Args &a, char *ws, const Layout &L, cuda
     a.cidx = reinterpret_cast<int32_t *>(ws + L.idx);
     a.coff = reinterpret_cast<int32_t *>(ws + L.off);
     a.ctotal = reinterpret_cast<int32_t *>(ws + L.total);
+    a.sorder = reinterpret_cast<int32_t *>(ws + L.order);
     return timed(K_PREP, s, [&] {
         return launch_prep_chunks(p->cu_seqlens, p->num_seqs, p->T, C, const_cast<int32_t *>(a.cidx), a.max_chunks,
-                                  const_cast<int32_t *>(a.coff), const_cast<int32_t *>(a.ctotal), a.err, s);
+                                  const_cast<int32_t *>(a.coff), const_cast<int32_t *>(a.ctotal),
+                                  const_cast<int32_t *>(a.sorder), a.err, s);
     });
 }
 
@@ -497,7 +522,7 @@ gdr_status gdr_prepare_chunks(const int32_t *cu_seqlens, int num_seqs, int total
     gdr_status st = device_state(&err);
     if (st != GDR_OK) return st;
     return cuda_status(launch_prep_chunks(cu_seqlens, num_seqs, total_tokens, chunk_size, chunk_indices,
-                                          max_chunks, chunk_offsets, total_chunks, err,
+                                          max_chunks, chunk_offsets, total_chunks, nullptr, err,
                                           static_cast<cudaStream_t>(stream)));
 }
 

@@ -265,7 +265,8 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
     const int Hv = geo.Hv, Hq = geo.Hq, hq = j / (Hv / Hq);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr bool bf16 = IsBf16<T>::value;
-    const int nseg = p.nseg > 1 ? p.nseg : 1, n = nz / nseg, seg = nz - n * nseg;
+    const int nseg = p.nseg > 1 ? p.nseg : 1, rank = nz / nseg, seg = nz - rank * nseg;
+    const int n = geo.sorder ? geo.sorder[rank] : rank;  // (packed batches: the longest sequences start first)
     long long tok0;
     int len, row0;
     geo.seq(n, tok0, len, row0);
@@ -881,7 +882,8 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
     const int Hv = geo.Hv, Hq = geo.Hq, hq = j / (Hv / Hq);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr bool bf16 = IsBf16<T>::value;
-    const int nseg = p.nseg > 1 ? p.nseg : 1, n = nz / nseg, seg = nz - n * nseg;
+    const int nseg = p.nseg > 1 ? p.nseg : 1, rank = nz / nseg, seg = nz - rank * nseg;
+    const int n = geo.sorder ? geo.sorder[rank] : rank;  // (packed batches: the longest sequences start first)
     long long tok0;
     int len, row0;
     geo.seq(n, tok0, len, row0);

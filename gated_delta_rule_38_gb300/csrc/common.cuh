@@ -283,6 +283,7 @@ struct Geo {
     const int32_t *cidx;      // varlen chunk table [*,2]
     const int32_t *coff;      // varlen chunk offsets [N+1]
     const int32_t *ctotal;    // varlen total chunks
+    const int32_t *sorder;    // varlen sequence order, longest first (nullable): the chains' block -> sequence
     unsigned *err;            // device error word
     __device__ __forceinline__ int nt_dense() const { return (T + C - 1) / C; }
     // Sequence n: first token, length, first chunk row.
@@ -330,6 +331,7 @@ inline Geo make_geo(const Args &a) {
     g.cidx = a.cidx;
     g.coff = a.coff;
     g.ctotal = a.ctotal;
+    g.sorder = a.sorder;
     g.err = a.err;
     return g;
 }

@@ -22,6 +22,7 @@ struct Args {
     const int32_t *cidx;     // device chunk table [max_chunks,2] (varlen)
     const int32_t *coff;     // device chunk offsets [N+1] (varlen)
     const int32_t *ctotal;   // device total chunks (varlen)
+    const int32_t *sorder;   // device sequence order, longest first (varlen; nullable)
     int64_t max_chunks;
     unsigned *err;           // device error word
     long long wait_polls;    // >= 0: poll budget of the waits that honour it (test support); < 0 = default
@@ -75,7 +76,7 @@ cudaError_t launch_pad_state(const float *src, float *dst, long long nh, int R, 
 cudaError_t launch_unpad_state(const float *src, float *dst, long long nh, int R, int Cc, cudaStream_t s);
 
 cudaError_t launch_prep_chunks(const int32_t *cu, int N, int T, int chunk, int32_t *idx, int64_t max_chunks,
-                               int32_t *off, int32_t *total, unsigned *err, cudaStream_t s);
+                               int32_t *off, int32_t *total, int32_t *order, unsigned *err, cudaStream_t s);
 
 // Forward: per-chunk gate cumsum, WY matrix A and (P != nullptr) the decayed causal attention block
 // P = scale (q^ k^T o Gamma) [tokens,Hv,64] with the inverse q/k norms rq, rk [tokens,Hv] (written only

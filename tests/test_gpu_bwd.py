@@ -90,6 +90,27 @@ def test_varlen_with_empty_and_short_sequences():
     check_bwd(custom(seq_lens=(7, 0, 130, 64, 1, 65), Hq=2, Hv=2), kernel_l2=False)
 
 
+@pytest.mark.parametrize("saved", [False, True])
+def test_varlen_many_sequences_with_equal_lengths(saved):
+    """The chains start a packed batch's longest sequences first (a rank by length, ties by index): many
+    sequences, repeated lengths, empty ones and more chains than SMs; forward and backward."""
+    lens = (64, 130, 64, 1, 300, 130, 0, 64, 7, 300, 65, 1, 0, 129, 300, 2)
+    w = custom(seq_lens=lens, Hq=4, Hv=8, host_l2=False)
+    check_bwd(w, kernel_l2=True, saved=saved)
+    check_fwd_states(w)
+
+
+def check_fwd_states(w):
+    """The forward's output and final states of a packed batch against the oracle."""
+    x = make_inputs(w)
+    d = to_dev(x)
+    _, _, o, _, fin = gpu_fwd(w, d, True)
+    torch.cuda.synchronize()
+    ref = oracle.fwd(oracle_problem(w, True), x["q"], x["k"], x["v"], x["g"], x["beta"], h0=x["h0"])
+    assert rel_l2(np64(o), ref["o"]) <= TOL
+    assert rel_l2(np64(fin), ref["final_state"]) <= TOL
+
+
 def test_gva_fp16():
     check_bwd(custom(B=2, T=150, Hq=1, Hv=4, dtype=torch.float16, host_l2=False), kernel_l2=True)
 
