@@ -100,6 +100,12 @@ def test_varlen_many_sequences_with_equal_lengths(saved):
     check_fwd_states(w)
 
 
+def test_reverse_chain_whole_width():
+    """Equal-length batches whose 64-column reverse-chain slices would need an extra wave of SMs run it in
+    whole-width CTAs: 2 sequences x 80 heads (320 slices, 160 whole-width CTAs), through the saved buffer."""
+    check_bwd(custom(B=2, T=130, Hq=40, Hv=80, host_l2=False), kernel_l2=True, saved=True)
+
+
 def check_fwd_states(w):
     """The forward's output and final states of a packed batch against the oracle."""
     x = make_inputs(w)
