@@ -22,12 +22,14 @@ __device__ unsigned int g_gdr_error_word = 0;
 // ceil(len/chunk) gives the offsets; each sequence's rows of the chunk table
 // follow.  `order` (nullable, N entries): the sequences longest first (ties by
 // index), for the chains to start the longest ones first; the identity when
-// N > kOrderMax.
+// N > kOrderMax or on an error.  On an error *total = bad_total (0 for the
+// public tables; -1 for the library's own, which its kernels read as "no
+// tables": every sequence empty).
 constexpr int kOrderMax = 2048;
 __global__ void __launch_bounds__(1024) prep_chunks_kernel(const int32_t *__restrict__ cu, int N, int T, int chunk,
                                                            int32_t *__restrict__ idx, long long max_chunks,
                                                            int32_t *__restrict__ off, int32_t *__restrict__ total,
-                                                           int32_t *__restrict__ order, unsigned *err) {
+                                                           int32_t *__restrict__ order, int bad_total, unsigned *err) {
     __shared__ int s_bad;
     __shared__ int s_warp[32];
     __shared__ long long s_carry;
@@ -50,9 +52,11 @@ __global__ void __launch_bounds__(1024) prep_chunks_kernel(const int32_t *__rest
     __syncthreads();
     if (s_bad || (long long)s_need > max_chunks) {
         if (tid == 0) {
-            *total = 0;
+            *total = bad_total;
             raise_error(err, s_bad ? GDR_ERR_CUSEQLENS : GDR_ERR_SHAPE);
         }
+        if (order)
+            for (int n = tid; n < N; n += blockDim.x) order[n] = n;
         return;
     }
     for (int base = 0; base < N; base += blockDim.x) {
@@ -116,8 +120,10 @@ __global__ void __launch_bounds__(1024) prep_chunks_kernel(const int32_t *__rest
 }
 
 cudaError_t launch_prep_chunks(const int32_t *cu, int N, int T, int chunk, int32_t *idx, int64_t max_chunks,
-                               int32_t *off, int32_t *total, int32_t *order, unsigned *err, cudaStream_t s) {
-    prep_chunks_kernel<<<1, 1024, 0, s>>>(cu, N, T, chunk, idx, (long long)max_chunks, off, total, order, err);
+                               int32_t *off, int32_t *total, int32_t *order, int bad_total, unsigned *err,
+                               cudaStream_t s) {
+    prep_chunks_kernel<<<1, 1024, 0, s>>>(cu, N, T, chunk, idx, (long long)max_chunks, off, total, order, bad_total,
+                                          err);
     return cudaGetLastError();
 }
 
@@ -493,7 +499,7 @@ gdr_status tables(const gdr_problem *p, Args &a, char *ws, const Layout &L, cuda
     return timed(K_PREP, s, [&] {
         return launch_prep_chunks(p->cu_seqlens, p->num_seqs, p->T, C, const_cast<int32_t *>(a.cidx), a.max_chunks,
                                   const_cast<int32_t *>(a.coff), const_cast<int32_t *>(a.ctotal),
-                                  const_cast<int32_t *>(a.sorder), a.err, s);
+                                  const_cast<int32_t *>(a.sorder), -1, a.err, s);
     });
 }
 
@@ -522,7 +528,7 @@ gdr_status gdr_prepare_chunks(const int32_t *cu_seqlens, int num_seqs, int total
     gdr_status st = device_state(&err);
     if (st != GDR_OK) return st;
     return cuda_status(launch_prep_chunks(cu_seqlens, num_seqs, total_tokens, chunk_size, chunk_indices,
-                                          max_chunks, chunk_offsets, total_chunks, nullptr, err,
+                                          max_chunks, chunk_offsets, total_chunks, nullptr, 0, err,
                                           static_cast<cudaStream_t>(stream)));
 }
 

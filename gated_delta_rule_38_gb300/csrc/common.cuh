@@ -282,16 +282,21 @@ struct Geo {
     const int32_t *cu;        // nullptr = dense
     const int32_t *cidx;      // varlen chunk table [*,2]
     const int32_t *coff;      // varlen chunk offsets [N+1]
-    const int32_t *ctotal;    // varlen total chunks
+    const int32_t *ctotal;    // varlen total chunks (< 0: the tables were not built, a malformed cu_seqlens)
     const int32_t *sorder;    // varlen sequence order, longest first (nullable): the chains' block -> sequence
     unsigned *err;            // device error word
     __device__ __forceinline__ int nt_dense() const { return (T + C - 1) / C; }
-    // Sequence n: first token, length, first chunk row.
+    // Sequence n: first token, length, first chunk row.  When the varlen tables were not built (the
+    // chunk-table kernel latched an error) every sequence is empty, so no kernel walks a malformed range.
     __device__ __forceinline__ void seq(int n, long long &tok0, int &len, int &row0) const {
         if (cu == nullptr) {
             tok0 = (long long)n * T;
             len = T;
             row0 = n * nt_dense();
+        } else if (*ctotal < 0) {
+            tok0 = 0;
+            len = 0;
+            row0 = 0;
         } else {
             tok0 = cu[n];
             len = cu[n + 1] - cu[n];

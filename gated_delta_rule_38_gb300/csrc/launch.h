@@ -76,7 +76,8 @@ cudaError_t launch_pad_state(const float *src, float *dst, long long nh, int R, 
 cudaError_t launch_unpad_state(const float *src, float *dst, long long nh, int R, int Cc, cudaStream_t s);
 
 cudaError_t launch_prep_chunks(const int32_t *cu, int N, int T, int chunk, int32_t *idx, int64_t max_chunks,
-                               int32_t *off, int32_t *total, int32_t *order, unsigned *err, cudaStream_t s);
+                               int32_t *off, int32_t *total, int32_t *order, int bad_total, unsigned *err,
+                               cudaStream_t s);
 
 // Forward: per-chunk gate cumsum, WY matrix A and (P != nullptr) the decayed causal attention block
 // P = scale (q^ k^T o Gamma) [tokens,Hv,64] with the inverse q/k norms rq, rk [tokens,Hv] (written only

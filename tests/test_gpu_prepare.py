@@ -132,3 +132,38 @@ def test_table_too_small_latches_shape_error():
     cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
     buf = torch.zeros(16, dtype=torch.int32, device="cuda")
     assert lib.gdr_prepare_chunks(_p(cu_d), 2, 300, 64, _p(buf), 3, _p(buf), _p(buf), _stream()) == 2
+
+
+@pytest.mark.parametrize("cu", [[0, 70, 40, 200], [0, 70, 150, 180]], ids=["decreasing", "last_entry_short"])
+@pytest.mark.parametrize("saved", [False, True])
+def test_malformed_cu_seqlens_in_forward_and_backward(cu, saved):
+    """The forward and backward with a malformed cu_seqlens latch GDR_ERR_CUSEQLENS: their kernels treat
+    every sequence as empty (the final states equal the initial ones, dh0 equals dht, nothing is read or
+    written past the tables), and the next call with a valid cu_seqlens matches the oracle."""
+    import gated_delta_rule_38_gb300 as gdr
+    from gated_delta_rule_38_gb300.inputs import custom, make_inputs
+    from harness import TOL, np64, oracle_problem, rel_l2, to_dev
+    w = custom(seq_lens=(70, 60, 70), Hq=2, Hv=2, host_l2=False)
+    x = make_inputs(w)
+    d = to_dev(x)
+    bad = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    assert gdr.get_error() == 0
+    sv = gdr.saved_buffer(d["q"], d["v"], d["g"], cu_seqlens=bad, use_qk_l2norm_in_kernel=True) if saved else None
+    gcs, A, o, _, fin = gdr.chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                                       initial_state=d["h0"], cu_seqlens=bad,
+                                                       use_qk_l2norm_in_kernel=True, saved=sv)
+    assert gdr.get_error() == 8                    # GDR_ERR_CUSEQLENS
+    assert torch.equal(fin, d["h0"])               # every sequence empty: the states pass through
+    grads = gdr.chunk_gated_delta_rule_bwd(d["q"], d["k"], d["v"], gcs, d["beta"], A, d["do"], dht=d["dht"],
+                                           initial_state=d["h0"], cu_seqlens=bad, use_qk_l2norm_in_kernel=True,
+                                           saved=sv)
+    assert gdr.get_error() == 8
+    assert torch.equal(grads[5], d["dht"])
+    # the context is intact: a valid call next
+    good = torch.tensor(w.cu_seqlens, dtype=torch.int32, device="cuda")
+    _, _, o, _, fin = gdr.chunk_gated_delta_rule_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], initial_state=d["h0"],
+                                                     cu_seqlens=good, use_qk_l2norm_in_kernel=True)
+    torch.cuda.synchronize()
+    assert gdr.get_error() == 0
+    ref = oracle.fwd(oracle_problem(w, True), x["q"], x["k"], x["v"], x["g"], x["beta"], h0=x["h0"])
+    assert rel_l2(np64(o), ref["o"]) <= TOL and rel_l2(np64(fin), ref["final_state"]) <= TOL
