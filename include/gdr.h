@@ -38,6 +38,10 @@
  * - Every call validates its arguments on the host first and launches
  *   nothing when it returns an error.  Errors found by kernels (a malformed
  *   cu_seqlens) are latched in a device error word that gdr_get_error reads.
+ *   A forward or backward whose cu_seqlens turns out malformed treats every
+ *   sequence as empty: final_state = initial_state (zero without one), dh0 =
+ *   dht, the other outputs unspecified; nothing outside the given buffers is
+ *   touched.
  */
 #ifndef GDR_H
 #define GDR_H
