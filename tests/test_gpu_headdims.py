@@ -64,6 +64,25 @@ def test_head_dim_64_split_path():
         assert rel_l2(np64(val), (ref if key in ref else gref)[key]) <= TOL, key
 
 
+@pytest.mark.parametrize("K,V", [(64, 64), (32, 96)])
+def test_head_dims_split_path_saved(K, V):
+    """Head dims below 128 on the intra-GPU split with the saved buffer (segments on the warp-specialised
+    chains, clipped stores of o, dq, dk, dv)."""
+    w = custom(B=1, T=64 * 9 + 21, Hq=1, Hv=2, K=K, V=V, host_l2=False)
+    x = make_inputs(w, seed=54)
+    d = to_dev(x)
+    sv = gpu_saved(w, d, True, num_segments=3)
+    gcs, A, o, _, fin = gpu_fwd(w, d, True, num_segments=3, saved=sv)
+    dq, dk, dv, db, dg, dh0 = gpu_bwd(w, d, gcs, A, True, num_segments=3, saved=sv)
+    torch.cuda.synchronize()
+    pb = oracle_problem(w, True)
+    ref = oracle.fwd(pb, x["q"], x["k"], x["v"], x["g"], x["beta"], h0=x["h0"])
+    gref = oracle.bwd(pb, x["q"], x["k"], x["v"], x["g"], x["beta"], x["do"], h0=x["h0"], dht=x["dht"])
+    for key, val in (("o", o), ("final_state", fin), ("dq", dq), ("dk", dk), ("dv", dv), ("dg", dg),
+                     ("dbeta", db), ("dh0", dh0)):
+        assert rel_l2(np64(val), (ref if key in ref else gref)[key]) <= TOL, key
+
+
 def test_per_chunk_states_not_offered_when_padded():
     import gated_delta_rule_38_gb300 as gdr
     w = custom(B=1, T=64, Hq=1, Hv=1, K=64, V=64)
