@@ -69,7 +69,7 @@ def gpu_bwd(w: Workload, d, gcs, A, kernel_l2: bool, num_segments=0, gate_f32=Fa
 
 
 def gpu_saved(w: Workload, d, kernel_l2: bool, num_segments=0, gate_f32=False):
-    """The forward-to-backward buffer for this workload (None when the problem keeps nothing)."""
+    """The forward-to-backward buffer for this workload."""
     import gated_delta_rule_38_gb300 as gdr
     g = d["g"].float() if gate_f32 else d["g"]
     return gdr.saved_buffer(d["q"], d["v"], g, cu_seqlens=cu_tensor(w), use_qk_l2norm_in_kernel=kernel_l2,
