@@ -785,12 +785,16 @@ static gdr_status bwd_core(const gdr_problem *p, int tk, int tv, const void *q, 
         dlw = const_cast<char *>(sv + S.delta);
         if ((st = timed(sw.nseg > 1 ? K_CHAIN_BWD : K_CHAIN_REV, s, [&] {
                  if (sw.nseg > 1) {
-                     const cudaError_t e = launch_chain_bwd_affine(
-                         a, q, k, g_cumsum, beta, A, dout, dht, reinterpret_cast<const float *>(sv + S.segp), sw, s);
+                     // the split: every segment's gradient at its start from a zero end (the same reverse chain,
+                     // no per-chunk outputs), then the scan with the forward's transfer matrices, transposed
+                     cudaError_t e = launch_chain_rev(a, q, k, g_cumsum, beta, A, Pw, rqw, rkw, dout, nullptr, nullptr,
+                                                      sw.nseg, nullptr, nullptr, nullptr, sw.end0, s);
+                     if (e == cudaSuccess)
+                         e = launch_rev_compose(a, dht, reinterpret_cast<const float *>(sv + S.segp), sw, s);
                      if (e != cudaSuccess) return e;
                  }
                  return launch_chain_rev(a, q, k, g_cumsum, beta, A, Pw, rqw, rkw, dout, dht,
-                                         sw.nseg > 1 ? sw.start : nullptr, sw.nseg, dhw, ddlw, dh0, s);
+                                         sw.nseg > 1 ? sw.start : nullptr, sw.nseg, dhw, ddlw, dh0, nullptr, s);
              })) != GDR_OK)
             return st;
     } else if (sw.nseg == 1) {

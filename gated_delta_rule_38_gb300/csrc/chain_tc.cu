@@ -510,10 +510,8 @@ struct TcBwdP {
     float scale;
     // sequence split, mirrored: segment seg covers chunks [cb, ce), walked from ce-1 down to cb;
     // the affine pass (block x = 2*seg + kind; kind 1 = identity start with dO = 0) writes the
-    // gradient at the segment start; the full pass starts from seg_start at the segment end.
-    // kinds = 1: the affine pass runs kind 0 alone (block x = seg), the transfer matrices coming from
-    // the forward
-    int nseg, kinds;
+    // gradient at the segment start; the full pass starts from seg_start at the segment end
+    int nseg;
     const float *seg_start;
     float *seg_end0, *seg_end1;
 };
@@ -539,9 +537,8 @@ __device__ __forceinline__ void chain_bwd_body(const Geo &geo, const TcBwdP &p, 
     int len, row0;
     geo.seq(n, tok0, len, row0);
     const int nc_all = (len + C - 1) / C;
-    const bool two = AFFINE && p.kinds != 1;
-    const int seg = two ? bx >> 1 : bx;
-    const int kind = two ? bx & 1 : 0;
+    const int seg = AFFINE ? bx >> 1 : bx;
+    const int kind = AFFINE ? bx & 1 : 0;
     const int sl = (nc_all + p.nseg - 1) / p.nseg;
     const int cb = min(nc_all, seg * sl), ce = min(nc_all, cb + sl);
     const long long st_base = ((long long)n * Hv + j) * DK * DV;
@@ -831,7 +828,7 @@ cudaError_t chain_bwd_tc_t(const Args &a, const TcBwdP &p, bool affine, cudaStre
     auto kern = affine ? chain_bwd_tc_kernel<T, true> : chain_bwd_tc_kernel<T, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, B_SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid(affine && p.kinds != 1 ? 2 * p.nseg : p.nseg, a.Hv, a.N);
+    dim3 grid(affine ? 2 * p.nseg : p.nseg, a.Hv, a.N);
     kern<<<grid, NT, B_SMEM_BYTES, s>>>(make_geo(a), p);
     return cudaGetLastError();
 }
@@ -955,11 +952,12 @@ __global__ void __launch_bounds__(SCAN_NT) seg_scan_kernel(int Hv, int nseg, boo
 
 namespace {
 
-// dst[b] = src[b]^T for a batch of 128 x 128 fp32 matrices (32 x 32 tiles through shared memory).
+// dst[b] = src[b]^T for a batch of 128 x 128 fp32 matrices (32 x 32 tiles through shared memory; block x = b,
+// block y = the tile).
 __global__ void __launch_bounds__(256) transpose128_kernel(const float *__restrict__ src, float *__restrict__ dst) {
     __shared__ float t[32][33];
-    const long long base = (long long)blockIdx.z * DK * DK;
-    const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32, tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const long long base = (long long)blockIdx.x * DK * DK;
+    const int r0 = (blockIdx.y >> 2) * 32, c0 = (blockIdx.y & 3) * 32, tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
     for (int i = ty; i < 32; i += 8) t[i][tx] = src[base + (long long)(r0 + i) * DK + c0 + tx];
     __syncthreads();
     for (int i = ty; i < 32; i += 8) dst[base + (long long)(c0 + i) * DK + r0 + tx] = t[tx][i];
@@ -1001,7 +999,6 @@ TcBwdP bwd_params(const Args &a, const void *q, const void *k, const float *g_cs
     p.v_first = a.v_first;
     p.scale = a.scale;
     p.nseg = sw.nseg;
-    p.kinds = 2;
     p.seg_start = nullptr;
     p.seg_end0 = sw.end0;
     p.seg_end1 = sw.end1;
@@ -1042,21 +1039,23 @@ TcP fwd_params(const Args &a, const void *q, const void *k, const void *v, const
 }  // namespace
 
 cudaError_t launch_chain_bwd_affine(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
-                                    const void *A, const void *dout, const float *dht, const float *fwd_transfer,
-                                    const SegWs &sw, cudaStream_t s) {
+                                    const void *A, const void *dout, const float *dht, const SegWs &sw, cudaStream_t s) {
     if (sw.nseg < 2) return cudaErrorInvalidValue;
     TcBwdP p = bwd_params(a, q, k, g_cs, beta, A, dout, dht, nullptr, nullptr, nullptr, sw);
     if (p.nseg < 1) return cudaErrorInvalidValue;
-    // the reverse chain is the adjoint of the forward's linear part: a segment's transfer matrix is the
-    // transpose of the forward's, so with the forward's at hand the zero-start pass alone remains
-    if (fwd_transfer && (long long)a.N * a.Hv * sw.nseg > 65535) fwd_transfer = nullptr;  // (grid z of the transpose)
-    if (fwd_transfer) p.kinds = 1;
     cudaError_t e = a.bf16 ? chain_bwd_tc_t<__nv_bfloat16>(a, p, true, s) : chain_bwd_tc_t<__half>(a, p, true, s);
     if (e != cudaSuccess) return e;
-    if (fwd_transfer) {
-        transpose128_kernel<<<dim3(4, 4, (unsigned)((long long)a.N * a.Hv * sw.nseg)), 256, 0, s>>>(fwd_transfer, sw.end1);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
+    return launch_seg_scan(a, sw, true, dht, s);
+}
+
+// The reverse chain is the adjoint of the forward's linear part: a segment's transfer matrix for the reverse
+// scan is the transpose of the forward's.
+cudaError_t launch_rev_compose(const Args &a, const float *dht, const float *fwd_transfer, const SegWs &sw,
+                               cudaStream_t s) {
+    if (sw.nseg < 2 || !fwd_transfer) return cudaErrorInvalidValue;
+    transpose128_kernel<<<dim3((unsigned)((long long)a.N * a.Hv * sw.nseg), 16), 256, 0, s>>>(fwd_transfer, sw.end1);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     return launch_seg_scan(a, sw, true, dht, s);
 }
 
@@ -1067,7 +1066,7 @@ cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const 
     if (p.nseg < 1) return cudaErrorInvalidValue;
     cudaError_t e;
     if (sw.nseg > 1) {
-        if ((e = launch_chain_bwd_affine(a, q, k, g_cs, beta, A, dout, dht, nullptr, sw, s)) != cudaSuccess) return e;
+        if ((e = launch_chain_bwd_affine(a, q, k, g_cs, beta, A, dout, dht, sw, s)) != cudaSuccess) return e;
         p.seg_start = sw.start;
     }
     return a.bf16 ? chain_bwd_tc_t<__nv_bfloat16>(a, p, false, s) : chain_bwd_tc_t<__half>(a, p, false, s);

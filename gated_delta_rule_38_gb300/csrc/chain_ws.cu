@@ -860,6 +860,8 @@ struct RevP {
     const float *g_cs, *rq, *rk, *dht;
     const float *seg_start;  // optional end-of-segment gradients, transposed [N,Hv,nseg,V,K] fp32 (replaces dht)
     int nseg;                // segments per sequence (1 = none): grid z = N x nseg
+    float *seg_end;          // optional: every segment's gradient at its start, transposed [N,Hv,nseg,V,K] fp32
+                             // (the split's zero-start reverse pass; dh0 is then not written)
     const void *beta;
     void *dhn;     // [rows,Hv,K,V]: the gradient after every chunk
     void *ddelta;  // [rows,Hv,64,V]
@@ -1231,7 +1233,10 @@ __device__ __forceinline__ void ws_rev_body(const Geo &geo, const RevP &p, const
             write_h(lc + 1);
         }
         if (lane == 0 && (p.dhn || p.ddelta)) tma::wait_all();  // the stored boxes are complete
-        if (!*flag && p.dh0 && seg == 0) {
+        if (!*flag && p.seg_end) {
+#pragma unroll
+            for (int i = 0; i < HW; ++i) p.seg_end[seg_base + (long long)(v0 + cb0 + i) * DK + d] = hS[i];
+        } else if (!*flag && p.dh0 && seg == 0) {
 #pragma unroll
             for (int i = 0; i < HW; ++i) {
                 const int e = v0 + cb0 + i;
@@ -1379,6 +1384,7 @@ cudaError_t launch_chain_ws_pair(const Args &a, const void *q, const void *k, co
     pb.dht = dht;
     pb.seg_start = nullptr;
     pb.nseg = 1;
+    pb.seg_end = nullptr;
     pb.beta = beta;
     pb.dhn = dhn;
     pb.ddelta = ddelta;
@@ -1393,7 +1399,7 @@ cudaError_t launch_chain_ws_pair(const Args &a, const void *q, const void *k, co
 cudaError_t launch_chain_rev(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
                              const void *A, const void *P, const float *rq, const float *rk, const void *dout,
                              const float *dht, const float *seg_start, int nseg, void *dhn, void *ddelta, float *dh0,
-                             cudaStream_t s) {
+                             float *seg_end, cudaStream_t s) {
     RevP pb;
     if (!ws_map(&pb.tq, q, a, a.Hq, a.K) || !ws_map(&pb.tk, k, a, a.Hq, a.K) || !ws_map(&pb.tdo, dout, a, a.Hv, a.V) ||
         !ws_map(&pb.tp, P, a, a.Hv, C) || !ws_map(&pb.ta, A, a, a.Hv, C) ||
@@ -1405,6 +1411,7 @@ cudaError_t launch_chain_rev(const Args &a, const void *q, const void *k, const 
     pb.dht = dht;
     pb.seg_start = seg_start;
     pb.nseg = nseg;
+    pb.seg_end = seg_end;
     pb.beta = beta;
     pb.dhn = dhn;
     pb.ddelta = ddelta;

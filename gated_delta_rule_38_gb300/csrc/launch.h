@@ -106,11 +106,8 @@ cudaError_t launch_chain_ws(const Args &a, const void *q, const void *k, const v
 // from dht).
 cudaError_t launch_chain_fwd_affine(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
                                     const void *beta, const void *A, const float *h0, const SegWs &sw, cudaStream_t s);
-// fwd_transfer (nullable): the forward's identity-start end states [N,Hv,nseg,V,K] (its sw.end1); the
-// reverse pass then runs its zero-start half alone and takes the transposes as its transfer matrices.
 cudaError_t launch_chain_bwd_affine(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
-                                    const void *A, const void *dout, const float *dht, const float *fwd_transfer,
-                                    const SegWs &sw, cudaStream_t s);
+                                    const void *A, const void *dout, const float *dht, const SegWs &sw, cudaStream_t s);
 // Backward without a sequence split, warp-specialised: the forward recompute (states h and Delta of every
 // chunk, no output) and the reverse chain (dH' and dDelta of every chunk, dh0) in one launch, one CTA each
 // per (sequence, value head).  P, rq, rk from launch_chunk_p_tc.
@@ -118,14 +115,21 @@ cudaError_t launch_chain_ws_pair(const Args &a, const void *q, const void *k, co
                                  const void *beta, const void *A, const void *P, const float *rq, const float *rk,
                                  const float *h0, void *h, void *delta, const void *dout, const float *dht,
                                  void *dhn, void *ddelta, float *dh0, cudaStream_t s);
-// The reverse chain alone (dH' and dDelta of every chunk, dh0), warp-specialised, one CTA per (sequence,
-// value head, 64-column slice, and segment when nseg > 1); for callers that hold the forward's states and
-// Delta.  seg_start: the gradients at the segments' ends [N,Hv,nseg,V,K] (from launch_chain_bwd_affine),
-// replacing dht.  P, rq, rk as for launch_chain_ws_pair.
+// The reverse chain alone (dH' and dDelta of every chunk (each nullable), dh0), warp-specialised, one CTA per
+// (sequence, value head, 64-column slice or whole width, and segment when nseg > 1); for callers that hold the
+// forward's states and Delta.  seg_start: the gradients at the segments' ends [N,Hv,nseg,V,K] (from the
+// scan), replacing dht.  seg_end (nullable): every segment's gradient at its start, [N,Hv,nseg,V,K], in
+// place of dh0 (with dht and seg_start NULL: the split's zero-start reverse pass).  P, rq, rk as for
+// launch_chain_ws_pair.
 cudaError_t launch_chain_rev(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
                              const void *A, const void *P, const float *rq, const float *rk, const void *dout,
                              const float *dht, const float *seg_start, int nseg, void *dhn, void *ddelta, float *dh0,
-                             cudaStream_t s);
+                             float *seg_end, cudaStream_t s);
+// The reverse scan of the split from the segments' zero-start gradients (sw.end0) and the forward's transfer
+// matrices fwd_transfer [N,Hv,nseg,V,K] (transposed into sw.end1): the gradient at every segment's end into
+// sw.start.
+cudaError_t launch_rev_compose(const Args &a, const float *dht, const float *fwd_transfer, const SegWs &sw,
+                               cudaStream_t s);
 // Backward: reverse state-gradient chain (dH' and dDelta of every chunk, dh0).
 cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
                              const void *A, const void *dout, const float *dht, void *dhn, void *ddelta, float *dh0,
