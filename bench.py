@@ -20,6 +20,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import statistics
 import subprocess
 import sys
 import threading
@@ -123,11 +124,12 @@ def recorded_traffic(name):
     return float(rec["dram_bytes"]) if h.hexdigest()[:16] == rec["sources_sha16"] else None
 
 
-def direction_report(ms, flops, nbytes, tokens, hbm, tflops):
-    """Throughput and roofline fraction of one direction (roofline = the slower of bytes at HBM bandwidth and
-    FLOPs at dense bf16 tensor peak)."""
+def direction_report(ms, flops, nbytes, tokens, hbm, tflops, median_ms=None):
+    """Throughput and roofline fraction of one direction from its mean time (roofline = the slower of bytes at
+    HBM bandwidth and FLOPs at dense bf16 tensor peak); the median time beside it when given."""
     rl_us = max(nbytes / (hbm * 1e9), flops / (tflops * 1e12)) * 1e6
-    return {"us": round(ms * 1e3, 2), "tokens_per_s": round(tokens / (ms * 1e-3), 1),
+    extra = {} if median_ms is None else {"us_median": round(median_ms * 1e3, 2)}
+    return {"us": round(ms * 1e3, 2), **extra, "tokens_per_s": round(tokens / (ms * 1e-3), 1),
             "tflops": round(flops / (ms * 1e-3) / 1e12, 2), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
             "roofline_us": round(rl_us, 2), "roofline_frac": round(rl_us / (ms * 1e3), 4),
             "algorithmic_bytes": int(nbytes), "algorithmic_flops": int(flops)}
@@ -249,7 +251,7 @@ def _make_step(gdr, w, cu, saved):
 
 def _direction_times(fwd, bwd, d, steps, flush, stream):
     """Mean device ms of the training forward, the backward, and an inference forward (no saving), each step
-    timed with CUDA events on the launching stream and the L2 flushed before it."""
+    timed with CUDA events on the launching stream and the L2 flushed before it; and their medians (a dict)."""
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     for i in range(steps):
         flush.zero_()
@@ -265,20 +267,26 @@ def _direction_times(fwd, bwd, d, steps, flush, stream):
         fwd(d, save=False)
         inf[i][1].record(stream)
     torch.cuda.synchronize()
-    tf = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
-    tb = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
-    ti = sum(a.elapsed_time(b) for a, b in inf) / steps
-    return tf, tb, ti
+    f_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    b_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    i_ms = [a.elapsed_time(b) for a, b in inf]
+    fb_ms = [x + y for x, y in zip(f_ms, b_ms)]
+    med = {"train_fwd": statistics.median(f_ms), "bwd": statistics.median(b_ms), "fwd_only": statistics.median(i_ms),
+           "fwd_bwd": statistics.median(fb_ms)}
+    return sum(f_ms) / steps, sum(b_ms) / steps, sum(i_ms) / steps, med
 
 
-def _directions(w, tf, tb, ti, hbm, tflops):
+def _directions(w, tf, tb, ti, hbm, tflops, med=None):
     wk = work(w)
+    med = med or {}
     return {
-        "fwd_only": direction_report(ti, wk["fwd_flops"], wk["fwd_only_bytes"], w.tokens, hbm, tflops),
-        "train_fwd": direction_report(tf, wk["fwd_flops"], wk["train_fwd_bytes"], w.tokens, hbm, tflops),
-        "bwd": direction_report(tb, wk["bwd_flops"], wk["bwd_bytes"], w.tokens, hbm, tflops),
+        "fwd_only": direction_report(ti, wk["fwd_flops"], wk["fwd_only_bytes"], w.tokens, hbm, tflops,
+                                     med.get("fwd_only")),
+        "train_fwd": direction_report(tf, wk["fwd_flops"], wk["train_fwd_bytes"], w.tokens, hbm, tflops,
+                                      med.get("train_fwd")),
+        "bwd": direction_report(tb, wk["bwd_flops"], wk["bwd_bytes"], w.tokens, hbm, tflops, med.get("bwd")),
         "fwd_bwd": direction_report(tf + tb, wk["fwd_flops"] + wk["bwd_flops"],
-                                    wk["train_fwd_bytes"] + wk["bwd_bytes"], w.tokens, hbm, tflops),
+                                    wk["train_fwd_bytes"] + wk["bwd_bytes"], w.tokens, hbm, tflops, med.get("fwd_bwd")),
     }
 
 
@@ -335,7 +343,7 @@ def run_ours(args):
     ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / args.steps, dist, dev)
 
     # ---- per direction (events between the forward and the backward), and the inference forward
-    tf, tb, ti = _direction_times(fwd, bwd, d, args.steps, flush, stream)
+    tf, tb, ti, med = _direction_times(fwd, bwd, d, args.steps, flush, stream)
     tf, tb, ti = (max_over_ranks(t, dist, dev) for t in (tf, tb, ti))
 
     # ---- per kernel: the library's own event pairs around each launch, in a pass of its own
@@ -392,7 +400,7 @@ def run_ours(args):
     wk = work(w)
     tokens = w.tokens * world
     value = job_throughput(w.tokens, world, ms * 1e-3)
-    directions = _directions(w, tf, tb, ti, hbm, tf_sus)
+    directions = _directions(w, tf, tb, ti, hbm, tf_sus, med if world == 1 else None)
     # dominant kernel by measured time share; its algorithmic bytes are the direction's tensors it must move
     tot = sum(v[1] for v in prof.values()) or 1.0
     name, (cnt, kms) = max(prof.items(), key=lambda kv: kv[1][1])
@@ -437,14 +445,14 @@ def run_ours(args):
                 so(do_)
             torch.cuda.synchronize()
             n = max(3, min(args.steps, 50))
-            a, b, c = _direction_times(fo, bo, do_, n, flush, stream)
+            a, b, c, mo = _direction_times(fo, bo, do_, n, flush, stream)
             _lib.profile_enable(True)
             so(do_)
             torch.cuda.synchronize()
             _lib.profile_enable(False)
             kp = _lib.profile_read()
             configs[other] = {"workload": WORKLOAD_TEXT[other], "steps": n,
-                              "directions": _directions(wo, a, b, c, hbm, tf_sus),
+                              "directions": _directions(wo, a, b, c, hbm, tf_sus, mo),
                               "kernels_ms": {k: round(v[1], 4) for k, v in kp.items()}}
             del xo, do_, cuo, svo, fo, bo, so
             torch.cuda.empty_cache()

@@ -35,6 +35,10 @@ def test_direction_report():
     assert r["roofline_us"] == pytest.approx(max(3.4e9 / 6.8e12, 1e11 / 1.7e15) * 1e6, rel=1e-3)
     assert r["roofline_frac"] == pytest.approx(500.0 / 500.0, rel=1e-3)
     assert r["tokens_per_s"] == pytest.approx(8192 / 5e-4, rel=1e-6)
+    assert "us_median" not in r
+    m = bench.direction_report(ms=0.5, flops=1e11, nbytes=3.4e9, tokens=8192, hbm=6800.0, tflops=1700.0,
+                               median_ms=0.45)
+    assert m["us_median"] == 450.0 and m["us"] == 500.0 and m["roofline_frac"] == r["roofline_frac"]
 
 
 def test_kernel_bytes_cover_only_the_kernel_io():
