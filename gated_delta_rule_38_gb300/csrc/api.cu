@@ -202,16 +202,16 @@ int choose_nseg(const gdr_problem *p) {
     // Time of the forward and reverse chains in units of one step of the warp-specialised chains (one chunk
     // of one 64-column slice; every chain CTA runs alone on an SM).  Unsplit: every (sequence, head) walks
     // its chunks in two slices, in both directions.  Split into s segments: the forward's segment-affine
-    // pass (two CTAs per segment and head, 1.7 units per chunk) and full pass (two slices per segment and
-    // head); the reverse zero-start pass and full pass in whole-width CTAs (one per segment and head, 1.0 and
-    // 1.2 units per chunk; the reverse transfer matrices are the forward's, transposed); the scans and the
-    // extra launches.
+    // pass (two whole-width CTAs per segment and head, one per kind, 1.0 units per chunk) and full pass (two
+    // slices per segment and head); the reverse zero-start pass and full pass in whole-width CTAs (one per
+    // segment and head, 1.0 and 1.2 units per chunk; the reverse transfer matrices are the forward's,
+    // transposed); the scans and the extra launches.
     double best = 2.0 * (double)waves(2 * streams) * (double)maxc;
     int best_s = 1;
     for (int64_t s = 2; s <= std::min<int64_t>(64, maxc); ++s) {
         const double per = (double)((maxc + s - 1) / s);
         const double w2 = (double)waves(2 * s * streams), w1 = (double)waves(s * streams);
-        const double cost = per * (2.7 * w2 + 2.2 * w1) + 3.0 * (double)s + 16.0;
+        const double cost = per * (2.0 * w2 + 2.2 * w1) + 3.0 * (double)s + 16.0;
         if (cost < 0.95 * best) {
             best = cost;
             best_s = (int)s;
@@ -674,7 +674,8 @@ static gdr_status fwd_core(const gdr_problem *p, int tk, int tv, const void *q, 
     // same warp-specialised recurrence runs every segment from its start
     return timed(K_CHAIN_FWD, s, [&] {
         if (sw.nseg > 1) {
-            const cudaError_t e = launch_chain_fwd_affine(a, q, k, v, gcs, beta, Aw, h0, sw, s);
+            cudaError_t e = launch_chain_ws_affine(a, q, k, v, gcs, beta, Aw, rqw, rkw, sw.nseg, sw.end0, sw.end1, s);
+            if (e == cudaSuccess) e = launch_fwd_compose(a, h0, sw, s);
             if (e != cudaSuccess) return e;
         }
         return launch_chain_ws(a, q, k, v, gcs, beta, Aw, Pw, rqw, rkw, h0, sw.nseg > 1 ? sw.start : nullptr, sw.nseg,

@@ -1048,6 +1048,11 @@ cudaError_t launch_chain_bwd_affine(const Args &a, const void *q, const void *k,
     return launch_seg_scan(a, sw, true, dht, s);
 }
 
+cudaError_t launch_fwd_compose(const Args &a, const float *h0, const SegWs &sw, cudaStream_t s) {
+    if (sw.nseg < 2) return cudaErrorInvalidValue;
+    return launch_seg_scan(a, sw, false, h0, s);
+}
+
 // The reverse chain is the adjoint of the forward's linear part: a segment's transfer matrix for the reverse
 // scan is the transpose of the forward's.
 cudaError_t launch_rev_compose(const Args &a, const float *dht, const float *fwd_transfer, const SegWs &sw,

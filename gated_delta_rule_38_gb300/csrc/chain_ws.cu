@@ -102,6 +102,11 @@ struct WsP {
     void *delta;   // optional: Delta of every chunk, [rows,Hv,64,V]
     const float *seg_start;  // optional start states, transposed [N,Hv,nseg,V,K] fp32 (replaces h0)
     int nseg;                // segments per sequence (the intra-GPU split; 1 = none): grid z = N x nseg
+    // the split's segment-affine pass (BV = 128, no output): block x = kind, 0 = zero start with the values,
+    // 1 = identity start with zero values (U = 0); every segment's end state, transposed, into
+    // seg_end[kind] [N,Hv,nseg,V,K] fp32
+    bool affine;
+    float *seg_end[2];
     bool gate_f32, l2norm, v_first, h_vfirst;
     float scale;
     // with all 128 value columns in one CTA and the [K,V] layout, h and Delta leave by TMA store from the
@@ -261,7 +266,8 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
     unsigned char *smem =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
-    const int v0 = vh * BV;
+    const int kind = p.affine ? vh : 0;  // (the affine pass: block x is the kind, the slice is the whole width)
+    const int v0 = p.affine ? 0 : vh * BV;
     const int Hv = geo.Hv, Hq = geo.Hq, hq = j / (Hv / Hq);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr bool bf16 = IsBf16<T>::value;
@@ -507,7 +513,7 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
                 fa(lc, FCQ)[r] = ok ? p.scale * rq * eg : 0.f;
                 fa(lc, FCK)[r] = ok ? rk * __expf(Gl - gr) : 0.f;
                 fa(lc, FAKG)[r] = ok ? be * eg * rk : 0.f;
-                fa(lc, FAB)[r] = ok ? be : 0.f;
+                fa(lc, FAB)[r] = (ok && kind == 0) ? be : 0.f;  // (identity-start affine kind: U = 0)
             }
             // the stage's tiles, and the previous chunk's W and U groups done with the scaled copies of A
             // (warp 14 polls the barriers and the four prep warps share the result through a hardware barrier:
@@ -570,7 +576,9 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
 #pragma unroll
         for (int i = 0; i < HW; ++i) {
             const int e = v0 + cb0 + i;
-            if (p.seg_start)
+            if (p.affine)
+                hS[i] = (kind == 1 && e == d) ? 1.f : 0.f;
+            else if (p.seg_start)
                 hS[i] = p.seg_start[seg_base + (long long)e * DK + d];
             else if (p.h0)
                 hS[i] = p.h0[st_base + (p.v_first ? (long long)e * DK + d : (long long)d * DV + e)];
@@ -708,7 +716,10 @@ __device__ __forceinline__ void ws_fwd_body(const Geo &geo, const WsP &p, const 
             write_h(lc + 1);
         }
         if (lane == 0 && (p.tma_h || p.tma_delta)) tma::wait_all();  // the stored boxes are complete (issuers)
-        if (!*flag && p.fin && seg == nseg - 1) {
+        if (!*flag && p.affine) {
+#pragma unroll
+            for (int i = 0; i < HW; ++i) p.seg_end[kind][seg_base + (long long)(v0 + cb0 + i) * DK + d] = hS[i];
+        } else if (!*flag && p.fin && seg == nseg - 1) {
 #pragma unroll
             for (int i = 0; i < HW; ++i) {
                 const int e = v0 + cb0 + i;
@@ -1373,6 +1384,7 @@ cudaError_t launch_chain_ws_pair(const Args &a, const void *q, const void *k, co
     pf.delta = delta;
     pf.seg_start = nullptr;
     pf.nseg = 1;
+    pf.affine = false;
     pf.gate_f32 = a.gate_f32;
     pf.l2norm = a.l2norm;
     pf.v_first = a.v_first;
@@ -1444,6 +1456,7 @@ cudaError_t launch_chain_ws(const Args &a, const void *q, const void *k, const v
     p.delta = delta;
     p.seg_start = seg_start;
     p.nseg = nseg;
+    p.affine = false;
     p.gate_f32 = a.gate_f32;
     p.l2norm = a.l2norm;
     p.v_first = a.v_first;
@@ -1457,6 +1470,42 @@ cudaError_t launch_chain_ws(const Args &a, const void *q, const void *k, const v
     if (o)
         return a.bf16 ? chain_ws_t<__nv_bfloat16, 64, true>(a, p, s) : chain_ws_t<__half, 64, true>(a, p, s);
     return a.bf16 ? chain_ws_t<__nv_bfloat16, 64, false>(a, p, s) : chain_ws_t<__half, 64, false>(a, p, s);
+}
+
+cudaError_t launch_chain_ws_affine(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
+                                   const void *beta, const void *A, const float *rq, const float *rk, int nseg,
+                                   float *end0, float *end1, cudaStream_t s) {
+    WsP p;
+    if (nseg < 2 || !ws_map(&p.tq, q, a, a.Hq, a.K) || !ws_map(&p.tk, k, a, a.Hq, a.K) ||
+        !ws_map(&p.tv, v, a, a.Hv, a.V) || !ws_map(&p.ta, A, a, a.Hv, C))
+        return cudaErrorInvalidValue;
+    p.g_cs = g_cs;
+    p.rq = rq;
+    p.rk = rk;
+    p.h0 = nullptr;
+    p.beta = beta;
+    p.o = nullptr;
+    p.fin = nullptr;
+    p.h = nullptr;
+    p.delta = nullptr;
+    p.seg_start = nullptr;
+    p.nseg = nseg;
+    p.affine = true;
+    p.seg_end[0] = end0;
+    p.seg_end[1] = end1;
+    p.gate_f32 = a.gate_f32;
+    p.l2norm = a.l2norm;
+    p.v_first = a.v_first;
+    p.h_vfirst = false;
+    p.scale = a.scale;
+    p.tma_h = false;
+    p.tma_delta = false;
+    auto kern = a.bf16 ? chain_ws_kernel<__nv_bfloat16, 128, false> : chain_ws_kernel<__half, 128, false>;
+    const uint32_t bytes = Lay<128, false>::BYTES;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    // block x: the kind (the slice is the whole width)
+    return launch_overlapped(kern, dim3(2, a.Hv, a.N * nseg), dim3(WS_NT), bytes, s, make_geo(a), p);
 }
 
 }  // namespace gdr

@@ -101,6 +101,14 @@ cudaError_t launch_chain_ws(const Args &a, const void *q, const void *k, const v
                             const void *beta, const void *A, const void *P, const float *rq, const float *rk,
                             const float *h0, const float *seg_start, int nseg, void *o, float *final_state, void *h,
                             bool h_vfirst, void *delta, cudaStream_t s);
+// The forward's segment-affine pass of the intra-GPU split on the warp-specialised chain (whole-width CTAs, no
+// output; block x = kind): every segment's end state from a zero start (end0) and from the identity with
+// zero values (end1), transposed [N,Hv,nseg,V,K] fp32.  rq, rk: with in-kernel L2 normalisation.
+cudaError_t launch_chain_ws_affine(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
+                                   const void *beta, const void *A, const float *rq, const float *rk, int nseg,
+                                   float *end0, float *end1, cudaStream_t s);
+// The forward segment scan alone (sw.end0, sw.end1 -> sw.start, from h0).
+cudaError_t launch_fwd_compose(const Args &a, const float *h0, const SegWs &sw, cudaStream_t s);
 // The intra-GPU split's first two steps (sw.nseg > 1): the segment-affine passes and the scan, leaving the
 // start state of every segment in sw.start (forward: from h0; reverse: the gradient at every segment's end,
 // from dht).
