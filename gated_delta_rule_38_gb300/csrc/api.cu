@@ -440,11 +440,11 @@ gdr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_E
 // ---- per-kernel timing: event pairs recorded around each launch while enabled
 enum KernelId {
     K_PREP = 0, K_WY_FWD, K_CHAIN_FWD, K_CHAIN_FWD_RECOMPUTE, K_CHAIN_BWD, K_CHAIN_PAIR, K_BWD_CHUNK, K_CHUNK_P,
-    K_CHAIN_REV, K_GATE_ACT, K_PAD, K_COUNT
+    K_CHAIN_REV, K_GATE_ACT, K_PAD, K_ONECHUNK, K_COUNT
 };
 const char *const kKernelNames[K_COUNT] = {"prep_chunks", "wy_fwd",     "chain_fwd", "chain_fwd_recompute",
                                            "chain_bwd",   "chain_pair", "bwd_chunk", "chunk_p",
-                                           "chain_rev",   "gate_act",   "pad"};
+                                           "chain_rev",   "gate_act",   "pad",       "onechunk_dg"};
 struct Pending {
     int id;
     cudaEvent_t a, b;
@@ -824,6 +824,11 @@ static gdr_status bwd_core(const gdr_problem *p, int tk, int tv, const void *q, 
              return launch_bwd_chunk_tc(a, q, k, v, g_cumsum, beta, A, dout, hw, dhw, dlw, ddlw, dq, dk, dv, dg, dbeta,
                                         s);
          })) != GDR_OK)
+        return st;
+    // sequences of one chunk with both states: the exact <dht, h0> in their dg (possible only in packed batches
+    // or when T <= 64)
+    if (h0 && dht && (p->cu_seqlens || p->T <= C) &&
+        (st = timed(K_ONECHUNK, s, [&] { return launch_onechunk_dg(a, h0, dht, g_cumsum, dg, s); })) != GDR_OK)
         return st;
     if (!(p->flags & kActFlags)) return GDR_OK;
     // gradients w.r.t. the raw gate and beta

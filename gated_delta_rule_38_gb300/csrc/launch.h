@@ -142,6 +142,10 @@ cudaError_t launch_rev_compose(const Args &a, const float *dht, const float *fwd
 cudaError_t launch_chain_bwd(const Args &a, const void *q, const void *k, const float *g_cs, const void *beta,
                              const void *A, const void *dout, const float *dht, void *dhn, void *ddelta, float *dh0,
                              const SegWs &sw, cudaStream_t s);
+// Backward, after launch_bwd_chunk_tc: for sequences of one chunk, the dg correction from the fp32 h0 and dht
+// (onechunk.cu); dg in the gate dtype (a.gate_f32) or fp32.
+cudaError_t launch_onechunk_dg(const Args &a, const float *h0, const float *dht, const float *g_cs, void *dg,
+                               cudaStream_t s);
 // Backward: per-chunk gradients (dq, dk, dv, dg, dbeta).
 cudaError_t launch_bwd_chunk_tc(const Args &a, const void *q, const void *k, const void *v, const float *g_cs,
                                 const void *beta, const void *A, const void *dout, const void *h, const void *dhn,

@@ -1,0 +1,65 @@
+"""Seeded combinations of the options against the fp64 oracle, forward and backward: input dtype, gate dtype,
+where the q/k L2 norm happens, the state layout, initial and final states, GVA grouping, head dims below 128,
+packed batches, the intra-GPU split, the saved buffer and the gate / beta activations.  Each case is small;
+together they cover interactions that the targeted tests take one at a time."""
+
+import random
+
+import pytest
+import torch
+
+import oracle
+from gated_delta_rule_38_gb300.inputs import custom, make_inputs
+from harness import TOL, gpu_bwd, gpu_fwd, gpu_saved, np64, oracle_problem, rel_l2, to_dev
+
+pytestmark = pytest.mark.gpu
+
+HEADS = [(1, 1), (1, 2), (2, 2), (2, 4)]
+DIMS = [(128, 128), (128, 128), (64, 64), (32, 96), (128, 64)]
+
+
+def draw(seed):
+    r = random.Random(seed)
+    hq, hv = r.choice(HEADS)
+    k, v = r.choice(DIMS)
+    varlen = r.random() < 0.4
+    spec = dict(Hq=hq, Hv=hv, K=k, V=v, dtype=r.choice([torch.bfloat16, torch.float16]),
+                host_l2=r.random() < 0.5, state_v_first=r.random() < 0.3, has_h0=r.random() < 0.7,
+                final_state=r.random() < 0.7, activations=r.random() < 0.3, mu_g=r.choice([0.0, 1.0, 2.0]))
+    if varlen:
+        lens = [r.choice([0, 1, 7, 63, 64, 65, 130, 200]) for _ in range(r.randint(2, 5))]
+        if sum(lens) == 0:
+            lens[0] = 65
+        spec["seq_lens"] = tuple(lens)
+    else:
+        spec.update(B=r.randint(1, 2), T=r.choice([1, 64, 100, 200, 300]))
+    nseg = r.choice([0, 0, 2, 3])
+    saved = r.random() < 0.6 or spec["activations"]   # the in-kernel gate's backward needs the saved buffer
+    gate_f32 = r.random() < 0.3
+    return spec, nseg, saved, gate_f32
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_option_combinations(seed):
+    spec, nseg, saved, gate_f32 = draw(1000 + seed)
+    w = custom(name="combo", **spec)
+    kernel_l2 = not w.host_l2
+    x = make_inputs(w, seed=2000 + seed)
+    d = to_dev(x)
+    sv = gpu_saved(w, d, kernel_l2, num_segments=nseg, gate_f32=gate_f32) if saved else None
+    gcs, A, o, _, fin = gpu_fwd(w, d, kernel_l2, num_segments=nseg, gate_f32=gate_f32, saved=sv)
+    dq, dk, dv, db, dg, dh0 = gpu_bwd(w, d, gcs, A, kernel_l2, num_segments=nseg, gate_f32=gate_f32, saved=sv)
+    torch.cuda.synchronize()
+    pb = oracle_problem(w, kernel_l2)
+    ref = oracle.fwd(pb, x["q"], x["k"], x["v"], x["g"], x["beta"], h0=x["h0"])
+    gref = oracle.bwd(pb, x["q"], x["k"], x["v"], x["g"], x["beta"], x["do"], h0=x["h0"], dht=x["dht"])
+    got = {"o": o, "dq": dq, "dk": dk, "dv": dv, "dbeta": db, "dg": dg}
+    if w.final_state:
+        got["final_state"] = fin
+    if w.has_h0:
+        got["dh0"] = dh0
+    want = {**ref, **gref}
+    errs = {key: rel_l2(np64(val), want[key]) for key, val in got.items()}
+    case = dict(spec, nseg=nseg, saved=saved, gate_f32=gate_f32)
+    for key, e in errs.items():
+        assert e <= TOL, (key, e, case)

@@ -27,7 +27,7 @@ def run_split(w, kernel_l2, nseg, saved=False):
     gref = oracle.bwd(pb, x["q"], x["k"], x["v"], x["g"], x["beta"], x["do"], h0=x["h0"], dht=x["dht"])
     errs = {"o": rel_l2(np64(o), ref["o"])}
     if not saved:
-        errs["h"] = rel_l2(np64(h)[:ref["h"].shape[0]], ref["h"])
+        errs["h"] = rel_l2(np64(h[:ref["h"].shape[0]]), ref["h"])
     if w.final_state:
         errs["final_state"] = rel_l2(np64(fin), ref["final_state"])
     for key, val in zip(("dq", "dk", "dv", "dbeta", "dg", "dh0"), grads):
