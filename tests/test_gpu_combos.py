@@ -1,7 +1,13 @@
 """Seeded combinations of the options against the fp64 oracle, forward and backward: input dtype, gate dtype,
 where the q/k L2 norm happens, the state layout, initial and final states, GVA grouping, head dims below 128,
 packed batches, the intra-GPU split, the saved buffer and the gate / beta activations.  Each case is small;
-together they cover interactions that the targeted tests take one at a time."""
+together they cover interactions that the targeted tests take one at a time.
+
+The bound is 8e-3 relative L2 (the PR #998 test plan's ratio), widened only where the exact result itself
+is ill-conditioned: the per-chunk states travel between the kernels in the input dtype, so for each output
+the bound adds four times the change that rounding the given initial state and final-state gradient to that
+dtype alone makes in the fp64 oracle's result.  That change is small wherever an output sums many terms; it
+is large for a single token whose gradient (dg, dbeta) is a small difference of state terms."""
 
 import random
 
@@ -60,6 +66,14 @@ def test_option_combinations(seed):
         got["dh0"] = dh0
     want = {**ref, **gref}
     errs = {key: rel_l2(np64(val), want[key]) for key, val in got.items()}
+    floor = {key: 0.0 for key in got}
+    if w.has_h0 or w.final_state:
+        # the same oracle with the given states rounded to the input dtype (what the chunk tiles hold)
+        rnd = {key: (x[key].to(w.dtype).float() if x[key] is not None else None) for key in ("h0", "dht")}
+        ref_r = oracle.fwd(pb, x["q"], x["k"], x["v"], x["g"], x["beta"], h0=rnd["h0"])
+        gref_r = oracle.bwd(pb, x["q"], x["k"], x["v"], x["g"], x["beta"], x["do"], h0=rnd["h0"], dht=rnd["dht"])
+        want_r = {**ref_r, **gref_r}
+        floor = {key: rel_l2(want_r[key], want[key]) for key in got}
     case = dict(spec, nseg=nseg, saved=saved, gate_f32=gate_f32)
     for key, e in errs.items():
-        assert e <= TOL, (key, e, case)
+        assert e <= TOL + 4.0 * floor[key], (key, e, floor[key], case)
