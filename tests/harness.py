@@ -74,3 +74,28 @@ def gpu_saved(w: Workload, d, kernel_l2: bool, num_segments=0, gate_f32=False):
     g = d["g"].float() if gate_f32 else d["g"]
     return gdr.saved_buffer(d["q"], d["v"], g, cu_seqlens=cu_tensor(w), use_qk_l2norm_in_kernel=kernel_l2,
                             state_v_first=w.state_v_first, num_segments=num_segments, **act_options(w))
+
+
+def train_step(w: Workload, d, nseg=0, poison=False):
+    """One forward + backward of ``w`` through the saved buffer (as the training step runs it), synchronised;
+    returns copies of every output and gradient.  ``poison`` fills the fresh saved buffer with a byte pattern
+    first (nothing may depend on what it held)."""
+    import torch
+    kernel_l2 = not w.host_l2
+    saved = gpu_saved(w, d, kernel_l2, num_segments=nseg)
+    if poison and saved is not None:
+        saved.fill_(0xA5)
+    gcs, A, o, _, fin = gpu_fwd(w, d, kernel_l2, num_segments=nseg, saved=saved)
+    dq, dk, dv, db, dg, dh0 = gpu_bwd(w, d, gcs, A, kernel_l2, num_segments=nseg, saved=saved)
+    torch.cuda.current_stream().synchronize()
+    out = {"g_cumsum": gcs, "A": A, "o": o, "final_state": fin, "dq": dq, "dk": dk, "dv": dv, "dbeta": db,
+           "dg": dg, "dh0": dh0}
+    return {k: v.clone() for k, v in out.items() if v is not None}
+
+
+def assert_bit_identical(first, second, what):
+    import torch
+    assert first.keys() == second.keys()
+    for k in first:
+        a, b = first[k], second[k]
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), (what, k, (a.float() - b.float()).abs().max().item())
