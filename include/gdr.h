@@ -19,6 +19,10 @@
  *   allocated by the caller (the library never allocates device memory and
  *   never synchronises the stream, except gdr_get_error).  Every tensor
  *   pointer must be 16-byte aligned (GDR_ERR_ALIGN otherwise).
+ * - Every launch goes to the caller's stream, and no call reads device memory
+ *   on the host: the compute calls (gdr_prepare_chunks, gdr_fwd*, gdr_bwd*,
+ *   gdr_decode) may be captured into a CUDA graph and replayed; gdr_get_error
+ *   synchronises and may not.
  * - Dense batches: q,k [B,T,Hq,K]; v,o,do,dv [B,T,Hv,V]; g,beta,g_cumsum,
  *   dg,dbeta [B,T,Hv]; A [B,T,Hv,64]; states [B,Hv,K,V].
  *   Packed variable-length batches (cu_seqlens != NULL): the same with B = 1

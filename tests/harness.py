@@ -44,8 +44,18 @@ def to_dev(x, dev="cuda"):
     return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in x.items()}
 
 
+_CU = {}
+
+
 def cu_tensor(w: Workload, dev="cuda"):
-    return None if w.cu_seqlens is None else torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
+    """The workload's cu_seqlens on the device, made once per (lengths, device) and shared (read-only): a call
+    captured in a CUDA graph must not copy it from host memory."""
+    if w.cu_seqlens is None:
+        return None
+    key = (tuple(w.cu_seqlens), str(dev))
+    if key not in _CU:
+        _CU[key] = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
+    return _CU[key]
 
 
 def gpu_fwd(w: Workload, d, kernel_l2: bool, output_h=False, num_segments=0, gate_f32=False, saved=None):
