@@ -39,6 +39,61 @@ def _stream(device) -> ctypes.c_void_p:
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
+def _check(t, name, shape=None, dtype=None, like=None, optional=False, contiguous=True):
+    """The library reads and writes every tensor through a raw device pointer as a contiguous row-major array
+    of the problem's shape: anything else is refused here, before a kernel could read past its end."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if like is not None and t.device != like.device:
+        raise ValueError(f"{name} is on {t.device}, the other tensors on {like.device}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _check_tokens(q, k, v, g=None, beta=None):
+    """q, k [B,T,Hq,K] and v [B,T,Hv,V] of one dtype; g, beta [B,T,Hv] of one dtype."""
+    _check(q, "q")
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k and v must be [B, T, H, D]")
+    B, T = q.shape[0], q.shape[1]
+    _check(k, "k", q.shape, q.dtype, q)
+    _check(v, "v", (B, T) + tuple(v.shape[2:]), q.dtype, q)
+    if g is not None or beta is not None:
+        _check(g, "g", (B, T, v.shape[2]), None, q)
+        _check(beta, "beta", (B, T, v.shape[2]), g.dtype, q)
+
+
+def _check_state(t, name, p, v_first, like):
+    # (states are copied to contiguous fp32 by the callers below when they are not already)
+    if t is not None:
+        _check(t, name, _state_shape(p, v_first), None, like, contiguous=False)
+
+
+def _check_cu(cu, q):
+    if cu is not None:
+        _check(cu, "cu_seqlens", (cu.numel(),), torch.int32, q)
+        if q.shape[0] != 1:
+            raise ValueError("a packed batch (cu_seqlens) has B = 1")
+
+
+def _check_saved(saved, p, q):
+    if saved is None:
+        return
+    _check(saved, "saved", None, torch.uint8, q)
+    n = ctypes.c_size_t(0)
+    _lib.check(_lib.load().gdr_saved_bytes(ctypes.byref(p), ctypes.byref(n)), "gdr_saved_bytes")
+    if saved.numel() < n.value:
+        raise ValueError(f"saved holds {saved.numel()} bytes, this problem needs {n.value} (saved_buffer)")
+
+
 def problem(q, v, g, scale=None, cu_seqlens=None, use_qk_l2norm_in_kernel=False, state_v_first=False,
             num_segments=0, extra_flags=0, use_gate_in_kernel=False, use_beta_sigmoid_in_kernel=False,
             allow_neg_eigval=False) -> _lib.Problem:
@@ -125,11 +180,16 @@ def chunk_gated_delta_rule_fwd(q, k, v, g, beta, scale=None, initial_state=None,
     """
     if output_h and saved is not None:
         raise ValueError("output_h and saved are exclusive: with saved, the states are kept in the saved buffer")
+    _check_tokens(q, k, v, g, beta)
     lib = _lib.load()
     cu = _cu(cu_seqlens)
+    _check_cu(cu, q)
     p = problem(q, v, g, scale, cu, use_qk_l2norm_in_kernel, state_v_first, num_segments,
                 use_gate_in_kernel=use_gate_in_kernel, use_beta_sigmoid_in_kernel=use_beta_sigmoid_in_kernel,
                 allow_neg_eigval=allow_neg_eigval)
+    _check_state(initial_state, "initial_state", p, state_v_first, q)
+    _check(out, "out", v.shape, v.dtype, q, optional=True)
+    _check_saved(saved, p, q)
     dev = q.device
     B, T, Hv, V = v.shape
     o = out if out is not None else torch.empty_like(v)
@@ -160,10 +220,13 @@ def recurrent_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None,
     (zero states); with ``inplace`` the final state is written into ``initial_state`` itself (contiguous
     fp32).  Same recurrence as chunk_gated_delta_rule over the same tokens; meant for T = 1 or a few.
     """
+    _check_tokens(q, k, v, g, beta)
     lib = _lib.load()
     p = problem(q, v, g, scale, None, use_qk_l2norm_in_kernel, state_v_first, 0,
                 use_gate_in_kernel=use_gate_in_kernel, use_beta_sigmoid_in_kernel=use_beta_sigmoid_in_kernel,
                 allow_neg_eigval=allow_neg_eigval)
+    _check_state(initial_state, "initial_state", p, state_v_first, q)
+    _check(out, "out", v.shape, v.dtype, q, optional=True)
     dev = q.device
     B, T, Hv, V = v.shape
     o = out if out is not None else torch.empty_like(v)
@@ -192,12 +255,22 @@ def chunk_gated_delta_rule_bwd(q, k, v, g, beta, A, do, dht=None, scale=None, in
     options, beta is the raw beta and dg, dbeta are gradients w.r.t. the raw inputs; ``use_gate_in_kernel``
     needs ``saved``.
     """
+    _check_tokens(q, k, v)
+    B, T, Hv, V = v.shape
+    gd = gate_dtype or beta.dtype
+    _check(g, "g_cumsum", (B, T, Hv), torch.float32, q)
+    _check(beta, "beta", (B, T, Hv), gd, q)
+    _check(A, "A", (B, T, Hv, _lib.GDR_CHUNK), q.dtype, q)
+    _check(do, "do", v.shape, v.dtype, q)
     lib = _lib.load()
     cu = _cu(cu_seqlens)
-    gd = gate_dtype or beta.dtype
+    _check_cu(cu, q)
     p = problem(q, v, torch.empty(0, dtype=gd), scale, cu, use_qk_l2norm_in_kernel, state_v_first, num_segments,
                 use_gate_in_kernel=use_gate_in_kernel, use_beta_sigmoid_in_kernel=use_beta_sigmoid_in_kernel,
                 allow_neg_eigval=allow_neg_eigval)
+    _check_state(initial_state, "initial_state", p, state_v_first, q)
+    _check_state(dht, "dht", p, state_v_first, q)
+    _check_saved(saved, p, q)
     dev = q.device
     dq = torch.empty_like(q)
     dk = torch.empty_like(k)
@@ -225,6 +298,7 @@ def prepare_chunks(cu_seqlens: torch.Tensor, chunk_size: int = _lib.GDR_CHUNK, t
     """
     lib = _lib.load()
     cu = _cu(cu_seqlens)
+    _check(cu, "cu_seqlens", (cu.numel(),), torch.int32)
     N = cu.numel() - 1
     T = int(total_tokens)
     if T < 0:
@@ -277,5 +351,7 @@ def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, out
     chunk_gated_delta_rule_fwd (gradients are w.r.t. the raw g and beta)."""
     act = dict(use_gate_in_kernel=use_gate_in_kernel, use_beta_sigmoid_in_kernel=use_beta_sigmoid_in_kernel,
                allow_neg_eigval=allow_neg_eigval)
+    # the library reads contiguous arrays: views (q, k, v sliced from one fused projection) are copied first
+    q, k, v, g, beta = (t.contiguous() for t in (q, k, v, g, beta))
     return _GDR.apply(q, k, v, g, beta, scale, initial_state, output_final_state, cu_seqlens,
                       use_qk_l2norm_in_kernel, state_v_first, num_segments, act)

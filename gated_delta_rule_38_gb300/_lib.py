@@ -28,7 +28,7 @@ STATUS_NAMES = {
 EXPORTS = ["gdr_max_chunks", "gdr_prepare_chunks", "gdr_fwd_workspace_size", "gdr_bwd_workspace_size",
            "gdr_fwd", "gdr_bwd", "gdr_get_error", "gdr_status_string", "gdr_version", "gdr_profile_enable",
            "gdr_profile_read", "gdr_fwd_noalloc", "gdr_saved_bytes", "gdr_saved_workspace_size", "gdr_fwd_ex",
-           "gdr_bwd_ex", "gdr_decode", "gdr_debug_set_wait_polls"]
+           "gdr_bwd_ex", "gdr_decode", "gdr_debug_set_wait_polls", "gdr_last_cuda_error"]
 
 
 class Problem(ctypes.Structure):
@@ -43,7 +43,10 @@ class Problem(ctypes.Structure):
 class GdrError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__("%s failed: %s (%s)" % (where, STATUS_NAMES.get(status, status), status_string(status)))
+        msg = "%s failed: %s (%s)" % (where, STATUS_NAMES.get(status, status), status_string(status))
+        if status == 10:  # GDR_ERR_CUDA: name the runtime error behind it
+            msg += ": " + last_cuda_error()
+        super().__init__(msg)
 
 
 _lock = threading.Lock()
@@ -93,6 +96,8 @@ def load() -> ctypes.CDLL:
         lib.gdr_get_error.restype = i32
         lib.gdr_status_string.argtypes = [i32]
         lib.gdr_status_string.restype = ctypes.c_char_p
+        lib.gdr_last_cuda_error.argtypes = []
+        lib.gdr_last_cuda_error.restype = ctypes.c_char_p
         lib.gdr_profile_enable.argtypes = [i32]
         lib.gdr_profile_enable.restype = i32
         lib.gdr_profile_read.argtypes = [i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_longlong),
@@ -109,6 +114,14 @@ def load() -> ctypes.CDLL:
 def status_string(st: int) -> str:
     try:
         return load().gdr_status_string(int(st)).decode()
+    except Exception:  # pragma: no cover
+        return "?"
+
+
+def last_cuda_error() -> str:
+    """Name of the CUDA runtime error behind this thread's latest GDR_ERR_CUDA."""
+    try:
+        return load().gdr_last_cuda_error().decode()
     except Exception:  # pragma: no cover
         return "?"
 

@@ -2,6 +2,7 @@
 // the varlen chunk-table kernel and the device error word.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdio.h>
 #include <string.h>
 
 #include <algorithm>
@@ -10,6 +11,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "tmap.h"
 
 namespace gdr {
 
@@ -122,9 +124,26 @@ __global__ void __launch_bounds__(1024) prep_chunks_kernel(const int32_t *__rest
 cudaError_t launch_prep_chunks(const int32_t *cu, int N, int T, int chunk, int32_t *idx, int64_t max_chunks,
                                int32_t *off, int32_t *total, int32_t *order, int bad_total, unsigned *err,
                                cudaStream_t s) {
-    prep_chunks_kernel<<<1, 1024, 0, s>>>(cu, N, T, chunk, idx, (long long)max_chunks, off, total, order, bad_total,
-                                          err);
-    return cudaGetLastError();
+    return launch_plain(prep_chunks_kernel, dim3(1), dim3(1024), 0, s, cu, N, T, chunk, idx, (long long)max_chunks,
+                        off, total, order, bad_total, err);
+}
+
+namespace {
+thread_local cudaError_t g_last_cuda = cudaSuccess;  // behind this thread's latest GDR_ERR_CUDA
+thread_local const char *g_last_where = nullptr;     // the launch it came from, when known
+thread_local char g_last_text[160];
+}  // namespace
+
+gdr_status cuda_fail(cudaError_t e) {
+    g_last_cuda = e;
+    g_last_where = nullptr;
+    return GDR_ERR_CUDA;
+}
+
+const char *last_cuda_error_name() {
+    if (!g_last_where) return cudaGetErrorName(g_last_cuda);
+    snprintf(g_last_text, sizeof(g_last_text), "%s (launching %s)", cudaGetErrorName(g_last_cuda), g_last_where);
+    return g_last_text;
 }
 
 // ---------------------------------------------------------------- host helpers
@@ -139,23 +158,26 @@ unsigned *g_err_ptr[kMaxDevices];    // device address of the error word
 
 gdr_status device_state(unsigned **err) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDR_ERR_CUDA;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess) return cuda_fail(ce);
+    if (dev < 0 || dev >= kMaxDevices) return GDR_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
     if (g_dev_ok[dev] == 0) {
         int major = 0, minor = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-            return GDR_ERR_CUDA;
+        if ((ce = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (ce = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return cuda_fail(ce);
         if (major != 10 || minor != 3) {
             g_dev_ok[dev] = 2;
         } else {
             void *p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_gdr_error_word) != cudaSuccess) return GDR_ERR_CUDA;
+            if ((ce = cudaGetSymbolAddress(&p, g_gdr_error_word)) != cudaSuccess) return cuda_fail(ce);
             g_err_ptr[dev] = static_cast<unsigned *>(p);
             g_dev_ok[dev] = 1;
         }
     }
     if (g_dev_ok[dev] != 1) return GDR_ERR_DEVICE;
+    if ((ce = ensure_context()) != cudaSuccess) return cuda_fail(ce);
     *err = g_err_ptr[dev];
     return GDR_OK;
 }
@@ -435,7 +457,7 @@ gdr_status check_ws(const Layout &L, void *ws, size_t bytes) {
     return GDR_OK;
 }
 
-gdr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA; }
+gdr_status cuda_status(cudaError_t e) { return e == cudaSuccess ? GDR_OK : cuda_fail(e); }
 
 // ---- per-kernel timing: event pairs recorded around each launch while enabled
 enum KernelId {
@@ -487,7 +509,9 @@ gdr_status timed(int id, cudaStream_t s, F &&f) {
         std::lock_guard<std::mutex> lk(g_prof.mu);
         g_prof.pending.push_back(Pending{id, a, b});
     }
-    return cuda_status(e);
+    const gdr_status st = cuda_status(e);
+    if (st != GDR_OK) g_last_where = kKernelNames[id];
+    return st;
 }
 
 // Build the varlen chunk tables in the workspace (no-op for dense batches).
@@ -861,9 +885,10 @@ gdr_status gdr_get_error(void *stream) {
     unsigned *err = nullptr;
     gdr_status st = device_state(&err);
     if (st != GDR_OK) return st;
-    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GDR_ERR_CUDA;
+    cudaError_t ce = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (ce != cudaSuccess) return cuda_fail(ce);
     unsigned code = 0;
-    if (cudaMemcpy(&code, err, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess) return GDR_ERR_CUDA;
+    if ((ce = cudaMemcpy(&code, err, sizeof(code), cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(ce);
     const unsigned zero = 0;
     if (code != 0 && cudaMemcpy(err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
         return GDR_ERR_CUDA;
@@ -887,6 +912,8 @@ const char *gdr_status_string(gdr_status s) {
     }
     return "unknown status";
 }
+
+const char *gdr_last_cuda_error(void) { return gdr::last_cuda_error_name(); }
 
 int gdr_version(void) { return 100; }
 

@@ -829,8 +829,7 @@ cudaError_t chain_bwd_tc_t(const Args &a, const TcBwdP &p, bool affine, cudaStre
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, B_SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid(affine ? 2 * p.nseg : p.nseg, a.Hv, a.N);
-    kern<<<grid, NT, B_SMEM_BYTES, s>>>(make_geo(a), p);
-    return cudaGetLastError();
+    return launch_plain(kern, grid, dim3(NT), B_SMEM_BYTES, s, make_geo(a), p);
 }
 
 template <typename T>
@@ -840,8 +839,7 @@ cudaError_t chain_fwd_tc_t(const Args &a, const TcP &p, bool write_o, bool affin
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid(affine ? 2 * p.nseg : p.nseg, a.Hv, a.N);
-    kern<<<grid, NT, SMEM_BYTES, s>>>(make_geo(a), p);
-    return cudaGetLastError();
+    return launch_plain(kern, grid, dim3(NT), SMEM_BYTES, s, make_geo(a), p);
 }
 
 // Segment start states: S_0 = init (API state layout, or zero), S_{s+1} = S_s P_s + Q_s in fp32,
@@ -966,10 +964,9 @@ __global__ void __launch_bounds__(256) transpose128_kernel(const float *__restri
 cudaError_t launch_seg_scan(const Args &a, const SegWs &sw, bool reverse, const float *init, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SCAN_BYTES);
     if (e != cudaSuccess) return e;
-    seg_scan_kernel<<<dim3(DV / 16, a.Hv, a.N), SCAN_NT, SCAN_BYTES, s>>>(
-        a.Hv, sw.nseg, reverse, init, a.v_first, sw.end1, sw.end0, sw.start, a.err,
-        a.wait_polls >= 0 ? (long)a.wait_polls : 200000000L);
-    return cudaGetLastError();
+    return launch_plain(seg_scan_kernel, dim3(DV / 16, a.Hv, a.N), dim3(SCAN_NT), SCAN_BYTES, s, a.Hv, sw.nseg,
+                        reverse, init, a.v_first, sw.end1, sw.end0, sw.start, a.err,
+                        a.wait_polls >= 0 ? (long)a.wait_polls : 200000000L);
 }
 
 // [tokens][heads][cols] map with 64 x 1 x 64 boxes
@@ -1058,8 +1055,8 @@ cudaError_t launch_fwd_compose(const Args &a, const float *h0, const SegWs &sw, 
 cudaError_t launch_rev_compose(const Args &a, const float *dht, const float *fwd_transfer, const SegWs &sw,
                                cudaStream_t s) {
     if (sw.nseg < 2 || !fwd_transfer) return cudaErrorInvalidValue;
-    transpose128_kernel<<<dim3((unsigned)((long long)a.N * a.Hv * sw.nseg), 16), 256, 0, s>>>(fwd_transfer, sw.end1);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_plain(transpose128_kernel, dim3((unsigned)((long long)a.N * a.Hv * sw.nseg), 16), dim3(256),
+                                 0, s, fwd_transfer, sw.end1);
     if (e != cudaSuccess) return e;
     return launch_seg_scan(a, sw, true, dht, s);
 }

@@ -1351,8 +1351,7 @@ cudaError_t chain_ws_pair_t(const Args &a, const WsP &pf, const RevP &pb, cudaSt
     const uint32_t bytes = Lay<128, false>::BYTES > RLay::BYTES ? Lay<128, false>::BYTES : RLay::BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(1, a.Hv, 2 * a.N), WS_NT, bytes, s>>>(make_geo(a), pf, pb);
-    return cudaGetLastError();
+    return launch_plain(kern, dim3(1, a.Hv, 2 * a.N), dim3(WS_NT), bytes, s, make_geo(a), pf, pb);
 }
 
 }  // namespace

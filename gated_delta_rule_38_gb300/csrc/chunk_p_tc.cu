@@ -289,8 +289,7 @@ cudaError_t chunk_p_tc_t(const Args &a, const PpP &p, cudaStream_t s) {
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const long items = (long)a.max_chunks * a.Hq;
     const unsigned grid = (unsigned)(items < 2L * sms ? items : 2L * sms);  // two persistent CTAs per SM
-    kern<<<grid, PT, S_BYTES, s>>>(make_geo(a), p);
-    return cudaGetLastError();
+    return launch_plain(kern, dim3(grid), dim3(PT), S_BYTES, s, make_geo(a), p);
 }
 
 }  // namespace

@@ -162,11 +162,8 @@ template <typename T>
 cudaError_t decode_t(const DecArgs &d, cudaStream_t s) {
     if (d.B == 0) return cudaSuccess;
     const dim3 grid((unsigned)((long long)d.Hv * d.B));
-    if (d.K == DN && d.V == DN)
-        decode_kernel<T, true><<<grid, 2 * DN, 0, s>>>(d);
-    else
-        decode_kernel<T, false><<<grid, 2 * DN, 0, s>>>(d);
-    return cudaGetLastError();
+    if (d.K == DN && d.V == DN) return launch_plain(decode_kernel<T, true>, grid, dim3(2 * DN), 0, s, d);
+    return launch_plain(decode_kernel<T, false>, grid, dim3(2 * DN), 0, s, d);
 }
 
 }  // namespace

@@ -67,20 +67,20 @@ cudaError_t launch_gate_act_fwd(const Args &a, const void *g, const void *beta, 
     const long long n = (long long)a.B * a.T * a.Hv;
     if (n == 0) return cudaSuccess;
     if (a.bf16)
-        gate_act_fwd_kernel<__nv_bfloat16><<<blocks_for(n), 256, 0, s>>>(g, beta, a.gate_f32, n, flags, geff, beff, sg);
-    else
-        gate_act_fwd_kernel<__half><<<blocks_for(n), 256, 0, s>>>(g, beta, a.gate_f32, n, flags, geff, beff, sg);
-    return cudaGetLastError();
+        return launch_plain(gate_act_fwd_kernel<__nv_bfloat16>, dim3(blocks_for(n)), dim3(256), 0, s, g, beta,
+                            a.gate_f32, n, flags, geff, beff, sg);
+    return launch_plain(gate_act_fwd_kernel<__half>, dim3(blocks_for(n)), dim3(256), 0, s, g, beta, a.gate_f32, n,
+                        flags, geff, beff, sg);
 }
 
 cudaError_t launch_gate_act_beta(const Args &a, const void *beta, unsigned flags, float *beff, cudaStream_t s) {
     const long long n = (long long)a.B * a.T * a.Hv;
     if (n == 0) return cudaSuccess;
     if (a.bf16)
-        gate_act_beta_kernel<__nv_bfloat16><<<blocks_for(n), 256, 0, s>>>(beta, a.gate_f32, n, flags, beff);
-    else
-        gate_act_beta_kernel<__half><<<blocks_for(n), 256, 0, s>>>(beta, a.gate_f32, n, flags, beff);
-    return cudaGetLastError();
+        return launch_plain(gate_act_beta_kernel<__nv_bfloat16>, dim3(blocks_for(n)), dim3(256), 0, s, beta,
+                            a.gate_f32, n, flags, beff);
+    return launch_plain(gate_act_beta_kernel<__half>, dim3(blocks_for(n)), dim3(256), 0, s, beta, a.gate_f32, n,
+                        flags, beff);
 }
 
 cudaError_t launch_gate_act_bwd(const Args &a, const float *dgeff, const float *dbeff, const float *sg,
@@ -88,12 +88,10 @@ cudaError_t launch_gate_act_bwd(const Args &a, const float *dgeff, const float *
     const long long n = (long long)a.B * a.T * a.Hv;
     if (n == 0) return cudaSuccess;
     if (a.bf16)
-        gate_act_bwd_kernel<__nv_bfloat16><<<blocks_for(n), 256, 0, s>>>(dgeff, dbeff, sg, beta, a.gate_f32, n, flags,
-                                                                          dg, dbeta);
-    else
-        gate_act_bwd_kernel<__half><<<blocks_for(n), 256, 0, s>>>(dgeff, dbeff, sg, beta, a.gate_f32, n, flags, dg,
-                                                                   dbeta);
-    return cudaGetLastError();
+        return launch_plain(gate_act_bwd_kernel<__nv_bfloat16>, dim3(blocks_for(n)), dim3(256), 0, s, dgeff, dbeff,
+                            sg, beta, a.gate_f32, n, flags, dg, dbeta);
+    return launch_plain(gate_act_bwd_kernel<__half>, dim3(blocks_for(n)), dim3(256), 0, s, dgeff, dbeff, sg, beta,
+                        a.gate_f32, n, flags, dg, dbeta);
 }
 
 }  // namespace gdr

@@ -55,6 +55,24 @@ cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// Launch on stream s and return the launch's own status: not the calling thread's last runtime error, which
+// can hold an unrelated earlier call's result (a launch checked with cudaGetLastError reported those).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_plain(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// Records e as the CUDA error behind the calling thread's latest GDR_ERR_CUDA (gdr_last_cuda_error) and
+// returns GDR_ERR_CUDA.
+gdr_status cuda_fail(cudaError_t e);
+
 // Recurrent decode: T tokens of B sequences applied one by one to the fp32 states (state_in may be null
 // for zero states and may alias state_out); o [B,T,Hv,V].
 cudaError_t launch_decode(const Args &a, const void *q, const void *k, const void *v, const void *g,

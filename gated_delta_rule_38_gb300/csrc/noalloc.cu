@@ -17,6 +17,7 @@
 #include <mutex>
 
 #include "gdr.h"
+#include "launch.h"
 
 namespace {
 
@@ -31,11 +32,14 @@ void *g_ptr[kMaxDevices];
 // Device address of the scratch array on the current device (looked up once per device).
 gdr_status scratch_ptr(void **out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDR_ERR_CUDA;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess) return gdr::cuda_fail(ce);
+    if (dev < 0 || dev >= kMaxDevices) return GDR_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_ptr[dev]) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return GDR_ERR_CUDA;
+        if ((ce = cudaGetSymbolAddress(&p, g_noalloc_scratch)) != cudaSuccess) return gdr::cuda_fail(ce);
+        if (p == nullptr) return GDR_ERR_CUDA;
         g_ptr[dev] = p;
     }
     *out = g_ptr[dev];

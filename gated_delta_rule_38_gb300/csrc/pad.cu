@@ -44,16 +44,14 @@ __global__ void unpad_state_kernel(const float4 *__restrict__ src, float4 *__res
 
 cudaError_t launch_pad_state(const float *src, float *dst, long long nh, int R, int Cc, cudaStream_t s) {
     if (nh == 0) return cudaSuccess;
-    pad_state_kernel<<<grid_for(nh * 128 * 32), 256, 0, s>>>(reinterpret_cast<const float4 *>(src),
-                                                              reinterpret_cast<float4 *>(dst), nh, R, Cc / 4);
-    return cudaGetLastError();
+    return launch_plain(pad_state_kernel, dim3(grid_for(nh * 128 * 32)), dim3(256), 0, s,
+                        reinterpret_cast<const float4 *>(src), reinterpret_cast<float4 *>(dst), nh, R, Cc / 4);
 }
 
 cudaError_t launch_unpad_state(const float *src, float *dst, long long nh, int R, int Cc, cudaStream_t s) {
     if (nh == 0) return cudaSuccess;
-    unpad_state_kernel<<<grid_for(nh * R * (Cc / 4)), 256, 0, s>>>(reinterpret_cast<const float4 *>(src),
-                                                                    reinterpret_cast<float4 *>(dst), nh, R, Cc / 4);
-    return cudaGetLastError();
+    return launch_plain(unpad_state_kernel, dim3(grid_for(nh * R * (Cc / 4))), dim3(256), 0, s,
+                        reinterpret_cast<const float4 *>(src), reinterpret_cast<float4 *>(dst), nh, R, Cc / 4);
 }
 
 }  // namespace gdr

@@ -13,21 +13,44 @@ using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, vo
                               const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                               CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+using CtxGetFn = CUresult (*)(CUcontext *);
+
+void *driver_symbol(const char *name) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        return p;
+    return nullptr;
+}
+
 EncodeFn encoder() {
     static std::once_flag once;
     static EncodeFn fn = nullptr;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeFn>(p);
-    });
+    std::call_once(once, [] { fn = reinterpret_cast<EncodeFn>(driver_symbol("cuTensorMapEncodeTiled")); });
+    return fn;
+}
+
+CtxGetFn ctx_get() {
+    static std::once_flag once;
+    static CtxGetFn fn = nullptr;
+    std::call_once(once, [] { fn = reinterpret_cast<CtxGetFn>(driver_symbol("cuCtxGetCurrent")); });
     return fn;
 }
 
 }  // namespace
+
+cudaError_t ensure_context() {
+    CtxGetFn get = ctx_get();
+    if (!get) return cudaErrorInitializationError;
+    CUcontext c = nullptr;
+    if (get(&c) != CUDA_SUCCESS) return cudaErrorInitializationError;
+    if (c) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    return cudaSetDevice(dev);
+}
 
 bool make_tmap_3d(CUtensorMap *map, const void *base, bool bf16, uint64_t dim0, uint64_t dim1, uint64_t dim2,
                   uint64_t stride1, uint64_t stride2, uint32_t box0, uint32_t box1, uint32_t box2) {

@@ -2,9 +2,16 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace gdr {
+
+// The tensor-map encoder is a driver call and needs a current context on the calling thread, which the
+// runtime binds only lazily: a thread that has made no runtime call yet (a framework's worker thread) has
+// none.  With no current context this makes the current device's primary context current (cudaSetDevice);
+// a context the caller made current is left in place.
+cudaError_t ensure_context();
 
 // A rank-3 tiled map over a row-major [dim2][dim1][dim0] tensor of 16-bit elements (dim0 contiguous),
 // strides in bytes for dims 1 and 2, a box of box0 x box1 x box2 elements, 128-byte swizzle, zero fill

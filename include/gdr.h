@@ -270,6 +270,12 @@ gdr_status gdr_get_error(void *stream);
 /* Static text for a status code. */
 const char *gdr_status_string(gdr_status s);
 
+/* The name of the CUDA runtime error (e.g. "cudaErrorInvalidValue") behind the
+ * calling thread's most recent GDR_ERR_CUDA, followed by the kernel whose launch
+ * failed when it came from one; "cudaSuccess" before any.  The text stays valid
+ * until the thread's next call that fails; the record is per host thread. */
+const char *gdr_last_cuda_error(void);
+
 /*
  * Per-kernel timing (tracing).  gdr_profile_enable(1) clears the counters and
  * from then on brackets every kernel the library launches with a pair of CUDA
