@@ -606,11 +606,29 @@ static gdr_status bwd_core(const gdr_problem *p, int tk, int tv, const void *q, 
                            const float *h0, void *dq, void *dk, void *dv, void *dg, void *dbeta, float *dh0,
                            void *workspace, size_t workspace_bytes, const void *saved, void *stream);
 
+// A problem with no tokens (T = 0) runs no step of the recurrence: the state passes through unchanged (the
+// final states are the initial ones, the initial states' gradient is the final states'; zeros where the
+// source is absent).  Nothing else is read or written, so the token pointers may be NULL; cu_seqlens is not
+// read.
+static gdr_status no_tokens(const gdr_problem *p, const float *src, float *dst, void *stream) {
+    if (src && !aligned16(src)) return GDR_ERR_ALIGN;
+    if (!dst) return GDR_OK;
+    if (!aligned16(dst)) return GDR_ERR_ALIGN;
+    unsigned *err = nullptr;
+    gdr_status st = device_state(&err);
+    if (st != GDR_OK) return st;
+    const size_t bytes = (size_t)num_seqs(p) * p->Hv * p->K * p->V * sizeof(float);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return cuda_status(src ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, s)
+                           : cudaMemsetAsync(dst, 0, bytes, s));
+}
+
 gdr_status gdr_fwd_ex(const gdr_problem *p, const void *q, const void *k, const void *v, const void *g,
                       const void *beta, const float *h0, void *o, float *final_state, float *g_cumsum, void *A,
                       void *h, void *workspace, size_t workspace_bytes, void *saved, void *stream) {
     gdr_status st = check_problem(p);
     if (st != GDR_OK) return st;
+    if (p->T == 0) return no_tokens(p, h0, final_state, stream);
     if (!q || !k || !v || !g || !beta || !o) return GDR_ERR_NULL;
     const void *ptrs[] = {q, k, v, g, beta, h0, o, final_state, g_cumsum, A, h, p->cu_seqlens, saved};
     for (const void *x : ptrs)
@@ -721,6 +739,7 @@ gdr_status gdr_bwd_ex(const gdr_problem *p, const void *q, const void *k, const 
                       size_t workspace_bytes, const void *saved, void *stream) {
     gdr_status st = check_problem(p);
     if (st != GDR_OK) return st;
+    if (p->T == 0) return no_tokens(p, dht, dh0, stream);
     if (!q || !k || !v || !g_cumsum || !beta || !A || !dout || !dq || !dk || !dv || !dg || !dbeta)
         return GDR_ERR_NULL;
     const void *ptrs[] = {q, k, v, g_cumsum, beta, A, dout, dht, h0, dq, dk, dv, dg, dbeta, dh0, p->cu_seqlens, saved};

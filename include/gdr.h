@@ -19,6 +19,9 @@
  *   allocated by the caller (the library never allocates device memory and
  *   never synchronises the stream, except gdr_get_error).  Every tensor
  *   pointer must be 16-byte aligned (GDR_ERR_ALIGN otherwise).
+ * - T = 0 (no tokens) is a valid problem: no step runs, the final states are
+ *   the initial ones (zeros without them) and dh0 is dht (zeros without it);
+ *   the token pointers may then be NULL and cu_seqlens is not read.
  * - Every launch goes to the caller's stream, and no call reads device memory
  *   on the host: the compute calls (gdr_prepare_chunks, gdr_fwd*, gdr_bwd*,
  *   gdr_decode) may be captured into a CUDA graph and replayed; gdr_get_error

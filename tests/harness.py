@@ -86,10 +86,11 @@ def gpu_saved(w: Workload, d, kernel_l2: bool, num_segments=0, gate_f32=False):
                             state_v_first=w.state_v_first, num_segments=num_segments, **act_options(w))
 
 
-def train_step(w: Workload, d, nseg=0, poison=False):
+def train_step(w: Workload, d, nseg=0, poison=False, sync=True):
     """One forward + backward of ``w`` through the saved buffer (as the training step runs it), synchronised;
     returns copies of every output and gradient.  ``poison`` fills the fresh saved buffer with a byte pattern
-    first (nothing may depend on what it held)."""
+    first (nothing may depend on what it held).  ``sync=False``: no synchronisation, the tensors themselves
+    (still being written on the current stream)."""
     import torch
     kernel_l2 = not w.host_l2
     saved = gpu_saved(w, d, kernel_l2, num_segments=nseg)
@@ -97,9 +98,11 @@ def train_step(w: Workload, d, nseg=0, poison=False):
         saved.fill_(0xA5)
     gcs, A, o, _, fin = gpu_fwd(w, d, kernel_l2, num_segments=nseg, saved=saved)
     dq, dk, dv, db, dg, dh0 = gpu_bwd(w, d, gcs, A, kernel_l2, num_segments=nseg, saved=saved)
-    torch.cuda.current_stream().synchronize()
     out = {"g_cumsum": gcs, "A": A, "o": o, "final_state": fin, "dq": dq, "dk": dk, "dv": dv, "dbeta": db,
            "dg": dg, "dh0": dh0}
+    if not sync:
+        return {k: v for k, v in out.items() if v is not None}
+    torch.cuda.current_stream().synchronize()
     return {k: v.clone() for k, v in out.items() if v is not None}
 
 

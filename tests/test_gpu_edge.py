@@ -103,3 +103,28 @@ def test_state_v_first_bit_exact_with_saved_buffer():
     for a, b in zip(ga[:5], gb[:5]):
         assert torch.equal(a, b)
     assert torch.equal(ga[5], gb[5].transpose(-1, -2))
+
+
+@pytest.mark.parametrize("packed", [False, True])
+@pytest.mark.parametrize("saved", [False, True])
+def test_no_tokens_at_all(packed, saved):
+    """A call with no tokens (a dense batch with T = 0, or a packed batch whose every sequence is empty) runs
+    no recurrence step: the final states are the initial ones and dh0 is dht, bit for bit."""
+    import gated_delta_rule_38_gb300 as gdr
+    H, D, N = 2, 128, 3
+    B = 1 if packed else N
+    gen = torch.Generator(device="cuda").manual_seed(11)
+    q = torch.zeros(B, 0, H, D, dtype=torch.bfloat16, device="cuda")
+    g = torch.zeros(B, 0, H, dtype=torch.bfloat16, device="cuda")
+    h0 = torch.randn(N, H, D, D, device="cuda", generator=gen)
+    dht = torch.randn(N, H, D, D, device="cuda", generator=gen)
+    cu = torch.zeros(N + 1, dtype=torch.int32, device="cuda") if packed else None
+    sv = gdr.saved_buffer(q, q, g, cu_seqlens=cu) if saved else None
+    gcs, A, o, _, fin = gdr.chunk_gated_delta_rule_fwd(q, q, q, g, g, initial_state=h0, output_final_state=True,
+                                                       cu_seqlens=cu, saved=sv)
+    assert o.numel() == 0 and torch.equal(fin, h0)
+    dq, dk, dv, db, dg, dh0 = gdr.chunk_gated_delta_rule_bwd(q, q, q, gcs, g, A, q, dht=dht, initial_state=h0,
+                                                             cu_seqlens=cu, saved=sv)
+    torch.cuda.synchronize()
+    assert gdr.get_error() == 0
+    assert dq.numel() == 0 and dg.numel() == 0 and torch.equal(dh0, dht)

@@ -29,3 +29,23 @@ def test_side_stream_behind_a_sleep(name, w, nseg):
         got = train_step(w, d, nseg)
     torch.cuda.synchronize()
     assert_bit_identical(want, got, name)
+
+
+def test_two_problems_on_two_streams_at_once():
+    """Two independent steps (a dense batch and a packed one) issued on two streams without synchronising
+    between them give, bit for bit, what each gives alone: the calls share no device state that they write."""
+    w1 = custom(name="st_two_a", B=2, T=700, Hq=4, Hv=4, has_h0=True, final_state=True)
+    w2 = custom(name="st_two_b", Hq=2, Hv=4, seq_lens=(500, 3, 129), has_h0=True, final_state=True)
+    d1, d2 = to_dev(make_inputs(w1, seed=21)), to_dev(make_inputs(w2, seed=22))
+    torch.cuda.synchronize()
+    want1, want2 = train_step(w1, d1), train_step(w2, d2)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for _ in range(3):
+        # both steps in flight at once: nothing waits between the two streams' launches
+        with torch.cuda.stream(s1):
+            got1 = train_step(w1, d1, sync=False)
+        with torch.cuda.stream(s2):
+            got2 = train_step(w2, d2, sync=False)
+        torch.cuda.synchronize()
+    assert_bit_identical(want1, got1, "dense")
+    assert_bit_identical(want2, got2, "packed")
