@@ -188,6 +188,10 @@ __global__ void __launch_bounds__(WT, 4) wy_tc_kernel(Geo geo, const __grid_cons
 
     // gates of (item u, value head j) for rows 0..63 (threads 0..63), fetched one step ahead as predicated
     // loads that nothing reads before the step that uses them
+    // A log-gate below kGateFloor is taken at kGateFloor: its decay factor e^g (< 2e-35) already wipes the
+    // state at fp32 resolution, and the chunk form subtracts cumulative gates, which a gate of -inf (a hard
+    // reset) would turn into -inf - (-inf).  NaN gates pass through.
+    constexpr float kGateFloor = -80.f;
     float gnext = 0.f, bnext = 0.f;
     auto fetch_g = [&](const int4 &u, int j_) {
         gnext = 0.f;
@@ -195,6 +199,7 @@ __global__ void __launch_bounds__(WT, 4) wy_tc_kernel(Geo geo, const __grid_cons
         if (tid < u.y && tid < C) {
             const long long ti = ((long long)u.x + tid) * Hv + j_;
             gnext = load_gate<T>(p.g, ti, p.gate_f32);
+            if (gnext < kGateFloor) gnext = kGateFloor;
             bnext = load_gate<T>(p.beta, ti, p.gate_f32);
         }
     };

@@ -19,6 +19,9 @@
  *   allocated by the caller (the library never allocates device memory and
  *   never synchronises the stream, except gdr_get_error).  Every tensor
  *   pointer must be 16-byte aligned (GDR_ERR_ALIGN otherwise).
+ * - A log-gate below -80 is taken as -80 (its factor e^g < 2e-35 already wipes
+ *   the state at fp32 resolution), so g = -inf works as a hard reset; the
+ *   returned g_cumsum holds the clamped sums.  NaN gates propagate.
  * - T = 0 (no tokens) is a valid problem: no step runs, the final states are
  *   the initial ones (zeros without them) and dh0 is dht (zeros without it);
  *   the token pointers may then be NULL and cu_seqlens is not read.

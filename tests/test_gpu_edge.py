@@ -128,3 +128,25 @@ def test_no_tokens_at_all(packed, saved):
     torch.cuda.synchronize()
     assert gdr.get_error() == 0
     assert dq.numel() == 0 and dg.numel() == 0 and torch.equal(dh0, dht)
+
+
+@pytest.mark.parametrize("packed", [False, True])
+@pytest.mark.parametrize("saved", [False, True])
+def test_infinite_gate_is_a_hard_reset(packed, saved):
+    """A log-gate of -inf at some tokens (e^g = 0: the state is wiped there, a hard reset) against the oracle,
+    which applies the token recurrence literally; the chunk form, which subtracts cumulative gates, takes such
+    gates at its floor, whose factor is already zero at fp32 resolution."""
+    if packed:
+        w = custom(name="neginf_v", Hq=2, Hv=2, seq_lens=(150, 70, 1), host_l2=False, has_h0=True,
+                   final_state=True)
+    else:
+        w = custom(name="neginf", B=2, T=200, Hq=2, Hv=2, host_l2=False, has_h0=True, final_state=True)
+    x = make_inputs(w, seed=13)
+    g = x["g"].clone()
+    g[0, 0] = float("-inf")  # the first token of one sequence only: a reference dh0 of all zeros has no scale
+    for t in (37, 64, 65, 130, 151):  # inside chunks, a chunk's first token, inside a later sequence
+        if t < g.shape[1]:
+            g[:, t] = float("-inf")
+    x["g"] = g
+    got, errs = parity(w, x, kernel_l2=True, saved=saved)
+    assert all(torch.isfinite(v).all() for v in got.values() if v is not None)
