@@ -45,3 +45,26 @@ def test_two_chained_layers():
     want = [dq1, dk1, dv1, dg1, db1, dk2, dv2, dg2, db2, dh01]
     for name, leaf, w in zip(("x", "k1", "v1", "g1", "beta1", "k2", "v2", "g2", "beta2", "h0"), leaves, want):
         assert torch.equal(leaf.grad, w), name
+
+
+def test_initial_state_in_bf16():
+    """A bf16 initial state that requires grad: the library runs the states in fp32, and the gradient comes
+    back in the leaf's dtype (the fp32 state's gradient, rounded)."""
+    gen = torch.Generator(device="cuda").manual_seed(52)
+    r = lambda *s: torch.randn(*s, device="cuda", generator=gen)
+    q, k, v = (r(B, T, H, D).bfloat16() for _ in range(3))
+    g = torch.nn.functional.logsigmoid(r(B, T, H) + 2).bfloat16()
+    beta = torch.sigmoid(r(B, T, H)).bfloat16()
+    h0 = r(B, H, D, D).bfloat16()
+    wgt = r(B, T, H, D).bfloat16()
+    hb = h0.clone().requires_grad_(True)
+    hf = h0.float().requires_grad_(True)
+    ob, fb = gdr.chunk_gated_delta_rule(q, k, v, g, beta, initial_state=hb, output_final_state=True,
+                                        use_qk_l2norm_in_kernel=True)
+    of, ff = gdr.chunk_gated_delta_rule(q, k, v, g, beta, initial_state=hf, output_final_state=True,
+                                        use_qk_l2norm_in_kernel=True)
+    assert torch.equal(ob, of) and torch.equal(fb, ff)
+    (ob.float() * wgt.float()).sum().backward()
+    (of.float() * wgt.float()).sum().backward()
+    assert hb.grad.dtype == torch.bfloat16
+    assert torch.equal(hb.grad, hf.grad.bfloat16())
