@@ -45,7 +45,7 @@ def draw(seed):
     return spec, nseg, saved, gate_f32
 
 
-@pytest.mark.parametrize("seed", range(40))
+@pytest.mark.parametrize("seed", range(120))
 def test_option_combinations(seed):
     spec, nseg, saved, gate_f32 = draw(1000 + seed)
     w = custom(name="combo", **spec)
