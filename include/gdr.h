@@ -45,6 +45,11 @@
  *   gate_dtype (g,beta,dg,dbeta) is dtype or fp32.  States, final_state,
  *   initial_state, dht, dh0 and g_cumsum are fp32.
  * - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ * - Calls may come from any host thread.  When the calling thread has no
+ *   current CUDA context (one that has made no runtime call yet), the call
+ *   makes the current device's primary context current on it (cudaSetDevice):
+ *   the TMA tensor maps are encoded by a driver call that needs one.  A
+ *   context the caller made current is used as it is.
  * - Every call validates its arguments on the host first and launches
  *   nothing when it returns an error.  Errors found by kernels (a malformed
  *   cu_seqlens) are latched in a device error word that gdr_get_error reads.
@@ -75,7 +80,7 @@ typedef enum gdr_status {
     GDR_ERR_WORKSPACE = 7,   /* workspace NULL or smaller than the size query returns */
     GDR_ERR_CUSEQLENS = 8,   /* cu_seqlens not starting at 0, decreasing, or not ending at T */
     GDR_ERR_TIMEOUT = 9,     /* a bounded device-side wait expired */
-    GDR_ERR_CUDA = 10,       /* a CUDA runtime call failed */
+    GDR_ERR_CUDA = 10,       /* a CUDA runtime call failed (gdr_last_cuda_error names it) */
     GDR_ERR_INTERNAL = 11
 } gdr_status;
 
