@@ -100,6 +100,18 @@ def test_varlen_many_sequences_with_equal_lengths(saved):
     check_fwd_states(w)
 
 
+@pytest.mark.parametrize("saved", [False, True])
+def test_varlen_more_sequences_than_the_order_table(saved):
+    """More than 2,048 sequences: the chunk-table kernel ranks at most 2,048 by length and otherwise starts
+    the chains in index order.  2,500 sequences of 0 to 40 tokens (empty ones included), states given;
+    forward and backward against the oracle."""
+    rng = np.random.default_rng(7)
+    lens = tuple(int(n) for n in rng.integers(0, 41, size=2500))
+    w = custom(name="many_seqs", seq_lens=lens, Hq=1, Hv=2, host_l2=False, has_h0=True, final_state=True)
+    check_bwd(w, kernel_l2=True, saved=saved)
+    check_fwd_states(w)
+
+
 def test_reverse_chain_whole_width():
     """Equal-length batches whose 64-column reverse-chain slices would need an extra wave of SMs run it in
     whole-width CTAs: 2 sequences x 80 heads (320 slices, 160 whole-width CTAs), through the saved buffer."""
