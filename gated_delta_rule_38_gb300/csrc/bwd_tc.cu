@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
     auto item_ok = [&](int w_) {
         long long t_;
         int v_, n_, c_;
-        return geo.chunk(w_ / Hq, t_, v_, n_, c_);
+        return geo.chunk(geo.div_hq(w_), t_, v_, n_, c_);
     };
     auto next_item = [&](int w_) -> int {
         for (; w_ < nitems; w_ += (int)gridDim.x)
@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
     };
     auto locate = [&](int w_, int jj_) {
         Pos u;
-        const int slot_ = w_ / Hq;
+        const int slot_ = geo.div_hq(w_);
         long long t_;
         int n_, c_;
         geo.chunk(slot_, t_, u.valid, n_, c_);

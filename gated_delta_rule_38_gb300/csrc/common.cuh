@@ -285,7 +285,18 @@ struct Geo {
     const int32_t *ctotal;    // varlen total chunks (< 0: the tables were not built, a malformed cu_seqlens)
     const int32_t *sorder;    // varlen sequence order, longest first (nullable): the chains' block -> sequence
     unsigned *err;            // device error word
+    // Division by Hq and by the dense chunks per sequence (divisors fixed for a call) as a multiply-high, the
+    // round-up method of Granlund and Montgomery ("Division by invariant integers using multiplication"):
+    // n / d = (umulhi(n, m) + n) >> s for 0 <= n < 2^31, s = ceil(log2 d), m = floor(2^32 (2^s - d) / d) + 1.
+    uint32_t hq_m, nt_m;
+    int hq_s, nt_s;
     __device__ __forceinline__ int nt_dense() const { return (T + C - 1) / C; }
+    __device__ __forceinline__ int div_hq(int n) const {
+        return (int)((__umulhi((uint32_t)n, hq_m) + (uint32_t)n) >> hq_s);
+    }
+    __device__ __forceinline__ int div_nt(int n) const {
+        return (int)((__umulhi((uint32_t)n, nt_m) + (uint32_t)n) >> nt_s);
+    }
     // Sequence n: first token, length, first chunk row.  When the varlen tables were not built (the
     // chunk-table kernel latched an error) every sequence is empty, so no kernel walks a malformed range.
     __device__ __forceinline__ void seq(int n, long long &tok0, int &len, int &row0) const {
@@ -308,8 +319,8 @@ struct Geo {
         if (cu == nullptr) {
             const int nt = nt_dense();
             if (slot >= B * nt) return false;
-            n = slot / nt;
-            ci = slot % nt;
+            n = div_nt(slot);
+            ci = slot - n * nt;
             tok0 = (long long)n * T + (long long)ci * C;
             len = min(C, T - ci * C);
             return true;
@@ -322,6 +333,14 @@ struct Geo {
         return true;
     }
 };
+
+// The multiplier and shift that divide by d (>= 1) in Geo::div_hq / div_nt.
+inline void div_magic(int d, uint32_t &m, int &s) {
+    if (d < 1) d = 1;  // (no division happens then: a dense call without tokens has no chunks)
+    s = 0;
+    while ((1ll << s) < d) ++s;
+    m = (uint32_t)((((1ull << 32) * ((1ull << s) - (uint64_t)d)) / (uint64_t)d) + 1);
+}
 
 inline Geo make_geo(const Args &a) {
     Geo g;
@@ -338,6 +357,8 @@ inline Geo make_geo(const Args &a) {
     g.ctotal = a.ctotal;
     g.sorder = a.sorder;
     g.err = a.err;
+    div_magic(a.Hq, g.hq_m, g.hq_s);
+    div_magic((a.T + C - 1) / C, g.nt_m, g.nt_s);
     return g;
 }
 

@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(WT, 4) wy_tc_kernel(Geo geo, const __grid_cons
     auto produce = [&]() {
         int4 u = make_int4(0, -1, 0, 0);
         for (; wiss < nitems; wiss += (int)gridDim.x) {
-            const int slot_ = wiss / Hq;
+            const int slot_ = geo.div_hq(wiss);
             long long t_;
             int n_, c_, v_;
             if (geo.chunk(slot_, t_, v_, n_, c_)) {
