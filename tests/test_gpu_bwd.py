@@ -202,3 +202,12 @@ def test_back_to_back_steps_bit_identical():
     for other in runs[1:]:
         for a, b in zip(runs[0], other):
             assert torch.equal(a, b)
+
+
+# q/k head counts that are not powers of two, with and without the saved buffer (the kernels' item -> chunk
+# slot, q/k head arithmetic divides by Hq and by the chunks per sequence)
+@pytest.mark.parametrize("saved", [False, True])
+@pytest.mark.parametrize("hq,hv", [(3, 3), (3, 6), (5, 10)])
+def test_head_counts_not_powers_of_two(hq, hv, saved):
+    check_bwd(custom(B=3, T=201, Hq=hq, Hv=hv, host_l2=False), kernel_l2=True, saved=saved)
+    check_bwd(custom(seq_lens=(65, 0, 7, 130), Hq=hq, Hv=hv), kernel_l2=False, saved=saved)

@@ -108,3 +108,11 @@ def test_rejects_unaligned_and_missing():
 def test_full_size_all_heads(name):
     w = WORKLOADS[name]
     check_fwd(w, kernel_l2=not w.host_l2, check_chunks=name not in ("long", "dense_hd64"))
+
+
+# q/k head counts that are not powers of two (the kernels' item -> chunk slot, q/k head arithmetic divides by Hq
+# and by the chunks per sequence)
+@pytest.mark.parametrize("hq,hv", [(3, 3), (3, 6), (5, 10)])
+def test_head_counts_not_powers_of_two(hq, hv):
+    check_fwd(custom(B=3, T=201, Hq=hq, Hv=hv, host_l2=False), kernel_l2=True)
+    check_fwd(custom(seq_lens=(65, 0, 7, 130), Hq=hq, Hv=hv), kernel_l2=False)
