@@ -169,14 +169,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_chunk_tc_kernel(Geo geo, const __gr
     // unit are prefetched into buffers as soon as the current unit is done with them.
     // (32-bit item arithmetic: the host keeps chunk slots x Hq below 2^31)
     const int nitems = p.nslots * Hq;
-    auto item_ok = [&](int w_) {
-        long long t_;
-        int v_, n_, c_;
-        return geo.chunk(geo.div_hq(w_), t_, v_, n_, c_);
-    };
     auto next_item = [&](int w_) -> int {
         for (; w_ < nitems; w_ += (int)gridDim.x)
-            if (item_ok(w_)) return w_;
+            if (geo.has_chunk(geo.div_hq(w_))) return w_;
         return -1;
     };
     // a unit's place: first token t, valid rows, q/k head, value head, state row (chunk row x Hv + value head)

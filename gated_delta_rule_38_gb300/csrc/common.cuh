@@ -314,6 +314,10 @@ struct Geo {
             row0 = coff[n];
         }
     }
+    // Whether chunk slot `slot` holds a chunk (the test of chunk() below, without its table reads).
+    __device__ __forceinline__ bool has_chunk(int slot) const {
+        return cu == nullptr ? slot < B * nt_dense() : slot < *ctotal;
+    }
     // Chunk slot -> (first token, valid rows, sequence); false when past the end.
     __device__ __forceinline__ bool chunk(int slot, long long &tok0, int &len, int &n, int &ci) const {
         if (cu == nullptr) {
