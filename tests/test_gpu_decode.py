@@ -80,3 +80,9 @@ def test_zero_tokens_copies_the_state():
                                             initial_state=d["h0"])
     torch.cuda.synchronize()
     assert torch.equal(fin, d["h0"])
+
+
+@pytest.mark.parametrize("hq,hv", [(3, 6), (5, 5)])
+def test_head_counts_not_powers_of_two(hq, hv):
+    """The decode's block -> (row, value head) -> q/k head mapping at head counts that are not powers of two."""
+    check_decode(custom(B=3, T=2, Hq=hq, Hv=hv, host_l2=False), kernel_l2=True)
